@@ -1,0 +1,189 @@
+/*
+ * pa.h -- C ABI of libpa.so: paged KV-cache decode attention for GB300 (sm_103a).
+ *
+ * The KV cache of every sequence is stored in fixed-size physical blocks of
+ * block_size (B) tokens.  Logical token t of sequence s lives in physical block
+ * block_tables[s][t / B], at row t % B of that block (daiw.org "Paged Attention",
+ * section 直觉 and 定义; aiqz.cc "vLLM PagedAttention engine", section 分页存储设计,
+ * N_i = ceil(S_i / B) and BlockTable_i[j]).  Attention itself is ordinary softmax
+ * attention over the logical sequence; only the way K/V addresses are found changes
+ * (chenyuan1125 "vllm-pagedattention", section 页表真正解开的，是逻辑连续和物理连续).
+ *
+ * Layouts (all row-major, all device memory unless stated otherwise):
+ *   q             [num_seqs, num_q_heads, head_dim]              fp16 or bf16
+ *   out           [num_seqs, num_q_heads, head_dim]              same dtype as q
+ *   k_cache       [num_blocks, num_kv_heads, block_size, head_dim] same dtype
+ *   v_cache       [num_blocks, num_kv_heads, block_size, head_dim] same dtype
+ *   block_tables  [num_seqs, max_blocks_per_seq] int32; entries past ceil(ctx/B) unread
+ *   context_lens  [num_seqs] int32, the number of tokens each query attends to
+ *   key, value    [num_tokens, num_kv_heads, head_dim]            same dtype
+ *   slot_mapping  [num_tokens] int64, slot = block * B + row; negative = skip
+ *   block_mapping [num_pairs, 2] int32, (src, dst) block ids
+ * Query head h reads kv head h / (num_q_heads / num_kv_heads): contiguous groups (GQA).
+ *
+ * Supported shapes: head_dim in {64, 128}; block_size in {8, 16, 32};
+ * num_q_heads a multiple of num_kv_heads.  Every pointer to q, out, caches, key and
+ * value must be 16-byte aligned.
+ *
+ * Ownership: the caller owns every buffer.  The library allocates no device memory;
+ * pa_decode's scratch is the caller's `workspace`.  Device calls are asynchronous on
+ * `stream` (NULL = the legacy default stream) and return before the GPU work ends.
+ *
+ * Status codes: every int-returning call returns PA_OK (0) or a negative PA_ERR_*.
+ * Argument errors are found on the host before anything is launched.  Errors that
+ * only the device can see (a block id outside the pool, a context length < 1 or
+ * > max_blocks_per_seq * B, a slot beyond the pool, a bad copy pair) make the kernel
+ * skip that work item -- decode writes zeros for the affected sequence -- and set a
+ * bit in a per-device error word that pa_get_device_error reads.  No kernel traps.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { PA_FP16 = 0, PA_BF16 = 1 } pa_dtype;
+
+enum {
+  PA_OK = 0,
+  PA_ERR_ARG = -1,            /* null pointer, unsupported shape or dtype, misalignment */
+  PA_ERR_WORKSPACE = -2,      /* workspace missing or smaller than pa_decode_workspace_size */
+  PA_ERR_CUDA = -3,           /* a CUDA runtime call failed (launch, attribute, copy) */
+  PA_ERR_POOL_EXHAUSTED = -4, /* not enough free blocks; the pool is unchanged */
+  PA_ERR_UNKNOWN_SEQ = -5     /* sequence id not live (or already live, for a new id) */
+};
+
+/* Bits of the per-device error word (pa_get_device_error). */
+#define PA_DEVERR_BAD_BLOCK   0x1u  /* decode: a used block-table entry is outside [0, num_blocks) */
+#define PA_DEVERR_BAD_CONTEXT 0x2u  /* decode: context length < 1 or > max_blocks_per_seq * B */
+#define PA_DEVERR_BAD_SLOT    0x4u  /* reshape_and_cache: slot >= num_blocks * B */
+#define PA_DEVERR_BAD_PAIR    0x8u  /* copy_blocks: a block id outside [0, num_blocks) */
+#define PA_DEVERR_TIMEOUT     0x10u /* decode: a pipeline wait gave up (about 1 s); output invalid */
+
+/*
+ * pa_reshape_and_cache -- write each new token's K and V rows into its cache slot.
+ *
+ * A new token's K/V row goes into the free slot of its sequence's last block; when
+ * that block is full a fresh block from the free pool is appended to the table first
+ * (chenyuan1125 "vllm-pagedattention", section 页表真正解开的…; horeb.top "vLLM
+ * PagedAttention：大模型推理的显存管理革命", section 分配策略).  The host chooses the
+ * slots (pa_pool_append_slot); this call only moves the bytes:
+ *   k_cache[slot / B, h, slot % B, :] = key[i, h, :]   (and v_cache from value)
+ * for every token i whose slot_mapping[i] >= 0.  Two tokens naming the same slot in
+ * one call give an undefined winner.  Slots >= num_blocks * B are skipped and flagged
+ * (PA_DEVERR_BAD_SLOT).  num_tokens == 0 is a no-op.
+ */
+int pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
+                         const int64_t* slot_mapping, int num_tokens, int num_blocks,
+                         int num_kv_heads, int head_dim, int block_size, pa_dtype dtype,
+                         cudaStream_t stream);
+
+/*
+ * pa_decode -- single-query (decode) attention over paged K/V.
+ *
+ * For every sequence s and query head h (kv head g = h / G):
+ *   z_t = scale * <q[s,h,:], K_s[t,g,:]>,  t < context_lens[s]
+ *   out[s,h,:] = sum_t softmax(z)_t * V_s[t,g,:]
+ * where K_s[t] = k_cache[block_tables[s][t / B], :, t % B, :] (same for V).  Scores,
+ * the softmax and the weighted sum run block by block through the table
+ * (daiw.org "Paged Attention", section 定义, Attention 内核; chenyuan1125, section
+ * 页表真正解开的…).  Accumulation is fp32; the output is rounded to nearest-even.
+ *
+ * Work is split into equal shares of 16-token K/V stages, one share per SM, so a long
+ * sequence may be cut into pieces that a second kernel merges with a log-sum-exp
+ * reduction (split-KV).  Cut points depend only on logical token positions and the
+ * batch's context lengths, never on where blocks sit, so permuting physical blocks
+ * (and the table with them) gives bit-identical output.
+ *
+ * workspace: device scratch of at least pa_decode_workspace_size(...) bytes for the
+ * split pieces, 16-byte aligned, owned by the caller, not read before it is written.
+ * Concurrent pa_decode calls must not share a workspace.  Returns PA_ERR_WORKSPACE if
+ * it is NULL or too small.  num_seqs == 0 is a no-op.
+ */
+int pa_decode(const void* q, const void* k_cache, const void* v_cache,
+              const int32_t* block_tables, int max_blocks_per_seq,
+              const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+              int head_dim, int block_size, int num_blocks, float scale, void* out,
+              void* workspace, size_t workspace_bytes, pa_dtype dtype, cudaStream_t stream);
+
+/* Bytes of workspace pa_decode needs on the current device for these head counts.
+ * It depends on the device's SM count and the head shape only, not on the batch. */
+size_t pa_decode_workspace_size(int num_q_heads, int num_kv_heads, int head_dim);
+
+/*
+ * pa_copy_blocks -- copy whole physical blocks (every kv head, every row) of both
+ * caches: k_cache[dst] = k_cache[src], v_cache[dst] = v_cache[src] for each pair.
+ *
+ * This is the copy behind copy-on-write: a branch that must write into a last block
+ * still shared with other sequences first copies it, then remaps and writes; full old
+ * blocks stay shared (chenyuan1125, section 一块内存，如何安全地属于多条序列; horeb.top,
+ * section 内存共享：写时复制).  block_mapping is device memory.  Pairs must not alias
+ * (distinct dst, no dst also a src); pa_check_block_mapping checks a host copy.  A pair
+ * with an id outside [0, num_blocks) is skipped and flagged (PA_DEVERR_BAD_PAIR).
+ */
+int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* block_mapping, int num_pairs,
+                   int num_blocks, int num_kv_heads, int head_dim, int block_size,
+                   pa_dtype dtype, cudaStream_t stream);
+
+/* Host-side check of a copy_blocks pair list (host memory): PA_OK, or PA_ERR_ARG when an
+ * id is outside [0, num_blocks), a dst repeats, or a dst is also a src. */
+int pa_check_block_mapping(const int32_t* host_block_mapping, int num_pairs, int num_blocks);
+
+/* Synchronise `stream`, then read and clear the current device's error word. */
+int pa_get_device_error(cudaStream_t stream, uint32_t* flags_out);
+
+/* Human-readable name of a status code (static string). */
+const char* pa_status_string(int status);
+
+/*
+ * Host block pool: free list, reference counts, fork and copy-on-write planning.
+ *
+ * Blocks leave the head of an ordered free list and return to its tail (aiqz.cc,
+ * section Python 演示).  Prefill takes ceil(n / B) blocks; decode takes a new block
+ * every B tokens; a finished sequence returns its blocks (horeb.top, section 分配策略).
+ * A block shared by several sequences is reclaimed only when its reference count
+ * reaches zero (daiw.org "Paged Attention", section 量化).  When a sequence must write
+ * into a partly filled last block whose count is above one, the pool plans a copy: it
+ * takes a new block, moves this sequence's table entry to it and returns the (src, dst)
+ * pair, which the caller copies with pa_copy_blocks before writing (chenyuan1125,
+ * section 一块内存…).  An operation that cannot get every block it needs changes
+ * nothing and returns PA_ERR_POOL_EXHAUSTED (daiw.org, section 速查卡: an exhausted pool
+ * rejects new requests instead of failing).  Host memory only; not thread-safe.
+ */
+typedef struct pa_pool pa_pool;
+
+/* initial_free_order: NULL for 0..num_blocks-1, else a permutation of it (host).
+ * Returns NULL on a bad argument or allocation failure. */
+pa_pool* pa_pool_create(int num_blocks, int block_size, const int32_t* initial_free_order);
+void pa_pool_destroy(pa_pool* pool);
+/* Prefill: a new sequence holding n_tokens tokens in ceil(n_tokens / B) blocks. */
+int pa_pool_allocate(pa_pool* pool, int64_t seq_id, int n_tokens);
+/* Reserve the next token's slot.  Returns 0, or 1 when a copy is planned (then
+ * *cow_src, *cow_dst name the blocks to copy before writing), or a negative error. */
+int pa_pool_append_slot(pa_pool* pool, int64_t seq_id, int64_t* slot_out, int32_t* cow_src,
+                        int32_t* cow_dst);
+/* The child shares every block of the parent (reference counts + 1). */
+int pa_pool_fork(pa_pool* pool, int64_t parent_id, int64_t child_id);
+/* End a sequence; blocks whose count reaches zero go to the free-list tail in table order. */
+int pa_pool_free(pa_pool* pool, int64_t seq_id);
+/* Copy up to `cap` table entries into out; returns the table length or an error. */
+int pa_pool_block_table(const pa_pool* pool, int64_t seq_id, int32_t* out, int cap);
+/* Tokens held by the sequence, or an error. */
+int pa_pool_context_len(const pa_pool* pool, int64_t seq_id);
+/* Slots of logical tokens [first, first + count) of the sequence (all < context_len). */
+int pa_pool_slots(const pa_pool* pool, int64_t seq_id, int first, int count, int64_t* slots_out);
+int pa_pool_num_free(const pa_pool* pool);
+/* Copy up to `cap` free-list entries, head first; returns the free-list length. */
+int pa_pool_free_list(const pa_pool* pool, int32_t* out, int cap);
+/* Reference count of a block, or PA_ERR_ARG for an id outside the pool. */
+int pa_pool_refcount(const pa_pool* pool, int32_t block);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PA_H_ */

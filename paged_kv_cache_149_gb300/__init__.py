@@ -1,0 +1,301 @@
+"""Python binding of libpa.so: paged KV-cache decode attention on GB300 (sm_103a).
+
+Argument marshalling only.  Every computation runs in the library's CUDA kernels (or,
+for the block pool, its C++ host code); PyTorch supplies device memory and streams.
+The functions take torch tensors, check dtypes/devices/shapes, pass raw pointers and
+the current CUDA stream to the C ABI (include/pa.h) and raise ``PagedAttentionError``
+on a negative status.  If libpa.so is missing the import of this package still works
+but every call raises: there is no fallback path.
+
+Layouts (row-major):
+    q, out        [num_seqs, num_q_heads, head_dim]            fp16 / bf16
+    k_cache       [num_blocks, num_kv_heads, block_size, head_dim]
+    v_cache       [num_blocks, num_kv_heads, block_size, head_dim]
+    block_tables  [num_seqs, max_blocks_per_seq] int32
+    context_lens  [num_seqs] int32
+    key, value    [num_tokens, num_kv_heads, head_dim]
+    slot_mapping  [num_tokens] int64
+    block_mapping [num_pairs, 2] int32
+"""
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpa.so")
+
+PA_OK = 0
+PA_ERR_ARG = -1
+PA_ERR_WORKSPACE = -2
+PA_ERR_CUDA = -3
+PA_ERR_POOL_EXHAUSTED = -4
+PA_ERR_UNKNOWN_SEQ = -5
+
+DEVERR_BAD_BLOCK = 0x1
+DEVERR_BAD_CONTEXT = 0x2
+DEVERR_BAD_SLOT = 0x4
+DEVERR_BAD_PAIR = 0x8
+DEVERR_TIMEOUT = 0x10
+
+PA_FP16 = 0
+PA_BF16 = 1
+
+_c = ctypes
+_vp, _i32, _i64, _sz, _f32 = _c.c_void_p, _c.c_int, _c.c_int64, _c.c_size_t, _c.c_float
+
+# name -> (restype, argtypes); mirrors include/pa.h
+SIGNATURES = {
+    "pa_reshape_and_cache": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp]),
+    "pa_decode": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
+                         _f32, _vp, _vp, _sz, _i32, _vp]),
+    "pa_decode_workspace_size": (_sz, [_i32, _i32, _i32]),
+    "pa_copy_blocks": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp]),
+    "pa_check_block_mapping": (_i32, [_vp, _i32, _i32]),
+    "pa_get_device_error": (_i32, [_vp, _c.POINTER(_c.c_uint32)]),
+    "pa_status_string": (_c.c_char_p, [_i32]),
+    "pa_pool_create": (_vp, [_i32, _i32, _vp]),
+    "pa_pool_destroy": (None, [_vp]),
+    "pa_pool_allocate": (_i32, [_vp, _i64, _i32]),
+    "pa_pool_append_slot": (_i32, [_vp, _i64, _c.POINTER(_i64), _c.POINTER(_c.c_int32),
+                                   _c.POINTER(_c.c_int32)]),
+    "pa_pool_fork": (_i32, [_vp, _i64, _i64]),
+    "pa_pool_free": (_i32, [_vp, _i64]),
+    "pa_pool_block_table": (_i32, [_vp, _i64, _vp, _i32]),
+    "pa_pool_context_len": (_i32, [_vp, _i64]),
+    "pa_pool_slots": (_i32, [_vp, _i64, _i32, _i32, _vp]),
+    "pa_pool_num_free": (_i32, [_vp]),
+    "pa_pool_free_list": (_i32, [_vp, _vp, _i32]),
+    "pa_pool_refcount": (_i32, [_vp, _c.c_int32]),
+}
+
+_lib = None
+
+
+class PagedAttentionError(RuntimeError):
+    def __init__(self, status, what=""):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})" if what else status_string(status))
+
+
+class PoolExhausted(PagedAttentionError):
+    pass
+
+
+class UnknownSequence(PagedAttentionError):
+    pass
+
+
+def lib():
+    """The loaded libpa.so (ctypes), with argument types set.  Raises if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(
+                f"{LIB_PATH} is missing: build it with `python -m paged_kv_cache_149_gb300.build` "
+                "(nvcc, sm_103a).  There is no CPU or PyTorch fallback.")
+        l = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(l, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = l
+    return _lib
+
+
+def status_string(status):
+    return lib().pa_status_string(int(status)).decode()
+
+
+def _check(status, what):
+    if status < 0:
+        if status == PA_ERR_POOL_EXHAUSTED:
+            raise PoolExhausted(status, what)
+        if status == PA_ERR_UNKNOWN_SEQ:
+            raise UnknownSequence(status, what)
+        raise PagedAttentionError(status, what)
+    return status
+
+
+# ----------------------------------------------------------------- device calls
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.float16:
+        return PA_FP16
+    if t.dtype == torch.bfloat16:
+        return PA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}; expected float16 or bfloat16")
+
+
+def _stream_ptr(stream, device):
+    import torch
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    return s.cuda_stream
+
+
+def _need(cond, msg):
+    if not cond:
+        raise ValueError(msg)
+
+
+def _dev(t, name, dtype=None):
+    _need(t.is_cuda, f"{name} must be a CUDA tensor")
+    _need(t.is_contiguous(), f"{name} must be contiguous")
+    if dtype is not None:
+        _need(t.dtype == dtype, f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, stream=None):
+    """k_cache[slot // B, h, slot % B] = key[i, h] (and V) for every slot >= 0."""
+    import torch
+    n, hkv, d = key.shape
+    nb, hkv2, bs, d2 = k_cache.shape
+    _need(value.shape == key.shape and v_cache.shape == k_cache.shape, "shape mismatch")
+    _need(hkv == hkv2 and d == d2 and slot_mapping.shape == (n,), "shape mismatch")
+    _need(key.dtype == value.dtype == k_cache.dtype == v_cache.dtype, "dtype mismatch")
+    st = lib().pa_reshape_and_cache(
+        _dev(key, "key"), _dev(value, "value"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        _dev(slot_mapping, "slot_mapping", torch.int64), n, nb, hkv, d, bs, _dtype_code(key),
+        _stream_ptr(stream, key.device))
+    _check(st, "pa_reshape_and_cache")
+
+
+def decode_workspace_size(num_q_heads, num_kv_heads, head_dim):
+    """Bytes of workspace pa_decode needs on the current device."""
+    n = lib().pa_decode_workspace_size(num_q_heads, num_kv_heads, head_dim)
+    if n == 0:
+        raise PagedAttentionError(PA_ERR_ARG, "pa_decode_workspace_size")
+    return n
+
+
+def make_workspace(num_q_heads, num_kv_heads, head_dim, device=None):
+    import torch
+    return torch.empty(decode_workspace_size(num_q_heads, num_kv_heads, head_dim),
+                       dtype=torch.uint8, device=device or "cuda")
+
+
+def decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=None, workspace=None,
+           stream=None):
+    """Paged decode attention; returns ``out`` [num_seqs, num_q_heads, head_dim]."""
+    import torch
+    n, hq, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    _need(v_cache.shape == k_cache.shape and d == d2, "shape mismatch")
+    _need(block_tables.dim() == 2 and block_tables.shape[0] == n, "block_tables must be [num_seqs, T]")
+    _need(context_lens.shape == (n,), "context_lens must be [num_seqs]")
+    _need(q.dtype == k_cache.dtype == v_cache.dtype, "dtype mismatch")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out.shape == q.shape and out.dtype == q.dtype, "out must match q")
+    if workspace is None:
+        workspace = make_workspace(hq, hkv, d, q.device)
+    st = lib().pa_decode(
+        _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+        _dev(context_lens, "context_lens", torch.int32), n, hq, hkv, d, bs, nb, float(scale),
+        _dev(out, "out"), _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _dtype_code(q), _stream_ptr(stream, q.device))
+    _check(st, "pa_decode")
+    return out
+
+
+def copy_blocks(k_cache, v_cache, block_mapping, stream=None):
+    """k_cache[dst] = k_cache[src] and v_cache[dst] = v_cache[src] for each (src, dst)."""
+    import torch
+    nb, hkv, bs, d = k_cache.shape
+    _need(v_cache.shape == k_cache.shape, "shape mismatch")
+    _need(block_mapping.dim() == 2 and block_mapping.shape[1] == 2, "block_mapping must be [n, 2]")
+    st = lib().pa_copy_blocks(
+        _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        _dev(block_mapping, "block_mapping", torch.int32), block_mapping.shape[0], nb, hkv, d, bs,
+        _dtype_code(k_cache), _stream_ptr(stream, k_cache.device))
+    _check(st, "pa_copy_blocks")
+
+
+def check_block_mapping(pairs, num_blocks):
+    """Host check of a copy_blocks pair list (sequence of (src, dst)); raises on aliasing."""
+    import numpy as np
+    arr = np.ascontiguousarray(np.asarray(pairs, dtype=np.int32).reshape(-1, 2))
+    st = lib().pa_check_block_mapping(arr.ctypes.data, arr.shape[0], num_blocks)
+    _check(st, "pa_check_block_mapping")
+
+
+def get_device_error(stream=None, device=None):
+    """Synchronise the stream, then read and clear the device error word."""
+    import torch
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    v = ctypes.c_uint32(0)
+    _check(lib().pa_get_device_error(_stream_ptr(stream, dev), ctypes.byref(v)), "pa_get_device_error")
+    return v.value
+
+
+# ------------------------------------------------------------------ block pool
+
+class BlockPool:
+    """Host block pool (C++): ordered free list, refcounts, fork, copy-on-write planning."""
+
+    def __init__(self, num_blocks, block_size, initial_free_order=None):
+        import numpy as np
+        self.num_blocks = int(num_blocks)
+        self.block_size = int(block_size)
+        order = None
+        if initial_free_order is not None:
+            self._order = np.ascontiguousarray(np.asarray(initial_free_order, dtype=np.int32))
+            _need(self._order.shape == (self.num_blocks,), "initial_free_order must have num_blocks entries")
+            order = self._order.ctypes.data
+        self._h = lib().pa_pool_create(self.num_blocks, self.block_size, order)
+        if not self._h:
+            raise PagedAttentionError(PA_ERR_ARG, "pa_pool_create")
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h and _lib is not None:
+            _lib.pa_pool_destroy(h)
+            self._h = None
+
+    def allocate(self, seq, n_tokens):
+        _check(lib().pa_pool_allocate(self._h, int(seq), int(n_tokens)), "allocate")
+
+    def append_slot(self, seq):
+        """Returns (slot, cow) with cow None or the (src, dst) pair to copy before writing."""
+        slot = ctypes.c_int64(0)
+        src = ctypes.c_int32(-1)
+        dst = ctypes.c_int32(-1)
+        st = _check(lib().pa_pool_append_slot(self._h, int(seq), ctypes.byref(slot),
+                                              ctypes.byref(src), ctypes.byref(dst)), "append_slot")
+        return slot.value, ((src.value, dst.value) if st == 1 else None)
+
+    def fork(self, parent, child):
+        _check(lib().pa_pool_fork(self._h, int(parent), int(child)), "fork")
+
+    def free(self, seq):
+        _check(lib().pa_pool_free(self._h, int(seq)), "free")
+
+    def block_table(self, seq):
+        import numpy as np
+        n = _check(lib().pa_pool_block_table(self._h, int(seq), None, 0), "block_table")
+        out = np.zeros(n, dtype=np.int32)
+        _check(lib().pa_pool_block_table(self._h, int(seq), out.ctypes.data, n), "block_table")
+        return out
+
+    def context_len(self, seq):
+        return _check(lib().pa_pool_context_len(self._h, int(seq)), "context_len")
+
+    def slots(self, seq, first, count):
+        import numpy as np
+        out = np.zeros(count, dtype=np.int64)
+        _check(lib().pa_pool_slots(self._h, int(seq), int(first), int(count), out.ctypes.data), "slots")
+        return out
+
+    def num_free(self):
+        return _check(lib().pa_pool_num_free(self._h), "num_free")
+
+    def free_list(self):
+        import numpy as np
+        n = self.num_free()
+        out = np.zeros(n, dtype=np.int32)
+        _check(lib().pa_pool_free_list(self._h, out.ctypes.data, n), "free_list")
+        return out
+
+    def refcount(self, block):
+        return _check(lib().pa_pool_refcount(self._h, int(block)), "refcount")

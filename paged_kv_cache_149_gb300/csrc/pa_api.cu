@@ -1,0 +1,208 @@
+// C ABI of libpa.so: argument validation, per-device state (SM count, error word) and
+// dispatch to the kernels.  Every check that can be made on the host is made here,
+// before anything is launched; the kernels only guard against values that live in
+// device memory (block ids, context lengths, slots).
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+#include <set>
+#include <unordered_map>
+#include <utility>
+
+#include "../../include/pa.h"
+#include "pa_internal.h"
+
+namespace {
+
+// One error word per device; kernels OR PA_DEVERR_* bits into it.
+__device__ unsigned int g_device_error;
+
+struct DeviceInfo {
+  int sm_count = 0;
+  int max_smem_optin = 0;
+  unsigned* err = nullptr;  // device address of g_device_error on this device
+};
+
+std::mutex g_mu;
+std::unordered_map<int, DeviceInfo> g_devices;
+std::set<std::pair<int, const void*>> g_smem_done;
+
+// Per-device facts, gathered once per device with that device current.
+bool device_info(DeviceInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> lock(g_mu);
+  auto it = g_devices.find(dev);
+  if (it == g_devices.end()) {
+    DeviceInfo di;
+    void* p = nullptr;
+    if (cudaDeviceGetAttribute(&di.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&di.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess ||
+        cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess)
+      return false;
+    di.err = static_cast<unsigned*>(p);
+    it = g_devices.emplace(dev, di).first;
+  }
+  *out = it->second;
+  return true;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool shape_ok(int num_kv_heads, int head_dim, int block_size) {
+  return num_kv_heads >= 1 && (head_dim == 64 || head_dim == 128) &&
+         (block_size == 8 || block_size == 16 || block_size == 32);
+}
+
+}  // namespace
+
+namespace pa {
+
+bool ensure_smem_attr(const void* func, size_t bytes) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_smem_done.count({dev, func})) return true;
+  if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(bytes)) != cudaSuccess)
+    return false;
+  g_smem_done.insert({dev, func});
+  return true;
+}
+
+int decode_heads_per_pair(int num_q_heads, int num_kv_heads) {
+  const int g = num_q_heads / num_kv_heads;
+  return g < 8 ? g : 8;
+}
+
+}  // namespace pa
+
+extern "C" {
+
+const char* pa_status_string(int status) {
+  switch (status) {
+    case PA_OK: return "ok";
+    case PA_ERR_ARG: return "invalid argument";
+    case PA_ERR_WORKSPACE: return "workspace missing or too small";
+    case PA_ERR_CUDA: return "CUDA runtime error";
+    case PA_ERR_POOL_EXHAUSTED: return "block pool exhausted";
+    case PA_ERR_UNKNOWN_SEQ: return "unknown (or already live) sequence id";
+    default: return status > 0 ? "ok (positive result)" : "unknown status";
+  }
+}
+
+int pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
+                         const int64_t* slot_mapping, int num_tokens, int num_blocks,
+                         int num_kv_heads, int head_dim, int block_size, pa_dtype dtype,
+                         cudaStream_t stream) {
+  if (num_tokens < 0 || num_blocks < 1 || !shape_ok(num_kv_heads, head_dim, block_size) ||
+      (dtype != PA_FP16 && dtype != PA_BF16))
+    return PA_ERR_ARG;
+  if (num_tokens == 0) return PA_OK;
+  if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PA_ERR_ARG;
+  if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PA_ERR_ARG;
+  DeviceInfo di;
+  if (!device_info(&di)) return PA_ERR_CUDA;
+  return pa::reshape_and_cache_launch(key, value, k_cache, v_cache, slot_mapping, num_tokens,
+                                      num_blocks, num_kv_heads, head_dim, block_size, di.err,
+                                      stream);
+}
+
+size_t pa_decode_workspace_size(int num_q_heads, int num_kv_heads, int head_dim) {
+  if (num_kv_heads < 1 || num_q_heads < num_kv_heads || num_q_heads % num_kv_heads != 0 ||
+      (head_dim != 64 && head_dim != 128))
+    return 0;
+  DeviceInfo di;
+  if (!device_info(&di)) return 0;
+  return pa::decode_workspace_bytes(di.sm_count, pa::decode_heads_per_pair(num_q_heads, num_kv_heads),
+                                    head_dim);
+}
+
+int pa_decode(const void* q, const void* k_cache, const void* v_cache,
+              const int32_t* block_tables, int max_blocks_per_seq,
+              const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+              int head_dim, int block_size, int num_blocks, float scale, void* out,
+              void* workspace, size_t workspace_bytes, pa_dtype dtype, cudaStream_t stream) {
+  if (num_seqs < 0 || num_blocks < 1 || max_blocks_per_seq < 1 ||
+      !shape_ok(num_kv_heads, head_dim, block_size) || num_q_heads < num_kv_heads ||
+      num_q_heads % num_kv_heads != 0 || !std::isfinite(scale) ||
+      (dtype != PA_FP16 && dtype != PA_BF16) ||
+      static_cast<long long>(max_blocks_per_seq) * block_size > 0x7fffffffLL)
+    return PA_ERR_ARG;
+  if (num_seqs == 0) return PA_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PA_ERR_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return PA_ERR_ARG;
+  DeviceInfo di;
+  if (!device_info(&di)) return PA_ERR_CUDA;
+  const size_t need = pa::decode_workspace_bytes(
+      di.sm_count, pa::decode_heads_per_pair(num_q_heads, num_kv_heads), head_dim);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PA_ERR_WORKSPACE;
+  pa::DecodeArgs a;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.out = out;
+  a.workspace = workspace;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.block_size = block_size;
+  a.num_blocks = num_blocks;
+  a.scale = scale;
+  a.bf16 = dtype == PA_BF16;
+  a.err = di.err;
+  return pa::decode_launch(a, di.sm_count, stream);
+}
+
+int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* block_mapping, int num_pairs,
+                   int num_blocks, int num_kv_heads, int head_dim, int block_size,
+                   pa_dtype dtype, cudaStream_t stream) {
+  if (num_pairs < 0 || num_blocks < 1 || !shape_ok(num_kv_heads, head_dim, block_size) ||
+      (dtype != PA_FP16 && dtype != PA_BF16))
+    return PA_ERR_ARG;
+  if (num_pairs == 0) return PA_OK;
+  if (!k_cache || !v_cache || !block_mapping) return PA_ERR_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_ARG;
+  DeviceInfo di;
+  if (!device_info(&di)) return PA_ERR_CUDA;
+  return pa::copy_blocks_launch(k_cache, v_cache, block_mapping, num_pairs, num_blocks,
+                                num_kv_heads, head_dim, block_size, di.err, stream);
+}
+
+int pa_check_block_mapping(const int32_t* host_block_mapping, int num_pairs, int num_blocks) {
+  if (num_pairs < 0 || num_blocks < 1 || (num_pairs > 0 && !host_block_mapping)) return PA_ERR_ARG;
+  std::set<int32_t> dsts, srcs;
+  for (int i = 0; i < num_pairs; ++i) {
+    const int32_t s = host_block_mapping[2 * i], d = host_block_mapping[2 * i + 1];
+    if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) return PA_ERR_ARG;
+    if (!dsts.insert(d).second) return PA_ERR_ARG;
+    srcs.insert(s);
+  }
+  for (int32_t d : dsts)
+    if (srcs.count(d)) return PA_ERR_ARG;
+  return PA_OK;
+}
+
+int pa_get_device_error(cudaStream_t stream, uint32_t* flags_out) {
+  if (!flags_out) return PA_ERR_ARG;
+  DeviceInfo di;
+  if (!device_info(&di)) return PA_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return PA_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpy(&v, di.err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return PA_ERR_CUDA;
+  if (cudaMemsetAsync(di.err, 0, sizeof(v), stream) != cudaSuccess) return PA_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return PA_ERR_CUDA;
+  *flags_out = v;
+  return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,94 @@
+// Cache writes and block copies: exact 16-byte moves of 16-bit K/V rows.
+//
+// reshape_and_cache: a new token's K/V row goes into its slot of the sequence's last
+// block (chenyuan1125 "vllm-pagedattention", section 页表真正解开的…; horeb.top, section
+// 分配策略): k_cache[slot / B, h, slot % B, :] = key[i, h, :].
+// copy_blocks: the copy behind copy-on-write of a still-shared last block (chenyuan1125,
+// section 一块内存，如何安全地属于多条序列; horeb.top, section 内存共享：写时复制).
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "pa_common.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+// One CTA per token: the token's Hkv rows of K and of V, 16 bytes per thread step.
+__global__ void __launch_bounds__(128) reshape_and_cache_kernel(
+    const uint4* __restrict__ key, const uint4* __restrict__ value, uint4* __restrict__ k_cache,
+    uint4* __restrict__ v_cache, const int64_t* __restrict__ slot_mapping, long long num_slots,
+    int num_kv_heads, int vec_per_row, int block_size, unsigned* err) {
+  const int i = blockIdx.x;
+  const long long slot = slot_mapping[i];
+  if (slot < 0) return;
+  if (slot >= num_slots) {
+    if (threadIdx.x == 0) atomicOr(err, kErrBadSlot);
+    return;
+  }
+  const long long blk = slot / block_size;
+  const int row = static_cast<int>(slot % block_size);
+  const int n = num_kv_heads * vec_per_row;
+  for (int j = threadIdx.x; j < n; j += blockDim.x) {
+    const int h = j / vec_per_row;
+    const int c = j - h * vec_per_row;
+    const size_t src = (static_cast<size_t>(i) * num_kv_heads + h) * vec_per_row + c;
+    const size_t dst =
+        ((static_cast<size_t>(blk) * num_kv_heads + h) * block_size + row) * vec_per_row + c;
+    k_cache[dst] = key[src];
+    v_cache[dst] = value[src];
+  }
+}
+
+// grid = (pairs, chunks of a block, 2 caches).  A pair with an id outside the pool is
+// skipped and flagged.
+__global__ void __launch_bounds__(256) copy_blocks_kernel(uint4* __restrict__ k_cache,
+                                                          uint4* __restrict__ v_cache,
+                                                          const int32_t* __restrict__ mapping,
+                                                          int num_blocks, size_t block_vecs,
+                                                          unsigned* err) {
+  const int pair = blockIdx.x;
+  const int src = mapping[2 * pair];
+  const int dst = mapping[2 * pair + 1];
+  if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+    if (threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) atomicOr(err, kErrBadPair);
+    return;
+  }
+  uint4* cache = blockIdx.z == 0 ? k_cache : v_cache;
+  const uint4* s = cache + static_cast<size_t>(src) * block_vecs;
+  uint4* d = cache + static_cast<size_t>(dst) * block_vecs;
+  for (size_t j = static_cast<size_t>(blockIdx.y) * blockDim.x + threadIdx.x; j < block_vecs;
+       j += static_cast<size_t>(gridDim.y) * blockDim.x)
+    d[j] = s[j];
+}
+
+}  // namespace
+
+int reshape_and_cache_launch(const void* key, const void* value, void* k_cache, void* v_cache,
+                             const int64_t* slot_mapping, int num_tokens, int num_blocks,
+                             int num_kv_heads, int head_dim, int block_size, unsigned* err,
+                             cudaStream_t stream) {
+  if (num_tokens == 0) return 0;
+  reshape_and_cache_kernel<<<num_tokens, 128, 0, stream>>>(
+      static_cast<const uint4*>(key), static_cast<const uint4*>(value),
+      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), slot_mapping,
+      static_cast<long long>(num_blocks) * block_size, num_kv_heads, head_dim / 8, block_size,
+      err);
+  return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
+
+int copy_blocks_launch(void* k_cache, void* v_cache, const int32_t* block_mapping, int num_pairs,
+                       int num_blocks, int num_kv_heads, int head_dim, int block_size,
+                       unsigned* err, cudaStream_t stream) {
+  if (num_pairs == 0) return 0;
+  const size_t block_vecs = static_cast<size_t>(num_kv_heads) * block_size * head_dim / 8;
+  int chunks = static_cast<int>((block_vecs + 255) / 256);
+  if (chunks > 32) chunks = 32;
+  copy_blocks_kernel<<<dim3(num_pairs, chunks, 2), 256, 0, stream>>>(
+      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), block_mapping, num_blocks,
+      block_vecs, err);
+  return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
+
+}  // namespace pa

@@ -1,0 +1,44 @@
+// Internal interface between the C ABI layer (pa_api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace pa {
+
+struct DecodeArgs {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  void* out;
+  void* workspace;
+  int num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size, num_blocks;
+  float scale;
+  bool bf16;
+  unsigned* err;  // device address of the per-device error word
+};
+
+// Workspace bytes for `grid` persistent CTAs and up to `heads_per_pair` heads per pair.
+size_t decode_workspace_bytes(int grid, int heads_per_pair, int head_dim);
+// Heads a decode work pair covers (query heads per kv head, at most 8).
+int decode_heads_per_pair(int num_q_heads, int num_kv_heads);
+// Launch the decode kernel and its merge kernel; 0 or a negative PA_ERR_* code.
+int decode_launch(const DecodeArgs& a, int grid, cudaStream_t stream);
+
+int reshape_and_cache_launch(const void* key, const void* value, void* k_cache, void* v_cache,
+                             const int64_t* slot_mapping, int num_tokens, int num_blocks,
+                             int num_kv_heads, int head_dim, int block_size, unsigned* err,
+                             cudaStream_t stream);
+
+int copy_blocks_launch(void* k_cache, void* v_cache, const int32_t* block_mapping, int num_pairs,
+                       int num_blocks, int num_kv_heads, int head_dim, int block_size,
+                       unsigned* err, cudaStream_t stream);
+
+// Raise a kernel's dynamic shared-memory limit once per device; false on failure.
+bool ensure_smem_attr(const void* func, size_t bytes);
+
+}  // namespace pa

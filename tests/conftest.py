@@ -23,3 +23,12 @@ def load_golden(name):
 @pytest.fixture(scope="session")
 def golden():
     return load_golden
+
+
+@pytest.fixture(scope="session")
+def libpa():
+    """libpa.so built in-tree (nvcc cross-compiles here; on a GPU machine build() ran first)."""
+    from paged_kv_cache_149_gb300 import build as _build
+    _build.build()
+    import paged_kv_cache_149_gb300 as pa
+    return pa
