@@ -1,0 +1,458 @@
+"""Benchmark: paged decode on the Llama-3.1-8B-shaped batch, one JSON line.
+
+A step is one pass of the whole hot path over one batch: the cache write of each
+sequence's newest token (64 tokens through pa_reshape_and_cache) followed by paged decode
+attention over every sequence (pa_decode: the persistent decode kernel and its split-KV
+merge kernel).  Workload (seeded, synthetic; no dataset, no weights): 64 sequences,
+32 query / 8 kv heads, head_dim 128, bf16, block_size 16, context lengths uniform in
+[128, 2048], K/V ~ N(0,1), blocks placed through the block pool from a shuffled
+16384-block free list.  Three such batches live in disjoint blocks and steps rotate
+through them, so every step reads K/V that the previous two steps did not touch
+(each batch's K/V alone is larger than the 129 MB L2).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--workload NAME]
+
+Under torchrun (N > 1) every rank runs its own replica on its own GPU (weak scaling; no
+collective on the data path, only a barrier and a max-reduce of the elapsed time).
+``--impl reference`` times the CPU oracle instead (rank 0 only).
+"""
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode KV GB/s and % of GB300 HBM peak; µs per decode step"
+FALLBACK_HBM_GBS = 6800.0
+ROTATE = 3
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_llama31_8b_traffic.json")
+KERNEL_SOURCES = ["paged_kv_cache_149_gb300/csrc/pa_decode.cu",
+                  "paged_kv_cache_149_gb300/csrc/pa_common.cuh"]
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def step_bytes(wl):
+    """Algorithmic bytes of one step: K and V of every valid token, q and out, the block
+    table entries used and the context lengths (decode); plus the new tokens' K/V rows read
+    and written and their slots (cache write)."""
+    e = 2
+    n, hq, hkv, d, bs = wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.block_size
+    ctx = [int(c) for c in wl.context_lens]
+    kv = sum(ctx) * hkv * d * e * 2
+    qo = 2 * n * hq * d * e
+    table = sum(-(-c // bs) for c in ctx) * 4 + 4 * n
+    decode = kv + qo + table
+    reshape = 2 * (n * hkv * d * e * 2) + 8 * n
+    padded_kv = sum(-(-c // bs) * bs for c in ctx) * hkv * d * e * 2
+    return decode, reshape, padded_kv
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic():
+    """DRAM bytes per decode launch from the committed ncu summary, if the kernel source
+    is unchanged since it was captured."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("source_hash") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle samples, taken while the timed region runs."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"pa_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        self.proc.wait()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                    rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        inside = [r for r in rows if t0 - 0.15 <= r[0] <= t1 + 0.15]
+        use = inside or rows[-3:]
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        mhz = sorted(r[1] for r in use)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i, v in enumerate(r[3]) if v == "Active"})
+        return {"sm_mhz": mhz[len(mhz) // 2], "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons, "samples": len(use),
+                "window": "timed region" if inside else "after the timed region (too short to sample)"}
+
+
+def build_batches(wl, device, rotate):
+    """Place `rotate` copies of the batch in disjoint blocks of one pool and write every
+    token except each sequence's newest one (the step writes those)."""
+    import numpy as np
+    import torch
+
+    import paged_kv_cache_149_gb300 as pa
+    dt = {"fp16": torch.float16, "bf16": torch.bfloat16}[wl.dtype]
+
+    def up(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(dt)
+
+    shape = (wl.num_blocks, wl.num_kv_heads, wl.block_size, wl.head_dim)
+    k_cache = torch.zeros(shape, dtype=dt, device=device)
+    v_cache = torch.zeros(shape, dtype=dt, device=device)
+    pool = pa.BlockPool(wl.num_blocks, wl.block_size, wl.free_order)
+    n, T = wl.num_seqs, wl.max_blocks_per_seq
+    keys, values = up(wl.keys), up(wl.values)
+    last_rows = torch.from_numpy(wl.seq_start[1:] - 1).to(device)
+    batches = []
+    for r in range(rotate):
+        tables = np.full((n, T), 0, dtype=np.int32)
+        slots = []
+        for s in range(n):
+            sid = r * n + s
+            c = int(wl.context_lens[s])
+            pool.allocate(sid, c)
+            t = pool.block_table(sid)
+            tables[s, :len(t)] = t
+            slots.append(pool.slots(sid, 0, c))
+        all_slots = torch.from_numpy(np.concatenate(slots)).to(device)
+        pa.reshape_and_cache(keys, values, k_cache, v_cache, all_slots)
+        new_slots = torch.from_numpy(np.array([sl[-1] for sl in slots], dtype=np.int64)).to(device)
+        batches.append({
+            "q": up(wl.q), "tables": torch.from_numpy(tables).to(device),
+            "ctx": torch.from_numpy(np.ascontiguousarray(wl.context_lens, np.int32)).to(device),
+            "slots": new_slots, "key": keys[last_rows].contiguous(),
+            "value": values[last_rows].contiguous(),
+            "out": torch.empty((n, wl.num_q_heads, wl.head_dim), dtype=dt, device=device),
+        })
+    return k_cache, v_cache, batches
+
+
+def run_gpu(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    import paged_kv_cache_149_gb300 as pa
+    import workloads
+    from paged_kv_cache_149_gb300 import build as _build
+
+    _build.build()
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    wl = workloads.RECIPES[args.workload]()
+    k_cache, v_cache, batches = build_batches(wl, device, ROTATE)
+    ws = pa.make_workspace(wl.num_q_heads, wl.num_kv_heads, wl.head_dim, device)
+    stream = torch.cuda.Stream(device)
+    torch.cuda.synchronize(device)
+    pa.get_device_error()
+
+    def step(i, ev_mid=None):
+        b = batches[i % ROTATE]
+        pa.reshape_and_cache(b["key"], b["value"], k_cache, v_cache, b["slots"], stream=stream)
+        if ev_mid is not None:
+            ev_mid.record(stream)
+        pa.decode(b["q"], k_cache, v_cache, b["tables"], b["ctx"], wl.scale, out=b["out"],
+                  workspace=ws, stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(device)
+    if pa.get_device_error(stream=stream):
+        raise RuntimeError("device error flags set during warm-up")
+
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    K = args.steps
+    ev_start = torch.cuda.Event(enable_timing=True)
+    ev_stop = torch.cuda.Event(enable_timing=True)
+    ev_mid = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_dec = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(device)
+    t0 = time.time()
+    ev_start.record(stream)
+    for i in range(K):
+        step(i, ev_mid[i])
+        ev_dec[i].record(stream)
+    ev_stop.record(stream)
+    torch.cuda.synchronize(device)
+    t1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop(t0, t1) if sampler else None
+    flags = pa.get_device_error(stream=stream)
+    total_ms = ev_start.elapsed_time(ev_stop)
+    decode_ms = sum(ev_mid[i].elapsed_time(ev_dec[i]) for i in range(K)) / K
+    if world > 1:
+        t = torch.tensor([total_ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # end to end through the binding with host buffers: inputs from pinned host memory
+    # every step, the output read back every step
+    names = ("q", "tables", "ctx", "slots", "key", "value")
+    host_in = [{k: b[k].cpu().pin_memory() for k in names} for b in batches]
+    host_out = torch.empty(batches[0]["out"].shape, dtype=batches[0]["out"].dtype).pin_memory()
+    dev_in = {k: torch.empty_like(batches[0][k]) for k in names}
+    dev_out = torch.empty_like(batches[0]["out"])
+    h2d = sum(v.numel() * v.element_size() for v in host_in[0].values())
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step(i):
+        with torch.cuda.stream(stream):
+            for k, v in host_in[i % ROTATE].items():
+                dev_in[k].copy_(v, non_blocking=True)
+            pa.reshape_and_cache(dev_in["key"], dev_in["value"], k_cache, v_cache, dev_in["slots"],
+                                 stream=stream)
+            pa.decode(dev_in["q"], k_cache, v_cache, dev_in["tables"], dev_in["ctx"], wl.scale,
+                      out=dev_out, workspace=ws, stream=stream)
+            host_out.copy_(dev_out, non_blocking=True)
+
+    for i in range(max(3, args.warmup)):
+        e2e_step(i)
+    torch.cuda.synchronize(device)
+    ke = max(1, min(K, 2000))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(ke):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms = e0.elapsed_time(e1) / ke
+    return {"wl": wl, "total_ms": total_ms, "decode_ms": decode_ms, "e2e_ms": e2e_ms,
+            "h2d": h2d, "d2h": d2h, "clocks": clocks, "flags": flags}
+
+
+def oracle_sample(name, budget_s, max_seqs, seed_seq=0):
+    """Time the CPU oracle's paged decode on sequences of the workload until `budget_s`
+    of CPU time is spent (at least one sequence).  Runs in a fresh single-threaded process."""
+    code = f"""
+import json, os, sys, time
+sys.path.insert(0, {ROOT!r})
+import numpy as np
+import workloads
+from oracle import attention, cache_ops, formats
+from oracle.block_pool import BlockPool
+wl = workloads.RECIPES[{name!r}]()
+pool = BlockPool(wl.num_blocks, wl.block_size, wl.free_order)
+n, T = wl.num_seqs, wl.max_blocks_per_seq
+tables = np.full((n, T), -1, dtype=np.int32)
+slots = []
+for s in range(n):
+    c = int(wl.context_lens[s]); pool.allocate(s, c)
+    t = pool.block_table(s); tables[s, :len(t)] = t
+    slots += [pool.slot(s, i) for i in range(c)]
+shape = (wl.num_blocks, wl.num_kv_heads, wl.block_size, wl.head_dim)
+nan = formats.FORMATS[wl.dtype]["qnan"]
+kc = np.full(shape, nan, dtype=np.uint16); vc = kc.copy()
+kc, vc = cache_ops.reshape_and_cache(kc, vc, wl.keys, wl.values, np.array(slots, dtype=np.int64))
+order = [({seed_seq} + i) % n for i in range(n)]
+per, t0 = [], time.process_time()
+while time.process_time() - t0 < {budget_s} and len(per) < {max_seqs}:
+    s = order[len(per) % n]
+    a = time.process_time()
+    attention.paged_decode_bits(wl.q, kc, vc, tables, wl.context_lens, wl.scale,
+                                wl.block_size, wl.dtype, seqs=[s])
+    c = int(wl.context_lens[s])
+    nb = (c * wl.num_kv_heads * wl.head_dim * 2 * 2 + 2 * wl.num_q_heads * wl.head_dim * 2
+          + (-(-c // wl.block_size)) * 4 + 4)
+    per.append((time.process_time() - a, nb))
+print(json.dumps({{"seqs": len(per), "seconds": sum(p[0] for p in per),
+                  "bytes": sum(p[1] for p in per), "per_seq": per}}))
+"""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
+    if r.returncode != 0:
+        raise RuntimeError("oracle baseline failed:\n" + r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default="llama31_8b")
+    ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        reference_arm(args)
+        return
+
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl")
+    res = run_gpu(args, rank, world, local_rank)
+    if rank != 0:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+        return
+    wl = res["wl"]
+    dec_b, resh_b, padded = step_bytes(wl)
+    step_s = res["total_ms"] / 1e3 / args.steps
+    value = world * (dec_b + resh_b) / step_s / 1e9
+    peak, peak_kind = measured_peak()
+    achieved = dec_b / (res["decode_ms"] / 1e3) / 1e9
+    traffic = recorded_traffic()
+    cpu = (oracle_sample(args.workload, args.cpu_baseline_seconds, 10 ** 9)
+           if args.cpu_baseline_seconds > 0 else None)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(res["total_ms"] / args.steps, 5),
+        "us_per_step": round(1e3 * res["total_ms"] / args.steps, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": wl.dtype,
+        "data": "synthetic (seeded normals; no dataset or weights)",
+        "config": {
+            "workload": (f"{wl.name}: {wl.num_seqs} seqs, ctx {int(wl.context_lens.min())}..."
+                         f"{int(wl.context_lens.max())} (sum {int(wl.context_lens.sum())}), "
+                         f"{wl.num_q_heads} q / {wl.num_kv_heads} kv heads, head_dim {wl.head_dim}, "
+                         f"block_size {wl.block_size}, pool {wl.num_blocks} blocks; step = "
+                         f"reshape_and_cache of {wl.num_seqs} new tokens + paged decode"),
+            "l2": f"each batch's K/V ({dec_b / 1e6:.0f} MB) exceeds L2; {ROTATE} batches in "
+                  "disjoint blocks rotated every step",
+            "parallelism": f"replicas x{world}",
+        },
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "pa_decode (decode kernel + split-KV merge kernel)",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "peak_kind": f"{peak_kind} (HBM copy)",
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": traffic,
+            "algorithmic_bytes": dec_b,
+            "padded_block_bytes": padded,
+            "decode_us": round(1e3 * res["decode_ms"], 2),
+        },
+        "cpu_baseline": None if cpu is None else {
+            "value": round(cpu["bytes"] / cpu["seconds"] / 1e9, 4),
+            "unit": "GB/s",
+            "cores": 1,
+            "kind": "oracle",
+            "sample": f"float64 NumPy oracle, single thread, {cpu['seqs']} sequences of the same "
+                      f"batch in {cpu['seconds']:.1f} s of CPU time",
+        },
+        "e2e": {
+            "value": round(world * (dec_b + resh_b) / (res["e2e_ms"] / 1e3) / 1e9, 1),
+            "unit": "GB/s",
+            "h2d_bytes_per_step": res["h2d"],
+            "d2h_bytes_per_step": res["d2h"],
+            "us_per_step": round(1e3 * res["e2e_ms"], 2),
+        },
+        "clocks": res["clocks"],
+        "gpu_launches": 3 * args.steps,
+        "device_error_flags": res["flags"],
+    }
+    print(json.dumps(line))
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+def reference_arm(args):
+    """The oracle as it stands, timed on the host cores: each step decodes a bounded
+    sample of the same batch."""
+    import workloads
+    wl = workloads.RECIPES[args.workload]()
+    # calibrate: the per-sequence cost sets how many sequences fit in one step
+    cal = oracle_sample(args.workload, 1.0, 4)
+    per_seq = cal["seconds"] / max(1, cal["seqs"])
+    budget = 120.0
+    per_step = max(1, min(wl.num_seqs, int(budget / (args.steps + args.warmup) / per_seq)))
+    t0 = time.time()
+    res = oracle_sample(args.workload, 1e9, per_step * (args.steps + args.warmup))
+    wall = time.time() - t0
+    timed = res["per_seq"][per_step * args.warmup:]      # warm-up steps are not counted
+    secs = sum(p[0] for p in timed)
+    nbytes = sum(p[1] for p in timed)
+    value = nbytes / secs / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * secs / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": f"{wl.name} (see the native arm's line)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{per_step} sequence(s) of the batch per step, single thread; "
+                                   f"{wall:.0f} s wall including setup"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

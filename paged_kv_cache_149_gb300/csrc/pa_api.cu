@@ -73,11 +73,6 @@ bool ensure_smem_attr(const void* func, size_t bytes) {
   return true;
 }
 
-int decode_heads_per_pair(int num_q_heads, int num_kv_heads) {
-  const int g = num_q_heads / num_kv_heads;
-  return g < 8 ? g : 8;
-}
-
 }  // namespace pa
 
 extern "C" {
@@ -131,8 +126,9 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache,
       !shape_ok(num_kv_heads, head_dim, block_size) || num_q_heads < num_kv_heads ||
       num_q_heads % num_kv_heads != 0 || !std::isfinite(scale) ||
       (dtype != PA_FP16 && dtype != PA_BF16) ||
-      static_cast<long long>(max_blocks_per_seq) * block_size > 0x7fffffffLL)
-    return PA_ERR_ARG;
+      static_cast<long long>(max_blocks_per_seq) * block_size > 0x7fffffffLL ||
+      static_cast<long long>(num_blocks) * num_kv_heads * block_size > 0x7fffffffLL)
+    return PA_ERR_ARG;  // (the last bound keeps TMA row coordinates within 32 bits)
   if (num_seqs == 0) return PA_OK;
   if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PA_ERR_ARG;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))

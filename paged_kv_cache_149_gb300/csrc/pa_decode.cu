@@ -7,27 +7,29 @@
 // kernel finds each K/V block through the table and does score, softmax and weighted sum
 // block by block).
 //
-// Design (GB300 has 152 SMs; decode is HBM-bound at <= 1 FLOP/byte per head group):
-// * Work unit = a 16-token "stage" of one (sequence, kv head[, head chunk]) pair.  The
-//   units of the whole batch are cut into gridDim.x equal contiguous shares, one per
-//   persistent CTA (one CTA per SM), so every SM streams the same number of bytes and
-//   there is no tail of idle SMs.  A pair cut between CTAs is merged afterwards by a
-//   log-sum-exp reduction (split-KV; the rescaling identity of online softmax that
-//   chenyuan1125, section 它和 FlashAttention…, names as FlashAttention's technique).
-//   Cut points depend on logical positions and context lengths only, so permuting
-//   physical blocks gives bit-identical output.
-// * Warp specialisation: one producer warp walks the CTA's share and issues 1-D
-//   cp.async.bulk copies of each stage's K rows, then V rows, into a ring of smem slots
-//   guarded by mbarriers (full: transaction bytes; empty: consumer arrivals).  Only the
-//   valid rows of a tail block are copied.  One q copy per pair goes through a 2-slot
-//   side ring.
-// * Eight consumer warps, in two groups taking alternate stages.  K stage: 8 lanes per
-//   token, each lane holds 16 (or 8) q values per head in fp32 (pre-scaled by
-//   scale*log2 e), packed fp32x2 FMAs, 3 xor-shuffles per head.  Scores of a chunk of
-//   up to 256 tokens go to smem; one warp per head turns them into exp2 weights with a
-//   running max/sum (online softmax across chunks).  V stage: each lane owns D/32
-//   output columns for every head; accumulators are rescaled once per chunk.
-// * Every mbarrier wait is bounded (about 1 s) and sets PA_DEVERR_TIMEOUT on expiry.
+// Design (GB300: 152 SMs, HBM-bound at <= 1 FLOP/byte per query head):
+// * Work unit = a 16-token "stage" (K and V rows) of one (sequence, kv head, head chunk)
+//   pair.  The batch's units are cut into gridDim.x equal contiguous shares, one per
+//   persistent CTA (one CTA per SM): every SM streams the same bytes, no SM idles at the
+//   end.  A pair cut between CTAs is merged afterwards with a log-sum-exp reduction
+//   (split-KV: the rescaling identity of online softmax that chenyuan1125, section
+//   它和 FlashAttention…, names as FlashAttention's technique).  Cut points depend on
+//   logical positions and context lengths only, so permuting physical blocks (and the
+//   table with them) gives bit-identical output.
+// * One producer warp: lane i owns stage i of a batch of up to 8 stages, waits for its
+//   ring slot (stage kk belongs to consumer warp kk % 8, which owns a private set of
+//   slots and takes them in order), and issues TMA tensor copies (cp.async.bulk.tensor, 128-byte swizzle) of
+//   the stage's K and V rows; the next batch's block-table entries load meanwhile.  A
+//   2-slot side ring carries each pair's q rows (1-D bulk copy).
+// * Eight consumer warps take stages round-robin.  The query heads of the pair form the
+//   M = 16 rows of warp-level tensor-core MMAs (m16n8k16, fp32 accumulate):
+//   S = Q K^T over the stage's 16 tokens, then O += P V with P = 2^(S - m) rounded to
+//   the input type.  Each warp keeps its own running max/sum (online softmax); the eight
+//   warps merge at the end of each segment.  Swizzled smem makes every ldmatrix
+//   conflict-free.
+// * Every mbarrier wait is bounded (about 1 s) and sets PA_DEVERR_TIMEOUT on expiry;
+//   exits after a failed wait are decided collectively so no warp is left at a barrier.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -42,17 +44,23 @@ constexpr int kStageTok = 16;
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
-constexpr int kChunk = 256;                      // tokens per softmax chunk
-constexpr int kMaxHeads = 8;                     // query heads per work pair
+constexpr int kBatch = 8;                        // stages the producer issues together
+constexpr int kMaxHeads = 16;                    // query heads per work pair (MMA rows)
 constexpr int kBarConsumers = 1;                 // named barrier id for the consumers
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
 struct Geo {
-  static constexpr int kStageBytes = kStageTok * D * 2;  // one stage of K (or V) rows
-  static constexpr int kStages = (128 * 1024) / kStageBytes;
-  static constexpr int kNch = D / 64;  // 16-byte chunks per lane in a K row (8 lanes/token)
-  static constexpr int kVe = D / 32;   // output columns per lane in the V stage
+  static constexpr int kHalves = D / 64;                    // 128-byte column halves of a row
+  static constexpr int kBoxBytes = kStageTok * 128;         // 16 rows of one half
+  static constexpr int kKBytes = kHalves * kBoxBytes;       // K rows of a stage
+  static constexpr int kStageBytes = 2 * kKBytes;           // K then V
+  // Ring slots per consumer warp; each warp owns its slots, so every slot has a single
+  // consumer that takes its rounds in order and mbarrier parity waits are exact.
+  static constexpr int kSlotsPerWarp = (128 * 1024) / (kStageBytes * 8);
+  static constexpr int kStages = kSlotsPerWarp * 8;
+  static constexpr int kKSteps = D / 16;                    // MMA k-steps of Q K^T
+  static constexpr int kNTiles = D / 8;                     // MMA n-tiles of P V
 };
 
 struct SplitRec {
@@ -64,17 +72,15 @@ struct SplitRec {
 
 struct Params {
   const uint8_t* q;
-  const uint8_t* k_cache;
-  const uint8_t* v_cache;
   const int32_t* block_tables;
   const int32_t* context_lens;
   uint8_t* out;
   int num_seqs, num_q_heads, num_kv_heads, group, heads_per_pair, head_chunks;
-  int max_blocks_per_seq, block_size, num_blocks, max_ctx;
+  int max_blocks_per_seq, block_size, log2_block, num_blocks, max_ctx;
   float scale_log2;
   SplitRec* recs;
-  float* part_acc;  // [grid][2][GP][D]
-  float* part_ml;   // [grid][2][GP][2]  (m, l); l < 0 marks a piece with a bad block
+  float* part_acc;  // [grid][2][kMaxHeads][D]
+  float* part_ml;   // [grid][2][kMaxHeads][2]  (m, l); l < 0 marks a piece with a bad block
   unsigned* err;
 };
 
@@ -94,11 +100,11 @@ struct Walk {
 
 struct Seg {
   int s, pair, ctx, ns;
-  int j0, j1;      // stage range within the pair
-  int ta, tb;      // token range [ta, tb)
-  bool bad_ctx;    // context length outside [1, max_ctx]
-  bool whole;      // the pair is not cut
-  bool cta_first;  // first segment of this CTA's share
+  int j0, j1;          // stage range within the pair
+  int ta, tb;          // token range [ta, tb)
+  bool bad_ctx;        // context length outside [1, max_ctx]
+  bool whole;          // the pair is not cut
+  bool cta_first;      // first segment of this CTA's share
   long long pair_end;  // one past the pair's last unit
 };
 
@@ -139,13 +145,129 @@ __device__ __forceinline__ int owner_of(long long x, long long W, int G) {
   return static_cast<int>(r + (x - r * (q + 1)) / q);
 }
 
-template <int D, int GP>
+struct PairHeads {
+  int kvh, h0, nh;
+};
+
+__device__ __forceinline__ PairHeads pair_heads(const Params& p, int pair) {
+  PairHeads ph;
+  ph.kvh = pair / p.head_chunks;
+  const int hc = pair - ph.kvh * p.head_chunks;
+  ph.h0 = ph.kvh * p.group + hc * p.heads_per_pair;
+  ph.nh = min(p.heads_per_pair, p.group - hc * p.heads_per_pair);
+  return ph;
+}
+
+// Batches (<= kBatch stages) of the segments of this CTA's share, skipping pairs with an
+// invalid context length (those carry no pipeline traffic).
+struct Batch {
+  int s, kvh, h0, nh, ca, cb;
+  bool seg_start;
+};
+
+struct BatchIt {
+  Walk wk;
+  Seg sg;
+  int cpos;
+  bool have_seg;
+};
+
+__device__ __forceinline__ bool next_batch(BatchIt& it, Batch& b, const Params& p) {
+  for (;;) {
+    if (it.have_seg && it.cpos < it.sg.tb) {
+      const PairHeads ph = pair_heads(p, it.sg.pair);
+      b.s = it.sg.s;
+      b.kvh = ph.kvh;
+      b.h0 = ph.h0;
+      b.nh = ph.nh;
+      b.ca = it.cpos;
+      b.cb = min(it.cpos + kBatch * kStageTok, it.sg.tb);
+      b.seg_start = (it.cpos == it.sg.ta);
+      it.cpos = b.cb;
+      return true;
+    }
+    if (!next_seg(it.wk, it.sg)) return false;
+    it.have_seg = !it.sg.bad_ctx;
+    it.cpos = it.sg.ta;
+  }
+}
+
+// Block-table entries of stage `lane` of batch `b`: x = the block holding the stage's
+// first token, y = the next block when the stage spans two blocks (block_size 8).
+__device__ __forceinline__ int2 stage_entries(const Batch& b, int lane, const Params& p) {
+  int2 e = make_int2(0, 0);
+  const int nst = (b.cb - b.ca + kStageTok - 1) / kStageTok;
+  if (lane < nst) {
+    const int t0 = b.ca + lane * kStageTok;
+    const int nt = min(kStageTok, b.cb - t0);
+    const int32_t* trow = p.block_tables + static_cast<size_t>(b.s) * p.max_blocks_per_seq;
+    const int j0 = t0 >> p.log2_block;
+    e.x = __ldg(trow + j0);
+    if ((t0 & (p.block_size - 1)) + nt > p.block_size) e.y = __ldg(trow + j0 + 1);
+  }
+  return e;
+}
+
+// 2-D TMA tile load (box of the tensor map at column x, row y) into swizzled smem.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// D += A * B, m16n8k16, fp32 accumulate.
+template <typename T>
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1);
+
+template <>
+__device__ __forceinline__ void mma16816<__nv_bfloat16>(float (&d)[4], const uint32_t (&a)[4],
+                                                        uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <>
+__device__ __forceinline__ void mma16816<__half>(float (&d)[4], const uint32_t (&a)[4],
+                                                 uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Byte offset of (row, 16-byte chunk) in a stage's K or V rows: chunk c of the row lives
+// in column half c / 8, and the 128-byte swizzle permutes chunks within each row.
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+  return static_cast<uint32_t>((chunk >> 3) * (kStageTok * 128) + row * 128 +
+                               (((chunk & 7) ^ (row & 7)) << 4));
+}
+
+template <int D>
 struct Smem {
-  uint8_t ring[Geo<D>::kStages][Geo<D>::kStageBytes];
+  uint8_t ring[Geo<D>::kStages][Geo<D>::kStageBytes];  // 1024-byte aligned
   uint8_t qbuf[2][kMaxHeads * D * 2];
-  float logits[2][kChunk][GP];
-  float xacc[kConsumerWarps][GP][D];
-  float m_run[GP], l_run[GP], alpha[GP];
+  float xo[kConsumerWarps][8][D];  // per-warp O rows, 8 heads per exchange round
+  float xm[kConsumerWarps][kMaxHeads], xl[kConsumerWarps][kMaxHeads];
   long long scan[kThreads / 32];
   long long start_pre;
   int start_s;
@@ -155,12 +277,17 @@ struct Smem {
   unsigned long long qfull[2], qempty[2];
 };
 
-template <int D, int GP, typename T>
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params p) {
+template <int D, typename T>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmap_k,
+                  const __grid_constant__ CUtensorMap tmap_v) {
   using G_ = Geo<D>;
   constexpr int S = G_::kStages;
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  Smem<D, GP>& sm = *reinterpret_cast<Smem<D, GP>*>(smem_raw);
+  constexpr int R = G_::kSlotsPerWarp;
+  extern __shared__ uint8_t smem_raw[];
+  // the 128-byte swizzle pattern repeats every 1024 bytes: align the ring to it
+  const uint32_t raw_addr = smem_addr(smem_raw);
+  Smem<D>& sm = *reinterpret_cast<Smem<D>*>(smem_raw + (((raw_addr + 1023) & ~1023u) - raw_addr));
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -174,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params p) {
   if (tid == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(smem_addr(&sm.full[i]), 1);
-      mbar_init(smem_addr(&sm.empty[i]), 4);  // the owning group's four warps
+      mbar_init(smem_addr(&sm.empty[i]), 1);  // the consuming warp
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_addr(&sm.qfull[i]), 1);
@@ -188,11 +315,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params p) {
   long long mine = 0;
   for (int s = sa; s < sb; ++s)
     mine += static_cast<long long>(pairs_per_seq) * pair_stages(__ldg(p.context_lens + s), p.max_ctx);
-  // inclusive scan of `mine` over the block: shuffles within warps, then warp totals
-  long long incl = mine;
+  long long incl = mine;  // inclusive scan of `mine` over the block
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    long long v = __shfl_up_sync(0xffffffffu, incl, o);
+    const long long v = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += v;
   }
   if (lane == 31) sm.scan[warp] = incl;
@@ -231,348 +357,321 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params p) {
   walk.w = w0;
   walk.w0 = w0;
   walk.w1 = w1;
-
   const volatile int* abort_flag = &sm.abort_flag;
-  const size_t kv_head_stride = static_cast<size_t>(p.block_size) * D * 2;  // bytes
 
   if (warp == kConsumerWarps) {
     // =============================== producer warp ===============================
+    BatchIt it;
+    it.wk = walk;
+    it.cpos = 0;
+    it.have_seg = false;
+    Batch cur, nxt;
+    bool has_cur = next_batch(it, cur, p);
+    int2 e_cur = has_cur ? stage_entries(cur, lane, p) : make_int2(0, 0);
+    const int box_rows = min(p.block_size, kStageTok);
+    const uint32_t box_bytes = box_rows * 128;
     uint32_t k = 0, qi = 0;
-    bool ok = true;
-    Seg sg;
-    while (ok && next_seg(walk, sg)) {
-      if (sg.bad_ctx) continue;
-      const int kvh = sg.pair / p.head_chunks;
-      const int hc = sg.pair % p.head_chunks;
-      const int h0 = kvh * p.group + hc * p.heads_per_pair;
-      const int nh = min(p.heads_per_pair, p.group - hc * p.heads_per_pair);
-      // q rows of the pair's heads (contiguous in q)
-      if (lane == 0) {
-        const uint32_t qs = qi & 1;
-        ok = mbar_wait_bounded(smem_addr(&sm.qempty[qs]), ((qi >> 1) & 1) ^ 1, abort_flag);
-        if (ok) {
-          const uint32_t bytes = nh * D * 2;
-          mbar_arrive_expect_tx(smem_addr(&sm.qfull[qs]), bytes);
-          bulk_g2s(smem_addr(sm.qbuf[qs]),
-                   p.q + (static_cast<size_t>(sg.s) * p.num_q_heads + h0) * D * 2, bytes,
-                   smem_addr(&sm.qfull[qs]));
-        }
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      ++qi;
-      const int32_t* trow = p.block_tables + static_cast<size_t>(sg.s) * p.max_blocks_per_seq;
-      for (int ca = sg.ta; ok && ca < sg.tb; ca += kChunk) {
-        const int cb = min(ca + kChunk, sg.tb);
-        const int fb = ca / p.block_size;
-        const int nblk = (cb - 1) / p.block_size - fb + 1;  // <= 32 for B >= 8
-        int ent = (lane < nblk) ? __ldg(trow + fb + lane) : 0;
-        const bool ent_ok = (ent >= 0 && ent < p.num_blocks);
-        if (!ent_ok) ent = 0;
-        const unsigned bad_mask = __ballot_sync(0xffffffffu, !ent_ok && lane < nblk);
-        const int nst = (cb - ca + kStageTok - 1) / kStageTok;
-        for (int pass = 0; ok && pass < 2; ++pass) {
-          const uint8_t* cache = pass == 0 ? p.k_cache : p.v_cache;
-          for (int st = 0; st < nst; ++st, ++k) {
-            const int t0 = ca + st * kStageTok;
-            const int nt = min(kStageTok, cb - t0);
-            const int i0 = t0 / p.block_size - fb;
-            const int row0 = t0 % p.block_size;
-            const int rows0 = min(nt, p.block_size - row0);
-            const int blk0 = __shfl_sync(0xffffffffu, ent, i0);
-            const int blk1 = __shfl_sync(0xffffffffu, ent, min(i0 + 1, 31));
-            const bool bad = ((bad_mask >> i0) & 1u) || (rows0 < nt && ((bad_mask >> (i0 + 1)) & 1u));
-            if (lane == 0) {
-              const uint32_t slot = k % S;
-              ok = mbar_wait_bounded(smem_addr(&sm.empty[slot]), ((k / S) & 1) ^ 1, abort_flag);
-              if (ok) {
-                const uint32_t fbar = smem_addr(&sm.full[slot]);
-                if (bad) {
-                  sm.slot_bad[slot] = 1;
-                  mbar_arrive(fbar);
-                } else {
-                  sm.slot_bad[slot] = 0;
-                  mbar_arrive_expect_tx(fbar, nt * D * 2);
-                  const uint8_t* src0 = cache +
-                      (static_cast<size_t>(blk0) * p.num_kv_heads + kvh) * kv_head_stride +
-                      static_cast<size_t>(row0) * D * 2;
-                  bulk_g2s(smem_addr(sm.ring[slot]), src0, rows0 * D * 2, fbar);
-                  if (rows0 < nt) {  // block_size 8: the stage spans two blocks
-                    const uint8_t* src1 =
-                        cache + (static_cast<size_t>(blk1) * p.num_kv_heads + kvh) * kv_head_stride;
-                    bulk_g2s(smem_addr(sm.ring[slot]) + rows0 * D * 2, src1, (nt - rows0) * D * 2,
-                             fbar);
-                  }
-                }
-              }
-            }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
+    bool ok = true, issued = false;
+    while (ok && has_cur) {
+      issued = false;
+      const bool has_nxt = next_batch(it, nxt, p);
+      const int2 e_nxt = has_nxt ? stage_entries(nxt, lane, p) : make_int2(0, 0);
+      if (cur.seg_start) {  // the pair's q rows, contiguous in q
+        if (lane == 0) {
+          const uint32_t qs = qi & 1;
+          ok = mbar_wait_bounded(smem_addr(&sm.qempty[qs]), ((qi >> 1) & 1) ^ 1, abort_flag);
+          if (ok) {
+            const uint32_t bytes = cur.nh * D * 2;
+            mbar_arrive_expect_tx(smem_addr(&sm.qfull[qs]), bytes);
+            bulk_g2s(smem_addr(sm.qbuf[qs]),
+                     p.q + (static_cast<size_t>(cur.s) * p.num_q_heads + cur.h0) * D * 2, bytes,
+                     smem_addr(&sm.qfull[qs]));
           }
         }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        ++qi;
+        if (!ok) break;
       }
+      const int nst = (cur.cb - cur.ca + kStageTok - 1) / kStageTok;
+      if (lane < nst) {
+        const int t0 = cur.ca + lane * kStageTok;
+        const int nt = min(kStageTok, cur.cb - t0);
+        const int row0 = t0 & (p.block_size - 1);
+        const bool two = row0 + nt > p.block_size;  // block_size 8: a second block
+        const bool bad = e_cur.x < 0 || e_cur.x >= p.num_blocks ||
+                         (two && (e_cur.y < 0 || e_cur.y >= p.num_blocks));
+        const uint32_t kk = k + lane;
+        const uint32_t u = kk / kConsumerWarps;  // round-robin: warp kk % 8, its u-th stage
+        const uint32_t slot = (kk % kConsumerWarps) * R + u % R;
+        ok = mbar_wait_bounded(smem_addr(&sm.empty[slot]), ((u / R) & 1) ^ 1, abort_flag);
+        if (ok) {
+          const uint32_t fbar = smem_addr(&sm.full[slot]);
+          if (bad) {
+            sm.slot_bad[slot] = 1;
+            mbar_arrive(fbar);
+          } else {
+            sm.slot_bad[slot] = 0;
+            const int nboxes = two ? 2 : 1;
+            mbar_arrive_expect_tx(fbar, 2 * G_::kHalves * nboxes * box_bytes);
+            const uint32_t base = smem_addr(sm.ring[slot]);
+            const int y0 = (e_cur.x * p.num_kv_heads + cur.kvh) * p.block_size + row0;
+            const int y1 = (e_cur.y * p.num_kv_heads + cur.kvh) * p.block_size;
+#pragma unroll
+            for (int hf = 0; hf < G_::kHalves; ++hf) {
+              const uint32_t kd = base + hf * G_::kBoxBytes;
+              const uint32_t vd = kd + G_::kKBytes;
+              tma_load_2d(kd, &tmap_k, hf * 64, y0, fbar);
+              tma_load_2d(vd, &tmap_v, hf * 64, y0, fbar);
+              if (two) {
+                tma_load_2d(kd + box_bytes, &tmap_k, hf * 64, y1, fbar);
+                tma_load_2d(vd + box_bytes, &tmap_v, hf * 64, y1, fbar);
+              }
+            }
+          }
+          issued = true;
+        }
+      }
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      k += nst;
+      cur = nxt;
+      e_cur = e_nxt;
+      has_cur = has_nxt;
     }
-    if (!ok && lane == 0) {
-      // A wait gave up: stop everyone, then let copies already in flight land.
-      sm.abort_flag = 1;
-      atomicOr(p.err, kErrTimeout);
+    if (!ok) {
+      // A wait gave up: stop everyone, then let the copies already issued land (the last
+      // S stages before this batch, plus this batch's stages whose lanes issued them).
       int zero = 0;
       const volatile int* never = &zero;
-      const uint32_t first = k > static_cast<uint32_t>(S) ? k - S : 0;
-      for (uint32_t kk = first; kk < k; ++kk)
-        mbar_wait_bounded(smem_addr(&sm.full[kk % S]), (kk / S) & 1, never);
-      for (uint32_t qq = qi > 2 ? qi - 2 : 0; qq < qi; ++qq)
-        mbar_wait_bounded(smem_addr(&sm.qfull[qq & 1]), (qq >> 1) & 1, never);
+      if (lane == 0) {
+        sm.abort_flag = 1;
+        atomicOr(p.err, kErrTimeout);
+      }
+      auto slot_of = [&](uint32_t kk) { return (kk % kConsumerWarps) * R + (kk / kConsumerWarps) % R; };
+      auto parity_of = [&](uint32_t kk) { return ((kk / kConsumerWarps) / R) & 1; };
+      if (issued) mbar_wait_bounded(smem_addr(&sm.full[slot_of(k + lane)]), parity_of(k + lane), never);
+      if (lane == 0) {
+        const uint32_t first = k > static_cast<uint32_t>(S) ? k - S : 0;
+        for (uint32_t kk = first; kk < k; ++kk)
+          mbar_wait_bounded(smem_addr(&sm.full[slot_of(kk)]), parity_of(kk), never);
+        for (uint32_t qq = qi > 2 ? qi - 2 : 0; qq < qi; ++qq)
+          mbar_wait_bounded(smem_addr(&sm.qfull[qq & 1]), (qq >> 1) & 1, never);
+      }
     }
     return;
   }
 
   // ================================ consumer warps ================================
-  // Control flow of the eight consumer warps must stay identical: every exit taken
-  // after a failed wait is decided collectively at a named barrier (bar.red.or).
-  const int cw = warp;        // 0..7
-  const int grp = cw >> 2;    // stage-parity group
-  const int wi = cw & 3;      // warp within group
-  const int ktok = wi * 4 + (lane >> 3);  // K stage: token of this lane
-  const int sub = lane & 7;               // K stage: lane within the token's 8
-  constexpr int NCH = G_::kNch;
-  constexpr int VE = G_::kVe;
+  // Control flow of the eight consumer warps stays identical: every exit taken after a
+  // failed wait is decided collectively at a named barrier (bar.red.or).
+  constexpr int KS = G_::kKSteps;
+  constexpr int NT = G_::kNTiles;
+  const int cw = warp;
+  const int r0 = lane >> 2;        // MMA row of this lane (query head r0, and r0 + 8)
+  const int qc = 2 * (lane & 3);   // MMA column pair of this lane
+  const int lrow = lane & 7;       // ldmatrix: row within an 8x8 matrix
+  const int lmat = lane >> 3;      // ldmatrix: which of the four matrices
 
-  float qf[GP][NCH][8];
-  float acc[GP][VE];
-  uint32_t k = 0, qi = 0, chunk_no = 0;
+  uint32_t k = 0, qi = 0;
   bool ok = true;
   Seg sg;
   int rec_seq = -1, rec_pair = 0, rec_last = 0, rec_slot = 0;
 
   while (next_seg(walk, sg)) {
-    const int kvh = sg.pair / p.head_chunks;
-    const int hc = sg.pair % p.head_chunks;
-    const int h0 = kvh * p.group + hc * p.heads_per_pair;
-    const int nh = min(p.heads_per_pair, p.group - hc * p.heads_per_pair);
-    T* out_rows = reinterpret_cast<T*>(p.out) + (static_cast<size_t>(sg.s) * p.num_q_heads + h0) * D;
-
+    const PairHeads ph = pair_heads(p, sg.pair);
+    T* out_rows =
+        reinterpret_cast<T*>(p.out) + (static_cast<size_t>(sg.s) * p.num_q_heads + ph.h0) * D;
     if (sg.bad_ctx) {  // no pipeline traffic for this pair: zeros and a flag
-      for (int i = tid; i < nh * D / 8; i += kConsumerThreads)
+      for (int i = tid; i < ph.nh * D / 8; i += kConsumerThreads)
         reinterpret_cast<uint4*>(out_rows)[i] = make_uint4(0, 0, 0, 0);
       if (tid == 0) atomicOr(p.err, kErrBadContext);
       continue;
     }
 
-    // ---- q of this pair: smem slot -> fp32 registers, pre-scaled by scale*log2(e) ----
+    // ---- Q of the pair as MMA A fragments (rows = heads; heads >= nh are zero) ----
+    uint32_t qa[KS][4];
     {
       const uint32_t qs = qi & 1;
-      ok = __all_sync(0xffffffffu, ok && mbar_wait_bounded(smem_addr(&sm.qfull[qs]), (qi >> 1) & 1, abort_flag));
-      if (ok) {
-        const uint8_t* qb = sm.qbuf[qs];
+      ok = __all_sync(0xffffffffu, ok && mbar_wait_bounded(smem_addr(&sm.qfull[qs]),
+                                                            (qi >> 1) & 1, abort_flag));
+      const uint8_t* qb = sm.qbuf[qs];
 #pragma unroll
-        for (int h = 0; h < GP; ++h) {
-#pragma unroll
-          for (int cch = 0; cch < NCH; ++cch) {
-            uint4 raw = make_uint4(0, 0, 0, 0);
-            if (h < nh) raw = *reinterpret_cast<const uint4*>(qb + (h * D + (sub + 8 * cch) * 8) * 2);
-            const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 f = unpack2<T>(wv[e]);
-              qf[h][cch][2 * e] = f.x * p.scale_log2;
-              qf[h][cch][2 * e + 1] = f.y * p.scale_log2;
-            }
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&sm.qempty[qs]));
-      } else {
-        sm.abort_flag = 1;
+      for (int ks = 0; ks < KS; ++ks) {
+        const int col = 16 * ks + qc;
+        const bool lo_ok = ok && r0 < ph.nh, hi_ok = ok && r0 + 8 < ph.nh;
+        qa[ks][0] = lo_ok ? *reinterpret_cast<const uint32_t*>(qb + (r0 * D + col) * 2) : 0u;
+        qa[ks][1] = hi_ok ? *reinterpret_cast<const uint32_t*>(qb + ((r0 + 8) * D + col) * 2) : 0u;
+        qa[ks][2] = lo_ok ? *reinterpret_cast<const uint32_t*>(qb + (r0 * D + col + 8) * 2) : 0u;
+        qa[ks][3] = hi_ok ? *reinterpret_cast<const uint32_t*>(qb + ((r0 + 8) * D + col + 8) * 2) : 0u;
       }
+      __syncwarp();
+      if (ok && lane == 0) mbar_arrive(smem_addr(&sm.qempty[qs]));
+      if (!ok) sm.abort_flag = 1;
       ++qi;
     }
+    const bool hi = ph.nh > 8;  // rows 8..15 carry real heads
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+    float o[NT][4];
 #pragma unroll
-    for (int h = 0; h < GP; ++h)
-#pragma unroll
-      for (int e = 0; e < VE; ++e) acc[h][e] = 0.f;
+    for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
     bool seg_bad = false;
 
-    for (int ca = sg.ta; ca < sg.tb; ca += kChunk) {
-      const int cb = min(ca + kChunk, sg.tb);
-      const int nst = (cb - ca + kStageTok - 1) / kStageTok;
-      const int buf = chunk_no & 1;
-      ++chunk_no;
-
-      // ---------------------------- K stages: scores ----------------------------
-      for (int st = 0; ok && st < nst; ++st) {
-        const uint32_t kk = k + st;
-        if (static_cast<int>(kk & 1) != grp) continue;
-        const uint32_t slot = kk % S;
-        ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&sm.full[slot]), (kk / S) & 1, abort_flag));
-        if (!ok) break;
-        const int nt = min(kStageTok, cb - (ca + st * kStageTok));
-        if (sm.slot_bad[slot]) {
-          seg_bad = true;
-        } else {
-          const uint8_t* row = sm.ring[slot] + ktok * D * 2;
-          float2 dot[GP];
+    const int nstage = (sg.tb - sg.ta + kStageTok - 1) / kStageTok;
+    // this warp's stages: global index k + i with (k + i) % 8 == cw
+    for (int i = (cw - static_cast<int>(k % kConsumerWarps) + kConsumerWarps) % kConsumerWarps;
+         ok && i < nstage; i += kConsumerWarps) {
+      const uint32_t u = (k + i) / kConsumerWarps;  // this warp's u-th stage
+      const uint32_t slot = cw * R + u % R;
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait_bounded(smem_addr(&sm.full[slot]), (u / R) & 1, abort_flag));
+      if (!ok) break;
+      const int nt = min(kStageTok, sg.tb - (sg.ta + i * kStageTok));
+      bool nt_last_zeroed = false;
+      if (sm.slot_bad[slot]) {
+        seg_bad = true;
+      } else {
+        const uint32_t kb = smem_addr(sm.ring[slot]);
+        const uint32_t vb = kb + G_::kKBytes;
+        // ---- S = Q K^T over the stage's 16 tokens (two n-tiles of 8 tokens) ----
+        float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-          for (int h = 0; h < GP; ++h) dot[h] = make_float2(0.f, 0.f);
-#pragma unroll
-          for (int cch = 0; cch < NCH; ++cch) {
-            const uint4 raw = *reinterpret_cast<const uint4*>(row + (sub + 8 * cch) * 16);
-            const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 kv = unpack2<T>(wv[e]);
-#pragma unroll
-              for (int h = 0; h < GP; ++h)
-                dot[h] = ffma2(make_float2(qf[h][cch][2 * e], qf[h][cch][2 * e + 1]), kv, dot[h]);
-            }
-          }
-          float sc[GP];
-#pragma unroll
-          for (int h = 0; h < GP; ++h) {
-            float v = dot[h].x + dot[h].y;
-            v += __shfl_xor_sync(0xffffffffu, v, 1);
-            v += __shfl_xor_sync(0xffffffffu, v, 2);
-            v += __shfl_xor_sync(0xffffffffu, v, 4);
-            sc[h] = v;
-          }
-          if (ktok < nt) {
-            float mine_sc = sc[0];
-#pragma unroll
-            for (int h = 1; h < GP; ++h)
-              if (sub == h) mine_sc = sc[h];
-            if (sub < GP) sm.logits[buf][st * kStageTok + ktok][sub] = mine_sc;
-          }
+        for (int ks = 0; ks < KS; ++ks) {
+          uint32_t b[4];
+          ldsm_x4(kb + swz(lrow + ((lmat >> 1) << 3), 2 * ks + (lmat & 1)), b);
+          mma16816<T>(sacc[0], qa[ks], b[0], b[1]);
+          mma16816<T>(sacc[1], qa[ks], b[2], b[3]);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&sm.empty[slot]));
-      }
-      if (!ok) sm.abort_flag = 1;
-      if (bar_red_or(kBarConsumers, kConsumerThreads, !ok)) {
-        ok = false;
-        break;
-      }
-      k += nst;
-
-      // ------------------- online softmax over the chunk, per head -------------------
-      if (cw < nh) {
-        const int h = cw;
-        const int ntok = cb - ca;
-        float mx = -INFINITY;
-        for (int i = lane; i < ntok; i += 32) mx = fmaxf(mx, sm.logits[buf][i][h]);
+        // ---- online softmax: rows r0 (c0,c1) and r0 + 8 (c2,c3); tokens >= nt masked ----
+        float x[2][4];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        const bool first = (ca == sg.ta);
-        const float m_old = first ? -INFINITY : sm.m_run[h];
-        const float m_new = fmaxf(m_old, mx);
-        const float alpha = first ? 0.f : exp2f(m_old - m_new);
-        float sum = 0.f;
-        for (int i = lane; i < ntok; i += 32) {
-          const float e = exp2f(sm.logits[buf][i][h] - m_new);
-          sm.logits[buf][i][h] = e;
-          sum += e;
+        for (int nti = 0; nti < 2; ++nti) {
+          const int t = nti * 8 + qc;
+          x[0][2 * nti] = t < nt ? sacc[nti][0] * p.scale_log2 : -INFINITY;
+          x[0][2 * nti + 1] = t + 1 < nt ? sacc[nti][1] * p.scale_log2 : -INFINITY;
+          x[1][2 * nti] = t < nt ? sacc[nti][2] * p.scale_log2 : -INFINITY;
+          x[1][2 * nti + 1] = t + 1 < nt ? sacc[nti][3] * p.scale_log2 : -INFINITY;
         }
+        float alpha[2];
+        float pr[2][4];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        if (lane == 0) {
-          sm.l_run[h] = first ? sum : sm.l_run[h] * alpha + sum;
-          sm.m_run[h] = m_new;
-          sm.alpha[h] = alpha;
+        for (int r = 0; r < 2; ++r) {
+          float mx = fmaxf(fmaxf(x[r][0], x[r][1]), fmaxf(x[r][2], x[r][3]));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+          const float m_new = fmaxf(m_run[r], mx);
+          alpha[r] = exp2f(m_run[r] - m_new);  // 0 on the first stage (m_run = -inf)
+          float sum = 0.f;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            pr[r][j] = exp2f(x[r][j] - m_new);
+            sum += pr[r][j];
+          }
+          sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+          sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+          l_run[r] = l_run[r] * alpha[r] + sum;
+          m_run[r] = m_new;
         }
-      }
-      named_bar_sync(kBarConsumers, kConsumerThreads);
-
-      // ------------------------- V stages: weighted sum -------------------------
+        if (!__all_sync(0xffffffffu, alpha[0] == 1.f && alpha[1] == 1.f)) {
 #pragma unroll
-      for (int h = 0; h < GP; ++h) {
-        const float a = sm.alpha[h];
-#pragma unroll
-        for (int e = 0; e < VE; ++e) acc[h][e] *= a;
-      }
-      for (int st = 0; ok && st < nst; ++st) {
-        const uint32_t kk = k + st;
-        if (static_cast<int>(kk & 1) != grp) continue;
-        const uint32_t slot = kk % S;
-        ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&sm.full[slot]), (kk / S) & 1, abort_flag));
-        if (!ok) break;
-        const int nt = min(kStageTok, cb - (ca + st * kStageTok));
-        if (!sm.slot_bad[slot]) {
-          for (int t = wi; t < nt; t += 4) {
-            const uint8_t* vrow = sm.ring[slot] + t * D * 2 + lane * VE * 2;
-            float pw[GP];
-            const float* prow = sm.logits[buf][st * kStageTok + t];
-            if constexpr (GP >= 4) {
-#pragma unroll
-              for (int h = 0; h < GP; h += 4) {
-                const float4 p4 = *reinterpret_cast<const float4*>(prow + h);
-                pw[h] = p4.x; pw[h + 1] = p4.y; pw[h + 2] = p4.z; pw[h + 3] = p4.w;
-              }
-            } else if constexpr (GP == 2) {
-              const float2 p2 = *reinterpret_cast<const float2*>(prow);
-              pw[0] = p2.x; pw[1] = p2.y;
-            } else {
-              pw[0] = prow[0];
-            }
-            if constexpr (VE == 4) {
-              const uint2 raw = *reinterpret_cast<const uint2*>(vrow);
-              const float2 v01 = unpack2<T>(raw.x), v23 = unpack2<T>(raw.y);
-#pragma unroll
-              for (int h = 0; h < GP; ++h) {
-                const float2 ph = make_float2(pw[h], pw[h]);
-                const float2 a01 = ffma2(ph, v01, make_float2(acc[h][0], acc[h][1]));
-                const float2 a23 = ffma2(ph, v23, make_float2(acc[h][2], acc[h][3]));
-                acc[h][0] = a01.x; acc[h][1] = a01.y; acc[h][2] = a23.x; acc[h][3] = a23.y;
-              }
-            } else {
-              const uint32_t raw = *reinterpret_cast<const uint32_t*>(vrow);
-              const float2 v01 = unpack2<T>(raw);
-#pragma unroll
-              for (int h = 0; h < GP; ++h) {
-                const float2 a01 =
-                    ffma2(make_float2(pw[h], pw[h]), v01, make_float2(acc[h][0], acc[h][1]));
-                acc[h][0] = a01.x; acc[h][1] = a01.y;
-              }
-            }
+          for (int n = 0; n < NT; ++n) {
+            o[n][0] *= alpha[0];
+            o[n][1] *= alpha[0];
+            o[n][2] *= alpha[1];
+            o[n][3] *= alpha[1];
           }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&sm.empty[slot]));
+        // ---- rows past the context may hold anything (even NaN): zero them in V ----
+        if (nt < kStageTok) {
+          const int per_half = (kStageTok - nt) * 8;  // 16-byte chunks per column half
+          for (int e = lane; e < per_half * G_::kHalves; e += 32) {
+            const int hf = e / per_half;
+            const int rem = e - hf * per_half;
+            const uint32_t addr = vb + hf * G_::kBoxBytes + (nt + rem / 8) * 128 + (rem % 8) * 16;
+            asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0) : "memory");
+          }
+          nt_last_zeroed = true;
+          __syncwarp();
+        }
+        // ---- O += P V: P (rows = heads, k = tokens) straight from the S fragments ----
+        uint32_t pa[4];
+        pa[0] = pack2<T>(pr[0][0], pr[0][1]);
+        pa[1] = hi ? pack2<T>(pr[1][0], pr[1][1]) : 0u;
+        pa[2] = pack2<T>(pr[0][2], pr[0][3]);
+        pa[3] = hi ? pack2<T>(pr[1][2], pr[1][3]) : 0u;
+#pragma unroll
+        for (int jp = 0; jp < NT / 2; ++jp) {
+          uint32_t b[4];
+          ldsm_x4_t(vb + swz(lrow + ((lmat & 1) << 3), 2 * jp + (lmat >> 1)), b);
+          mma16816<T>(o[2 * jp], pa, b[0], b[1]);
+          mma16816<T>(o[2 * jp + 1], pa, b[2], b[3]);
+        }
       }
-      if (!ok) sm.abort_flag = 1;
-      k += nst;
+      // generic-proxy stores (the zeroed rows) must be ordered before the next TMA write
+      if (nt_last_zeroed) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&sm.empty[slot]));
     }
+    k += nstage;
+    if (!ok) sm.abort_flag = 1;
 
-    // ---------------- segment end: combine the 8 warps, write out ----------------
+    // ---------------- segment end: merge the 8 warps, write out ----------------
     if (bar_red_or(kBarConsumers, kConsumerThreads, !ok)) {
       ok = false;
       break;
     }
-#pragma unroll
-    for (int h = 0; h < GP; ++h)
-#pragma unroll
-      for (int e = 0; e < VE; ++e) sm.xacc[cw][h][lane * VE + e] = acc[h][e];
-    const bool any_bad = bar_red_or(kBarConsumers, kConsumerThreads, seg_bad);
+    if ((lane & 3) == 0) {
+      sm.xm[cw][r0] = m_run[0];
+      sm.xl[cw][r0] = l_run[0];
+      sm.xm[cw][r0 + 8] = m_run[1];
+      sm.xl[cw][r0 + 8] = l_run[1];
+    }
     const int slot_out = sg.cta_first ? 0 : 1;
-    float* pacc = p.part_acc + (static_cast<size_t>(blockIdx.x) * 2 + slot_out) * GP * D;
-    float* pml = p.part_ml + (static_cast<size_t>(blockIdx.x) * 2 + slot_out) * GP * 2;
-    for (int i = tid; i < nh * (D / 4); i += kConsumerThreads) {
-      const int h = i / (D / 4);
-      const int d4 = (i % (D / 4)) * 4;
-      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    float* pacc = p.part_acc + (static_cast<size_t>(blockIdx.x) * 2 + slot_out) * kMaxHeads * D;
+    float* pml = p.part_ml + (static_cast<size_t>(blockIdx.x) * 2 + slot_out) * kMaxHeads * 2;
+    bool any_bad = false;
+    for (int round = 0; round < (hi ? 2 : 1); ++round) {
+      if (round == 1) named_bar_sync(kBarConsumers, kConsumerThreads);  // round 0 reads done
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        const float4 x = *reinterpret_cast<const float4*>(&sm.xacc[w][h][d4]);
-        o.x += x.x; o.y += x.y; o.z += x.z; o.w += x.w;
+      for (int n = 0; n < NT; ++n) {
+        const float2 v = round == 0 ? make_float2(o[n][0], o[n][1]) : make_float2(o[n][2], o[n][3]);
+        *reinterpret_cast<float2*>(&sm.xo[cw][r0][8 * n + qc]) = v;
       }
-      if (sg.whole) {
-        const float inv = any_bad ? 0.f : 1.f / sm.l_run[h];
-        uint2 packed;
-        packed.x = pack2<T>(o.x * inv, o.y * inv);
-        packed.y = pack2<T>(o.z * inv, o.w * inv);
-        *reinterpret_cast<uint2*>(out_rows + h * D + d4) = packed;
-      } else {
-        *reinterpret_cast<float4*>(pacc + h * D + d4) = o;
-        if (d4 == 0) {
-          pml[h * 2 + 0] = sm.m_run[h];
-          pml[h * 2 + 1] = any_bad ? -1.f : sm.l_run[h];
+      any_bad = bar_red_or(kBarConsumers, kConsumerThreads, seg_bad);
+      const int hbase = round * 8;
+      const int rows = min(8, ph.nh - hbase);
+      for (int idx = tid; idx < rows * (D / 4); idx += kConsumerThreads) {
+        const int hr = idx / (D / 4);
+        const int h = hbase + hr;
+        const int d4 = (idx - hr * (D / 4)) * 4;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm.xm[w][h]);
+        float L = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          const float wt = exp2f(sm.xm[w][h] - M);  // 0 for warps without stages here
+          L += sm.xl[w][h] * wt;
+          const float4 x4 = *reinterpret_cast<const float4*>(&sm.xo[w][hr][d4]);
+          acc.x += x4.x * wt;
+          acc.y += x4.y * wt;
+          acc.z += x4.z * wt;
+          acc.w += x4.w * wt;
+        }
+        if (sg.whole) {
+          uint2 packed = make_uint2(0u, 0u);  // zeros for a pair with a bad block
+          if (!any_bad) {
+            const float inv = 1.f / L;
+            packed.x = pack2<T>(acc.x * inv, acc.y * inv);
+            packed.y = pack2<T>(acc.z * inv, acc.w * inv);
+          }
+          *reinterpret_cast<uint2*>(out_rows + h * D + d4) = packed;
+        } else {
+          *reinterpret_cast<float4*>(pacc + h * D + d4) = acc;
+          if (d4 == 0) {
+            pml[h * 2 + 0] = M;
+            pml[h * 2 + 1] = any_bad ? -1.f : L;
+          }
         }
       }
     }
@@ -597,24 +696,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params p) {
 
 // Merge the pieces of every cut pair: M = max m_i, L = sum l_i 2^(m_i - M),
 // out = sum acc_i 2^(m_i - M) / L, pieces taken in CTA order (deterministic).
-template <int D, int GP, typename T>
-__global__ void __launch_bounds__(128) merge_kernel(const Params p) {
+template <int D, typename T>
+__global__ void __launch_bounds__(128) merge_kernel(const __grid_constant__ Params p) {
   pdl_wait_primary();
   const SplitRec r = p.recs[blockIdx.x];
   if (r.seq < 0) return;
-  const int kvh = r.pair / p.head_chunks;
-  const int hc = r.pair % p.head_chunks;
-  const int h0 = kvh * p.group + hc * p.heads_per_pair;
-  const int nh = min(p.heads_per_pair, p.group - hc * p.heads_per_pair);
-  T* out_rows = reinterpret_cast<T*>(p.out) + (static_cast<size_t>(r.seq) * p.num_q_heads + h0) * D;
-  for (int i = threadIdx.x; i < nh * D; i += blockDim.x) {
+  const PairHeads ph = pair_heads(p, r.pair);
+  T* out_rows = reinterpret_cast<T*>(p.out) + (static_cast<size_t>(r.seq) * p.num_q_heads + ph.h0) * D;
+  for (int i = threadIdx.x; i < ph.nh * D; i += blockDim.x) {
     const int h = i / D;
-    const int d = i % D;
+    const int d = i - h * D;
     float M = -INFINITY;
     bool bad = false;
     for (int cc = blockIdx.x; cc <= r.c_last; ++cc) {
       const int slot = (cc == static_cast<int>(blockIdx.x)) ? r.first_slot : 0;
-      const float* ml = p.part_ml + ((static_cast<size_t>(cc) * 2 + slot) * GP + h) * 2;
+      const float* ml = p.part_ml + ((static_cast<size_t>(cc) * 2 + slot) * kMaxHeads + h) * 2;
       M = fmaxf(M, ml[0]);
       bad |= ml[1] < 0.f;
     }
@@ -622,27 +718,50 @@ __global__ void __launch_bounds__(128) merge_kernel(const Params p) {
     for (int cc = blockIdx.x; cc <= r.c_last; ++cc) {
       const int slot = (cc == static_cast<int>(blockIdx.x)) ? r.first_slot : 0;
       const size_t base = static_cast<size_t>(cc) * 2 + slot;
-      const float* ml = p.part_ml + (base * GP + h) * 2;
+      const float* ml = p.part_ml + (base * kMaxHeads + h) * 2;
       const float w = exp2f(ml[0] - M);
       L += ml[1] * w;
-      o += p.part_acc[base * GP * D + h * D + d] * w;
+      o += p.part_acc[(base * kMaxHeads + h) * D + d] * w;
     }
-    const float v = bad ? 0.f : o / L;
-    out_rows[h * D + d] = from_float<T>(v);
+    out_rows[h * D + d] = from_float<T>(bad ? 0.f : o / L);
   }
 }
 
-template <int D, int GP>
-constexpr size_t smem_bytes() {
-  return sizeof(Smem<D, GP>);
+// Tensor map over one cache viewed as rows of D elements: [num_blocks * Hkv * B, D],
+// boxes of 64 columns x min(B, 16) rows, 128-byte swizzle.
+bool make_cache_map(CUtensorMap* map, const void* base, bool bf16, int head_dim, long long rows,
+                    int box_rows) {
+  using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static EncodeFn encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return false;
+    encode = reinterpret_cast<EncodeFn>(fn);
+  }
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  return encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int GP, typename T>
-int launch(const Params& prm, int grid, cudaStream_t stream) {
-  const size_t smem = smem_bytes<D, GP>();
-  auto* kern = decode_kernel<D, GP, T>;
+template <int D, typename T>
+int launch(const Params& prm, const CUtensorMap& mk, const CUtensorMap& mv, int grid,
+           cudaStream_t stream) {
+  const size_t smem = sizeof(Smem<D>) + 1024;  // + alignment slack for the ring
+  auto* kern = decode_kernel<D, T>;
   if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), smem)) return -3;
-  kern<<<grid, kThreads, smem, stream>>>(prm);
+  kern<<<grid, kThreads, smem, stream>>>(prm, mk, mv);
   if (cudaGetLastError() != cudaSuccess) return -3;
 
   cudaLaunchConfig_t cfg = {};
@@ -655,18 +774,21 @@ int launch(const Params& prm, int grid, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, merge_kernel<D, GP, T>, prm) != cudaSuccess) return -3;
+  if (cudaLaunchKernelEx(&cfg, merge_kernel<D, T>, prm) != cudaSuccess) return -3;
   return 0;
 }
 
 }  // namespace decode
 
-size_t decode_workspace_bytes(int grid, int heads_per_pair, int head_dim) {
-  int gp = 1;
-  while (gp < heads_per_pair) gp <<= 1;
+int decode_heads_per_pair(int num_q_heads, int num_kv_heads) {
+  const int g = num_q_heads / num_kv_heads;
+  return g < decode::kMaxHeads ? g : decode::kMaxHeads;
+}
+
+size_t decode_workspace_bytes(int grid, int /*heads_per_pair*/, int head_dim) {
   const size_t recs = static_cast<size_t>(grid) * sizeof(decode::SplitRec);
-  const size_t acc = static_cast<size_t>(grid) * 2 * gp * head_dim * sizeof(float);
-  const size_t ml = static_cast<size_t>(grid) * 2 * gp * 2 * sizeof(float);
+  const size_t acc = static_cast<size_t>(grid) * 2 * decode::kMaxHeads * head_dim * sizeof(float);
+  const size_t ml = static_cast<size_t>(grid) * 2 * decode::kMaxHeads * 2 * sizeof(float);
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   return up(recs) + up(acc) + up(ml);
 }
@@ -674,8 +796,6 @@ size_t decode_workspace_bytes(int grid, int heads_per_pair, int head_dim) {
 int decode_launch(const DecodeArgs& a, int grid, cudaStream_t stream) {
   decode::Params p;
   p.q = static_cast<const uint8_t*>(a.q);
-  p.k_cache = static_cast<const uint8_t*>(a.k_cache);
-  p.v_cache = static_cast<const uint8_t*>(a.v_cache);
   p.block_tables = a.block_tables;
   p.context_lens = a.context_lens;
   p.out = static_cast<uint8_t*>(a.out);
@@ -683,38 +803,35 @@ int decode_launch(const DecodeArgs& a, int grid, cudaStream_t stream) {
   p.num_q_heads = a.num_q_heads;
   p.num_kv_heads = a.num_kv_heads;
   p.group = a.num_q_heads / a.num_kv_heads;
-  p.heads_per_pair = p.group < decode::kMaxHeads ? p.group : decode::kMaxHeads;
+  p.heads_per_pair = decode_heads_per_pair(a.num_q_heads, a.num_kv_heads);
   p.head_chunks = (p.group + p.heads_per_pair - 1) / p.heads_per_pair;
   p.max_blocks_per_seq = a.max_blocks_per_seq;
   p.block_size = a.block_size;
+  p.log2_block = a.block_size == 8 ? 3 : (a.block_size == 16 ? 4 : 5);
   p.num_blocks = a.num_blocks;
   p.max_ctx = a.max_blocks_per_seq * a.block_size;
   p.scale_log2 = a.scale * decode::kLog2e;
   p.err = a.err;
-  int gp = 1;
-  while (gp < p.heads_per_pair) gp <<= 1;
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   p.recs = reinterpret_cast<decode::SplitRec*>(ws);
   ws += up(static_cast<size_t>(grid) * sizeof(decode::SplitRec));
   p.part_acc = reinterpret_cast<float*>(ws);
-  ws += up(static_cast<size_t>(grid) * 2 * gp * a.head_dim * sizeof(float));
+  ws += up(static_cast<size_t>(grid) * 2 * decode::kMaxHeads * a.head_dim * sizeof(float));
   p.part_ml = reinterpret_cast<float*>(ws);
 
-#define PA_DECODE_CASE(DD, GG)                                                   \
-  if (a.head_dim == DD && gp == GG) {                                            \
-    return a.bf16 ? decode::launch<DD, GG, __nv_bfloat16>(p, grid, stream)       \
-                  : decode::launch<DD, GG, __half>(p, grid, stream);             \
-  }
-  PA_DECODE_CASE(128, 1)
-  PA_DECODE_CASE(128, 2)
-  PA_DECODE_CASE(128, 4)
-  PA_DECODE_CASE(128, 8)
-  PA_DECODE_CASE(64, 1)
-  PA_DECODE_CASE(64, 2)
-  PA_DECODE_CASE(64, 4)
-  PA_DECODE_CASE(64, 8)
-#undef PA_DECODE_CASE
+  const long long rows = static_cast<long long>(a.num_blocks) * a.num_kv_heads * a.block_size;
+  const int box_rows = a.block_size < decode::kStageTok ? a.block_size : decode::kStageTok;
+  CUtensorMap mk, mv;
+  if (!decode::make_cache_map(&mk, a.k_cache, a.bf16, a.head_dim, rows, box_rows) ||
+      !decode::make_cache_map(&mv, a.v_cache, a.bf16, a.head_dim, rows, box_rows))
+    return -3;
+  if (a.head_dim == 128)
+    return a.bf16 ? decode::launch<128, __nv_bfloat16>(p, mk, mv, grid, stream)
+                  : decode::launch<128, __half>(p, mk, mv, grid, stream);
+  if (a.head_dim == 64)
+    return a.bf16 ? decode::launch<64, __nv_bfloat16>(p, mk, mv, grid, stream)
+                  : decode::launch<64, __half>(p, mk, mv, grid, stream);
   return -1;
 }
 

@@ -24,7 +24,7 @@ struct DecodeArgs {
 
 // Workspace bytes for `grid` persistent CTAs and up to `heads_per_pair` heads per pair.
 size_t decode_workspace_bytes(int grid, int heads_per_pair, int head_dim);
-// Heads a decode work pair covers (query heads per kv head, at most 8).
+// Heads a decode work pair covers (query heads per kv head, at most 16).
 int decode_heads_per_pair(int num_q_heads, int num_kv_heads);
 // Launch the decode kernel and its merge kernel; 0 or a negative PA_ERR_* code.
 int decode_launch(const DecodeArgs& a, int grid, cudaStream_t stream);
