@@ -111,6 +111,29 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache,
               int head_dim, int block_size, int num_blocks, float scale, void* out,
               void* workspace, size_t workspace_bytes, pa_dtype dtype, cudaStream_t stream);
 
+/*
+ * pa_decode_fixed_scratch -- pa_decode for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this call; it exists for library users.  Some callers
+ * may not call cudaMalloc at all -- a server that gave nearly all HBM to the KV block pool
+ * up front, or a host framework that owns every device buffer -- and so cannot supply
+ * pa_decode's workspace.  This call takes the same arguments minus the workspace and uses
+ * a fixed 4 MiB scratch array built into the library instead (held on every GPU that loads
+ * the library until the process exits).  It allocates nothing.
+ *   - Every call on a device shares that scratch and leaves its contents behind; nothing in
+ *     it needs to start at zero.  Calls whose GPU work overlaps (unordered streams) race on
+ *     it and give undefined output.
+ *   - The first call on a device looks up the scratch's device address there; make that
+ *     first call before any stream capture begins.
+ *   - A device needing more than 4 MiB of decode scratch (very many SMs) gets
+ *     PA_ERR_WORKSPACE and nothing is launched.  Other errors are pa_decode's.
+ */
+int pa_decode_fixed_scratch(const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, int max_blocks_per_seq,
+                            const int32_t* context_lens, int num_seqs, int num_q_heads,
+                            int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                            float scale, void* out, pa_dtype dtype, cudaStream_t stream);
+
 /* Bytes of workspace pa_decode needs on the current device for these head counts.
  * It depends on the device's SM count and the head shape only, not on the batch. */
 size_t pa_decode_workspace_size(int num_q_heads, int num_kv_heads, int head_dim);

@@ -48,6 +48,8 @@ SIGNATURES = {
     "pa_decode": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
                          _f32, _vp, _vp, _sz, _i32, _vp]),
     "pa_decode_workspace_size": (_sz, [_i32, _i32, _i32]),
+    "pa_decode_fixed_scratch": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
+                                       _i32, _f32, _vp, _i32, _vp]),
     "pa_copy_blocks": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp]),
     "pa_check_block_mapping": (_i32, [_vp, _i32, _i32]),
     "pa_get_device_error": (_i32, [_vp, _c.POINTER(_c.c_uint32)]),
@@ -196,6 +198,30 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=None, wor
         _dev(out, "out"), _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
         _dtype_code(q), _stream_ptr(stream, q.device))
     _check(st, "pa_decode")
+    return out
+
+
+def decode_fixed_scratch(q, k_cache, v_cache, block_tables, context_lens, scale, out=None,
+                         stream=None):
+    """Paged decode that allocates nothing on the device: its scratch is a fixed array
+    inside the library (see pa_decode_fixed_scratch in include/pa.h).  For callers that
+    cannot allocate device memory; calls whose GPU work overlaps race on that scratch."""
+    import torch
+    n, hq, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    _need(v_cache.shape == k_cache.shape and d == d2, "shape mismatch")
+    _need(block_tables.dim() == 2 and block_tables.shape[0] == n, "block_tables must be [num_seqs, T]")
+    _need(context_lens.shape == (n,), "context_lens must be [num_seqs]")
+    _need(q.dtype == k_cache.dtype == v_cache.dtype, "dtype mismatch")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out.shape == q.shape and out.dtype == q.dtype, "out must match q")
+    st = lib().pa_decode_fixed_scratch(
+        _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+        _dev(context_lens, "context_lens", torch.int32), n, hq, hkv, d, bs, nb, float(scale),
+        _dev(out, "out"), _dtype_code(q), _stream_ptr(stream, q.device))
+    _check(st, "pa_decode_fixed_scratch")
     return out
 
 
