@@ -9,9 +9,8 @@
 //
 // Design (GB300: 152 SMs, HBM-bound at <= 1 FLOP/byte per query head):
 // * Work unit = a 16-token "stage" (K and V rows) of one (sequence, kv head, head chunk)
-//   pair.  The batch's units are cut into gridDim.x equal contiguous shares, one per
-//   persistent CTA (one CTA per SM): every SM streams the same bytes, no SM idles at the
-//   end.  A pair cut between CTAs is merged afterwards with a log-sum-exp reduction
+//   pair, plus a fixed charge per pair.  The batch's units are cut into gridDim.x equal
+//   contiguous shares, one per persistent CTA (one CTA per SM), so SMs finish together.  A pair cut between CTAs is merged afterwards with a log-sum-exp reduction
 //   (split-KV: the rescaling identity of online softmax that chenyuan1125, section
 //   它和 FlashAttention…, names as FlashAttention's technique).  Cut points depend on
 //   logical positions and context lengths only, so permuting physical blocks (and the
@@ -48,6 +47,10 @@ constexpr int kBatch = 8;                        // stages the producer issues t
 constexpr int kMaxHeads = 16;                    // query heads per work pair (MMA rows)
 constexpr int kBarConsumers = 1;                 // named barrier id for the consumers
 constexpr float kLog2e = 1.4426950408889634f;
+// A pair costs its stages plus this many stage-equivalents of fixed work (q load, the
+// eight-warp merge and the output write at its end).  Charging it when cutting the batch
+// into per-SM shares keeps SMs whose shares hold many short pairs from finishing last.
+constexpr int kSegCost = 5;
 
 template <int D>
 struct Geo {
@@ -57,7 +60,7 @@ struct Geo {
   static constexpr int kStageBytes = 2 * kKBytes;           // K then V
   // Ring slots per consumer warp; each warp owns its slots, so every slot has a single
   // consumer that takes its rounds in order and mbarrier parity waits are exact.
-  static constexpr int kSlotsPerWarp = (128 * 1024) / (kStageBytes * 8);
+  static constexpr int kSlotsPerWarp = (192 * 1024) / (kStageBytes * 8);
   static constexpr int kStages = kSlotsPerWarp * 8;
   static constexpr int kKSteps = D / 16;                    // MMA k-steps of Q K^T
   static constexpr int kNTiles = D / 8;                     // MMA n-tiles of P V
@@ -77,6 +80,7 @@ struct Params {
   uint8_t* out;
   int num_seqs, num_q_heads, num_kv_heads, group, heads_per_pair, head_chunks;
   int max_blocks_per_seq, block_size, log2_block, num_blocks, max_ctx;
+  int seg_cost;  // work units charged per pair on top of its stages (see Walk)
   float scale_log2;
   SplitRec* recs;
   float* part_acc;  // [grid][2][kMaxHeads][D]
@@ -88,14 +92,16 @@ __device__ __forceinline__ int pair_stages(int ctx, int max_ctx) {
   return (ctx >= 1 && ctx <= max_ctx) ? (ctx + kStageTok - 1) / kStageTok : 1;
 }
 
-// Deterministic walk over this CTA's share [w, w1) of the batch's stage units.
-// Units of sequence s: pairs_per_seq * ns(s); pair p owns units [p*ns, (p+1)*ns).
+// Deterministic walk over this CTA's share [w, w1) of the batch's work units.  Pair p of
+// sequence s weighs ns(s) + seg_cost units: seg_cost leading units of fixed work, then one
+// unit per 16-token stage.  Sequence s holds pairs_per_seq such pairs.
 struct Walk {
   const int32_t* ctx_lens;
-  int pairs_per_seq, max_ctx;
+  int pairs_per_seq, max_ctx, seg_cost;
   int s;
   long long pre;  // first unit of sequence s
   long long w, w0, w1;
+  bool first_done;  // a segment of this share has been returned already
 };
 
 struct Seg {
@@ -112,27 +118,34 @@ __device__ __forceinline__ bool next_seg(Walk& wk, Seg& sg) {
   while (wk.w < wk.w1) {
     const int ctx = __ldg(wk.ctx_lens + wk.s);
     const int ns = pair_stages(ctx, wk.max_ctx);
-    const long long units = static_cast<long long>(wk.pairs_per_seq) * ns;
+    const long long pw = ns + wk.seg_cost;
+    const long long units = static_cast<long long>(wk.pairs_per_seq) * pw;
     if (wk.w >= wk.pre + units) {
       wk.pre += units;
       ++wk.s;
       continue;
     }
     const long long local = wk.w - wk.pre;
+    const int pair = static_cast<int>(local / pw);
+    const long long pstart = wk.pre + pair * pw;
+    const long long end_w = min(wk.w1, pstart + pw);
+    const int j0 = static_cast<int>(max(0ll, local - pair * pw - wk.seg_cost));
+    const int j1 = static_cast<int>(max(0ll, end_w - pstart - wk.seg_cost));
+    wk.w = end_w;
+    if (j1 <= j0) continue;  // this share holds only the pair's fixed-cost units
     sg.s = wk.s;
     sg.ctx = ctx;
     sg.ns = ns;
-    sg.pair = static_cast<int>(local / ns);
-    sg.j0 = static_cast<int>(local % ns);
-    const long long left = wk.w1 - wk.w;
-    sg.j1 = static_cast<int>(left < ns - sg.j0 ? sg.j0 + left : ns);
+    sg.pair = pair;
+    sg.j0 = j0;
+    sg.j1 = j1;
     sg.bad_ctx = !(ctx >= 1 && ctx <= wk.max_ctx);
-    sg.ta = sg.j0 * kStageTok;
-    sg.tb = sg.bad_ctx ? sg.ta : min(sg.j1 * kStageTok, ctx);
-    sg.whole = (sg.j0 == 0 && sg.j1 == ns);
-    sg.cta_first = (wk.w == wk.w0);
-    sg.pair_end = wk.pre + static_cast<long long>(sg.pair + 1) * ns;
-    wk.w += sg.j1 - sg.j0;
+    sg.ta = j0 * kStageTok;
+    sg.tb = sg.bad_ctx ? sg.ta : min(j1 * kStageTok, ctx);
+    sg.whole = (j0 == 0 && j1 == ns);
+    sg.cta_first = !wk.first_done;
+    wk.first_done = true;
+    sg.pair_end = pstart + pw;
     return true;
   }
   return false;
@@ -266,7 +279,7 @@ template <int D>
 struct Smem {
   uint8_t ring[Geo<D>::kStages][Geo<D>::kStageBytes];  // 1024-byte aligned
   uint8_t qbuf[2][kMaxHeads * D * 2];
-  float xo[kConsumerWarps][8][D];  // per-warp O rows, 8 heads per exchange round
+  float xo[kConsumerWarps][4][D];  // per-warp O rows, 4 heads per exchange round
   float xm[kConsumerWarps][kMaxHeads], xl[kConsumerWarps][kMaxHeads];
   long long scan[kThreads / 32];
   long long start_pre;
@@ -314,7 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int sa = min(p.num_seqs, tid * per), sb = min(p.num_seqs, sa + per);
   long long mine = 0;
   for (int s = sa; s < sb; ++s)
-    mine += static_cast<long long>(pairs_per_seq) * pair_stages(__ldg(p.context_lens + s), p.max_ctx);
+    mine += static_cast<long long>(pairs_per_seq) *
+            (pair_stages(__ldg(p.context_lens + s), p.max_ctx) + p.seg_cost);
   long long incl = mine;  // inclusive scan of `mine` over the block
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -338,8 +352,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     long long pre = excl;
     int s = sa;
     for (;; ++s) {
-      const long long u =
-          static_cast<long long>(pairs_per_seq) * pair_stages(__ldg(p.context_lens + s), p.max_ctx);
+      const long long u = static_cast<long long>(pairs_per_seq) *
+                          (pair_stages(__ldg(p.context_lens + s), p.max_ctx) + p.seg_cost);
       if (w0 < pre + u) break;
       pre += u;
     }
@@ -352,6 +366,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   walk.ctx_lens = p.context_lens;
   walk.pairs_per_seq = pairs_per_seq;
   walk.max_ctx = p.max_ctx;
+  walk.seg_cost = p.seg_cost;
+  walk.first_done = false;
   walk.s = (w0 < w1) ? sm.start_s : 0;
   walk.pre = (w0 < w1) ? sm.start_pre : 0;
   walk.w = w0;
@@ -533,13 +549,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t kb = smem_addr(sm.ring[slot]);
         const uint32_t vb = kb + G_::kKBytes;
         // ---- S = Q K^T over the stage's 16 tokens (two n-tiles of 8 tokens) ----
+        // even and odd k-steps accumulate separately (four independent MMA chains)
         float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        float sodd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
           uint32_t b[4];
           ldsm_x4(kb + swz(lrow + ((lmat >> 1) << 3), 2 * ks + (lmat & 1)), b);
-          mma16816<T>(sacc[0], qa[ks], b[0], b[1]);
-          mma16816<T>(sacc[1], qa[ks], b[2], b[3]);
+          if (ks & 1) {
+            mma16816<T>(sodd[0], qa[ks], b[0], b[1]);
+            mma16816<T>(sodd[1], qa[ks], b[2], b[3]);
+          } else {
+            mma16816<T>(sacc[0], qa[ks], b[0], b[1]);
+            mma16816<T>(sacc[1], qa[ks], b[2], b[3]);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          sacc[0][j] += sodd[0][j];
+          sacc[1][j] += sodd[1][j];
         }
         // ---- online softmax: rows r0 (c0,c1) and r0 + 8 (c2,c3); tokens >= nt masked ----
         float x[2][4];
@@ -629,19 +657,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* pacc = p.part_acc + (static_cast<size_t>(blockIdx.x) * 2 + slot_out) * kMaxHeads * D;
     float* pml = p.part_ml + (static_cast<size_t>(blockIdx.x) * 2 + slot_out) * kMaxHeads * 2;
     bool any_bad = false;
-    for (int round = 0; round < (hi ? 2 : 1); ++round) {
-      if (round == 1) named_bar_sync(kBarConsumers, kConsumerThreads);  // round 0 reads done
+    // Exchange O four heads (MMA rows) at a time: round r covers rows 4r..4r+3, held in
+    // c0,c1 by lanes with r0 in that range for rows < 8 and in c2,c3 for rows >= 8.
+    const int rounds = (ph.nh + 3) / 4;
+    for (int round = 0; round < rounds; ++round) {
+      if (round > 0) named_bar_sync(kBarConsumers, kConsumerThreads);  // previous reads done
+      const int rbase = round * 4;
+      const int myrow = (rbase < 8) ? r0 : r0 + 8;
+      if (myrow >= rbase && myrow < rbase + 4) {
 #pragma unroll
-      for (int n = 0; n < NT; ++n) {
-        const float2 v = round == 0 ? make_float2(o[n][0], o[n][1]) : make_float2(o[n][2], o[n][3]);
-        *reinterpret_cast<float2*>(&sm.xo[cw][r0][8 * n + qc]) = v;
+        for (int n = 0; n < NT; ++n) {
+          const float2 v = rbase < 8 ? make_float2(o[n][0], o[n][1]) : make_float2(o[n][2], o[n][3]);
+          *reinterpret_cast<float2*>(&sm.xo[cw][myrow - rbase][8 * n + qc]) = v;
+        }
       }
       any_bad = bar_red_or(kBarConsumers, kConsumerThreads, seg_bad);
-      const int hbase = round * 8;
-      const int rows = min(8, ph.nh - hbase);
+      const int rows = min(4, ph.nh - rbase);
       for (int idx = tid; idx < rows * (D / 4); idx += kConsumerThreads) {
         const int hr = idx / (D / 4);
-        const int h = hbase + hr;
+        const int h = rbase + hr;
         const int d4 = (idx - hr * (D / 4)) * 4;
         float M = -INFINITY;
 #pragma unroll
@@ -810,6 +844,7 @@ int decode_launch(const DecodeArgs& a, int grid, cudaStream_t stream) {
   p.log2_block = a.block_size == 8 ? 3 : (a.block_size == 16 ? 4 : 5);
   p.num_blocks = a.num_blocks;
   p.max_ctx = a.max_blocks_per_seq * a.block_size;
+  p.seg_cost = decode::kSegCost;
   p.scale_log2 = a.scale * decode::kLog2e;
   p.err = a.err;
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
