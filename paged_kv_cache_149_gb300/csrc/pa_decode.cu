@@ -20,12 +20,13 @@
 //   slots and takes them in order), and issues TMA tensor copies (cp.async.bulk.tensor, 128-byte swizzle) of
 //   the stage's K and V rows; the next batch's block-table entries load meanwhile.  A
 //   2-slot side ring carries each pair's q rows (1-D bulk copy).
-// * Eight consumer warps take stages round-robin.  The query heads of the pair form the
-//   M = 16 rows of warp-level tensor-core MMAs (m16n8k16, fp32 accumulate):
-//   S = Q K^T over the stage's 16 tokens, then O += P V with P = 2^(S - m) rounded to
-//   the input type.  Each warp keeps its own running max/sum (online softmax); the eight
-//   warps merge at the end of each segment.  Swizzled smem makes every ldmatrix
-//   conflict-free.
+// * Eight consumer warps take stages round-robin.  Warp-level tensor-core MMAs
+//   (m16n8k16, fp32 accumulate) with the pair's query heads as the N = 8 (or 16) columns:
+//   S^T = K Q^T (rows = the stage's 16 tokens), then O^T += V^T P^T (rows = d) with
+//   P = 2^(S - m) rounded to the input type and moved into B-fragment layout by an
+//   in-register transpose (movmatrix).  Each warp keeps its own running max/sum (online
+//   softmax); the eight warps merge at the end of each segment.  Swizzled smem makes
+//   every ldmatrix conflict-free.
 // * Every mbarrier wait is bounded (about 1 s) and sets PA_DEVERR_TIMEOUT on expiry;
 //   exits after a failed wait are decided collectively so no warp is left at a barrier.
 #include <cuda.h>
@@ -243,6 +244,13 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
                : "r"(addr));
 }
 
+// Transpose of an 8x8 matrix of 16-bit values held one 32-bit pair per lane.
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
 // D += A * B, m16n8k16, fp32 accumulate.
 template <typename T>
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
@@ -290,7 +298,7 @@ struct Smem {
   unsigned long long qfull[2], qempty[2];
 };
 
-template <int D, typename T>
+template <int D, int NTH, typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v) {
@@ -481,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Control flow of the eight consumer warps stays identical: every exit taken after a
   // failed wait is decided collectively at a named barrier (bar.red.or).
   constexpr int KS = G_::kKSteps;
-  constexpr int NT = G_::kNTiles;
+  constexpr int MT = D / 16;  // m-tiles of O^T (16 rows of d each)
   const int cw = warp;
   const int r0 = lane >> 2;        // MMA row of this lane (query head r0, and r0 + 8)
   const int qc = 2 * (lane & 3);   // MMA column pair of this lane
@@ -504,32 +512,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       continue;
     }
 
-    // ---- Q of the pair as MMA A fragments (rows = heads; heads >= nh are zero) ----
-    uint32_t qa[KS][4];
+    // ---- Q^T of the pair as MMA B fragments: column n = head 8*nt + (lane >> 2) ----
+    // (heads >= nh are zero)
+    uint32_t qb[KS][NTH][2];
     {
       const uint32_t qs = qi & 1;
       ok = __all_sync(0xffffffffu, ok && mbar_wait_bounded(smem_addr(&sm.qfull[qs]),
                                                             (qi >> 1) & 1, abort_flag));
-      const uint8_t* qb = sm.qbuf[qs];
+      const uint8_t* qbuf = sm.qbuf[qs];
 #pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        const int col = 16 * ks + qc;
-        const bool lo_ok = ok && r0 < ph.nh, hi_ok = ok && r0 + 8 < ph.nh;
-        qa[ks][0] = lo_ok ? *reinterpret_cast<const uint32_t*>(qb + (r0 * D + col) * 2) : 0u;
-        qa[ks][1] = hi_ok ? *reinterpret_cast<const uint32_t*>(qb + ((r0 + 8) * D + col) * 2) : 0u;
-        qa[ks][2] = lo_ok ? *reinterpret_cast<const uint32_t*>(qb + (r0 * D + col + 8) * 2) : 0u;
-        qa[ks][3] = hi_ok ? *reinterpret_cast<const uint32_t*>(qb + ((r0 + 8) * D + col + 8) * 2) : 0u;
+      for (int nt = 0; nt < NTH; ++nt) {
+        const int h = nt * 8 + r0;
+        const bool hv = ok && h < ph.nh;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          const int col = 16 * ks + qc;
+          qb[ks][nt][0] = hv ? *reinterpret_cast<const uint32_t*>(qbuf + (h * D + col) * 2) : 0u;
+          qb[ks][nt][1] = hv ? *reinterpret_cast<const uint32_t*>(qbuf + (h * D + col + 8) * 2) : 0u;
+        }
       }
       __syncwarp();
       if (ok && lane == 0) mbar_arrive(smem_addr(&sm.qempty[qs]));
       if (!ok) sm.abort_flag = 1;
       ++qi;
     }
-    const bool hi = ph.nh > 8;  // rows 8..15 carry real heads
-    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-    float o[NT][4];
+    // This lane's softmax columns: heads hc0 = 8*nt + qc and hc0 + 1 of every n-tile.
+    float m_run[NTH][2], l_run[NTH][2];
+    float o[MT][NTH][4];  // O^T: rows d = 16*mt + r0 (+8), columns = heads
 #pragma unroll
-    for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    for (int nt = 0; nt < NTH; ++nt) {
+      m_run[nt][0] = m_run[nt][1] = -INFINITY;
+      l_run[nt][0] = l_run[nt][1] = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) o[mt][nt][0] = o[mt][nt][1] = o[mt][nt][2] = o[mt][nt][3] = 0.f;
+    }
     bool seg_bad = false;
 
     const int nstage = (sg.tb - sg.ta + kStageTok - 1) / kStageTok;
@@ -541,101 +557,103 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu,
                       mbar_wait_bounded(smem_addr(&sm.full[slot]), (u / R) & 1, abort_flag));
       if (!ok) break;
-      const int nt = min(kStageTok, sg.tb - (sg.ta + i * kStageTok));
-      bool nt_last_zeroed = false;
+      const int nt_tok = min(kStageTok, sg.tb - (sg.ta + i * kStageTok));
+      bool zeroed = false;
       if (sm.slot_bad[slot]) {
         seg_bad = true;
       } else {
         const uint32_t kb = smem_addr(sm.ring[slot]);
         const uint32_t vb = kb + G_::kKBytes;
-        // ---- S = Q K^T over the stage's 16 tokens (two n-tiles of 8 tokens) ----
-        // even and odd k-steps accumulate separately (four independent MMA chains)
-        float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        float sodd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        // ---- S^T = K Q^T: rows = the stage's 16 tokens, columns = heads ----
+        float sacc[NTH][4], sodd[NTH][4];
+#pragma unroll
+        for (int nt = 0; nt < NTH; ++nt)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) sacc[nt][j] = sodd[nt][j] = 0.f;
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
-          uint32_t b[4];
-          ldsm_x4(kb + swz(lrow + ((lmat >> 1) << 3), 2 * ks + (lmat & 1)), b);
-          if (ks & 1) {
-            mma16816<T>(sodd[0], qa[ks], b[0], b[1]);
-            mma16816<T>(sodd[1], qa[ks], b[2], b[3]);
-          } else {
-            mma16816<T>(sacc[0], qa[ks], b[0], b[1]);
-            mma16816<T>(sacc[1], qa[ks], b[2], b[3]);
+          uint32_t a[4];  // rows tok 0-7 / 8-15, d chunks 2ks / 2ks+1
+          ldsm_x4(kb + swz(lrow + ((lmat & 1) << 3), 2 * ks + (lmat >> 1)), a);
+#pragma unroll
+          for (int nt = 0; nt < NTH; ++nt) {
+            if (ks & 1)
+              mma16816<T>(sodd[nt], a, qb[ks][nt][0], qb[ks][nt][1]);
+            else
+              mma16816<T>(sacc[nt], a, qb[ks][nt][0], qb[ks][nt][1]);
           }
         }
+        // ---- online softmax per head (column) over the 16 tokens (rows) ----
+        // c0,c1: token r0, heads qc, qc+1; c2,c3: token r0 + 8, same heads
+        const bool v_lo = r0 < nt_tok, v_hi = r0 + 8 < nt_tok;
+        uint32_t pb[NTH][2];
+        float alpha[NTH][2];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          sacc[0][j] += sodd[0][j];
-          sacc[1][j] += sodd[1][j];
-        }
-        // ---- online softmax: rows r0 (c0,c1) and r0 + 8 (c2,c3); tokens >= nt masked ----
-        float x[2][4];
-#pragma unroll
-        for (int nti = 0; nti < 2; ++nti) {
-          const int t = nti * 8 + qc;
-          x[0][2 * nti] = t < nt ? sacc[nti][0] * p.scale_log2 : -INFINITY;
-          x[0][2 * nti + 1] = t + 1 < nt ? sacc[nti][1] * p.scale_log2 : -INFINITY;
-          x[1][2 * nti] = t < nt ? sacc[nti][2] * p.scale_log2 : -INFINITY;
-          x[1][2 * nti + 1] = t + 1 < nt ? sacc[nti][3] * p.scale_log2 : -INFINITY;
-        }
-        float alpha[2];
-        float pr[2][4];
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          float mx = fmaxf(fmaxf(x[r][0], x[r][1]), fmaxf(x[r][2], x[r][3]));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-          const float m_new = fmaxf(m_run[r], mx);
-          alpha[r] = exp2f(m_run[r] - m_new);  // 0 on the first stage (m_run = -inf)
-          float sum = 0.f;
+        for (int nt = 0; nt < NTH; ++nt) {
+          float x[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            pr[r][j] = exp2f(x[r][j] - m_new);
-            sum += pr[r][j];
+            const float v = (sacc[nt][j] + sodd[nt][j]) * p.scale_log2;
+            x[j] = (j < 2 ? v_lo : v_hi) ? v : -INFINITY;
           }
-          sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-          sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-          l_run[r] = l_run[r] * alpha[r] + sum;
-          m_run[r] = m_new;
-        }
-        if (!__all_sync(0xffffffffu, alpha[0] == 1.f && alpha[1] == 1.f)) {
+          float pr[4];
 #pragma unroll
-          for (int n = 0; n < NT; ++n) {
-            o[n][0] *= alpha[0];
-            o[n][1] *= alpha[0];
-            o[n][2] *= alpha[1];
-            o[n][3] *= alpha[1];
+          for (int c = 0; c < 2; ++c) {
+            float mx = fmaxf(x[c], x[c + 2]);
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float m_new = fmaxf(m_run[nt][c], mx);
+            alpha[nt][c] = exp2f(m_run[nt][c] - m_new);  // 0 on the first stage
+            pr[c] = exp2f(x[c] - m_new);
+            pr[c + 2] = exp2f(x[c + 2] - m_new);
+            float sum = pr[c] + pr[c + 2];
+            sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 8);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 16);
+            l_run[nt][c] = l_run[nt][c] * alpha[nt][c] + sum;
+            m_run[nt][c] = m_new;
           }
+          // P^T as B fragments: transpose the (token x head) 8x8 blocks in registers
+          pb[nt][0] = movmatrix_t(pack2<T>(pr[0], pr[1]));  // tokens 0-7
+          pb[nt][1] = movmatrix_t(pack2<T>(pr[2], pr[3]));  // tokens 8-15
+        }
+        bool all_one = true;
+#pragma unroll
+        for (int nt = 0; nt < NTH; ++nt) all_one = all_one && alpha[nt][0] == 1.f && alpha[nt][1] == 1.f;
+        if (!__all_sync(0xffffffffu, all_one)) {
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NTH; ++nt) {
+              o[mt][nt][0] *= alpha[nt][0];
+              o[mt][nt][1] *= alpha[nt][1];
+              o[mt][nt][2] *= alpha[nt][0];
+              o[mt][nt][3] *= alpha[nt][1];
+            }
         }
         // ---- rows past the context may hold anything (even NaN): zero them in V ----
-        if (nt < kStageTok) {
-          const int per_half = (kStageTok - nt) * 8;  // 16-byte chunks per column half
+        if (nt_tok < kStageTok) {
+          const int per_half = (kStageTok - nt_tok) * 8;  // 16-byte chunks per column half
           for (int e = lane; e < per_half * G_::kHalves; e += 32) {
             const int hf = e / per_half;
             const int rem = e - hf * per_half;
-            const uint32_t addr = vb + hf * G_::kBoxBytes + (nt + rem / 8) * 128 + (rem % 8) * 16;
+            const uint32_t addr = vb + hf * G_::kBoxBytes + (nt_tok + rem / 8) * 128 + (rem % 8) * 16;
             asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0) : "memory");
           }
-          nt_last_zeroed = true;
+          zeroed = true;
           __syncwarp();
         }
-        // ---- O += P V: P (rows = heads, k = tokens) straight from the S fragments ----
-        uint32_t pa[4];
-        pa[0] = pack2<T>(pr[0][0], pr[0][1]);
-        pa[1] = hi ? pack2<T>(pr[1][0], pr[1][1]) : 0u;
-        pa[2] = pack2<T>(pr[0][2], pr[0][3]);
-        pa[3] = hi ? pack2<T>(pr[1][2], pr[1][3]) : 0u;
+        // ---- O^T += V^T P^T: rows = d (16 per m-tile), k = tokens, columns = heads ----
 #pragma unroll
-        for (int jp = 0; jp < NT / 2; ++jp) {
-          uint32_t b[4];
-          ldsm_x4_t(vb + swz(lrow + ((lmat & 1) << 3), 2 * jp + (lmat >> 1)), b);
-          mma16816<T>(o[2 * jp], pa, b[0], b[1]);
-          mma16816<T>(o[2 * jp + 1], pa, b[2], b[3]);
+        for (int mt = 0; mt < MT; ++mt) {
+          uint32_t a[4];  // V^T: d chunks 2mt / 2mt+1, tokens 0-7 / 8-15
+          ldsm_x4_t(vb + swz(lrow + ((lmat >> 1) << 3), 2 * mt + (lmat & 1)), a);
+#pragma unroll
+          for (int nt = 0; nt < NTH; ++nt) mma16816<T>(o[mt][nt], a, pb[nt][0], pb[nt][1]);
         }
       }
       // generic-proxy stores (the zeroed rows) must be ordered before the next TMA write
-      if (nt_last_zeroed) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      if (zeroed) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&sm.empty[slot]));
     }
@@ -647,28 +665,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = false;
       break;
     }
-    if ((lane & 3) == 0) {
-      sm.xm[cw][r0] = m_run[0];
-      sm.xl[cw][r0] = l_run[0];
-      sm.xm[cw][r0 + 8] = m_run[1];
-      sm.xl[cw][r0 + 8] = l_run[1];
+    if (r0 == 0) {  // lanes 0..3 hold the running max/sum of heads 8*nt + qc, + 1
+#pragma unroll
+      for (int nt = 0; nt < NTH; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          sm.xm[cw][nt * 8 + qc + c] = m_run[nt][c];
+          sm.xl[cw][nt * 8 + qc + c] = l_run[nt][c];
+        }
     }
     const int slot_out = sg.cta_first ? 0 : 1;
     float* pacc = p.part_acc + (static_cast<size_t>(blockIdx.x) * 2 + slot_out) * kMaxHeads * D;
     float* pml = p.part_ml + (static_cast<size_t>(blockIdx.x) * 2 + slot_out) * kMaxHeads * 2;
     bool any_bad = false;
-    // Exchange O four heads (MMA rows) at a time: round r covers rows 4r..4r+3, held in
-    // c0,c1 by lanes with r0 in that range for rows < 8 and in c2,c3 for rows >= 8.
+    // Exchange O four heads at a time: round r covers heads 4r..4r+3.
     const int rounds = (ph.nh + 3) / 4;
     for (int round = 0; round < rounds; ++round) {
       if (round > 0) named_bar_sync(kBarConsumers, kConsumerThreads);  // previous reads done
       const int rbase = round * 4;
-      const int myrow = (rbase < 8) ? r0 : r0 + 8;
-      if (myrow >= rbase && myrow < rbase + 4) {
 #pragma unroll
-        for (int n = 0; n < NT; ++n) {
-          const float2 v = rbase < 8 ? make_float2(o[n][0], o[n][1]) : make_float2(o[n][2], o[n][3]);
-          *reinterpret_cast<float2*>(&sm.xo[cw][myrow - rbase][8 * n + qc]) = v;
+      for (int nt = 0; nt < NTH; ++nt) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int h = nt * 8 + qc + c;
+          if (h >= rbase && h < rbase + 4) {
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+              sm.xo[cw][h - rbase][16 * mt + r0] = o[mt][nt][c];
+              sm.xo[cw][h - rbase][16 * mt + r0 + 8] = o[mt][nt][c + 2];
+            }
+          }
         }
       }
       any_bad = bar_red_or(kBarConsumers, kConsumerThreads, seg_bad);
@@ -789,11 +815,11 @@ bool make_cache_map(CUtensorMap* map, const void* base, bool bf16, int head_dim,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, typename T>
+template <int D, int NTH, typename T>
 int launch(const Params& prm, const CUtensorMap& mk, const CUtensorMap& mv, int grid,
            cudaStream_t stream) {
   const size_t smem = sizeof(Smem<D>) + 1024;  // + alignment slack for the ring
-  auto* kern = decode_kernel<D, T>;
+  auto* kern = decode_kernel<D, NTH, T>;
   if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), smem)) return -3;
   kern<<<grid, kThreads, smem, stream>>>(prm, mk, mv);
   if (cudaGetLastError() != cudaSuccess) return -3;
@@ -861,12 +887,16 @@ int decode_launch(const DecodeArgs& a, int grid, cudaStream_t stream) {
   if (!decode::make_cache_map(&mk, a.k_cache, a.bf16, a.head_dim, rows, box_rows) ||
       !decode::make_cache_map(&mv, a.v_cache, a.bf16, a.head_dim, rows, box_rows))
     return -3;
-  if (a.head_dim == 128)
-    return a.bf16 ? decode::launch<128, __nv_bfloat16>(p, mk, mv, grid, stream)
-                  : decode::launch<128, __half>(p, mk, mv, grid, stream);
-  if (a.head_dim == 64)
-    return a.bf16 ? decode::launch<64, __nv_bfloat16>(p, mk, mv, grid, stream)
-                  : decode::launch<64, __half>(p, mk, mv, grid, stream);
+  // heads of a pair are MMA columns: one n-tile of 8, or two for up to 16
+#define PA_DECODE_CASE(DD, NN)                                                        \
+  if (a.head_dim == DD && (p.heads_per_pair > 8) == (NN == 2))                        \
+    return a.bf16 ? decode::launch<DD, NN, __nv_bfloat16>(p, mk, mv, grid, stream)    \
+                  : decode::launch<DD, NN, __half>(p, mk, mv, grid, stream);
+  PA_DECODE_CASE(128, 1)
+  PA_DECODE_CASE(128, 2)
+  PA_DECODE_CASE(64, 1)
+  PA_DECODE_CASE(64, 2)
+#undef PA_DECODE_CASE
   return -1;
 }
 
