@@ -10,9 +10,11 @@
 // Design (GB300: 152 SMs, HBM-bound at <= 1 FLOP/byte per query head):
 // * Work unit = a 16-token "stage" (K and V rows) of one (sequence, kv head, head chunk)
 //   pair, plus a fixed charge per pair.  The batch's units are cut into gridDim.x equal
-//   contiguous shares, one per persistent CTA (one CTA per SM), so SMs finish together.  A pair cut between CTAs is merged afterwards with a log-sum-exp reduction
-//   (split-KV: the rescaling identity of online softmax that chenyuan1125, section
-//   它和 FlashAttention…, names as FlashAttention's technique).  Cut points depend on
+//   contiguous shares, one per persistent CTA (one CTA per SM), so SMs finish together.  A pair cut between CTAs is merged with a log-sum-exp reduction by the CTA holding
+//   its first piece, once the later pieces (written first thing by the next CTAs) are
+//   published (split-KV: the rescaling identity of online softmax that chenyuan1125,
+//   section 它和 FlashAttention…, names as FlashAttention's technique).  The launch is
+//   cooperative, so all CTAs are resident; a CTA only waits for higher-numbered CTAs.  Cut points depend on
 //   logical positions and context lengths only, so permuting physical blocks (and the
 //   table with them) gives bit-identical output.
 // * One producer warp: lane i owns stage i of a batch of up to 8 stages, waits for its
@@ -32,7 +34,10 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+#include <chrono>
 #include <cstdint>
+#include <random>
 
 #include "pa_common.cuh"
 #include "pa_internal.h"
@@ -67,13 +72,6 @@ struct Geo {
   static constexpr int kNTiles = D / 8;                     // MMA n-tiles of P V
 };
 
-struct SplitRec {
-  int seq;         // -1: this CTA starts no split pair
-  int pair;        // kv head * head_chunks + head chunk
-  int c_last;      // last CTA holding a piece of the pair
-  int first_slot;  // partial slot of the starting CTA's piece
-};
-
 struct Params {
   const uint8_t* q;
   const int32_t* block_tables;
@@ -83,7 +81,8 @@ struct Params {
   int max_blocks_per_seq, block_size, log2_block, num_blocks, max_ctx;
   int seg_cost;  // work units charged per pair on top of its stages (see Walk)
   float scale_log2;
-  SplitRec* recs;
+  unsigned long long* flags;  // [grid]: epoch once the CTA's leading piece is written
+  unsigned long long epoch;   // unique per call
   float* part_acc;  // [grid][2][kMaxHeads][D]
   float* part_ml;   // [grid][2][kMaxHeads][2]  (m, l); l < 0 marks a piece with a bad block
   unsigned* err;
@@ -283,6 +282,58 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
                                (((chunk & 7) ^ (row & 7)) << 4));
 }
 
+__device__ __forceinline__ void st_release_gpu(unsigned long long* addr, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(addr), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire_gpu(const unsigned long long* addr) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(addr) : "memory");
+  return v;
+}
+
+// Spin (bounded by kWaitLimitNs) until *flag holds this call's epoch.
+__device__ __forceinline__ bool wait_flag_bounded(const unsigned long long* flag,
+                                                  unsigned long long epoch) {
+  if (ld_acquire_gpu(flag) == epoch) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (;;) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(flag) == epoch) return true;
+    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// Merge the pieces of a cut pair held by CTAs c..c_last (c's piece in slot `first_slot`,
+// the others in slot 0): M = max m_i, L = sum l_i 2^(m_i - M), out = sum acc_i 2^(m_i - M) / L,
+// pieces taken in CTA order (deterministic).  Zeros when a piece saw a bad block or a
+// wait for a piece gave up.
+template <int D, typename T>
+__device__ void merge_pieces(const Params& p, int c, int first_slot, int c_last, int nh, bool failed,
+                             T* out_rows, int tid, int nthreads) {
+  for (int i = tid; i < nh * D; i += nthreads) {
+    const int h = i / D;
+    const int d = i - h * D;
+    float M = -INFINITY;
+    bool bad = failed;
+    for (int cc = c; cc <= c_last; ++cc) {
+      const size_t base = static_cast<size_t>(cc) * 2 + (cc == c ? first_slot : 0);
+      const float* ml = p.part_ml + (base * kMaxHeads + h) * 2;
+      M = fmaxf(M, __ldcg(ml));
+      bad |= __ldcg(ml + 1) < 0.f;
+    }
+    float L = 0.f, o = 0.f;
+    for (int cc = c; cc <= c_last; ++cc) {
+      const size_t base = static_cast<size_t>(cc) * 2 + (cc == c ? first_slot : 0);
+      const float* ml = p.part_ml + (base * kMaxHeads + h) * 2;
+      const float w = exp2f(__ldcg(ml) - M);
+      L += __ldcg(ml + 1) * w;
+      o += __ldcg(p.part_acc + (base * kMaxHeads + h) * D + d) * w;
+    }
+    out_rows[h * D + d] = from_float<T>(bad ? 0.f : o / L);
+  }
+}
+
 template <int D>
 struct Smem {
   uint8_t ring[Geo<D>::kStages][Geo<D>::kStageBytes];  // 1024-byte aligned
@@ -314,9 +365,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int pairs_per_seq = p.num_kv_heads * p.head_chunks;
-
-  // Let the merge kernel launch early; it waits for this grid before reading anything.
-  pdl_launch_dependents();
 
   // ---- setup: total units W, this CTA's share, and the sequence where it starts ----
   if (tid == 0) {
@@ -499,8 +547,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t k = 0, qi = 0;
   bool ok = true;
   Seg sg;
-  int rec_seq = -1, rec_pair = 0, rec_last = 0, rec_slot = 0;
-
   while (next_seg(walk, sg)) {
     const PairHeads ph = pair_heads(p, sg.pair);
     T* out_rows =
@@ -735,56 +781,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (tid == 0 && any_bad) atomicOr(p.err, kErrBadBlock);
-    if (!sg.whole && sg.j0 == 0) {  // this CTA holds the first piece of a cut pair
-      rec_seq = sg.s;
-      rec_pair = sg.pair;
-      rec_last = owner_of(sg.pair_end - 1, W, G);
-      rec_slot = slot_out;
+    if (!sg.whole) {
+      __threadfence();  // this thread's partial writes, before the piece is published or merged
+      named_bar_sync(kBarConsumers, kConsumerThreads);
+      if (sg.j0 > 0) {
+        // A later piece of a cut pair (this share's first segment): publish it.
+        if (tid == 0) st_release_gpu(p.flags + blockIdx.x, p.epoch);
+      } else {
+        // The first piece (this share's last segment): wait for the later pieces, which
+        // the next CTAs wrote at the start of their shares, then merge in CTA order.
+        const int c_last = owner_of(sg.pair_end - 1, W, G);
+        bool waited_ok = true;
+        if (tid == 0) {
+          for (int cc = blockIdx.x + 1; cc <= c_last && waited_ok; ++cc)
+            waited_ok = wait_flag_bounded(p.flags + cc, p.epoch);
+          if (!waited_ok) atomicOr(p.err, kErrTimeout);
+        }
+        const bool failed = bar_red_or(kBarConsumers, kConsumerThreads, !waited_ok);
+        merge_pieces<D, T>(p, blockIdx.x, slot_out, c_last, ph.nh, failed, out_rows, tid,
+                           kConsumerThreads);
+      }
     }
+    if (tid == 0 && any_bad) atomicOr(p.err, kErrBadBlock);
   }
   if (!ok && tid == 0) atomicOr(p.err, kErrTimeout);
-  if (tid == 0) {
-    SplitRec r;
-    r.seq = ok ? rec_seq : -1;
-    r.pair = rec_pair;
-    r.c_last = rec_last;
-    r.first_slot = rec_slot;
-    p.recs[blockIdx.x] = r;
-  }
-}
-
-// Merge the pieces of every cut pair: M = max m_i, L = sum l_i 2^(m_i - M),
-// out = sum acc_i 2^(m_i - M) / L, pieces taken in CTA order (deterministic).
-template <int D, typename T>
-__global__ void __launch_bounds__(128) merge_kernel(const __grid_constant__ Params p) {
-  pdl_wait_primary();
-  const SplitRec r = p.recs[blockIdx.x];
-  if (r.seq < 0) return;
-  const PairHeads ph = pair_heads(p, r.pair);
-  T* out_rows = reinterpret_cast<T*>(p.out) + (static_cast<size_t>(r.seq) * p.num_q_heads + ph.h0) * D;
-  for (int i = threadIdx.x; i < ph.nh * D; i += blockDim.x) {
-    const int h = i / D;
-    const int d = i - h * D;
-    float M = -INFINITY;
-    bool bad = false;
-    for (int cc = blockIdx.x; cc <= r.c_last; ++cc) {
-      const int slot = (cc == static_cast<int>(blockIdx.x)) ? r.first_slot : 0;
-      const float* ml = p.part_ml + ((static_cast<size_t>(cc) * 2 + slot) * kMaxHeads + h) * 2;
-      M = fmaxf(M, ml[0]);
-      bad |= ml[1] < 0.f;
-    }
-    float L = 0.f, o = 0.f;
-    for (int cc = blockIdx.x; cc <= r.c_last; ++cc) {
-      const int slot = (cc == static_cast<int>(blockIdx.x)) ? r.first_slot : 0;
-      const size_t base = static_cast<size_t>(cc) * 2 + slot;
-      const float* ml = p.part_ml + (base * kMaxHeads + h) * 2;
-      const float w = exp2f(ml[0] - M);
-      L += ml[1] * w;
-      o += p.part_acc[(base * kMaxHeads + h) * D + d] * w;
-    }
-    out_rows[h * D + d] = from_float<T>(bad ? 0.f : o / L);
-  }
 }
 
 // Tensor map over one cache viewed as rows of D elements: [num_blocks * Hkv * B, D],
@@ -821,20 +841,19 @@ int launch(const Params& prm, const CUtensorMap& mk, const CUtensorMap& mv, int 
   const size_t smem = sizeof(Smem<D>) + 1024;  // + alignment slack for the ring
   auto* kern = decode_kernel<D, NTH, T>;
   if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), smem)) return -3;
-  kern<<<grid, kThreads, smem, stream>>>(prm, mk, mv);
-  if (cudaGetLastError() != cudaSuccess) return -3;
-
+  // Cooperative launch: every CTA is resident at once, so a CTA may wait (bounded) for the
+  // pieces that higher-numbered CTAs write at the start of their shares.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(128);
-  cfg.dynamicSmemBytes = 0;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, merge_kernel<D, T>, prm) != cudaSuccess) return -3;
+  if (cudaLaunchKernelEx(&cfg, kern, prm, mk, mv) != cudaSuccess) return -3;
   return 0;
 }
 
@@ -846,11 +865,21 @@ int decode_heads_per_pair(int num_q_heads, int num_kv_heads) {
 }
 
 size_t decode_workspace_bytes(int grid, int /*heads_per_pair*/, int head_dim) {
-  const size_t recs = static_cast<size_t>(grid) * sizeof(decode::SplitRec);
+  const size_t flags = static_cast<size_t>(grid) * sizeof(unsigned long long);
   const size_t acc = static_cast<size_t>(grid) * 2 * decode::kMaxHeads * head_dim * sizeof(float);
   const size_t ml = static_cast<size_t>(grid) * 2 * decode::kMaxHeads * 2 * sizeof(float);
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
-  return up(recs) + up(acc) + up(ml);
+  return up(flags) + up(acc) + up(ml);
+}
+
+// Epochs tag the pieces of one call: a flag in the (caller-owned, never cleared) workspace
+// counts only when it holds the current call's epoch.  64-bit values, random high half.
+static unsigned long long next_epoch() {
+  static std::atomic<unsigned long long> counter{
+      (static_cast<unsigned long long>(std::random_device{}()) << 32) ^
+      static_cast<unsigned long long>(
+          std::chrono::steady_clock::now().time_since_epoch().count())};
+  return counter.fetch_add(1, std::memory_order_relaxed) + 1;
 }
 
 int decode_launch(const DecodeArgs& a, int grid, cudaStream_t stream) {
@@ -875,8 +904,9 @@ int decode_launch(const DecodeArgs& a, int grid, cudaStream_t stream) {
   p.err = a.err;
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
-  p.recs = reinterpret_cast<decode::SplitRec*>(ws);
-  ws += up(static_cast<size_t>(grid) * sizeof(decode::SplitRec));
+  p.flags = reinterpret_cast<unsigned long long*>(ws);
+  ws += up(static_cast<size_t>(grid) * sizeof(unsigned long long));
+  p.epoch = next_epoch();
   p.part_acc = reinterpret_cast<float*>(ws);
   ws += up(static_cast<size_t>(grid) * 2 * decode::kMaxHeads * a.head_dim * sizeof(float));
   p.part_ml = reinterpret_cast<float*>(ws);
