@@ -2,8 +2,8 @@
 
 A step is one pass of the whole hot path over one batch: the cache write of each
 sequence's newest token (64 tokens through pa_reshape_and_cache) followed by paged decode
-attention over every sequence (pa_decode: the persistent decode kernel and its split-KV
-merge kernel).  Workload (seeded, synthetic; no dataset, no weights): 64 sequences,
+attention over every sequence (pa_decode: one persistent, cooperatively launched kernel
+that also merges the split-KV partials of sequences cut between CTAs).  Workload (seeded, synthetic; no dataset, no weights): 64 sequences,
 32 query / 8 kv heads, head_dim 128, bf16, block_size 16, context lengths uniform in
 [128, 2048], K/V ~ N(0,1), blocks placed through the block pool from a shuffled
 16384-block free list.  Three such batches live in disjoint blocks and steps rotate
@@ -385,7 +385,7 @@ def main():
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": "pa_decode (decode kernel + split-KV merge kernel)",
+            "kernel": "decode_kernel (pa_decode: persistent paged decode with in-kernel split-KV merge)",
             "achieved": round(achieved, 1),
             "peak": peak,
             "peak_kind": f"{peak_kind} (HBM copy)",
@@ -412,7 +412,7 @@ def main():
             "us_per_step": round(1e3 * res["e2e_ms"], 2),
         },
         "clocks": res["clocks"],
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 2 * args.steps,  # reshape_and_cache_kernel + decode_kernel per step
         "device_error_flags": res["flags"],
     }
     print(json.dumps(line))
