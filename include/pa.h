@@ -95,10 +95,10 @@ int pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void
  * 页表真正解开的…).  Accumulation is fp32; the output is rounded to nearest-even.
  *
  * Work is split into equal shares of 16-token K/V stages, one share per SM, so a long
- * sequence may be cut into pieces that a second kernel merges with a log-sum-exp
- * reduction (split-KV).  Cut points depend only on logical token positions and the
- * batch's context lengths, never on where blocks sit, so permuting physical blocks
- * (and the table with them) gives bit-identical output.
+ * sequence may be cut into pieces; the SM holding a pair's first piece merges them with
+ * a log-sum-exp reduction (split-KV) inside the same kernel.  Cut points depend only on
+ * logical token positions and the batch's context lengths, never on where blocks sit,
+ * so permuting physical blocks (and the table with them) gives bit-identical output.
  *
  * workspace: device scratch of at least pa_decode_workspace_size(...) bytes for the
  * split pieces, 16-byte aligned, owned by the caller, not read before it is written.
@@ -118,15 +118,16 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache,
  * may not call cudaMalloc at all -- a server that gave nearly all HBM to the KV block pool
  * up front, or a host framework that owns every device buffer -- and so cannot supply
  * pa_decode's workspace.  This call takes the same arguments minus the workspace and uses
- * a fixed 4 MiB scratch array built into the library instead (held on every GPU that loads
- * the library until the process exits).  It allocates nothing.
+ * a fixed 32 MiB scratch array built into the library instead (held on every GPU that
+ * loads the library until the process exits).  It allocates nothing.
  *   - Every call on a device shares that scratch and leaves its contents behind; nothing in
  *     it needs to start at zero.  Calls whose GPU work overlaps (unordered streams) race on
  *     it and give undefined output.
  *   - The first call on a device looks up the scratch's device address there; make that
  *     first call before any stream capture begins.
- *   - A device needing more than 4 MiB of decode scratch (very many SMs) gets
- *     PA_ERR_WORKSPACE and nothing is launched.  Other errors are pa_decode's.
+ *   - A device and head shape needing more than 32 MiB of decode scratch (more than about
+ *     250 SMs at 16 query heads per kv head and head_dim 128) gets PA_ERR_WORKSPACE and
+ *     nothing is launched.  Other errors are pa_decode's.
  */
 int pa_decode_fixed_scratch(const void* q, const void* k_cache, const void* v_cache,
                             const int32_t* block_tables, int max_blocks_per_seq,
@@ -135,7 +136,8 @@ int pa_decode_fixed_scratch(const void* q, const void* k_cache, const void* v_ca
                             float scale, void* out, pa_dtype dtype, cudaStream_t stream);
 
 /* Bytes of workspace pa_decode needs on the current device for these head counts.
- * It depends on the device's SM count and the head shape only, not on the batch. */
+ * It depends on the device's SM count and the head shape only, not on the batch
+ * (152 SMs: 5.1 MB for 32 query / 8 kv heads at head_dim 128, at most about 20 MB). */
 size_t pa_decode_workspace_size(int num_q_heads, int num_kv_heads, int head_dim);
 
 /*

@@ -113,8 +113,7 @@ size_t pa_decode_workspace_size(int num_q_heads, int num_kv_heads, int head_dim)
     return 0;
   DeviceInfo di;
   if (!device_info(&di)) return 0;
-  return pa::decode_workspace_bytes(di.sm_count, pa::decode_heads_per_pair(num_q_heads, num_kv_heads),
-                                    head_dim);
+  return pa::decode_workspace_bytes(di.sm_count, num_q_heads, num_kv_heads, head_dim);
 }
 
 int pa_decode(const void* q, const void* k_cache, const void* v_cache,
@@ -128,15 +127,15 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache,
       (dtype != PA_FP16 && dtype != PA_BF16) ||
       static_cast<long long>(max_blocks_per_seq) * block_size > 0x7fffffffLL ||
       static_cast<long long>(num_blocks) * num_kv_heads * block_size > 0x7fffffffLL)
-    return PA_ERR_ARG;  // (the last bound keeps TMA row coordinates within 32 bits)
+    return PA_ERR_ARG;  // (the last bound keeps cache row indices within 32 bits)
   if (num_seqs == 0) return PA_OK;
   if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PA_ERR_ARG;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
     return PA_ERR_ARG;
   DeviceInfo di;
   if (!device_info(&di)) return PA_ERR_CUDA;
-  const size_t need = pa::decode_workspace_bytes(
-      di.sm_count, pa::decode_heads_per_pair(num_q_heads, num_kv_heads), head_dim);
+  const size_t need =
+      pa::decode_workspace_bytes(di.sm_count, num_q_heads, num_kv_heads, head_dim);
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PA_ERR_WORKSPACE;
   pa::DecodeArgs a;
   a.q = q;

@@ -8,30 +8,36 @@
 // block by block).
 //
 // Design (GB300: 152 SMs, HBM-bound at <= 1 FLOP/byte per query head):
-// * Work unit = a 16-token "stage" (K and V rows) of one (sequence, kv head, head chunk)
-//   pair, plus a fixed charge per pair.  The batch's units are cut into gridDim.x equal
-//   contiguous shares, one per persistent CTA (one CTA per SM), so SMs finish together.  A pair cut between CTAs is merged with a log-sum-exp reduction by the CTA holding
-//   its first piece, once the later pieces (written first thing by the next CTAs) are
-//   published (split-KV: the rescaling identity of online softmax that chenyuan1125,
-//   section 它和 FlashAttention…, names as FlashAttention's technique).  The launch is
-//   cooperative, so all CTAs are resident; a CTA only waits for higher-numbered CTAs.  Cut points depend on
-//   logical positions and context lengths only, so permuting physical blocks (and the
-//   table with them) gives bit-identical output.
-// * One producer warp: lane i owns stage i of a batch of up to 8 stages, waits for its
-//   ring slot (stage kk belongs to consumer warp kk % 8, which owns a private set of
-//   slots and takes them in order), and issues TMA tensor copies (cp.async.bulk.tensor, 128-byte swizzle) of
-//   the stage's K and V rows; the next batch's block-table entries load meanwhile.  A
-//   2-slot side ring carries each pair's q rows (1-D bulk copy).
-// * Eight consumer warps take stages round-robin.  Warp-level tensor-core MMAs
-//   (m16n8k16, fp32 accumulate) with the pair's query heads as the N = 8 (or 16) columns:
-//   S^T = K Q^T (rows = the stage's 16 tokens), then O^T += V^T P^T (rows = d) with
-//   P = 2^(S - m) rounded to the input type and moved into B-fragment layout by an
-//   in-register transpose (movmatrix).  Each warp keeps its own running max/sum (online
-//   softmax); the eight warps merge at the end of each segment.  Swizzled smem makes
-//   every ldmatrix conflict-free.
-// * Every mbarrier wait is bounded (about 1 s) and sets PA_DEVERR_TIMEOUT on expiry;
-//   exits after a failed wait are decided collectively so no warp is left at a barrier.
-#include <cuda.h>
+// * A "pair" is one kv head (or a chunk of up to 16 of its query heads) of one sequence.
+//   The pairs of a sequence are taken in groups of gs (the largest power of two <= 8 that
+//   divides the pair count); a "family" is one sequence's group.  A family's work is
+//   ns(s) units of 16 tokens x gs pairs (a "stage" is one unit of one pair: 16 K rows and
+//   16 V rows), plus a fixed charge.  The batch's stages, in (family, unit, pair) order,
+//   are cut into gridDim.x equal contiguous shares, one per persistent CTA (one per SM).
+// * Warp w of a CTA works on pair w / P of every family (P = 8 / gs warps per pair, each
+//   taking every P-th unit).  With 8 or more kv heads (gs = 8) a warp owns one kv head
+//   outright: it streams its pair's stages straight across family boundaries and never
+//   waits for another warp.  With fewer, the P warps of a pair merge their partial
+//   softmax states through shared memory under a named barrier of their own.
+// * Loads: each warp copies its own stages, kAhead ahead of the one it computes, with
+//   16-byte cp.async copies (every lane copies a slice of the stage's K and V rows) into a
+//   private ring of swizzled shared-memory slots, and waits with cp.async.wait_group.
+//   Spreading the copies over all eight warps keeps enough bytes in flight per SM to reach
+//   the HBM limit; a single issuing warp, with TMA or with cp.async, streams about 26 GB/s
+//   per SM on GB300.  Rows past the context are zero-filled by the copy itself (source
+//   size 0) and never read.
+// * Math per stage on warp-level tensor cores (m16n8k16, fp32 accumulate) with the pair's
+//   query heads as the N = 8 (or 16) columns: S^T = K Q^T (rows = the stage's 16 tokens),
+//   then O^T += V^T P^T (rows = d) with P = 2^(S - m) rounded to the input type and moved
+//   into B-fragment layout by an in-register transpose (movmatrix); online softmax with a
+//   running max and sum per head.  The swizzle makes every ldmatrix conflict-free.
+// * A pair cut between CTAs (split-KV) is merged with a log-sum-exp reduction by the CTA
+//   holding its first piece, once the later pieces (written first thing by the next CTAs)
+//   are published (the rescaling identity of online softmax that chenyuan1125, section
+//   它和 FlashAttention…, names as FlashAttention's technique).  The launch is cooperative,
+//   so all CTAs are resident; a CTA only waits (bounded, about 1 s; PA_DEVERR_TIMEOUT and
+//   zeros on expiry) for higher-numbered CTAs.  Cut points depend on logical positions and
+//   context lengths only, so permuting physical blocks gives bit-identical output.
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -46,112 +52,104 @@ namespace pa {
 namespace decode {
 
 constexpr int kStageTok = 16;
-constexpr int kConsumerWarps = 8;
-constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
-constexpr int kBatch = 8;                        // stages the producer issues together
-constexpr int kMaxHeads = 16;                    // query heads per work pair (MMA rows)
-constexpr int kBarConsumers = 1;                 // named barrier id for the consumers
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kMaxHeads = 16;  // query heads per pair (MMA columns)
 constexpr float kLog2e = 1.4426950408889634f;
-// A pair costs its stages plus this many stage-equivalents of fixed work (q load, the
-// eight-warp merge and the output write at its end).  Charging it when cutting the batch
-// into per-SM shares keeps SMs whose shares hold many short pairs from finishing last.
-constexpr int kSegCost = 5;
+// Stage-equivalents charged per family on top of its stages (the q load and the output or
+// partial write at each pair's end) when cutting the batch into per-SM shares.
+constexpr int kSegCost = 2;
 
 template <int D>
 struct Geo {
-  static constexpr int kHalves = D / 64;                    // 128-byte column halves of a row
-  static constexpr int kBoxBytes = kStageTok * 128;         // 16 rows of one half
-  static constexpr int kKBytes = kHalves * kBoxBytes;       // K rows of a stage
+  static constexpr int kRowChunks = D / 8;                  // 16-byte chunks per row
+  static constexpr int kKBytes = kStageTok * D * 2;         // K rows of a stage
   static constexpr int kStageBytes = 2 * kKBytes;           // K then V
-  // Ring slots per consumer warp; each warp owns its slots, so every slot has a single
-  // consumer that takes its rounds in order and mbarrier parity waits are exact.
-  static constexpr int kSlotsPerWarp = (192 * 1024) / (kStageBytes * 8);
-  static constexpr int kStages = kSlotsPerWarp * 8;
-  static constexpr int kKSteps = D / 16;                    // MMA k-steps of Q K^T
-  static constexpr int kNTiles = D / 8;                     // MMA n-tiles of P V
+  // Ring slots per warp (192 KB in all) and how many stages ahead a warp loads.
+  static constexpr int kSlots = (192 * 1024) / (kStageBytes * kWarps);
+  static constexpr int kAhead = kSlots - 1;
+  static constexpr int kRowsPerPass = 32 / kRowChunks;      // rows one warp-wide copy covers
+  static constexpr int kPasses = kStageTok / kRowsPerPass;  // copies per lane per K (or V)
+  static constexpr int kKSteps = D / 16;                    // MMA k-steps of K Q^T
 };
 
 struct Params {
   const uint8_t* q;
+  const uint8_t* k_cache;
+  const uint8_t* v_cache;
   const int32_t* block_tables;
   const int32_t* context_lens;
   uint8_t* out;
   int num_seqs, num_q_heads, num_kv_heads, group, heads_per_pair, head_chunks;
+  int gs, log2_gs, ngroups, phases;  // pairs per family, families per sequence, warps per pair
   int max_blocks_per_seq, block_size, log2_block, num_blocks, max_ctx;
-  int seg_cost;  // work units charged per pair on top of its stages (see Walk)
+  int seg_cost;  // stage units charged per family on top of its stages
   float scale_log2;
-  unsigned long long* flags;  // [grid]: epoch once the CTA's leading piece is written
+  unsigned long long* flags;  // [grid][gs]: epoch once the CTA's leading piece of pair is written
   unsigned long long epoch;   // unique per call
-  float* part_acc;  // [grid][2][kMaxHeads][D]
-  float* part_ml;   // [grid][2][kMaxHeads][2]  (m, l); l < 0 marks a piece with a bad block
+  float* part_acc;  // [grid][2][gs][heads_per_pair][D]
+  float* part_ml;   // [grid][2][gs][heads_per_pair][2]  (m, l); l < 0: the piece saw a bad block
   unsigned* err;
 };
 
+// Units (16-token stages per pair) of a sequence; an invalid context length counts one.
 __device__ __forceinline__ int pair_stages(int ctx, int max_ctx) {
   return (ctx >= 1 && ctx <= max_ctx) ? (ctx + kStageTok - 1) / kStageTok : 1;
 }
 
-// Deterministic walk over this CTA's share [w, w1) of the batch's work units.  Pair p of
-// sequence s weighs ns(s) + seg_cost units: seg_cost leading units of fixed work, then one
-// unit per 16-token stage.  Sequence s holds pairs_per_seq such pairs.
-struct Walk {
-  const int32_t* ctx_lens;
-  int pairs_per_seq, max_ctx, seg_cost;
-  int s;
-  long long pre;  // first unit of sequence s
-  long long w, w0, w1;
-  bool first_done;  // a segment of this share has been returned already
+// Family (sequence s, pair group g) and its place in the batch's stage order.
+struct Fam {
+  int s, g, ctx, ns;
+  bool ok;        // 1 <= ctx <= max_ctx
+  long long pre;  // first stage unit of the family
+  long long fw;   // its weight: ns * gs + seg_cost
 };
 
-struct Seg {
-  int s, pair, ctx, ns;
-  int j0, j1;          // stage range within the pair
-  int ta, tb;          // token range [ta, tb)
-  bool bad_ctx;        // context length outside [1, max_ctx]
-  bool whole;          // the pair is not cut
-  bool cta_first;      // first segment of this CTA's share
-  long long pair_end;  // one past the pair's last unit
-};
-
-__device__ __forceinline__ bool next_seg(Walk& wk, Seg& sg) {
-  while (wk.w < wk.w1) {
-    const int ctx = __ldg(wk.ctx_lens + wk.s);
-    const int ns = pair_stages(ctx, wk.max_ctx);
-    const long long pw = ns + wk.seg_cost;
-    const long long units = static_cast<long long>(wk.pairs_per_seq) * pw;
-    if (wk.w >= wk.pre + units) {
-      wk.pre += units;
-      ++wk.s;
-      continue;
-    }
-    const long long local = wk.w - wk.pre;
-    const int pair = static_cast<int>(local / pw);
-    const long long pstart = wk.pre + pair * pw;
-    const long long end_w = min(wk.w1, pstart + pw);
-    const int j0 = static_cast<int>(max(0ll, local - pair * pw - wk.seg_cost));
-    const int j1 = static_cast<int>(max(0ll, end_w - pstart - wk.seg_cost));
-    wk.w = end_w;
-    if (j1 <= j0) continue;  // this share holds only the pair's fixed-cost units
-    sg.s = wk.s;
-    sg.ctx = ctx;
-    sg.ns = ns;
-    sg.pair = pair;
-    sg.j0 = j0;
-    sg.j1 = j1;
-    sg.bad_ctx = !(ctx >= 1 && ctx <= wk.max_ctx);
-    sg.ta = j0 * kStageTok;
-    sg.tb = sg.bad_ctx ? sg.ta : min(j1 * kStageTok, ctx);
-    sg.whole = (j0 == 0 && j1 == ns);
-    sg.cta_first = !wk.first_done;
-    wk.first_done = true;
-    sg.pair_end = pstart + pw;
-    return true;
-  }
-  return false;
+__device__ __forceinline__ void fam_load(Fam& f, const Params& p) {
+  f.ctx = __ldg(p.context_lens + f.s);
+  f.ok = f.ctx >= 1 && f.ctx <= p.max_ctx;
+  f.ns = pair_stages(f.ctx, p.max_ctx);
+  f.fw = static_cast<long long>(f.ns) * p.gs + p.seg_cost;
 }
 
-// Owner CTA of unit x when W units are cut into G shares, the first W % G one larger.
+__device__ __forceinline__ void fam_next(Fam& f, const Params& p) {
+  f.pre += f.fw;
+  if (++f.g == p.ngroups) {
+    f.g = 0;
+    if (++f.s < p.num_seqs) fam_load(f, p);
+  }
+}
+
+__device__ __forceinline__ bool fam_valid(const Fam& f) { return f.ok; }
+
+// ceil(x / 2^k) for any sign of x.
+__device__ __forceinline__ long long ceil_shift(long long x, int k) {
+  return x > 0 ? (x + (1ll << k) - 1) >> k : -((-x) >> k);
+}
+
+// Units [x, y) of pair pi of family f whose stages lie in the share [w0, w1).
+__device__ __forceinline__ int2 unit_range(const Fam& f, int pi, long long w0, long long w1,
+                                           const Params& p) {
+  const long long base = f.pre + p.seg_cost + pi;
+  const long long a = ceil_shift(w0 - base, p.log2_gs), b = ceil_shift(w1 - base, p.log2_gs);
+  return make_int2(static_cast<int>(max(0ll, min(static_cast<long long>(f.ns), a))),
+                   static_cast<int>(max(0ll, min(static_cast<long long>(f.ns), b))));
+}
+
+// Does this share hold a piece of the pair: some of its units, or none while the pair runs
+// on both sides of the share (an empty middle piece, published so the merge can count on it)?
+__device__ __forceinline__ bool has_piece(int2 r, int ns) {
+  return r.x < r.y || (r.x > 0 && r.x < ns);
+}
+
+// Share [w0, w1) of CTA c when W units are cut into G shares, the first W % G one larger.
+__device__ __forceinline__ void share_of(int c, long long W, int G, long long& w0, long long& w1) {
+  const long long q = W / G, r = W % G;
+  w0 = c * q + min(static_cast<long long>(c), r);
+  w1 = w0 + q + (c < r ? 1 : 0);
+}
+
+// Owner CTA of stage unit x.
 __device__ __forceinline__ int owner_of(long long x, long long W, int G) {
   const long long q = W / G, r = W % G;
   if (x < r * (q + 1)) return static_cast<int>(x / (q + 1));
@@ -171,64 +169,70 @@ __device__ __forceinline__ PairHeads pair_heads(const Params& p, int pair) {
   return ph;
 }
 
-// Batches (<= kBatch stages) of the segments of this CTA's share, skipping pairs with an
-// invalid context length (those carry no pipeline traffic).
-struct Batch {
-  int s, kvh, h0, nh, ca, cb;
-  bool seg_start;
+// This warp's stages in order: for every family of the share, the units of its pair with
+// unit index = its phase (mod P).  Families with an invalid context carry no stages.
+struct Stage {
+  int s, kvh, t0, nt;  // sequence, kv head, first token, valid tokens (1..16)
 };
 
-struct BatchIt {
-  Walk wk;
-  Seg sg;
-  int cpos;
-  bool have_seg;
+struct StageIt {
+  Fam f;
+  int kvh, j, jb;
 };
 
-__device__ __forceinline__ bool next_batch(BatchIt& it, Batch& b, const Params& p) {
+__device__ __forceinline__ void stage_it_enter(StageIt& it, int pi, int phase, long long w0,
+                                               long long w1, const Params& p) {
+  const int2 r = unit_range(it.f, pi, w0, w1, p);
+  if (!fam_valid(it.f) || r.x >= r.y) {
+    it.j = it.jb = 0;
+    return;
+  }
+  it.kvh = pair_heads(p, it.f.g * p.gs + pi).kvh;
+  it.j = r.x + (phase - r.x % p.phases + p.phases) % p.phases;
+  it.jb = r.y;
+}
+
+__device__ __forceinline__ bool next_stage(StageIt& it, int pi, int phase, long long w0, long long w1,
+                                           Stage& st, const Params& p) {
   for (;;) {
-    if (it.have_seg && it.cpos < it.sg.tb) {
-      const PairHeads ph = pair_heads(p, it.sg.pair);
-      b.s = it.sg.s;
-      b.kvh = ph.kvh;
-      b.h0 = ph.h0;
-      b.nh = ph.nh;
-      b.ca = it.cpos;
-      b.cb = min(it.cpos + kBatch * kStageTok, it.sg.tb);
-      b.seg_start = (it.cpos == it.sg.ta);
-      it.cpos = b.cb;
+    if (it.j < it.jb) {
+      st.s = it.f.s;
+      st.kvh = it.kvh;
+      st.t0 = it.j * kStageTok;
+      st.nt = min(kStageTok, it.f.ctx - st.t0);
+      it.j += p.phases;
       return true;
     }
-    if (!next_seg(it.wk, it.sg)) return false;
-    it.have_seg = !it.sg.bad_ctx;
-    it.cpos = it.sg.ta;
+    fam_next(it.f, p);
+    if (it.f.s >= p.num_seqs || it.f.pre >= w1) return false;
+    stage_it_enter(it, pi, phase, w0, w1, p);
   }
 }
 
-// Block-table entries of stage `lane` of batch `b`: x = the block holding the stage's
-// first token, y = the next block when the stage spans two blocks (block_size 8).
-__device__ __forceinline__ int2 stage_entries(const Batch& b, int lane, const Params& p) {
-  int2 e = make_int2(0, 0);
-  const int nst = (b.cb - b.ca + kStageTok - 1) / kStageTok;
-  if (lane < nst) {
-    const int t0 = b.ca + lane * kStageTok;
-    const int nt = min(kStageTok, b.cb - t0);
-    const int32_t* trow = p.block_tables + static_cast<size_t>(b.s) * p.max_blocks_per_seq;
-    const int j0 = t0 >> p.log2_block;
-    e.x = __ldg(trow + j0);
-    if ((t0 & (p.block_size - 1)) + nt > p.block_size) e.y = __ldg(trow + j0 + 1);
-  }
+// Block-table entries of a stage: x = the block holding its first token, y = the next
+// block when the stage spans two blocks (block_size 8), else x.
+__device__ __forceinline__ int2 stage_entries(const Stage& st, const Params& p) {
+  const int32_t* trow = p.block_tables + static_cast<size_t>(st.s) * p.max_blocks_per_seq;
+  const int j0 = st.t0 >> p.log2_block;
+  int2 e;
+  e.x = __ldg(trow + j0);
+  e.y = ((st.t0 & (p.block_size - 1)) + st.nt > p.block_size) ? __ldg(trow + j0 + 1) : e.x;
   return e;
 }
 
-// 2-D TMA tile load (box of the tensor map at column x, row y) into swizzled smem.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
+// 16-byte global -> shared copy through L2 only; the bytes past src_bytes (0 or 16) are
+// zero-filled, and src_bytes = 0 reads nothing.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
@@ -305,86 +309,166 @@ __device__ __forceinline__ bool wait_flag_bounded(const unsigned long long* flag
 }
 
 // Merge the pieces of a cut pair held by CTAs c..c_last (c's piece in slot `first_slot`,
-// the others in slot 0): M = max m_i, L = sum l_i 2^(m_i - M), out = sum acc_i 2^(m_i - M) / L,
-// pieces taken in CTA order (deterministic).  Zeros when a piece saw a bad block or a
-// wait for a piece gave up.
+// the others in slot 0), taken in CTA order so the result is deterministic:
+//   (M, L, O) <- (max(M, m_i), L a + l_i b, O a + acc_i b),  a = 2^(M - M'), b = 2^(m_i - M'),
+// then out = O / L (the log-sum-exp rescaling of online softmax).  Empty pieces (m = -inf)
+// are skipped; zeros when a piece saw a bad block or a wait for a piece gave up.  Each
+// thread takes one 4-float column chunk of up to 4 heads and loads 4 pieces of each at a
+// time, so the L2 round trips overlap instead of queueing one behind another.
 template <int D, typename T>
-__device__ void merge_pieces(const Params& p, int c, int first_slot, int c_last, int nh, bool failed,
-                             T* out_rows, int tid, int nthreads) {
-  for (int i = tid; i < nh * D; i += nthreads) {
-    const int h = i / D;
-    const int d = i - h * D;
-    float M = -INFINITY;
-    bool bad = failed;
-    for (int cc = c; cc <= c_last; ++cc) {
-      const size_t base = static_cast<size_t>(cc) * 2 + (cc == c ? first_slot : 0);
-      const float* ml = p.part_ml + (base * kMaxHeads + h) * 2;
-      M = fmaxf(M, __ldcg(ml));
-      bad |= __ldcg(ml + 1) < 0.f;
+__device__ void merge_pieces(const Params& p, int pi, int c, int first_slot, int c_last, int nh,
+                             bool failed, T* out_rows, int gt, int gthreads) {
+  constexpr int C4 = D / 4;  // 4-float chunks per head row
+  constexpr int HB = 4;      // heads per pass
+  constexpr int PB = 4;      // pieces per load round
+  const int hpp = p.heads_per_pair;
+  const int hstep = gthreads / C4;  // heads the group covers side by side
+  const int d4 = (gt % C4) * 4;
+  for (int hb = gt / C4; hb < nh; hb += hstep * HB) {
+    float M[HB], L[HB];
+    float4 O[HB];
+    bool bad[HB];
+#pragma unroll
+    for (int k = 0; k < HB; ++k) {
+      M[k] = -INFINITY;
+      L[k] = 0.f;
+      O[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      bad[k] = failed;
     }
-    float L = 0.f, o = 0.f;
-    for (int cc = c; cc <= c_last; ++cc) {
-      const size_t base = static_cast<size_t>(cc) * 2 + (cc == c ? first_slot : 0);
-      const float* ml = p.part_ml + (base * kMaxHeads + h) * 2;
-      const float w = exp2f(__ldcg(ml) - M);
-      L += __ldcg(ml + 1) * w;
-      o += __ldcg(p.part_acc + (base * kMaxHeads + h) * D + d) * w;
+    for (int cc0 = c; cc0 <= c_last; cc0 += PB) {
+      float m[PB][HB], l[PB][HB];
+      float4 a[PB][HB];
+#pragma unroll
+      for (int i = 0; i < PB; ++i) {
+        const int cc = cc0 + i;
+        const size_t piece = (static_cast<size_t>(cc) * 2 + (cc == c ? first_slot : 0)) * p.gs + pi;
+#pragma unroll
+        for (int k = 0; k < HB; ++k) {
+          const int h = hb + k * hstep;
+          if (cc <= c_last && h < nh) {
+            const float* ml = p.part_ml + (piece * hpp + h) * 2;
+            m[i][k] = __ldcg(ml);
+            l[i][k] = __ldcg(ml + 1);
+            a[i][k] = __ldcg(reinterpret_cast<const float4*>(p.part_acc + (piece * hpp + h) * D + d4));
+          } else {
+            m[i][k] = -INFINITY;
+            l[i][k] = 0.f;
+            a[i][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < PB; ++i)
+#pragma unroll
+        for (int k = 0; k < HB; ++k) {
+          bad[k] |= l[i][k] < 0.f;
+          if (m[i][k] != -INFINITY) {
+            const float mn = fmaxf(M[k], m[i][k]);
+            const float sa = exp2f(M[k] - mn), sb = exp2f(m[i][k] - mn);
+            L[k] = L[k] * sa + l[i][k] * sb;
+            O[k].x = O[k].x * sa + a[i][k].x * sb;
+            O[k].y = O[k].y * sa + a[i][k].y * sb;
+            O[k].z = O[k].z * sa + a[i][k].z * sb;
+            O[k].w = O[k].w * sa + a[i][k].w * sb;
+            M[k] = mn;
+          }
+        }
     }
-    out_rows[h * D + d] = from_float<T>(bad ? 0.f : o / L);
+#pragma unroll
+    for (int k = 0; k < HB; ++k) {
+      const int h = hb + k * hstep;
+      if (h < nh) {
+        uint2 packed = make_uint2(0u, 0u);
+        if (!bad[k]) {
+          const float inv = 1.f / L[k];
+          packed.x = pack2<T>(O[k].x * inv, O[k].y * inv);
+          packed.y = pack2<T>(O[k].z * inv, O[k].w * inv);
+        }
+        *reinterpret_cast<uint2*>(out_rows + h * D + d4) = packed;
+      }
+    }
   }
 }
 
 template <int D>
 struct Smem {
-  uint8_t ring[Geo<D>::kStages][Geo<D>::kStageBytes];  // 1024-byte aligned
-  uint8_t qbuf[2][kMaxHeads * D * 2];
-  float xo[kConsumerWarps][4][D];  // per-warp O rows, 4 heads per exchange round
-  float xm[kConsumerWarps][kMaxHeads], xl[kConsumerWarps][kMaxHeads];
-  long long scan[kThreads / 32];
+  uint8_t ring[kWarps][Geo<D>::kSlots][Geo<D>::kStageBytes];  // 1024-byte aligned
+  float xo[kWarps][4][D];  // per-warp O rows, 4 heads per exchange round
+  float xm[kWarps][kMaxHeads], xl[kWarps][kMaxHeads];
+  long long scan[kWarps];
   long long start_pre;
   int start_s;
-  int slot_bad[Geo<D>::kStages];
-  int abort_flag;
-  unsigned long long full[Geo<D>::kStages], empty[Geo<D>::kStages];
-  unsigned long long qfull[2], qempty[2];
 };
 
+// Q^T of a pair as MMA B fragments (column n = head 8*nt + lane / 4; heads >= nh are zero).
+template <int D, int NTH>
+__device__ __forceinline__ void load_q(const Params& p, int s, int h0, int nh, int lane,
+                                       uint32_t (&qb)[D / 16][NTH][2]) {
+  const int r0 = lane >> 2, qc = 2 * (lane & 3);
+  const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+      p.q + (static_cast<size_t>(s) * p.num_q_heads + h0) * D * 2);
+#pragma unroll
+  for (int nt = 0; nt < NTH; ++nt) {
+    const int h = nt * 8 + r0;
+    const bool hv = h < nh;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      const int col = 16 * ks + qc;
+      qb[ks][nt][0] = hv ? __ldg(qrow + (h * D + col) / 2) : 0u;
+      qb[ks][nt][1] = hv ? __ldg(qrow + (h * D + col + 8) / 2) : 0u;
+    }
+  }
+}
+
+// The next family (after f) where pair pi has units to compute; false at the share's end.
+__device__ __forceinline__ bool next_busy_fam(Fam f, int pi, long long w0, long long w1,
+                                              const Params& p, Fam& out) {
+  for (;;) {
+    fam_next(f, p);
+    if (f.s >= p.num_seqs || f.pre >= w1) return false;
+    const int2 r = unit_range(f, pi, w0, w1, p);
+    if (fam_valid(f) && r.x < r.y) {
+      out = f;
+      return true;
+    }
+  }
+}
+
 template <int D, int NTH, typename T>
-__global__ void __launch_bounds__(kThreads, 1)
-    decode_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmap_k,
-                  const __grid_constant__ CUtensorMap tmap_v) {
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ Params p) {
   using G_ = Geo<D>;
-  constexpr int S = G_::kStages;
-  constexpr int R = G_::kSlotsPerWarp;
+  constexpr int R = G_::kSlots;
+  constexpr int KS = G_::kKSteps;
+  constexpr int MT = D / 16;  // m-tiles of O^T (16 rows of d each)
   extern __shared__ uint8_t smem_raw[];
-  // the 128-byte swizzle pattern repeats every 1024 bytes: align the ring to it
   const uint32_t raw_addr = smem_addr(smem_raw);
   Smem<D>& sm = *reinterpret_cast<Smem<D>*>(smem_raw + (((raw_addr + 1023) & ~1023u) - raw_addr));
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int pairs_per_seq = p.num_kv_heads * p.head_chunks;
+  const int P = p.phases;
+  const int pi = warp / P;     // this warp's pair within each family
+  const int phase = warp % P;  // and its units: unit index = phase (mod P)
+  const int gt = phase * 32 + lane;  // thread index within the pair's P warps
+  const int gthreads = P * 32;
+  // the pair's P warps: their own named barrier (ids 1..8), or just the warp when P = 1
+  auto gsync = [&]() {
+    if (P == 1) __syncwarp();
+    else named_bar_sync(1 + pi, gthreads);
+  };
+  auto gor = [&](bool v) -> bool {
+    return P == 1 ? (__any_sync(0xffffffffu, v) != 0) : bar_red_or(1 + pi, gthreads, v);
+  };
 
-  // ---- setup: total units W, this CTA's share, and the sequence where it starts ----
-  if (tid == 0) {
-    for (int i = 0; i < S; ++i) {
-      mbar_init(smem_addr(&sm.full[i]), 1);
-      mbar_init(smem_addr(&sm.empty[i]), 1);  // the consuming warp
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_addr(&sm.qfull[i]), 1);
-      mbar_init(smem_addr(&sm.qempty[i]), kConsumerWarps);
-    }
-    sm.abort_flag = 0;
-    fence_mbar_init();
-  }
+  // ---- setup: total units W, this CTA's share [w0, w1), and its first family ----
   const int per = (p.num_seqs + kThreads - 1) / kThreads;
   const int sa = min(p.num_seqs, tid * per), sb = min(p.num_seqs, sa + per);
   long long mine = 0;
   for (int s = sa; s < sb; ++s)
-    mine += static_cast<long long>(pairs_per_seq) *
-            (pair_stages(__ldg(p.context_lens + s), p.max_ctx) + p.seg_cost);
+    mine += static_cast<long long>(p.ngroups) *
+            (static_cast<long long>(pair_stages(__ldg(p.context_lens + s), p.max_ctx)) * p.gs +
+             p.seg_cost);
   long long incl = mine;  // inclusive scan of `mine` over the block
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -394,22 +478,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (lane == 31) sm.scan[warp] = incl;
   __syncthreads();
   long long before = 0, W = 0;
-  for (int w = 0; w < kThreads / 32; ++w) {
+  for (int w = 0; w < kWarps; ++w) {
     if (w < warp) before += sm.scan[w];
     W += sm.scan[w];
   }
   const long long excl = before + incl - mine;
   const int G = gridDim.x;
   const int c = blockIdx.x;
-  const long long qd = W / G, rm = W % G;
-  const long long w0 = c * qd + min(static_cast<long long>(c), rm);
-  const long long w1 = w0 + qd + (c < rm ? 1 : 0);
+  long long w0, w1;
+  share_of(c, W, G, w0, w1);
   if (w0 < w1 && excl <= w0 && w0 < excl + mine) {
     long long pre = excl;
     int s = sa;
     for (;; ++s) {
-      const long long u = static_cast<long long>(pairs_per_seq) *
-                          (pair_stages(__ldg(p.context_lens + s), p.max_ctx) + p.seg_cost);
+      const long long u = static_cast<long long>(p.ngroups) *
+                          (static_cast<long long>(pair_stages(__ldg(p.context_lens + s), p.max_ctx)) *
+                               p.gs + p.seg_cost);
       if (w0 < pre + u) break;
       pre += u;
     }
@@ -417,172 +501,118 @@ __global__ void __launch_bounds__(kThreads, 1)
     sm.start_pre = pre;
   }
   __syncthreads();
+  if (w0 >= w1) return;  // more CTAs than units: nothing here (uniform over the CTA)
 
-  Walk walk;
-  walk.ctx_lens = p.context_lens;
-  walk.pairs_per_seq = pairs_per_seq;
-  walk.max_ctx = p.max_ctx;
-  walk.seg_cost = p.seg_cost;
-  walk.first_done = false;
-  walk.s = (w0 < w1) ? sm.start_s : 0;
-  walk.pre = (w0 < w1) ? sm.start_pre : 0;
-  walk.w = w0;
-  walk.w0 = w0;
-  walk.w1 = w1;
-  const volatile int* abort_flag = &sm.abort_flag;
-
-  if (warp == kConsumerWarps) {
-    // =============================== producer warp ===============================
-    BatchIt it;
-    it.wk = walk;
-    it.cpos = 0;
-    it.have_seg = false;
-    Batch cur, nxt;
-    bool has_cur = next_batch(it, cur, p);
-    int2 e_cur = has_cur ? stage_entries(cur, lane, p) : make_int2(0, 0);
-    const int box_rows = min(p.block_size, kStageTok);
-    const uint32_t box_bytes = box_rows * 128;
-    uint32_t k = 0, qi = 0;
-    bool ok = true, issued = false;
-    while (ok && has_cur) {
-      issued = false;
-      const bool has_nxt = next_batch(it, nxt, p);
-      const int2 e_nxt = has_nxt ? stage_entries(nxt, lane, p) : make_int2(0, 0);
-      if (cur.seg_start) {  // the pair's q rows, contiguous in q
-        if (lane == 0) {
-          const uint32_t qs = qi & 1;
-          ok = mbar_wait_bounded(smem_addr(&sm.qempty[qs]), ((qi >> 1) & 1) ^ 1, abort_flag);
-          if (ok) {
-            const uint32_t bytes = cur.nh * D * 2;
-            mbar_arrive_expect_tx(smem_addr(&sm.qfull[qs]), bytes);
-            bulk_g2s(smem_addr(sm.qbuf[qs]),
-                     p.q + (static_cast<size_t>(cur.s) * p.num_q_heads + cur.h0) * D * 2, bytes,
-                     smem_addr(&sm.qfull[qs]));
-          }
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        ++qi;
-        if (!ok) break;
-      }
-      const int nst = (cur.cb - cur.ca + kStageTok - 1) / kStageTok;
-      if (lane < nst) {
-        const int t0 = cur.ca + lane * kStageTok;
-        const int nt = min(kStageTok, cur.cb - t0);
-        const int row0 = t0 & (p.block_size - 1);
-        const bool two = row0 + nt > p.block_size;  // block_size 8: a second block
-        const bool bad = e_cur.x < 0 || e_cur.x >= p.num_blocks ||
-                         (two && (e_cur.y < 0 || e_cur.y >= p.num_blocks));
-        const uint32_t kk = k + lane;
-        const uint32_t u = kk / kConsumerWarps;  // round-robin: warp kk % 8, its u-th stage
-        const uint32_t slot = (kk % kConsumerWarps) * R + u % R;
-        ok = mbar_wait_bounded(smem_addr(&sm.empty[slot]), ((u / R) & 1) ^ 1, abort_flag);
-        if (ok) {
-          const uint32_t fbar = smem_addr(&sm.full[slot]);
-          if (bad) {
-            sm.slot_bad[slot] = 1;
-            mbar_arrive(fbar);
-          } else {
-            sm.slot_bad[slot] = 0;
-            const int nboxes = two ? 2 : 1;
-            mbar_arrive_expect_tx(fbar, 2 * G_::kHalves * nboxes * box_bytes);
-            const uint32_t base = smem_addr(sm.ring[slot]);
-            const int y0 = (e_cur.x * p.num_kv_heads + cur.kvh) * p.block_size + row0;
-            const int y1 = (e_cur.y * p.num_kv_heads + cur.kvh) * p.block_size;
-#pragma unroll
-            for (int hf = 0; hf < G_::kHalves; ++hf) {
-              const uint32_t kd = base + hf * G_::kBoxBytes;
-              const uint32_t vd = kd + G_::kKBytes;
-              tma_load_2d(kd, &tmap_k, hf * 64, y0, fbar);
-              tma_load_2d(vd, &tmap_v, hf * 64, y0, fbar);
-              if (two) {
-                tma_load_2d(kd + box_bytes, &tmap_k, hf * 64, y1, fbar);
-                tma_load_2d(vd + box_bytes, &tmap_v, hf * 64, y1, fbar);
-              }
-            }
-          }
-          issued = true;
-        }
-      }
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      k += nst;
-      cur = nxt;
-      e_cur = e_nxt;
-      has_cur = has_nxt;
-    }
-    if (!ok) {
-      // A wait gave up: stop everyone, then let the copies already issued land (the last
-      // S stages before this batch, plus this batch's stages whose lanes issued them).
-      int zero = 0;
-      const volatile int* never = &zero;
-      if (lane == 0) {
-        sm.abort_flag = 1;
-        atomicOr(p.err, kErrTimeout);
-      }
-      auto slot_of = [&](uint32_t kk) { return (kk % kConsumerWarps) * R + (kk / kConsumerWarps) % R; };
-      auto parity_of = [&](uint32_t kk) { return ((kk / kConsumerWarps) / R) & 1; };
-      if (issued) mbar_wait_bounded(smem_addr(&sm.full[slot_of(k + lane)]), parity_of(k + lane), never);
-      if (lane == 0) {
-        const uint32_t first = k > static_cast<uint32_t>(S) ? k - S : 0;
-        for (uint32_t kk = first; kk < k; ++kk)
-          mbar_wait_bounded(smem_addr(&sm.full[slot_of(kk)]), parity_of(kk), never);
-        for (uint32_t qq = qi > 2 ? qi - 2 : 0; qq < qi; ++qq)
-          mbar_wait_bounded(smem_addr(&sm.qfull[qq & 1]), (qq >> 1) & 1, never);
-      }
-    }
-    return;
+  Fam first;
+  first.s = sm.start_s;
+  first.g = 0;
+  first.pre = sm.start_pre;
+  fam_load(first, p);
+  while (w0 >= first.pre + first.fw) {  // the family holding unit w0
+    first.pre += first.fw;
+    ++first.g;
   }
 
-  // ================================ consumer warps ================================
-  // Control flow of the eight consumer warps stays identical: every exit taken after a
-  // failed wait is decided collectively at a named barrier (bar.red.or).
-  constexpr int KS = G_::kKSteps;
-  constexpr int MT = D / 16;  // m-tiles of O^T (16 rows of d each)
-  const int cw = warp;
-  const int r0 = lane >> 2;        // MMA row of this lane (query head r0, and r0 + 8)
+  // ---- this warp's copy stream: kAhead stages in flight ahead of the one computed ----
+  const uint32_t ring = smem_addr(sm.ring[warp][0]);
+  const int ch = lane % G_::kRowChunks;    // this lane's 16-byte column chunk of a row
+  const int rsub = lane / G_::kRowChunks;  // and its first row
+  StageIt sit;
+  sit.f = first;
+  stage_it_enter(sit, pi, phase, w0, w1, p);
+  Stage nxt;
+  bool nxt_ok = next_stage(sit, pi, phase, w0, w1, nxt, p);
+  int2 nxt_e = nxt_ok ? stage_entries(nxt, p) : make_int2(0, 0);
+  uint32_t issued = 0;   // stages this warp has issued (slot = count % R)
+  uint32_t badbits = 0;  // slots whose stage has an out-of-range block id
+
+  auto issue_one = [&]() {
+    if (nxt_ok) {
+      const uint32_t slot = issued % R;
+      const bool two = (nxt.t0 & (p.block_size - 1)) + nxt.nt > p.block_size;
+      const bool bad = nxt_e.x < 0 || nxt_e.x >= p.num_blocks ||
+                       (two && (nxt_e.y < 0 || nxt_e.y >= p.num_blocks));
+      badbits = bad ? (badbits | (1u << slot)) : (badbits & ~(1u << slot));
+      if (!bad) {
+        const uint32_t dst = ring + slot * G_::kStageBytes;
+        const int row0 = nxt.t0 & (p.block_size - 1);
+        const size_t row_x = static_cast<size_t>((nxt_e.x * p.num_kv_heads + nxt.kvh) * p.block_size);
+        const size_t row_y = static_cast<size_t>((nxt_e.y * p.num_kv_heads + nxt.kvh) * p.block_size);
+#pragma unroll
+        for (int j = 0; j < G_::kPasses; ++j) {
+          const int row = rsub + j * G_::kRowsPerPass;
+          const int r = row0 + row;
+          const bool live = row < nxt.nt;
+          // rows past the context: zero-filled, nothing read (the source stays in block x)
+          const size_t grow = !live ? row_x : (r < p.block_size ? row_x + r : row_y + (r - p.block_size));
+          const size_t src = (grow * D + ch * 8) * 2;
+          const uint32_t so = swz(row, ch);
+          cp_async16(dst + so, p.k_cache + src, live ? 16u : 0u);
+          cp_async16(dst + G_::kKBytes + so, p.v_cache + src, live ? 16u : 0u);
+        }
+      }
+      ++issued;
+      nxt_ok = next_stage(sit, pi, phase, w0, w1, nxt, p);
+      if (nxt_ok) nxt_e = stage_entries(nxt, p);
+    }
+    cp_async_commit();  // one group per call, empty or not
+  };
+#pragma unroll
+  for (int a = 0; a < G_::kAhead; ++a) issue_one();
+
+  const int r0 = lane >> 2;        // MMA row of this lane
   const int qc = 2 * (lane & 3);   // MMA column pair of this lane
   const int lrow = lane & 7;       // ldmatrix: row within an 8x8 matrix
   const int lmat = lane >> 3;      // ldmatrix: which of the four matrices
 
-  uint32_t k = 0, qi = 0;
-  bool ok = true;
-  Seg sg;
-  while (next_seg(walk, sg)) {
-    const PairHeads ph = pair_heads(p, sg.pair);
+  // q of the first family where this pair computes; later ones are loaded a family ahead
+  uint32_t qn[KS][NTH][2];
+  {
+    const int2 r = unit_range(first, pi, w0, w1, p);
+    Fam qf;
+    bool have = fam_valid(first) && r.x < r.y;
+    if (have) qf = first;
+    else have = next_busy_fam(first, pi, w0, w1, p, qf);
+    if (have) {
+      const PairHeads ph = pair_heads(p, qf.g * p.gs + pi);
+      load_q<D, NTH>(p, qf.s, ph.h0, ph.nh, lane, qn);
+    }
+  }
+
+  uint32_t used = 0;  // stages this warp has computed
+  bool cta_first = true;
+  for (Fam f = first; f.s < p.num_seqs && f.pre < w1; fam_next(f, p), cta_first = false) {
+    const int2 r = unit_range(f, pi, w0, w1, p);
+    if (!has_piece(r, f.ns)) continue;
+    const PairHeads ph = pair_heads(p, f.g * p.gs + pi);
     T* out_rows =
-        reinterpret_cast<T*>(p.out) + (static_cast<size_t>(sg.s) * p.num_q_heads + ph.h0) * D;
-    if (sg.bad_ctx) {  // no pipeline traffic for this pair: zeros and a flag
-      for (int i = tid; i < ph.nh * D / 8; i += kConsumerThreads)
-        reinterpret_cast<uint4*>(out_rows)[i] = make_uint4(0, 0, 0, 0);
-      if (tid == 0) atomicOr(p.err, kErrBadContext);
+        reinterpret_cast<T*>(p.out) + (static_cast<size_t>(f.s) * p.num_q_heads + ph.h0) * D;
+    if (!fam_valid(f)) {  // invalid context length: the unit-0 holder writes zeros
+      if (r.x == 0 && r.x < r.y) {
+        for (int i = gt; i < ph.nh * D / 8; i += gthreads)
+          reinterpret_cast<uint4*>(out_rows)[i] = make_uint4(0, 0, 0, 0);
+        if (gt == 0) atomicOr(p.err, kErrBadContext);
+      }
       continue;
     }
-
-    // ---- Q^T of the pair as MMA B fragments: column n = head 8*nt + (lane >> 2) ----
-    // (heads >= nh are zero)
+    const bool computes = r.x < r.y;  // (an empty middle piece computes nothing)
     uint32_t qb[KS][NTH][2];
-    {
-      const uint32_t qs = qi & 1;
-      ok = __all_sync(0xffffffffu, ok && mbar_wait_bounded(smem_addr(&sm.qfull[qs]),
-                                                            (qi >> 1) & 1, abort_flag));
-      const uint8_t* qbuf = sm.qbuf[qs];
+    if (computes) {
 #pragma unroll
-      for (int nt = 0; nt < NTH; ++nt) {
-        const int h = nt * 8 + r0;
-        const bool hv = ok && h < ph.nh;
+      for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-          const int col = 16 * ks + qc;
-          qb[ks][nt][0] = hv ? *reinterpret_cast<const uint32_t*>(qbuf + (h * D + col) * 2) : 0u;
-          qb[ks][nt][1] = hv ? *reinterpret_cast<const uint32_t*>(qbuf + (h * D + col + 8) * 2) : 0u;
+        for (int nt = 0; nt < NTH; ++nt) {
+          qb[ks][nt][0] = qn[ks][nt][0];
+          qb[ks][nt][1] = qn[ks][nt][1];
         }
+      Fam qf;
+      if (next_busy_fam(f, pi, w0, w1, p, qf)) {
+        const PairHeads lh = pair_heads(p, qf.g * p.gs + pi);
+        load_q<D, NTH>(p, qf.s, lh.h0, lh.nh, lane, qn);
       }
-      __syncwarp();
-      if (ok && lane == 0) mbar_arrive(smem_addr(&sm.qempty[qs]));
-      if (!ok) sm.abort_flag = 1;
-      ++qi;
     }
-    // This lane's softmax columns: heads hc0 = 8*nt + qc and hc0 + 1 of every n-tile.
+
+    // This lane's softmax columns: heads 8*nt + qc and + 1 of every n-tile.
     float m_run[NTH][2], l_run[NTH][2];
     float o[MT][NTH][4];  // O^T: rows d = 16*mt + r0 (+8), columns = heads
 #pragma unroll
@@ -594,28 +624,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     bool seg_bad = false;
 
-    const int nstage = (sg.tb - sg.ta + kStageTok - 1) / kStageTok;
-    // this warp's stages: global index k + i with (k + i) % 8 == cw
-    for (int i = (cw - static_cast<int>(k % kConsumerWarps) + kConsumerWarps) % kConsumerWarps;
-         ok && i < nstage; i += kConsumerWarps) {
-      const uint32_t u = (k + i) / kConsumerWarps;  // this warp's u-th stage
-      const uint32_t slot = cw * R + u % R;
-      ok = __all_sync(0xffffffffu,
-                      mbar_wait_bounded(smem_addr(&sm.full[slot]), (u / R) & 1, abort_flag));
-      if (!ok) break;
-      const int nt_tok = min(kStageTok, sg.tb - (sg.ta + i * kStageTok));
-      bool zeroed = false;
-      if (sm.slot_bad[slot]) {
+    const int j_first = r.x + (phase - r.x % P + P) % P;
+    for (int j = j_first; j < r.y; j += P) {
+      issue_one();                   // stage used + kAhead goes in flight
+      cp_async_wait<G_::kAhead>();   // this lane's copies of stage `used` have landed
+      __syncwarp();                  // ... and every other lane's
+      const uint32_t slot = used % R;
+      ++used;
+      const int nt_tok = min(kStageTok, f.ctx - j * kStageTok);
+      if (badbits & (1u << slot)) {
         seg_bad = true;
       } else {
-        const uint32_t kb = smem_addr(sm.ring[slot]);
+        const uint32_t kb = ring + slot * G_::kStageBytes;
         const uint32_t vb = kb + G_::kKBytes;
         // ---- S^T = K Q^T: rows = the stage's 16 tokens, columns = heads ----
         float sacc[NTH][4], sodd[NTH][4];
 #pragma unroll
         for (int nt = 0; nt < NTH; ++nt)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) sacc[nt][j] = sodd[nt][j] = 0.f;
+          for (int e = 0; e < 4; ++e) sacc[nt][e] = sodd[nt][e] = 0.f;
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
           uint32_t a[4];  // rows tok 0-7 / 8-15, d chunks 2ks / 2ks+1
@@ -637,27 +664,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int nt = 0; nt < NTH; ++nt) {
           float x[4];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float v = (sacc[nt][j] + sodd[nt][j]) * p.scale_log2;
-            x[j] = (j < 2 ? v_lo : v_hi) ? v : -INFINITY;
+          for (int e = 0; e < 4; ++e) {
+            const float v = (sacc[nt][e] + sodd[nt][e]) * p.scale_log2;
+            x[e] = (e < 2 ? v_lo : v_hi) ? v : -INFINITY;
           }
           float pr[4];
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            float mx = fmaxf(x[c], x[c + 2]);
+          for (int cc = 0; cc < 2; ++cc) {
+            float mx = fmaxf(x[cc], x[cc + 2]);
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-            const float m_new = fmaxf(m_run[nt][c], mx);
-            alpha[nt][c] = exp2f(m_run[nt][c] - m_new);  // 0 on the first stage
-            pr[c] = exp2f(x[c] - m_new);
-            pr[c + 2] = exp2f(x[c + 2] - m_new);
-            float sum = pr[c] + pr[c + 2];
+            const float m_new = fmaxf(m_run[nt][cc], mx);
+            alpha[nt][cc] = exp2f(m_run[nt][cc] - m_new);  // 0 on the first stage
+            pr[cc] = exp2f(x[cc] - m_new);
+            pr[cc + 2] = exp2f(x[cc + 2] - m_new);
+            float sum = pr[cc] + pr[cc + 2];
             sum += __shfl_xor_sync(0xffffffffu, sum, 4);
             sum += __shfl_xor_sync(0xffffffffu, sum, 8);
             sum += __shfl_xor_sync(0xffffffffu, sum, 16);
-            l_run[nt][c] = l_run[nt][c] * alpha[nt][c] + sum;
-            m_run[nt][c] = m_new;
+            l_run[nt][cc] = l_run[nt][cc] * alpha[nt][cc] + sum;
+            m_run[nt][cc] = m_new;
           }
           // P^T as B fragments: transpose the (token x head) 8x8 blocks in registers
           pb[nt][0] = movmatrix_t(pack2<T>(pr[0], pr[1]));  // tokens 0-7
@@ -677,19 +704,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               o[mt][nt][3] *= alpha[nt][1];
             }
         }
-        // ---- rows past the context may hold anything (even NaN): zero them in V ----
-        if (nt_tok < kStageTok) {
-          const int per_half = (kStageTok - nt_tok) * 8;  // 16-byte chunks per column half
-          for (int e = lane; e < per_half * G_::kHalves; e += 32) {
-            const int hf = e / per_half;
-            const int rem = e - hf * per_half;
-            const uint32_t addr = vb + hf * G_::kBoxBytes + (nt_tok + rem / 8) * 128 + (rem % 8) * 16;
-            asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0) : "memory");
-          }
-          zeroed = true;
-          __syncwarp();
-        }
         // ---- O^T += V^T P^T: rows = d (16 per m-tile), k = tokens, columns = heads ----
+        // (V rows past the context were zero-filled by the copy, so 0 * garbage cannot occur)
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
           uint32_t a[4];  // V^T: d chunks 2mt / 2mt+1, tokens 0-7 / 8-15
@@ -698,65 +714,158 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int nt = 0; nt < NTH; ++nt) mma16816<T>(o[mt][nt], a, pb[nt][0], pb[nt][1]);
         }
       }
-      // generic-proxy stores (the zeroed rows) must be ordered before the next TMA write
-      if (zeroed) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&sm.empty[slot]));
+      __syncwarp();  // every lane is done with the slot before a later stage refills it
     }
-    k += nstage;
-    if (!ok) sm.abort_flag = 1;
 
-    // ---------------- segment end: merge the 8 warps, write out ----------------
-    if (bar_red_or(kBarConsumers, kConsumerThreads, !ok)) {
-      ok = false;
-      break;
+    const bool whole = r.x == 0 && r.y == f.ns;
+    const int slot_out = cta_first ? 0 : 1;
+    const size_t piece = (static_cast<size_t>(c) * 2 + slot_out) * p.gs + pi;
+    float* pacc = p.part_acc + piece * p.heads_per_pair * D;
+    float* pml = p.part_ml + piece * p.heads_per_pair * 2;
+
+    if (P == 1) {
+      // ---------- pair end, one warp per pair: everything stays in registers ----------
+      // Lane (r0, qc) holds O^T rows d = 16*mt + r0 (+8) for heads h = 8*nt + qc (+1), and
+      // the running max/sum of those heads.
+      const bool any_bad = __any_sync(0xffffffffu, seg_bad);
+      if (!whole && r.x > 0) {
+        // A later piece of a cut pair (in this share's first family): store (O, m, l) in
+        // [head][d] order, then publish it with one release store after the warp barrier.
+#pragma unroll
+        for (int nt = 0; nt < NTH; ++nt)
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const int h = nt * 8 + qc + cc;
+            if (h < ph.nh) {
+#pragma unroll
+              for (int mt = 0; mt < MT; ++mt) {
+                pacc[h * D + 16 * mt + r0] = o[mt][nt][cc];
+                pacc[h * D + 16 * mt + r0 + 8] = o[mt][nt][cc + 2];
+              }
+              if (r0 == 0) {
+                pml[h * 2 + 0] = m_run[nt][cc];
+                pml[h * 2 + 1] = any_bad ? -1.f : (m_run[nt][cc] == -INFINITY ? 0.f : l_run[nt][cc]);
+              }
+            }
+          }
+        __syncwarp();
+        if (lane == 0) st_release_gpu(p.flags + static_cast<size_t>(c) * p.gs + pi, p.epoch);
+        if (lane == 0 && any_bad) atomicOr(p.err, kErrBadBlock);
+        continue;
+      }
+      bool bad = any_bad;
+      if (!whole) {
+        // The first piece (in this share's last family): wait for the later pieces, which
+        // the next CTAs store in their first families, and fold them into the registers in
+        // CTA order (the log-sum-exp rescaling of online softmax; deterministic).
+        const long long last_unit =
+            f.pre + p.seg_cost + static_cast<long long>(f.ns - 1) * p.gs + pi;
+        const int c_last = owner_of(last_unit, W, G);
+        bool waited_ok = true;
+        if (lane == 0) {
+          for (int cc = c + 1; cc <= c_last && waited_ok; ++cc)
+            waited_ok = wait_flag_bounded(p.flags + static_cast<size_t>(cc) * p.gs + pi, p.epoch);
+          if (!waited_ok) atomicOr(p.err, kErrTimeout);
+        }
+        waited_ok = __shfl_sync(0xffffffffu, waited_ok, 0);
+        bad = bad || !waited_ok;
+        for (int cc = c + 1; waited_ok && cc <= c_last; ++cc) {
+          const size_t pc = static_cast<size_t>(cc) * 2 * p.gs + pi;  // slot 0 of CTA cc
+          const float* qacc = p.part_acc + pc * p.heads_per_pair * D;
+          const float* qml = p.part_ml + pc * p.heads_per_pair * 2;
+#pragma unroll
+          for (int nt = 0; nt < NTH; ++nt)
+#pragma unroll
+            for (int cc2 = 0; cc2 < 2; ++cc2) {
+              const int h = min(nt * 8 + qc + cc2, ph.nh - 1);  // (columns past nh: unused)
+              const float mi = __ldcg(qml + h * 2), li = __ldcg(qml + h * 2 + 1);
+              float a[2 * MT];
+#pragma unroll
+              for (int mt = 0; mt < MT; ++mt) {
+                a[2 * mt] = __ldcg(qacc + h * D + 16 * mt + r0);
+                a[2 * mt + 1] = __ldcg(qacc + h * D + 16 * mt + r0 + 8);
+              }
+              bad = bad || li < 0.f;
+              if (mi != -INFINITY) {  // an empty piece adds nothing
+                const float mn = fmaxf(m_run[nt][cc2], mi);
+                const float sa = exp2f(m_run[nt][cc2] - mn), sb = exp2f(mi - mn);
+                l_run[nt][cc2] = l_run[nt][cc2] * sa + li * sb;
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                  o[mt][nt][cc2] = o[mt][nt][cc2] * sa + a[2 * mt] * sb;
+                  o[mt][nt][cc2 + 2] = o[mt][nt][cc2 + 2] * sa + a[2 * mt + 1] * sb;
+                }
+                m_run[nt][cc2] = mn;
+              }
+            }
+        }
+        bad = __any_sync(0xffffffffu, bad);
+      }
+      // out = O / l, rounded; transposed in registers (movmatrix) so that each lane stores
+      // two adjacent d of one head: lane (r0, qc) writes out[h = 8*nt + r0][16*mt + qc (+8)].
+#pragma unroll
+      for (int nt = 0; nt < NTH; ++nt) {
+        const float i0 = bad ? 0.f : 1.f / l_run[nt][0];
+        const float i1 = bad ? 0.f : 1.f / l_run[nt][1];
+        const int h = nt * 8 + r0;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          const uint32_t lo = movmatrix_t(pack2<T>(o[mt][nt][0] * i0, o[mt][nt][1] * i1));
+          const uint32_t hi = movmatrix_t(pack2<T>(o[mt][nt][2] * i0, o[mt][nt][3] * i1));
+          if (h < ph.nh) {
+            *reinterpret_cast<uint32_t*>(out_rows + h * D + 16 * mt + qc) = lo;
+            *reinterpret_cast<uint32_t*>(out_rows + h * D + 16 * mt + 8 + qc) = hi;
+          }
+        }
+      }
+      if (lane == 0 && any_bad) atomicOr(p.err, kErrBadBlock);
+      continue;
     }
+
+    // ---------------- pair end, P warps per pair: merge them, write out ----------------
+    gsync();  // the previous pair end's reads of xo/xm/xl are done
     if (r0 == 0) {  // lanes 0..3 hold the running max/sum of heads 8*nt + qc, + 1
 #pragma unroll
       for (int nt = 0; nt < NTH; ++nt)
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          sm.xm[cw][nt * 8 + qc + c] = m_run[nt][c];
-          sm.xl[cw][nt * 8 + qc + c] = l_run[nt][c];
+        for (int cc = 0; cc < 2; ++cc) {
+          sm.xm[warp][nt * 8 + qc + cc] = m_run[nt][cc];
+          sm.xl[warp][nt * 8 + qc + cc] = l_run[nt][cc];
         }
     }
-    const int slot_out = sg.cta_first ? 0 : 1;
-    float* pacc = p.part_acc + (static_cast<size_t>(blockIdx.x) * 2 + slot_out) * kMaxHeads * D;
-    float* pml = p.part_ml + (static_cast<size_t>(blockIdx.x) * 2 + slot_out) * kMaxHeads * 2;
-    bool any_bad = false;
+    const bool any_bad = gor(seg_bad);  // (also orders the xm/xl writes before the reads)
+    const int wbase = pi * P;  // first warp of the pair
     // Exchange O four heads at a time: round r covers heads 4r..4r+3.
     const int rounds = (ph.nh + 3) / 4;
     for (int round = 0; round < rounds; ++round) {
-      if (round > 0) named_bar_sync(kBarConsumers, kConsumerThreads);  // previous reads done
+      if (round > 0) gsync();  // previous round's reads done
       const int rbase = round * 4;
 #pragma unroll
       for (int nt = 0; nt < NTH; ++nt) {
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const int h = nt * 8 + qc + c;
+        for (int cc = 0; cc < 2; ++cc) {
+          const int h = nt * 8 + qc + cc;
           if (h >= rbase && h < rbase + 4) {
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
-              sm.xo[cw][h - rbase][16 * mt + r0] = o[mt][nt][c];
-              sm.xo[cw][h - rbase][16 * mt + r0 + 8] = o[mt][nt][c + 2];
+              sm.xo[warp][h - rbase][16 * mt + r0] = o[mt][nt][cc];
+              sm.xo[warp][h - rbase][16 * mt + r0 + 8] = o[mt][nt][cc + 2];
             }
           }
         }
       }
-      any_bad = bar_red_or(kBarConsumers, kConsumerThreads, seg_bad);
+      gsync();
       const int rows = min(4, ph.nh - rbase);
-      for (int idx = tid; idx < rows * (D / 4); idx += kConsumerThreads) {
+      for (int idx = gt; idx < rows * (D / 4); idx += gthreads) {
         const int hr = idx / (D / 4);
         const int h = rbase + hr;
         const int d4 = (idx - hr * (D / 4)) * 4;
         float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm.xm[w][h]);
+        for (int w = wbase; w < wbase + P; ++w) M = fmaxf(M, sm.xm[w][h]);
         float L = 0.f;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
-          const float wt = exp2f(sm.xm[w][h] - M);  // 0 for warps without stages here
+        for (int w = wbase; w < wbase + P; ++w) {
+          const float wt = exp2f(sm.xm[w][h] - M);  // 0 for a warp without units here
           L += sm.xl[w][h] * wt;
           const float4 x4 = *reinterpret_cast<const float4*>(&sm.xo[w][hr][d4]);
           acc.x += x4.x * wt;
@@ -764,7 +873,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           acc.z += x4.z * wt;
           acc.w += x4.w * wt;
         }
-        if (sg.whole) {
+        if (whole) {
           uint2 packed = make_uint2(0u, 0u);  // zeros for a pair with a bad block
           if (!any_bad) {
             const float inv = 1.f / L;
@@ -773,76 +882,50 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           *reinterpret_cast<uint2*>(out_rows + h * D + d4) = packed;
         } else {
-          *reinterpret_cast<float4*>(pacc + h * D + d4) = acc;
+          // An empty piece (no units here) has M = -inf, and the weights above are NaN:
+          // store acc = 0, l = 0 so that its weight in the merge, 2^(-inf - M'), is 0.
+          const bool empty = M == -INFINITY;
+          *reinterpret_cast<float4*>(pacc + h * D + d4) = empty ? make_float4(0.f, 0.f, 0.f, 0.f) : acc;
           if (d4 == 0) {
             pml[h * 2 + 0] = M;
-            pml[h * 2 + 1] = any_bad ? -1.f : L;
+            pml[h * 2 + 1] = any_bad ? -1.f : (empty ? 0.f : L);
           }
         }
       }
     }
-    if (!sg.whole) {
+    if (!whole) {
       __threadfence();  // this thread's partial writes, before the piece is published or merged
-      named_bar_sync(kBarConsumers, kConsumerThreads);
-      if (sg.j0 > 0) {
-        // A later piece of a cut pair (this share's first segment): publish it.
-        if (tid == 0) st_release_gpu(p.flags + blockIdx.x, p.epoch);
+      gsync();
+      if (r.x > 0) {
+        // A later piece of a cut pair (in this share's first family): publish it.
+        if (gt == 0) st_release_gpu(p.flags + static_cast<size_t>(c) * p.gs + pi, p.epoch);
       } else {
-        // The first piece (this share's last segment): wait for the later pieces, which
-        // the next CTAs wrote at the start of their shares, then merge in CTA order.
-        const int c_last = owner_of(sg.pair_end - 1, W, G);
+        // The first piece (in this share's last family): wait for the later pieces, which
+        // the next CTAs wrote in their first families, then merge them in CTA order.
+        const long long last_unit = f.pre + p.seg_cost + static_cast<long long>(f.ns - 1) * p.gs + pi;
+        const int c_last = owner_of(last_unit, W, G);
         bool waited_ok = true;
-        if (tid == 0) {
-          for (int cc = blockIdx.x + 1; cc <= c_last && waited_ok; ++cc)
-            waited_ok = wait_flag_bounded(p.flags + cc, p.epoch);
+        if (gt == 0) {
+          for (int cc = c + 1; cc <= c_last && waited_ok; ++cc)
+            waited_ok = wait_flag_bounded(p.flags + static_cast<size_t>(cc) * p.gs + pi, p.epoch);
           if (!waited_ok) atomicOr(p.err, kErrTimeout);
         }
-        const bool failed = bar_red_or(kBarConsumers, kConsumerThreads, !waited_ok);
-        merge_pieces<D, T>(p, blockIdx.x, slot_out, c_last, ph.nh, failed, out_rows, tid,
-                           kConsumerThreads);
+        const bool failed = gor(!waited_ok);
+        merge_pieces<D, T>(p, pi, c, slot_out, c_last, ph.nh, failed, out_rows, gt, gthreads);
       }
     }
-    if (tid == 0 && any_bad) atomicOr(p.err, kErrBadBlock);
+    if (gt == 0 && any_bad) atomicOr(p.err, kErrBadBlock);
   }
-  if (!ok && tid == 0) atomicOr(p.err, kErrTimeout);
-}
-
-// Tensor map over one cache viewed as rows of D elements: [num_blocks * Hkv * B, D],
-// boxes of 64 columns x min(B, 16) rows, 128-byte swizzle.
-bool make_cache_map(CUtensorMap* map, const void* base, bool bf16, int head_dim, long long rows,
-                    int box_rows) {
-  using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-  static EncodeFn encode = nullptr;
-  if (!encode) {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess || !fn)
-      return false;
-    encode = reinterpret_cast<EncodeFn>(fn);
-  }
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * 2};
-  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
-  const cuuint32_t estr[2] = {1, 1};
-  return encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-                const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  cp_async_wait<0>();  // (only empty groups can be left; leave none behind)
 }
 
 template <int D, int NTH, typename T>
-int launch(const Params& prm, const CUtensorMap& mk, const CUtensorMap& mv, int grid,
-           cudaStream_t stream) {
+int launch(const Params& prm, int grid, cudaStream_t stream) {
   const size_t smem = sizeof(Smem<D>) + 1024;  // + alignment slack for the ring
   auto* kern = decode_kernel<D, NTH, T>;
   if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), smem)) return -3;
   // Cooperative launch: every CTA is resident at once, so a CTA may wait (bounded) for the
-  // pieces that higher-numbered CTAs write at the start of their shares.
+  // pieces that higher-numbered CTAs write in their first families.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
@@ -853,7 +936,7 @@ int launch(const Params& prm, const CUtensorMap& mk, const CUtensorMap& mv, int 
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, prm, mk, mv) != cudaSuccess) return -3;
+  if (cudaLaunchKernelEx(&cfg, kern, prm) != cudaSuccess) return -3;
   return 0;
 }
 
@@ -864,10 +947,22 @@ int decode_heads_per_pair(int num_q_heads, int num_kv_heads) {
   return g < decode::kMaxHeads ? g : decode::kMaxHeads;
 }
 
-size_t decode_workspace_bytes(int grid, int /*heads_per_pair*/, int head_dim) {
-  const size_t flags = static_cast<size_t>(grid) * sizeof(unsigned long long);
-  const size_t acc = static_cast<size_t>(grid) * 2 * decode::kMaxHeads * head_dim * sizeof(float);
-  const size_t ml = static_cast<size_t>(grid) * 2 * decode::kMaxHeads * 2 * sizeof(float);
+// Pairs per family: the largest power of two <= 8 dividing the pair count of a sequence.
+static int pair_group_size(int num_q_heads, int num_kv_heads) {
+  const int hpp = decode_heads_per_pair(num_q_heads, num_kv_heads);
+  const int group = num_q_heads / num_kv_heads;
+  const int pairs = num_kv_heads * ((group + hpp - 1) / hpp);
+  int gs = 8;
+  while (pairs % gs) gs >>= 1;
+  return gs;
+}
+
+size_t decode_workspace_bytes(int grid, int num_q_heads, int num_kv_heads, int head_dim) {
+  const size_t gs = pair_group_size(num_q_heads, num_kv_heads);
+  const size_t hpp = decode_heads_per_pair(num_q_heads, num_kv_heads);
+  const size_t flags = static_cast<size_t>(grid) * gs * sizeof(unsigned long long);
+  const size_t acc = static_cast<size_t>(grid) * 2 * gs * hpp * head_dim * sizeof(float);
+  const size_t ml = static_cast<size_t>(grid) * 2 * gs * hpp * 2 * sizeof(float);
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   return up(flags) + up(acc) + up(ml);
 }
@@ -885,6 +980,8 @@ static unsigned long long next_epoch() {
 int decode_launch(const DecodeArgs& a, int grid, cudaStream_t stream) {
   decode::Params p;
   p.q = static_cast<const uint8_t*>(a.q);
+  p.k_cache = static_cast<const uint8_t*>(a.k_cache);
+  p.v_cache = static_cast<const uint8_t*>(a.v_cache);
   p.block_tables = a.block_tables;
   p.context_lens = a.context_lens;
   p.out = static_cast<uint8_t*>(a.out);
@@ -894,6 +991,10 @@ int decode_launch(const DecodeArgs& a, int grid, cudaStream_t stream) {
   p.group = a.num_q_heads / a.num_kv_heads;
   p.heads_per_pair = decode_heads_per_pair(a.num_q_heads, a.num_kv_heads);
   p.head_chunks = (p.group + p.heads_per_pair - 1) / p.heads_per_pair;
+  p.gs = pair_group_size(a.num_q_heads, a.num_kv_heads);
+  p.log2_gs = p.gs == 8 ? 3 : (p.gs == 4 ? 2 : (p.gs == 2 ? 1 : 0));
+  p.ngroups = a.num_kv_heads * p.head_chunks / p.gs;
+  p.phases = decode::kWarps / p.gs;
   p.max_blocks_per_seq = a.max_blocks_per_seq;
   p.block_size = a.block_size;
   p.log2_block = a.block_size == 8 ? 3 : (a.block_size == 16 ? 4 : 5);
@@ -905,23 +1006,17 @@ int decode_launch(const DecodeArgs& a, int grid, cudaStream_t stream) {
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   p.flags = reinterpret_cast<unsigned long long*>(ws);
-  ws += up(static_cast<size_t>(grid) * sizeof(unsigned long long));
+  ws += up(static_cast<size_t>(grid) * p.gs * sizeof(unsigned long long));
   p.epoch = next_epoch();
   p.part_acc = reinterpret_cast<float*>(ws);
-  ws += up(static_cast<size_t>(grid) * 2 * decode::kMaxHeads * a.head_dim * sizeof(float));
+  ws += up(static_cast<size_t>(grid) * 2 * p.gs * p.heads_per_pair * a.head_dim * sizeof(float));
   p.part_ml = reinterpret_cast<float*>(ws);
 
-  const long long rows = static_cast<long long>(a.num_blocks) * a.num_kv_heads * a.block_size;
-  const int box_rows = a.block_size < decode::kStageTok ? a.block_size : decode::kStageTok;
-  CUtensorMap mk, mv;
-  if (!decode::make_cache_map(&mk, a.k_cache, a.bf16, a.head_dim, rows, box_rows) ||
-      !decode::make_cache_map(&mv, a.v_cache, a.bf16, a.head_dim, rows, box_rows))
-    return -3;
   // heads of a pair are MMA columns: one n-tile of 8, or two for up to 16
-#define PA_DECODE_CASE(DD, NN)                                                        \
-  if (a.head_dim == DD && (p.heads_per_pair > 8) == (NN == 2))                        \
-    return a.bf16 ? decode::launch<DD, NN, __nv_bfloat16>(p, mk, mv, grid, stream)    \
-                  : decode::launch<DD, NN, __half>(p, mk, mv, grid, stream);
+#define PA_DECODE_CASE(DD, NN)                                       \
+  if (a.head_dim == DD && (p.heads_per_pair > 8) == (NN == 2))       \
+    return a.bf16 ? decode::launch<DD, NN, __nv_bfloat16>(p, grid, stream) \
+                  : decode::launch<DD, NN, __half>(p, grid, stream);
   PA_DECODE_CASE(128, 1)
   PA_DECODE_CASE(128, 2)
   PA_DECODE_CASE(64, 1)

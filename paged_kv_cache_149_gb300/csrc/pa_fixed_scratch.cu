@@ -27,7 +27,9 @@
 
 namespace {
 
-constexpr size_t kFixedScratchBytes = 4u << 20;  // 4 MiB: enough for ~240 SMs at head_dim 128
+// 32 MiB: the largest decode workspace (16 query heads per kv head, 8 or more kv heads,
+// head_dim 128) of a device with up to about 250 SMs
+constexpr size_t kFixedScratchBytes = 32u << 20;
 
 static __device__ __align__(256) unsigned char g_fixed_scratch[kFixedScratchBytes];
 

@@ -22,11 +22,11 @@ struct DecodeArgs {
   unsigned* err;  // device address of the per-device error word
 };
 
-// Workspace bytes for `grid` persistent CTAs and up to `heads_per_pair` heads per pair.
-size_t decode_workspace_bytes(int grid, int heads_per_pair, int head_dim);
+// Workspace bytes for `grid` persistent CTAs and this head layout.
+size_t decode_workspace_bytes(int grid, int num_q_heads, int num_kv_heads, int head_dim);
 // Heads a decode work pair covers (query heads per kv head, at most 16).
 int decode_heads_per_pair(int num_q_heads, int num_kv_heads);
-// Launch the decode kernel and its merge kernel; 0 or a negative PA_ERR_* code.
+// Launch the decode kernel; 0 or a negative PA_ERR_* code.
 int decode_launch(const DecodeArgs& a, int grid, cudaStream_t stream);
 
 int reshape_and_cache_launch(const void* key, const void* value, void* k_cache, void* v_cache,

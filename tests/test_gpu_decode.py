@@ -44,6 +44,11 @@ for dtype in ("fp16", "bf16"):
         for bs in (8, 16, 32):
             for hq, hkv in ((4, 4), (4, 2), (6, 2), (8, 2), (16, 2), (12, 1)):
                 CASES.append((dtype, d, bs, hq, hkv))
+# kv-head counts that give every pair-group size (8, 4, 2, 1 pairs per family), several
+# families per sequence, and query-head chunks (64 / 2: two chunks of 16)
+CASES += [("bf16", 128, 16, 32, 8), ("fp16", 64, 8, 8, 8), ("bf16", 128, 16, 32, 32),
+          ("fp16", 128, 32, 24, 12), ("bf16", 64, 16, 12, 6), ("fp16", 128, 16, 6, 3),
+          ("bf16", 128, 16, 64, 2), ("fp16", 128, 16, 48, 16)]
 
 
 @pytest.mark.parametrize("dtype,d,bs,hq,hkv", CASES)
