@@ -2,9 +2,12 @@
 
 A step is one pass of the whole hot path over one batch: the cache write of each
 sequence's newest token (64 tokens through pa_reshape_and_cache) followed by paged decode
-attention over every sequence (pa_decode: one persistent, cooperatively launched kernel
-that also merges the split-KV partials of sequences cut between CTAs).  Workload (seeded, synthetic; no dataset, no weights): 64 sequences,
-32 query / 8 kv heads, head_dim 128, bf16, block_size 16, context lengths uniform in
+attention over every sequence (pa_decode: one persistent kernel; the last CTA to finish
+a pair cut between CTAs merges its split-KV pieces).  The decode kernel's own duration is
+timed separately: --steps launches back to back in the same clock-sampled window.
+
+Workload (seeded, synthetic; no dataset, no weights): 64 sequences, 32 query / 8 kv
+heads, head_dim 128, bf16, block_size 16, context lengths uniform in
 [128, 2048], K/V ~ N(0,1), blocks placed through the block pool from a shuffled
 16384-block free list.  Three such batches live in disjoint blocks and steps rotate
 through them, so every step reads K/V that the previous two steps did not touch
@@ -193,16 +196,20 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.synchronize(device)
     pa.get_device_error()
 
-    def step(i, ev_mid=None):
+    def step(i):
         b = batches[i % ROTATE]
         pa.reshape_and_cache(b["key"], b["value"], k_cache, v_cache, b["slots"], stream=stream)
-        if ev_mid is not None:
-            ev_mid.record(stream)
+        pa.decode(b["q"], k_cache, v_cache, b["tables"], b["ctx"], wl.scale, out=b["out"],
+                  workspace=ws, stream=stream)
+
+    def decode_only(i):
+        b = batches[i % ROTATE]
         pa.decode(b["q"], k_cache, v_cache, b["tables"], b["ctx"], wl.scale, out=b["out"],
                   workspace=ws, stream=stream)
 
     for i in range(args.warmup):
         step(i)
+        decode_only(i)
     torch.cuda.synchronize(device)
     if pa.get_device_error(stream=stream):
         raise RuntimeError("device error flags set during warm-up")
@@ -212,31 +219,35 @@ def run_gpu(args, rank, world, local_rank):
         sampler.start()
         time.sleep(0.3)
     K = args.steps
-    ev_start = torch.cuda.Event(enable_timing=True)
-    ev_stop = torch.cuda.Event(enable_timing=True)
-    ev_mid = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ev_dec = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(device)
     t0 = time.time()
-    ev_start.record(stream)
+    # the step loop: nothing between the launches, so each kernel may start while the one
+    # before it drains (programmatic dependent launch)
+    ev[0].record(stream)
     for i in range(K):
-        step(i, ev_mid[i])
-        ev_dec[i].record(stream)
-    ev_stop.record(stream)
+        step(i)
+    ev[1].record(stream)
     torch.cuda.synchronize(device)
-    t1 = time.time()
     if world > 1:
         torch.distributed.barrier()
+    # the decode kernel alone, K launches back to back on the same stream: its duration
+    ev[2].record(stream)
+    for i in range(K):
+        decode_only(i)
+    ev[3].record(stream)
+    torch.cuda.synchronize(device)
+    t1 = time.time()
     clocks = sampler.stop(t0, t1) if sampler else None
     flags = pa.get_device_error(stream=stream)
-    total_ms = ev_start.elapsed_time(ev_stop)
-    decode_ms = sum(ev_mid[i].elapsed_time(ev_dec[i]) for i in range(K)) / K
+    total_ms = ev[0].elapsed_time(ev[1])
+    decode_ms = ev[2].elapsed_time(ev[3]) / K
     if world > 1:
-        t = torch.tensor([total_ms], device=device)
+        t = torch.tensor([total_ms, decode_ms], device=device)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+        total_ms, decode_ms = float(t[0].item()), float(t[1].item())
 
     # end to end through the binding with host buffers: inputs from pinned host memory
     # every step, the output read back every step
@@ -395,6 +406,8 @@ def main():
             "algorithmic_bytes": dec_b,
             "padded_block_bytes": padded,
             "decode_us": round(1e3 * res["decode_ms"], 2),
+            "decode_timing": "decode kernel alone, --steps launches back to back on the bench "
+                             "stream, CUDA events around the loop (same clock window)",
         },
         "cpu_baseline": None if cpu is None else {
             "value": round(cpu["bytes"] / cpu["seconds"] / 1e9, 4),
@@ -412,7 +425,8 @@ def main():
             "us_per_step": round(1e3 * res["e2e_ms"], 2),
         },
         "clocks": res["clocks"],
-        "gpu_launches": 2 * args.steps,  # reshape_and_cache_kernel + decode_kernel per step
+        # per timed step: reshape_and_cache_kernel + decode_kernel; plus the decode-only loop
+        "gpu_launches": 3 * args.steps,
         "device_error_flags": res["flags"],
     }
     print(json.dumps(line))

@@ -20,6 +20,10 @@ __global__ void __launch_bounds__(128) reshape_and_cache_kernel(
     const uint4* __restrict__ key, const uint4* __restrict__ value, uint4* __restrict__ k_cache,
     uint4* __restrict__ v_cache, const int64_t* __restrict__ slot_mapping, long long num_slots,
     int num_kv_heads, int vec_per_row, int block_size, unsigned* err) {
+  // a programmatic dependent of the previous kernel (say the last decode step, which may
+  // still read the cache): wait for it before touching anything, then let the next start
+  pdl_wait_primary();
+  pdl_launch_dependents();
   const int i = blockIdx.x;
   const long long slot = slot_mapping[i];
   if (slot < 0) return;
@@ -70,12 +74,21 @@ int reshape_and_cache_launch(const void* key, const void* value, void* k_cache, 
                              int num_kv_heads, int head_dim, int block_size, unsigned* err,
                              cudaStream_t stream) {
   if (num_tokens == 0) return 0;
-  reshape_and_cache_kernel<<<num_tokens, 128, 0, stream>>>(
-      static_cast<const uint4*>(key), static_cast<const uint4*>(value),
-      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), slot_mapping,
-      static_cast<long long>(num_blocks) * block_size, num_kv_heads, head_dim / 8, block_size,
-      err);
-  return cudaGetLastError() == cudaSuccess ? 0 : -3;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_tokens);
+  cfg.blockDim = dim3(128);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(
+      &cfg, reshape_and_cache_kernel, static_cast<const uint4*>(key),
+      static_cast<const uint4*>(value), static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
+      slot_mapping, static_cast<long long>(num_blocks) * block_size, num_kv_heads, head_dim / 8,
+      block_size, err);
+  return e == cudaSuccess ? 0 : -3;
 }
 
 int copy_blocks_launch(void* k_cache, void* v_cache, const int32_t* block_mapping, int num_pairs,

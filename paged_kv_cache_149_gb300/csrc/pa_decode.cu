@@ -31,13 +31,16 @@
 //   then O^T += V^T P^T (rows = d) with P = 2^(S - m) rounded to the input type and moved
 //   into B-fragment layout by an in-register transpose (movmatrix); online softmax with a
 //   running max and sum per head.  The swizzle makes every ldmatrix conflict-free.
-// * A pair cut between CTAs (split-KV) is merged with a log-sum-exp reduction by the CTA
-//   holding its first piece, once the later pieces (written first thing by the next CTAs)
-//   are published (the rescaling identity of online softmax that chenyuan1125, section
-//   它和 FlashAttention…, names as FlashAttention's technique).  The launch is cooperative,
-//   so all CTAs are resident; a CTA only waits (bounded, about 1 s; PA_DEVERR_TIMEOUT and
-//   zeros on expiry) for higher-numbered CTAs.  Cut points depend on logical positions and
-//   context lengths only, so permuting physical blocks gives bit-identical output.
+// * A pair cut between CTAs (split-KV) leaves one partial softmax state (O, m, l) per
+//   piece in the workspace.  When a CTA has streamed its whole share (no copies left in
+//   flight, so a fence is cheap), it counts its pieces in on a per-pair counter; the CTA
+//   that brings a pair's count to its number of pieces merges them in CTA order with a
+//   log-sum-exp reduction (the rescaling identity of online softmax that chenyuan1125,
+//   section 它和 FlashAttention…, names as FlashAttention's technique).  No CTA ever waits
+//   for another.  Cut points depend on logical positions and context lengths only, and
+//   the merge order is fixed, so permuting physical blocks gives bit-identical output.
+// * Launched as a programmatic dependent of the kernel before it in the stream: the grid
+//   is resident while that kernel drains and starts at griddepcontrol.wait.
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -56,9 +59,10 @@ constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxHeads = 16;  // query heads per pair (MMA columns)
 constexpr float kLog2e = 1.4426950408889634f;
-// Stage-equivalents charged per family on top of its stages (the q load and the output or
-// partial write at each pair's end) when cutting the batch into per-SM shares.
-constexpr int kSegCost = 2;
+// Stage-equivalents charged per family on top of its stages when cutting the batch into
+// per-SM shares: switching families (a new table row, the pair-end writes) costs a share
+// about as much time on GB300 as streaming 16 more stages.
+constexpr int kSegCost = 16;
 
 template <int D>
 struct Geo {
@@ -85,8 +89,9 @@ struct Params {
   int max_blocks_per_seq, block_size, log2_block, num_blocks, max_ctx;
   int seg_cost;  // stage units charged per family on top of its stages
   float scale_log2;
-  unsigned long long* flags;  // [grid][gs]: epoch once the CTA's leading piece of pair is written
-  unsigned long long epoch;   // unique per call
+  // [grid][gs]: arrivals at cut pair (first CTA, pi): epoch tag << 24 | pieces counted in
+  unsigned long long* counters;
+  unsigned long long epoch;  // 40-bit tag, different from the previous call's
   float* part_acc;  // [grid][2][gs][heads_per_pair][D]
   float* part_ml;   // [grid][2][gs][heads_per_pair][2]  (m, l); l < 0: the piece saw a bad block
   unsigned* err;
@@ -286,38 +291,54 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
                                (((chunk & 7) ^ (row & 7)) << 4));
 }
 
-__device__ __forceinline__ void st_release_gpu(unsigned long long* addr, unsigned long long v) {
-  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(addr), "l"(v) : "memory");
+// A piece of a cut pair as every holder of a piece sees it: the CTAs holding its first and
+// last pieces, where the first CTA stored its piece (slot 0 when the pair's family is that
+// CTA's first family), and the pair's sequence and heads.
+struct CutPiece {
+  int c_first, c_last, first_slot, s, h0, nh;
+};
+
+__device__ __forceinline__ CutPiece cut_piece(const Fam& f, int pi, const PairHeads& ph,
+                                              long long W, int G, const Params& p) {
+  CutPiece cp;
+  const long long first_unit = f.pre + p.seg_cost + pi;
+  const long long last_unit = first_unit + static_cast<long long>(f.ns - 1) * p.gs;
+  cp.c_first = owner_of(first_unit, W, G);
+  cp.c_last = owner_of(last_unit, W, G);
+  long long w0f, w1f;
+  share_of(cp.c_first, W, G, w0f, w1f);
+  cp.first_slot = w0f >= f.pre ? 0 : 1;
+  cp.s = f.s;
+  cp.h0 = ph.h0;
+  cp.nh = ph.nh;
+  return cp;
 }
 
-__device__ __forceinline__ unsigned long long ld_acquire_gpu(const unsigned long long* addr) {
-  unsigned long long v;
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(addr) : "memory");
-  return v;
-}
-
-// Spin (bounded by kWaitLimitNs) until *flag holds this call's epoch.
-__device__ __forceinline__ bool wait_flag_bounded(const unsigned long long* flag,
-                                                  unsigned long long epoch) {
-  if (ld_acquire_gpu(flag) == epoch) return true;
-  const unsigned long long t0 = global_timer_ns();
-  for (;;) {
-    __nanosleep(64);
-    if (ld_acquire_gpu(flag) == epoch) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+// Count one piece in at a pair's counter; returns the pieces counted so far this call.  The
+// counter holds epoch << 24 | count; a value with another epoch is stale (an earlier call
+// or never-written workspace) and counts as zero.  The loop retries only when another
+// arrival changed the counter in between, so it ends after at most one try per piece.
+__device__ __forceinline__ int arrive(unsigned long long* ctr, unsigned long long epoch) {
+  unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(ctr);
+  for (int tries = 0; tries < (1 << 20); ++tries) {
+    const unsigned long long want = (cur >> 24) == epoch ? cur + 1 : (epoch << 24) | 1ull;
+    const unsigned long long prev = atomicCAS(ctr, cur, want);
+    if (prev == cur) return static_cast<int>(want & 0xffffffull);
+    cur = prev;
   }
+  return -1;  // (unreachable in practice: no merge rather than a wrong one)
 }
 
 // Merge the pieces of a cut pair held by CTAs c..c_last (c's piece in slot `first_slot`,
 // the others in slot 0), taken in CTA order so the result is deterministic:
 //   (M, L, O) <- (max(M, m_i), L a + l_i b, O a + acc_i b),  a = 2^(M - M'), b = 2^(m_i - M'),
 // then out = O / L (the log-sum-exp rescaling of online softmax).  Empty pieces (m = -inf)
-// are skipped; zeros when a piece saw a bad block or a wait for a piece gave up.  Each
+// are skipped; zeros when a piece saw a bad block.  Each
 // thread takes one 4-float column chunk of up to 4 heads and loads 4 pieces of each at a
 // time, so the L2 round trips overlap instead of queueing one behind another.
 template <int D, typename T>
 __device__ void merge_pieces(const Params& p, int pi, int c, int first_slot, int c_last, int nh,
-                             bool failed, T* out_rows, int gt, int gthreads) {
+                             T* out_rows, int gt, int gthreads) {
   constexpr int C4 = D / 4;  // 4-float chunks per head row
   constexpr int HB = 4;      // heads per pass
   constexpr int PB = 4;      // pieces per load round
@@ -333,7 +354,7 @@ __device__ void merge_pieces(const Params& p, int pi, int c, int first_slot, int
       M[k] = -INFINITY;
       L[k] = 0.f;
       O[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-      bad[k] = failed;
+      bad[k] = false;
     }
     for (int cc0 = c; cc0 <= c_last; cc0 += PB) {
       float m[PB][HB], l[PB][HB];
@@ -398,6 +419,7 @@ struct Smem {
   long long scan[kWarps];
   long long start_pre;
   int start_s;
+  int last[kWarps];  // per pair group: this CTA's arrival completed the pair
 };
 
 // Q^T of a pair as MMA B fragments (column n = head 8*nt + lane / 4; heads >= nh are zero).
@@ -460,6 +482,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   auto gor = [&](bool v) -> bool {
     return P == 1 ? (__any_sync(0xffffffffu, v) != 0) : bar_red_or(1 + pi, gthreads, v);
   };
+
+  // The kernel before this one in the stream (say the cache write) has finished and its
+  // writes are visible past this point; the next one may start launching.
+  pdl_wait_primary();
+  pdl_launch_dependents();
 
   // ---- setup: total units W, this CTA's share [w0, w1), and its first family ----
   const int per = (p.num_seqs + kThreads - 1) / kThreads;
@@ -581,6 +608,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
 
   uint32_t used = 0;  // stages this warp has computed
   bool cta_first = true;
+  // This warp's pieces of cut pairs (at most two: in the share's first and last families),
+  // counted in after the share is streamed.
+  CutPiece cut_a, cut_b;
+  int ncut = 0;
   for (Fam f = first; f.s < p.num_seqs && f.pre < w1; fam_next(f, p), cta_first = false) {
     const int2 r = unit_range(f, pi, w0, w1, p);
     if (!has_piece(r, f.ns)) continue;
@@ -728,9 +759,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       // Lane (r0, qc) holds O^T rows d = 16*mt + r0 (+8) for heads h = 8*nt + qc (+1), and
       // the running max/sum of those heads.
       const bool any_bad = __any_sync(0xffffffffu, seg_bad);
-      if (!whole && r.x > 0) {
-        // A later piece of a cut pair (in this share's first family): store (O, m, l) in
-        // [head][d] order, then publish it with one release store after the warp barrier.
+      if (!whole) {
+        // A piece of a cut pair: store (O, m, l) in [head][d] order; it is counted in (and
+        // maybe merged) after the share is streamed.
 #pragma unroll
         for (int nt = 0; nt < NTH; ++nt)
 #pragma unroll
@@ -742,65 +773,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
                 pacc[h * D + 16 * mt + r0] = o[mt][nt][cc];
                 pacc[h * D + 16 * mt + r0 + 8] = o[mt][nt][cc + 2];
               }
-              if (r0 == 0) {
+              if (r0 == 0) {  // an empty piece (m = -inf) gets l = 0: weight 0 in the merge
                 pml[h * 2 + 0] = m_run[nt][cc];
                 pml[h * 2 + 1] = any_bad ? -1.f : (m_run[nt][cc] == -INFINITY ? 0.f : l_run[nt][cc]);
               }
             }
           }
-        __syncwarp();
-        if (lane == 0) st_release_gpu(p.flags + static_cast<size_t>(c) * p.gs + pi, p.epoch);
+        (ncut == 0 ? cut_a : cut_b) = cut_piece(f, pi, ph, W, G, p);
+        ++ncut;
         if (lane == 0 && any_bad) atomicOr(p.err, kErrBadBlock);
         continue;
       }
-      bool bad = any_bad;
-      if (!whole) {
-        // The first piece (in this share's last family): wait for the later pieces, which
-        // the next CTAs store in their first families, and fold them into the registers in
-        // CTA order (the log-sum-exp rescaling of online softmax; deterministic).
-        const long long last_unit =
-            f.pre + p.seg_cost + static_cast<long long>(f.ns - 1) * p.gs + pi;
-        const int c_last = owner_of(last_unit, W, G);
-        bool waited_ok = true;
-        if (lane == 0) {
-          for (int cc = c + 1; cc <= c_last && waited_ok; ++cc)
-            waited_ok = wait_flag_bounded(p.flags + static_cast<size_t>(cc) * p.gs + pi, p.epoch);
-          if (!waited_ok) atomicOr(p.err, kErrTimeout);
-        }
-        waited_ok = __shfl_sync(0xffffffffu, waited_ok, 0);
-        bad = bad || !waited_ok;
-        for (int cc = c + 1; waited_ok && cc <= c_last; ++cc) {
-          const size_t pc = static_cast<size_t>(cc) * 2 * p.gs + pi;  // slot 0 of CTA cc
-          const float* qacc = p.part_acc + pc * p.heads_per_pair * D;
-          const float* qml = p.part_ml + pc * p.heads_per_pair * 2;
-#pragma unroll
-          for (int nt = 0; nt < NTH; ++nt)
-#pragma unroll
-            for (int cc2 = 0; cc2 < 2; ++cc2) {
-              const int h = min(nt * 8 + qc + cc2, ph.nh - 1);  // (columns past nh: unused)
-              const float mi = __ldcg(qml + h * 2), li = __ldcg(qml + h * 2 + 1);
-              float a[2 * MT];
-#pragma unroll
-              for (int mt = 0; mt < MT; ++mt) {
-                a[2 * mt] = __ldcg(qacc + h * D + 16 * mt + r0);
-                a[2 * mt + 1] = __ldcg(qacc + h * D + 16 * mt + r0 + 8);
-              }
-              bad = bad || li < 0.f;
-              if (mi != -INFINITY) {  // an empty piece adds nothing
-                const float mn = fmaxf(m_run[nt][cc2], mi);
-                const float sa = exp2f(m_run[nt][cc2] - mn), sb = exp2f(mi - mn);
-                l_run[nt][cc2] = l_run[nt][cc2] * sa + li * sb;
-#pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                  o[mt][nt][cc2] = o[mt][nt][cc2] * sa + a[2 * mt] * sb;
-                  o[mt][nt][cc2 + 2] = o[mt][nt][cc2 + 2] * sa + a[2 * mt + 1] * sb;
-                }
-                m_run[nt][cc2] = mn;
-              }
-            }
-        }
-        bad = __any_sync(0xffffffffu, bad);
-      }
+      const bool bad = any_bad;
       // out = O / l, rounded; transposed in registers (movmatrix) so that each lane stores
       // two adjacent d of one head: lane (r0, qc) writes out[h = 8*nt + r0][16*mt + qc (+8)].
 #pragma unroll
@@ -894,29 +878,46 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       }
     }
     if (!whole) {
-      __threadfence();  // this thread's partial writes, before the piece is published or merged
-      gsync();
-      if (r.x > 0) {
-        // A later piece of a cut pair (in this share's first family): publish it.
-        if (gt == 0) st_release_gpu(p.flags + static_cast<size_t>(c) * p.gs + pi, p.epoch);
-      } else {
-        // The first piece (in this share's last family): wait for the later pieces, which
-        // the next CTAs wrote in their first families, then merge them in CTA order.
-        const long long last_unit = f.pre + p.seg_cost + static_cast<long long>(f.ns - 1) * p.gs + pi;
-        const int c_last = owner_of(last_unit, W, G);
-        bool waited_ok = true;
-        if (gt == 0) {
-          for (int cc = c + 1; cc <= c_last && waited_ok; ++cc)
-            waited_ok = wait_flag_bounded(p.flags + static_cast<size_t>(cc) * p.gs + pi, p.epoch);
-          if (!waited_ok) atomicOr(p.err, kErrTimeout);
-        }
-        const bool failed = gor(!waited_ok);
-        merge_pieces<D, T>(p, pi, c, slot_out, c_last, ph.nh, failed, out_rows, gt, gthreads);
-      }
+      (ncut == 0 ? cut_a : cut_b) = cut_piece(f, pi, ph, W, G, p);
+      ++ncut;
     }
     if (gt == 0 && any_bad) atomicOr(p.err, kErrBadBlock);
   }
   cp_async_wait<0>();  // (only empty groups can be left; leave none behind)
+
+  // ---- count this share's pieces in; the last arrival at a pair merges its pieces ----
+  // (ncut is the same in every warp of a pair.)  Lanes 0 and 1 of the pair's first warp
+  // count in its two pieces side by side, each after a fence ordering the piece's stores
+  // before its arrival; an arrival that completes a pair fences again before the merge's
+  // loads.
+  if (ncut > 0) {
+    gsync();  // every thread of the pair has stored its parts of the pieces
+    int bits = 0;
+    if (gt < ncut) {
+      const CutPiece& cp = gt == 0 ? cut_a : cut_b;
+      __threadfence();
+      const int n = cp.c_last - cp.c_first + 1;
+      if (arrive(p.counters + static_cast<size_t>(cp.c_first) * p.gs + pi, p.epoch) == n) {
+        __threadfence();
+        bits = 1 << gt;
+      }
+    }
+    __syncwarp();
+    bits = static_cast<int>(__reduce_or_sync(0xffffffffu, static_cast<unsigned>(bits)));
+    if (P > 1) {
+      if (gt == 0) sm.last[pi] = bits;
+      gsync();
+      bits = sm.last[pi];
+    }
+    for (int k = 0; k < ncut; ++k) {
+      if (!(bits & (1 << k))) continue;
+      const CutPiece& cp = k == 0 ? cut_a : cut_b;
+      T* out_rows =
+          reinterpret_cast<T*>(p.out) + (static_cast<size_t>(cp.s) * p.num_q_heads + cp.h0) * D;
+      merge_pieces<D, T>(p, pi, cp.c_first, cp.first_slot, cp.c_last, cp.nh, out_rows, gt,
+                         gthreads);
+    }
+  }
 }
 
 template <int D, int NTH, typename T>
@@ -924,16 +925,15 @@ int launch(const Params& prm, int grid, cudaStream_t stream) {
   const size_t smem = sizeof(Smem<D>) + 1024;  // + alignment slack for the ring
   auto* kern = decode_kernel<D, NTH, T>;
   if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), smem)) return -3;
-  // Cooperative launch: every CTA is resident at once, so a CTA may wait (bounded) for the
-  // pieces that higher-numbered CTAs write in their first families.
+  // a programmatic dependent of the previous kernel in the stream (see pdl_wait_primary)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, kern, prm) != cudaSuccess) return -3;
@@ -960,21 +960,19 @@ static int pair_group_size(int num_q_heads, int num_kv_heads) {
 size_t decode_workspace_bytes(int grid, int num_q_heads, int num_kv_heads, int head_dim) {
   const size_t gs = pair_group_size(num_q_heads, num_kv_heads);
   const size_t hpp = decode_heads_per_pair(num_q_heads, num_kv_heads);
-  const size_t flags = static_cast<size_t>(grid) * gs * sizeof(unsigned long long);
+  const size_t ctrs = static_cast<size_t>(grid) * gs * sizeof(unsigned long long);
   const size_t acc = static_cast<size_t>(grid) * 2 * gs * hpp * head_dim * sizeof(float);
   const size_t ml = static_cast<size_t>(grid) * 2 * gs * hpp * 2 * sizeof(float);
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
-  return up(flags) + up(acc) + up(ml);
+  return up(ctrs) + up(acc) + up(ml);
 }
 
-// Epochs tag the pieces of one call: a flag in the (caller-owned, never cleared) workspace
-// counts only when it holds the current call's epoch.  64-bit values, random high half.
+// Epoch tags of the pair counters: 40 bits, a different value on every call (random start).
 static unsigned long long next_epoch() {
   static std::atomic<unsigned long long> counter{
-      (static_cast<unsigned long long>(std::random_device{}()) << 32) ^
-      static_cast<unsigned long long>(
-          std::chrono::steady_clock::now().time_since_epoch().count())};
-  return counter.fetch_add(1, std::memory_order_relaxed) + 1;
+      (static_cast<unsigned long long>(std::random_device{}()) << 8) ^
+      static_cast<unsigned long long>(std::chrono::steady_clock::now().time_since_epoch().count())};
+  return (counter.fetch_add(1, std::memory_order_relaxed) + 1) & ((1ull << 40) - 1);
 }
 
 int decode_launch(const DecodeArgs& a, int grid, cudaStream_t stream) {
@@ -1005,7 +1003,7 @@ int decode_launch(const DecodeArgs& a, int grid, cudaStream_t stream) {
   p.err = a.err;
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
-  p.flags = reinterpret_cast<unsigned long long*>(ws);
+  p.counters = reinterpret_cast<unsigned long long*>(ws);
   ws += up(static_cast<size_t>(grid) * p.gs * sizeof(unsigned long long));
   p.epoch = next_epoch();
   p.part_acc = reinterpret_cast<float*>(ws);
