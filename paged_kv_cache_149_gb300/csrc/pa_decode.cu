@@ -330,85 +330,186 @@ __device__ __forceinline__ int arrive(unsigned long long* ctr, unsigned long lon
 }
 
 // Merge the pieces of a cut pair held by CTAs c..c_last (c's piece in slot `first_slot`,
-// the others in slot 0), taken in CTA order so the result is deterministic:
-//   (M, L, O) <- (max(M, m_i), L a + l_i b, O a + acc_i b),  a = 2^(M - M'), b = 2^(m_i - M'),
-// then out = O / L (the log-sum-exp rescaling of online softmax).  Empty pieces (m = -inf)
-// are skipped; zeros when a piece saw a bad block.  Each
-// thread takes one 4-float column chunk of up to 4 heads and loads 4 pieces of each at a
-// time, so the L2 round trips overlap instead of queueing one behind another.
+// the others in slot 0), pieces taken in CTA order so the result is deterministic:
+//   M = max m_i,  w_i = 2^(m_i - M) (0 for an empty piece),  L = sum l_i w_i,
+//   out = sum w_i acc_i / L
+// (the log-sum-exp rescaling of online softmax); zeros when a piece saw a bad block.
+// merge_staged computes the same sums in the same order with the same fused multiply-adds,
+// so a pair's output does not depend on which of the two merges it.
 template <int D, typename T>
 __device__ void merge_pieces(const Params& p, int pi, int c, int first_slot, int c_last, int nh,
                              T* out_rows, int gt, int gthreads) {
   constexpr int C4 = D / 4;  // 4-float chunks per head row
-  constexpr int HB = 4;      // heads per pass
-  constexpr int PB = 4;      // pieces per load round
   const int hpp = p.heads_per_pair;
   const int hstep = gthreads / C4;  // heads the group covers side by side
   const int d4 = (gt % C4) * 4;
-  for (int hb = gt / C4; hb < nh; hb += hstep * HB) {
-    float M[HB], L[HB];
-    float4 O[HB];
-    bool bad[HB];
-#pragma unroll
-    for (int k = 0; k < HB; ++k) {
-      M[k] = -INFINITY;
-      L[k] = 0.f;
-      O[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-      bad[k] = false;
+  auto piece_of = [&](int cc) {
+    return (static_cast<size_t>(cc) * 2 + (cc == c ? first_slot : 0)) * p.gs + pi;
+  };
+  for (int h = gt / C4; h < nh; h += hstep) {
+    float M = -INFINITY;
+    bool bad = false;
+    for (int cc = c; cc <= c_last; ++cc) {
+      const float* ml = p.part_ml + (piece_of(cc) * hpp + h) * 2;
+      M = fmaxf(M, __ldcg(ml));
+      bad |= __ldcg(ml + 1) < 0.f;
     }
-    for (int cc0 = c; cc0 <= c_last; cc0 += PB) {
-      float m[PB][HB], l[PB][HB];
-      float4 a[PB][HB];
-#pragma unroll
-      for (int i = 0; i < PB; ++i) {
-        const int cc = cc0 + i;
-        const size_t piece = (static_cast<size_t>(cc) * 2 + (cc == c ? first_slot : 0)) * p.gs + pi;
-#pragma unroll
-        for (int k = 0; k < HB; ++k) {
-          const int h = hb + k * hstep;
-          if (cc <= c_last && h < nh) {
-            const float* ml = p.part_ml + (piece * hpp + h) * 2;
-            m[i][k] = __ldcg(ml);
-            l[i][k] = __ldcg(ml + 1);
-            a[i][k] = __ldcg(reinterpret_cast<const float4*>(p.part_acc + (piece * hpp + h) * D + d4));
-          } else {
-            m[i][k] = -INFINITY;
-            l[i][k] = 0.f;
-            a[i][k] = make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < PB; ++i)
-#pragma unroll
-        for (int k = 0; k < HB; ++k) {
-          bad[k] |= l[i][k] < 0.f;
-          if (m[i][k] != -INFINITY) {
-            const float mn = fmaxf(M[k], m[i][k]);
-            const float sa = exp2f(M[k] - mn), sb = exp2f(m[i][k] - mn);
-            L[k] = L[k] * sa + l[i][k] * sb;
-            O[k].x = O[k].x * sa + a[i][k].x * sb;
-            O[k].y = O[k].y * sa + a[i][k].y * sb;
-            O[k].z = O[k].z * sa + a[i][k].z * sb;
-            O[k].w = O[k].w * sa + a[i][k].w * sb;
-            M[k] = mn;
-          }
-        }
+    float L = 0.f;
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int cc = c; cc <= c_last; ++cc) {
+      const size_t pc = piece_of(cc);
+      const float* ml = p.part_ml + (pc * hpp + h) * 2;
+      const float m = __ldcg(ml), l = __ldcg(ml + 1);
+      const float w = m == -INFINITY ? 0.f : exp2f(m - M);
+      L = fmaf(l, w, L);
+      const float4 a = __ldcg(reinterpret_cast<const float4*>(p.part_acc + (pc * hpp + h) * D + d4));
+      O.x = fmaf(a.x, w, O.x);
+      O.y = fmaf(a.y, w, O.y);
+      O.z = fmaf(a.z, w, O.z);
+      O.w = fmaf(a.w, w, O.w);
     }
-#pragma unroll
-    for (int k = 0; k < HB; ++k) {
-      const int h = hb + k * hstep;
-      if (h < nh) {
-        uint2 packed = make_uint2(0u, 0u);
-        if (!bad[k]) {
-          const float inv = 1.f / L[k];
-          packed.x = pack2<T>(O[k].x * inv, O[k].y * inv);
-          packed.y = pack2<T>(O[k].z * inv, O[k].w * inv);
-        }
-        *reinterpret_cast<uint2*>(out_rows + h * D + d4) = packed;
+    uint2 packed = make_uint2(0u, 0u);
+    if (!bad) {
+      const float inv = 1.f / L;
+      packed.x = pack2<T>(O.x * inv, O.y * inv);
+      packed.y = pack2<T>(O.z * inv, O.w * inv);
+    }
+    *reinterpret_cast<uint2*>(out_rows + h * D + d4) = packed;
+  }
+}
+
+// Wait for phase 0 of a single-use mbarrier, bounded by kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait_once(uint32_t bar) {
+  if (mbar_try_wait(bar, 0)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, 0)) return true;
+    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// One warp merges the cut pairs it completed (up to two) through its own ring, which is
+// idle once the share is streamed: every piece's O is copied in by one bulk copy per piece
+// and its (m, l) by plain loads (a single round trip to L2 for all pieces), then the
+// pieces are folded in CTA order: M = max m_i, w_i = 2^(m_i - M), L = sum l_i w_i,
+// out = sum w_i acc_i / L.  Returns false, having done nothing, when the pieces do not fit
+// in the ring.
+template <int D, typename T>
+__device__ bool merge_staged(const Params& p, int pi, const CutPiece& job0, const CutPiece& job1,
+                             int njobs, uint32_t ring, uint8_t* ring_ptr, int ring_bytes,
+                             uint32_t bar, int lane) {
+  const int hpp = p.heads_per_pair;
+  int need = 0;
+  for (int j = 0; j < njobs; ++j) {
+    const CutPiece& cp = j == 0 ? job0 : job1;
+    need += (cp.c_last - cp.c_first + 1) * cp.nh * (D * 4 + 8);
+  }
+  if (need > ring_bytes) return false;
+  // layout in the ring: per job, per piece: acc [nh][D] floats, then all (m, l) pairs.
+  // Lane i copies piece i's acc with one bulk copy (cp.async.bulk; completion counted in
+  // bytes on this warp's mbarrier); the (m, l) pairs come in through plain loads.
+  const int np0 = job0.c_last - job0.c_first + 1;
+  const int np1 = njobs > 1 ? job1.c_last - job1.c_first + 1 : 0;
+  const uint32_t rb0 = job0.nh * D * 4, rb1 = job1.nh * D * 4;
+  const uint32_t acc_bytes = np0 * rb0 + np1 * rb1;
+  __syncwarp();
+  if (lane == 0) mbar_arrive_expect_tx(bar, acc_bytes);
+  __syncwarp();
+  // the ring was last read through the generic proxy; the bulk copies write it through
+  // the async proxy
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  for (int i = lane; i < np0 + np1; i += 32) {
+    const bool first = i < np0;
+    const CutPiece& cp = first ? job0 : job1;
+    const int cc = cp.c_first + (first ? i : i - np0);
+    const size_t piece = (static_cast<size_t>(cc) * 2 + (cc == cp.c_first ? cp.first_slot : 0)) * p.gs + pi;
+    const uint32_t off = first ? i * rb0 : np0 * rb0 + (i - np0) * rb1;
+    bulk_g2s(ring + off, p.part_acc + piece * hpp * D, first ? rb0 : rb1, bar);
+  }
+  float2* ml = reinterpret_cast<float2*>(ring_ptr + acc_bytes);
+  {
+    int k = 0;
+    for (int j = 0; j < njobs; ++j) {
+      const CutPiece& cp = j == 0 ? job0 : job1;
+      const int np = cp.c_last - cp.c_first + 1;
+      for (int i = lane; i < np * cp.nh; i += 32) {
+        const int cc = cp.c_first + i / cp.nh, h = i % cp.nh;
+        const size_t piece = (static_cast<size_t>(cc) * 2 + (cc == cp.c_first ? cp.first_slot : 0)) * p.gs + pi;
+        const float* src = p.part_ml + (piece * hpp + h) * 2;
+        ml[k + i] = make_float2(__ldcg(src), __ldcg(src + 1));
       }
+      k += np * cp.nh;
     }
   }
+  __syncwarp();  // (the (m, l) stores, before lanes read other lanes' entries)
+  // Pass 1, one lane per (job, head): M = max m_i, then each piece's weight 2^(m_i - M)
+  // (0 for an empty piece) in place of m_i, and L = sum l_i 2^(m_i - M) in place of the
+  // first piece's l (bad pieces, l < 0, make L negative: the head's output is zeros).
+  {
+    int moff = 0;
+    for (int j = 0; j < njobs; ++j) {
+      const CutPiece& cp = j == 0 ? job0 : job1;
+      const int np = cp.c_last - cp.c_first + 1;
+      if (lane < cp.nh) {
+        const int h = lane;
+        float M = -INFINITY;
+        bool bad = false;
+        for (int i = 0; i < np; ++i) {
+          const float2 v = ml[moff + i * cp.nh + h];
+          M = fmaxf(M, v.x);
+          bad |= v.y < 0.f;
+        }
+        float L = 0.f;
+        for (int i = 0; i < np; ++i) {
+          float2 v = ml[moff + i * cp.nh + h];
+          const float w = v.x == -INFINITY ? 0.f : exp2f(v.x - M);
+          L = fmaf(v.y, w, L);
+          v.x = w;
+          ml[moff + i * cp.nh + h] = v;
+        }
+        ml[moff + h].y = bad ? -1.f : L;  // (read back below only through this slot)
+      }
+      moff += np * cp.nh;
+    }
+  }
+  if (!mbar_wait_once(bar)) {  // (bounded; never expected to expire)
+    if (lane == 0) atomicOr(p.err, kErrTimeout);
+    return true;
+  }
+  __syncwarp();
+  // Pass 2: out = sum_i w_i acc_i / L, pieces in CTA order.
+  constexpr int C4 = D / 4;
+  int aoff = 0, moff = 0;
+  for (int j = 0; j < njobs; ++j) {
+    const CutPiece& cp = j == 0 ? job0 : job1;
+    const int np = cp.c_last - cp.c_first + 1;
+    T* out_rows = reinterpret_cast<T*>(p.out) + (static_cast<size_t>(cp.s) * p.num_q_heads + cp.h0) * D;
+    const float* acc = reinterpret_cast<const float*>(ring_ptr + aoff);
+    for (int idx = lane; idx < cp.nh * C4; idx += 32) {
+      const int h = idx / C4, d4 = (idx % C4) * 4;
+      float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+      for (int i = 0; i < np; ++i) {
+        const float w = ml[moff + i * cp.nh + h].x;
+        const float4 a = *reinterpret_cast<const float4*>(acc + (i * cp.nh + h) * D + d4);
+        O.x = fmaf(a.x, w, O.x);
+        O.y = fmaf(a.y, w, O.y);
+        O.z = fmaf(a.z, w, O.z);
+        O.w = fmaf(a.w, w, O.w);
+      }
+      const float L = ml[moff + h].y;
+      uint2 packed = make_uint2(0u, 0u);
+      if (L >= 0.f) {
+        const float inv = 1.f / L;
+        packed.x = pack2<T>(O.x * inv, O.y * inv);
+        packed.y = pack2<T>(O.z * inv, O.w * inv);
+      }
+      *reinterpret_cast<uint2*>(out_rows + h * D + d4) = packed;
+    }
+    aoff += np * cp.nh * D * 4;
+    moff += np * cp.nh;
+  }
+  return true;
 }
 
 template <int D>
@@ -420,6 +521,7 @@ struct Smem {
   long long start_pre;
   int start_s;
   int last[kWarps];  // per pair group: this CTA's arrival completed the pair
+  unsigned long long merge_bar[kWarps];  // per warp, single use: the staged merge's copies
 };
 
 // Q^T of a pair as MMA B fragments (column n = head 8*nt + lane / 4; heads >= nh are zero).
@@ -487,6 +589,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   // writes are visible past this point; the next one may start launching.
   pdl_wait_primary();
   pdl_launch_dependents();
+
+  if (lane == 0) {
+    mbar_init(smem_addr(&sm.merge_bar[warp]), 1);
+    fence_mbar_init();
+  }
 
   // ---- setup: total units W, this CTA's share [w0, w1), and its first family ----
   const int per = (p.num_seqs + kThreads - 1) / kThreads;
@@ -908,6 +1015,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       if (gt == 0) sm.last[pi] = bits;
       gsync();
       bits = sm.last[pi];
+    }
+    if (P == 1 && bits) {
+      const int nj = (bits & 1) + ((bits >> 1) & 1);
+      const CutPiece& j0 = (bits & 1) ? cut_a : cut_b;
+      if (merge_staged<D, T>(p, pi, j0, cut_b, nj, ring, sm.ring[warp][0], R * G_::kStageBytes,
+                             smem_addr(&sm.merge_bar[warp]), lane))
+        bits = 0;
     }
     for (int k = 0; k < ncut; ++k) {
       if (!(bits & (1 << k))) continue;
