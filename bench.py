@@ -1,10 +1,12 @@
 """Benchmark: paged decode on the Llama-3.1-8B-shaped batch, one JSON line.
 
 A step is one pass of the whole hot path over one batch: the cache write of each
-sequence's newest token (64 tokens through pa_reshape_and_cache) followed by paged decode
-attention over every sequence (pa_decode: one persistent kernel; the last CTA to finish
-a pair cut between CTAs merges its split-KV pieces).  The decode kernel's own duration is
-timed separately: --steps launches back to back in the same clock-sampled window.
+sequence's newest token followed by paged decode attention over every sequence,
+contexts including that token.  The step runs as one kernel (pa_decode_append: one
+persistent kernel; the last CTA to finish a pair cut between CTAs merges its split-KV
+pieces); the same step as two calls (pa_reshape_and_cache, then pa_decode) is timed
+too and reported beside it.  The decode kernel's own duration is timed separately:
+--steps launches of pa_decode back to back in the same clock-sampled window.
 
 Workload (seeded, synthetic; no dataset, no weights): 64 sequences, 32 query / 8 kv
 heads, head_dim 128, bf16, block_size 16, context lengths uniform in
@@ -47,9 +49,9 @@ def kernel_source_hash():
 
 
 def step_bytes(wl):
-    """Algorithmic bytes of one step: K and V of every valid token, q and out, the block
-    table entries used and the context lengths (decode); plus the new tokens' K/V rows read
-    and written and their slots (cache write)."""
+    """Algorithmic bytes of one step: K and V of every valid token (the newest included),
+    q and out, the block table entries used and the context lengths (decode); plus the
+    newest tokens' K/V rows written to the cache (cache write)."""
     e = 2
     n, hq, hkv, d, bs = wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.block_size
     ctx = [int(c) for c in wl.context_lens]
@@ -57,7 +59,7 @@ def step_bytes(wl):
     qo = 2 * n * hq * d * e
     table = sum(-(-c // bs) for c in ctx) * 4 + 4 * n
     decode = kv + qo + table
-    reshape = 2 * (n * hkv * d * e * 2) + 8 * n
+    reshape = n * hkv * d * e * 2
     padded_kv = sum(-(-c // bs) * bs for c in ctx) * hkv * d * e * 2
     return decode, reshape, padded_kv
 
@@ -198,6 +200,11 @@ def run_gpu(args, rank, world, local_rank):
 
     def step(i):
         b = batches[i % ROTATE]
+        pa.decode_append(b["q"], b["key"], b["value"], k_cache, v_cache, b["tables"], b["ctx"],
+                         wl.scale, out=b["out"], workspace=ws, stream=stream)
+
+    def step_two_calls(i):
+        b = batches[i % ROTATE]
         pa.reshape_and_cache(b["key"], b["value"], k_cache, v_cache, b["slots"], stream=stream)
         pa.decode(b["q"], k_cache, v_cache, b["tables"], b["ctx"], wl.scale, out=b["out"],
                   workspace=ws, stream=stream)
@@ -210,6 +217,7 @@ def run_gpu(args, rank, world, local_rank):
     for i in range(args.warmup):
         step(i)
         decode_only(i)
+        step_two_calls(i)
     torch.cuda.synchronize(device)
     if pa.get_device_error(stream=stream):
         raise RuntimeError("device error flags set during warm-up")
@@ -219,7 +227,7 @@ def run_gpu(args, rank, world, local_rank):
         sampler.start()
         time.sleep(0.3)
     K = args.steps
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(device)
@@ -239,19 +247,26 @@ def run_gpu(args, rank, world, local_rank):
         decode_only(i)
     ev[3].record(stream)
     torch.cuda.synchronize(device)
+    # the same step as two calls
+    ev[4].record(stream)
+    for i in range(K):
+        step_two_calls(i)
+    ev[5].record(stream)
+    torch.cuda.synchronize(device)
     t1 = time.time()
     clocks = sampler.stop(t0, t1) if sampler else None
     flags = pa.get_device_error(stream=stream)
     total_ms = ev[0].elapsed_time(ev[1])
     decode_ms = ev[2].elapsed_time(ev[3]) / K
+    two_calls_ms = ev[4].elapsed_time(ev[5]) / K
     if world > 1:
-        t = torch.tensor([total_ms, decode_ms], device=device)
+        t = torch.tensor([total_ms, decode_ms, two_calls_ms], device=device)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms, decode_ms = float(t[0].item()), float(t[1].item())
+        total_ms, decode_ms, two_calls_ms = (float(x) for x in t.tolist())
 
     # end to end through the binding with host buffers: inputs from pinned host memory
     # every step, the output read back every step
-    names = ("q", "tables", "ctx", "slots", "key", "value")
+    names = ("q", "tables", "ctx", "key", "value")
     host_in = [{k: b[k].cpu().pin_memory() for k in names} for b in batches]
     host_out = torch.empty(batches[0]["out"].shape, dtype=batches[0]["out"].dtype).pin_memory()
     dev_in = {k: torch.empty_like(batches[0][k]) for k in names}
@@ -263,10 +278,9 @@ def run_gpu(args, rank, world, local_rank):
         with torch.cuda.stream(stream):
             for k, v in host_in[i % ROTATE].items():
                 dev_in[k].copy_(v, non_blocking=True)
-            pa.reshape_and_cache(dev_in["key"], dev_in["value"], k_cache, v_cache, dev_in["slots"],
-                                 stream=stream)
-            pa.decode(dev_in["q"], k_cache, v_cache, dev_in["tables"], dev_in["ctx"], wl.scale,
-                      out=dev_out, workspace=ws, stream=stream)
+            pa.decode_append(dev_in["q"], dev_in["key"], dev_in["value"], k_cache, v_cache,
+                             dev_in["tables"], dev_in["ctx"], wl.scale, out=dev_out,
+                             workspace=ws, stream=stream)
             host_out.copy_(dev_out, non_blocking=True)
 
     for i in range(max(3, args.warmup)):
@@ -282,6 +296,7 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.synchronize(device)
     e2e_ms = e0.elapsed_time(e1) / ke
     return {"wl": wl, "total_ms": total_ms, "decode_ms": decode_ms, "e2e_ms": e2e_ms,
+            "two_calls_ms": two_calls_ms,
             "h2d": h2d, "d2h": d2h, "clocks": clocks, "flags": flags}
 
 
@@ -330,6 +345,56 @@ print(json.dumps({{"seqs": len(per), "seconds": sum(p[0] for p in per),
     return json.loads(r.stdout.strip().splitlines()[-1])
 
 
+def oracle_parallel(name, passes=3):
+    """The same oracle sharded by sequence over every host core: the batch's paged caches
+    are built once in a CUDA-free process, then worker processes forked from it (fork is
+    safe there: no CUDA in that process) decode disjoint sequence sets.  Wall time of
+    `passes` whole-batch passes."""
+    code = f"""
+import json, os, sys, time
+sys.path.insert(0, {ROOT!r})
+import multiprocessing as mp
+import numpy as np
+import workloads
+from oracle import attention, cache_ops, formats
+from oracle.block_pool import BlockPool
+wl = workloads.RECIPES[{name!r}]()
+pool = BlockPool(wl.num_blocks, wl.block_size, wl.free_order)
+n, T = wl.num_seqs, wl.max_blocks_per_seq
+tables = np.full((n, T), -1, dtype=np.int32)
+slots = []
+for s in range(n):
+    c = int(wl.context_lens[s]); pool.allocate(s, c)
+    t = pool.block_table(s); tables[s, :len(t)] = t
+    slots += [pool.slot(s, i) for i in range(c)]
+shape = (wl.num_blocks, wl.num_kv_heads, wl.block_size, wl.head_dim)
+nan = formats.FORMATS[wl.dtype]["qnan"]
+kc = np.full(shape, nan, dtype=np.uint16); vc = kc.copy()
+kc, vc = cache_ops.reshape_and_cache(kc, vc, wl.keys, wl.values, np.array(slots, dtype=np.int64))
+def work(seqs):
+    attention.paged_decode_bits(wl.q, kc, vc, tables, wl.context_lens, wl.scale,
+                                wl.block_size, wl.dtype, seqs=seqs)
+    return len(seqs)
+cores = len(os.sched_getaffinity(0))
+shards = [list(range(k, n, cores)) for k in range(cores) if k < n]
+nbytes = sum(int(c) * wl.num_kv_heads * wl.head_dim * 4 + 2 * wl.num_q_heads * wl.head_dim * 2
+             + (-(-int(c) // wl.block_size)) * 4 + 4 for c in wl.context_lens)
+with mp.get_context("fork").Pool(len(shards)) as p:
+    p.map(work, shards)  # warm-up
+    t0 = time.time()
+    for _ in range({passes}):
+        p.map(work, shards)
+    wall = (time.time() - t0) / {passes}
+print(json.dumps({{"cores": cores, "workers": len(shards), "seconds": wall, "bytes": nbytes}}))
+"""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
+    if r.returncode != 0:
+        raise RuntimeError("parallel oracle baseline failed:\n" + r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -370,6 +435,7 @@ def main():
     traffic = recorded_traffic()
     cpu = (oracle_sample(args.workload, args.cpu_baseline_seconds, 10 ** 9)
            if args.cpu_baseline_seconds > 0 else None)
+    cpu_par = oracle_parallel(args.workload) if args.cpu_baseline_seconds > 0 else None
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -379,6 +445,7 @@ def main():
         "warmup": args.warmup,
         "ms_per_step": round(res["total_ms"] / args.steps, 5),
         "us_per_step": round(1e3 * res["total_ms"] / args.steps, 2),
+        "us_per_step_two_calls": round(1e3 * res["two_calls_ms"], 2),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -389,7 +456,8 @@ def main():
                          f"{int(wl.context_lens.max())} (sum {int(wl.context_lens.sum())}), "
                          f"{wl.num_q_heads} q / {wl.num_kv_heads} kv heads, head_dim {wl.head_dim}, "
                          f"block_size {wl.block_size}, pool {wl.num_blocks} blocks; step = "
-                         f"reshape_and_cache of {wl.num_seqs} new tokens + paged decode"),
+                         f"cache write of {wl.num_seqs} new tokens + paged decode, one kernel "
+                         f"(pa_decode_append)"),
             "l2": f"each batch's K/V ({dec_b / 1e6:.0f} MB) exceeds L2; {ROTATE} batches in "
                   "disjoint blocks rotated every step",
             "parallelism": f"replicas x{world}",
@@ -417,6 +485,15 @@ def main():
             "sample": f"float64 NumPy oracle, single thread, {cpu['seqs']} sequences of the same "
                       f"batch in {cpu['seconds']:.1f} s of CPU time",
         },
+        "cpu_baseline_parallel": None if cpu_par is None else {
+            "value": round(cpu_par["bytes"] / cpu_par["seconds"] / 1e9, 4),
+            "unit": "GB/s",
+            "cores": cpu_par["workers"],
+            "kind": "oracle",
+            "sample": f"float64 NumPy oracle, the whole batch sharded by sequence over "
+                      f"{cpu_par['workers']} processes ({cpu_par['cores']} host cores), "
+                      f"{cpu_par['seconds'] * 1e3:.0f} ms per batch (wall)",
+        },
         "e2e": {
             "value": round(world * (dec_b + resh_b) / (res["e2e_ms"] / 1e3) / 1e9, 1),
             "unit": "GB/s",
@@ -425,8 +502,8 @@ def main():
             "us_per_step": round(1e3 * res["e2e_ms"], 2),
         },
         "clocks": res["clocks"],
-        # per timed step: reshape_and_cache_kernel + decode_kernel; plus the decode-only loop
-        "gpu_launches": 3 * args.steps,
+        # timed: steps (1 kernel each), decode alone (1 each), two-call steps (2 each)
+        "gpu_launches": 4 * args.steps,
         "device_error_flags": res["flags"],
     }
     print(json.dumps(line))

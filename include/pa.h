@@ -112,6 +112,30 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache,
               void* workspace, size_t workspace_bytes, pa_dtype dtype, cudaStream_t stream);
 
 /*
+ * pa_decode_append -- one whole decode step in one kernel: the cache write of every
+ * sequence's newest token followed by pa_decode over contexts that include it.
+ *
+ * key_new, value_new: [num_seqs, Hkv, d] device, row s = the token just produced by
+ * sequence s, at its position ctx_s - 1, so its slot is
+ * block_tables[s][(ctx_s - 1) / B] * B + (ctx_s - 1) % B (the slot formula of
+ * pa_reshape_and_cache; chenyuan1125, section 页表真正解开的…: the new token goes into the
+ * last block's free slot, then attention reads the context through the table).
+ * Results -- out and both caches -- are bit-identical to pa_reshape_and_cache of those rows
+ * into those slots followed by pa_decode with the same arguments.  The attention takes the
+ * newest row from key_new/value_new, and the cache row is stored during the same kernel,
+ * so that slot must not lie inside another sequence's context in the same call (true once
+ * copy-on-write has given every written last block a single owner).  A sequence whose
+ * context length or newest block id is invalid writes nothing and is flagged as in
+ * pa_decode.  Other arguments, errors and the workspace are pa_decode's.
+ */
+int pa_decode_append(const void* q, const void* key_new, const void* value_new, void* k_cache,
+                     void* v_cache, const int32_t* block_tables, int max_blocks_per_seq,
+                     const int32_t* context_lens, int num_seqs, int num_q_heads,
+                     int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+                     void* out, void* workspace, size_t workspace_bytes, pa_dtype dtype,
+                     cudaStream_t stream);
+
+/*
  * pa_decode_fixed_scratch -- pa_decode for callers that cannot allocate device memory.
  *
  * The pages have no counterpart to this call; it exists for library users.  Some callers

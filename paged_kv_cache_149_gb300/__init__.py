@@ -47,6 +47,8 @@ SIGNATURES = {
     "pa_reshape_and_cache": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp]),
     "pa_decode": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
                          _f32, _vp, _vp, _sz, _i32, _vp]),
+    "pa_decode_append": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
+                                _i32, _i32, _f32, _vp, _vp, _sz, _i32, _vp]),
     "pa_decode_workspace_size": (_sz, [_i32, _i32, _i32]),
     "pa_decode_fixed_scratch": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                                        _i32, _f32, _vp, _i32, _vp]),
@@ -198,6 +200,38 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=None, wor
         _dev(out, "out"), _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
         _dtype_code(q), _stream_ptr(stream, q.device))
     _check(st, "pa_decode")
+    return out
+
+
+def decode_append(q, key_new, value_new, k_cache, v_cache, block_tables, context_lens, scale,
+                  out=None, workspace=None, stream=None):
+    """One decode step in one kernel: writes each sequence's newest token (``key_new`` /
+    ``value_new`` [num_seqs, num_kv_heads, head_dim], at position context_lens[s] - 1) into
+    the caches and returns attention over contexts that include it.  Same results as
+    reshape_and_cache into those slots followed by decode."""
+    import torch
+    n, hq, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    _need(v_cache.shape == k_cache.shape and d == d2, "shape mismatch")
+    _need(key_new.shape == (n, hkv, d) and value_new.shape == (n, hkv, d),
+          "key_new / value_new must be [num_seqs, num_kv_heads, head_dim]")
+    _need(block_tables.dim() == 2 and block_tables.shape[0] == n, "block_tables must be [num_seqs, T]")
+    _need(context_lens.shape == (n,), "context_lens must be [num_seqs]")
+    _need(q.dtype == k_cache.dtype == v_cache.dtype == key_new.dtype == value_new.dtype,
+          "dtype mismatch")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out.shape == q.shape and out.dtype == q.dtype, "out must match q")
+    if workspace is None:
+        workspace = make_workspace(hq, hkv, d, q.device)
+    st = lib().pa_decode_append(
+        _dev(q, "q"), _dev(key_new, "key_new"), _dev(value_new, "value_new"),
+        _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+        _dev(context_lens, "context_lens", torch.int32), n, hq, hkv, d, bs, nb, float(scale),
+        _dev(out, "out"), _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _dtype_code(q), _stream_ptr(stream, q.device))
+    _check(st, "pa_decode_append")
     return out
 
 

@@ -116,11 +116,14 @@ size_t pa_decode_workspace_size(int num_q_heads, int num_kv_heads, int head_dim)
   return pa::decode_workspace_bytes(di.sm_count, num_q_heads, num_kv_heads, head_dim);
 }
 
-int pa_decode(const void* q, const void* k_cache, const void* v_cache,
-              const int32_t* block_tables, int max_blocks_per_seq,
-              const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
-              int head_dim, int block_size, int num_blocks, float scale, void* out,
-              void* workspace, size_t workspace_bytes, pa_dtype dtype, cudaStream_t stream) {
+namespace {
+
+// pa_decode and pa_decode_append: argument checks, then one launch.
+int decode_call(const void* q, const void* key_new, const void* value_new, const void* k_cache,
+                const void* v_cache, const int32_t* block_tables, int max_blocks_per_seq,
+                const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+                int head_dim, int block_size, int num_blocks, float scale, void* out,
+                void* workspace, size_t workspace_bytes, pa_dtype dtype, cudaStream_t stream) {
   if (num_seqs < 0 || num_blocks < 1 || max_blocks_per_seq < 1 ||
       !shape_ok(num_kv_heads, head_dim, block_size) || num_q_heads < num_kv_heads ||
       num_q_heads % num_kv_heads != 0 || !std::isfinite(scale) ||
@@ -132,6 +135,8 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache,
   if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PA_ERR_ARG;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
     return PA_ERR_ARG;
+  if ((key_new != nullptr) != (value_new != nullptr)) return PA_ERR_ARG;
+  if (key_new && (!aligned16(key_new) || !aligned16(value_new))) return PA_ERR_ARG;
   DeviceInfo di;
   if (!device_info(&di)) return PA_ERR_CUDA;
   const size_t need =
@@ -141,6 +146,8 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache,
   a.q = q;
   a.k_cache = k_cache;
   a.v_cache = v_cache;
+  a.key_new = key_new;
+  a.value_new = value_new;
   a.block_tables = block_tables;
   a.context_lens = context_lens;
   a.out = out;
@@ -156,6 +163,30 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache,
   a.bf16 = dtype == PA_BF16;
   a.err = di.err;
   return pa::decode_launch(a, di.sm_count, stream);
+}
+
+}  // namespace
+
+int pa_decode(const void* q, const void* k_cache, const void* v_cache,
+              const int32_t* block_tables, int max_blocks_per_seq,
+              const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+              int head_dim, int block_size, int num_blocks, float scale, void* out,
+              void* workspace, size_t workspace_bytes, pa_dtype dtype, cudaStream_t stream) {
+  return decode_call(q, nullptr, nullptr, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                     context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                     num_blocks, scale, out, workspace, workspace_bytes, dtype, stream);
+}
+
+int pa_decode_append(const void* q, const void* key_new, const void* value_new, void* k_cache,
+                     void* v_cache, const int32_t* block_tables, int max_blocks_per_seq,
+                     const int32_t* context_lens, int num_seqs, int num_q_heads,
+                     int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+                     void* out, void* workspace, size_t workspace_bytes, pa_dtype dtype,
+                     cudaStream_t stream) {
+  if (num_seqs > 0 && (!key_new || !value_new)) return PA_ERR_ARG;
+  return decode_call(q, key_new, value_new, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                     context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                     num_blocks, scale, out, workspace, workspace_bytes, dtype, stream);
 }
 
 int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* block_mapping, int num_pairs,

@@ -81,6 +81,10 @@ struct Params {
   const uint8_t* q;
   const uint8_t* k_cache;
   const uint8_t* v_cache;
+  // Fused cache write (pa_decode_append), else null: the newest token of each sequence,
+  // [n][Hkv][D].  Its row is attended from here and stored at position ctx - 1.
+  const uint8_t* key_new;
+  const uint8_t* value_new;
   const int32_t* block_tables;
   const int32_t* context_lens;
   uint8_t* out;
@@ -178,6 +182,7 @@ __device__ __forceinline__ PairHeads pair_heads(const Params& p, int pair) {
 // unit index = its phase (mod P).  Families with an invalid context carry no stages.
 struct Stage {
   int s, kvh, t0, nt;  // sequence, kv head, first token, valid tokens (1..16)
+  bool last;           // holds the context's last token
 };
 
 struct StageIt {
@@ -205,6 +210,7 @@ __device__ __forceinline__ bool next_stage(StageIt& it, int pi, int phase, long 
       st.kvh = it.kvh;
       st.t0 = it.j * kStageTok;
       st.nt = min(kStageTok, it.f.ctx - st.t0);
+      st.last = st.t0 + st.nt == it.f.ctx;
       it.j += p.phases;
       return true;
     }
@@ -681,8 +687,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
           const size_t grow = !live ? row_x : (r < p.block_size ? row_x + r : row_y + (r - p.block_size));
           const size_t src = (grow * D + ch * 8) * 2;
           const uint32_t so = swz(row, ch);
-          cp_async16(dst + so, p.k_cache + src, live ? 16u : 0u);
-          cp_async16(dst + G_::kKBytes + so, p.v_cache + src, live ? 16u : 0u);
+          if (p.key_new && nxt.last && row == nxt.nt - 1) {
+            // the newest token: from the step's input (the cache row is written later)
+            const size_t nsrc = ((static_cast<size_t>(nxt.s) * p.num_kv_heads + nxt.kvh) * D + ch * 8) * 2;
+            cp_async16(dst + so, p.key_new + nsrc, 16u);
+            cp_async16(dst + G_::kKBytes + so, p.value_new + nsrc, 16u);
+          } else {
+            cp_async16(dst + so, p.k_cache + src, live ? 16u : 0u);
+            cp_async16(dst + G_::kKBytes + so, p.v_cache + src, live ? 16u : 0u);
+          }
         }
       }
       ++issued;
@@ -850,6 +863,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
           ldsm_x4_t(vb + swz(lrow + ((lmat >> 1) << 3), 2 * mt + (lmat & 1)), a);
 #pragma unroll
           for (int nt = 0; nt < NTH; ++nt) mma16816<T>(o[mt][nt], a, pb[nt][0], pb[nt][1]);
+        }
+        if (p.key_new && j == f.ns - 1) {
+          // fused cache write: the newest token's K and V rows, from the slot, to position
+          // ctx - 1 of the sequence (lanes take the 16-byte chunks of K, then of V)
+          constexpr int CH = G_::kRowChunks;
+          const int t = f.ctx - 1;
+          const int blk = __ldg(p.block_tables + static_cast<size_t>(f.s) * p.max_blocks_per_seq +
+                                (t >> p.log2_block));
+          if (lane < 2 * CH && blk >= 0 && blk < p.num_blocks) {
+            const int c16 = lane % CH;
+            const uint32_t from = (lane < CH ? kb : vb) + swz(nt_tok - 1, c16);
+            const size_t to = ((static_cast<size_t>(blk) * p.num_kv_heads + ph.kvh) * p.block_size +
+                               (t & (p.block_size - 1))) * D + c16 * 8;
+            uint4 v;
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                         : "r"(from));
+            reinterpret_cast<uint4*>(const_cast<uint8_t*>(lane < CH ? p.k_cache : p.v_cache))[to / 8] = v;
+          }
         }
       }
       __syncwarp();  // every lane is done with the slot before a later stage refills it
@@ -1094,6 +1126,8 @@ int decode_launch(const DecodeArgs& a, int grid, cudaStream_t stream) {
   p.q = static_cast<const uint8_t*>(a.q);
   p.k_cache = static_cast<const uint8_t*>(a.k_cache);
   p.v_cache = static_cast<const uint8_t*>(a.v_cache);
+  p.key_new = static_cast<const uint8_t*>(a.key_new);
+  p.value_new = static_cast<const uint8_t*>(a.value_new);
   p.block_tables = a.block_tables;
   p.context_lens = a.context_lens;
   p.out = static_cast<uint8_t*>(a.out);

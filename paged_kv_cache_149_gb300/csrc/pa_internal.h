@@ -10,8 +10,10 @@ namespace pa {
 
 struct DecodeArgs {
   const void* q;
-  const void* k_cache;
+  const void* k_cache;  // written only by the fused cache write (key_new != null)
   const void* v_cache;
+  const void* key_new;  // pa_decode_append: newest token per sequence [n][Hkv][d], else null
+  const void* value_new;
   const int32_t* block_tables;
   const int32_t* context_lens;
   void* out;
