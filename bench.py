@@ -259,10 +259,6 @@ def run_gpu(args, rank, world, local_rank):
     total_ms = ev[0].elapsed_time(ev[1])
     decode_ms = ev[2].elapsed_time(ev[3]) / K
     two_calls_ms = ev[4].elapsed_time(ev[5]) / K
-    if world > 1:
-        t = torch.tensor([total_ms, decode_ms, two_calls_ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms, decode_ms, two_calls_ms = (float(x) for x in t.tolist())
 
     # end to end through the binding with host buffers: inputs from pinned host memory
     # every step, the output read back every step
@@ -395,7 +391,24 @@ print(json.dumps({{"cores": cores, "workers": len(shards), "seconds": wall, "byt
     return json.loads(r.stdout.strip().splitlines()[-1])
 
 
-def main():
+def max_over_ranks(values):
+    """Element-wise maximum of per-rank floats over the process group (NCCL on GPUs, or any
+    other backend on CPU tensors)."""
+    import torch
+    dev = (torch.device("cuda", torch.cuda.current_device())
+           if torch.distributed.get_backend() == "nccl" else torch.device("cpu"))
+    t = torch.tensor(values, dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+# per-rank times that the JSON line takes as the maximum over ranks
+RANK_TIMES = ("total_ms", "decode_ms", "two_calls_ms", "e2e_ms")
+
+
+def main(argv=None, runner=None, backend="nccl"):
+    """One JSON line on rank 0.  `runner` (default: the GPU run) and `backend` are
+    parameters so that the multi-rank host logic can run on CPU ranks."""
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=5000)
@@ -403,7 +416,7 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="llama31_8b")
     ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
-    args = ap.parse_args()
+    args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
 
@@ -419,8 +432,10 @@ def main():
 
     if world > 1:
         import torch
-        torch.distributed.init_process_group("nccl")
-    res = run_gpu(args, rank, world, local_rank)
+        torch.distributed.init_process_group(backend)
+    res = (runner or run_gpu)(args, rank, world, local_rank)
+    if world > 1:
+        res.update(zip(RANK_TIMES, max_over_ranks([res[k] for k in RANK_TIMES])))
     if rank != 0:
         if world > 1:
             import torch
