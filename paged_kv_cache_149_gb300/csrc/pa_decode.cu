@@ -60,9 +60,11 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kMaxHeads = 16;  // query heads per pair (MMA columns)
 constexpr float kLog2e = 1.4426950408889634f;
 // Stage-equivalents charged per family on top of its stages when cutting the batch into
-// per-SM shares: switching families (a new table row, the pair-end writes) costs a share
-// about as much time on GB300 as streaming 16 more stages.
-constexpr int kSegCost = 16;
+// per-SM shares.  A family switch (a new table row, the pair-end writes) and the cut-pair
+// work at the ends of a share cost it time; on GB300 a charge of 32 stages balanced the
+// shares best over batches of long, short and mixed sequences (16: 58.7 us, 32: 56.8 us,
+// 64: 58.4 us on 64 sequences of 128..2048 tokens; 16 x 8192 tokens: 102.9 / 96.5 / 93.9).
+constexpr int kSegCost = 32;
 
 template <int D>
 struct Geo {
