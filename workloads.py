@@ -23,6 +23,15 @@ Recipes (the shapes of the pages' workloads; no dataset or weights are involved)
                  1..15 private tokens per beam; 32 q / 8 kv heads, d=128, bf16, B=16
     long         8 seqs, ctx {8192,16384,24576,32768 x5}, 32 q / 8 kv heads, d=128, bf16,
                  B in {8,16,32}, K/V ~ N(0,1), pool 1.25x the blocks needed, shuffled
+
+Prefill recipes (q holds every new token of every sequence; query_start marks them):
+    prefill_tiny        4 seqs, ctx {5,40,100,33}, new tokens {5,17,33,1}, B=16, pool 64,
+                        4 q / 2 kv heads, d=64, fp16
+    prefill_llama31_8b  8 prompts of 2048 tokens from scratch, 32 q / 8 kv heads, d=128,
+                        bf16, B=16, pool 3.3x the blocks one batch needs (three batches
+                        rotate in disjoint blocks), shuffled
+    prefill_chunked     16 seqs, ctx ~ U[1024, 4096], the last 512 tokens new (a chunk of
+                        a longer prompt), otherwise as prefill_llama31_8b
 """
 from dataclasses import dataclass, field
 import math
@@ -174,6 +183,45 @@ def beam(seed=0, prompts=2, beams=8, prefix=1024, num_blocks=256):
                         private_values=pv, q=q)
 
 
+@dataclass
+class PrefillWorkload(DecodeWorkload):
+    """A prefill batch: like a decode batch, but q holds the newest q_len_s tokens of every
+    sequence, rows query_start[s] .. query_start[s+1]-1 (q is [total new tokens, Hq, d])."""
+    query_start: np.ndarray = None  # int64 [n + 1]
+
+
+def _prefill(name, rng, ctx, qlen, dtype, hq, hkv, d, bsz, num_blocks, max_ctx, scale,
+             kv_std=1.0, q_std=1.0):
+    base = _decode(name, rng, ctx, dtype, hq, hkv, d, bsz, num_blocks, max_ctx, scale, kv_std)
+    qlen = np.asarray(qlen, dtype=np.int64)
+    query_start = np.zeros(len(qlen) + 1, dtype=np.int64)
+    np.cumsum(qlen, out=query_start[1:])
+    q = normal_bits(rng, (int(query_start[-1]), hq, d), q_std, dtype)
+    fields = {k: getattr(base, k) for k in base.__dataclass_fields__}
+    fields["q"] = q
+    return PrefillWorkload(**fields, query_start=query_start)
+
+
+def prefill_tiny(seed=0):
+    rng = np.random.default_rng(seed)
+    return _prefill("prefill_tiny", rng, [5, 40, 100, 33], [5, 17, 33, 1], "fp16", 4, 2, 64,
+                    16, 64, 128, 1.0 / math.sqrt(64))
+
+
+def prefill_llama31_8b(seed=0, num_seqs=8, prompt=2048):
+    rng = np.random.default_rng(seed)
+    ctx = [prompt] * num_seqs
+    return _prefill("prefill_llama31_8b", rng, ctx, ctx, "bf16", 32, 8, 128, 16,
+                    int(3.3 * num_seqs * (prompt // 16)), prompt, 1.0 / math.sqrt(128))
+
+
+def prefill_chunked(seed=0, num_seqs=16, chunk=512):
+    rng = np.random.default_rng(seed)
+    ctx = rng.integers(1024, 4096, size=num_seqs, endpoint=True)
+    return _prefill("prefill_chunked", rng, ctx, [chunk] * num_seqs, "bf16", 32, 8, 128, 16,
+                    int(3.3 * sum(-(-int(c) // 16) for c in ctx)), 4096, 1.0 / math.sqrt(128))
+
+
 RECIPES = {
     "tiny": tiny,
     "llama31_8b": llama31_8b,
@@ -181,4 +229,7 @@ RECIPES = {
     "long_b8": lambda seed=0: long_context(8, seed),
     "long_b16": lambda seed=0: long_context(16, seed),
     "long_b32": lambda seed=0: long_context(32, seed),
+    "prefill_tiny": prefill_tiny,
+    "prefill_llama31_8b": prefill_llama31_8b,
+    "prefill_chunked": prefill_chunked,
 }
