@@ -112,6 +112,35 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache,
               void* workspace, size_t workspace_bytes, pa_dtype dtype, cudaStream_t stream);
 
 /*
+ * pa_prefill -- causal multi-query attention of each sequence's newest tokens over its
+ * paged context (a prompt from scratch, or a chunk of one).
+ *
+ * Sequence s owns query rows query_start[s] .. query_start[s+1]-1 of q: its newest
+ * q_len_s = query_start[s+1] - query_start[s] tokens, at positions ctx_s - q_len_s ..
+ * ctx_s - 1, whose K/V rows are already in the cache (write them first with
+ * pa_reshape_and_cache).  The token at position p attends to positions 0 .. p:
+ *   out[row, h, :] = sum_{t <= p} softmax(scale * <q[row, h, :], K_s[t, h / G, :]>) V_s[t, h / G, :]
+ * with K_s[t] = k_cache[block_tables[s][t / B], :, t % B, :] (horeb.top "vLLM
+ * PagedAttention：大模型推理的显存管理革命", section 分配策略: a prompt is allotted its
+ * blocks at prefill; daiw.org "Paged Attention", section 回顾与衔接: the attention kernel
+ * reads the block table).  Accumulation is fp32, the output rounded to nearest-even.
+ *
+ * q, out: [query_start[num_seqs], Hq, d] device, 16-byte aligned; query_start: int32
+ * [num_seqs + 1] device, non-decreasing from 0; max_query_len: host bound on q_len_s
+ * (the launch covers it; larger q_len_s are not computed).  Requires Hq / Hkv <= 64.
+ * A sequence whose context is invalid (ctx < 1, ctx > T * B, or q_len_s > ctx_s) gets
+ * zeros and PA_DEVERR_BAD_CONTEXT; a block id out of range gives zeros for the query
+ * block that reads it and PA_DEVERR_BAD_BLOCK.  Uses no workspace.  A launch is a
+ * programmatic dependent of the kernel before it in the stream.
+ */
+int pa_prefill(const void* q, const void* k_cache, const void* v_cache,
+               const int32_t* block_tables, int max_blocks_per_seq,
+               const int32_t* context_lens, const int32_t* query_start, int num_seqs,
+               int max_query_len, int num_q_heads, int num_kv_heads, int head_dim,
+               int block_size, int num_blocks, float scale, void* out, pa_dtype dtype,
+               cudaStream_t stream);
+
+/*
  * pa_decode_append -- one whole decode step in one kernel: the cache write of every
  * sequence's newest token followed by pa_decode over contexts that include it.
  *

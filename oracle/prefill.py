@@ -28,10 +28,11 @@ from .formats import decode_bits, encode_bits
 
 
 def paged_prefill(q_bits, k_cache_bits, v_cache_bits, block_tables, context_lens,
-                  query_start, scale, block_size, dtype):
+                  query_start, scale, block_size, dtype, seqs=None):
     """Returns (out float64 [num_q_rows, Hq, d], error bits int64 [n]).  A sequence with an
     invalid context, a bad block id among the blocks it uses, or q_len > ctx yields zeros
-    and its error bits."""
+    and its error bits.  With ``seqs``, only those sequences are computed (the rows of the
+    others stay zero)."""
     q_bits = np.asarray(q_bits)
     ntok, hq, d = q_bits.shape
     hkv = k_cache_bits.shape[1]
@@ -40,7 +41,7 @@ def paged_prefill(q_bits, k_cache_bits, v_cache_bits, block_tables, context_lens
     n = len(context_lens)
     out = np.zeros((ntok, hq, d), dtype=np.float64)
     errs = np.zeros(n, dtype=np.int64)
-    for s in range(n):
+    for s in (range(n) if seqs is None else seqs):
         qs, qe = int(query_start[s]), int(query_start[s + 1])
         qlen, ctx = qe - qs, int(context_lens[s])
         if qlen == 0:

@@ -49,6 +49,8 @@ SIGNATURES = {
                          _f32, _vp, _vp, _sz, _i32, _vp]),
     "pa_decode_append": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
                                 _i32, _i32, _f32, _vp, _vp, _sz, _i32, _vp]),
+    "pa_prefill": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
+                          _i32, _i32, _f32, _vp, _i32, _vp]),
     "pa_decode_workspace_size": (_sz, [_i32, _i32, _i32]),
     "pa_decode_fixed_scratch": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                                        _i32, _f32, _vp, _i32, _vp]),
@@ -232,6 +234,32 @@ def decode_append(q, key_new, value_new, k_cache, v_cache, block_tables, context
         _dev(out, "out"), _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
         _dtype_code(q), _stream_ptr(stream, q.device))
     _check(st, "pa_decode_append")
+    return out
+
+
+def prefill(q, k_cache, v_cache, block_tables, context_lens, query_start, scale,
+            max_query_len, out=None, stream=None):
+    """Causal attention of each sequence's newest tokens (q rows query_start[s] ..
+    query_start[s+1]-1, at positions ctx - q_len .. ctx - 1, their K/V already in the cache)
+    over its paged context; returns ``out`` shaped like q."""
+    import torch
+    ntok, hq, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    n = context_lens.shape[0]
+    _need(v_cache.shape == k_cache.shape and d == d2, "shape mismatch")
+    _need(block_tables.dim() == 2 and block_tables.shape[0] == n, "block_tables must be [num_seqs, T]")
+    _need(query_start.shape == (n + 1,), "query_start must be [num_seqs + 1]")
+    _need(q.dtype == k_cache.dtype == v_cache.dtype, "dtype mismatch")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out.shape == q.shape and out.dtype == q.dtype, "out must match q")
+    st = lib().pa_prefill(
+        _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+        _dev(context_lens, "context_lens", torch.int32),
+        _dev(query_start, "query_start", torch.int32), n, int(max_query_len), hq, hkv, d, bs,
+        nb, float(scale), _dev(out, "out"), _dtype_code(q), _stream_ptr(stream, q.device))
+    _check(st, "pa_prefill")
     return out
 
 

@@ -177,6 +177,48 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache,
                      num_blocks, scale, out, workspace, workspace_bytes, dtype, stream);
 }
 
+int pa_prefill(const void* q, const void* k_cache, const void* v_cache,
+               const int32_t* block_tables, int max_blocks_per_seq,
+               const int32_t* context_lens, const int32_t* query_start, int num_seqs,
+               int max_query_len, int num_q_heads, int num_kv_heads, int head_dim,
+               int block_size, int num_blocks, float scale, void* out, pa_dtype dtype,
+               cudaStream_t stream) {
+  if (num_seqs < 0 || max_query_len < 0 || num_blocks < 1 || max_blocks_per_seq < 1 ||
+      !shape_ok(num_kv_heads, head_dim, block_size) || num_q_heads < num_kv_heads ||
+      num_q_heads % num_kv_heads != 0 || num_q_heads / num_kv_heads > 64 ||
+      !std::isfinite(scale) || (dtype != PA_FP16 && dtype != PA_BF16) ||
+      static_cast<long long>(max_blocks_per_seq) * block_size > 0x7fffffffLL ||
+      static_cast<long long>(num_blocks) * num_kv_heads * block_size > 0x7fffffffLL)
+    return PA_ERR_ARG;
+  if (num_seqs == 0 || max_query_len == 0) return PA_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start || !out)
+    return PA_ERR_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return PA_ERR_ARG;
+  DeviceInfo di;
+  if (!device_info(&di)) return PA_ERR_CUDA;
+  pa::PrefillArgs a;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.query_start = query_start;
+  a.out = out;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.block_size = block_size;
+  a.num_blocks = num_blocks;
+  a.max_query_len = max_query_len;
+  a.scale = scale;
+  a.bf16 = dtype == PA_BF16;
+  a.err = di.err;
+  return pa::prefill_launch(a, stream);
+}
+
 int pa_decode_append(const void* q, const void* key_new, const void* value_new, void* k_cache,
                      void* v_cache, const int32_t* block_tables, int max_blocks_per_seq,
                      const int32_t* context_lens, int num_seqs, int num_q_heads,

@@ -31,6 +31,24 @@ int decode_heads_per_pair(int num_q_heads, int num_kv_heads);
 // Launch the decode kernel; 0 or a negative PA_ERR_* code.
 int decode_launch(const DecodeArgs& a, int grid, cudaStream_t stream);
 
+struct PrefillArgs {
+  const void* q;  // [num_q_rows, Hq, d]
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  const int32_t* query_start;  // [num_seqs + 1]
+  void* out;
+  int num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size,
+      num_blocks, max_query_len;
+  float scale;
+  bool bf16;
+  unsigned* err;
+};
+
+// Launch the paged prefill kernel; 0 or a negative PA_ERR_* code.
+int prefill_launch(const PrefillArgs& a, cudaStream_t stream);
+
 int reshape_and_cache_launch(const void* key, const void* value, void* k_cache, void* v_cache,
                              const int64_t* slot_mapping, int num_tokens, int num_blocks,
                              int num_kv_heads, int head_dim, int block_size, unsigned* err,

@@ -1,0 +1,110 @@
+"""GPU parity of paged prefill against the oracle: prompts from scratch and chunks, ragged
+lengths, every GQA group shape the kernel packs (G = 1..64, with and without a remainder
+of rows), both head sizes, all block sizes, both dtypes; physical-block permutations
+(bit-identical); invalid items; the benchmark batches on sampled sequences."""
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_149_gb300 as pa
+import workloads
+from gpu_harness import TOL, GpuBatch, device_error, max_err, oracle_place, to_bits
+from oracle import prefill as oracle_prefill
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(libpa):
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    device_error()
+
+
+def run_gpu(wl, free_order=None, ctx=None, tables=None):
+    gb = GpuBatch(wl, free_order=free_order)
+    qs = torch.from_numpy(wl.query_start.astype(np.int32)).cuda()
+    qlen = np.diff(wl.query_start)
+    out = pa.prefill(gb.q, gb.k_cache, gb.v_cache, gb.tables if tables is None else tables,
+                     gb.ctx if ctx is None else ctx, qs, wl.scale, int(qlen.max()))
+    torch.cuda.synchronize()
+    return gb, to_bits(out)
+
+
+def check(wl, seqs=None):
+    gb, got = run_gpu(wl)
+    assert device_error() == 0
+    kc, vc, tables = oracle_place(wl)
+    ref, err = oracle_prefill.paged_prefill_bits(wl.q, kc, vc, tables, wl.context_lens,
+                                                 wl.query_start, wl.scale, wl.block_size,
+                                                 wl.dtype, seqs=seqs)
+    assert not err.any()
+    rows = (np.concatenate([np.arange(wl.query_start[s], wl.query_start[s + 1]) for s in seqs])
+            if seqs is not None else slice(None))
+    e = max_err(got[rows], ref[rows], wl.dtype)
+    assert e <= TOL[wl.dtype], f"max abs error {e}"
+    return got
+
+
+def test_tiny():
+    check(workloads.prefill_tiny())
+
+
+CASES = []
+for dtype in ("fp16", "bf16"):
+    for d in (64, 128):
+        for bs in (8, 16, 32):
+            for hq, hkv in ((4, 4), (8, 2), (12, 4), (32, 8), (64, 1), (6, 2)):
+                CASES.append((dtype, d, bs, hq, hkv))
+
+
+@pytest.mark.parametrize("dtype,d,bs,hq,hkv", CASES)
+def test_shapes_ragged(dtype, d, bs, hq, hkv):
+    ctx = [1, 15, 16, 17, 64, 65, 130, 200]
+    qlen = [1, 15, 16, 5, 64, 20, 130, 77]
+    T = max(ctx) // bs + 2
+    nb = sum(-(-c // bs) for c in ctx) + 7
+    seed = CASES.index((dtype, d, bs, hq, hkv))
+    rng = np.random.default_rng(seed)
+    wl = workloads._prefill("ragged", rng, ctx, qlen, dtype, hq, hkv, d, bs, nb, T * bs,
+                            1.0 / np.sqrt(d))
+    check(wl)
+
+
+def test_physical_block_permutation_is_bit_identical():
+    rng = np.random.default_rng(60)
+    wl = workloads._prefill("perm", rng, [300, 77, 513], [300, 40, 129], "bf16", 32, 8, 128,
+                            16, 80, 528, 1.0 / np.sqrt(128))
+    outs = []
+    for seed in (0, 1, 2):
+        order = np.random.default_rng(200 + seed).permutation(wl.num_blocks).astype(np.int32)
+        outs.append(run_gpu(wl, free_order=order)[1])
+    np.testing.assert_array_equal(outs[0], outs[1])
+    np.testing.assert_array_equal(outs[0], outs[2])
+
+
+def test_invalid_items_give_zeros_and_flags():
+    wl = workloads.prefill_tiny()
+    gb = GpuBatch(wl)
+    ctx = gb.ctx.clone()
+    ctx[0] = 3                                  # q_len 5 > ctx 3
+    tables = gb.tables.clone()
+    tables[1, 0] = wl.num_blocks                # a bad block id in sequence 1
+    qs = torch.from_numpy(wl.query_start.astype(np.int32)).cuda()
+    out = pa.prefill(gb.q, gb.k_cache, gb.v_cache, tables, ctx, qs, wl.scale, 33)
+    flags = device_error()
+    assert flags & 0x2 and flags & 0x1
+    got = to_bits(out)
+    assert not got[:wl.query_start[2]].any()
+    kc, vc, t_or = oracle_place(wl)
+    ref, _ = oracle_prefill.paged_prefill_bits(wl.q, kc, vc, t_or, wl.context_lens,
+                                               wl.query_start, wl.scale, wl.block_size,
+                                               wl.dtype, seqs=[2, 3])
+    assert max_err(got[wl.query_start[2]:], ref[wl.query_start[2]:], wl.dtype) <= TOL[wl.dtype]
+
+
+def test_chunked_batch_sampled():
+    check(workloads.prefill_chunked(), seqs=[0, 7, 15])
+
+
+def test_prompts_from_scratch_sampled():
+    check(workloads.prefill_llama31_8b(num_seqs=4, prompt=2048), seqs=[1])
