@@ -29,6 +29,8 @@ import subprocess
 import sys
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
@@ -391,6 +393,213 @@ print(json.dumps({{"cores": cores, "workers": len(shards), "seconds": wall, "byt
     return json.loads(r.stdout.strip().splitlines()[-1])
 
 
+def prefill_flops(wl):
+    """Algorithmic FLOPs of one prefill pass: every query row at position p scores p + 1
+    keys (2 d FLOPs each) and sums as many V rows (2 d FLOPs each), for every query head."""
+    qlen = np.diff(wl.query_start)
+    total = 0
+    for s in range(wl.num_seqs):
+        c, n = int(wl.context_lens[s]), int(qlen[s])
+        # positions c - n .. c - 1 attend to p + 1 keys each
+        total += n * (2 * c - n + 1) // 2
+    return 4 * wl.head_dim * wl.num_q_heads * total
+
+
+def run_gpu_prefill(args, rank, world, local_rank):
+    """K prefill passes over ROTATE batches in disjoint blocks (each batch's q alone is
+    larger than L2), CUDA events around the loop; then end to end with host buffers."""
+    import torch
+
+    import paged_kv_cache_149_gb300 as pa
+    import workloads
+    from paged_kv_cache_149_gb300 import build as _build
+
+    _build.build()
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    wl = workloads.RECIPES[args.workload]()
+    dt = {"fp16": torch.float16, "bf16": torch.bfloat16}[wl.dtype]
+
+    def up(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(dt)
+
+    shape = (wl.num_blocks, wl.num_kv_heads, wl.block_size, wl.head_dim)
+    k_cache = torch.zeros(shape, dtype=dt, device=device)
+    v_cache = torch.zeros(shape, dtype=dt, device=device)
+    pool = pa.BlockPool(wl.num_blocks, wl.block_size, wl.free_order)
+    n, T = wl.num_seqs, wl.max_blocks_per_seq
+    keys, values, q = up(wl.keys), up(wl.values), up(wl.q)
+    qs = torch.from_numpy(wl.query_start.astype(np.int32)).to(device)
+    maxq = int(np.diff(wl.query_start).max())
+    batches = []
+    for r in range(ROTATE):
+        tables = np.full((n, T), 0, dtype=np.int32)
+        slots = []
+        for s in range(n):
+            c = int(wl.context_lens[s])
+            pool.allocate(r * n + s, c)
+            t = pool.block_table(r * n + s)
+            tables[s, :len(t)] = t
+            slots.append(pool.slots(r * n + s, 0, c))
+        pa.reshape_and_cache(keys, values, k_cache, v_cache,
+                             torch.from_numpy(np.concatenate(slots)).to(device))
+        batches.append({"q": q if r == 0 else q.clone(), "tables": torch.from_numpy(tables).to(device),
+                        "ctx": torch.from_numpy(np.ascontiguousarray(wl.context_lens, np.int32)).to(device),
+                        "out": torch.empty_like(q)})
+    stream = torch.cuda.Stream(device)
+    torch.cuda.synchronize(device)
+    pa.get_device_error()
+
+    def step(i):
+        b = batches[i % ROTATE]
+        pa.prefill(b["q"], k_cache, v_cache, b["tables"], b["ctx"], qs, wl.scale, maxq,
+                   out=b["out"], stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(device)
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    K = args.steps
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(device)
+    t0 = time.time()
+    ev[0].record(stream)
+    for i in range(K):
+        step(i)
+    ev[1].record(stream)
+    torch.cuda.synchronize(device)
+    t1 = time.time()
+    clocks = sampler.stop(t0, t1) if sampler else None
+    flags = pa.get_device_error(stream=stream)
+    total_ms = ev[0].elapsed_time(ev[1])
+    # end to end: q from pinned host memory, out read back, every pass
+    host_q = batches[0]["q"].cpu().pin_memory()
+    host_out = torch.empty_like(host_q).pin_memory()
+    dev_q = torch.empty_like(batches[0]["q"])
+    b0 = batches[0]
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            dev_q.copy_(host_q, non_blocking=True)
+            pa.prefill(dev_q, k_cache, v_cache, b0["tables"], b0["ctx"], qs, wl.scale, maxq,
+                       out=b0["out"], stream=stream)
+            host_out.copy_(b0["out"], non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(device)
+    ke = max(1, min(K, 20))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(ke):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    nbytes = host_q.numel() * host_q.element_size()
+    return {"wl": wl, "total_ms": total_ms, "decode_ms": total_ms / K,
+            "two_calls_ms": total_ms / K, "e2e_ms": e0.elapsed_time(e1) / ke,
+            "h2d": nbytes, "d2h": nbytes, "clocks": clocks, "flags": flags}
+
+
+def oracle_prefill_sample(name, budget_s):
+    """The prefill oracle on a bounded sample: the first k tokens of the first sequence
+    (a prompt from scratch of k tokens: the same rows and keys), k doubled while the
+    single-threaded run stays within budget_s."""
+    code = f"""
+import json, sys, time
+sys.path.insert(0, {ROOT!r})
+import numpy as np
+import workloads
+from oracle import cache_ops, formats, prefill
+from oracle.block_pool import BlockPool
+wl = workloads.RECIPES[{name!r}]()
+c0 = int(wl.context_lens[0]); q0 = int(wl.query_start[1] - wl.query_start[0])
+best = None
+k = 64
+while True:
+    k = min(k, q0)
+    shape = (k // wl.block_size + 2, wl.num_kv_heads, wl.block_size, wl.head_dim)
+    kc = np.zeros(shape, np.uint16); vc = np.zeros(shape, np.uint16)
+    pool = BlockPool(shape[0], wl.block_size, np.arange(shape[0], dtype=np.int32))
+    pool.allocate(0, k)
+    tab = np.array([pool.block_table(0) + [0] * 2], dtype=np.int32)
+    a = int(wl.seq_start[0]) + (c0 - q0)
+    kc, vc = cache_ops.reshape_and_cache(kc, vc, wl.keys[a:a + k], wl.values[a:a + k],
+                                         np.array([pool.slot(0, i) for i in range(k)], np.int64))
+    q = wl.q[int(wl.query_start[0]):int(wl.query_start[0]) + k]
+    t = time.process_time()
+    prefill.paged_prefill(q, kc, vc, tab, np.array([k], np.int32), np.array([0, k]), wl.scale,
+                          wl.block_size, wl.dtype)
+    dt = time.process_time() - t
+    best = (k, dt)
+    if k >= q0 or dt * 4 > {budget_s}:
+        break
+    k *= 2
+k, dt = best
+flops = 4 * wl.head_dim * wl.num_q_heads * k * (k + 1) // 2
+print(json.dumps({{"tokens": k, "seconds": dt, "flops": flops}}))
+"""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
+    if r.returncode != 0:
+        raise RuntimeError("prefill oracle baseline failed:\n" + r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def prefill_line(args, res, world):
+    wl = res["wl"]
+    flops = prefill_flops(wl)
+    step_s = res["total_ms"] / 1e3 / args.steps
+    value = world * flops / step_s / 1e12
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak, kind = float(json.load(f)["bf16_tflops"]), "measured (cuBLAS bf16, burst)"
+    except (OSError, KeyError, ValueError):
+        peak, kind = 1900.0, "fallback"
+    cpu = oracle_prefill_sample(args.workload, args.cpu_baseline_seconds) \
+        if args.cpu_baseline_seconds > 0 else None
+    qlen = np.diff(wl.query_start)
+    return {
+        "metric": "paged prefill attention TFLOP/s (causal, over the block table)",
+        "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(res["total_ms"] / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "data": "synthetic (seeded normals; no dataset or weights)",
+        "config": {
+            "workload": (f"{wl.name}: {wl.num_seqs} seqs, ctx {int(wl.context_lens.min())}.."
+                         f"{int(wl.context_lens.max())}, new tokens {int(qlen.min())}.."
+                         f"{int(qlen.max())} (sum {int(qlen.sum())}), {wl.num_q_heads} q / "
+                         f"{wl.num_kv_heads} kv heads, head_dim {wl.head_dim}, block_size "
+                         f"{wl.block_size}"),
+            "l2": f"{ROTATE} batches in disjoint blocks rotated every pass; each batch's q "
+                  "alone exceeds L2",
+            "parallelism": f"replicas x{world}",
+        },
+        "roofline": {"bound": "tensor", "kernel": "prefill_kernel (pa_prefill)",
+                     "achieved": round(value / world, 2), "peak": peak, "peak_kind": kind,
+                     "unit": "TFLOP/s", "frac": round(value / world / peak, 4), "traffic": None,
+                     "algorithmic_flops": flops},
+        "cpu_baseline": None if cpu is None else {
+            "value": round(cpu["flops"] / cpu["seconds"] / 1e12, 6), "unit": "TFLOP/s",
+            "cores": 1, "kind": "oracle",
+            "sample": f"float64 NumPy prefill oracle, single thread, the first {cpu['tokens']} "
+                      f"tokens of sequence 0 (a {cpu['tokens']}-token prompt)"},
+        "e2e": {"value": round(world * flops / (res["e2e_ms"] / 1e3) / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
+                "us_per_step": round(1e3 * res["e2e_ms"], 2)},
+        "clocks": res["clocks"],
+        "gpu_launches": args.steps,
+        "device_error_flags": res["flags"],
+    }
+
+
 def max_over_ranks(values):
     """Element-wise maximum of per-rank floats over the process group (NCCL on GPUs, or any
     other backend on CPU tensors)."""
@@ -433,10 +642,17 @@ def main(argv=None, runner=None, backend="nccl"):
     if world > 1:
         import torch
         torch.distributed.init_process_group(backend)
-    res = (runner or run_gpu)(args, rank, world, local_rank)
+    is_prefill = args.workload.startswith("prefill")
+    res = (runner or (run_gpu_prefill if is_prefill else run_gpu))(args, rank, world, local_rank)
     if world > 1:
         res.update(zip(RANK_TIMES, max_over_ranks([res[k] for k in RANK_TIMES])))
     if rank != 0:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+        return
+    if is_prefill:
+        print(json.dumps(prefill_line(args, res, world)))
         if world > 1:
             import torch
             torch.distributed.destroy_process_group()
