@@ -1,5 +1,5 @@
 // Paged prefill attention for sm_103a: causal multi-query attention of each sequence's
-// newest tokens over its paged context.
+// newest tokens over its paged context, on the 5th-generation tensor cores (tcgen05).
 //
 // Sequence s owns query rows query_start[s] .. query_start[s+1]-1, its newest q_len tokens
 // at positions p = ctx - q_len .. ctx - 1 (their K/V rows are already in the cache); the
@@ -8,18 +8,22 @@
 // has to read the block table; chenyuan1125 "vllm-pagedattention", section 它和
 // FlashAttention…: prefill works on large blocks of queries).
 //
-// Design (one CTA per (query block, sequence, kv head); 4 warps):
-// * The CTA's 64 query rows are (token, query head of the kv head) pairs: TQ = 64 / G
-//   tokens x G heads, so every K/V tile is read once for all G heads of a kv head (GQA).
-//   Each warp owns 16 rows; its Q rows stay in registers as MMA A fragments.
-// * Key tiles of 64 tokens (four 16-row groups, each one block row range found through the
-//   table) are copied by all 128 threads with 16-byte cp.async into a double-buffered,
-//   swizzled shared-memory ring (rows past the context are zero-filled, never read).
-// * Per tile, warp-level tensor-core MMAs (m16n8k16, fp32 accumulate): S = Q K^T, online
-//   softmax per row in exp2 (the causal mask only on tiles that reach past a row's
-//   position), P rounded to the input type straight from the S accumulators into A
-//   fragments, O += P V with V through ldmatrix.trans.  Tiles entirely in the future of
-//   every row of the CTA are never loaded.
+// Design (one CTA per (query block, sequence, kv head); 4 warps, one thread per query row):
+// * The CTA's 128 query rows are (token, query head of the kv head) pairs: 128 / G tokens x
+//   G heads, so every K/V tile is read once for all G heads of a kv head (GQA).  Q sits in
+//   shared memory, K-major with the 128-byte swizzle (the layout tcgen05 descriptors read).
+// * Key tiles of 64 tokens are gathered through the table by 16-byte cp.async into a
+//   double-buffered ring, in the same swizzled layout: K is the K-major B operand of
+//   S = Q K^T, V (keys x d, d contiguous) the MN-major B operand of P V.  Rows past the
+//   context are zero-filled, never read.
+// * Per tile: one thread issues S = Q K^T (tcgen05.mma kind::f16, M 128, N 64, fp32 in
+//   tensor memory) and commits it to an mbarrier; every thread reads its own row of S with
+//   tcgen05.ld (row = TMEM lane: no shuffles), applies the causal mask and the online
+//   softmax in exp2, and writes its row of P (rounded to the input type) into the K
+//   buffer just consumed; then one thread issues P V (M 128, N d) into a second TMEM
+//   region, and every thread folds its row of P V into its fp32 O held in registers.
+// * Every mbarrier wait is bounded (about 1 s, PA_DEVERR_TIMEOUT); tiles entirely in the
+//   future of every row of the CTA are never loaded.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -30,10 +34,9 @@
 namespace pa {
 namespace prefill {
 
-constexpr int kWarps = 4;
-constexpr int kThreads = kWarps * 32;
-constexpr int kRows = 64;   // query rows of a CTA
-constexpr int kKeys = 64;   // keys of a tile
+constexpr int kThreads = 128;  // one per query row
+constexpr int kRows = 128;     // query rows of a CTA (MMA M)
+constexpr int kKeys = 64;      // keys of a tile (MMA N of S, K of P V)
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Params {
@@ -44,24 +47,83 @@ struct Params {
   const int32_t* context_lens;
   const int32_t* query_start;  // [n + 1]
   uint8_t* out;
-  int num_seqs, num_q_heads, num_kv_heads, group, tq;  // tq = tokens per CTA = 64 / G
+  int num_seqs, num_q_heads, num_kv_heads, group, tq;  // tq = tokens per CTA = 128 / G
   int max_blocks_per_seq, block_size, log2_block, num_blocks;
   float scale_log2;
   unsigned* err;
 };
 
+// P of a tile ([128 rows][64 keys], 16 KB) takes the place of the tile's K when K is at
+// least as large (d >= 128), else a buffer of its own.
+template <int D>
+constexpr bool kAliasP = kKeys * D >= kRows * kKeys;
+
 template <int D>
 struct Smem {
-  uint8_t kv[2][2][kKeys * D * 2];  // [buffer][K, V][tile], 1024-byte aligned
-  int bad;                          // a block id of this CTA's tiles is out of range
+  uint8_t q[kRows * D * 2];            // K-major, 128-byte swizzle; 1024-byte aligned
+  uint8_t kv[2][2][kKeys * D * 2];     // [buffer][K, V]
+  uint8_t p[kAliasP<D> ? 1024 : kRows * kKeys * 2];
+  unsigned long long bar_s, bar_o;     // S and P V done (one phase per tile)
+  uint32_t tmem;                       // tensor-memory base address
+  int bad;                             // a block id of this CTA's tiles is out of range
 };
 
-// Byte offset of (row, 16-byte chunk) in a [kKeys][D] tile: chunk c of a row lives in
-// column half c / 8 (128 bytes of each row per half), and the 128-byte swizzle permutes the
-// chunks of a row so that ldmatrix reads are conflict-free.
-__device__ __forceinline__ uint32_t swz(int row, int chunk) {
-  return static_cast<uint32_t>((chunk >> 3) * (kKeys * 128) + row * 128 +
-                               (((chunk & 7) ^ (row & 7)) << 4));
+// Byte offset of (row, 16-byte chunk) in a [rows][D] 16-bit tile stored K-major with the
+// 128-byte swizzle: chunk c lives in the 64-element column block c / 8 (blocks rows * 128
+// bytes apart), row r at r * 128 inside it, the chunk index XORed with r % 8.
+__device__ __forceinline__ uint32_t swz(int rows, int r, int c) {
+  return static_cast<uint32_t>((c >> 3) * rows * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+// tcgen05 shared-memory matrix descriptor with the 128-byte swizzle (version 1 = sm_100
+// family): lbo / sbo in bytes.  K-major operands: sbo = 1024 (8-row groups), lbo unused.
+// MN-major operands: lbo = distance between 64-element MN blocks, sbo = 1024 (8-row K
+// groups).
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((addr >> 4) & 0x3FFF) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFF) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// tcgen05 instruction descriptor, kind::f16: fp32 accumulate, A and B of the same 16-bit
+// type (bf16 or fp16), A K-major, B K-major or MN-major, M, N.
+template <typename T>
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn_major) {
+  return (1u << 4) | ((std::is_same<T, __nv_bfloat16>::value ? 1u : 0u) << 7) |
+         ((std::is_same<T, __nv_bfloat16>::value ? 1u : 0u) << 10) |
+         ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t idesc,
+                                        bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(da), "l"(db), "r"(idesc), "r"(static_cast<uint32_t>(accumulate))
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
@@ -77,45 +139,24 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-
-template <typename T>
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1);
-template <>
-__device__ __forceinline__ void mma16816<__nv_bfloat16>(float (&d)[4], const uint32_t (&a)[4],
-                                                        uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-      "{%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-template <>
-__device__ __forceinline__ void mma16816<__half>(float (&d)[4], const uint32_t (&a)[4],
-                                                 uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-      "{%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+// Wait for the phase of `bar` with parity `par`, bounded by kWaitLimitNs.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t par) {
+  if (mbar_try_wait(bar, par)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, par)) return true;
+    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
 }
 
 template <int D, typename T>
 __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant__ Params p) {
-  constexpr int KS = D / 16;      // k-steps of Q K^T
-  constexpr int NK = kKeys / 8;   // n-tiles of S (8 keys each)
-  constexpr int ND = D / 8;       // n-tiles of O (8 d each)
-  constexpr int CH = D / 8;       // 16-byte chunks per row
+  constexpr int CH = D / 8;            // 16-byte chunks per row
+  constexpr int KS1 = D / 16;          // MMA k-steps of S = Q K^T
+  constexpr int KS2 = kKeys / 16;      // MMA k-steps of P V
+  constexpr uint32_t kColS = 0;        // TMEM columns: S [0, 64), P V [64, 64 + D)
+  constexpr uint32_t kColO = kKeys;
+  constexpr uint32_t kTmemCols = kKeys + D <= 128 ? 128 : 256;  // power of two >= 64 + D
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
   Smem<D>& sm = *reinterpret_cast<Smem<D>*>(smem_raw + (((raw_addr + 1023) & ~1023u) - raw_addr));
@@ -123,66 +164,57 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant
   pdl_wait_primary();
   pdl_launch_dependents();
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int s = blockIdx.y, g = blockIdx.z;
   const int tb = gridDim.x - 1 - blockIdx.x;  // later token blocks (more keys) first
   const int qs = __ldg(p.query_start + s), qlen = __ldg(p.query_start + s + 1) - qs;
   const int tok0 = tb * p.tq;
   if (tok0 >= qlen) return;  // (uniform over the CTA)
   const int ctx = __ldg(p.context_lens + s);
-  const int ntok = min(p.tq, qlen - tok0);  // tokens of this CTA
+  const int ntok = min(p.tq, qlen - tok0);
   const int G = p.group;
   T* outp = reinterpret_cast<T*>(p.out);
-  const bool bad_ctx = ctx < 1 || ctx > p.max_blocks_per_seq * p.block_size || qlen > ctx;
-  if (bad_ctx) {  // zeros for this CTA's rows, and a flag
-    for (int i = tid; i < ntok * G * D / 8; i += kThreads) {
-      const int r = i / (D / 8), c = i % (D / 8);
-      const int t = r / G, hh = r % G;
-      reinterpret_cast<uint4*>(outp + ((static_cast<size_t>(qs + tok0 + t) * p.num_q_heads +
-                                        g * G + hh) * D))[c] = make_uint4(0, 0, 0, 0);
+  if (ctx < 1 || ctx > p.max_blocks_per_seq * p.block_size || qlen > ctx) {
+    for (int i = tid; i < ntok * G * CH; i += kThreads) {
+      const int r = i / CH, c = i % CH;
+      reinterpret_cast<uint4*>(outp + ((static_cast<size_t>(qs + tok0 + r / G) * p.num_q_heads +
+                                        g * G + r % G) * D))[c] = make_uint4(0, 0, 0, 0);
     }
     if (tid == 0) atomicOr(p.err, kErrBadContext);
     return;
   }
-  if (tid == 0) sm.bad = 0;
-  __syncthreads();  // (before any copy can set it)
 
-  // ---- this warp's 16 rows: r = 16*warp + {r0, r0+8}; row = (token r / G, head r % G) ----
-  const int r0 = lane >> 2, qc = 2 * (lane & 3);
-  const int rows_used = ntok * G;
-  int pos[2];             // position of each of this lane's two rows (-1: an unused row)
-  long long qrow_off[2];  // element offset of the row's q / out vector (-1: unused)
-  for (int i = 0; i < 2; ++i) {
-    const int r = 16 * warp + r0 + 8 * i;
-    if (r < rows_used) {
-      const int t = r / G, hh = r % G;
-      pos[i] = ctx - qlen + tok0 + t;
-      qrow_off[i] = (static_cast<long long>(qs + tok0 + t) * p.num_q_heads + g * G + hh) * D;
-    } else {
-      pos[i] = -1;
-      qrow_off[i] = -1;
-    }
-  }
-  // Q as A fragments: a0 (row r0, k 2lq..), a1 (row r0+8), a2 (row r0, k +8), a3 (row r0+8)
-  uint32_t qa[KS][4];
-  {
-    const uint32_t* q32 = reinterpret_cast<const uint32_t*>(p.q);
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      const int col = 16 * ks + qc;
-      qa[ks][0] = qrow_off[0] >= 0 ? __ldg(q32 + (qrow_off[0] + col) / 2) : 0u;
-      qa[ks][1] = qrow_off[1] >= 0 ? __ldg(q32 + (qrow_off[1] + col) / 2) : 0u;
-      qa[ks][2] = qrow_off[0] >= 0 ? __ldg(q32 + (qrow_off[0] + col + 8) / 2) : 0u;
-      qa[ks][3] = qrow_off[1] >= 0 ? __ldg(q32 + (qrow_off[1] + col + 8) / 2) : 0u;
-    }
-  }
-
-  // key tiles this CTA needs: 0 .. (highest position of its rows) / 64
-  const int pos_hi = ctx - qlen + tok0 + ntok - 1;
-  const int pos_lo = ctx - qlen + tok0;
+  // ---- this thread's row: (token tid / G, head tid % G) ----
+  const bool row_ok = tid < ntok * G;
+  const int pos = row_ok ? ctx - qlen + tok0 + tid / G : -1;
+  const long long row_off =
+      row_ok ? (static_cast<long long>(qs + tok0 + tid / G) * p.num_q_heads + g * G + tid % G) * D
+             : -1;
+  const int pos_lo = ctx - qlen + tok0, pos_hi = ctx - qlen + tok0 + ntok - 1;
   const int ntiles = pos_hi / kKeys + 1;
 
-  // ---- copy of key tile kt into buffer b (all threads) ----
+  // ---- set-up: barriers, tensor memory, Q into shared memory ----
+  if (tid == 0) {
+    mbar_init(smem_addr(&sm.bar_s), 1);
+    mbar_init(smem_addr(&sm.bar_o), 1);
+    fence_mbar_init();
+    sm.bad = 0;
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(&sm.tmem)), "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(p.q + (row_ok ? row_off : 0) * 2);
+#pragma unroll 4
+    for (int c = 0; c < CH; ++c) {
+      const uint4 v = row_ok ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(sm.q + swz(kRows, tid, c)) = v;
+    }
+  }
+
   const int32_t* trow = p.block_tables + static_cast<size_t>(s) * p.max_blocks_per_seq;
   auto issue_tile = [&](int kt, int b) {
     const uint32_t kbase = smem_addr(sm.kv[b][0]);
@@ -201,22 +233,29 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant
       }
       const size_t src = ((static_cast<size_t>(blk) * p.num_kv_heads + g) * p.block_size +
                           (live ? (t & (p.block_size - 1)) : 0)) * D + c * 8;
-      const uint32_t so = swz(row, c);
-      const bool ok = live && blk >= 0;
-      cp_async16(kbase + so, p.k_cache + src * 2, ok ? 16u : 0u);
-      cp_async16(vbase + so, p.v_cache + src * 2, ok ? 16u : 0u);
+      const uint32_t so = swz(kKeys, row, c);
+      cp_async16(kbase + so, p.k_cache + src * 2, live ? 16u : 0u);
+      cp_async16(vbase + so, p.v_cache + src * 2, live ? 16u : 0u);
     }
     cp_async_commit();
   };
-
-  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-  float o[ND][4];
-#pragma unroll
-  for (int nd = 0; nd < ND; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
-  const int lrow = lane & 7, lmat = lane >> 3;
-
+  __syncthreads();  // (sm.bad cleared before any copy sets it)
   issue_tile(0, 0);
-  for (int kt = 0; kt < ntiles; ++kt) {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = sm.tmem;
+  const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;  // this warp's TMEM lanes
+
+  float o[D];
+#pragma unroll
+  for (int i = 0; i < D; ++i) o[i] = 0.f;
+  float m_run = -INFINITY, l_run = 0.f;
+  bool ok = true;
+  constexpr uint32_t id_s = idesc_f16<T>(kRows, kKeys, false);
+  constexpr uint32_t id_o = idesc_f16<T>(kRows, D, true);
+
+  for (int kt = 0; kt < ntiles && ok; ++kt) {
     const int b = kt & 1;
     if (kt + 1 < ntiles) {
       issue_tile(kt + 1, b ^ 1);
@@ -224,109 +263,139 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant
     } else {
       cp_async_wait<0>();
     }
-    __syncthreads();  // tile kt has landed for every thread
-    const uint32_t kb = smem_addr(sm.kv[b][0]);
-    const uint32_t vb = smem_addr(sm.kv[b][1]);
+    // the tile's copies (generic proxy) before the tensor cores read it (async proxy)
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t qa = smem_addr(sm.q), kb = smem_addr(sm.kv[b][0]), vb = smem_addr(sm.kv[b][1]);
 
-    // ---- S = Q K^T: 16 rows x 64 keys ----
-    float sc[NK][4];
+    // ---- S = Q K^T ----
+    if (tid == 0) {
 #pragma unroll
-    for (int nk = 0; nk < NK; ++nk) sc[nk][0] = sc[nk][1] = sc[nk][2] = sc[nk][3] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-#pragma unroll
-      for (int np = 0; np < NK / 2; ++np) {
-        // B fragments of two n-tiles (keys 16np..16np+15), k = d chunks 2ks, 2ks+1
-        uint32_t bf[4];
-        ldsm_x4(kb + swz(16 * np + lrow + ((lmat >> 1) << 3), 2 * ks + (lmat & 1)), bf);
-        mma16816<T>(sc[2 * np], qa[ks], bf[0], bf[1]);
-        mma16816<T>(sc[2 * np + 1], qa[ks], bf[2], bf[3]);
+      for (int ks = 0; ks < KS1; ++ks) {
+        const uint32_t koff = (ks & 3) * 32;  // 16 columns = 32 bytes within a 64-column block
+        mma_f16(tmem + kColS,
+                desc_sw128(qa + (ks >> 2) * kRows * 128 + koff, 16, 1024),
+                desc_sw128(kb + (ks >> 2) * kKeys * 128 + koff, 16, 1024), id_s, ks > 0);
       }
+      mma_commit(smem_addr(&sm.bar_s));
     }
-    // ---- causal mask, online softmax (rows r0: c0,c1; r0+8: c2,c3) ----
+    ok = wait_bounded(smem_addr(&sm.bar_s), kt & 1);
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (!__syncthreads_and(ok)) {
+      ok = false;
+      break;
+    }
+
+    // ---- this row of S: mask, online softmax, P into the K buffer ----
+    float sv[kKeys];
+    {
+      float tmp[32];
+      tmem_ld32(tmem + lane_base + kColS, tmp);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) sv[i] = tmp[i];
+      tmem_ld32(tmem + lane_base + kColS + 32, tmp);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) sv[32 + i] = tmp[i];
+    }
     const bool needs_mask = kt * kKeys + kKeys - 1 > pos_lo;
-    float mx[2] = {-INFINITY, -INFINITY};
+    float mx = -INFINITY;
 #pragma unroll
-    for (int nk = 0; nk < NK; ++nk) {
+    for (int i = 0; i < kKeys; ++i) {
+      float v = sv[i] * p.scale_log2;
+      if (needs_mask && kt * kKeys + i > pos) v = -INFINITY;
+      sv[i] = v;
+      mx = fmaxf(mx, v);
+    }
+    const float m_new = fmaxf(m_run, mx);
+    // (a row whose keys are all masked so far keeps m = -inf; its weights stay 0)
+    const float alpha = m_new == -INFINITY ? 1.f : exp2f(m_run - m_new);
+    m_run = m_new;
+    float rs = 0.f;
+    uint8_t* prow = kAliasP<D> ? sm.kv[b][0] : sm.p;  // P [128][64], K-major: one column block
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = e >> 1;
-        const int key = kt * kKeys + 8 * nk + qc + (e & 1);
-        float v = sc[nk][e] * p.scale_log2;
-        if (needs_mask && key > pos[i]) v = -INFINITY;
-        sc[nk][e] = v;
-        mx[i] = fmaxf(mx[i], v);
+    for (int c = 0; c < kKeys / 8; ++c) {
+      float e[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        e[j] = m_new == -INFINITY ? 0.f : exp2f(sv[8 * c + j] - m_new);
+        rs += e[j];
       }
+      uint4 w;
+      w.x = pack2<T>(e[0], e[1]);
+      w.y = pack2<T>(e[2], e[3]);
+      w.z = pack2<T>(e[4], e[5]);
+      w.w = pack2<T>(e[6], e[7]);
+      *reinterpret_cast<uint4*>(prow + swz(kRows, tid, c)) = w;
     }
-    float alpha[2];
+    l_run = l_run * alpha + rs;
+    if (alpha != 1.f) {
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 1));
-      mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 2));
-      const float m_new = fmaxf(m_run[i], mx[i]);
-      // (a row with every key masked so far keeps m = -inf; its weights stay 0)
-      alpha[i] = m_new == -INFINITY ? 1.f : exp2f(m_run[i] - m_new);
-      m_run[i] = m_new;
+      for (int i = 0; i < D; ++i) o[i] *= alpha;
     }
-    float rs[2] = {0.f, 0.f};
-    uint32_t pa[NK / 2][4];  // P as A fragments: k-step kk covers keys 16kk..16kk+15
+    // P (generic writes) before the tensor cores read it; every S read is done
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+
+    // ---- P V into its own TMEM columns, then O += P V ----
+    if (tid == 0) {
+      const uint32_t pa = smem_addr(kAliasP<D> ? sm.kv[b][0] : sm.p);
 #pragma unroll
-    for (int nk = 0; nk < NK; ++nk) {
-      float pr[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = e >> 1;
-        pr[e] = m_run[i] == -INFINITY ? 0.f : exp2f(sc[nk][e] - m_run[i]);
-        rs[i] += pr[e];
-      }
-      // C layout of n-tile nk (keys 8nk + qc, +1) is A layout of k-step nk/2, half nk%2
-      pa[nk >> 1][(nk & 1) * 2 + 0] = pack2<T>(pr[0], pr[1]);  // row r0
-      pa[nk >> 1][(nk & 1) * 2 + 1] = pack2<T>(pr[2], pr[3]);  // row r0 + 8
+      for (int ks = 0; ks < KS2; ++ks)
+        mma_f16(tmem + kColO, desc_sw128(pa + ks * 32, 16, 1024),
+                desc_sw128(vb + ks * 16 * 128, kKeys * 128, 1024), id_o, ks > 0);
+      mma_commit(smem_addr(&sm.bar_o));
     }
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      rs[i] += __shfl_xor_sync(0xffffffffu, rs[i], 1);
-      rs[i] += __shfl_xor_sync(0xffffffffu, rs[i], 2);
-      l_run[i] = l_run[i] * alpha[i] + rs[i];
+    ok = wait_bounded(smem_addr(&sm.bar_o), kt & 1);
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (!__syncthreads_and(ok)) {
+      ok = false;
+      break;
     }
 #pragma unroll
-    for (int nd = 0; nd < ND; ++nd) {
-      o[nd][0] *= alpha[0];
-      o[nd][1] *= alpha[0];
-      o[nd][2] *= alpha[1];
-      o[nd][3] *= alpha[1];
-    }
-    // ---- O += P V: k = 64 keys (4 k-steps), n = d ----
+    for (int c0 = 0; c0 < D; c0 += 32) {
+      float tmp[32];
+      tmem_ld32(tmem + lane_base + kColO + c0, tmp);
 #pragma unroll
-    for (int kk = 0; kk < NK / 2; ++kk) {
-      // the A fragment registers a0..a3 are (r0, k lo), (r0+8, k lo), (r0, k hi), (r0+8, k hi)
-      const uint32_t a[4] = {pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3]};
-#pragma unroll
-      for (int np = 0; np < ND / 2; ++np) {
-        // B fragments of two n-tiles (d 16np..16np+15), k = keys 16kk..16kk+15, V^T
-        uint32_t bf[4];
-        ldsm_x4_t(vb + swz(16 * kk + lrow + ((lmat & 1) << 3), 2 * np + (lmat >> 1)), bf);
-        mma16816<T>(o[2 * np], a, bf[0], bf[1]);
-        mma16816<T>(o[2 * np + 1], a, bf[2], bf[3]);
-      }
+      for (int i = 0; i < 32; ++i) o[c0 + i] += tmp[i];
     }
-    __syncthreads();  // every warp is done with buffer b before it is refilled
+    // every P V read and every thread's use of buffer b is done before it is refilled
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  }
+  if (!ok) {  // a wait gave up: flag it; let the copies land before leaving
+    cp_async_wait<0>();
+    if (tid == 0) atomicOr(p.err, kErrTimeout);
   }
 
   // ---- out = O / l ----
-  const bool bad = sm.bad != 0;
+  const bool bad = sm.bad != 0 || !ok;
+  if (row_ok) {
+    uint4* dst = reinterpret_cast<uint4*>(outp + row_off);
+    const float inv = 1.f / l_run;
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    if (qrow_off[i] < 0) continue;
-    const float inv = 1.f / l_run[i];
-#pragma unroll
-    for (int nd = 0; nd < ND; ++nd) {
-      // (a bad block's rows were read from block 0, whatever it holds: zeros, not 0 * O)
-      const uint32_t v = bad ? 0u : pack2<T>(o[nd][2 * i] * inv, o[nd][2 * i + 1] * inv);
-      *reinterpret_cast<uint32_t*>(outp + qrow_off[i] + 8 * nd + qc) = v;
+    for (int c = 0; c < CH; ++c) {
+      uint4 w = make_uint4(0, 0, 0, 0);
+      if (!bad) {
+        w.x = pack2<T>(o[8 * c + 0] * inv, o[8 * c + 1] * inv);
+        w.y = pack2<T>(o[8 * c + 2] * inv, o[8 * c + 3] * inv);
+        w.z = pack2<T>(o[8 * c + 4] * inv, o[8 * c + 5] * inv);
+        w.w = pack2<T>(o[8 * c + 6] * inv, o[8 * c + 7] * inv);
+      }
+      dst[c] = w;
     }
   }
-  if (bad && tid == 0) atomicOr(p.err, kErrBadBlock);
+  if (sm.bad && tid == 0) atomicOr(p.err, kErrBadBlock);
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
 }
 
 template <int D, typename T>
