@@ -20,8 +20,9 @@ to check by eye against the pages it follows:
 Modules:
     formats     -- 16-bit float encodings and round-to-nearest-even from float64.
     attention   -- paged decode attention, its split-KV partials and their merge.
-    cache_ops   -- reshape_and_cache (slot writes) and copy_blocks (block copies).
-    block_pool  -- free list, reference counts, fork and copy-on-write bookkeeping.
+    cache_ops   -- reshape_and_cache (slot writes), copy_blocks and swap_blocks (block
+                   copies within a pool and between the device and a CPU pool).
+    block_pool  -- free list, reference counts, fork, copy-on-write and swap bookkeeping.
     sizing      -- the closed forms the pages print (block counts, bytes, capacity).
 
 Every function is pinned by ``tests/test_oracle_*.py`` against something other than

@@ -19,12 +19,24 @@ Test infrastructure only.  The steps, in the pages' order:
   blocks stay shared (chenyuan1125, section 一块内存…; horeb.top, section 内存共享).
 * When the pool is exhausted the request is rejected rather than the process failing
   (daiw.org, section 速查卡, 运维提示; the demo's allocate returns False).
+* Preemption: when device memory runs short, a request's blocks can be moved out whole
+  into CPU memory and moved back once room returns; the block table is what makes the
+  move cheap (aiqz.cc, section 连续批处理：随到随走的新秩序).  The CPU side is a second
+  pool of blocks with the same free list and reference count rules.
 
 Readings where the pages are silent:
 * a write copies when the last block's reference count is above one at write time, so
   with k sharers the first k-1 writers copy and the last writes in place;
 * blocks freed together return to the tail in table order;
-* an operation that cannot get every block it needs changes nothing.
+* an operation that cannot get every block it needs changes nothing;
+* swap_out moves a group of resident sequences: every distinct device block of their
+  tables (sequences in the order given, tables in order, first appearance) gets one CPU
+  block from the head of the CPU free list, carrying the group's references; the device
+  block loses those references and, at zero, returns to the device tail in that same
+  order.  swap_in is the mirror image.  A block also held outside the group keeps its
+  other references where it is (the group then owns a separate copy);
+* a swapped-out sequence can be freed (its CPU blocks return to the CPU tail) or swapped
+  in, but not grown or forked.
 """
 import math
 
@@ -37,19 +49,30 @@ class UnknownSequence(KeyError):
     """The sequence id is not live (or, for allocate/fork targets, already live)."""
 
 
+class WrongTier(Exception):
+    """The sequence is swapped out where a resident one is needed, or the reverse."""
+
+
+def _order(n, order):
+    order = list(range(n)) if order is None else [int(b) for b in order]
+    if sorted(order) != list(range(n)):
+        raise ValueError("a free order must be a permutation of 0..n-1")
+    return order
+
+
 class BlockPool:
-    def __init__(self, num_blocks, block_size, initial_free_order=None):
-        if initial_free_order is None:
-            initial_free_order = range(num_blocks)
-        order = [int(b) for b in initial_free_order]
-        if sorted(order) != list(range(num_blocks)):
-            raise ValueError("initial free order must be a permutation of 0..num_blocks-1")
+    def __init__(self, num_blocks, block_size, initial_free_order=None, num_cpu_blocks=0,
+                 cpu_free_order=None):
         self.num_blocks = num_blocks
         self.block_size = block_size
-        self.free_list = order          # head = index 0
+        self.free_list = _order(num_blocks, initial_free_order)   # head = index 0
         self.refcount = [0] * num_blocks
-        self.tables = {}                # seq id -> list of physical block ids
+        self.num_cpu_blocks = num_cpu_blocks
+        self.cpu_free_list = _order(num_cpu_blocks, cpu_free_order)
+        self.cpu_refcount = [0] * num_cpu_blocks
+        self.tables = {}                # seq id -> list of block ids (CPU ids if swapped)
         self.ctx = {}                   # seq id -> tokens held
+        self.swapped = set()            # seq ids whose blocks are in the CPU pool
 
     # -- queries ------------------------------------------------------------------------
     def num_free(self):
@@ -64,6 +87,11 @@ class BlockPool:
         if seq not in self.ctx:
             raise UnknownSequence(seq)
         return self.ctx[seq]
+
+    def is_swapped(self, seq):
+        if seq not in self.tables:
+            raise UnknownSequence(seq)
+        return seq in self.swapped
 
     def slot(self, seq, t):
         """Slot of logical token t of ``seq``: table[t // B] * B + t % B."""
@@ -98,6 +126,8 @@ class BlockPool:
         """
         if seq not in self.tables:
             raise UnknownSequence(seq)
+        if seq in self.swapped:
+            raise WrongTier(f"sequence {seq} is swapped out")
         table = self.tables[seq]
         t = self.ctx[seq]
         cow = None
@@ -118,6 +148,8 @@ class BlockPool:
             raise UnknownSequence(parent)
         if child in self.tables:
             raise UnknownSequence(f"sequence {child} already live")
+        if parent in self.swapped:
+            raise WrongTier(f"sequence {parent} is swapped out")
         self.tables[child] = list(self.tables[parent])
         self.ctx[child] = self.ctx[parent]
         for b in self.tables[child]:
@@ -127,8 +159,58 @@ class BlockPool:
         """End a sequence: drop one reference per block; blocks at zero go to the tail."""
         if seq not in self.tables:
             raise UnknownSequence(seq)
+        on_cpu = seq in self.swapped
+        refcount = self.cpu_refcount if on_cpu else self.refcount
+        free_list = self.cpu_free_list if on_cpu else self.free_list
         for b in self.tables.pop(seq):
-            self.refcount[b] -= 1
-            if self.refcount[b] == 0:
-                self.free_list.append(b)
+            refcount[b] -= 1
+            if refcount[b] == 0:
+                free_list.append(b)
         del self.ctx[seq]
+        self.swapped.discard(seq)
+
+    def _move(self, seqs, to_cpu):
+        """Move a group of sequences to the other pool; return the (from, to) block pairs
+        the caller copies."""
+        seqs = list(seqs)
+        if len(set(seqs)) != len(seqs):
+            raise ValueError("a sequence appears twice in the group")
+        for seq in seqs:
+            if seq not in self.tables:
+                raise UnknownSequence(seq)
+            if (seq in self.swapped) == to_cpu:
+                raise WrongTier(f"sequence {seq} is already {'out' if to_cpu else 'in'}")
+        src_ref, src_free = ((self.refcount, self.free_list) if to_cpu
+                             else (self.cpu_refcount, self.cpu_free_list))
+        dst_ref, dst_free = ((self.cpu_refcount, self.cpu_free_list) if to_cpu
+                             else (self.refcount, self.free_list))
+        # the group's references to each distinct block, in order of first appearance
+        refs = {}
+        for seq in seqs:
+            for b in self.tables[seq]:
+                refs[b] = refs.get(b, 0) + 1
+        if len(refs) > len(dst_free):
+            raise PoolExhausted(f"need {len(refs)} blocks, {len(dst_free)} free")
+        new = dict(zip(refs, dst_free[:len(refs)]))
+        del dst_free[:len(refs)]
+        for b, n in refs.items():
+            dst_ref[new[b]] = n
+            src_ref[b] -= n
+            if src_ref[b] == 0:
+                src_free.append(b)
+        for seq in seqs:
+            self.tables[seq] = [new[b] for b in self.tables[seq]]
+            if to_cpu:
+                self.swapped.add(seq)
+            else:
+                self.swapped.discard(seq)
+        return [(b, new[b]) for b in refs]
+
+    def swap_out(self, seqs):
+        """Preempt a group of resident sequences: returns (device block, CPU block) pairs."""
+        return self._move(seqs, True)
+
+    def swap_in(self, seqs):
+        """Bring a group of swapped-out sequences back: returns (CPU block, device block)
+        pairs."""
+        return self._move(seqs, False)

@@ -11,7 +11,12 @@ block is copied, the branch's mapping is updated, then the write goes ahead; ful
 blocks stay shared (chenyuan1125, section 一块内存，如何安全地属于多条序列; horeb.top,
 section 内存共享：写时复制).  A copy moves every kv head and every row of the block.
 
-Both are exact copies of 16-bit patterns; the oracle works on ``uint16`` arrays.
+swap_blocks: a preempted request's blocks move whole between the device pool and a
+CPU pool, and back when room returns (aiqz.cc "vLLM PagedAttention engine", section
+连续批处理：随到随走的新秩序): block dst of the destination pool := block src of the source
+pool, every kv head and row.
+
+All are exact copies of 16-bit patterns; the oracle works on ``uint16`` arrays.
 """
 import numpy as np
 
@@ -67,4 +72,26 @@ def copy_blocks(k_cache, v_cache, pairs):
     for s, d in pairs:
         k_out[d] = k_cache[s]
         v_out[d] = v_cache[s]
+    return k_out, v_out
+
+
+def swap_blocks(src_k, src_v, dst_k, dst_v, pairs):
+    """Return copies of (dst_k, dst_v) with dst[d] := src[s] for every (s, d) pair.
+
+    The source and destination are different pools (shapes [NBs, Hkv, B, d] and
+    [NBd, Hkv, B, d]); destination ids must be distinct; ids must lie in their pool.
+    """
+    nbs, nbd = src_k.shape[0], dst_k.shape[0]
+    pairs = [(int(s), int(d)) for s, d in np.asarray(pairs, dtype=np.int64).reshape(-1, 2)]
+    dsts = [d for _, d in pairs]
+    if len(set(dsts)) != len(dsts):
+        raise ValueError("swap_blocks destinations repeat")
+    for s, d in pairs:
+        if not (0 <= s < nbs and 0 <= d < nbd):
+            raise IndexError(f"block pair ({s}, {d}) outside [0, {nbs}) x [0, {nbd})")
+    k_out = dst_k.copy()
+    v_out = dst_v.copy()
+    for s, d in pairs:
+        k_out[d] = src_k[s]
+        v_out[d] = src_v[s]
     return k_out, v_out
