@@ -600,6 +600,207 @@ def prefill_line(args, res, world):
     }
 
 
+SWAP_WORKLOADS = {"swap_llama31_8b": "llama31_8b", "swap_llama7b_mha": "llama7b_mha"}
+
+
+def run_gpu_swap(args, rank, world, local_rank):
+    """Preemption of a whole decode batch: swap-out of every sequence's blocks from the
+    device pool to a pinned CPU pool, then swap-in to fresh device blocks -- one
+    pa_swap_blocks launch per direction.  Timed three ways: the two launches alone on
+    planned pair lists (CUDA events around K steps); the same bytes as two contiguous
+    cudaMemcpyAsync copies (copy engines, the link's reference rate in this run); and end
+    to end through the public API (pool planning, pair upload, both launches)."""
+    import torch
+
+    import paged_kv_cache_149_gb300 as pa
+    import workloads
+    from paged_kv_cache_149_gb300 import build as _build
+
+    _build.build()
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    wl = workloads.RECIPES[SWAP_WORKLOADS[args.workload]]()
+    dt = {"fp16": torch.float16, "bf16": torch.bfloat16}[wl.dtype]
+    n = wl.num_seqs
+    used = sum(-(-int(c) // wl.block_size) for c in wl.context_lens)
+    ncpu = used + 64
+    pool = pa.BlockPool(wl.num_blocks, wl.block_size, wl.free_order, num_cpu_blocks=ncpu)
+    shape = (wl.num_blocks, wl.num_kv_heads, wl.block_size, wl.head_dim)
+    cshape = (ncpu,) + shape[1:]
+    k_cache = torch.zeros(shape, dtype=dt, device=device)
+    v_cache = torch.zeros(shape, dtype=dt, device=device)
+    hk = torch.zeros(cshape, dtype=dt).pin_memory()
+    hv = torch.zeros(cshape, dtype=dt).pin_memory()
+    slots = []
+    for s in range(n):
+        pool.allocate(s, int(wl.context_lens[s]))
+        slots.append(pool.slots(s, 0, int(wl.context_lens[s])))
+
+    def up(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(dt)
+    pa.reshape_and_cache(up(wl.keys), up(wl.values), k_cache, v_cache,
+                         torch.from_numpy(np.concatenate(slots)).to(device))
+    seqs = list(range(n))
+    # planned pairs of one out / in cycle (the pool's own plan, uploaded once)
+    out_pairs = pool.swap_out(seqs)
+    in_pairs = pool.swap_in(seqs)  # (resident again; the end-to-end steps plan afresh)
+    d_out = torch.from_numpy(out_pairs).to(device)
+    d_in = torch.from_numpy(in_pairs).to(device)
+    block_bytes = 2 * wl.num_kv_heads * wl.block_size * wl.head_dim * 2  # K and V
+    moved = len(out_pairs) * block_bytes  # per direction
+    stream = torch.cuda.Stream(device)
+    torch.cuda.synchronize(device)
+    pa.get_device_error()
+
+    def step(i):
+        pa.swap_blocks(k_cache, v_cache, hk, hv, d_out, stream=stream, device=device)
+        pa.swap_blocks(hk, hv, k_cache, v_cache, d_in, stream=stream, device=device)
+
+    def timed(fn, K):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(device)
+        e0.record(stream)
+        for i in range(K):
+            fn(i)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        return e0.elapsed_time(e1)
+
+    for i in range(args.warmup):
+        step(i)
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    K = args.steps
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(device)
+    t0 = time.time()
+    total_ms = timed(step, K)
+    t1 = time.time()
+    clocks = sampler.stop(t0, t1) if sampler else None
+    flags = pa.get_device_error(stream=stream)
+    # the link's reference rate: the same bytes as one contiguous copy each way
+    flat_dev = torch.empty(moved // 2, dtype=torch.int16, device=device)
+    flat_host = torch.empty(moved // 2, dtype=torch.int16).pin_memory()
+
+    def ce_step(i):
+        with torch.cuda.stream(stream):
+            flat_host.copy_(flat_dev, non_blocking=True)
+            flat_dev.copy_(flat_host, non_blocking=True)
+    for i in range(3):
+        ce_step(i)
+    ce_ms = timed(ce_step, max(3, min(K, 20))) / max(3, min(K, 20))
+    # end to end through the public API: plan on the host, upload the pairs, move
+    pin_pairs = torch.zeros((2, len(out_pairs) + 8, 2), dtype=torch.int32).pin_memory()
+    dev_pairs = torch.zeros((2, len(out_pairs) + 8, 2), dtype=torch.int32, device=device)
+
+    def e2e_step(i):
+        # the swap-in is planned on the host while the swap-out copy runs
+        for j, (fn, src, dst) in enumerate(((pool.swap_out, (k_cache, v_cache), (hk, hv)),
+                                            (pool.swap_in, (hk, hv), (k_cache, v_cache)))):
+            pairs = fn(seqs)
+            m = len(pairs)
+            pin_pairs[j, :m].numpy()[:] = pairs
+            with torch.cuda.stream(stream):
+                dev_pairs[j, :m].copy_(pin_pairs[j, :m], non_blocking=True)
+            pa.swap_blocks(*src, *dst, dev_pairs[j, :m], stream=stream, device=device)
+        stream.synchronize()  # (the pinned pair buffers are refilled next step)
+    for i in range(3):
+        e2e_step(i)
+    ke = max(3, min(K, 20))
+    torch.cuda.synchronize(device)
+    w0 = time.perf_counter()
+    for i in range(ke):
+        e2e_step(i)
+    torch.cuda.synchronize(device)
+    e2e_ms = (time.perf_counter() - w0) * 1e3 / ke
+    flags |= pa.get_device_error(stream=stream)
+    return {"wl": wl, "total_ms": total_ms, "decode_ms": total_ms / K, "two_calls_ms": ce_ms,
+            "e2e_ms": e2e_ms, "h2d": moved + 8 * (len(out_pairs) + len(in_pairs)), "d2h": moved,
+            "moved": moved, "blocks": len(out_pairs), "clocks": clocks, "flags": flags}
+
+
+def oracle_swap_sample(name, budget_s):
+    """The oracle's swap_blocks on a bounded sample of the batch's blocks (both
+    directions), block count doubled while the single-threaded run stays within budget."""
+    code = f"""
+import json, sys, time
+sys.path.insert(0, {ROOT!r})
+import numpy as np
+import workloads
+from oracle import cache_ops
+wl = workloads.RECIPES[{SWAP_WORKLOADS[name]!r}]()
+rng = np.random.default_rng(0)
+m = 16
+while True:
+    shape = (m, wl.num_kv_heads, wl.block_size, wl.head_dim)
+    dk = rng.integers(0, 65535, size=shape, dtype=np.uint16)
+    dv = rng.integers(0, 65535, size=shape, dtype=np.uint16)
+    ck, cv = np.zeros_like(dk), np.zeros_like(dv)
+    pairs = np.stack([np.arange(m), rng.permutation(m)], axis=1)
+    t = time.process_time()
+    ck, cv = cache_ops.swap_blocks(dk, dv, ck, cv, pairs)
+    dk, dv = cache_ops.swap_blocks(ck, cv, dk, dv, pairs[:, ::-1])
+    dt = time.process_time() - t
+    if dt * 4 > {budget_s} or m >= 4096:
+        break
+    m *= 2
+print(json.dumps({{"blocks": m, "seconds": dt, "bytes": 2 * dk.nbytes * 2}}))
+"""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
+    if r.returncode != 0:
+        raise RuntimeError("swap oracle baseline failed:\n" + r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def swap_line(args, res, world):
+    wl = res["wl"]
+    step_bytes_ = 2 * res["moved"]  # out and in
+    step_s = res["total_ms"] / 1e3 / args.steps
+    value = world * step_bytes_ / step_s / 1e9
+    link = step_bytes_ / (res["two_calls_ms"] / 1e3) / 1e9
+    cpu = oracle_swap_sample(args.workload, args.cpu_baseline_seconds) \
+        if args.cpu_baseline_seconds > 0 else None
+    return {
+        "metric": "paged KV swap GB/s (device pool -> pinned CPU pool -> device pool, "
+                  "through the block tables)",
+        "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(res["total_ms"] / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u16 (bit copy)",
+        "data": "synthetic (seeded normals; no dataset or weights)",
+        "config": {
+            "workload": (f"{args.workload}: the {wl.name} batch ({wl.num_seqs} seqs, "
+                         f"{res['blocks']} blocks of {wl.num_kv_heads} kv heads x "
+                         f"{wl.block_size} x {wl.head_dim}, K and V) swapped out and back in "
+                         "every step"),
+            "l2": f"{res['moved'] / 1e6:.0f} MB each way per step (above L2)",
+            "parallelism": f"replicas x{world}",
+        },
+        "roofline": {"bound": "c2c", "kernel": "block_copy_kernel (pa_swap_blocks)",
+                     "achieved": round(value / world, 1), "peak": round(link, 1),
+                     "peak_kind": "measured in this run: the same bytes as one contiguous "
+                                  "cudaMemcpyAsync each way (copy engines)",
+                     "unit": "GB/s", "frac": round(value / world / link, 4), "traffic": None},
+        "cpu_baseline": None if cpu is None else {
+            "value": round(cpu["bytes"] / cpu["seconds"] / 1e9, 3), "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"NumPy oracle swap_blocks (exact 16-bit copies), single thread, "
+                      f"{cpu['blocks']} blocks out and back in"},
+        "e2e": {"value": round(world * step_bytes_ / (res["e2e_ms"] / 1e3) / 1e9, 1),
+                "unit": "GB/s", "h2d_bytes_per_step": res["h2d"],
+                "d2h_bytes_per_step": res["d2h"], "us_per_step": round(1e3 * res["e2e_ms"], 2),
+                "includes": "host planning by the C++ pool, pair upload, both launches"},
+        "clocks": res["clocks"],
+        "gpu_launches": 2 * args.steps,
+        "device_error_flags": res["flags"],
+    }
+
+
 def max_over_ranks(values):
     """Element-wise maximum of per-rank floats over the process group (NCCL on GPUs, or any
     other backend on CPU tensors)."""
@@ -643,7 +844,9 @@ def main(argv=None, runner=None, backend="nccl"):
         import torch
         torch.distributed.init_process_group(backend)
     is_prefill = args.workload.startswith("prefill")
-    res = (runner or (run_gpu_prefill if is_prefill else run_gpu))(args, rank, world, local_rank)
+    is_swap = args.workload in SWAP_WORKLOADS
+    default_runner = run_gpu_prefill if is_prefill else (run_gpu_swap if is_swap else run_gpu)
+    res = (runner or default_runner)(args, rank, world, local_rank)
     if world > 1:
         res.update(zip(RANK_TIMES, max_over_ranks([res[k] for k in RANK_TIMES])))
     if rank != 0:
@@ -651,8 +854,8 @@ def main(argv=None, runner=None, backend="nccl"):
             import torch
             torch.distributed.destroy_process_group()
         return
-    if is_prefill:
-        print(json.dumps(prefill_line(args, res, world)))
+    if is_prefill or is_swap:
+        print(json.dumps((prefill_line if is_prefill else swap_line)(args, res, world)))
         if world > 1:
             import torch
             torch.distributed.destroy_process_group()

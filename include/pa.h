@@ -55,14 +55,16 @@ enum {
   PA_ERR_WORKSPACE = -2,      /* workspace missing or smaller than pa_decode_workspace_size */
   PA_ERR_CUDA = -3,           /* a CUDA runtime call failed (launch, attribute, copy) */
   PA_ERR_POOL_EXHAUSTED = -4, /* not enough free blocks; the pool is unchanged */
-  PA_ERR_UNKNOWN_SEQ = -5     /* sequence id not live (or already live, for a new id) */
+  PA_ERR_UNKNOWN_SEQ = -5,    /* sequence id not live (or already live, for a new id) */
+  PA_ERR_WRONG_TIER = -6      /* sequence swapped out where a resident one is needed, or
+                                 resident where a swapped-out one is needed */
 };
 
 /* Bits of the per-device error word (pa_get_device_error). */
 #define PA_DEVERR_BAD_BLOCK   0x1u  /* decode: a used block-table entry is outside [0, num_blocks) */
 #define PA_DEVERR_BAD_CONTEXT 0x2u  /* decode: context length < 1 or > max_blocks_per_seq * B */
 #define PA_DEVERR_BAD_SLOT    0x4u  /* reshape_and_cache: slot >= num_blocks * B */
-#define PA_DEVERR_BAD_PAIR    0x8u  /* copy_blocks: a block id outside [0, num_blocks) */
+#define PA_DEVERR_BAD_PAIR    0x8u  /* copy_blocks / swap_blocks: a block id outside its pool */
 #define PA_DEVERR_TIMEOUT     0x10u /* decode: a pipeline wait gave up (about 1 s); output invalid */
 
 /*
@@ -208,6 +210,29 @@ int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* block_mapping, i
                    int num_blocks, int num_kv_heads, int head_dim, int block_size,
                    pa_dtype dtype, cudaStream_t stream);
 
+/*
+ * pa_swap_blocks -- copy whole blocks from one pool to another:
+ *   dst_k[d] = src_k[s], dst_v[d] = src_v[s]  for each pair (s, d) of block_mapping.
+ *
+ * This moves a preempted request's blocks to CPU memory (swap-out) and back (swap-in);
+ * the block table is what makes the move a plain block copy (aiqz.cc "vLLM
+ * PagedAttention engine", section 连续批处理：随到随走的新秩序).  pa_pool_swap_out /
+ * pa_pool_swap_in plan the pairs.
+ *
+ * Pools: src [src_num_blocks, Hkv, B, d], dst [dst_num_blocks, Hkv, B, d], same dtype.
+ * Each of the five pointers may be device memory or page-locked host memory registered
+ * with CUDA (cudaHostAlloc, cudaMallocHost, cudaHostRegister; a pinned torch tensor):
+ * the GPU reads and writes host memory directly (over NVLink-C2C on GB300), so one
+ * kernel launch moves every pair.  Anything else (pageable host memory) is PA_ERR_ARG.
+ * block_mapping is int32 [num_pairs, 2].  Destination ids must be distinct and the two
+ * pools must not overlap.  A pair with an id outside its pool is skipped and flagged
+ * (PA_DEVERR_BAD_PAIR).  num_pairs == 0 is a no-op.
+ */
+int pa_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_v,
+                   const int32_t* block_mapping, int num_pairs, int src_num_blocks,
+                   int dst_num_blocks, int num_kv_heads, int head_dim, int block_size,
+                   pa_dtype dtype, cudaStream_t stream);
+
 /* Host-side check of a copy_blocks pair list (host memory): PA_OK, or PA_ERR_ARG when an
  * id is outside [0, num_blocks), a dst repeats, or a dst is also a src. */
 int pa_check_block_mapping(const int32_t* host_block_mapping, int num_pairs, int num_blocks);
@@ -232,12 +257,25 @@ const char* pa_status_string(int status);
  * section 一块内存…).  An operation that cannot get every block it needs changes
  * nothing and returns PA_ERR_POOL_EXHAUSTED (daiw.org, section 速查卡: an exhausted pool
  * rejects new requests instead of failing).  Host memory only; not thread-safe.
+ *
+ * A second pool of CPU blocks (pa_pool_create_tiered) backs preemption: a group of
+ * resident sequences is swapped out whole and later swapped back in (aiqz.cc, section
+ * 连续批处理：随到随走的新秩序).  Each distinct block of the group's tables (sequences in
+ * the order given, tables in order, first appearance) takes one block from the head of
+ * the other pool's free list and carries the group's references to it; the old block
+ * loses them and, at zero, returns to its pool's tail in that order.  The tables are
+ * rewritten to the new ids.  A swapped-out sequence can be freed or swapped in; grow,
+ * fork and pa_pool_slots return PA_ERR_WRONG_TIER.
  */
 typedef struct pa_pool pa_pool;
 
 /* initial_free_order: NULL for 0..num_blocks-1, else a permutation of it (host).
  * Returns NULL on a bad argument or allocation failure. */
 pa_pool* pa_pool_create(int num_blocks, int block_size, const int32_t* initial_free_order);
+/* The same with a CPU pool of num_cpu_blocks (>= 0) blocks, free order cpu_free_order
+ * (NULL for 0..num_cpu_blocks-1, else a permutation of it). */
+pa_pool* pa_pool_create_tiered(int num_blocks, int block_size, const int32_t* initial_free_order,
+                               int num_cpu_blocks, const int32_t* cpu_free_order);
 void pa_pool_destroy(pa_pool* pool);
 /* Prefill: a new sequence holding n_tokens tokens in ceil(n_tokens / B) blocks. */
 int pa_pool_allocate(pa_pool* pool, int64_t seq_id, int n_tokens);
@@ -260,6 +298,19 @@ int pa_pool_num_free(const pa_pool* pool);
 int pa_pool_free_list(const pa_pool* pool, int32_t* out, int cap);
 /* Reference count of a block, or PA_ERR_ARG for an id outside the pool. */
 int pa_pool_refcount(const pa_pool* pool, int32_t block);
+/* Swap a group of n distinct resident sequences out to the CPU pool.  Writes the
+ * (device block, CPU block) pairs to pairs_out [cap][2] and returns their number, or an
+ * error (PA_ERR_ARG for a repeated id or cap too small, PA_ERR_UNKNOWN_SEQ,
+ * PA_ERR_WRONG_TIER, PA_ERR_POOL_EXHAUSTED); on error nothing changes.  The caller then
+ * copies the pairs with pa_swap_blocks (device pool -> CPU pool). */
+int pa_pool_swap_out(pa_pool* pool, const int64_t* seq_ids, int n, int32_t* pairs_out, int cap);
+/* The mirror image: (CPU block, device block) pairs, copied CPU pool -> device pool. */
+int pa_pool_swap_in(pa_pool* pool, const int64_t* seq_ids, int n, int32_t* pairs_out, int cap);
+/* 1 if the sequence is swapped out, 0 if resident, or PA_ERR_UNKNOWN_SEQ. */
+int pa_pool_is_swapped(const pa_pool* pool, int64_t seq_id);
+int pa_pool_num_free_cpu(const pa_pool* pool);
+int pa_pool_cpu_free_list(const pa_pool* pool, int32_t* out, int cap);
+int pa_pool_cpu_refcount(const pa_pool* pool, int32_t block);
 
 #ifdef __cplusplus
 }

@@ -29,6 +29,7 @@ PA_ERR_WORKSPACE = -2
 PA_ERR_CUDA = -3
 PA_ERR_POOL_EXHAUSTED = -4
 PA_ERR_UNKNOWN_SEQ = -5
+PA_ERR_WRONG_TIER = -6
 
 DEVERR_BAD_BLOCK = 0x1
 DEVERR_BAD_CONTEXT = 0x2
@@ -55,10 +56,13 @@ SIGNATURES = {
     "pa_decode_fixed_scratch": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                                        _i32, _f32, _vp, _i32, _vp]),
     "pa_copy_blocks": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp]),
+    "pa_swap_blocks": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+                              _vp]),
     "pa_check_block_mapping": (_i32, [_vp, _i32, _i32]),
     "pa_get_device_error": (_i32, [_vp, _c.POINTER(_c.c_uint32)]),
     "pa_status_string": (_c.c_char_p, [_i32]),
     "pa_pool_create": (_vp, [_i32, _i32, _vp]),
+    "pa_pool_create_tiered": (_vp, [_i32, _i32, _vp, _i32, _vp]),
     "pa_pool_destroy": (None, [_vp]),
     "pa_pool_allocate": (_i32, [_vp, _i64, _i32]),
     "pa_pool_append_slot": (_i32, [_vp, _i64, _c.POINTER(_i64), _c.POINTER(_c.c_int32),
@@ -71,6 +75,12 @@ SIGNATURES = {
     "pa_pool_num_free": (_i32, [_vp]),
     "pa_pool_free_list": (_i32, [_vp, _vp, _i32]),
     "pa_pool_refcount": (_i32, [_vp, _c.c_int32]),
+    "pa_pool_swap_out": (_i32, [_vp, _vp, _i32, _vp, _i32]),
+    "pa_pool_swap_in": (_i32, [_vp, _vp, _i32, _vp, _i32]),
+    "pa_pool_is_swapped": (_i32, [_vp, _i64]),
+    "pa_pool_num_free_cpu": (_i32, [_vp]),
+    "pa_pool_cpu_free_list": (_i32, [_vp, _vp, _i32]),
+    "pa_pool_cpu_refcount": (_i32, [_vp, _c.c_int32]),
 }
 
 _lib = None
@@ -87,6 +97,10 @@ class PoolExhausted(PagedAttentionError):
 
 
 class UnknownSequence(PagedAttentionError):
+    pass
+
+
+class WrongTier(PagedAttentionError):
     pass
 
 
@@ -117,6 +131,8 @@ def _check(status, what):
             raise PoolExhausted(status, what)
         if status == PA_ERR_UNKNOWN_SEQ:
             raise UnknownSequence(status, what)
+        if status == PA_ERR_WRONG_TIER:
+            raise WrongTier(status, what)
         raise PagedAttentionError(status, what)
     return status
 
@@ -300,6 +316,36 @@ def copy_blocks(k_cache, v_cache, block_mapping, stream=None):
     _check(st, "pa_copy_blocks")
 
 
+def _reachable(t, name, dtype=None):
+    """A CUDA tensor, or a page-locked (pinned) CPU tensor that the GPU can address."""
+    _need(t.is_cuda or t.is_pinned(), f"{name} must be a CUDA tensor or a pinned CPU tensor")
+    _need(t.is_contiguous(), f"{name} must be contiguous")
+    if dtype is not None:
+        _need(t.dtype == dtype, f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def swap_blocks(src_k, src_v, dst_k, dst_v, block_mapping, stream=None, device=None):
+    """dst_k[d] = src_k[s] and dst_v[d] = src_v[s] for each (s, d) of block_mapping, in one
+    kernel launch.  Pools and mapping may be CUDA tensors or pinned CPU tensors (swap-out:
+    device pool -> pinned CPU pool; swap-in: the reverse)."""
+    import torch
+    nbs, hkv, bs, d = src_k.shape
+    nbd = dst_k.shape[0]
+    _need(src_v.shape == src_k.shape and dst_v.shape == dst_k.shape, "shape mismatch")
+    _need(dst_k.shape[1:] == src_k.shape[1:], "pools must share Hkv, B, d")
+    _need(src_k.dtype == src_v.dtype == dst_k.dtype == dst_v.dtype, "dtype mismatch")
+    _need(block_mapping.dim() == 2 and block_mapping.shape[1] == 2, "block_mapping must be [n, 2]")
+    if device is None:
+        device = next((t.device for t in (src_k, dst_k) if t.is_cuda), torch.device("cuda"))
+    st = lib().pa_swap_blocks(
+        _reachable(src_k, "src_k"), _reachable(src_v, "src_v"), _reachable(dst_k, "dst_k"),
+        _reachable(dst_v, "dst_v"), _reachable(block_mapping, "block_mapping", torch.int32),
+        block_mapping.shape[0], nbs, nbd, hkv, d, bs, _dtype_code(src_k),
+        _stream_ptr(stream, device))
+    _check(st, "pa_swap_blocks")
+
+
 def check_block_mapping(pairs, num_blocks):
     """Host check of a copy_blocks pair list (sequence of (src, dst)); raises on aliasing."""
     import numpy as np
@@ -320,20 +366,28 @@ def get_device_error(stream=None, device=None):
 # ------------------------------------------------------------------ block pool
 
 class BlockPool:
-    """Host block pool (C++): ordered free list, refcounts, fork, copy-on-write planning."""
+    """Host block pool (C++): ordered free list, refcounts, fork, copy-on-write planning,
+    and an optional CPU pool for swap-out / swap-in."""
 
-    def __init__(self, num_blocks, block_size, initial_free_order=None):
+    def __init__(self, num_blocks, block_size, initial_free_order=None, num_cpu_blocks=0,
+                 cpu_free_order=None):
         import numpy as np
         self.num_blocks = int(num_blocks)
         self.block_size = int(block_size)
-        order = None
-        if initial_free_order is not None:
-            self._order = np.ascontiguousarray(np.asarray(initial_free_order, dtype=np.int32))
-            _need(self._order.shape == (self.num_blocks,), "initial_free_order must have num_blocks entries")
-            order = self._order.ctypes.data
-        self._h = lib().pa_pool_create(self.num_blocks, self.block_size, order)
+        self.num_cpu_blocks = int(num_cpu_blocks)
+
+        def order_ptr(order, n, name):
+            if order is None:
+                return None, None
+            arr = np.ascontiguousarray(np.asarray(order, dtype=np.int32))
+            _need(arr.shape == (n,), f"{name} must have {n} entries")
+            return arr, arr.ctypes.data
+        self._order, order = order_ptr(initial_free_order, self.num_blocks, "initial_free_order")
+        self._cpu_order, cpu_order = order_ptr(cpu_free_order, self.num_cpu_blocks, "cpu_free_order")
+        self._h = lib().pa_pool_create_tiered(self.num_blocks, self.block_size, order,
+                                              self.num_cpu_blocks, cpu_order)
         if not self._h:
-            raise PagedAttentionError(PA_ERR_ARG, "pa_pool_create")
+            raise PagedAttentionError(PA_ERR_ARG, "pa_pool_create_tiered")
 
     def __del__(self):
         h = getattr(self, "_h", None)
@@ -387,3 +441,37 @@ class BlockPool:
 
     def refcount(self, block):
         return _check(lib().pa_pool_refcount(self._h, int(block)), "refcount")
+
+    def _move(self, fn, seqs, what):
+        import numpy as np
+        ids = np.ascontiguousarray(np.asarray(list(seqs), dtype=np.int64))
+        cap = sum(len(self.block_table(int(s))) for s in set(ids.tolist())) if ids.size else 0
+        pairs = np.zeros((max(cap, 1), 2), dtype=np.int32)
+        n = _check(fn(self._h, ids.ctypes.data, ids.size, pairs.ctypes.data, cap), what)
+        return pairs[:n]
+
+    def swap_out(self, seqs):
+        """Move a group of resident sequences to the CPU pool; returns the (device block,
+        CPU block) pairs [n, 2] int32 to copy with swap_blocks."""
+        return self._move(lib().pa_pool_swap_out, seqs, "swap_out")
+
+    def swap_in(self, seqs):
+        """Bring a group of swapped-out sequences back; returns (CPU block, device block)
+        pairs."""
+        return self._move(lib().pa_pool_swap_in, seqs, "swap_in")
+
+    def is_swapped(self, seq):
+        return bool(_check(lib().pa_pool_is_swapped(self._h, int(seq)), "is_swapped"))
+
+    def num_free_cpu(self):
+        return _check(lib().pa_pool_num_free_cpu(self._h), "num_free_cpu")
+
+    def cpu_free_list(self):
+        import numpy as np
+        n = self.num_free_cpu()
+        out = np.zeros(max(n, 1), dtype=np.int32)
+        _check(lib().pa_pool_cpu_free_list(self._h, out.ctypes.data, n), "cpu_free_list")
+        return out[:n]
+
+    def cpu_refcount(self, block):
+        return _check(lib().pa_pool_cpu_refcount(self._h, int(block)), "cpu_refcount")

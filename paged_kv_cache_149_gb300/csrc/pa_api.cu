@@ -57,6 +57,21 @@ bool shape_ok(int num_kv_heads, int head_dim, int block_size) {
          (block_size == 8 || block_size == 16 || block_size == 32);
 }
 
+// The address a kernel uses for p: p itself for device or managed memory, the mapped
+// device address for page-locked host memory registered with CUDA, NULL otherwise.
+void* device_view(const void* p) {
+  if (!p) return nullptr;
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged)
+    return const_cast<void*>(p);
+  if (a.type == cudaMemoryTypeHost) return a.devicePointer;
+  return nullptr;
+}
+
 }  // namespace
 
 namespace pa {
@@ -85,6 +100,7 @@ const char* pa_status_string(int status) {
     case PA_ERR_CUDA: return "CUDA runtime error";
     case PA_ERR_POOL_EXHAUSTED: return "block pool exhausted";
     case PA_ERR_UNKNOWN_SEQ: return "unknown (or already live) sequence id";
+    case PA_ERR_WRONG_TIER: return "sequence is in the other pool (swapped out / resident)";
     default: return status > 0 ? "ok (positive result)" : "unknown status";
   }
 }
@@ -244,6 +260,28 @@ int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* block_mapping, i
   if (!device_info(&di)) return PA_ERR_CUDA;
   return pa::copy_blocks_launch(k_cache, v_cache, block_mapping, num_pairs, num_blocks,
                                 num_kv_heads, head_dim, block_size, di.err, stream);
+}
+
+int pa_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_v,
+                   const int32_t* block_mapping, int num_pairs, int src_num_blocks,
+                   int dst_num_blocks, int num_kv_heads, int head_dim, int block_size,
+                   pa_dtype dtype, cudaStream_t stream) {
+  if (num_pairs < 0 || src_num_blocks < 1 || dst_num_blocks < 1 ||
+      !shape_ok(num_kv_heads, head_dim, block_size) || (dtype != PA_FP16 && dtype != PA_BF16))
+    return PA_ERR_ARG;
+  if (num_pairs == 0) return PA_OK;
+  const void* ptrs[5] = {src_k, src_v, dst_k, dst_v, block_mapping};
+  void* dev[5];
+  for (int i = 0; i < 5; ++i) {
+    dev[i] = device_view(ptrs[i]);
+    if (!dev[i]) return PA_ERR_ARG;
+    if (i < 4 && !aligned16(dev[i])) return PA_ERR_ARG;
+  }
+  DeviceInfo di;
+  if (!device_info(&di)) return PA_ERR_CUDA;
+  return pa::swap_blocks_launch(dev[0], dev[1], dev[2], dev[3], static_cast<const int32_t*>(dev[4]),
+                                num_pairs, src_num_blocks, dst_num_blocks, num_kv_heads, head_dim,
+                                block_size, di.err, stream);
 }
 
 int pa_check_block_mapping(const int32_t* host_block_mapping, int num_pairs, int num_blocks) {

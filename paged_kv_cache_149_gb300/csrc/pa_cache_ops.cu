@@ -5,6 +5,10 @@
 // 分配策略): k_cache[slot / B, h, slot % B, :] = key[i, h, :].
 // copy_blocks: the copy behind copy-on-write of a still-shared last block (chenyuan1125,
 // section 一块内存，如何安全地属于多条序列; horeb.top, section 内存共享：写时复制).
+// swap_blocks: a preempted request's blocks move whole to CPU memory and back (aiqz.cc
+// "vLLM PagedAttention engine", section 连续批处理：随到随走的新秩序).  The same block
+// copy serves both: copy_blocks within one pool, swap_blocks between a device pool and a
+// page-locked host pool that the GPU reads and writes directly over NVLink-C2C.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -45,26 +49,53 @@ __global__ void __launch_bounds__(128) reshape_and_cache_kernel(
   }
 }
 
-// grid = (pairs, chunks of a block, 2 caches).  A pair with an id outside the pool is
-// skipped and flagged.
-__global__ void __launch_bounds__(256) copy_blocks_kernel(uint4* __restrict__ k_cache,
-                                                          uint4* __restrict__ v_cache,
-                                                          const int32_t* __restrict__ mapping,
-                                                          int num_blocks, size_t block_vecs,
-                                                          unsigned* err) {
+constexpr int kCopyThreads = 256;
+constexpr int kCopyUnroll = 4;  // 16-byte loads in flight per thread before its stores
+
+// grid = (pairs, chunks of a block, 2 caches): block mapping[p][1] of the destination
+// pool := block mapping[p][0] of the source pool.  Each thread has kCopyUnroll loads in
+// flight (host memory across the chip-to-chip link answers slower than HBM).  The source
+// and destination blocks of a pair never overlap (distinct pools, or, within one pool, a
+// checked pair list).  A pair with an id outside its pool is skipped and flagged.
+__global__ void __launch_bounds__(kCopyThreads) block_copy_kernel(
+    const uint4* __restrict__ src_k, const uint4* __restrict__ src_v, uint4* __restrict__ dst_k,
+    uint4* __restrict__ dst_v, const int32_t* __restrict__ mapping, int src_blocks,
+    int dst_blocks, size_t block_vecs, unsigned* err) {
   const int pair = blockIdx.x;
   const int src = mapping[2 * pair];
   const int dst = mapping[2 * pair + 1];
-  if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+  if (src < 0 || src >= src_blocks || dst < 0 || dst >= dst_blocks) {
     if (threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) atomicOr(err, kErrBadPair);
     return;
   }
-  uint4* cache = blockIdx.z == 0 ? k_cache : v_cache;
-  const uint4* s = cache + static_cast<size_t>(src) * block_vecs;
-  uint4* d = cache + static_cast<size_t>(dst) * block_vecs;
-  for (size_t j = static_cast<size_t>(blockIdx.y) * blockDim.x + threadIdx.x; j < block_vecs;
-       j += static_cast<size_t>(gridDim.y) * blockDim.x)
-    d[j] = s[j];
+  const uint4* s = (blockIdx.z == 0 ? src_k : src_v) + static_cast<size_t>(src) * block_vecs;
+  uint4* d = (blockIdx.z == 0 ? dst_k : dst_v) + static_cast<size_t>(dst) * block_vecs;
+  const size_t step = static_cast<size_t>(gridDim.y) * kCopyThreads;
+  for (size_t j0 = static_cast<size_t>(blockIdx.y) * kCopyThreads + threadIdx.x; j0 < block_vecs;
+       j0 += step * kCopyUnroll) {
+    uint4 v[kCopyUnroll];
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u)
+      if (j0 + u * step < block_vecs) v[u] = s[j0 + u * step];
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u)
+      if (j0 + u * step < block_vecs) d[j0 + u * step] = v[u];
+  }
+}
+
+int block_copy_launch(const void* src_k, const void* src_v, void* dst_k, void* dst_v,
+                      const int32_t* mapping, int num_pairs, int src_blocks, int dst_blocks,
+                      int num_kv_heads, int head_dim, int block_size, unsigned* err,
+                      cudaStream_t stream) {
+  if (num_pairs == 0) return 0;
+  const size_t block_vecs = static_cast<size_t>(num_kv_heads) * block_size * head_dim / 8;
+  const size_t per_cta = static_cast<size_t>(kCopyThreads) * kCopyUnroll;
+  int chunks = static_cast<int>((block_vecs + per_cta - 1) / per_cta);
+  if (chunks > 64) chunks = 64;
+  block_copy_kernel<<<dim3(num_pairs, chunks, 2), kCopyThreads, 0, stream>>>(
+      static_cast<const uint4*>(src_k), static_cast<const uint4*>(src_v), static_cast<uint4*>(dst_k),
+      static_cast<uint4*>(dst_v), mapping, src_blocks, dst_blocks, block_vecs, err);
+  return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
 }  // namespace
@@ -94,14 +125,16 @@ int reshape_and_cache_launch(const void* key, const void* value, void* k_cache, 
 int copy_blocks_launch(void* k_cache, void* v_cache, const int32_t* block_mapping, int num_pairs,
                        int num_blocks, int num_kv_heads, int head_dim, int block_size,
                        unsigned* err, cudaStream_t stream) {
-  if (num_pairs == 0) return 0;
-  const size_t block_vecs = static_cast<size_t>(num_kv_heads) * block_size * head_dim / 8;
-  int chunks = static_cast<int>((block_vecs + 255) / 256);
-  if (chunks > 32) chunks = 32;
-  copy_blocks_kernel<<<dim3(num_pairs, chunks, 2), 256, 0, stream>>>(
-      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), block_mapping, num_blocks,
-      block_vecs, err);
-  return cudaGetLastError() == cudaSuccess ? 0 : -3;
+  return block_copy_launch(k_cache, v_cache, k_cache, v_cache, block_mapping, num_pairs,
+                           num_blocks, num_blocks, num_kv_heads, head_dim, block_size, err, stream);
+}
+
+int swap_blocks_launch(const void* src_k, const void* src_v, void* dst_k, void* dst_v,
+                       const int32_t* block_mapping, int num_pairs, int src_num_blocks,
+                       int dst_num_blocks, int num_kv_heads, int head_dim, int block_size,
+                       unsigned* err, cudaStream_t stream) {
+  return block_copy_launch(src_k, src_v, dst_k, dst_v, block_mapping, num_pairs, src_num_blocks,
+                           dst_num_blocks, num_kv_heads, head_dim, block_size, err, stream);
 }
 
 }  // namespace pa

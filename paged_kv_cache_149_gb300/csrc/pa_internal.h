@@ -57,6 +57,10 @@ int reshape_and_cache_launch(const void* key, const void* value, void* k_cache, 
 int copy_blocks_launch(void* k_cache, void* v_cache, const int32_t* block_mapping, int num_pairs,
                        int num_blocks, int num_kv_heads, int head_dim, int block_size,
                        unsigned* err, cudaStream_t stream);
+int swap_blocks_launch(const void* src_k, const void* src_v, void* dst_k, void* dst_v,
+                       const int32_t* block_mapping, int num_pairs, int src_num_blocks,
+                       int dst_num_blocks, int num_kv_heads, int head_dim, int block_size,
+                       unsigned* err, cudaStream_t stream);
 
 // Raise a kernel's dynamic shared-memory limit once per device; false on failure.
 bool ensure_smem_attr(const void* func, size_t bytes);
