@@ -19,6 +19,12 @@ Test infrastructure only.  The steps, in the pages' order:
   blocks stay shared (chenyuan1125, section 一块内存…; horeb.top, section 内存共享).
 * When the pool is exhausted the request is rejected rather than the process failing
   (daiw.org, section 速查卡, 运维提示; the demo's allocate returns False).
+* Automatic prefix caching: a full block is identified by its parent block's hash, its
+  own tokens and extra keys (LoRA, multimodal inputs, a cache salt), so that a new
+  request whose prompt starts with the same blocks finds and reuses their K/V instead of
+  recomputing them (chenyuan1125 "vllm-pagedattention", section 一块内存，如何安全地属于
+  多条序列); which cached blocks to keep is an eviction policy, and a per-tenant salt
+  keeps tenants' prefixes apart (same page, section 分页不是免费午餐).
 * Preemption: when device memory runs short, a request's blocks can be moved out whole
   into CPU memory and moved back once room returns; the block table is what makes the
   move cheap (aiqz.cc, section 连续批处理：随到随走的新秩序).  The CPU side is a second
@@ -36,9 +42,22 @@ Readings where the pages are silent:
   order.  swap_in is the mirror image.  A block also held outside the group keeps its
   other references where it is (the group then owns a separate copy);
 * a swapped-out sequence can be freed (its CPU blocks return to the CPU tail) or swapped
-  in, but not grown or forked.
+  in, but not grown or forked;
+* prefix hashing: digest_i = SHA-256(digest_{i-1} || B as u32 || the block's B tokens as
+  i32 || len(extra) as u32 || extra), all little-endian, digest_{-1} = 32 zero bytes;
+  the request's extra bytes (salt, adapter id, ...) enter every block;
+* a prompt's lookup walks its full blocks in order and stops at the first miss; a hit
+  adds a reference (a cached block sitting in the free list leaves it); the rest of the
+  prompt gets fresh blocks from the head, and every full block among them is registered
+  under its digest unless that digest already names a block;
+* a cached block whose count reaches zero stays cached in the free list (eviction order =
+  free-list order); it is evicted -- its digest forgotten -- when it is taken from the
+  head for any other use.  Partly filled blocks and blocks filled by decode are not
+  registered.
 """
+import hashlib
 import math
+import struct
 
 
 class PoolExhausted(Exception):
@@ -51,6 +70,20 @@ class UnknownSequence(KeyError):
 
 class WrongTier(Exception):
     """The sequence is swapped out where a resident one is needed, or the reverse."""
+
+
+def block_hashes(tokens, block_size, extra=b""):
+    """Chained SHA-256 digests of the full blocks of a token list (hashlib)."""
+    tokens = [int(t) for t in tokens]
+    extra = bytes(extra)
+    out, parent = [], bytes(32)
+    for i in range(len(tokens) // block_size):
+        blk = tokens[i * block_size:(i + 1) * block_size]
+        msg = (parent + struct.pack("<I", block_size) + struct.pack(f"<{block_size}i", *blk)
+               + struct.pack("<I", len(extra)) + extra)
+        parent = hashlib.sha256(msg).digest()
+        out.append(parent)
+    return out
 
 
 def _order(n, order):
@@ -73,6 +106,8 @@ class BlockPool:
         self.tables = {}                # seq id -> list of block ids (CPU ids if swapped)
         self.ctx = {}                   # seq id -> tokens held
         self.swapped = set()            # seq ids whose blocks are in the CPU pool
+        self.digest_of = [None] * num_blocks   # device block -> its registered digest
+        self.cached = {}                # digest -> device block
 
     # -- queries ------------------------------------------------------------------------
     def num_free(self):
@@ -106,7 +141,47 @@ class BlockPool:
         del self.free_list[:n]
         for b in blocks:
             self.refcount[b] = 1
+            self._evict(b)
         return blocks
+
+    def _evict(self, b):
+        if self.digest_of[b] is not None:
+            del self.cached[self.digest_of[b]]
+            self.digest_of[b] = None
+
+    def num_cached(self):
+        return len(self.cached)
+
+    def allocate_prefix(self, seq, tokens, extra=b""):
+        """Prefill with prefix caching: reuse the cached blocks of the longest run of
+        leading full blocks, take fresh blocks for the rest, register the new full blocks.
+        Returns the number of leading tokens whose K/V are already cached."""
+        if seq in self.tables:
+            raise UnknownSequence(f"sequence {seq} already live")
+        n = len(tokens)
+        digests = block_hashes(tokens, self.block_size, extra)
+        hits = []
+        for dg in digests:
+            if dg not in self.cached:
+                break
+            hits.append(self.cached[dg])
+        need = math.ceil(n / self.block_size) - len(hits)
+        revived = sum(1 for b in hits if self.refcount[b] == 0)
+        if need > len(self.free_list) - revived:
+            raise PoolExhausted(f"need {need} blocks, {len(self.free_list) - revived} free")
+        for b in hits:
+            if self.refcount[b] == 0:
+                self.free_list.remove(b)
+            self.refcount[b] += 1
+        fresh = self._take(need)
+        table = hits + fresh
+        for i in range(len(hits), len(digests)):
+            if digests[i] not in self.cached:
+                self.cached[digests[i]] = table[i]
+                self.digest_of[table[i]] = digests[i]
+        self.tables[seq] = table
+        self.ctx[seq] = n
+        return len(hits) * self.block_size
 
     def allocate(self, seq, n_tokens):
         """Prefill: give a new sequence ceil(n_tokens / B) blocks holding n_tokens tokens."""
@@ -193,6 +268,9 @@ class BlockPool:
             raise PoolExhausted(f"need {len(refs)} blocks, {len(dst_free)} free")
         new = dict(zip(refs, dst_free[:len(refs)]))
         del dst_free[:len(refs)]
+        if not to_cpu:
+            for b in new.values():
+                self._evict(b)
         for b, n in refs.items():
             dst_ref[new[b]] = n
             src_ref[b] -= n
