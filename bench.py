@@ -23,6 +23,7 @@ collective on the data path, only a barrier and a max-reduce of the elapsed time
 """
 import argparse
 import hashlib
+import itertools
 import json
 import os
 import subprocess
@@ -801,6 +802,313 @@ def swap_line(args, res, world):
     }
 
 
+PREFIX_WORKLOADS = ("prefix_llama31_8b", "prefix_tiny")
+
+
+def run_gpu_prefix(args, rank, world, local_rank):
+    """Serving prompts that share a system prompt, warm prefix cache.  A step serves every
+    request of the batch: the C++ pool looks up each prompt's full blocks by digest
+    (pa_pool_allocate_prefix), one pa_reshape_and_cache writes the K/V rows of the
+    tokens not found cached, one pa_prefill computes attention for those tokens over
+    their whole context, and the requests end (their blocks stay cached in the free
+    list).  The same batch served without the cache (every token written and
+    prefilled) is timed beside it.  Host planning is inside the timed region; inputs
+    (the new tokens' q and K/V rows, as a model's projection would produce them) are
+    resident, and again from pinned host memory for the end-to-end number."""
+    import torch
+
+    import paged_kv_cache_149_gb300 as pa
+    import workloads
+    from paged_kv_cache_149_gb300 import build as _build
+
+    _build.build()
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    wl = workloads.RECIPES[args.workload]()
+    dt = {"fp16": torch.float16, "bf16": torch.bfloat16}[wl.dtype]
+    n, T, B = wl.num_seqs, wl.max_blocks_per_seq, wl.block_size
+    L = wl.context_lens.astype(np.int64)
+    toks = [wl.tokens[int(wl.seq_start[s]):int(wl.seq_start[s + 1])] for s in range(n)]
+    hit = (wl.system_len // B) * B
+    own = L - hit
+
+    def up(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(dt)
+
+    def rows_of(arr, first):   # rows first_s .. end of every request, concatenated
+        return np.concatenate([arr[int(wl.seq_start[s]) + int(first[s]):int(wl.seq_start[s + 1])]
+                               for s in range(n)])
+    shape = (wl.num_blocks, wl.num_kv_heads, B, wl.head_dim)
+    ctx = torch.from_numpy(L.astype(np.int32)).to(device)
+    arms = {}
+    for name, first in (("cached", np.full(n, hit)), ("uncached", np.zeros(n, np.int64))):
+        cnt = L - first
+        qs = np.zeros(n + 1, dtype=np.int32)
+        np.cumsum(cnt, out=qs[1:])
+        qsel = np.concatenate([np.arange(wl.query_start[s] + first[s], wl.query_start[s + 1])
+                               for s in range(n)])
+        # each arm has its own pool and caches: the uncached arm must not evict or
+        # overwrite what the cached arm has cached
+        arms[name] = {"first": first, "qs": torch.from_numpy(qs).to(device),
+                      "q": up(wl.q[qsel]), "k": up(rows_of(wl.keys, first)),
+                      "v": up(rows_of(wl.values, first)), "maxq": int(cnt.max()),
+                      "rows": int(cnt.sum()),
+                      "pool": pa.BlockPool(wl.num_blocks, B, wl.free_order),
+                      "kc": torch.zeros(shape, dtype=dt, device=device),
+                      "vc": torch.zeros(shape, dtype=dt, device=device)}
+        arms[name]["out"] = torch.empty_like(arms[name]["q"])
+    stream = torch.cuda.Stream(device)
+    bufs = [{"slots": torch.zeros(int(L.sum()), dtype=torch.int64).pin_memory(),
+             "tables": torch.zeros((n, T), dtype=torch.int32).pin_memory(),
+             "ev": torch.cuda.Event()} for _ in range(2)]
+    dslots = torch.zeros(int(L.sum()), dtype=torch.int64, device=device)
+    dtables = torch.zeros((n, T), dtype=torch.int32, device=device)
+    vocab = 128256
+    base_tokens = np.ascontiguousarray(wl.tokens, dtype=np.int64)
+    own_mask = np.ones(len(base_tokens), dtype=bool)
+    for s in range(n):
+        own_mask[int(wl.seq_start[s]):int(wl.seq_start[s]) + wl.system_len] = False
+    token_start = wl.seq_start.astype(np.int64)
+    ids = np.arange(n, dtype=np.int64)
+    step_tokens = np.zeros(len(base_tokens), dtype=np.int32)
+
+    def prompts(i):
+        """The batch of step i: every request is the shared system prompt followed by its
+        own tokens, new ones every step (new requests, not repeats of earlier ones)."""
+        np.copyto(step_tokens, np.where(own_mask, (base_tokens + 7919 * (i + 1)) % vocab,
+                                        base_tokens).astype(np.int32))
+        return step_tokens
+
+    fresh = itertools.count()
+    cached_out = np.zeros(n, dtype=np.int32)
+
+    def serve(arm, i, host_inputs=None):
+        a = arms[arm]
+        pool, kc, vc = a["pool"], a["kc"], a["vc"]
+        buf = bufs[i % 2]
+        buf["ev"].synchronize()          # the copy that last read this buffer is done
+        slots, tables = buf["slots"].numpy(), buf["tables"].numpy()
+        if arm == "cached":
+            # one call: digests of every request (in parallel), lookups, allocation,
+            # slots of the uncached tokens and the block tables
+            _, sl, _ = pool.allocate_prefix_batch(ids, prompts(next(fresh)), token_start,
+                                                  table_width=T,
+                                                  out=(cached_out, slots, tables))
+            if not np.array_equal(cached_out, a["first"]):
+                raise RuntimeError(f"cached tokens {cached_out.tolist()}, expected {a['first'][0]}")
+            o = len(sl)
+        else:
+            o = 0
+            for s in range(n):
+                pool.allocate(s, int(L[s]))
+                slots[o:o + int(L[s])] = pool.slots(s, 0, int(L[s]))
+                o += int(L[s])
+                t = pool.block_table(s)
+                tables[s, :len(t)] = t
+        with torch.cuda.stream(stream):
+            dslots[:o].copy_(buf["slots"][:o], non_blocking=True)
+            dtables.copy_(buf["tables"], non_blocking=True)
+            buf["ev"].record(stream)
+            q, k, v = a["q"], a["k"], a["v"]
+            if host_inputs is not None:
+                hq, hk, hv, hout = host_inputs[arm]
+                q.copy_(hq, non_blocking=True)
+                k.copy_(hk, non_blocking=True)
+                v.copy_(hv, non_blocking=True)
+        pa.reshape_and_cache(k, v, kc, vc, dslots[:o], stream=stream)
+        pa.prefill(q, kc, vc, dtables, ctx, a["qs"], wl.scale, a["maxq"], out=a["out"],
+                   stream=stream)
+        if host_inputs is not None:
+            with torch.cuda.stream(stream):
+                host_inputs[arm][3].copy_(a["out"], non_blocking=True)
+        pool.free_batch(ids)
+
+    def timed(arm, K, host_inputs=None):
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        w0 = time.perf_counter()
+        e0.record(stream)
+        for i in range(K):
+            serve(arm, i, host_inputs)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        return (time.perf_counter() - w0) * 1e3 / K, e0.elapsed_time(e1) / K
+
+    # cold pass: the first request finds nothing cached and writes every row; the system
+    # prompt's full blocks are cached from then on
+    ca, ua = arms["cached"], arms["uncached"]   # ua's k / v hold every row of every request
+    slot_all = []
+    first_prompts = np.ascontiguousarray(base_tokens.astype(np.int32))
+    for s in range(n):
+        c = ca["pool"].allocate_prefix(s, first_prompts[int(token_start[s]):int(token_start[s + 1])])
+        sl = np.full(int(L[s]), -1, dtype=np.int64)
+        sl[c:] = ca["pool"].slots(s, c, int(L[s]) - c)
+        slot_all.append(sl)
+    pa.reshape_and_cache(ua["k"], ua["v"], ca["kc"], ca["vc"],
+                         torch.from_numpy(np.concatenate(slot_all)).to(device), stream=stream)
+    for s in range(n):
+        ca["pool"].free(s)
+    torch.cuda.synchronize(device)
+    pa.get_device_error()
+    for arm in ("cached", "uncached"):
+        for i in range(args.warmup):
+            serve(arm, i)
+    # kernel-only: the prefill launch of a cached step, timed alone on its planned inputs
+    K = args.steps
+    serve("cached", K + 1)
+    torch.cuda.synchronize(device)
+    kev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    kev[0].record(stream)
+    for i in range(K):
+        pa.prefill(ca["q"], ca["kc"], ca["vc"], dtables, ctx, ca["qs"], wl.scale, ca["maxq"],
+                   out=ca["out"], stream=stream)
+    kev[1].record(stream)
+    torch.cuda.synchronize(device)
+    prefill_ms = kev[0].elapsed_time(kev[1]) / K
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.time()
+    cached_ms, cached_dev_ms = timed("cached", K)
+    t1 = time.time()
+    clocks = sampler.stop(t0, t1) if sampler else None
+    uncached_ms, _ = timed("uncached", max(3, K // 4))
+    # the host planning of a cached step alone (digests, lookups, slots, tables, free)
+    hb = bufs[0]
+    h0 = time.perf_counter()
+    for _ in range(20):
+        ca["pool"].allocate_prefix_batch(ids, prompts(next(fresh)), token_start, table_width=T,
+                                         out=(cached_out, hb["slots"].numpy(), hb["tables"].numpy()))
+        ca["pool"].free_batch(ids)
+    planning_us = (time.perf_counter() - h0) * 1e6 / 20
+    host = {}
+    for arm in arms:
+        x = arms[arm]
+        host[arm] = tuple(t.cpu().pin_memory() for t in (x["q"], x["k"], x["v"], x["out"]))
+    e2e_ms, _ = timed("cached", max(3, min(K, 20)), host)
+    flags = pa.get_device_error(stream=stream)
+    h = host["cached"]
+    return {"wl": wl, "total_ms": cached_ms * K, "decode_ms": prefill_ms,
+            "two_calls_ms": uncached_ms, "e2e_ms": e2e_ms, "cached_dev_ms": cached_dev_ms,
+            "h2d": sum(t.numel() * t.element_size() for t in h[:3]) + int(own.sum()) * 8 + n * T * 4,
+            "d2h": h[3].numel() * h[3].element_size(), "hit": hit,
+            "rows": ca["rows"], "clocks": clocks, "flags": flags, "planning_us": planning_us}
+
+
+def oracle_prefix_sample(name, budget_s):
+    """The oracle serving request 1 of the batch warm: its pool finds the system prompt
+    cached (request 0 placed first), then its prefill computes the first k own tokens
+    over the cached prefix, k doubled while the single-threaded run stays within budget.
+    Tokens served = the cached prefix + k."""
+    code = f"""
+import json, sys, time
+sys.path.insert(0, {ROOT!r})
+import numpy as np
+import workloads
+from oracle import cache_ops, prefill
+from oracle.block_pool import BlockPool
+wl = workloads.RECIPES[{name!r}]()
+B = wl.block_size
+toks = [wl.tokens[int(wl.seq_start[s]):int(wl.seq_start[s + 1])] for s in range(2)]
+k = 16
+while True:
+    t0 = time.process_time()
+    pool = BlockPool(wl.num_blocks, B, wl.free_order)
+    shape = (wl.num_blocks, wl.num_kv_heads, B, wl.head_dim)
+    kc = np.zeros(shape, np.uint16); vc = np.zeros(shape, np.uint16)
+    pool.allocate_prefix(0, toks[0])
+    a = int(wl.seq_start[0])
+    kc, vc = cache_ops.reshape_and_cache(kc, vc, wl.keys[a:a + len(toks[0])],
+                                         wl.values[a:a + len(toks[0])],
+                                         np.array([pool.slot(0, i) for i in range(len(toks[0]))]))
+    t = time.process_time()
+    c = pool.allocate_prefix(1, toks[1][:wl.system_len + k])
+    a = int(wl.seq_start[1])
+    kc, vc = cache_ops.reshape_and_cache(kc, vc, wl.keys[a + c:a + c + k], wl.values[a + c:a + c + k],
+                                         np.array([pool.slot(1, c + i) for i in range(k)]))
+    tab = np.array([pool.block_table(1)], dtype=np.int32)
+    q = wl.q[int(wl.query_start[1]) + c:int(wl.query_start[1]) + c + k]
+    prefill.paged_prefill(q, kc, vc, tab, np.array([c + k], np.int32), np.array([0, k]),
+                          wl.scale, B, wl.dtype)
+    dt = time.process_time() - t
+    if dt * 4 > {budget_s} or c + k >= len(toks[1]):
+        break
+    k *= 2
+print(json.dumps({{"tokens": c + k, "own": k, "seconds": dt}}))
+"""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
+    if r.returncode != 0:
+        raise RuntimeError("prefix oracle baseline failed:\n" + r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def prefix_line(args, res, world):
+    wl = res["wl"]
+    n = wl.num_seqs
+    tokens = int(wl.context_lens.sum())
+    step_s = res["total_ms"] / 1e3 / args.steps
+    value = world * tokens / step_s
+    # FLOPs of the prefill launch: each uncached row at position p scores p + 1 keys
+    flops = 0
+    for s in range(n):
+        c, L = res["hit"], int(wl.context_lens[s])
+        flops += (L - c) * (L + c + 1) // 2
+    flops *= 4 * wl.head_dim * wl.num_q_heads
+    achieved = flops / (res["decode_ms"] / 1e3) / 1e12
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak, kind = float(json.load(f)["bf16_tflops"]), "measured (cuBLAS bf16, burst)"
+    except (OSError, KeyError, ValueError):
+        peak, kind = 1900.0, "fallback"
+    uncached = world * tokens / (res["two_calls_ms"] / 1e3)
+    cpu = oracle_prefix_sample(args.workload, args.cpu_baseline_seconds) \
+        if args.cpu_baseline_seconds > 0 else None
+    return {
+        "metric": "prompt tokens served per second with a warm prefix cache (shared system "
+                  "prompt; host lookup + cache write + paged prefill of the uncached tokens)",
+        "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(res["total_ms"] / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "data": "synthetic (seeded normals and token ids; no dataset or weights)",
+        "config": {
+            "workload": (f"{wl.name}: {n} requests x ({wl.system_len} shared + "
+                         f"{int(wl.context_lens[0]) - wl.system_len} own tokens), "
+                         f"{wl.num_q_heads} q / {wl.num_kv_heads} kv heads, head_dim "
+                         f"{wl.head_dim}, block_size {wl.block_size}; {res['hit']} tokens of "
+                         "each prompt found cached"),
+            "l2": "no flush: the shared system prompt's K/V (a few MB) stays in L2 across "
+                  "steps, as it does in serving; each step's new rows are written fresh",
+            "parallelism": f"replicas x{world}",
+        },
+        "host_planning_us": round(res["planning_us"], 1),
+        "uncached": {"value": round(uncached, 1), "unit": "tokens/s",
+                     "ms_per_step": round(res["two_calls_ms"], 4),
+                     "speedup_from_cache": round(value / uncached, 3)},
+        "roofline": {"bound": "tensor", "kernel": "prefill_kernel (pa_prefill, uncached rows)",
+                     "achieved": round(achieved, 2), "peak": peak, "peak_kind": kind,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "prefill_us": round(1e3 * res["decode_ms"], 2),
+                     "device_ms_per_step": round(res["cached_dev_ms"], 4)},
+        "cpu_baseline": None if cpu is None else {
+            "value": round(cpu["tokens"] / cpu["seconds"], 1), "unit": "tokens/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"the oracle pool and float64 prefill oracle serving request 1 warm: "
+                      f"{cpu['tokens'] - cpu['own']} tokens found cached, {cpu['own']} own "
+                      "tokens written and prefilled, single thread"},
+        "e2e": {"value": round(world * tokens / (res["e2e_ms"] / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
+                "us_per_step": round(1e3 * res["e2e_ms"], 2)},
+        "clocks": res["clocks"],
+        "gpu_launches": 2 * args.steps,
+        "device_error_flags": res["flags"],
+    }
+
+
 def max_over_ranks(values):
     """Element-wise maximum of per-rank floats over the process group (NCCL on GPUs, or any
     other backend on CPU tensors)."""
@@ -845,7 +1153,9 @@ def main(argv=None, runner=None, backend="nccl"):
         torch.distributed.init_process_group(backend)
     is_prefill = args.workload.startswith("prefill")
     is_swap = args.workload in SWAP_WORKLOADS
-    default_runner = run_gpu_prefill if is_prefill else (run_gpu_swap if is_swap else run_gpu)
+    is_prefix = args.workload in PREFIX_WORKLOADS
+    default_runner = (run_gpu_prefill if is_prefill else run_gpu_swap if is_swap else
+                      run_gpu_prefix if is_prefix else run_gpu)
     res = (runner or default_runner)(args, rank, world, local_rank)
     if world > 1:
         res.update(zip(RANK_TIMES, max_over_ranks([res[k] for k in RANK_TIMES])))
@@ -854,8 +1164,9 @@ def main(argv=None, runner=None, backend="nccl"):
             import torch
             torch.distributed.destroy_process_group()
         return
-    if is_prefill or is_swap:
-        print(json.dumps((prefill_line if is_prefill else swap_line)(args, res, world)))
+    if is_prefill or is_swap or is_prefix:
+        line = (prefill_line if is_prefill else swap_line if is_swap else prefix_line)
+        print(json.dumps(line(args, res, world)))
         if world > 1:
             import torch
             torch.distributed.destroy_process_group()

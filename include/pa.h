@@ -312,6 +312,57 @@ int pa_pool_num_free_cpu(const pa_pool* pool);
 int pa_pool_cpu_free_list(const pa_pool* pool, int32_t* out, int cap);
 int pa_pool_cpu_refcount(const pa_pool* pool, int32_t block);
 
+/*
+ * Automatic prefix caching.  A full block is named by its parent's digest, its tokens and
+ * the request's extra keys, so a prompt that starts with blocks already in the pool
+ * reuses their K/V and skips that part of prefill (chenyuan1125, section
+ * 一块内存，如何安全地属于多条序列); `extra` (a tenant's cache salt, an adapter id, ...)
+ * keeps requests that must not share apart (same page, section 分页不是免费午餐).
+ * Digest of full block i (SHA-256, FIPS 180-4; integers little-endian):
+ *   SHA-256(digest_{i-1} || B as u32 || tokens[iB .. iB+B-1] as i32 || extra_len as u32
+ *           || extra),   digest_{-1} = 32 zero bytes.
+ * The lookup walks the prompt's full blocks in order and stops at the first miss.  A hit
+ * adds a reference to the cached block (taking it out of the free list if its count was
+ * zero); the rest of the prompt gets blocks from the head of the free list, and each full
+ * block among them is registered under its digest unless the digest already names a
+ * block.  A cached block at count zero stays cached in the free list, so the free-list
+ * order is the eviction order; any block taken from the head loses its digest.  Partly
+ * filled blocks and blocks filled by decode are not registered.
+ */
+/* Prefill with prefix caching: a new sequence holding tokens[0 .. n_tokens-1] (host
+ * int32).  *cached_tokens_out (may be NULL) receives the number of leading tokens whose
+ * K/V the reused blocks already hold (a multiple of B); the caller computes and writes
+ * the rest.  Errors as pa_pool_allocate; on error nothing changes. */
+int pa_pool_allocate_prefix(pa_pool* pool, int64_t seq_id, const int32_t* tokens, int n_tokens,
+                            const uint8_t* extra, int extra_len, int* cached_tokens_out);
+/* A scheduler step's prompts in one call: requests r = 0..n-1 with ids seq_ids[r], tokens
+ * tokens[token_start[r] .. token_start[r+1]-1] and extra bytes extras[extra_start[r] ..
+ * extra_start[r+1]-1] (extras NULL: none), placed in order exactly as n calls of
+ * pa_pool_allocate_prefix would.  The digest chains of different requests are computed in
+ * parallel on a small pool of host threads (the library's own; batch calls are serialised
+ * on it).  Outputs: cached_out[n]; slots_out (may be NULL) the slots of every request's
+ * uncached tokens, request after request (what pa_reshape_and_cache takes for the new
+ * rows); tables_out (may be NULL) [n][table_width] block tables padded with 0.  On an
+ * error the requests before the failing one stay allocated: *n_done (may be NULL) says
+ * how many. */
+int pa_pool_allocate_prefix_batch(pa_pool* pool, int n, const int64_t* seq_ids,
+                                  const int32_t* tokens, const int64_t* token_start,
+                                  const uint8_t* extras, const int64_t* extra_start,
+                                  int* cached_out, int64_t* slots_out, int32_t* tables_out,
+                                  int table_width, int* n_done);
+/* pa_pool_free of n sequences in order; stops at the first error. */
+int pa_pool_free_batch(pa_pool* pool, const int64_t* seq_ids, int n);
+/* Number of blocks registered under a digest (in use or waiting in the free list). */
+int pa_pool_num_cached(const pa_pool* pool);
+/* 1 and the block's 32-byte digest, 0 if the block has none, or PA_ERR_ARG. */
+int pa_pool_block_digest(const pa_pool* pool, int32_t block, uint8_t* digest_out);
+/* The digests of the n_tokens / B full blocks of a token list into digests_out
+ * [cap][32]; returns their number (pure host function). */
+int pa_prefix_block_hashes(const int32_t* tokens, int n_tokens, int block_size,
+                           const uint8_t* extra, int extra_len, uint8_t* digests_out, int cap);
+/* SHA-256 of `len` bytes (FIPS 180-4) into digest_out[32]. */
+int pa_sha256(const void* data, size_t len, uint8_t* digest_out);
+
 #ifdef __cplusplus
 }
 #endif

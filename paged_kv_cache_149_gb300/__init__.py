@@ -81,6 +81,14 @@ SIGNATURES = {
     "pa_pool_num_free_cpu": (_i32, [_vp]),
     "pa_pool_cpu_free_list": (_i32, [_vp, _vp, _i32]),
     "pa_pool_cpu_refcount": (_i32, [_vp, _c.c_int32]),
+    "pa_pool_allocate_prefix": (_i32, [_vp, _i64, _vp, _i32, _vp, _i32, _c.POINTER(_c.c_int)]),
+    "pa_pool_num_cached": (_i32, [_vp]),
+    "pa_pool_allocate_prefix_batch": (_i32, [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                             _i32, _c.POINTER(_c.c_int)]),
+    "pa_pool_free_batch": (_i32, [_vp, _vp, _i32]),
+    "pa_pool_block_digest": (_i32, [_vp, _c.c_int32, _vp]),
+    "pa_prefix_block_hashes": (_i32, [_vp, _i32, _i32, _vp, _i32, _vp, _i32]),
+    "pa_sha256": (_i32, [_vp, _sz, _vp]),
 }
 
 _lib = None
@@ -365,6 +373,26 @@ def get_device_error(stream=None, device=None):
 
 # ------------------------------------------------------------------ block pool
 
+def sha256(data):
+    """SHA-256 digest of a bytes object, computed by the library (FIPS 180-4)."""
+    buf = ctypes.create_string_buffer(bytes(data), max(len(data), 1))
+    out = ctypes.create_string_buffer(32)
+    _check(lib().pa_sha256(buf, len(data), out), "pa_sha256")
+    return out.raw
+
+
+def block_hashes(tokens, block_size, extra=b""):
+    """The chained digests (list of 32-byte strings) of the full blocks of a token list."""
+    import numpy as np
+    tok = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+    m = len(tok) // int(block_size)
+    out = ctypes.create_string_buffer(32 * max(m, 1))
+    ex = bytes(extra)
+    n = _check(lib().pa_prefix_block_hashes(tok.ctypes.data, len(tok), int(block_size), ex or None,
+                                            len(ex), out, m), "pa_prefix_block_hashes")
+    return [out.raw[32 * i:32 * (i + 1)] for i in range(n)]
+
+
 class BlockPool:
     """Host block pool (C++): ordered free list, refcounts, fork, copy-on-write planning,
     and an optional CPU pool for swap-out / swap-in."""
@@ -475,3 +503,63 @@ class BlockPool:
 
     def cpu_refcount(self, block):
         return _check(lib().pa_pool_cpu_refcount(self._h, int(block)), "cpu_refcount")
+
+    def allocate_prefix(self, seq, tokens, extra=b""):
+        """Prefill with prefix caching; returns the number of leading tokens whose K/V
+        the reused blocks already hold."""
+        import numpy as np
+        tok = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        ex = bytes(extra)
+        cached = ctypes.c_int(0)
+        _check(lib().pa_pool_allocate_prefix(self._h, int(seq), tok.ctypes.data, len(tok),
+                                             ex or None, len(ex), ctypes.byref(cached)),
+               "allocate_prefix")
+        return cached.value
+
+    def num_cached(self):
+        return _check(lib().pa_pool_num_cached(self._h), "num_cached")
+
+    def block_digest(self, block):
+        out = ctypes.create_string_buffer(32)
+        st = _check(lib().pa_pool_block_digest(self._h, int(block), out), "block_digest")
+        return out.raw if st == 1 else None
+
+    def allocate_prefix_batch(self, seq_ids, tokens, token_start, extras=None, extra_start=None,
+                              table_width=None, out=None):
+        """Place a batch of prompts through the prefix cache in one call (see
+        pa_pool_allocate_prefix_batch).  tokens: int32 [total], token_start: int64 [n + 1].
+        Returns (cached [n] int32, slots of the uncached tokens int64, tables [n, width]
+        int32).  `out` may pass (cached, slots, tables) arrays to fill."""
+        import numpy as np
+        ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
+        n = ids.size
+        tok = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        ts = np.ascontiguousarray(np.asarray(token_start, dtype=np.int64))
+        _need(ts.shape == (n + 1,), "token_start must have n + 1 entries")
+        lens = np.diff(ts)
+        if table_width is None:
+            table_width = int(-(-lens.max() // self.block_size)) if n else 0
+        if out is None:
+            cached = np.zeros(n, dtype=np.int32)
+            slots = np.zeros(int(lens.sum()), dtype=np.int64)
+            tables = np.zeros((n, table_width), dtype=np.int32)
+        else:
+            cached, slots, tables = out
+        ex = es = None
+        if extras is not None:
+            ex = np.ascontiguousarray(np.frombuffer(bytes(extras), dtype=np.uint8)) if not \
+                isinstance(extras, np.ndarray) else np.ascontiguousarray(extras, dtype=np.uint8)
+            es = np.ascontiguousarray(np.asarray(extra_start, dtype=np.int64))
+        done = ctypes.c_int(0)
+        _check(lib().pa_pool_allocate_prefix_batch(
+            self._h, n, ids.ctypes.data, tok.ctypes.data, ts.ctypes.data,
+            None if ex is None else ex.ctypes.data, None if es is None else es.ctypes.data,
+            cached.ctypes.data, slots.ctypes.data, tables.ctypes.data, int(table_width),
+            ctypes.byref(done)), "allocate_prefix_batch")
+        used = int((lens - cached).sum())
+        return cached, slots[:used], tables
+
+    def free_batch(self, seq_ids):
+        import numpy as np
+        ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
+        _check(lib().pa_pool_free_batch(self._h, ids.ctypes.data, ids.size), "free_batch")

@@ -220,3 +220,127 @@ def test_random_operations_with_swaps_match_oracle(libpa, seed):
             ref.free(seq)
             native.free(seq)
         same_tiers(native, ref)
+
+
+def test_sha256_published_vectors_and_hashlib(libpa, golden):
+    import hashlib
+    for v in golden("sha256_vectors.json")["vectors"]:
+        assert libpa.sha256(v["ascii"].encode()).hex() == v["sha256"]
+    rng = np.random.default_rng(0)
+    for n in [1, 3, 55, 56, 57, 63, 64, 65, 119, 120, 127, 128, 129, 1000, 4099]:
+        data = rng.integers(0, 256, size=n, dtype=np.uint8).tobytes()
+        assert libpa.sha256(data) == hashlib.sha256(data).digest(), n
+
+
+@pytest.mark.parametrize("bs", [1, 4, 16])
+def test_block_hashes_match_oracle(libpa, bs):
+    from oracle.block_pool import block_hashes
+    rng = np.random.default_rng(bs)
+    for n in [0, bs - 1, bs, 5 * bs + 3]:
+        toks = rng.integers(-2 ** 31, 2 ** 31, size=n).tolist()
+        for extra in (b"", b"tenant-7", bytes(range(200))):
+            assert libpa.block_hashes(toks, bs, extra) == block_hashes(toks, bs, extra)
+
+
+def same_cache(native, ref):
+    same_tiers(native, ref)
+    assert native.num_cached() == ref.num_cached()
+    for b in range(ref.num_blocks):
+        assert native.block_digest(b) == ref.digest_of[b]
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_random_operations_with_prefix_caching_match_oracle(libpa, seed):
+    from oracle.block_pool import WrongTier
+    rng = random.Random(5000 + seed)
+    nb, bs = rng.choice([12, 24]), rng.choice([1, 2, 4])
+    order = rng.sample(range(nb), nb)
+    native = libpa.BlockPool(nb, bs, np.array(order), num_cpu_blocks=8)
+    ref = OraclePool(nb, bs, order, num_cpu_blocks=8)
+    errors = {PoolExhausted: libpa.PoolExhausted, WrongTier: libpa.WrongTier,
+              UnknownSequence: libpa.UnknownSequence}
+
+    def both(f_ref, f_nat, convert=lambda x: x):
+        try:
+            want = f_ref()
+        except tuple(errors) as e:
+            with pytest.raises(errors[type(e)]):
+                f_nat()
+            return
+        assert convert(f_nat()) == want
+    next_id = 0
+    stems = [[1] * 8, [2, 1] * 4, []]
+    for _ in range(150):
+        seqs = list(ref.tables)
+        op = rng.random()
+        if op < 0.35 or not seqs:
+            n = rng.randint(0, 4 * bs + 2)
+            toks = (rng.choice(stems) + [rng.randint(0, 2) for _ in range(n)])[:max(n, 1)]
+            extra = rng.choice([b"", b"", b"salt"])
+            both(lambda: ref.allocate_prefix(next_id, toks, extra),
+                 lambda: native.allocate_prefix(next_id, toks, extra))
+            next_id += 1
+        elif op < 0.45:
+            n = rng.randint(0, 2 * bs)
+            both(lambda: ref.allocate(next_id, n), lambda: native.allocate(next_id, n))
+            next_id += 1
+        elif op < 0.65:
+            seq = rng.choice(seqs)
+            both(lambda: ref.append_slot(seq), lambda: native.append_slot(seq))
+        elif op < 0.72:
+            parent = rng.choice(seqs)
+            both(lambda: ref.fork(parent, next_id), lambda: native.fork(parent, next_id))
+            next_id += 1
+        elif op < 0.85:
+            group = rng.sample(seqs, rng.randint(1, min(2, len(seqs))))
+            pairs = lambda x: [tuple(int(v) for v in p) for p in x]
+            if rng.random() < 0.5:
+                both(lambda: ref.swap_out(group), lambda: native.swap_out(group), pairs)
+            else:
+                both(lambda: ref.swap_in(group), lambda: native.swap_in(group), pairs)
+        else:
+            seq = rng.choice(seqs)
+            ref.free(seq)
+            native.free(seq)
+        same_cache(native, ref)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_batch_allocation_equals_sequential_calls(libpa, seed):
+    """One batched call (digests hashed in parallel) leaves the pool exactly as the same
+    requests placed one by one, and returns the same cached counts, slots and tables."""
+    rng = np.random.default_rng(seed)
+    nb, bs = 4096, rng.choice([4, 16])
+    order = rng.permutation(nb)
+    system = rng.integers(0, 1000, size=64 * bs).tolist()
+    batch, seq = libpa.BlockPool(nb, bs, order), libpa.BlockPool(nb, bs, order)
+    ref = OraclePool(nb, bs, order.tolist())
+    for rnd in range(3):
+        n = int(rng.integers(1, 20))
+        ids = [rnd * 100 + r for r in range(n)]
+        prompts = [(system[:int(rng.integers(0, len(system)))] +
+                    rng.integers(0, 1000, size=int(rng.integers(0, 5 * bs))).tolist())
+                   for _ in range(n)]
+        salts = [bytes([int(rng.integers(0, 2))]) * int(rng.integers(0, 3)) for _ in range(n)]
+        ts = np.zeros(n + 1, dtype=np.int64)
+        np.cumsum([len(p) for p in prompts], out=ts[1:])
+        es = np.zeros(n + 1, dtype=np.int64)
+        np.cumsum([len(x) for x in salts], out=es[1:])
+        cached, slots, tables = batch.allocate_prefix_batch(
+            ids, np.concatenate([np.asarray(p, np.int32) for p in prompts] + [np.zeros(0, np.int32)]),
+            ts, b"".join(salts), es, table_width=80)
+        want_slots = []
+        for r, (i, p, x) in enumerate(zip(ids, prompts, salts)):
+            c = seq.allocate_prefix(i, p, x)
+            assert c == cached[r] == ref.allocate_prefix(i, p, x)
+            want_slots.append(seq.slots(i, c, len(p) - c))
+            t = seq.block_table(i)
+            assert list(tables[r][:len(t)]) == list(t) and not tables[r][len(t):].any()
+        np.testing.assert_array_equal(slots, np.concatenate(want_slots))
+        same_cache(batch, ref)
+        drop = ids[::2]
+        batch.free_batch(drop)
+        for i in drop:
+            seq.free(i)
+            ref.free(i)
+        same_cache(batch, ref)

@@ -32,6 +32,15 @@ Prefill recipes (q holds every new token of every sequence; query_start marks th
                         rotate in disjoint blocks), shuffled
     prefill_chunked     16 seqs, ctx ~ U[1024, 4096], the last 512 tokens new (a chunk of
                         a longer prompt), otherwise as prefill_llama31_8b
+
+Shared-prefix prompts (prefix caching): every request starts with the same system
+prompt; the K/V rows of those positions are the same draw for every request (a model
+computes a position's K/V from the tokens up to it), the rest are drawn per request.
+Token ids are uniform over a 128256-entry vocabulary.
+    prefix_tiny         4 requests, system prompt 40 tokens, own tokens {5,17,33,1}, B=16,
+                        4 q / 2 kv heads, d=64, fp16
+    prefix_llama31_8b   16 requests, system prompt 1024 tokens, 512 own tokens each,
+                        32 q / 8 kv heads, d=128, bf16, B=16
 """
 from dataclasses import dataclass, field
 import math
@@ -222,6 +231,45 @@ def prefill_chunked(seed=0, num_seqs=16, chunk=512):
                     int(3.3 * sum(-(-int(c) // 16) for c in ctx)), 4096, 1.0 / math.sqrt(128))
 
 
+@dataclass
+class PrefixWorkload(PrefillWorkload):
+    """Prompts from scratch that share a system prompt: q holds every token of every
+    prompt; tokens holds their ids (int32 [sum(ctx)], same layout as keys)."""
+    tokens: np.ndarray = None
+    system_len: int = 0
+
+
+def _prefix(name, rng, system_len, own, dtype, hq, hkv, d, bsz, num_blocks, scale,
+            vocab=128256):
+    own = np.asarray(own, dtype=np.int32)
+    ctx = system_len + own
+    base = _prefill(name, rng, ctx, ctx, dtype, hq, hkv, d, bsz, num_blocks,
+                    int(-(-int(ctx.max()) // bsz) * bsz), scale)
+    sys_tok = rng.integers(0, vocab, size=system_len).astype(np.int32)
+    sys_k = normal_bits(rng, (system_len, hkv, d), 1.0, dtype)
+    sys_v = normal_bits(rng, (system_len, hkv, d), 1.0, dtype)
+    toks = []
+    for s in range(len(ctx)):
+        a = int(base.seq_start[s])
+        base.keys[a:a + system_len] = sys_k
+        base.values[a:a + system_len] = sys_v
+        toks.append(np.concatenate([sys_tok, rng.integers(0, vocab, size=int(own[s])).astype(np.int32)]))
+    fields = {k: getattr(base, k) for k in base.__dataclass_fields__}
+    return PrefixWorkload(**fields, tokens=np.concatenate(toks), system_len=system_len)
+
+
+def prefix_tiny(seed=0):
+    rng = np.random.default_rng(seed)
+    return _prefix("prefix_tiny", rng, 40, [5, 17, 33, 1], "fp16", 4, 2, 64, 16, 64,
+                   1.0 / math.sqrt(64))
+
+
+def prefix_llama31_8b(seed=0, num_reqs=16, system_len=1024, own=512):
+    rng = np.random.default_rng(seed)
+    return _prefix("prefix_llama31_8b", rng, system_len, [own] * num_reqs, "bf16", 32, 8, 128,
+                   16, 4 * num_reqs * ((system_len + own) // 16), 1.0 / math.sqrt(128))
+
+
 RECIPES = {
     "tiny": tiny,
     "llama31_8b": llama31_8b,
@@ -232,4 +280,6 @@ RECIPES = {
     "prefill_tiny": prefill_tiny,
     "prefill_llama31_8b": prefill_llama31_8b,
     "prefill_chunked": prefill_chunked,
+    "prefix_tiny": prefix_tiny,
+    "prefix_llama31_8b": prefix_llama31_8b,
 }
