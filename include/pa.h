@@ -47,7 +47,10 @@
 extern "C" {
 #endif
 
-typedef enum { PA_FP16 = 0, PA_BF16 = 1 } pa_dtype;
+/* PA_FP8_E4M3 names FP8 K/V blocks; it is accepted only where a call handles caches
+ * alone (pa_copy_blocks, pa_swap_blocks).  The FP8 decode and cache write take the
+ * 16-bit type of q / out / key / value instead. */
+typedef enum { PA_FP16 = 0, PA_BF16 = 1, PA_FP8_E4M3 = 2 } pa_dtype;
 
 enum {
   PA_OK = 0,
@@ -112,6 +115,36 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache,
               const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
               int head_dim, int block_size, int num_blocks, float scale, void* out,
               void* workspace, size_t workspace_bytes, pa_dtype dtype, cudaStream_t stream);
+
+/*
+ * FP8 KV blocks.  Paging does not reduce the bytes the cache needs; quantising the cached
+ * K/V does (daiw.org "Paged Attention", section 量化, callout; horeb.top, section 生态现状:
+ * serving engines store KV in FP8 or INT4).  Format: each cache element is an E4M3 code
+ * (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; exponent field 0 = subnormals
+ * m * 2^-9; no infinities; S.1111.111 is NaN; largest finite 448), in the same
+ * [num_blocks][Hkv][B][d] layout, one byte per element.  One float32 scale per cache: a
+ * code c means decode(c) * k_scale in the K cache and decode(c) * v_scale in the V cache.
+ * Scales are the caller's (calibrated or fixed); both must be finite and > 0.
+ */
+/* Quantising cache write: k_cache[slot / B, h, slot % B, :] = E4M3(key[i, h, :] / k_scale)
+ * (V likewise), the division in IEEE float32, rounding to nearest-even, magnitudes above
+ * 448 clamped to 448.  key / value are fp16 or bf16 (`dtype`); other rules as
+ * pa_reshape_and_cache. */
+int pa_reshape_and_cache_fp8(const void* key, const void* value, void* k_cache, void* v_cache,
+                             const int64_t* slot_mapping, int num_tokens, int num_blocks,
+                             int num_kv_heads, int head_dim, int block_size, float k_scale,
+                             float v_scale, pa_dtype dtype, cudaStream_t stream);
+/* pa_decode over FP8 blocks: z_t = scale * k_scale * <q, decode(K codes)>, out = v_scale *
+ * sum_t softmax(z)_t decode(V codes).  q and out are fp16 or bf16 (`dtype`).  The codes
+ * are widened to f16 exactly and multiplied on the tensor cores in f16 (bf16 queries are
+ * rounded to f16 for that product); accumulation fp32.  Same workspace, error and
+ * determinism rules as pa_decode; there is no fused cache write for FP8 blocks. */
+int pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
+                  const int32_t* block_tables, int max_blocks_per_seq,
+                  const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+                  int head_dim, int block_size, int num_blocks, float scale, float k_scale,
+                  float v_scale, void* out, void* workspace, size_t workspace_bytes,
+                  pa_dtype dtype, cudaStream_t stream);
 
 /*
  * pa_prefill -- causal multi-query attention of each sequence's newest tokens over its

@@ -39,6 +39,7 @@ DEVERR_TIMEOUT = 0x10
 
 PA_FP16 = 0
 PA_BF16 = 1
+PA_FP8_E4M3 = 2
 
 _c = ctypes
 _vp, _i32, _i64, _sz, _f32 = _c.c_void_p, _c.c_int, _c.c_int64, _c.c_size_t, _c.c_float
@@ -50,6 +51,10 @@ SIGNATURES = {
                          _f32, _vp, _vp, _sz, _i32, _vp]),
     "pa_decode_append": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
                                 _i32, _i32, _f32, _vp, _vp, _sz, _i32, _vp]),
+    "pa_decode_fp8": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
+                             _f32, _f32, _f32, _vp, _vp, _sz, _i32, _vp]),
+    "pa_reshape_and_cache_fp8": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
+                                        _f32, _f32, _i32, _vp]),
     "pa_prefill": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
                           _i32, _i32, _f32, _vp, _i32, _vp]),
     "pa_decode_workspace_size": (_sz, [_i32, _i32, _i32]),
@@ -154,6 +159,15 @@ def _dtype_code(t):
     if t.dtype == torch.bfloat16:
         return PA_BF16
     raise TypeError(f"unsupported dtype {t.dtype}; expected float16 or bfloat16")
+
+
+def _cache_code(t):
+    """dtype code of a K/V cache tensor: 16-bit floats, or FP8 E4M3 codes (uint8 or
+    torch.float8_e4m3fn)."""
+    import torch
+    if t.dtype in (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8)):
+        return PA_FP8_E4M3
+    return _dtype_code(t)
 
 
 def _stream_ptr(stream, device):
@@ -261,6 +275,55 @@ def decode_append(q, key_new, value_new, k_cache, v_cache, block_tables, context
     return out
 
 
+def _fp8_cache(t, name):
+    import torch
+    _need(t.dtype in (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8)),
+          f"{name} must hold E4M3 codes (uint8 or float8_e4m3fn), got {t.dtype}")
+    return _dev(t, name)
+
+
+def reshape_and_cache_fp8(key, value, k_cache, v_cache, slot_mapping, k_scale, v_scale,
+                          stream=None):
+    """FP8 cache write: k_cache[slot // B, h, slot % B] = E4M3(key[i, h] / k_scale) (and V)."""
+    import torch
+    n, hkv, d = key.shape
+    nb, hkv2, bs, d2 = k_cache.shape
+    _need(value.shape == key.shape and v_cache.shape == k_cache.shape, "shape mismatch")
+    _need(hkv == hkv2 and d == d2 and slot_mapping.shape == (n,), "shape mismatch")
+    _need(key.dtype == value.dtype, "dtype mismatch")
+    st = lib().pa_reshape_and_cache_fp8(
+        _dev(key, "key"), _dev(value, "value"), _fp8_cache(k_cache, "k_cache"),
+        _fp8_cache(v_cache, "v_cache"), _dev(slot_mapping, "slot_mapping", torch.int64), n, nb,
+        hkv, d, bs, float(k_scale), float(v_scale), _dtype_code(key),
+        _stream_ptr(stream, key.device))
+    _check(st, "pa_reshape_and_cache_fp8")
+
+
+def decode_fp8(q, k_cache, v_cache, block_tables, context_lens, scale, k_scale, v_scale,
+               out=None, workspace=None, stream=None):
+    """Paged decode over FP8 E4M3 blocks (codes times k_scale / v_scale); q and out are
+    fp16 or bf16."""
+    import torch
+    n, hq, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    _need(v_cache.shape == k_cache.shape and d == d2, "shape mismatch")
+    _need(block_tables.dim() == 2 and block_tables.shape[0] == n, "block_tables must be [num_seqs, T]")
+    _need(context_lens.shape == (n,), "context_lens must be [num_seqs]")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out.shape == q.shape and out.dtype == q.dtype, "out must match q")
+    if workspace is None:
+        workspace = make_workspace(hq, hkv, d, q.device)
+    st = lib().pa_decode_fp8(
+        _dev(q, "q"), _fp8_cache(k_cache, "k_cache"), _fp8_cache(v_cache, "v_cache"),
+        _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+        _dev(context_lens, "context_lens", torch.int32), n, hq, hkv, d, bs, nb, float(scale),
+        float(k_scale), float(v_scale), _dev(out, "out"), _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _dtype_code(q), _stream_ptr(stream, q.device))
+    _check(st, "pa_decode_fp8")
+    return out
+
+
 def prefill(q, k_cache, v_cache, block_tables, context_lens, query_start, scale,
             max_query_len, out=None, stream=None):
     """Causal attention of each sequence's newest tokens (q rows query_start[s] ..
@@ -320,7 +383,7 @@ def copy_blocks(k_cache, v_cache, block_mapping, stream=None):
     st = lib().pa_copy_blocks(
         _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
         _dev(block_mapping, "block_mapping", torch.int32), block_mapping.shape[0], nb, hkv, d, bs,
-        _dtype_code(k_cache), _stream_ptr(stream, k_cache.device))
+        _cache_code(k_cache), _stream_ptr(stream, k_cache.device))
     _check(st, "pa_copy_blocks")
 
 
@@ -349,7 +412,7 @@ def swap_blocks(src_k, src_v, dst_k, dst_v, block_mapping, stream=None, device=N
     st = lib().pa_swap_blocks(
         _reachable(src_k, "src_k"), _reachable(src_v, "src_v"), _reachable(dst_k, "dst_k"),
         _reachable(dst_v, "dst_v"), _reachable(block_mapping, "block_mapping", torch.int32),
-        block_mapping.shape[0], nbs, nbd, hkv, d, bs, _dtype_code(src_k),
+        block_mapping.shape[0], nbs, nbd, hkv, d, bs, _cache_code(src_k),
         _stream_ptr(stream, device))
     _check(st, "pa_swap_blocks")
 

@@ -139,7 +139,11 @@ int decode_call(const void* q, const void* key_new, const void* value_new, const
                 const void* v_cache, const int32_t* block_tables, int max_blocks_per_seq,
                 const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
                 int head_dim, int block_size, int num_blocks, float scale, void* out,
-                void* workspace, size_t workspace_bytes, pa_dtype dtype, cudaStream_t stream) {
+                void* workspace, size_t workspace_bytes, pa_dtype dtype, cudaStream_t stream,
+                bool kv_fp8 = false, float k_scale = 1.f, float v_scale = 1.f) {
+  if (kv_fp8 && (!std::isfinite(k_scale) || !std::isfinite(v_scale) || !(k_scale > 0.f) ||
+                 !(v_scale > 0.f)))
+    return PA_ERR_ARG;
   if (num_seqs < 0 || num_blocks < 1 || max_blocks_per_seq < 1 ||
       !shape_ok(num_kv_heads, head_dim, block_size) || num_q_heads < num_kv_heads ||
       num_q_heads % num_kv_heads != 0 || !std::isfinite(scale) ||
@@ -177,6 +181,9 @@ int decode_call(const void* q, const void* key_new, const void* value_new, const
   a.num_blocks = num_blocks;
   a.scale = scale;
   a.bf16 = dtype == PA_BF16;
+  a.kv_fp8 = kv_fp8;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
   a.err = di.err;
   return pa::decode_launch(a, di.sm_count, stream);
 }
@@ -191,6 +198,37 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache,
   return decode_call(q, nullptr, nullptr, k_cache, v_cache, block_tables, max_blocks_per_seq,
                      context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                      num_blocks, scale, out, workspace, workspace_bytes, dtype, stream);
+}
+
+int pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
+                  const int32_t* block_tables, int max_blocks_per_seq,
+                  const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+                  int head_dim, int block_size, int num_blocks, float scale, float k_scale,
+                  float v_scale, void* out, void* workspace, size_t workspace_bytes,
+                  pa_dtype dtype, cudaStream_t stream) {
+  return decode_call(q, nullptr, nullptr, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                     context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                     num_blocks, scale, out, workspace, workspace_bytes, dtype, stream, true,
+                     k_scale, v_scale);
+}
+
+int pa_reshape_and_cache_fp8(const void* key, const void* value, void* k_cache, void* v_cache,
+                             const int64_t* slot_mapping, int num_tokens, int num_blocks,
+                             int num_kv_heads, int head_dim, int block_size, float k_scale,
+                             float v_scale, pa_dtype dtype, cudaStream_t stream) {
+  if (num_tokens < 0 || num_blocks < 1 || !shape_ok(num_kv_heads, head_dim, block_size) ||
+      (dtype != PA_FP16 && dtype != PA_BF16) || !std::isfinite(k_scale) ||
+      !std::isfinite(v_scale) || !(k_scale > 0.f) || !(v_scale > 0.f))
+    return PA_ERR_ARG;
+  if (num_tokens == 0) return PA_OK;
+  if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PA_ERR_ARG;
+  if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PA_ERR_ARG;
+  DeviceInfo di;
+  if (!device_info(&di)) return PA_ERR_CUDA;
+  return pa::reshape_and_cache_fp8_launch(key, value, k_cache, v_cache, slot_mapping, num_tokens,
+                                          num_blocks, num_kv_heads, head_dim, block_size, k_scale,
+                                          v_scale, dtype == PA_BF16, di.err, stream);
 }
 
 int pa_prefill(const void* q, const void* k_cache, const void* v_cache,
@@ -251,7 +289,7 @@ int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* block_mapping, i
                    int num_blocks, int num_kv_heads, int head_dim, int block_size,
                    pa_dtype dtype, cudaStream_t stream) {
   if (num_pairs < 0 || num_blocks < 1 || !shape_ok(num_kv_heads, head_dim, block_size) ||
-      (dtype != PA_FP16 && dtype != PA_BF16))
+      (dtype != PA_FP16 && dtype != PA_BF16 && dtype != PA_FP8_E4M3))
     return PA_ERR_ARG;
   if (num_pairs == 0) return PA_OK;
   if (!k_cache || !v_cache || !block_mapping) return PA_ERR_ARG;
@@ -259,7 +297,8 @@ int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* block_mapping, i
   DeviceInfo di;
   if (!device_info(&di)) return PA_ERR_CUDA;
   return pa::copy_blocks_launch(k_cache, v_cache, block_mapping, num_pairs, num_blocks,
-                                num_kv_heads, head_dim, block_size, di.err, stream);
+                                num_kv_heads, head_dim * (dtype == PA_FP8_E4M3 ? 1 : 2),
+                                block_size, di.err, stream);
 }
 
 int pa_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_v,
@@ -267,7 +306,8 @@ int pa_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_
                    int dst_num_blocks, int num_kv_heads, int head_dim, int block_size,
                    pa_dtype dtype, cudaStream_t stream) {
   if (num_pairs < 0 || src_num_blocks < 1 || dst_num_blocks < 1 ||
-      !shape_ok(num_kv_heads, head_dim, block_size) || (dtype != PA_FP16 && dtype != PA_BF16))
+      !shape_ok(num_kv_heads, head_dim, block_size) ||
+      (dtype != PA_FP16 && dtype != PA_BF16 && dtype != PA_FP8_E4M3))
     return PA_ERR_ARG;
   if (num_pairs == 0) return PA_OK;
   const void* ptrs[5] = {src_k, src_v, dst_k, dst_v, block_mapping};
@@ -280,8 +320,9 @@ int pa_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_
   DeviceInfo di;
   if (!device_info(&di)) return PA_ERR_CUDA;
   return pa::swap_blocks_launch(dev[0], dev[1], dev[2], dev[3], static_cast<const int32_t*>(dev[4]),
-                                num_pairs, src_num_blocks, dst_num_blocks, num_kv_heads, head_dim,
-                                block_size, di.err, stream);
+                                num_pairs, src_num_blocks, dst_num_blocks, num_kv_heads,
+                                head_dim * (dtype == PA_FP8_E4M3 ? 1 : 2), block_size, di.err,
+                                stream);
 }
 
 int pa_check_block_mapping(const int32_t* host_block_mapping, int num_pairs, int num_blocks) {

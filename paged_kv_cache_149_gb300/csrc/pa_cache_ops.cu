@@ -49,6 +49,62 @@ __global__ void __launch_bounds__(128) reshape_and_cache_kernel(
   }
 }
 
+// Two float32 values -> two E4M3 codes, round to nearest-even, magnitudes above 448
+// clamped to 448 (satfinite): `hi` in the upper byte, `lo` in the lower.
+__device__ __forceinline__ uint16_t e4m3x2_of(float hi, float lo) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// FP8 cache write: each 16-bit input x becomes the E4M3 code of x / scale, the division in
+// IEEE float32 and the rounding to nearest-even with magnitudes above 448 clamped (the
+// hardware's satfinite conversion).  A thread makes one 16-byte chunk of codes (16
+// values, 32 input bytes).  One CTA per token, as above.
+template <typename T>
+__global__ void __launch_bounds__(128) reshape_and_cache_fp8_kernel(
+    const uint4* __restrict__ key, const uint4* __restrict__ value, uint4* __restrict__ k_cache,
+    uint4* __restrict__ v_cache, const int64_t* __restrict__ slot_mapping, long long num_slots,
+    int num_kv_heads, int chunks_per_row, int block_size, float k_scale, float v_scale,
+    unsigned* err) {
+  pdl_wait_primary();
+  pdl_launch_dependents();
+  const int i = blockIdx.x;
+  const long long slot = slot_mapping[i];
+  if (slot < 0) return;
+  if (slot >= num_slots) {
+    if (threadIdx.x == 0) atomicOr(err, kErrBadSlot);
+    return;
+  }
+  const long long blk = slot / block_size;
+  const int row = static_cast<int>(slot % block_size);
+  const int n = num_kv_heads * chunks_per_row;
+  for (int j = threadIdx.x; j < 2 * n; j += blockDim.x) {
+    const bool is_v = j >= n;
+    const int jj = is_v ? j - n : j;
+    const int h = jj / chunks_per_row;
+    const int c = jj - h * chunks_per_row;
+    const float scale = is_v ? v_scale : k_scale;
+    // 16 inputs = two 16-byte vectors of the 16-bit row
+    const uint4* src = (is_v ? value : key) +
+                       ((static_cast<size_t>(i) * num_kv_heads + h) * chunks_per_row + c) * 2;
+    const uint4 a = src[0], b = src[1];
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t out[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 x0 = unpack2<T>(w[2 * k]), x1 = unpack2<T>(w[2 * k + 1]);
+      // codes of elements 4k .. 4k+3, element 4k in the low byte
+      out[k] = static_cast<uint32_t>(e4m3x2_of(__fdiv_rn(x0.y, scale), __fdiv_rn(x0.x, scale))) |
+               (static_cast<uint32_t>(e4m3x2_of(__fdiv_rn(x1.y, scale), __fdiv_rn(x1.x, scale)))
+                << 16);
+    }
+    const size_t dst =
+        ((static_cast<size_t>(blk) * num_kv_heads + h) * block_size + row) * chunks_per_row + c;
+    (is_v ? v_cache : k_cache)[dst] = make_uint4(out[0], out[1], out[2], out[3]);
+  }
+}
+
 constexpr int kCopyThreads = 256;
 constexpr int kCopyUnroll = 4;  // 16-byte loads in flight per thread before its stores
 
@@ -85,10 +141,10 @@ __global__ void __launch_bounds__(kCopyThreads) block_copy_kernel(
 
 int block_copy_launch(const void* src_k, const void* src_v, void* dst_k, void* dst_v,
                       const int32_t* mapping, int num_pairs, int src_blocks, int dst_blocks,
-                      int num_kv_heads, int head_dim, int block_size, unsigned* err,
+                      int num_kv_heads, int row_bytes, int block_size, unsigned* err,
                       cudaStream_t stream) {
   if (num_pairs == 0) return 0;
-  const size_t block_vecs = static_cast<size_t>(num_kv_heads) * block_size * head_dim / 8;
+  const size_t block_vecs = static_cast<size_t>(num_kv_heads) * block_size * row_bytes / 16;
   const size_t per_cta = static_cast<size_t>(kCopyThreads) * kCopyUnroll;
   int chunks = static_cast<int>((block_vecs + per_cta - 1) / per_cta);
   if (chunks > 64) chunks = 64;
@@ -122,19 +178,49 @@ int reshape_and_cache_launch(const void* key, const void* value, void* k_cache, 
   return e == cudaSuccess ? 0 : -3;
 }
 
+int reshape_and_cache_fp8_launch(const void* key, const void* value, void* k_cache,
+                                 void* v_cache, const int64_t* slot_mapping, int num_tokens,
+                                 int num_blocks, int num_kv_heads, int head_dim, int block_size,
+                                 float k_scale, float v_scale, bool bf16, unsigned* err,
+                                 cudaStream_t stream) {
+  if (num_tokens == 0) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_tokens);
+  cfg.blockDim = dim3(128);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const long long slots = static_cast<long long>(num_blocks) * block_size;
+  const cudaError_t e =
+      bf16 ? cudaLaunchKernelEx(&cfg, reshape_and_cache_fp8_kernel<__nv_bfloat16>,
+                                static_cast<const uint4*>(key), static_cast<const uint4*>(value),
+                                static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
+                                slot_mapping, slots, num_kv_heads, head_dim / 16, block_size,
+                                k_scale, v_scale, err)
+           : cudaLaunchKernelEx(&cfg, reshape_and_cache_fp8_kernel<__half>,
+                                static_cast<const uint4*>(key), static_cast<const uint4*>(value),
+                                static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
+                                slot_mapping, slots, num_kv_heads, head_dim / 16, block_size,
+                                k_scale, v_scale, err);
+  return e == cudaSuccess ? 0 : -3;
+}
+
 int copy_blocks_launch(void* k_cache, void* v_cache, const int32_t* block_mapping, int num_pairs,
-                       int num_blocks, int num_kv_heads, int head_dim, int block_size,
+                       int num_blocks, int num_kv_heads, int row_bytes, int block_size,
                        unsigned* err, cudaStream_t stream) {
   return block_copy_launch(k_cache, v_cache, k_cache, v_cache, block_mapping, num_pairs,
-                           num_blocks, num_blocks, num_kv_heads, head_dim, block_size, err, stream);
+                           num_blocks, num_blocks, num_kv_heads, row_bytes, block_size, err, stream);
 }
 
 int swap_blocks_launch(const void* src_k, const void* src_v, void* dst_k, void* dst_v,
                        const int32_t* block_mapping, int num_pairs, int src_num_blocks,
-                       int dst_num_blocks, int num_kv_heads, int head_dim, int block_size,
+                       int dst_num_blocks, int num_kv_heads, int row_bytes, int block_size,
                        unsigned* err, cudaStream_t stream) {
   return block_copy_launch(src_k, src_v, dst_k, dst_v, block_mapping, num_pairs, src_num_blocks,
-                           dst_num_blocks, num_kv_heads, head_dim, block_size, err, stream);
+                           dst_num_blocks, num_kv_heads, row_bytes, block_size, err, stream);
 }
 
 }  // namespace pa

@@ -47,6 +47,7 @@
 #include <chrono>
 #include <cstdint>
 #include <random>
+#include <type_traits>
 
 #include "pa_common.cuh"
 #include "pa_internal.h"
@@ -66,13 +67,16 @@ constexpr float kLog2e = 1.4426950408889634f;
 // 64: 58.4 us on 64 sequences of 128..2048 tokens; 16 x 8192 tokens: 102.9 / 96.5 / 93.9).
 constexpr int kSegCost = 32;
 
-template <int D>
+// EB: bytes per cached K/V element (2 for fp16/bf16 blocks, 1 for FP8 E4M3 blocks).
+template <int D, int EB = 2>
 struct Geo {
-  static constexpr int kRowChunks = D / 8;                  // 16-byte chunks per row
-  static constexpr int kKBytes = kStageTok * D * 2;         // K rows of a stage
+  static constexpr int kRowBytes = D * EB;
+  static constexpr int kRowChunks = kRowBytes / 16;         // 16-byte chunks per row
+  static constexpr int kKBytes = kStageTok * kRowBytes;     // K rows of a stage
   static constexpr int kStageBytes = 2 * kKBytes;           // K then V
-  // Ring slots per warp (192 KB in all) and how many stages ahead a warp loads.
-  static constexpr int kSlots = (192 * 1024) / (kStageBytes * kWarps);
+  // Ring slots per warp (192 KB in all, at most 32) and how many stages ahead a warp loads.
+  static constexpr int kSlots0 = (192 * 1024) / (kStageBytes * kWarps);
+  static constexpr int kSlots = kSlots0 > 32 ? 32 : kSlots0;
   static constexpr int kAhead = kSlots - 1;
   static constexpr int kRowsPerPass = 32 / kRowChunks;      // rows one warp-wide copy covers
   static constexpr int kPasses = kStageTok / kRowsPerPass;  // copies per lane per K (or V)
@@ -95,6 +99,7 @@ struct Params {
   int max_blocks_per_seq, block_size, log2_block, num_blocks, max_ctx;
   int seg_cost;  // stage units charged per family on top of its stages
   float scale_log2;
+  float out_scale;  // FP8 blocks: v_scale, applied to every output row (else unused)
   // [grid][gs]: arrivals at cut pair (first CTA, pi): epoch tag << 24 | pieces counted in
   unsigned long long* counters;
   unsigned long long epoch;  // 40-bit tag, different from the previous call's
@@ -299,6 +304,31 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
                                (((chunk & 7) ^ (row & 7)) << 4));
 }
 
+// FP8 stages: a row is D bytes.  At D = 128 the 16-byte chunk c of row r sits at c ^ (r % 8)
+// so that the fragment loads below (eight lanes: four chunks of two rows, or one chunk of
+// eight rows) hit distinct banks; at D = 64 rows are packed as they come.
+template <int D>
+__device__ __forceinline__ uint32_t swz8(int row, int chunk) {
+  return D == 128 ? static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4))
+                  : static_cast<uint32_t>(row * D + (chunk << 4));
+}
+
+// Row of O^T held in MMA accumulator row r (0..15) of m-tile mt.  16-bit blocks: d = 16 mt
+// + r.  FP8 blocks permute d so that every lane builds its V fragments from contiguous
+// bytes: rows r and r + 8 are the adjacent d = (D/8)(r % 8) + 2 mt and that + 1.
+template <int D, bool F8>
+__device__ __forceinline__ int drow(int mt, int r) {
+  return F8 ? (r & 7) * (D / 8) + 2 * mt + (r >> 3) : 16 * mt + r;
+}
+
+// Two E4M3 values (low byte first) -> f16x2, exact (every E4M3 value is an f16 normal).
+__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t two_bytes) {
+  uint32_t r;
+  const uint16_t v = static_cast<uint16_t>(two_bytes);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+  return r;
+}
+
 // A piece of a cut pair as every holder of a piece sees it: the CTAs holding its first and
 // last pieces, where the first CTA stored its piece (slot 0 when the pair's family is that
 // CTA's first family), and the pair's sequence and heads.
@@ -344,7 +374,7 @@ __device__ __forceinline__ int arrive(unsigned long long* ctr, unsigned long lon
 // (the log-sum-exp rescaling of online softmax); zeros when a piece saw a bad block.
 // merge_staged computes the same sums in the same order with the same fused multiply-adds,
 // so a pair's output does not depend on which of the two merges it.
-template <int D, typename T>
+template <int D, typename T, bool F8>
 __device__ void merge_pieces(const Params& p, int pi, int c, int first_slot, int c_last, int nh,
                              T* out_rows, int gt, int gthreads) {
   constexpr int C4 = D / 4;  // 4-float chunks per head row
@@ -378,7 +408,7 @@ __device__ void merge_pieces(const Params& p, int pi, int c, int first_slot, int
     }
     uint2 packed = make_uint2(0u, 0u);
     if (!bad) {
-      const float inv = 1.f / L;
+      const float inv = F8 ? p.out_scale / L : 1.f / L;
       packed.x = pack2<T>(O.x * inv, O.y * inv);
       packed.y = pack2<T>(O.z * inv, O.w * inv);
     }
@@ -402,7 +432,7 @@ __device__ __forceinline__ bool mbar_wait_once(uint32_t bar) {
 // pieces are folded in CTA order: M = max m_i, w_i = 2^(m_i - M), L = sum l_i w_i,
 // out = sum w_i acc_i / L.  Returns false, having done nothing, when the pieces do not fit
 // in the ring.
-template <int D, typename T>
+template <int D, typename T, bool F8>
 __device__ bool merge_staged(const Params& p, int pi, const CutPiece& job0, const CutPiece& job1,
                              int njobs, uint32_t ring, uint8_t* ring_ptr, int ring_bytes,
                              uint32_t bar, int lane) {
@@ -508,7 +538,7 @@ __device__ bool merge_staged(const Params& p, int pi, const CutPiece& job0, cons
       const float L = ml[moff + h].y;
       uint2 packed = make_uint2(0u, 0u);
       if (L >= 0.f) {
-        const float inv = 1.f / L;
+        const float inv = F8 ? p.out_scale / L : 1.f / L;
         packed.x = pack2<T>(O.x * inv, O.y * inv);
         packed.y = pack2<T>(O.z * inv, O.w * inv);
       }
@@ -520,9 +550,9 @@ __device__ bool merge_staged(const Params& p, int pi, const CutPiece& job0, cons
   return true;
 }
 
-template <int D>
+template <int D, int EB>
 struct Smem {
-  uint8_t ring[kWarps][Geo<D>::kSlots][Geo<D>::kStageBytes];  // 1024-byte aligned
+  uint8_t ring[kWarps][Geo<D, EB>::kSlots][Geo<D, EB>::kStageBytes];  // 1024-byte aligned
   float xo[kWarps][4][D];  // per-warp O rows, 4 heads per exchange round
   float xm[kWarps][kMaxHeads], xl[kWarps][kMaxHeads];
   long long scan[kWarps];
@@ -552,6 +582,35 @@ __device__ __forceinline__ void load_q(const Params& p, int s, int h0, int nh, i
   }
 }
 
+// The same for FP8 blocks, as f16 (the type the E4M3 values are widened to), with d in the
+// order the K fragments use: k-step ks takes d = (D/4) t + 4 ks + {0, 1} into b0 and
+// + {2, 3} into b1, t = lane % 4.  bf16 queries are rounded to f16 (exact within the f16
+// normal range).
+template <int D, int NTH, typename T>
+__device__ __forceinline__ void load_q8(const Params& p, int s, int h0, int nh, int lane,
+                                        uint32_t (&qb)[D / 16][NTH][2]) {
+  const int r0 = lane >> 2, t = lane & 3;
+  const uint2* qrow = reinterpret_cast<const uint2*>(
+      p.q + (static_cast<size_t>(s) * p.num_q_heads + h0) * D * 2);
+#pragma unroll
+  for (int nt = 0; nt < NTH; ++nt) {
+    const int h = nt * 8 + r0;
+    const bool hv = h < nh;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      const uint2 w = hv ? __ldg(qrow + (h * D + (D / 4) * t + 4 * ks) / 4) : make_uint2(0u, 0u);
+      if (std::is_same<T, __half>::value) {
+        qb[ks][nt][0] = w.x;
+        qb[ks][nt][1] = w.y;
+      } else {
+        const float2 a = unpack2<T>(w.x), b = unpack2<T>(w.y);
+        qb[ks][nt][0] = pack2<__half>(a.x, a.y);
+        qb[ks][nt][1] = pack2<__half>(b.x, b.y);
+      }
+    }
+  }
+}
+
 // The next family (after f) where pair pi has units to compute; false at the share's end.
 __device__ __forceinline__ bool next_busy_fam(Fam f, int pi, long long w0, long long w1,
                                               const Params& p, Fam& out) {
@@ -566,15 +625,19 @@ __device__ __forceinline__ bool next_busy_fam(Fam f, int pi, long long w0, long 
   }
 }
 
-template <int D, int NTH, typename T>
+// F8: K/V blocks hold E4M3 codes (scales folded into scale_log2 and out_scale); the MMAs
+// then run in f16 on the widened values.
+template <int D, int NTH, typename T, bool F8>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ Params p) {
-  using G_ = Geo<D>;
+  constexpr int EB = F8 ? 1 : 2;
+  using G_ = Geo<D, EB>;
+  using TM = typename std::conditional<F8, __half, T>::type;  // MMA operand type
   constexpr int R = G_::kSlots;
   constexpr int KS = G_::kKSteps;
   constexpr int MT = D / 16;  // m-tiles of O^T (16 rows of d each)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
-  Smem<D>& sm = *reinterpret_cast<Smem<D>*>(smem_raw + (((raw_addr + 1023) & ~1023u) - raw_addr));
+  Smem<D, EB>& sm = *reinterpret_cast<Smem<D, EB>*>(smem_raw + (((raw_addr + 1023) & ~1023u) - raw_addr));
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -687,9 +750,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
           const bool live = row < nxt.nt;
           // rows past the context: zero-filled, nothing read (the source stays in block x)
           const size_t grow = !live ? row_x : (r < p.block_size ? row_x + r : row_y + (r - p.block_size));
-          const size_t src = (grow * D + ch * 8) * 2;
-          const uint32_t so = swz(row, ch);
-          if (p.key_new && nxt.last && row == nxt.nt - 1) {
+          const size_t src = grow * G_::kRowBytes + ch * 16;
+          const uint32_t so = F8 ? swz8<D>(row, ch) : swz(row, ch);
+          if (!F8 && p.key_new && nxt.last && row == nxt.nt - 1) {
             // the newest token: from the step's input (the cache row is written later)
             const size_t nsrc = ((static_cast<size_t>(nxt.s) * p.num_kv_heads + nxt.kvh) * D + ch * 8) * 2;
             cp_async16(dst + so, p.key_new + nsrc, 16u);
@@ -724,7 +787,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     else have = next_busy_fam(first, pi, w0, w1, p, qf);
     if (have) {
       const PairHeads ph = pair_heads(p, qf.g * p.gs + pi);
-      load_q<D, NTH>(p, qf.s, ph.h0, ph.nh, lane, qn);
+      if (F8) load_q8<D, NTH, T>(p, qf.s, ph.h0, ph.nh, lane, qn);
+      else load_q<D, NTH>(p, qf.s, ph.h0, ph.nh, lane, qn);
     }
   }
 
@@ -761,7 +825,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       Fam qf;
       if (next_busy_fam(f, pi, w0, w1, p, qf)) {
         const PairHeads lh = pair_heads(p, qf.g * p.gs + pi);
-        load_q<D, NTH>(p, qf.s, lh.h0, lh.nh, lane, qn);
+        if (F8) load_q8<D, NTH, T>(p, qf.s, lh.h0, lh.nh, lane, qn);
+        else load_q<D, NTH>(p, qf.s, lh.h0, lh.nh, lane, qn);
       }
     }
 
@@ -796,16 +861,47 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         for (int nt = 0; nt < NTH; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) sacc[nt][e] = sodd[nt][e] = 0.f;
+        if (F8) {
+          // K rows r0 and r0 + 8, bytes [(D/4) t, (D/4)(t+1)): word ks of a row holds the
+          // four d of k-step ks (the order load_q8 gives q)
+          uint32_t kw[2][KS];
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-          uint32_t a[4];  // rows tok 0-7 / 8-15, d chunks 2ks / 2ks+1
-          ldsm_x4(kb + swz(lrow + ((lmat & 1) << 3), 2 * ks + (lmat >> 1)), a);
+          for (int hr = 0; hr < 2; ++hr)
 #pragma unroll
-          for (int nt = 0; nt < NTH; ++nt) {
-            if (ks & 1)
-              mma16816<T>(sodd[nt], a, qb[ks][nt][0], qb[ks][nt][1]);
-            else
-              mma16816<T>(sacc[nt], a, qb[ks][nt][0], qb[ks][nt][1]);
+            for (int i = 0; i < KS / 4; ++i) {
+              const uint32_t addr = kb + swz8<D>(r0 + 8 * hr, (KS / 4) * (lane & 3) + i);
+              asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                           : "=r"(kw[hr][4 * i]), "=r"(kw[hr][4 * i + 1]), "=r"(kw[hr][4 * i + 2]),
+                             "=r"(kw[hr][4 * i + 3])
+                           : "r"(addr));
+            }
+#pragma unroll
+          for (int ks = 0; ks < KS; ++ks) {
+            uint32_t a[4];
+            a[0] = e4m3x2_f16x2(kw[0][ks]);
+            a[1] = e4m3x2_f16x2(kw[1][ks]);
+            a[2] = e4m3x2_f16x2(kw[0][ks] >> 16);
+            a[3] = e4m3x2_f16x2(kw[1][ks] >> 16);
+#pragma unroll
+            for (int nt = 0; nt < NTH; ++nt) {
+              if (ks & 1)
+                mma16816<TM>(sodd[nt], a, qb[ks][nt][0], qb[ks][nt][1]);
+              else
+                mma16816<TM>(sacc[nt], a, qb[ks][nt][0], qb[ks][nt][1]);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int ks = 0; ks < KS; ++ks) {
+            uint32_t a[4];  // rows tok 0-7 / 8-15, d chunks 2ks / 2ks+1
+            ldsm_x4(kb + swz(lrow + ((lmat & 1) << 3), 2 * ks + (lmat >> 1)), a);
+#pragma unroll
+            for (int nt = 0; nt < NTH; ++nt) {
+              if (ks & 1)
+                mma16816<TM>(sodd[nt], a, qb[ks][nt][0], qb[ks][nt][1]);
+              else
+                mma16816<TM>(sacc[nt], a, qb[ks][nt][0], qb[ks][nt][1]);
+            }
           }
         }
         // ---- online softmax per head (column) over the 16 tokens (rows) ----
@@ -840,8 +936,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
             m_run[nt][cc] = m_new;
           }
           // P^T as B fragments: transpose the (token x head) 8x8 blocks in registers
-          pb[nt][0] = movmatrix_t(pack2<T>(pr[0], pr[1]));  // tokens 0-7
-          pb[nt][1] = movmatrix_t(pack2<T>(pr[2], pr[3]));  // tokens 8-15
+          pb[nt][0] = movmatrix_t(pack2<TM>(pr[0], pr[1]));  // tokens 0-7
+          pb[nt][1] = movmatrix_t(pack2<TM>(pr[2], pr[3]));  // tokens 8-15
         }
         bool all_one = true;
 #pragma unroll
@@ -859,14 +955,51 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         }
         // ---- O^T += V^T P^T: rows = d (16 per m-tile), k = tokens, columns = heads ----
         // (V rows past the context were zero-filled by the copy, so 0 * garbage cannot occur)
+        if (F8) {
+          // V rows (tokens) 2t, 2t+1, 2t+8, 2t+9, bytes [(D/8) r0, (D/8)(r0+1)): m-tile mt
+          // takes bytes 2 mt and 2 mt + 1 (its rows r0 and r0 + 8, see drow); a byte
+          // permute pairs the two tokens of each A register before widening
+          constexpr int VW = D / 32;  // 32-bit words of this lane's bytes of one V row
+          uint32_t vw[4][VW];
+          const int tq = lane & 3;
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          uint32_t a[4];  // V^T: d chunks 2mt / 2mt+1, tokens 0-7 / 8-15
-          ldsm_x4_t(vb + swz(lrow + ((lmat >> 1) << 3), 2 * mt + (lmat & 1)), a);
+          for (int k = 0; k < 4; ++k) {
+            const int row = 2 * tq + (k & 1) + 8 * (k >> 1);
+            if constexpr (VW == 4) {
+              const uint32_t addr = vb + swz8<D>(row, r0);
+              asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                           : "=r"(vw[k][0]), "=r"(vw[k][1]), "=r"(vw[k][2]), "=r"(vw[k][3])
+                           : "r"(addr));
+            } else {
+              const uint32_t addr = vb + swz8<D>(row, r0 >> 1) + 8 * (r0 & 1);
+              asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
+                           : "=r"(vw[k][0]), "=r"(vw[k][1])
+                           : "r"(addr));
+            }
+          }
 #pragma unroll
-          for (int nt = 0; nt < NTH; ++nt) mma16816<T>(o[mt][nt], a, pb[nt][0], pb[nt][1]);
+          for (int mt = 0; mt < MT; ++mt) {
+            const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+            const uint32_t lo = __byte_perm(vw[0][mt >> 1], vw[1][mt >> 1], sel);  // tokens 2t, 2t+1
+            const uint32_t hi = __byte_perm(vw[2][mt >> 1], vw[3][mt >> 1], sel);  // 2t+8, 2t+9
+            uint32_t a[4];
+            a[0] = e4m3x2_f16x2(lo);
+            a[1] = e4m3x2_f16x2(lo >> 16);
+            a[2] = e4m3x2_f16x2(hi);
+            a[3] = e4m3x2_f16x2(hi >> 16);
+#pragma unroll
+            for (int nt = 0; nt < NTH; ++nt) mma16816<TM>(o[mt][nt], a, pb[nt][0], pb[nt][1]);
+          }
+        } else {
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            uint32_t a[4];  // V^T: d chunks 2mt / 2mt+1, tokens 0-7 / 8-15
+            ldsm_x4_t(vb + swz(lrow + ((lmat >> 1) << 3), 2 * mt + (lmat & 1)), a);
+#pragma unroll
+            for (int nt = 0; nt < NTH; ++nt) mma16816<TM>(o[mt][nt], a, pb[nt][0], pb[nt][1]);
+          }
         }
-        if (p.key_new && j == f.ns - 1) {
+        if (!F8 && p.key_new && j == f.ns - 1) {
           // fused cache write: the newest token's K and V rows, from the slot, to position
           // ctx - 1 of the sequence (lanes take the 16-byte chunks of K, then of V)
           constexpr int CH = G_::kRowChunks;
@@ -911,8 +1044,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
             if (h < ph.nh) {
 #pragma unroll
               for (int mt = 0; mt < MT; ++mt) {
-                pacc[h * D + 16 * mt + r0] = o[mt][nt][cc];
-                pacc[h * D + 16 * mt + r0 + 8] = o[mt][nt][cc + 2];
+                pacc[h * D + drow<D, F8>(mt, r0)] = o[mt][nt][cc];
+                pacc[h * D + drow<D, F8>(mt, r0 + 8)] = o[mt][nt][cc + 2];
               }
               if (r0 == 0) {  // an empty piece (m = -inf) gets l = 0: weight 0 in the merge
                 pml[h * 2 + 0] = m_run[nt][cc];
@@ -928,18 +1061,36 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       const bool bad = any_bad;
       // out = O / l, rounded; transposed in registers (movmatrix) so that each lane stores
       // two adjacent d of one head: lane (r0, qc) writes out[h = 8*nt + r0][16*mt + qc (+8)].
+      if (F8) {
+        // rows r0 and r0 + 8 of an m-tile are the adjacent d = drow(mt, r0), + 1: each lane
+        // stores its two heads' pairs directly
 #pragma unroll
-      for (int nt = 0; nt < NTH; ++nt) {
-        const float i0 = bad ? 0.f : 1.f / l_run[nt][0];
-        const float i1 = bad ? 0.f : 1.f / l_run[nt][1];
-        const int h = nt * 8 + r0;
+        for (int nt = 0; nt < NTH; ++nt)
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          const uint32_t lo = movmatrix_t(pack2<T>(o[mt][nt][0] * i0, o[mt][nt][1] * i1));
-          const uint32_t hi = movmatrix_t(pack2<T>(o[mt][nt][2] * i0, o[mt][nt][3] * i1));
-          if (h < ph.nh) {
-            *reinterpret_cast<uint32_t*>(out_rows + h * D + 16 * mt + qc) = lo;
-            *reinterpret_cast<uint32_t*>(out_rows + h * D + 16 * mt + 8 + qc) = hi;
+          for (int cc = 0; cc < 2; ++cc) {
+            const float inv = bad ? 0.f : p.out_scale / l_run[nt][cc];
+            const int h = nt * 8 + qc + cc;
+            if (h < ph.nh) {
+#pragma unroll
+              for (int mt = 0; mt < MT; ++mt)
+                *reinterpret_cast<uint32_t*>(out_rows + h * D + drow<D, F8>(mt, r0)) =
+                    pack2<T>(o[mt][nt][cc] * inv, o[mt][nt][cc + 2] * inv);
+            }
+          }
+      } else {
+#pragma unroll
+        for (int nt = 0; nt < NTH; ++nt) {
+          const float i0 = bad ? 0.f : 1.f / l_run[nt][0];
+          const float i1 = bad ? 0.f : 1.f / l_run[nt][1];
+          const int h = nt * 8 + r0;
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            const uint32_t lo = movmatrix_t(pack2<T>(o[mt][nt][0] * i0, o[mt][nt][1] * i1));
+            const uint32_t hi = movmatrix_t(pack2<T>(o[mt][nt][2] * i0, o[mt][nt][3] * i1));
+            if (h < ph.nh) {
+              *reinterpret_cast<uint32_t*>(out_rows + h * D + 16 * mt + qc) = lo;
+              *reinterpret_cast<uint32_t*>(out_rows + h * D + 16 * mt + 8 + qc) = hi;
+            }
           }
         }
       }
@@ -973,8 +1124,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
           if (h >= rbase && h < rbase + 4) {
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
-              sm.xo[warp][h - rbase][16 * mt + r0] = o[mt][nt][cc];
-              sm.xo[warp][h - rbase][16 * mt + r0 + 8] = o[mt][nt][cc + 2];
+              sm.xo[warp][h - rbase][drow<D, F8>(mt, r0)] = o[mt][nt][cc];
+              sm.xo[warp][h - rbase][drow<D, F8>(mt, r0 + 8)] = o[mt][nt][cc + 2];
             }
           }
         }
@@ -1001,7 +1152,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         if (whole) {
           uint2 packed = make_uint2(0u, 0u);  // zeros for a pair with a bad block
           if (!any_bad) {
-            const float inv = 1.f / L;
+            const float inv = F8 ? p.out_scale / L : 1.f / L;
             packed.x = pack2<T>(acc.x * inv, acc.y * inv);
             packed.y = pack2<T>(acc.z * inv, acc.w * inv);
           }
@@ -1053,7 +1204,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     if (P == 1 && bits) {
       const int nj = (bits & 1) + ((bits >> 1) & 1);
       const CutPiece& j0 = (bits & 1) ? cut_a : cut_b;
-      if (merge_staged<D, T>(p, pi, j0, cut_b, nj, ring, sm.ring[warp][0], R * G_::kStageBytes,
+      if (merge_staged<D, T, F8>(p, pi, j0, cut_b, nj, ring, sm.ring[warp][0], R * G_::kStageBytes,
                              smem_addr(&sm.merge_bar[warp]), lane))
         bits = 0;
     }
@@ -1062,16 +1213,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       const CutPiece& cp = k == 0 ? cut_a : cut_b;
       T* out_rows =
           reinterpret_cast<T*>(p.out) + (static_cast<size_t>(cp.s) * p.num_q_heads + cp.h0) * D;
-      merge_pieces<D, T>(p, pi, cp.c_first, cp.first_slot, cp.c_last, cp.nh, out_rows, gt,
+      merge_pieces<D, T, F8>(p, pi, cp.c_first, cp.first_slot, cp.c_last, cp.nh, out_rows, gt,
                          gthreads);
     }
   }
 }
 
-template <int D, int NTH, typename T>
+template <int D, int NTH, typename T, bool F8>
 int launch(const Params& prm, int grid, cudaStream_t stream) {
-  const size_t smem = sizeof(Smem<D>) + 1024;  // + alignment slack for the ring
-  auto* kern = decode_kernel<D, NTH, T>;
+  const size_t smem = sizeof(Smem<D, F8 ? 1 : 2>) + 1024;  // + alignment slack for the ring
+  auto* kern = decode_kernel<D, NTH, T, F8>;
   if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), smem)) return -3;
   // a programmatic dependent of the previous kernel in the stream (see pdl_wait_primary)
   cudaLaunchConfig_t cfg = {};
@@ -1149,7 +1300,9 @@ int decode_launch(const DecodeArgs& a, int grid, cudaStream_t stream) {
   p.num_blocks = a.num_blocks;
   p.max_ctx = a.max_blocks_per_seq * a.block_size;
   p.seg_cost = decode::kSegCost;
-  p.scale_log2 = a.scale * decode::kLog2e;
+  // FP8 blocks: scores are k_scale * <q, codes>, outputs v_scale * (weighted codes)
+  p.scale_log2 = a.scale * (a.kv_fp8 ? a.k_scale : 1.f) * decode::kLog2e;
+  p.out_scale = a.kv_fp8 ? a.v_scale : 1.f;
   p.err = a.err;
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
@@ -1161,10 +1314,14 @@ int decode_launch(const DecodeArgs& a, int grid, cudaStream_t stream) {
   p.part_ml = reinterpret_cast<float*>(ws);
 
   // heads of a pair are MMA columns: one n-tile of 8, or two for up to 16
-#define PA_DECODE_CASE(DD, NN)                                       \
-  if (a.head_dim == DD && (p.heads_per_pair > 8) == (NN == 2))       \
-    return a.bf16 ? decode::launch<DD, NN, __nv_bfloat16>(p, grid, stream) \
-                  : decode::launch<DD, NN, __half>(p, grid, stream);
+#define PA_DECODE_CASE(DD, NN)                                                           \
+  if (a.head_dim == DD && (p.heads_per_pair > 8) == (NN == 2)) {                         \
+    if (a.kv_fp8)                                                                        \
+      return a.bf16 ? decode::launch<DD, NN, __nv_bfloat16, true>(p, grid, stream)       \
+                    : decode::launch<DD, NN, __half, true>(p, grid, stream);             \
+    return a.bf16 ? decode::launch<DD, NN, __nv_bfloat16, false>(p, grid, stream)        \
+                  : decode::launch<DD, NN, __half, false>(p, grid, stream);              \
+  }
   PA_DECODE_CASE(128, 1)
   PA_DECODE_CASE(128, 2)
   PA_DECODE_CASE(64, 1)

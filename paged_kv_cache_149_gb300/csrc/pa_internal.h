@@ -20,7 +20,9 @@ struct DecodeArgs {
   void* workspace;
   int num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size, num_blocks;
   float scale;
-  bool bf16;
+  bool bf16;       // q / out type (and the cache type unless kv_fp8)
+  bool kv_fp8;     // caches hold FP8 E4M3 codes with scales k_scale, v_scale
+  float k_scale = 1.f, v_scale = 1.f;
   unsigned* err;  // device address of the per-device error word
 };
 
@@ -54,12 +56,18 @@ int reshape_and_cache_launch(const void* key, const void* value, void* k_cache, 
                              int num_kv_heads, int head_dim, int block_size, unsigned* err,
                              cudaStream_t stream);
 
+// row_bytes: bytes of one cached row (head_dim x element size)
 int copy_blocks_launch(void* k_cache, void* v_cache, const int32_t* block_mapping, int num_pairs,
-                       int num_blocks, int num_kv_heads, int head_dim, int block_size,
+                       int num_blocks, int num_kv_heads, int row_bytes, int block_size,
                        unsigned* err, cudaStream_t stream);
+int reshape_and_cache_fp8_launch(const void* key, const void* value, void* k_cache,
+                                 void* v_cache, const int64_t* slot_mapping, int num_tokens,
+                                 int num_blocks, int num_kv_heads, int head_dim, int block_size,
+                                 float k_scale, float v_scale, bool bf16, unsigned* err,
+                                 cudaStream_t stream);
 int swap_blocks_launch(const void* src_k, const void* src_v, void* dst_k, void* dst_v,
                        const int32_t* block_mapping, int num_pairs, int src_num_blocks,
-                       int dst_num_blocks, int num_kv_heads, int head_dim, int block_size,
+                       int dst_num_blocks, int num_kv_heads, int row_bytes, int block_size,
                        unsigned* err, cudaStream_t stream);
 
 // Raise a kernel's dynamic shared-memory limit once per device; false on failure.
