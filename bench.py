@@ -1109,6 +1109,232 @@ def prefix_line(args, res, world):
     }
 
 
+FP8_WORKLOADS = {"kv8_llama31_8b": "llama31_8b", "kv8_llama7b_mha": "llama7b_mha",
+                 "kv8_tiny": "tiny"}
+FP8_SCALE = 0.0123   # k_scale = v_scale: about max|N(0,1) draw| / 448 for these batches
+
+
+def fp8_step_bytes(wl):
+    """Algorithmic bytes of one FP8 step: decode reads the valid tokens' K/V codes (one
+    byte each), q, the table entries and lengths, and writes out; the cache write reads
+    the newest rows (16-bit) and writes their codes."""
+    n, hq, hkv, d, bs = wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.block_size
+    ctx = [int(c) for c in wl.context_lens]
+    decode = sum(ctx) * hkv * d * 2 + 2 * n * hq * d * 2 + sum(-(-c // bs) for c in ctx) * 4 + 4 * n
+    reshape = n * hkv * d * (2 + 1) * 2
+    return decode, reshape
+
+
+def run_gpu_fp8(args, rank, world, local_rank):
+    """The decode step over FP8 blocks: the newest tokens' rows quantised into the cache
+    (pa_reshape_and_cache_fp8), then paged decode over the codes (pa_decode_fp8), the two
+    launches back to back (programmatic dependent launch); the decode kernel alone timed
+    beside it; end to end with host buffers.  ROTATE batches in disjoint blocks."""
+    import torch
+
+    import paged_kv_cache_149_gb300 as pa
+    import workloads
+    from paged_kv_cache_149_gb300 import build as _build
+
+    _build.build()
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    wl = workloads.RECIPES[FP8_WORKLOADS[args.workload]]()
+    dt = {"fp16": torch.float16, "bf16": torch.bfloat16}[wl.dtype]
+    ks = vs = FP8_SCALE
+
+    def up(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(dt)
+    shape = (wl.num_blocks, wl.num_kv_heads, wl.block_size, wl.head_dim)
+    k8 = torch.zeros(shape, dtype=torch.uint8, device=device)
+    v8 = torch.zeros(shape, dtype=torch.uint8, device=device)
+    pool = pa.BlockPool(wl.num_blocks, wl.block_size, wl.free_order)
+    n, T = wl.num_seqs, wl.max_blocks_per_seq
+    keys, values = up(wl.keys), up(wl.values)
+    last_rows = torch.from_numpy(wl.seq_start[1:] - 1).to(device)
+    batches = []
+    for r in range(ROTATE):
+        tables = np.full((n, T), 0, dtype=np.int32)
+        slots = []
+        for s in range(n):
+            pool.allocate(r * n + s, int(wl.context_lens[s]))
+            t = pool.block_table(r * n + s)
+            tables[s, :len(t)] = t
+            slots.append(pool.slots(r * n + s, 0, int(wl.context_lens[s])))
+        pa.reshape_and_cache_fp8(keys, values, k8, v8,
+                                 torch.from_numpy(np.concatenate(slots)).to(device), ks, vs)
+        batches.append({
+            "q": up(wl.q), "tables": torch.from_numpy(tables).to(device),
+            "ctx": torch.from_numpy(np.ascontiguousarray(wl.context_lens, np.int32)).to(device),
+            "slots": torch.from_numpy(np.array([sl[-1] for sl in slots], np.int64)).to(device),
+            "key": keys[last_rows].contiguous(), "value": values[last_rows].contiguous(),
+            "out": torch.empty((n, wl.num_q_heads, wl.head_dim), dtype=dt, device=device)})
+    del keys, values
+    ws = pa.make_workspace(wl.num_q_heads, wl.num_kv_heads, wl.head_dim, device)
+    stream = torch.cuda.Stream(device)
+    torch.cuda.synchronize(device)
+    pa.get_device_error()
+
+    def step(i, b=None):
+        b = b or batches[i % ROTATE]
+        pa.reshape_and_cache_fp8(b["key"], b["value"], k8, v8, b["slots"], ks, vs, stream=stream)
+        pa.decode_fp8(b["q"], k8, v8, b["tables"], b["ctx"], wl.scale, ks, vs, out=b["out"],
+                      workspace=ws, stream=stream)
+
+    def decode_only(i):
+        b = batches[i % ROTATE]
+        pa.decode_fp8(b["q"], k8, v8, b["tables"], b["ctx"], wl.scale, ks, vs, out=b["out"],
+                      workspace=ws, stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+        decode_only(i)
+    torch.cuda.synchronize(device)
+    if pa.get_device_error(stream=stream):
+        raise RuntimeError("device error flags set during warm-up")
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    K = args.steps
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(device)
+    t0 = time.time()
+    ev[0].record(stream)
+    for i in range(K):
+        step(i)
+    ev[1].record(stream)
+    torch.cuda.synchronize(device)
+    ev[2].record(stream)
+    for i in range(K):
+        decode_only(i)
+    ev[3].record(stream)
+    torch.cuda.synchronize(device)
+    t1 = time.time()
+    clocks = sampler.stop(t0, t1) if sampler else None
+    flags = pa.get_device_error(stream=stream)
+    names = ("q", "tables", "ctx", "key", "value", "slots")
+    host_in = [{k: b[k].cpu().pin_memory() for k in names} for b in batches]
+    host_out = torch.empty(batches[0]["out"].shape, dtype=dt).pin_memory()
+    dev = {k: torch.empty_like(batches[0][k]) for k in names}
+    dev["out"] = torch.empty_like(batches[0]["out"])
+
+    def e2e_step(i):
+        with torch.cuda.stream(stream):
+            for k, v in host_in[i % ROTATE].items():
+                dev[k].copy_(v, non_blocking=True)
+        step(i, dev)
+        with torch.cuda.stream(stream):
+            host_out.copy_(dev["out"], non_blocking=True)
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize(device)
+    ke = max(1, min(K, 2000))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(ke):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    flags |= pa.get_device_error(stream=stream)
+    return {"wl": wl, "total_ms": ev[0].elapsed_time(ev[1]), "decode_ms": ev[2].elapsed_time(ev[3]) / K,
+            "two_calls_ms": ev[0].elapsed_time(ev[1]) / K, "e2e_ms": e0.elapsed_time(e1) / ke,
+            "h2d": sum(v.numel() * v.element_size() for v in host_in[0].values()),
+            "d2h": host_out.numel() * host_out.element_size(), "clocks": clocks, "flags": flags}
+
+
+def oracle_fp8_sample(name, budget_s):
+    """The FP8 decode oracle on whole sequences of the batch (codes made by the oracle's own
+    cache write), single thread, until budget_s of CPU time is spent."""
+    code = f"""
+import json, sys, time
+sys.path.insert(0, {ROOT!r})
+import numpy as np
+import workloads
+from oracle import fp8
+from oracle.block_pool import BlockPool
+wl = workloads.RECIPES[{FP8_WORKLOADS[name]!r}]()
+pool = BlockPool(wl.num_blocks, wl.block_size, wl.free_order)
+n, T = wl.num_seqs, wl.max_blocks_per_seq
+tables = np.full((n, T), -1, dtype=np.int32)
+slots = []
+for s in range(n):
+    c = int(wl.context_lens[s]); pool.allocate(s, c)
+    t = pool.block_table(s); tables[s, :len(t)] = t
+    slots += [pool.slot(s, i) for i in range(c)]
+shape = (wl.num_blocks, wl.num_kv_heads, wl.block_size, wl.head_dim)
+k8 = np.zeros(shape, np.uint8); v8 = k8.copy()
+k8, v8 = fp8.reshape_and_cache(k8, v8, wl.keys, wl.values, np.array(slots), {FP8_SCALE},
+                               {FP8_SCALE}, wl.dtype)
+done, nbytes, t0 = 0, 0, time.process_time()
+while time.process_time() - t0 < {budget_s} and done < n:
+    fp8.paged_decode_bits(wl.q, k8, v8, tables, wl.context_lens, wl.scale, {FP8_SCALE},
+                          {FP8_SCALE}, wl.block_size, wl.dtype, seqs=[done])
+    c = int(wl.context_lens[done])
+    nbytes += c * wl.num_kv_heads * wl.head_dim * 2 + 2 * wl.num_q_heads * wl.head_dim * 2
+    done += 1
+print(json.dumps({{"seqs": done, "seconds": time.process_time() - t0, "bytes": nbytes}}))
+"""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
+    if r.returncode != 0:
+        raise RuntimeError("fp8 oracle baseline failed:\n" + r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def fp8_line(args, res, world):
+    wl = res["wl"]
+    dec_b, resh_b = fp8_step_bytes(wl)
+    step_s = res["total_ms"] / 1e3 / args.steps
+    value = world * (dec_b + resh_b) / step_s / 1e9
+    peak, peak_kind = measured_peak()
+    achieved = dec_b / (res["decode_ms"] / 1e3) / 1e9
+    cpu = oracle_fp8_sample(args.workload, args.cpu_baseline_seconds) \
+        if args.cpu_baseline_seconds > 0 else None
+    ctx = wl.context_lens
+    return {
+        "metric": "paged decode KV GB/s over FP8 (E4M3) blocks and % of GB300 HBM peak; "
+                  "µs per decode step",
+        "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(res["total_ms"] / args.steps, 5),
+        "us_per_step": round(1e3 * res["total_ms"] / args.steps, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": f"e4m3 K/V, {wl.dtype} q/out, f16 MMA",
+        "data": "synthetic (seeded normals; no dataset or weights)",
+        "config": {
+            "workload": (f"{args.workload}: the {wl.name} batch ({wl.num_seqs} seqs, ctx "
+                         f"{int(ctx.min())}..{int(ctx.max())}, sum {int(ctx.sum())}, "
+                         f"{wl.num_q_heads} q / {wl.num_kv_heads} kv heads, head_dim "
+                         f"{wl.head_dim}, block_size {wl.block_size}) with E4M3 K/V blocks, "
+                         f"k_scale = v_scale = {FP8_SCALE}"),
+            "l2": f"{ROTATE} batches in disjoint blocks rotated every step "
+                  f"({dec_b / 1e6:.0f} MB of decode bytes per batch)",
+            "parallelism": f"replicas x{world}",
+            "step": "pa_reshape_and_cache_fp8 + pa_decode_fp8 (two launches)",
+        },
+        "roofline": {"bound": "hbm", "kernel": "decode_kernel<F8> (pa_decode_fp8)",
+                     "achieved": round(achieved, 1), "peak": peak,
+                     "peak_kind": f"{peak_kind} (copy bandwidth)", "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "decode_us": round(1e3 * res["decode_ms"], 2),
+                     "algorithmic_bytes_per_launch": dec_b},
+        "cpu_baseline": None if cpu is None else {
+            "value": round(cpu["bytes"] / cpu["seconds"] / 1e9, 4), "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"float64 FP8 decode oracle, single thread, {cpu['seqs']} whole "
+                      "sequences of the batch"},
+        "e2e": {"value": round(world * (dec_b + resh_b) / (res["e2e_ms"] / 1e3) / 1e9, 1),
+                "unit": "GB/s", "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
+                "us_per_step": round(1e3 * res["e2e_ms"], 2)},
+        "clocks": res["clocks"],
+        "gpu_launches": 2 * args.steps,
+        "device_error_flags": res["flags"],
+    }
+
+
 def max_over_ranks(values):
     """Element-wise maximum of per-rank floats over the process group (NCCL on GPUs, or any
     other backend on CPU tensors)."""
@@ -1154,8 +1380,9 @@ def main(argv=None, runner=None, backend="nccl"):
     is_prefill = args.workload.startswith("prefill")
     is_swap = args.workload in SWAP_WORKLOADS
     is_prefix = args.workload in PREFIX_WORKLOADS
+    is_fp8 = args.workload in FP8_WORKLOADS
     default_runner = (run_gpu_prefill if is_prefill else run_gpu_swap if is_swap else
-                      run_gpu_prefix if is_prefix else run_gpu)
+                      run_gpu_prefix if is_prefix else run_gpu_fp8 if is_fp8 else run_gpu)
     res = (runner or default_runner)(args, rank, world, local_rank)
     if world > 1:
         res.update(zip(RANK_TIMES, max_over_ranks([res[k] for k in RANK_TIMES])))
@@ -1164,8 +1391,9 @@ def main(argv=None, runner=None, backend="nccl"):
             import torch
             torch.distributed.destroy_process_group()
         return
-    if is_prefill or is_swap or is_prefix:
-        line = (prefill_line if is_prefill else swap_line if is_swap else prefix_line)
+    if is_prefill or is_swap or is_prefix or is_fp8:
+        line = (prefill_line if is_prefill else swap_line if is_swap else
+                prefix_line if is_prefix else fp8_line)
         print(json.dumps(line(args, res, world)))
         if world > 1:
             import torch
