@@ -53,6 +53,9 @@ SIGNATURES = {
                                 _i32, _i32, _f32, _vp, _vp, _sz, _i32, _vp]),
     "pa_decode_fp8": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
                              _f32, _f32, _f32, _vp, _vp, _sz, _i32, _vp]),
+    "pa_decode_append_fp8": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32,
+                                    _i32, _i32, _i32, _f32, _f32, _f32, _vp, _vp, _sz, _i32,
+                                    _vp]),
     "pa_reshape_and_cache_fp8": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
                                         _f32, _f32, _i32, _vp]),
     "pa_prefill": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
@@ -321,6 +324,34 @@ def decode_fp8(q, k_cache, v_cache, block_tables, context_lens, scale, k_scale, 
         float(k_scale), float(v_scale), _dev(out, "out"), _dev(workspace, "workspace"),
         workspace.numel() * workspace.element_size(), _dtype_code(q), _stream_ptr(stream, q.device))
     _check(st, "pa_decode_fp8")
+    return out
+
+
+def decode_append_fp8(q, key_new, value_new, k_cache, v_cache, block_tables, context_lens,
+                      scale, k_scale, v_scale, out=None, workspace=None, stream=None):
+    """One FP8 decode step: quantise each sequence's newest K/V row into its slot at
+    position ctx - 1 and decode, in one kernel (= reshape_and_cache_fp8 + decode_fp8)."""
+    import torch
+    n, hq, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    _need(v_cache.shape == k_cache.shape and d == d2, "shape mismatch")
+    _need(key_new.shape == (n, hkv, d) and value_new.shape == key_new.shape, "key_new must be [n, Hkv, d]")
+    _need(key_new.dtype == value_new.dtype == q.dtype, "dtype mismatch")
+    _need(block_tables.dim() == 2 and block_tables.shape[0] == n, "block_tables must be [num_seqs, T]")
+    _need(context_lens.shape == (n,), "context_lens must be [num_seqs]")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out.shape == q.shape and out.dtype == q.dtype, "out must match q")
+    if workspace is None:
+        workspace = make_workspace(hq, hkv, d, q.device)
+    st = lib().pa_decode_append_fp8(
+        _dev(q, "q"), _dev(key_new, "key_new"), _dev(value_new, "value_new"),
+        _fp8_cache(k_cache, "k_cache"), _fp8_cache(v_cache, "v_cache"),
+        _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+        _dev(context_lens, "context_lens", torch.int32), n, hq, hkv, d, bs, nb, float(scale),
+        float(k_scale), float(v_scale), _dev(out, "out"), _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _dtype_code(q), _stream_ptr(stream, q.device))
+    _check(st, "pa_decode_append_fp8")
     return out
 
 

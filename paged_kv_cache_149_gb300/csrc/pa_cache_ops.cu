@@ -49,14 +49,6 @@ __global__ void __launch_bounds__(128) reshape_and_cache_kernel(
   }
 }
 
-// Two float32 values -> two E4M3 codes, round to nearest-even, magnitudes above 448
-// clamped to 448 (satfinite): `hi` in the upper byte, `lo` in the lower.
-__device__ __forceinline__ uint16_t e4m3x2_of(float hi, float lo) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
 // FP8 cache write: each 16-bit input x becomes the E4M3 code of x / scale, the division in
 // IEEE float32 and the rounding to nearest-even with magnitudes above 448 clamped (the
 // hardware's satfinite conversion).  A thread makes one 16-byte chunk of codes (16
@@ -88,20 +80,43 @@ __global__ void __launch_bounds__(128) reshape_and_cache_fp8_kernel(
     // 16 inputs = two 16-byte vectors of the 16-bit row
     const uint4* src = (is_v ? value : key) +
                        ((static_cast<size_t>(i) * num_kv_heads + h) * chunks_per_row + c) * 2;
-    const uint4 a = src[0], b = src[1];
-    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    uint32_t out[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float2 x0 = unpack2<T>(w[2 * k]), x1 = unpack2<T>(w[2 * k + 1]);
-      // codes of elements 4k .. 4k+3, element 4k in the low byte
-      out[k] = static_cast<uint32_t>(e4m3x2_of(__fdiv_rn(x0.y, scale), __fdiv_rn(x0.x, scale))) |
-               (static_cast<uint32_t>(e4m3x2_of(__fdiv_rn(x1.y, scale), __fdiv_rn(x1.x, scale)))
-                << 16);
-    }
     const size_t dst =
         ((static_cast<size_t>(blk) * num_kv_heads + h) * block_size + row) * chunks_per_row + c;
-    (is_v ? v_cache : k_cache)[dst] = make_uint4(out[0], out[1], out[2], out[3]);
+    (is_v ? v_cache : k_cache)[dst] = quantize16_e4m3<T>(src[0], src[1], scale);
+  }
+}
+
+// The FP8 cache write of one decode step's newest tokens: sequence s's row goes to position
+// context_lens[s] - 1, found through the table.  A sequence whose length or table entry is
+// invalid writes nothing (the decode that follows flags and zeroes it).  One CTA per
+// sequence.
+template <typename T>
+__global__ void __launch_bounds__(128) append_newest_fp8_kernel(
+    const uint4* __restrict__ key, const uint4* __restrict__ value, uint4* __restrict__ k_cache,
+    uint4* __restrict__ v_cache, const int32_t* __restrict__ block_tables, int max_blocks_per_seq,
+    const int32_t* __restrict__ context_lens, int num_blocks, int num_kv_heads, int chunks_per_row,
+    int block_size, float k_scale, float v_scale) {
+  pdl_wait_primary();
+  pdl_launch_dependents();
+  const int s = blockIdx.x;
+  const int ctx = context_lens[s];
+  if (ctx < 1 || static_cast<long long>(ctx) > static_cast<long long>(max_blocks_per_seq) * block_size)
+    return;
+  const int t = ctx - 1;
+  const int blk = block_tables[static_cast<size_t>(s) * max_blocks_per_seq + t / block_size];
+  if (blk < 0 || blk >= num_blocks) return;
+  const int row = t % block_size;
+  const int n = num_kv_heads * chunks_per_row;
+  for (int j = threadIdx.x; j < 2 * n; j += blockDim.x) {
+    const bool is_v = j >= n;
+    const int jj = is_v ? j - n : j;
+    const int h = jj / chunks_per_row;
+    const int c = jj - h * chunks_per_row;
+    const uint4* src = (is_v ? value : key) +
+                       ((static_cast<size_t>(s) * num_kv_heads + h) * chunks_per_row + c) * 2;
+    const size_t dst =
+        ((static_cast<size_t>(blk) * num_kv_heads + h) * block_size + row) * chunks_per_row + c;
+    (is_v ? v_cache : k_cache)[dst] = quantize16_e4m3<T>(src[0], src[1], is_v ? v_scale : k_scale);
   }
 }
 
@@ -205,6 +220,35 @@ int reshape_and_cache_fp8_launch(const void* key, const void* value, void* k_cac
                                 static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
                                 slot_mapping, slots, num_kv_heads, head_dim / 16, block_size,
                                 k_scale, v_scale, err);
+  return e == cudaSuccess ? 0 : -3;
+}
+
+int append_newest_fp8_launch(const void* key, const void* value, void* k_cache, void* v_cache,
+                             const int32_t* block_tables, int max_blocks_per_seq,
+                             const int32_t* context_lens, int num_seqs, int num_blocks,
+                             int num_kv_heads, int head_dim, int block_size, float k_scale,
+                             float v_scale, bool bf16, cudaStream_t stream) {
+  if (num_seqs == 0) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_seqs);
+  cfg.blockDim = dim3(128);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e =
+      bf16 ? cudaLaunchKernelEx(&cfg, append_newest_fp8_kernel<__nv_bfloat16>,
+                                static_cast<const uint4*>(key), static_cast<const uint4*>(value),
+                                static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
+                                block_tables, max_blocks_per_seq, context_lens, num_blocks,
+                                num_kv_heads, head_dim / 16, block_size, k_scale, v_scale)
+           : cudaLaunchKernelEx(&cfg, append_newest_fp8_kernel<__half>,
+                                static_cast<const uint4*>(key), static_cast<const uint4*>(value),
+                                static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
+                                block_tables, max_blocks_per_seq, context_lens, num_blocks,
+                                num_kv_heads, head_dim / 16, block_size, k_scale, v_scale);
   return e == cudaSuccess ? 0 : -3;
 }
 

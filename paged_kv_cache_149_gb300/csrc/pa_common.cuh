@@ -160,4 +160,29 @@ __device__ __forceinline__ __half from_float<__half>(float v) {
   return __float2half_rn(v);
 }
 
+// FP8 (E4M3) quantisation shared by the cache-write kernel and the fused decode step, so
+// that both produce the same codes: x / scale in IEEE float32, then round to nearest-even
+// with magnitudes above 448 clamped (the hardware's satfinite conversion).
+// Two float32 values -> two codes, `hi` in the upper byte, `lo` in the lower.
+__device__ __forceinline__ uint16_t e4m3x2_of(float hi, float lo) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Sixteen 16-bit values (two 16-byte vectors, element 0 first) -> their 16 codes.
+template <typename T>
+__device__ __forceinline__ uint4 quantize16_e4m3(const uint4& a, const uint4& b, float scale) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  uint32_t out[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 x0 = unpack2<T>(w[2 * k]), x1 = unpack2<T>(w[2 * k + 1]);
+    out[k] = static_cast<uint32_t>(e4m3x2_of(__fdiv_rn(x0.y, scale), __fdiv_rn(x0.x, scale))) |
+             (static_cast<uint32_t>(e4m3x2_of(__fdiv_rn(x1.y, scale), __fdiv_rn(x1.x, scale)))
+              << 16);
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
 }  // namespace pa

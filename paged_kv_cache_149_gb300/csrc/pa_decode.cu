@@ -1,1246 +1,15 @@
-// Paged decode attention for sm_103a.
-//
-// Per sequence s and query head h (kv head g = h / G):
-//   z_t = scale * <q[s,h], K_s[t,g]>,  out[s,h] = sum_t softmax(z)_t V_s[t,g],  t < ctx_s
-// with K_s[t] = k_cache[block_tables[s][t / B], g, t % B, :] (daiw.org "Paged Attention",
-// sections 直觉 and 定义; chenyuan1125 "vllm-pagedattention", section 页表真正解开的…: the
-// kernel finds each K/V block through the table and does score, softmax and weighted sum
-// block by block).
-//
-// Design (GB300: 152 SMs, HBM-bound at <= 1 FLOP/byte per query head):
-// * A "pair" is one kv head (or a chunk of up to 16 of its query heads) of one sequence.
-//   The pairs of a sequence are taken in groups of gs (the largest power of two <= 8 that
-//   divides the pair count); a "family" is one sequence's group.  A family's work is
-//   ns(s) units of 16 tokens x gs pairs (a "stage" is one unit of one pair: 16 K rows and
-//   16 V rows), plus a fixed charge.  The batch's stages, in (family, unit, pair) order,
-//   are cut into gridDim.x equal contiguous shares, one per persistent CTA (one per SM).
-// * Warp w of a CTA works on pair w / P of every family (P = 8 / gs warps per pair, each
-//   taking every P-th unit).  With 8 or more kv heads (gs = 8) a warp owns one kv head
-//   outright: it streams its pair's stages straight across family boundaries and never
-//   waits for another warp.  With fewer, the P warps of a pair merge their partial
-//   softmax states through shared memory under a named barrier of their own.
-// * Loads: each warp copies its own stages, kAhead ahead of the one it computes, with
-//   16-byte cp.async copies (every lane copies a slice of the stage's K and V rows) into a
-//   private ring of swizzled shared-memory slots, and waits with cp.async.wait_group.
-//   Spreading the copies over all eight warps keeps enough bytes in flight per SM to reach
-//   the HBM limit; a single issuing warp, with TMA or with cp.async, streams about 26 GB/s
-//   per SM on GB300.  Rows past the context are zero-filled by the copy itself (source
-//   size 0) and never read.
-// * Math per stage on warp-level tensor cores (m16n8k16, fp32 accumulate) with the pair's
-//   query heads as the N = 8 (or 16) columns: S^T = K Q^T (rows = the stage's 16 tokens),
-//   then O^T += V^T P^T (rows = d) with P = 2^(S - m) rounded to the input type and moved
-//   into B-fragment layout by an in-register transpose (movmatrix); online softmax with a
-//   running max and sum per head.  The swizzle makes every ldmatrix conflict-free.
-// * A pair cut between CTAs (split-KV) leaves one partial softmax state (O, m, l) per
-//   piece in the workspace.  When a CTA has streamed its whole share (no copies left in
-//   flight, so a fence is cheap), it counts its pieces in on a per-pair counter; the CTA
-//   that brings a pair's count to its number of pieces merges them in CTA order with a
-//   log-sum-exp reduction (the rescaling identity of online softmax that chenyuan1125,
-//   section 它和 FlashAttention…, names as FlashAttention's technique).  No CTA ever waits
-//   for another.  Cut points depend on logical positions and context lengths only, and
-//   the merge order is fixed, so permuting physical blocks gives bit-identical output.
-// * Launched as a programmatic dependent of the kernel before it in the stream: the grid
-//   is resident while that kernel drains and starts at griddepcontrol.wait.
+// Paged decode attention for sm_103a: host side and the 16-bit instantiations of the
+// kernel in pa_decode_kernel.cuh (whose header comment describes the design).
 #include <cuda_runtime.h>
 
 #include <atomic>
 #include <chrono>
 #include <cstdint>
 #include <random>
-#include <type_traits>
 
-#include "pa_common.cuh"
-#include "pa_internal.h"
+#include "pa_decode_kernel.cuh"
 
 namespace pa {
-namespace decode {
-
-constexpr int kStageTok = 16;
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
-constexpr int kMaxHeads = 16;  // query heads per pair (MMA columns)
-constexpr float kLog2e = 1.4426950408889634f;
-// Stage-equivalents charged per family on top of its stages when cutting the batch into
-// per-SM shares.  A family switch (a new table row, the pair-end writes) and the cut-pair
-// work at the ends of a share cost it time; on GB300 a charge of 32 stages balanced the
-// shares best over batches of long, short and mixed sequences (16: 58.7 us, 32: 56.8 us,
-// 64: 58.4 us on 64 sequences of 128..2048 tokens; 16 x 8192 tokens: 102.9 / 96.5 / 93.9).
-constexpr int kSegCost = 32;
-
-// EB: bytes per cached K/V element (2 for fp16/bf16 blocks, 1 for FP8 E4M3 blocks).
-template <int D, int EB = 2>
-struct Geo {
-  static constexpr int kRowBytes = D * EB;
-  static constexpr int kRowChunks = kRowBytes / 16;         // 16-byte chunks per row
-  static constexpr int kKBytes = kStageTok * kRowBytes;     // K rows of a stage
-  static constexpr int kStageBytes = 2 * kKBytes;           // K then V
-  // Ring slots per warp (192 KB in all, at most 32) and how many stages ahead a warp loads.
-  static constexpr int kSlots0 = (192 * 1024) / (kStageBytes * kWarps);
-  static constexpr int kSlots = kSlots0 > 32 ? 32 : kSlots0;
-  static constexpr int kAhead = kSlots - 1;
-  static constexpr int kRowsPerPass = 32 / kRowChunks;      // rows one warp-wide copy covers
-  static constexpr int kPasses = kStageTok / kRowsPerPass;  // copies per lane per K (or V)
-  static constexpr int kKSteps = D / 16;                    // MMA k-steps of K Q^T
-};
-
-struct Params {
-  const uint8_t* q;
-  const uint8_t* k_cache;
-  const uint8_t* v_cache;
-  // Fused cache write (pa_decode_append), else null: the newest token of each sequence,
-  // [n][Hkv][D].  Its row is attended from here and stored at position ctx - 1.
-  const uint8_t* key_new;
-  const uint8_t* value_new;
-  const int32_t* block_tables;
-  const int32_t* context_lens;
-  uint8_t* out;
-  int num_seqs, num_q_heads, num_kv_heads, group, heads_per_pair, head_chunks;
-  int gs, log2_gs, ngroups, phases;  // pairs per family, families per sequence, warps per pair
-  int max_blocks_per_seq, block_size, log2_block, num_blocks, max_ctx;
-  int seg_cost;  // stage units charged per family on top of its stages
-  float scale_log2;
-  float out_scale;  // FP8 blocks: v_scale, applied to every output row (else unused)
-  // [grid][gs]: arrivals at cut pair (first CTA, pi): epoch tag << 24 | pieces counted in
-  unsigned long long* counters;
-  unsigned long long epoch;  // 40-bit tag, different from the previous call's
-  float* part_acc;  // [grid][2][gs][heads_per_pair][D]
-  float* part_ml;   // [grid][2][gs][heads_per_pair][2]  (m, l); l < 0: the piece saw a bad block
-  unsigned* err;
-};
-
-// Units (16-token stages per pair) of a sequence; an invalid context length counts one.
-__device__ __forceinline__ int pair_stages(int ctx, int max_ctx) {
-  return (ctx >= 1 && ctx <= max_ctx) ? (ctx + kStageTok - 1) / kStageTok : 1;
-}
-
-// Family (sequence s, pair group g) and its place in the batch's stage order.
-struct Fam {
-  int s, g, ctx, ns;
-  bool ok;        // 1 <= ctx <= max_ctx
-  long long pre;  // first stage unit of the family
-  long long fw;   // its weight: ns * gs + seg_cost
-};
-
-__device__ __forceinline__ void fam_load(Fam& f, const Params& p) {
-  f.ctx = __ldg(p.context_lens + f.s);
-  f.ok = f.ctx >= 1 && f.ctx <= p.max_ctx;
-  f.ns = pair_stages(f.ctx, p.max_ctx);
-  f.fw = static_cast<long long>(f.ns) * p.gs + p.seg_cost;
-}
-
-__device__ __forceinline__ void fam_next(Fam& f, const Params& p) {
-  f.pre += f.fw;
-  if (++f.g == p.ngroups) {
-    f.g = 0;
-    if (++f.s < p.num_seqs) fam_load(f, p);
-  }
-}
-
-__device__ __forceinline__ bool fam_valid(const Fam& f) { return f.ok; }
-
-// ceil(x / 2^k) for any sign of x.
-__device__ __forceinline__ long long ceil_shift(long long x, int k) {
-  return x > 0 ? (x + (1ll << k) - 1) >> k : -((-x) >> k);
-}
-
-// Units [x, y) of pair pi of family f whose stages lie in the share [w0, w1).
-__device__ __forceinline__ int2 unit_range(const Fam& f, int pi, long long w0, long long w1,
-                                           const Params& p) {
-  const long long base = f.pre + p.seg_cost + pi;
-  const long long a = ceil_shift(w0 - base, p.log2_gs), b = ceil_shift(w1 - base, p.log2_gs);
-  return make_int2(static_cast<int>(max(0ll, min(static_cast<long long>(f.ns), a))),
-                   static_cast<int>(max(0ll, min(static_cast<long long>(f.ns), b))));
-}
-
-// Does this share hold a piece of the pair: some of its units, or none while the pair runs
-// on both sides of the share (an empty middle piece, published so the merge can count on it)?
-__device__ __forceinline__ bool has_piece(int2 r, int ns) {
-  return r.x < r.y || (r.x > 0 && r.x < ns);
-}
-
-// Share [w0, w1) of CTA c when W units are cut into G shares, the first W % G one larger.
-__device__ __forceinline__ void share_of(int c, long long W, int G, long long& w0, long long& w1) {
-  const long long q = W / G, r = W % G;
-  w0 = c * q + min(static_cast<long long>(c), r);
-  w1 = w0 + q + (c < r ? 1 : 0);
-}
-
-// Owner CTA of stage unit x.
-__device__ __forceinline__ int owner_of(long long x, long long W, int G) {
-  const long long q = W / G, r = W % G;
-  if (x < r * (q + 1)) return static_cast<int>(x / (q + 1));
-  return static_cast<int>(r + (x - r * (q + 1)) / q);
-}
-
-struct PairHeads {
-  int kvh, h0, nh;
-};
-
-__device__ __forceinline__ PairHeads pair_heads(const Params& p, int pair) {
-  PairHeads ph;
-  ph.kvh = pair / p.head_chunks;
-  const int hc = pair - ph.kvh * p.head_chunks;
-  ph.h0 = ph.kvh * p.group + hc * p.heads_per_pair;
-  ph.nh = min(p.heads_per_pair, p.group - hc * p.heads_per_pair);
-  return ph;
-}
-
-// This warp's stages in order: for every family of the share, the units of its pair with
-// unit index = its phase (mod P).  Families with an invalid context carry no stages.
-struct Stage {
-  int s, kvh, t0, nt;  // sequence, kv head, first token, valid tokens (1..16)
-  bool last;           // holds the context's last token
-};
-
-struct StageIt {
-  Fam f;
-  int kvh, j, jb;
-};
-
-__device__ __forceinline__ void stage_it_enter(StageIt& it, int pi, int phase, long long w0,
-                                               long long w1, const Params& p) {
-  const int2 r = unit_range(it.f, pi, w0, w1, p);
-  if (!fam_valid(it.f) || r.x >= r.y) {
-    it.j = it.jb = 0;
-    return;
-  }
-  it.kvh = pair_heads(p, it.f.g * p.gs + pi).kvh;
-  it.j = r.x + (phase - r.x % p.phases + p.phases) % p.phases;
-  it.jb = r.y;
-}
-
-__device__ __forceinline__ bool next_stage(StageIt& it, int pi, int phase, long long w0, long long w1,
-                                           Stage& st, const Params& p) {
-  for (;;) {
-    if (it.j < it.jb) {
-      st.s = it.f.s;
-      st.kvh = it.kvh;
-      st.t0 = it.j * kStageTok;
-      st.nt = min(kStageTok, it.f.ctx - st.t0);
-      st.last = st.t0 + st.nt == it.f.ctx;
-      it.j += p.phases;
-      return true;
-    }
-    fam_next(it.f, p);
-    if (it.f.s >= p.num_seqs || it.f.pre >= w1) return false;
-    stage_it_enter(it, pi, phase, w0, w1, p);
-  }
-}
-
-// Block-table entries of a stage: x = the block holding its first token, y = the next
-// block when the stage spans two blocks (block_size 8), else x.
-__device__ __forceinline__ int2 stage_entries(const Stage& st, const Params& p) {
-  const int32_t* trow = p.block_tables + static_cast<size_t>(st.s) * p.max_blocks_per_seq;
-  const int j0 = st.t0 >> p.log2_block;
-  int2 e;
-  e.x = __ldg(trow + j0);
-  e.y = ((st.t0 & (p.block_size - 1)) + st.nt > p.block_size) ? __ldg(trow + j0 + 1) : e.x;
-  return e;
-}
-
-// 16-byte global -> shared copy through L2 only; the bytes past src_bytes (0 or 16) are
-// zero-filled, and src_bytes = 0 reads nothing.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-               "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-
-// Transpose of an 8x8 matrix of 16-bit values held one 32-bit pair per lane.
-__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
-  uint32_t y;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
-  return y;
-}
-
-// D += A * B, m16n8k16, fp32 accumulate.
-template <typename T>
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1);
-
-template <>
-__device__ __forceinline__ void mma16816<__nv_bfloat16>(float (&d)[4], const uint32_t (&a)[4],
-                                                        uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-      "{%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-template <>
-__device__ __forceinline__ void mma16816<__half>(float (&d)[4], const uint32_t (&a)[4],
-                                                 uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-      "{%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// Byte offset of (row, 16-byte chunk) in a stage's K or V rows: chunk c of the row lives
-// in column half c / 8, and the 128-byte swizzle permutes chunks within each row.
-__device__ __forceinline__ uint32_t swz(int row, int chunk) {
-  return static_cast<uint32_t>((chunk >> 3) * (kStageTok * 128) + row * 128 +
-                               (((chunk & 7) ^ (row & 7)) << 4));
-}
-
-// FP8 stages: a row is D bytes.  At D = 128 the 16-byte chunk c of row r sits at c ^ (r % 8)
-// so that the fragment loads below (eight lanes: four chunks of two rows, or one chunk of
-// eight rows) hit distinct banks; at D = 64 rows are packed as they come.
-template <int D>
-__device__ __forceinline__ uint32_t swz8(int row, int chunk) {
-  return D == 128 ? static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4))
-                  : static_cast<uint32_t>(row * D + (chunk << 4));
-}
-
-// Row of O^T held in MMA accumulator row r (0..15) of m-tile mt.  16-bit blocks: d = 16 mt
-// + r.  FP8 blocks permute d so that every lane builds its V fragments from contiguous
-// bytes: rows r and r + 8 are the adjacent d = (D/8)(r % 8) + 2 mt and that + 1.
-template <int D, bool F8>
-__device__ __forceinline__ int drow(int mt, int r) {
-  return F8 ? (r & 7) * (D / 8) + 2 * mt + (r >> 3) : 16 * mt + r;
-}
-
-// Two E4M3 values (low byte first) -> f16x2, exact (every E4M3 value is an f16 normal).
-__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t two_bytes) {
-  uint32_t r;
-  const uint16_t v = static_cast<uint16_t>(two_bytes);
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
-  return r;
-}
-
-// A piece of a cut pair as every holder of a piece sees it: the CTAs holding its first and
-// last pieces, where the first CTA stored its piece (slot 0 when the pair's family is that
-// CTA's first family), and the pair's sequence and heads.
-struct CutPiece {
-  int c_first, c_last, first_slot, s, h0, nh;
-};
-
-__device__ __forceinline__ CutPiece cut_piece(const Fam& f, int pi, const PairHeads& ph,
-                                              long long W, int G, const Params& p) {
-  CutPiece cp;
-  const long long first_unit = f.pre + p.seg_cost + pi;
-  const long long last_unit = first_unit + static_cast<long long>(f.ns - 1) * p.gs;
-  cp.c_first = owner_of(first_unit, W, G);
-  cp.c_last = owner_of(last_unit, W, G);
-  long long w0f, w1f;
-  share_of(cp.c_first, W, G, w0f, w1f);
-  cp.first_slot = w0f >= f.pre ? 0 : 1;
-  cp.s = f.s;
-  cp.h0 = ph.h0;
-  cp.nh = ph.nh;
-  return cp;
-}
-
-// Count one piece in at a pair's counter; returns the pieces counted so far this call.  The
-// counter holds epoch << 24 | count; a value with another epoch is stale (an earlier call
-// or never-written workspace) and counts as zero.  The loop retries only when another
-// arrival changed the counter in between, so it ends after at most one try per piece.
-__device__ __forceinline__ int arrive(unsigned long long* ctr, unsigned long long epoch) {
-  unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(ctr);
-  for (int tries = 0; tries < (1 << 20); ++tries) {
-    const unsigned long long want = (cur >> 24) == epoch ? cur + 1 : (epoch << 24) | 1ull;
-    const unsigned long long prev = atomicCAS(ctr, cur, want);
-    if (prev == cur) return static_cast<int>(want & 0xffffffull);
-    cur = prev;
-  }
-  return -1;  // (unreachable in practice: no merge rather than a wrong one)
-}
-
-// Merge the pieces of a cut pair held by CTAs c..c_last (c's piece in slot `first_slot`,
-// the others in slot 0), pieces taken in CTA order so the result is deterministic:
-//   M = max m_i,  w_i = 2^(m_i - M) (0 for an empty piece),  L = sum l_i w_i,
-//   out = sum w_i acc_i / L
-// (the log-sum-exp rescaling of online softmax); zeros when a piece saw a bad block.
-// merge_staged computes the same sums in the same order with the same fused multiply-adds,
-// so a pair's output does not depend on which of the two merges it.
-template <int D, typename T, bool F8>
-__device__ void merge_pieces(const Params& p, int pi, int c, int first_slot, int c_last, int nh,
-                             T* out_rows, int gt, int gthreads) {
-  constexpr int C4 = D / 4;  // 4-float chunks per head row
-  const int hpp = p.heads_per_pair;
-  const int hstep = gthreads / C4;  // heads the group covers side by side
-  const int d4 = (gt % C4) * 4;
-  auto piece_of = [&](int cc) {
-    return (static_cast<size_t>(cc) * 2 + (cc == c ? first_slot : 0)) * p.gs + pi;
-  };
-  for (int h = gt / C4; h < nh; h += hstep) {
-    float M = -INFINITY;
-    bool bad = false;
-    for (int cc = c; cc <= c_last; ++cc) {
-      const float* ml = p.part_ml + (piece_of(cc) * hpp + h) * 2;
-      M = fmaxf(M, __ldcg(ml));
-      bad |= __ldcg(ml + 1) < 0.f;
-    }
-    float L = 0.f;
-    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int cc = c; cc <= c_last; ++cc) {
-      const size_t pc = piece_of(cc);
-      const float* ml = p.part_ml + (pc * hpp + h) * 2;
-      const float m = __ldcg(ml), l = __ldcg(ml + 1);
-      const float w = m == -INFINITY ? 0.f : exp2f(m - M);
-      L = fmaf(l, w, L);
-      const float4 a = __ldcg(reinterpret_cast<const float4*>(p.part_acc + (pc * hpp + h) * D + d4));
-      O.x = fmaf(a.x, w, O.x);
-      O.y = fmaf(a.y, w, O.y);
-      O.z = fmaf(a.z, w, O.z);
-      O.w = fmaf(a.w, w, O.w);
-    }
-    uint2 packed = make_uint2(0u, 0u);
-    if (!bad) {
-      const float inv = F8 ? p.out_scale / L : 1.f / L;
-      packed.x = pack2<T>(O.x * inv, O.y * inv);
-      packed.y = pack2<T>(O.z * inv, O.w * inv);
-    }
-    *reinterpret_cast<uint2*>(out_rows + h * D + d4) = packed;
-  }
-}
-
-// Wait for phase 0 of a single-use mbarrier, bounded by kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait_once(uint32_t bar) {
-  if (mbar_try_wait(bar, 0)) return true;
-  const unsigned long long t0 = global_timer_ns();
-  for (;;) {
-    if (mbar_try_wait(bar, 0)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
-  }
-}
-
-// One warp merges the cut pairs it completed (up to two) through its own ring, which is
-// idle once the share is streamed: every piece's O is copied in by one bulk copy per piece
-// and its (m, l) by plain loads (a single round trip to L2 for all pieces), then the
-// pieces are folded in CTA order: M = max m_i, w_i = 2^(m_i - M), L = sum l_i w_i,
-// out = sum w_i acc_i / L.  Returns false, having done nothing, when the pieces do not fit
-// in the ring.
-template <int D, typename T, bool F8>
-__device__ bool merge_staged(const Params& p, int pi, const CutPiece& job0, const CutPiece& job1,
-                             int njobs, uint32_t ring, uint8_t* ring_ptr, int ring_bytes,
-                             uint32_t bar, int lane) {
-  const int hpp = p.heads_per_pair;
-  int need = 0;
-  for (int j = 0; j < njobs; ++j) {
-    const CutPiece& cp = j == 0 ? job0 : job1;
-    need += (cp.c_last - cp.c_first + 1) * cp.nh * (D * 4 + 8);
-  }
-  if (need > ring_bytes) return false;
-  // layout in the ring: per job, per piece: acc [nh][D] floats, then all (m, l) pairs.
-  // Lane i copies piece i's acc with one bulk copy (cp.async.bulk; completion counted in
-  // bytes on this warp's mbarrier); the (m, l) pairs come in through plain loads.
-  const int np0 = job0.c_last - job0.c_first + 1;
-  const int np1 = njobs > 1 ? job1.c_last - job1.c_first + 1 : 0;
-  const uint32_t rb0 = job0.nh * D * 4, rb1 = job1.nh * D * 4;
-  const uint32_t acc_bytes = np0 * rb0 + np1 * rb1;
-  __syncwarp();
-  if (lane == 0) mbar_arrive_expect_tx(bar, acc_bytes);
-  __syncwarp();
-  // the ring was last read through the generic proxy; the bulk copies write it through
-  // the async proxy
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  for (int i = lane; i < np0 + np1; i += 32) {
-    const bool first = i < np0;
-    const CutPiece& cp = first ? job0 : job1;
-    const int cc = cp.c_first + (first ? i : i - np0);
-    const size_t piece = (static_cast<size_t>(cc) * 2 + (cc == cp.c_first ? cp.first_slot : 0)) * p.gs + pi;
-    const uint32_t off = first ? i * rb0 : np0 * rb0 + (i - np0) * rb1;
-    bulk_g2s(ring + off, p.part_acc + piece * hpp * D, first ? rb0 : rb1, bar);
-  }
-  float2* ml = reinterpret_cast<float2*>(ring_ptr + acc_bytes);
-  {
-    int k = 0;
-    for (int j = 0; j < njobs; ++j) {
-      const CutPiece& cp = j == 0 ? job0 : job1;
-      const int np = cp.c_last - cp.c_first + 1;
-      for (int i = lane; i < np * cp.nh; i += 32) {
-        const int cc = cp.c_first + i / cp.nh, h = i % cp.nh;
-        const size_t piece = (static_cast<size_t>(cc) * 2 + (cc == cp.c_first ? cp.first_slot : 0)) * p.gs + pi;
-        const float* src = p.part_ml + (piece * hpp + h) * 2;
-        ml[k + i] = make_float2(__ldcg(src), __ldcg(src + 1));
-      }
-      k += np * cp.nh;
-    }
-  }
-  __syncwarp();  // (the (m, l) stores, before lanes read other lanes' entries)
-  // Pass 1, one lane per (job, head): M = max m_i, then each piece's weight 2^(m_i - M)
-  // (0 for an empty piece) in place of m_i, and L = sum l_i 2^(m_i - M) in place of the
-  // first piece's l (bad pieces, l < 0, make L negative: the head's output is zeros).
-  {
-    int moff = 0;
-    for (int j = 0; j < njobs; ++j) {
-      const CutPiece& cp = j == 0 ? job0 : job1;
-      const int np = cp.c_last - cp.c_first + 1;
-      if (lane < cp.nh) {
-        const int h = lane;
-        float M = -INFINITY;
-        bool bad = false;
-        for (int i = 0; i < np; ++i) {
-          const float2 v = ml[moff + i * cp.nh + h];
-          M = fmaxf(M, v.x);
-          bad |= v.y < 0.f;
-        }
-        float L = 0.f;
-        for (int i = 0; i < np; ++i) {
-          float2 v = ml[moff + i * cp.nh + h];
-          const float w = v.x == -INFINITY ? 0.f : exp2f(v.x - M);
-          L = fmaf(v.y, w, L);
-          v.x = w;
-          ml[moff + i * cp.nh + h] = v;
-        }
-        ml[moff + h].y = bad ? -1.f : L;  // (read back below only through this slot)
-      }
-      moff += np * cp.nh;
-    }
-  }
-  if (!mbar_wait_once(bar)) {  // (bounded; never expected to expire)
-    if (lane == 0) atomicOr(p.err, kErrTimeout);
-    return true;
-  }
-  __syncwarp();
-  // Pass 2: out = sum_i w_i acc_i / L, pieces in CTA order.
-  constexpr int C4 = D / 4;
-  int aoff = 0, moff = 0;
-  for (int j = 0; j < njobs; ++j) {
-    const CutPiece& cp = j == 0 ? job0 : job1;
-    const int np = cp.c_last - cp.c_first + 1;
-    T* out_rows = reinterpret_cast<T*>(p.out) + (static_cast<size_t>(cp.s) * p.num_q_heads + cp.h0) * D;
-    const float* acc = reinterpret_cast<const float*>(ring_ptr + aoff);
-    for (int idx = lane; idx < cp.nh * C4; idx += 32) {
-      const int h = idx / C4, d4 = (idx % C4) * 4;
-      float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-      for (int i = 0; i < np; ++i) {
-        const float w = ml[moff + i * cp.nh + h].x;
-        const float4 a = *reinterpret_cast<const float4*>(acc + (i * cp.nh + h) * D + d4);
-        O.x = fmaf(a.x, w, O.x);
-        O.y = fmaf(a.y, w, O.y);
-        O.z = fmaf(a.z, w, O.z);
-        O.w = fmaf(a.w, w, O.w);
-      }
-      const float L = ml[moff + h].y;
-      uint2 packed = make_uint2(0u, 0u);
-      if (L >= 0.f) {
-        const float inv = F8 ? p.out_scale / L : 1.f / L;
-        packed.x = pack2<T>(O.x * inv, O.y * inv);
-        packed.y = pack2<T>(O.z * inv, O.w * inv);
-      }
-      *reinterpret_cast<uint2*>(out_rows + h * D + d4) = packed;
-    }
-    aoff += np * cp.nh * D * 4;
-    moff += np * cp.nh;
-  }
-  return true;
-}
-
-template <int D, int EB>
-struct Smem {
-  uint8_t ring[kWarps][Geo<D, EB>::kSlots][Geo<D, EB>::kStageBytes];  // 1024-byte aligned
-  float xo[kWarps][4][D];  // per-warp O rows, 4 heads per exchange round
-  float xm[kWarps][kMaxHeads], xl[kWarps][kMaxHeads];
-  long long scan[kWarps];
-  long long start_pre;
-  int start_s;
-  int last[kWarps];  // per pair group: this CTA's arrival completed the pair
-  unsigned long long merge_bar[kWarps];  // per warp, single use: the staged merge's copies
-};
-
-// Q^T of a pair as MMA B fragments (column n = head 8*nt + lane / 4; heads >= nh are zero).
-template <int D, int NTH>
-__device__ __forceinline__ void load_q(const Params& p, int s, int h0, int nh, int lane,
-                                       uint32_t (&qb)[D / 16][NTH][2]) {
-  const int r0 = lane >> 2, qc = 2 * (lane & 3);
-  const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-      p.q + (static_cast<size_t>(s) * p.num_q_heads + h0) * D * 2);
-#pragma unroll
-  for (int nt = 0; nt < NTH; ++nt) {
-    const int h = nt * 8 + r0;
-    const bool hv = h < nh;
-#pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-      const int col = 16 * ks + qc;
-      qb[ks][nt][0] = hv ? __ldg(qrow + (h * D + col) / 2) : 0u;
-      qb[ks][nt][1] = hv ? __ldg(qrow + (h * D + col + 8) / 2) : 0u;
-    }
-  }
-}
-
-// The same for FP8 blocks, as f16 (the type the E4M3 values are widened to), with d in the
-// order the K fragments use: k-step ks takes d = (D/4) t + 4 ks + {0, 1} into b0 and
-// + {2, 3} into b1, t = lane % 4.  bf16 queries are rounded to f16 (exact within the f16
-// normal range).
-template <int D, int NTH, typename T>
-__device__ __forceinline__ void load_q8(const Params& p, int s, int h0, int nh, int lane,
-                                        uint32_t (&qb)[D / 16][NTH][2]) {
-  const int r0 = lane >> 2, t = lane & 3;
-  const uint2* qrow = reinterpret_cast<const uint2*>(
-      p.q + (static_cast<size_t>(s) * p.num_q_heads + h0) * D * 2);
-#pragma unroll
-  for (int nt = 0; nt < NTH; ++nt) {
-    const int h = nt * 8 + r0;
-    const bool hv = h < nh;
-#pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-      const uint2 w = hv ? __ldg(qrow + (h * D + (D / 4) * t + 4 * ks) / 4) : make_uint2(0u, 0u);
-      if (std::is_same<T, __half>::value) {
-        qb[ks][nt][0] = w.x;
-        qb[ks][nt][1] = w.y;
-      } else {
-        const float2 a = unpack2<T>(w.x), b = unpack2<T>(w.y);
-        qb[ks][nt][0] = pack2<__half>(a.x, a.y);
-        qb[ks][nt][1] = pack2<__half>(b.x, b.y);
-      }
-    }
-  }
-}
-
-// The next family (after f) where pair pi has units to compute; false at the share's end.
-__device__ __forceinline__ bool next_busy_fam(Fam f, int pi, long long w0, long long w1,
-                                              const Params& p, Fam& out) {
-  for (;;) {
-    fam_next(f, p);
-    if (f.s >= p.num_seqs || f.pre >= w1) return false;
-    const int2 r = unit_range(f, pi, w0, w1, p);
-    if (fam_valid(f) && r.x < r.y) {
-      out = f;
-      return true;
-    }
-  }
-}
-
-// F8: K/V blocks hold E4M3 codes (scales folded into scale_log2 and out_scale); the MMAs
-// then run in f16 on the widened values.
-template <int D, int NTH, typename T, bool F8>
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ Params p) {
-  constexpr int EB = F8 ? 1 : 2;
-  using G_ = Geo<D, EB>;
-  using TM = typename std::conditional<F8, __half, T>::type;  // MMA operand type
-  constexpr int R = G_::kSlots;
-  constexpr int KS = G_::kKSteps;
-  constexpr int MT = D / 16;  // m-tiles of O^T (16 rows of d each)
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw_addr = smem_addr(smem_raw);
-  Smem<D, EB>& sm = *reinterpret_cast<Smem<D, EB>*>(smem_raw + (((raw_addr + 1023) & ~1023u) - raw_addr));
-
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
-  const int P = p.phases;
-  const int pi = warp / P;     // this warp's pair within each family
-  const int phase = warp % P;  // and its units: unit index = phase (mod P)
-  const int gt = phase * 32 + lane;  // thread index within the pair's P warps
-  const int gthreads = P * 32;
-  // the pair's P warps: their own named barrier (ids 1..8), or just the warp when P = 1
-  auto gsync = [&]() {
-    if (P == 1) __syncwarp();
-    else named_bar_sync(1 + pi, gthreads);
-  };
-  auto gor = [&](bool v) -> bool {
-    return P == 1 ? (__any_sync(0xffffffffu, v) != 0) : bar_red_or(1 + pi, gthreads, v);
-  };
-
-  // The kernel before this one in the stream (say the cache write) has finished and its
-  // writes are visible past this point; the next one may start launching.
-  pdl_wait_primary();
-  pdl_launch_dependents();
-
-  if (lane == 0) {
-    mbar_init(smem_addr(&sm.merge_bar[warp]), 1);
-    fence_mbar_init();
-  }
-
-  // ---- setup: total units W, this CTA's share [w0, w1), and its first family ----
-  const int per = (p.num_seqs + kThreads - 1) / kThreads;
-  const int sa = min(p.num_seqs, tid * per), sb = min(p.num_seqs, sa + per);
-  long long mine = 0;
-  for (int s = sa; s < sb; ++s)
-    mine += static_cast<long long>(p.ngroups) *
-            (static_cast<long long>(pair_stages(__ldg(p.context_lens + s), p.max_ctx)) * p.gs +
-             p.seg_cost);
-  long long incl = mine;  // inclusive scan of `mine` over the block
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const long long v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  if (lane == 31) sm.scan[warp] = incl;
-  __syncthreads();
-  long long before = 0, W = 0;
-  for (int w = 0; w < kWarps; ++w) {
-    if (w < warp) before += sm.scan[w];
-    W += sm.scan[w];
-  }
-  const long long excl = before + incl - mine;
-  const int G = gridDim.x;
-  const int c = blockIdx.x;
-  long long w0, w1;
-  share_of(c, W, G, w0, w1);
-  if (w0 < w1 && excl <= w0 && w0 < excl + mine) {
-    long long pre = excl;
-    int s = sa;
-    for (;; ++s) {
-      const long long u = static_cast<long long>(p.ngroups) *
-                          (static_cast<long long>(pair_stages(__ldg(p.context_lens + s), p.max_ctx)) *
-                               p.gs + p.seg_cost);
-      if (w0 < pre + u) break;
-      pre += u;
-    }
-    sm.start_s = s;
-    sm.start_pre = pre;
-  }
-  __syncthreads();
-  if (w0 >= w1) return;  // more CTAs than units: nothing here (uniform over the CTA)
-
-  Fam first;
-  first.s = sm.start_s;
-  first.g = 0;
-  first.pre = sm.start_pre;
-  fam_load(first, p);
-  while (w0 >= first.pre + first.fw) {  // the family holding unit w0
-    first.pre += first.fw;
-    ++first.g;
-  }
-
-  // ---- this warp's copy stream: kAhead stages in flight ahead of the one computed ----
-  const uint32_t ring = smem_addr(sm.ring[warp][0]);
-  const int ch = lane % G_::kRowChunks;    // this lane's 16-byte column chunk of a row
-  const int rsub = lane / G_::kRowChunks;  // and its first row
-  StageIt sit;
-  sit.f = first;
-  stage_it_enter(sit, pi, phase, w0, w1, p);
-  Stage nxt;
-  bool nxt_ok = next_stage(sit, pi, phase, w0, w1, nxt, p);
-  int2 nxt_e = nxt_ok ? stage_entries(nxt, p) : make_int2(0, 0);
-  uint32_t issued = 0;   // stages this warp has issued (slot = count % R)
-  uint32_t badbits = 0;  // slots whose stage has an out-of-range block id
-
-  auto issue_one = [&]() {
-    if (nxt_ok) {
-      const uint32_t slot = issued % R;
-      const bool two = (nxt.t0 & (p.block_size - 1)) + nxt.nt > p.block_size;
-      const bool bad = nxt_e.x < 0 || nxt_e.x >= p.num_blocks ||
-                       (two && (nxt_e.y < 0 || nxt_e.y >= p.num_blocks));
-      badbits = bad ? (badbits | (1u << slot)) : (badbits & ~(1u << slot));
-      if (!bad) {
-        const uint32_t dst = ring + slot * G_::kStageBytes;
-        const int row0 = nxt.t0 & (p.block_size - 1);
-        const size_t row_x = static_cast<size_t>((nxt_e.x * p.num_kv_heads + nxt.kvh) * p.block_size);
-        const size_t row_y = static_cast<size_t>((nxt_e.y * p.num_kv_heads + nxt.kvh) * p.block_size);
-#pragma unroll
-        for (int j = 0; j < G_::kPasses; ++j) {
-          const int row = rsub + j * G_::kRowsPerPass;
-          const int r = row0 + row;
-          const bool live = row < nxt.nt;
-          // rows past the context: zero-filled, nothing read (the source stays in block x)
-          const size_t grow = !live ? row_x : (r < p.block_size ? row_x + r : row_y + (r - p.block_size));
-          const size_t src = grow * G_::kRowBytes + ch * 16;
-          const uint32_t so = F8 ? swz8<D>(row, ch) : swz(row, ch);
-          if (!F8 && p.key_new && nxt.last && row == nxt.nt - 1) {
-            // the newest token: from the step's input (the cache row is written later)
-            const size_t nsrc = ((static_cast<size_t>(nxt.s) * p.num_kv_heads + nxt.kvh) * D + ch * 8) * 2;
-            cp_async16(dst + so, p.key_new + nsrc, 16u);
-            cp_async16(dst + G_::kKBytes + so, p.value_new + nsrc, 16u);
-          } else {
-            cp_async16(dst + so, p.k_cache + src, live ? 16u : 0u);
-            cp_async16(dst + G_::kKBytes + so, p.v_cache + src, live ? 16u : 0u);
-          }
-        }
-      }
-      ++issued;
-      nxt_ok = next_stage(sit, pi, phase, w0, w1, nxt, p);
-      if (nxt_ok) nxt_e = stage_entries(nxt, p);
-    }
-    cp_async_commit();  // one group per call, empty or not
-  };
-#pragma unroll
-  for (int a = 0; a < G_::kAhead; ++a) issue_one();
-
-  const int r0 = lane >> 2;        // MMA row of this lane
-  const int qc = 2 * (lane & 3);   // MMA column pair of this lane
-  const int lrow = lane & 7;       // ldmatrix: row within an 8x8 matrix
-  const int lmat = lane >> 3;      // ldmatrix: which of the four matrices
-
-  // q of the first family where this pair computes; later ones are loaded a family ahead
-  uint32_t qn[KS][NTH][2];
-  {
-    const int2 r = unit_range(first, pi, w0, w1, p);
-    Fam qf;
-    bool have = fam_valid(first) && r.x < r.y;
-    if (have) qf = first;
-    else have = next_busy_fam(first, pi, w0, w1, p, qf);
-    if (have) {
-      const PairHeads ph = pair_heads(p, qf.g * p.gs + pi);
-      if (F8) load_q8<D, NTH, T>(p, qf.s, ph.h0, ph.nh, lane, qn);
-      else load_q<D, NTH>(p, qf.s, ph.h0, ph.nh, lane, qn);
-    }
-  }
-
-  uint32_t used = 0;  // stages this warp has computed
-  bool cta_first = true;
-  // This warp's pieces of cut pairs (at most two: in the share's first and last families),
-  // counted in after the share is streamed.
-  CutPiece cut_a, cut_b;
-  int ncut = 0;
-  for (Fam f = first; f.s < p.num_seqs && f.pre < w1; fam_next(f, p), cta_first = false) {
-    const int2 r = unit_range(f, pi, w0, w1, p);
-    if (!has_piece(r, f.ns)) continue;
-    const PairHeads ph = pair_heads(p, f.g * p.gs + pi);
-    T* out_rows =
-        reinterpret_cast<T*>(p.out) + (static_cast<size_t>(f.s) * p.num_q_heads + ph.h0) * D;
-    if (!fam_valid(f)) {  // invalid context length: the unit-0 holder writes zeros
-      if (r.x == 0 && r.x < r.y) {
-        for (int i = gt; i < ph.nh * D / 8; i += gthreads)
-          reinterpret_cast<uint4*>(out_rows)[i] = make_uint4(0, 0, 0, 0);
-        if (gt == 0) atomicOr(p.err, kErrBadContext);
-      }
-      continue;
-    }
-    const bool computes = r.x < r.y;  // (an empty middle piece computes nothing)
-    uint32_t qb[KS][NTH][2];
-    if (computes) {
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks)
-#pragma unroll
-        for (int nt = 0; nt < NTH; ++nt) {
-          qb[ks][nt][0] = qn[ks][nt][0];
-          qb[ks][nt][1] = qn[ks][nt][1];
-        }
-      Fam qf;
-      if (next_busy_fam(f, pi, w0, w1, p, qf)) {
-        const PairHeads lh = pair_heads(p, qf.g * p.gs + pi);
-        if (F8) load_q8<D, NTH, T>(p, qf.s, lh.h0, lh.nh, lane, qn);
-        else load_q<D, NTH>(p, qf.s, lh.h0, lh.nh, lane, qn);
-      }
-    }
-
-    // This lane's softmax columns: heads 8*nt + qc and + 1 of every n-tile.
-    float m_run[NTH][2], l_run[NTH][2];
-    float o[MT][NTH][4];  // O^T: rows d = 16*mt + r0 (+8), columns = heads
-#pragma unroll
-    for (int nt = 0; nt < NTH; ++nt) {
-      m_run[nt][0] = m_run[nt][1] = -INFINITY;
-      l_run[nt][0] = l_run[nt][1] = 0.f;
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) o[mt][nt][0] = o[mt][nt][1] = o[mt][nt][2] = o[mt][nt][3] = 0.f;
-    }
-    bool seg_bad = false;
-
-    const int j_first = r.x + (phase - r.x % P + P) % P;
-    for (int j = j_first; j < r.y; j += P) {
-      issue_one();                   // stage used + kAhead goes in flight
-      cp_async_wait<G_::kAhead>();   // this lane's copies of stage `used` have landed
-      __syncwarp();                  // ... and every other lane's
-      const uint32_t slot = used % R;
-      ++used;
-      const int nt_tok = min(kStageTok, f.ctx - j * kStageTok);
-      if (badbits & (1u << slot)) {
-        seg_bad = true;
-      } else {
-        const uint32_t kb = ring + slot * G_::kStageBytes;
-        const uint32_t vb = kb + G_::kKBytes;
-        // ---- S^T = K Q^T: rows = the stage's 16 tokens, columns = heads ----
-        float sacc[NTH][4], sodd[NTH][4];
-#pragma unroll
-        for (int nt = 0; nt < NTH; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) sacc[nt][e] = sodd[nt][e] = 0.f;
-        if (F8) {
-          // K rows r0 and r0 + 8, bytes [(D/4) t, (D/4)(t+1)): word ks of a row holds the
-          // four d of k-step ks (the order load_q8 gives q)
-          uint32_t kw[2][KS];
-#pragma unroll
-          for (int hr = 0; hr < 2; ++hr)
-#pragma unroll
-            for (int i = 0; i < KS / 4; ++i) {
-              const uint32_t addr = kb + swz8<D>(r0 + 8 * hr, (KS / 4) * (lane & 3) + i);
-              asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                           : "=r"(kw[hr][4 * i]), "=r"(kw[hr][4 * i + 1]), "=r"(kw[hr][4 * i + 2]),
-                             "=r"(kw[hr][4 * i + 3])
-                           : "r"(addr));
-            }
-#pragma unroll
-          for (int ks = 0; ks < KS; ++ks) {
-            uint32_t a[4];
-            a[0] = e4m3x2_f16x2(kw[0][ks]);
-            a[1] = e4m3x2_f16x2(kw[1][ks]);
-            a[2] = e4m3x2_f16x2(kw[0][ks] >> 16);
-            a[3] = e4m3x2_f16x2(kw[1][ks] >> 16);
-#pragma unroll
-            for (int nt = 0; nt < NTH; ++nt) {
-              if (ks & 1)
-                mma16816<TM>(sodd[nt], a, qb[ks][nt][0], qb[ks][nt][1]);
-              else
-                mma16816<TM>(sacc[nt], a, qb[ks][nt][0], qb[ks][nt][1]);
-            }
-          }
-        } else {
-#pragma unroll
-          for (int ks = 0; ks < KS; ++ks) {
-            uint32_t a[4];  // rows tok 0-7 / 8-15, d chunks 2ks / 2ks+1
-            ldsm_x4(kb + swz(lrow + ((lmat & 1) << 3), 2 * ks + (lmat >> 1)), a);
-#pragma unroll
-            for (int nt = 0; nt < NTH; ++nt) {
-              if (ks & 1)
-                mma16816<TM>(sodd[nt], a, qb[ks][nt][0], qb[ks][nt][1]);
-              else
-                mma16816<TM>(sacc[nt], a, qb[ks][nt][0], qb[ks][nt][1]);
-            }
-          }
-        }
-        // ---- online softmax per head (column) over the 16 tokens (rows) ----
-        // c0,c1: token r0, heads qc, qc+1; c2,c3: token r0 + 8, same heads
-        const bool v_lo = r0 < nt_tok, v_hi = r0 + 8 < nt_tok;
-        uint32_t pb[NTH][2];
-        float alpha[NTH][2];
-#pragma unroll
-        for (int nt = 0; nt < NTH; ++nt) {
-          float x[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float v = (sacc[nt][e] + sodd[nt][e]) * p.scale_log2;
-            x[e] = (e < 2 ? v_lo : v_hi) ? v : -INFINITY;
-          }
-          float pr[4];
-#pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            float mx = fmaxf(x[cc], x[cc + 2]);
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-            const float m_new = fmaxf(m_run[nt][cc], mx);
-            alpha[nt][cc] = exp2f(m_run[nt][cc] - m_new);  // 0 on the first stage
-            pr[cc] = exp2f(x[cc] - m_new);
-            pr[cc + 2] = exp2f(x[cc + 2] - m_new);
-            float sum = pr[cc] + pr[cc + 2];
-            sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-            sum += __shfl_xor_sync(0xffffffffu, sum, 8);
-            sum += __shfl_xor_sync(0xffffffffu, sum, 16);
-            l_run[nt][cc] = l_run[nt][cc] * alpha[nt][cc] + sum;
-            m_run[nt][cc] = m_new;
-          }
-          // P^T as B fragments: transpose the (token x head) 8x8 blocks in registers
-          pb[nt][0] = movmatrix_t(pack2<TM>(pr[0], pr[1]));  // tokens 0-7
-          pb[nt][1] = movmatrix_t(pack2<TM>(pr[2], pr[3]));  // tokens 8-15
-        }
-        bool all_one = true;
-#pragma unroll
-        for (int nt = 0; nt < NTH; ++nt) all_one = all_one && alpha[nt][0] == 1.f && alpha[nt][1] == 1.f;
-        if (!__all_sync(0xffffffffu, all_one)) {
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-            for (int nt = 0; nt < NTH; ++nt) {
-              o[mt][nt][0] *= alpha[nt][0];
-              o[mt][nt][1] *= alpha[nt][1];
-              o[mt][nt][2] *= alpha[nt][0];
-              o[mt][nt][3] *= alpha[nt][1];
-            }
-        }
-        // ---- O^T += V^T P^T: rows = d (16 per m-tile), k = tokens, columns = heads ----
-        // (V rows past the context were zero-filled by the copy, so 0 * garbage cannot occur)
-        if (F8) {
-          // V rows (tokens) 2t, 2t+1, 2t+8, 2t+9, bytes [(D/8) r0, (D/8)(r0+1)): m-tile mt
-          // takes bytes 2 mt and 2 mt + 1 (its rows r0 and r0 + 8, see drow); a byte
-          // permute pairs the two tokens of each A register before widening
-          constexpr int VW = D / 32;  // 32-bit words of this lane's bytes of one V row
-          uint32_t vw[4][VW];
-          const int tq = lane & 3;
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int row = 2 * tq + (k & 1) + 8 * (k >> 1);
-            if constexpr (VW == 4) {
-              const uint32_t addr = vb + swz8<D>(row, r0);
-              asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                           : "=r"(vw[k][0]), "=r"(vw[k][1]), "=r"(vw[k][2]), "=r"(vw[k][3])
-                           : "r"(addr));
-            } else {
-              const uint32_t addr = vb + swz8<D>(row, r0 >> 1) + 8 * (r0 & 1);
-              asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
-                           : "=r"(vw[k][0]), "=r"(vw[k][1])
-                           : "r"(addr));
-            }
-          }
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
-            const uint32_t lo = __byte_perm(vw[0][mt >> 1], vw[1][mt >> 1], sel);  // tokens 2t, 2t+1
-            const uint32_t hi = __byte_perm(vw[2][mt >> 1], vw[3][mt >> 1], sel);  // 2t+8, 2t+9
-            uint32_t a[4];
-            a[0] = e4m3x2_f16x2(lo);
-            a[1] = e4m3x2_f16x2(lo >> 16);
-            a[2] = e4m3x2_f16x2(hi);
-            a[3] = e4m3x2_f16x2(hi >> 16);
-#pragma unroll
-            for (int nt = 0; nt < NTH; ++nt) mma16816<TM>(o[mt][nt], a, pb[nt][0], pb[nt][1]);
-          }
-        } else {
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            uint32_t a[4];  // V^T: d chunks 2mt / 2mt+1, tokens 0-7 / 8-15
-            ldsm_x4_t(vb + swz(lrow + ((lmat >> 1) << 3), 2 * mt + (lmat & 1)), a);
-#pragma unroll
-            for (int nt = 0; nt < NTH; ++nt) mma16816<TM>(o[mt][nt], a, pb[nt][0], pb[nt][1]);
-          }
-        }
-        if (!F8 && p.key_new && j == f.ns - 1) {
-          // fused cache write: the newest token's K and V rows, from the slot, to position
-          // ctx - 1 of the sequence (lanes take the 16-byte chunks of K, then of V)
-          constexpr int CH = G_::kRowChunks;
-          const int t = f.ctx - 1;
-          const int blk = __ldg(p.block_tables + static_cast<size_t>(f.s) * p.max_blocks_per_seq +
-                                (t >> p.log2_block));
-          if (lane < 2 * CH && blk >= 0 && blk < p.num_blocks) {
-            const int c16 = lane % CH;
-            const uint32_t from = (lane < CH ? kb : vb) + swz(nt_tok - 1, c16);
-            const size_t to = ((static_cast<size_t>(blk) * p.num_kv_heads + ph.kvh) * p.block_size +
-                               (t & (p.block_size - 1))) * D + c16 * 8;
-            uint4 v;
-            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                         : "r"(from));
-            reinterpret_cast<uint4*>(const_cast<uint8_t*>(lane < CH ? p.k_cache : p.v_cache))[to / 8] = v;
-          }
-        }
-      }
-      __syncwarp();  // every lane is done with the slot before a later stage refills it
-    }
-
-    const bool whole = r.x == 0 && r.y == f.ns;
-    const int slot_out = cta_first ? 0 : 1;
-    const size_t piece = (static_cast<size_t>(c) * 2 + slot_out) * p.gs + pi;
-    float* pacc = p.part_acc + piece * p.heads_per_pair * D;
-    float* pml = p.part_ml + piece * p.heads_per_pair * 2;
-
-    if (P == 1) {
-      // ---------- pair end, one warp per pair: everything stays in registers ----------
-      // Lane (r0, qc) holds O^T rows d = 16*mt + r0 (+8) for heads h = 8*nt + qc (+1), and
-      // the running max/sum of those heads.
-      const bool any_bad = __any_sync(0xffffffffu, seg_bad);
-      if (!whole) {
-        // A piece of a cut pair: store (O, m, l) in [head][d] order; it is counted in (and
-        // maybe merged) after the share is streamed.
-#pragma unroll
-        for (int nt = 0; nt < NTH; ++nt)
-#pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            const int h = nt * 8 + qc + cc;
-            if (h < ph.nh) {
-#pragma unroll
-              for (int mt = 0; mt < MT; ++mt) {
-                pacc[h * D + drow<D, F8>(mt, r0)] = o[mt][nt][cc];
-                pacc[h * D + drow<D, F8>(mt, r0 + 8)] = o[mt][nt][cc + 2];
-              }
-              if (r0 == 0) {  // an empty piece (m = -inf) gets l = 0: weight 0 in the merge
-                pml[h * 2 + 0] = m_run[nt][cc];
-                pml[h * 2 + 1] = any_bad ? -1.f : (m_run[nt][cc] == -INFINITY ? 0.f : l_run[nt][cc]);
-              }
-            }
-          }
-        (ncut == 0 ? cut_a : cut_b) = cut_piece(f, pi, ph, W, G, p);
-        ++ncut;
-        if (lane == 0 && any_bad) atomicOr(p.err, kErrBadBlock);
-        continue;
-      }
-      const bool bad = any_bad;
-      // out = O / l, rounded; transposed in registers (movmatrix) so that each lane stores
-      // two adjacent d of one head: lane (r0, qc) writes out[h = 8*nt + r0][16*mt + qc (+8)].
-      if (F8) {
-        // rows r0 and r0 + 8 of an m-tile are the adjacent d = drow(mt, r0), + 1: each lane
-        // stores its two heads' pairs directly
-#pragma unroll
-        for (int nt = 0; nt < NTH; ++nt)
-#pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            const float inv = bad ? 0.f : p.out_scale / l_run[nt][cc];
-            const int h = nt * 8 + qc + cc;
-            if (h < ph.nh) {
-#pragma unroll
-              for (int mt = 0; mt < MT; ++mt)
-                *reinterpret_cast<uint32_t*>(out_rows + h * D + drow<D, F8>(mt, r0)) =
-                    pack2<T>(o[mt][nt][cc] * inv, o[mt][nt][cc + 2] * inv);
-            }
-          }
-      } else {
-#pragma unroll
-        for (int nt = 0; nt < NTH; ++nt) {
-          const float i0 = bad ? 0.f : 1.f / l_run[nt][0];
-          const float i1 = bad ? 0.f : 1.f / l_run[nt][1];
-          const int h = nt * 8 + r0;
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            const uint32_t lo = movmatrix_t(pack2<T>(o[mt][nt][0] * i0, o[mt][nt][1] * i1));
-            const uint32_t hi = movmatrix_t(pack2<T>(o[mt][nt][2] * i0, o[mt][nt][3] * i1));
-            if (h < ph.nh) {
-              *reinterpret_cast<uint32_t*>(out_rows + h * D + 16 * mt + qc) = lo;
-              *reinterpret_cast<uint32_t*>(out_rows + h * D + 16 * mt + 8 + qc) = hi;
-            }
-          }
-        }
-      }
-      if (lane == 0 && any_bad) atomicOr(p.err, kErrBadBlock);
-      continue;
-    }
-
-    // ---------------- pair end, P warps per pair: merge them, write out ----------------
-    gsync();  // the previous pair end's reads of xo/xm/xl are done
-    if (r0 == 0) {  // lanes 0..3 hold the running max/sum of heads 8*nt + qc, + 1
-#pragma unroll
-      for (int nt = 0; nt < NTH; ++nt)
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          sm.xm[warp][nt * 8 + qc + cc] = m_run[nt][cc];
-          sm.xl[warp][nt * 8 + qc + cc] = l_run[nt][cc];
-        }
-    }
-    const bool any_bad = gor(seg_bad);  // (also orders the xm/xl writes before the reads)
-    const int wbase = pi * P;  // first warp of the pair
-    // Exchange O four heads at a time: round r covers heads 4r..4r+3.
-    const int rounds = (ph.nh + 3) / 4;
-    for (int round = 0; round < rounds; ++round) {
-      if (round > 0) gsync();  // previous round's reads done
-      const int rbase = round * 4;
-#pragma unroll
-      for (int nt = 0; nt < NTH; ++nt) {
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int h = nt * 8 + qc + cc;
-          if (h >= rbase && h < rbase + 4) {
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-              sm.xo[warp][h - rbase][drow<D, F8>(mt, r0)] = o[mt][nt][cc];
-              sm.xo[warp][h - rbase][drow<D, F8>(mt, r0 + 8)] = o[mt][nt][cc + 2];
-            }
-          }
-        }
-      }
-      gsync();
-      const int rows = min(4, ph.nh - rbase);
-      for (int idx = gt; idx < rows * (D / 4); idx += gthreads) {
-        const int hr = idx / (D / 4);
-        const int h = rbase + hr;
-        const int d4 = (idx - hr * (D / 4)) * 4;
-        float M = -INFINITY;
-        for (int w = wbase; w < wbase + P; ++w) M = fmaxf(M, sm.xm[w][h]);
-        float L = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int w = wbase; w < wbase + P; ++w) {
-          const float wt = exp2f(sm.xm[w][h] - M);  // 0 for a warp without units here
-          L += sm.xl[w][h] * wt;
-          const float4 x4 = *reinterpret_cast<const float4*>(&sm.xo[w][hr][d4]);
-          acc.x += x4.x * wt;
-          acc.y += x4.y * wt;
-          acc.z += x4.z * wt;
-          acc.w += x4.w * wt;
-        }
-        if (whole) {
-          uint2 packed = make_uint2(0u, 0u);  // zeros for a pair with a bad block
-          if (!any_bad) {
-            const float inv = F8 ? p.out_scale / L : 1.f / L;
-            packed.x = pack2<T>(acc.x * inv, acc.y * inv);
-            packed.y = pack2<T>(acc.z * inv, acc.w * inv);
-          }
-          *reinterpret_cast<uint2*>(out_rows + h * D + d4) = packed;
-        } else {
-          // An empty piece (no units here) has M = -inf, and the weights above are NaN:
-          // store acc = 0, l = 0 so that its weight in the merge, 2^(-inf - M'), is 0.
-          const bool empty = M == -INFINITY;
-          *reinterpret_cast<float4*>(pacc + h * D + d4) = empty ? make_float4(0.f, 0.f, 0.f, 0.f) : acc;
-          if (d4 == 0) {
-            pml[h * 2 + 0] = M;
-            pml[h * 2 + 1] = any_bad ? -1.f : (empty ? 0.f : L);
-          }
-        }
-      }
-    }
-    if (!whole) {
-      (ncut == 0 ? cut_a : cut_b) = cut_piece(f, pi, ph, W, G, p);
-      ++ncut;
-    }
-    if (gt == 0 && any_bad) atomicOr(p.err, kErrBadBlock);
-  }
-  cp_async_wait<0>();  // (only empty groups can be left; leave none behind)
-
-  // ---- count this share's pieces in; the last arrival at a pair merges its pieces ----
-  // (ncut is the same in every warp of a pair.)  Lanes 0 and 1 of the pair's first warp
-  // count in its two pieces side by side, each after a fence ordering the piece's stores
-  // before its arrival; an arrival that completes a pair fences again before the merge's
-  // loads.
-  if (ncut > 0) {
-    gsync();  // every thread of the pair has stored its parts of the pieces
-    int bits = 0;
-    if (gt < ncut) {
-      const CutPiece& cp = gt == 0 ? cut_a : cut_b;
-      __threadfence();
-      const int n = cp.c_last - cp.c_first + 1;
-      if (arrive(p.counters + static_cast<size_t>(cp.c_first) * p.gs + pi, p.epoch) == n) {
-        __threadfence();
-        bits = 1 << gt;
-      }
-    }
-    __syncwarp();
-    bits = static_cast<int>(__reduce_or_sync(0xffffffffu, static_cast<unsigned>(bits)));
-    if (P > 1) {
-      if (gt == 0) sm.last[pi] = bits;
-      gsync();
-      bits = sm.last[pi];
-    }
-    if (P == 1 && bits) {
-      const int nj = (bits & 1) + ((bits >> 1) & 1);
-      const CutPiece& j0 = (bits & 1) ? cut_a : cut_b;
-      if (merge_staged<D, T, F8>(p, pi, j0, cut_b, nj, ring, sm.ring[warp][0], R * G_::kStageBytes,
-                             smem_addr(&sm.merge_bar[warp]), lane))
-        bits = 0;
-    }
-    for (int k = 0; k < ncut; ++k) {
-      if (!(bits & (1 << k))) continue;
-      const CutPiece& cp = k == 0 ? cut_a : cut_b;
-      T* out_rows =
-          reinterpret_cast<T*>(p.out) + (static_cast<size_t>(cp.s) * p.num_q_heads + cp.h0) * D;
-      merge_pieces<D, T, F8>(p, pi, cp.c_first, cp.first_slot, cp.c_last, cp.nh, out_rows, gt,
-                         gthreads);
-    }
-  }
-}
-
-template <int D, int NTH, typename T, bool F8>
-int launch(const Params& prm, int grid, cudaStream_t stream) {
-  const size_t smem = sizeof(Smem<D, F8 ? 1 : 2>) + 1024;  // + alignment slack for the ring
-  auto* kern = decode_kernel<D, NTH, T, F8>;
-  if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), smem)) return -3;
-  // a programmatic dependent of the previous kernel in the stream (see pdl_wait_primary)
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, prm) != cudaSuccess) return -3;
-  return 0;
-}
-
-}  // namespace decode
-
 int decode_heads_per_pair(int num_q_heads, int num_kv_heads) {
   const int g = num_q_heads / num_kv_heads;
   return g < decode::kMaxHeads ? g : decode::kMaxHeads;
@@ -1314,14 +83,11 @@ int decode_launch(const DecodeArgs& a, int grid, cudaStream_t stream) {
   p.part_ml = reinterpret_cast<float*>(ws);
 
   // heads of a pair are MMA columns: one n-tile of 8, or two for up to 16
+  if (a.kv_fp8) return decode_launch_fp8(p, grid, a.head_dim, a.bf16, stream);
 #define PA_DECODE_CASE(DD, NN)                                                           \
-  if (a.head_dim == DD && (p.heads_per_pair > 8) == (NN == 2)) {                         \
-    if (a.kv_fp8)                                                                        \
-      return a.bf16 ? decode::launch<DD, NN, __nv_bfloat16, true>(p, grid, stream)       \
-                    : decode::launch<DD, NN, __half, true>(p, grid, stream);             \
-    return a.bf16 ? decode::launch<DD, NN, __nv_bfloat16, false>(p, grid, stream)        \
-                  : decode::launch<DD, NN, __half, false>(p, grid, stream);              \
-  }
+  if (a.head_dim == DD && (p.heads_per_pair > 8) == (NN == 2))                           \
+    return a.bf16 ? decode::launch<DD, NN, __nv_bfloat16, false>(p, grid, stream) \
+                  : decode::launch<DD, NN, __half, false>(p, grid, stream);
   PA_DECODE_CASE(128, 1)
   PA_DECODE_CASE(128, 2)
   PA_DECODE_CASE(64, 1)

@@ -65,6 +65,11 @@ int reshape_and_cache_fp8_launch(const void* key, const void* value, void* k_cac
                                  int num_blocks, int num_kv_heads, int head_dim, int block_size,
                                  float k_scale, float v_scale, bool bf16, unsigned* err,
                                  cudaStream_t stream);
+int append_newest_fp8_launch(const void* key, const void* value, void* k_cache, void* v_cache,
+                             const int32_t* block_tables, int max_blocks_per_seq,
+                             const int32_t* context_lens, int num_seqs, int num_blocks,
+                             int num_kv_heads, int head_dim, int block_size, float k_scale,
+                             float v_scale, bool bf16, cudaStream_t stream);
 int swap_blocks_launch(const void* src_k, const void* src_v, void* dst_k, void* dst_v,
                        const int32_t* block_mapping, int num_pairs, int src_num_blocks,
                        int dst_num_blocks, int num_kv_heads, int row_bytes, int block_size,

@@ -186,3 +186,43 @@ def test_fp8_blocks_copy_and_swap_exactly():
     torch.cuda.synchronize()
     assert np.array_equal(hk.numpy()[0], want[10]) and np.array_equal(hk.numpy()[7], want[5])
     assert device_error() == 0
+
+
+@pytest.mark.parametrize("recipe", ["tiny", "b8", "llama"])
+def test_fused_step_equals_cache_write_then_decode(recipe):
+    """pa_decode_append_fp8 quantises each sequence's newest row in the kernel; caches and
+    output equal pa_reshape_and_cache_fp8 + pa_decode_fp8 bit for bit."""
+    if recipe == "tiny":
+        wl = workloads.tiny()
+    elif recipe == "b8":
+        wl = workloads.custom("f8b8", [1, 8, 9, 16, 17, 33, 200], "bf16", 16, 4, 128, 8,
+                              80, 256, seed=12)
+    else:
+        wl = workloads.llama31_8b(num_seqs=24)
+    ks, vs = 0.0123, 0.0234
+    outs, caches = [], []
+    for fused in (False, True):
+        gb = Fp8Batch(wl, ks, vs)   # every token written, the newest included ...
+        last = wl.seq_start[1:] - 1
+        key_new = to_device(wl.keys[last], wl.dtype)
+        value_new = to_device(wl.values[last], wl.dtype)
+        # ... then the newest rows' slots poisoned, so only the step can make them right
+        slots = np.array([gb.tables_np[s][(int(c) - 1) // wl.block_size] * wl.block_size +
+                          (int(c) - 1) % wl.block_size for s, c in enumerate(wl.context_lens)])
+        idx = torch.from_numpy(slots).cuda()
+        blk, row = idx // wl.block_size, idx % wl.block_size
+        gb.k8[blk, :, row] = 0x7F
+        gb.v8[blk, :, row] = 0x7F
+        if fused:
+            out = pa.decode_append_fp8(gb.q, key_new, value_new, gb.k8, gb.v8, gb.tables, gb.ctx,
+                                       wl.scale, ks, vs)
+        else:
+            pa.reshape_and_cache_fp8(key_new, value_new, gb.k8, gb.v8, idx.to(torch.int64), ks, vs)
+            out = pa.decode_fp8(gb.q, gb.k8, gb.v8, gb.tables, gb.ctx, wl.scale, ks, vs)
+        torch.cuda.synchronize()
+        assert device_error() == 0
+        outs.append(to_bits(out))
+        caches.append((codes(gb.k8), codes(gb.v8)))
+    np.testing.assert_array_equal(outs[0], outs[1])
+    np.testing.assert_array_equal(caches[0][0], caches[1][0])
+    np.testing.assert_array_equal(caches[0][1], caches[1][1])
