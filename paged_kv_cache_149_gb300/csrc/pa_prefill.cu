@@ -8,25 +8,34 @@
 // has to read the block table; chenyuan1125 "vllm-pagedattention", section 它和
 // FlashAttention…: prefill works on large blocks of queries).
 //
-// Design (one CTA per (query block, sequence, kv head); 4 warps, one thread per query row):
-// * The CTA's 128 query rows are (token, query head of the kv head) pairs: 128 / G tokens x
-//   G heads, so every K/V tile is read once for all G heads of a kv head (GQA).  Q sits in
-//   shared memory, K-major with the 128-byte swizzle (the layout tcgen05 descriptors read).
-// * Key tiles of 64 tokens are gathered through the table by 16-byte cp.async into a
-//   double-buffered ring, in the same swizzled layout: K is the K-major B operand of
-//   S = Q K^T, V (keys x d, d contiguous) the MN-major B operand of P V.  Rows past the
-//   context are zero-filled, never read.
-// * Per tile: one thread issues S = Q K^T (tcgen05.mma kind::f16, M 128, N 64, fp32 in
-//   tensor memory) and commits it to an mbarrier; every thread reads its own row of S with
-//   tcgen05.ld (row = TMEM lane: no shuffles), applies the causal mask and the online
-//   softmax in exp2, and writes its row of P (rounded to the input type) into the K
-//   buffer just consumed; then one thread issues P V (M 128, N d) into a second TMEM
-//   region, and every thread folds its row of P V into its fp32 O held in registers.
-// * Every mbarrier wait is bounded (about 1 s, PA_DEVERR_TIMEOUT); tiles entirely in the
-//   future of every row of the CTA are never loaded.
+// Design: one CTA per (pair of 128-row query tiles, sequence, kv head), 320 threads in
+// four roles that run concurrently and hand work over through mbarriers:
+// * A query tile's rows are (token, query head of the kv head) pairs, 128 / G tokens x G
+//   heads, so every K/V tile is read once for all heads of the group (GQA), and both
+//   query tiles of the CTA share the K/V tiles.
+// * Loader warp: Q of both tiles once (16-byte cp.async, zero-filled past the batch), then
+//   64-key K and V tiles into a four-stage ring, in the 128-byte swizzled layout the
+//   tcgen05 descriptors read.  Whole blocks come by TMA (a 4-D tensor map over the
+//   cache: d, row, kv head, block; one copy per block and 64-column half); the ragged last
+//   block and the blocks past the context by cp.async with zero fill, so no row past the
+//   context is ever read (its V row must be zero: P is 0 there, and 0 x NaN is NaN).
+// * MMA warp (one thread): S = Q K^T per query tile into tensor memory (two buffers per
+//   tile), and O += P V with O kept in tensor memory across the whole key range.  The two
+//   tiles alternate so that the tensor cores work on one tile while the other's softmax
+//   runs (S of tile 0 for the next keys is issued between the P V of tiles 0 and 1).
+// * Two softmax warpgroups, one per query tile, one thread per row (= tensor-memory
+//   lane): read the row of S, mask causally, keep the running maximum m and sum l in
+//   exp2 units, write the row of P (input type) into shared memory.  O is rescaled only
+//   when a row's maximum grows by more than 8 (in log2 units), so P <= 2^8 and the
+//   rescale (a read-modify-write of the row in tensor memory) is rare after the first
+//   tiles; the final O / l uses the same m, so the result is exact softmax.
+// Every mbarrier wait is bounded (about 1 s) and checks a shared abort flag, so a stuck
+// role ends the CTA with PA_DEVERR_TIMEOUT instead of hanging.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "pa_common.cuh"
 #include "pa_internal.h"
@@ -34,12 +43,19 @@
 namespace pa {
 namespace prefill {
 
-constexpr int kThreads = 128;  // one per query row
-constexpr int kRows = 128;     // query rows of a CTA (MMA M)
-constexpr int kKeys = 64;      // keys of a tile (MMA N of S, K of P V)
+constexpr int kTiles = 2;       // query tiles per CTA (softmax warpgroups)
+constexpr int kRows = 128;      // rows of a query tile (MMA M, tensor-memory lanes)
+constexpr int kKeys = 64;       // keys of a K/V tile (MMA N of S, K of P V)
+constexpr int kStages = 4;      // K/V ring
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;   // 2 x 128 softmax threads, a loader warp, an MMA warp
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescale = 8.f;  // log2 growth of a row's maximum that forces a rescale of O
 
 struct Params {
+  CUtensorMap kmap;  // the caches as [num_blocks][Hkv][B][d] 16-bit, box (64, B, 1, 1)
+  CUtensorMap vmap;
   const uint8_t* q;
   const uint8_t* k_cache;
   const uint8_t* v_cache;
@@ -47,38 +63,40 @@ struct Params {
   const int32_t* context_lens;
   const int32_t* query_start;  // [n + 1]
   uint8_t* out;
-  int num_seqs, num_q_heads, num_kv_heads, group, tq;  // tq = tokens per CTA = 128 / G
-  int max_blocks_per_seq, block_size, log2_block, num_blocks;
+  int num_seqs, num_q_heads, num_kv_heads, group, tpt;  // tpt = tokens per query tile = 128 / G
+  int max_blocks_per_seq, block_size, num_blocks;
   float scale_log2;
   unsigned* err;
 };
 
-// P of a tile ([128 rows][64 keys], 16 KB) takes the place of the tile's K when K is at
-// least as large (d >= 128), else a buffer of its own.
-template <int D>
-constexpr bool kAliasP = kKeys * D >= kRows * kKeys;
-
 template <int D>
 struct Smem {
-  uint8_t q[kRows * D * 2];            // K-major, 128-byte swizzle; 1024-byte aligned
-  uint8_t kv[2][2][kKeys * D * 2];     // [buffer][K, V]
-  uint8_t p[kAliasP<D> ? 1024 : kRows * kKeys * 2];
-  unsigned long long bar_s, bar_o;     // S and P V done (one phase per tile)
-  uint32_t tmem;                       // tensor-memory base address
-  int bad;                             // a block id of this CTA's tiles is out of range
+  uint8_t q[kTiles][kRows * D * 2];            // K-major, 128-byte swizzle; 1024-byte aligned
+  uint8_t k[kStages][kKeys * D * 2];           // [64-column half][64 keys][128 B]
+  uint8_t v[kStages][kKeys * D * 2];
+  uint8_t p[kTiles][kRows * kKeys * 2];        // P of a tile (reused once S of the next keys is
+                                               // done: the tensor cores complete in order)
+  unsigned long long q_full;
+  unsigned long long kv_full[kStages], kv_empty[kStages];
+  unsigned long long s_full[kTiles][2], s_free[kTiles][2];
+  unsigned long long p_full[kTiles][2], o_done[kTiles][2];
+  unsigned long long fin;  // the MMA thread's last commit
+  uint32_t tmem;
+  int bad;    // a block id of this CTA's keys is out of range
+  int abort;  // a wait gave up: every role stops
 };
 
 // Byte offset of (row, 16-byte chunk) in a [rows][D] 16-bit tile stored K-major with the
 // 128-byte swizzle: chunk c lives in the 64-element column block c / 8 (blocks rows * 128
-// bytes apart), row r at r * 128 inside it, the chunk index XORed with r % 8.
+// bytes apart), row r at r * 128 inside it, the chunk index XORed with r % 8.  TMA with
+// the 128-byte swizzle writes the same pattern into a 1024-byte aligned box.
 __device__ __forceinline__ uint32_t swz(int rows, int r, int c) {
   return static_cast<uint32_t>((c >> 3) * rows * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
 // tcgen05 shared-memory matrix descriptor with the 128-byte swizzle (version 1 = sm_100
 // family): lbo / sbo in bytes.  K-major operands: sbo = 1024 (8-row groups), lbo unused.
-// MN-major operands: lbo = distance between 64-element MN blocks, sbo = 1024 (8-row K
-// groups).
+// MN-major operands: lbo = distance between 64-element MN blocks, sbo = 1024.
 __device__ __forceinline__ uint64_t desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
   return static_cast<uint64_t>((addr >> 4) & 0x3FFF) |
          (static_cast<uint64_t>((lbo >> 4) & 0x3FFF) << 16) |
@@ -109,6 +127,16 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                : "memory");
 }
 
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // 32 consecutive fp32 columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
@@ -126,37 +154,64 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// The same 32 columns written back.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
+          taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
                "r"(src_bytes)
                : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+// One arrival on `bar` once every cp.async this thread has issued so far has landed.
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-// Wait for the phase of `bar` with parity `par`, bounded by kWaitLimitNs.
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t par) {
-  if (mbar_try_wait(bar, par)) return true;
-  const unsigned long long t0 = global_timer_ns();
-  for (;;) {
-    if (mbar_try_wait(bar, par)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
-  }
+// 2^x by the special-function unit (approximate, subnormal results flushed to zero; the
+// arguments here are <= 8 and results below 2^-126 only lose weights that small).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// 4-D tiled TMA load (x = d, y = row in the block, z = kv head, w = block), completion
+// counted in bytes on `bar`.  x is 0 or 64 (128-byte multiples).
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, int w, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+      : "memory");
 }
 
 template <int D, typename T>
-__global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant__ Params p) {
-  constexpr int CH = D / 8;            // 16-byte chunks per row
-  constexpr int KS1 = D / 16;          // MMA k-steps of S = Q K^T
-  constexpr int KS2 = kKeys / 16;      // MMA k-steps of P V
-  constexpr uint32_t kColS = 0;        // TMEM columns: S [0, 64), P V [64, 64 + D)
-  constexpr uint32_t kColO = kKeys;
-  constexpr uint32_t kTmemCols = kKeys + D <= 128 ? 128 : 256;  // power of two >= 64 + D
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ Params p) {
+  constexpr int CH = D / 8;                  // 16-byte chunks of a 16-bit row
+  constexpr int KS1 = D / 16;                // MMA k-steps of S = Q K^T
+  constexpr int KS2 = kKeys / 16;            // MMA k-steps of P V
+  constexpr uint32_t kTileCols = 256;        // TMEM columns per query tile
+  constexpr uint32_t kColO = 2 * kKeys;      //   S buffers [0, 128), O [128, 128 + D)
+  constexpr uint32_t kTmemCols = kTiles * kTileCols;
+  constexpr uint32_t kHalf = kKeys * 128;    // bytes of a 64-column half of a K/V tile
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
   Smem<D>& sm = *reinterpret_cast<Smem<D>*>(smem_raw + (((raw_addr + 1023) & ~1023u) - raw_addr));
@@ -164,17 +219,17 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant
   pdl_wait_primary();
   pdl_launch_dependents();
 
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int s = blockIdx.y, g = blockIdx.z;
-  const int tb = gridDim.x - 1 - blockIdx.x;  // later token blocks (more keys) first
+  const int cb = gridDim.x - 1 - blockIdx.x;  // later query blocks (more keys) first
   const int qs = __ldg(p.query_start + s), qlen = __ldg(p.query_start + s + 1) - qs;
-  const int tok0 = tb * p.tq;
+  const int tpt = p.tpt, G = p.group;
+  const int tok0 = cb * kTiles * tpt;
   if (tok0 >= qlen) return;  // (uniform over the CTA)
   const int ctx = __ldg(p.context_lens + s);
-  const int ntok = min(p.tq, qlen - tok0);
-  const int G = p.group;
   T* outp = reinterpret_cast<T*>(p.out);
   if (ctx < 1 || ctx > p.max_blocks_per_seq * p.block_size || qlen > ctx) {
+    const int ntok = min(kTiles * tpt, qlen - tok0);
     for (int i = tid; i < ntok * G * CH; i += kThreads) {
       const int r = i / CH, c = i % CH;
       reinterpret_cast<uint4*>(outp + ((static_cast<size_t>(qs + tok0 + r / G) * p.num_q_heads +
@@ -183,219 +238,296 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(const __grid_constant
     if (tid == 0) atomicOr(p.err, kErrBadContext);
     return;
   }
+  // keys each query tile needs: 0 .. the position of its last token
+  int nt[kTiles];
+#pragma unroll
+  for (int t = 0; t < kTiles; ++t) {
+    const int ntok = min(tpt, qlen - (tok0 + t * tpt));
+    nt[t] = ntok > 0 ? (ctx - qlen + tok0 + t * tpt + ntok - 1) / kKeys + 1 : 0;
+  }
+  const int n = max(nt[0], nt[1]);
 
-  // ---- this thread's row: (token tid / G, head tid % G) ----
-  const bool row_ok = tid < ntok * G;
-  const int pos = row_ok ? ctx - qlen + tok0 + tid / G : -1;
-  const long long row_off =
-      row_ok ? (static_cast<long long>(qs + tok0 + tid / G) * p.num_q_heads + g * G + tid % G) * D
-             : -1;
-  const int pos_lo = ctx - qlen + tok0, pos_hi = ctx - qlen + tok0 + ntok - 1;
-  const int ntiles = pos_hi / kKeys + 1;
-
-  // ---- set-up: barriers, tensor memory, Q into shared memory ----
+  // ---- set-up: barriers, tensor memory ----
   if (tid == 0) {
-    mbar_init(smem_addr(&sm.bar_s), 1);
-    mbar_init(smem_addr(&sm.bar_o), 1);
+    mbar_init(smem_addr(&sm.q_full), 32);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(smem_addr(&sm.kv_full[i]), 33);  // the TMA issuer's expect-tx + 32 copy lanes
+      mbar_init(smem_addr(&sm.kv_empty[i]), 1);
+    }
+    for (int t = 0; t < kTiles; ++t)
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(smem_addr(&sm.s_full[t][b]), 1);
+        mbar_init(smem_addr(&sm.s_free[t][b]), kRows);
+        mbar_init(smem_addr(&sm.p_full[t][b]), kRows);
+        mbar_init(smem_addr(&sm.o_done[t][b]), 1);
+      }
+    mbar_init(smem_addr(&sm.fin), 1);
     fence_mbar_init();
     sm.bad = 0;
+    sm.abort = 0;
   }
-  if (warp == 0) {
+  if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_addr(&sm.tmem)), "r"(kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(p.q + (row_ok ? row_off : 0) * 2);
-#pragma unroll 4
-    for (int c = 0; c < CH; ++c) {
-      const uint4 v = row_ok ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(sm.q + swz(kRows, tid, c)) = v;
-    }
-  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem;
+  // a bounded wait; on failure every role stops (the flag is checked inside the waits)
+  auto wait = [&](unsigned long long& bar, int parity) -> bool {
+    if (mbar_wait_bounded(smem_addr(&bar), static_cast<uint32_t>(parity), &sm.abort)) return true;
+    if (atomicExch(&sm.abort, 1) == 0) atomicOr(p.err, kErrTimeout);
+    return false;
+  };
 
-  const int32_t* trow = p.block_tables + static_cast<size_t>(s) * p.max_blocks_per_seq;
-  auto issue_tile = [&](int kt, int b) {
-    const uint32_t kbase = smem_addr(sm.kv[b][0]);
-    const uint32_t vbase = smem_addr(sm.kv[b][1]);
-    for (int e = tid; e < kKeys * CH; e += kThreads) {
-      const int row = e / CH, c = e % CH;
-      const int t = kt * kKeys + row;
-      const bool live = t < ctx;
-      int blk = 0;
-      if (live) {
-        blk = __ldg(trow + (t >> p.log2_block));
-        if (blk < 0 || blk >= p.num_blocks) {
-          sm.bad = 1;
-          blk = 0;
+  if (warp == kLoadWarp) {
+    // ================= loader: Q once, then the K/V ring =================
+    for (int e = lane; e < kTiles * kRows * CH; e += 32) {
+      const int t = e / (kRows * CH), rem = e % (kRows * CH), r = rem / CH, c = rem % CH;
+      const int tok = tok0 + t * tpt + r / G;
+      const bool live = r / G < tpt && tok < qlen;
+      const size_t row = live ? static_cast<size_t>(qs + tok) * p.num_q_heads + g * G + r % G : 0;
+      cp_async16(smem_addr(sm.q[t]) + swz(kRows, r, c), p.q + (row * D + c * 8) * 2, live ? 16u : 0u);
+    }
+    cp_async_arrive(smem_addr(&sm.q_full));
+    const int B = p.block_size, nbk = kKeys / B;
+    const int32_t* trow = p.block_tables + static_cast<size_t>(s) * p.max_blocks_per_seq;
+    for (int kt = 0; kt < n; ++kt) {
+      const int st = kt % kStages;
+      // this tile's blocks: lane j looks up block j (one round trip for all)
+      int my_e = -1;
+      if (lane < nbk) {
+        const int lb = kt * nbk + lane;
+        if (lb * B < ctx) my_e = __ldg(trow + lb);
+      }
+      if (kt >= kStages && !wait(sm.kv_empty[st], ((kt - kStages) / kStages) & 1)) break;
+      const uint32_t kb = smem_addr(sm.k[st]), vb = smem_addr(sm.v[st]);
+      uint32_t full_mask = 0;  // blocks that come whole by TMA
+      for (int j = 0; j < nbk; ++j) {
+        const int e = __shfl_sync(0xffffffffu, my_e, j);
+        const int rows = min(B, max(0, ctx - (kt * nbk + j) * B));
+        if (rows == B && e >= 0 && e < p.num_blocks) full_mask |= 1u << j;
+      }
+      if (lane == 0) {  // whole blocks by TMA
+        mbar_arrive_expect_tx(smem_addr(&sm.kv_full[st]),
+                              static_cast<uint32_t>(__popc(full_mask)) * 2u * B * D * 2);
+      }
+      for (int j = 0; j < nbk; ++j) {
+        const int e = __shfl_sync(0xffffffffu, my_e, j);
+        if (lane == 0 && (full_mask >> j & 1)) {
+#pragma unroll
+          for (int h = 0; h < D / 64; ++h) {
+            const uint32_t off = h * kHalf + j * B * 128;
+            tma_load_4d(kb + off, &p.kmap, h * 64, 0, g, e, smem_addr(&sm.kv_full[st]));
+            tma_load_4d(vb + off, &p.vmap, h * 64, 0, g, e, smem_addr(&sm.kv_full[st]));
+          }
         }
       }
-      const size_t src = ((static_cast<size_t>(blk) * p.num_kv_heads + g) * p.block_size +
-                          (live ? (t & (p.block_size - 1)) : 0)) * D + c * 8;
-      const uint32_t so = swz(kKeys, row, c);
-      cp_async16(kbase + so, p.k_cache + src * 2, live ? 16u : 0u);
-      cp_async16(vbase + so, p.v_cache + src * 2, live ? 16u : 0u);
-    }
-    cp_async_commit();
-  };
-  __syncthreads();  // (sm.bad cleared before any copy sets it)
-  issue_tile(0, 0);
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-  __syncthreads();
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-  const uint32_t tmem = sm.tmem;
-  const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;  // this warp's TMEM lanes
-
-  float o[D];
-#pragma unroll
-  for (int i = 0; i < D; ++i) o[i] = 0.f;
-  float m_run = -INFINITY, l_run = 0.f;
-  bool ok = true;
-  constexpr uint32_t id_s = idesc_f16<T>(kRows, kKeys, false);
-  constexpr uint32_t id_o = idesc_f16<T>(kRows, D, true);
-
-  for (int kt = 0; kt < ntiles && ok; ++kt) {
-    const int b = kt & 1;
-    if (kt + 1 < ntiles) {
-      issue_tile(kt + 1, b ^ 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    // the tile's copies (generic proxy) before the tensor cores read it (async proxy)
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-    __syncthreads();
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    const uint32_t qa = smem_addr(sm.q), kb = smem_addr(sm.kv[b][0]), vb = smem_addr(sm.kv[b][1]);
-
-    // ---- S = Q K^T ----
-    if (tid == 0) {
-#pragma unroll
-      for (int ks = 0; ks < KS1; ++ks) {
-        const uint32_t koff = (ks & 3) * 32;  // 16 columns = 32 bytes within a 64-column block
-        mma_f16(tmem + kColS,
-                desc_sw128(qa + (ks >> 2) * kRows * 128 + koff, 16, 1024),
-                desc_sw128(kb + (ks >> 2) * kKeys * 128 + koff, 16, 1024), id_s, ks > 0);
+      // the ragged block and blocks past the context: rows by cp.async, zero-filled
+      for (int j = 0; j < nbk; ++j) {
+        if (full_mask >> j & 1) continue;
+        const int lb = kt * nbk + j, rows = min(B, max(0, ctx - lb * B));
+        const int e = __shfl_sync(0xffffffffu, my_e, j);
+        const bool ok = e >= 0 && e < p.num_blocks;
+        if (rows > 0 && !ok && lane == 0) sm.bad = 1;
+        for (int i = lane; i < B * CH; i += 32) {
+          const int r = i / CH, c = i % CH;
+          const bool live = ok && r < rows;
+          const size_t src =
+              (((static_cast<size_t>(live ? e : 0) * p.num_kv_heads + g) * B + (live ? r : 0)) * D + c * 8) * 2;
+          const uint32_t so = swz(kKeys, j * B + r, c);
+          cp_async16(kb + so, p.k_cache + src, live ? 16u : 0u);
+          cp_async16(vb + so, p.v_cache + src, live ? 16u : 0u);
+        }
       }
-      mma_commit(smem_addr(&sm.bar_s));
+      cp_async_arrive(smem_addr(&sm.kv_full[st]));
     }
-    ok = wait_bounded(smem_addr(&sm.bar_s), kt & 1);
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    if (!__syncthreads_and(ok)) {
-      ok = false;
-      break;
-    }
-
-    // ---- this row of S: mask, online softmax, P into the K buffer ----
-    float sv[kKeys];
-    {
-      float tmp[32];
-      tmem_ld32(tmem + lane_base + kColS, tmp);
+    asm volatile("cp.async.wait_all;" ::: "memory");
+  } else if (warp == kMmaWarp) {
+    // ================= MMA issue: one thread =================
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_f16<T>(kRows, kKeys, false);
+      constexpr uint32_t id_o = idesc_f16<T>(kRows, D, true);
+      auto issue_s = [&](int t, int kt) -> bool {
+        const int b = kt & 1;
+        if (kt >= 2 && !wait(sm.s_free[t][b], ((kt - 2) >> 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t d = tmem + t * kTileCols + b * kKeys;
+        const uint32_t qa = smem_addr(sm.q[t]), kb = smem_addr(sm.k[kt % kStages]);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) sv[i] = tmp[i];
-      tmem_ld32(tmem + lane_base + kColS + 32, tmp);
+        for (int ks = 0; ks < KS1; ++ks) {
+          const uint32_t koff = (ks & 3) * 32;  // 16 columns = 32 bytes within a column block
+          mma_f16(d, desc_sw128(qa + (ks >> 2) * kRows * 128 + koff, 16, 1024),
+                  desc_sw128(kb + (ks >> 2) * kKeys * 128 + koff, 16, 1024), id_s, ks > 0);
+        }
+        mma_commit(smem_addr(&sm.s_full[t][b]));
+        return true;
+      };
+      auto issue_pv = [&](int t, int kt) -> bool {
+        const int b = kt & 1;
+        if (!wait(sm.p_full[t][b], (kt >> 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t pa = smem_addr(sm.p[t]), vb = smem_addr(sm.v[kt % kStages]);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) sv[32 + i] = tmp[i];
-    }
-    const bool needs_mask = kt * kKeys + kKeys - 1 > pos_lo;
-    float mx = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < kKeys; ++i) {
-      float v = sv[i] * p.scale_log2;
-      if (needs_mask && kt * kKeys + i > pos) v = -INFINITY;
-      sv[i] = v;
-      mx = fmaxf(mx, v);
-    }
-    const float m_new = fmaxf(m_run, mx);
-    // (a row whose keys are all masked so far keeps m = -inf; its weights stay 0)
-    const float alpha = m_new == -INFINITY ? 1.f : exp2f(m_run - m_new);
-    m_run = m_new;
-    float rs = 0.f;
-    uint8_t* prow = kAliasP<D> ? sm.kv[b][0] : sm.p;  // P [128][64], K-major: one column block
-#pragma unroll
-    for (int c = 0; c < kKeys / 8; ++c) {
-      float e[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        e[j] = m_new == -INFINITY ? 0.f : exp2f(sv[8 * c + j] - m_new);
-        rs += e[j];
+        for (int ks = 0; ks < KS2; ++ks)
+          mma_f16(tmem + t * kTileCols + kColO, desc_sw128(pa + ks * 32, 16, 1024),
+                  desc_sw128(vb + ks * 16 * 128, kKeys * 128, 1024), id_o, kt > 0 || ks > 0);
+        mma_commit(smem_addr(&sm.o_done[t][b]));
+        return true;
+      };
+      auto kv_ready = [&](int kt) -> bool {
+        if (!wait(sm.kv_full[kt % kStages], (kt / kStages) & 1)) return false;
+        fence_async_smem();  // rows the loader's lanes copied (generic proxy) -> tensor cores
+        return true;
+      };
+      bool ok = wait(sm.q_full, 0);
+      if (ok) fence_async_smem();
+      ok = ok && kv_ready(0);
+      ok = ok && (nt[0] == 0 || issue_s(0, 0));
+      ok = ok && (nt[1] == 0 || issue_s(1, 0));
+      for (int kt = 0; ok && kt < n; ++kt) {
+        const bool more = kt + 1 < n;
+        ok = kt >= nt[0] || issue_pv(0, kt);
+        ok = ok && (!more || kv_ready(kt + 1));
+        ok = ok && (!more || kt + 1 >= nt[0] || issue_s(0, kt + 1));
+        ok = ok && (kt >= nt[1] || issue_pv(1, kt));
+        if (ok) mma_commit(smem_addr(&sm.kv_empty[kt % kStages]));
+        ok = ok && (!more || kt + 1 >= nt[1] || issue_s(1, kt + 1));
       }
-      uint4 w;
-      w.x = pack2<T>(e[0], e[1]);
-      w.y = pack2<T>(e[2], e[3]);
-      w.z = pack2<T>(e[4], e[5]);
-      w.w = pack2<T>(e[6], e[7]);
-      *reinterpret_cast<uint4*>(prow + swz(kRows, tid, c)) = w;
+      mma_commit(smem_addr(&sm.fin));  // every MMA issued so far
+      wait(sm.fin, 0);
     }
-    l_run = l_run * alpha + rs;
-    if (alpha != 1.f) {
+    __syncwarp();
+  } else {
+    // ================= softmax: warpgroup t, one thread per row =================
+    const int t = warp >> 2, r = tid & (kRows - 1);
+    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + t * kTileCols;
+    const int tok = tok0 + t * tpt + r / G;
+    const bool row_ok = r / G < tpt && tok < qlen;
+    const int pos = row_ok ? ctx - qlen + tok : -1;
+    const int pos_lo = ctx - qlen + tok0 + t * tpt;  // the tile's first position
+    float m_used = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    auto wwait = [&](unsigned long long& bar, int parity) -> bool {  // warp-uniform result
+      return __all_sync(0xffffffffu, wait(bar, parity)) != 0;
+    };
+    for (int kt = 0; kt < nt[t]; ++kt) {
+      const int b = kt & 1;
+      if (!(ok = wwait(sm.s_full[t][b], (kt >> 1) & 1))) break;
+      tc_fence_after();
+      float sv[kKeys];
+      {
+        float tmp[32];
+        tmem_ld32(tl + b * kKeys, tmp);
 #pragma unroll
-      for (int i = 0; i < D; ++i) o[i] *= alpha;
+        for (int i = 0; i < 32; ++i) sv[i] = tmp[i];
+        tmem_ld32(tl + b * kKeys + 32, tmp);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sv[32 + i] = tmp[i];
+      }
+      tc_fence_before();
+      mbar_arrive(smem_addr(&sm.s_free[t][b]));
+      const bool needs_mask = kt * kKeys + kKeys - 1 > pos_lo;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < kKeys; ++i) {
+        float v = sv[i] * p.scale_log2;
+        if (needs_mask && kt * kKeys + i > pos) v = -INFINITY;
+        sv[i] = v;
+        mx = fmaxf(mx, v);
+      }
+      const float m_new = fmaxf(m_used, mx);
+      // (the P buffer is free: P V of tile kt - 1 was issued before S of tile kt, and the
+      // tensor cores complete in issue order, so it is done now that S is)
+      const bool need = kt > 0 && m_new > m_used + kRescale;
+      if (__any_sync(0xffffffffu, need)) {
+        // rescale O (rows whose maximum grew too far) once P V of tile kt - 1 is done
+        if (!(ok = wwait(sm.o_done[t][(kt - 1) & 1], ((kt - 1) >> 1) & 1))) break;
+        tc_fence_after();
+        const float alpha = need ? ex2(m_used - m_new) : 1.f;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          float o[32];
+          tmem_ld32(tl + kColO + c0, o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= alpha;
+          tmem_st32(tl + kColO + c0, o);
+        }
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        if (need) {
+          l_run *= alpha;
+          m_used = m_new;
+        }
+      }
+      if (kt == 0) m_used = m_new;
+      // P = 2^(s - m) (0 for a row with nothing unmasked yet), rounded, into its buffer
+      float rs = 0.f;
+      uint8_t* prow = sm.p[t];
+#pragma unroll
+      for (int c = 0; c < kKeys / 8; ++c) {
+        float e[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          e[j] = m_used == -INFINITY ? 0.f : ex2(sv[8 * c + j] - m_used);
+          rs += e[j];
+        }
+        uint4 w;
+        w.x = pack2<T>(e[0], e[1]);
+        w.y = pack2<T>(e[2], e[3]);
+        w.z = pack2<T>(e[4], e[5]);
+        w.w = pack2<T>(e[6], e[7]);
+        *reinterpret_cast<uint4*>(prow + swz(kRows, r, c)) = w;
+      }
+      l_run += rs;
+      fence_async_smem();  // P (generic writes) before the tensor cores read it
+      tc_fence_before();
+      mbar_arrive(smem_addr(&sm.p_full[t][b]));
     }
-    // P (generic writes) before the tensor cores read it; every S read is done
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    if (ok && nt[t] > 0) {
+      const int last = nt[t] - 1;
+      ok = wwait(sm.o_done[t][last & 1], (last >> 1) & 1);
+    }
+    // ---- out = O / l, after every role is done (the loader's bad-block flag is final) ----
+    tc_fence_before();
     __syncthreads();
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-
-    // ---- P V into its own TMEM columns, then O += P V ----
-    if (tid == 0) {
-      const uint32_t pa = smem_addr(kAliasP<D> ? sm.kv[b][0] : sm.p);
-#pragma unroll
-      for (int ks = 0; ks < KS2; ++ks)
-        mma_f16(tmem + kColO, desc_sw128(pa + ks * 32, 16, 1024),
-                desc_sw128(vb + ks * 16 * 128, kKeys * 128, 1024), id_o, ks > 0);
-      mma_commit(smem_addr(&sm.bar_o));
-    }
-    ok = wait_bounded(smem_addr(&sm.bar_o), kt & 1);
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    if (!__syncthreads_and(ok)) {
-      ok = false;
-      break;
-    }
+    tc_fence_after();
+    const bool good = ok && sm.abort == 0 && sm.bad == 0;
+    const float inv = 1.f / l_run;
+    T* dst = outp + (row_ok ? (static_cast<size_t>(qs + tok) * p.num_q_heads + g * G + r % G) * D : 0);
 #pragma unroll
     for (int c0 = 0; c0 < D; c0 += 32) {
-      float tmp[32];
-      tmem_ld32(tmem + lane_base + kColO + c0, tmp);
+      float o[32];
+      if (nt[t] > 0 && sm.abort == 0) tmem_ld32(tl + kColO + c0, o);  // (warp-uniform)
 #pragma unroll
-      for (int i = 0; i < 32; ++i) o[c0 + i] += tmp[i];
-    }
-    // every P V read and every thread's use of buffer b is done before it is refilled
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-    __syncthreads();
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-  }
-  if (!ok) {  // a wait gave up: flag it; let the copies land before leaving
-    cp_async_wait<0>();
-    if (tid == 0) atomicOr(p.err, kErrTimeout);
-  }
-
-  // ---- out = O / l ----
-  const bool bad = sm.bad != 0 || !ok;
-  if (row_ok) {
-    uint4* dst = reinterpret_cast<uint4*>(outp + row_off);
-    const float inv = 1.f / l_run;
-#pragma unroll
-    for (int c = 0; c < CH; ++c) {
-      uint4 w = make_uint4(0, 0, 0, 0);
-      if (!bad) {
-        w.x = pack2<T>(o[8 * c + 0] * inv, o[8 * c + 1] * inv);
-        w.y = pack2<T>(o[8 * c + 2] * inv, o[8 * c + 3] * inv);
-        w.z = pack2<T>(o[8 * c + 4] * inv, o[8 * c + 5] * inv);
-        w.w = pack2<T>(o[8 * c + 6] * inv, o[8 * c + 7] * inv);
+      for (int c = 0; c < 4; ++c) {
+        uint4 w = make_uint4(0, 0, 0, 0);
+        if (good && nt[t] > 0) {
+          w.x = pack2<T>(o[8 * c + 0] * inv, o[8 * c + 1] * inv);
+          w.y = pack2<T>(o[8 * c + 2] * inv, o[8 * c + 3] * inv);
+          w.z = pack2<T>(o[8 * c + 4] * inv, o[8 * c + 5] * inv);
+          w.w = pack2<T>(o[8 * c + 6] * inv, o[8 * c + 7] * inv);
+        }
+        if (row_ok) reinterpret_cast<uint4*>(dst + c0)[c] = w;
       }
-      dst[c] = w;
     }
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && sm.bad) atomicOr(p.err, kErrBadBlock);
+    return;
   }
-  if (sm.bad && tid == 0) atomicOr(p.err, kErrBadBlock);
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  // loader and MMA warps: the two CTA-wide barriers of the softmax epilogue
+  tc_fence_before();
   __syncthreads();
-  if (warp == 0)
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(kTmemCols)
                  : "memory");
+  }
 }
 
 template <int D, typename T>
@@ -404,7 +536,8 @@ int launch(const Params& prm, int max_query_len, cudaStream_t stream) {
   auto* kern = prefill_kernel<D, T>;
   if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), smem)) return -3;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((max_query_len + prm.tq - 1) / prm.tq, prm.num_seqs, prm.num_kv_heads);
+  const int per_cta = kTiles * prm.tpt;
+  cfg.gridDim = dim3((max_query_len + per_cta - 1) / per_cta, prm.num_seqs, prm.num_kv_heads);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
@@ -417,10 +550,52 @@ int launch(const Params& prm, int max_query_len, cudaStream_t stream) {
   return 0;
 }
 
+// cuTensorMapEncodeTiled, looked up once through the runtime (no link to the driver
+// library).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  return fn;
+}
+
+// A cache [num_blocks][Hkv][B][d] of 16-bit values as a 4-D tensor (d, row, kv head,
+// block) read in boxes of (64, B, 1, 1) with the 128-byte swizzle.
+bool cache_map(CUtensorMap* map, const void* base, int num_blocks, int hkv, int bs, int d) {
+  EncodeTiledFn fn = encode_tiled();
+  if (!fn) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(bs),
+                              static_cast<cuuint64_t>(hkv), static_cast<cuuint64_t>(num_blocks)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(bs) * d * 2,
+                                 static_cast<cuuint64_t>(hkv) * bs * d * 2};
+  const cuuint32_t box[4] = {64u, static_cast<cuuint32_t>(bs), 1u, 1u};
+  const cuuint32_t es[4] = {1u, 1u, 1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace prefill
 
 int prefill_launch(const PrefillArgs& a, cudaStream_t stream) {
   prefill::Params p;
+  if (!prefill::cache_map(&p.kmap, a.k_cache, a.num_blocks, a.num_kv_heads, a.block_size,
+                          a.head_dim) ||
+      !prefill::cache_map(&p.vmap, a.v_cache, a.num_blocks, a.num_kv_heads, a.block_size,
+                          a.head_dim))
+    return -3;
   p.q = static_cast<const uint8_t*>(a.q);
   p.k_cache = static_cast<const uint8_t*>(a.k_cache);
   p.v_cache = static_cast<const uint8_t*>(a.v_cache);
@@ -432,10 +607,9 @@ int prefill_launch(const PrefillArgs& a, cudaStream_t stream) {
   p.num_q_heads = a.num_q_heads;
   p.num_kv_heads = a.num_kv_heads;
   p.group = a.num_q_heads / a.num_kv_heads;
-  p.tq = prefill::kRows / p.group;
+  p.tpt = prefill::kRows / p.group;
   p.max_blocks_per_seq = a.max_blocks_per_seq;
   p.block_size = a.block_size;
-  p.log2_block = a.block_size == 8 ? 3 : (a.block_size == 16 ? 4 : 5);
   p.num_blocks = a.num_blocks;
   p.scale_log2 = a.scale * prefill::kLog2e;
   p.err = a.err;
