@@ -430,16 +430,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       }
       tc_fence_before();
       mbar_arrive(smem_addr(&sm.s_free[t][b]));
-      const bool needs_mask = kt * kKeys + kKeys - 1 > pos_lo;
-      float mx = -INFINITY;
+      // causal mask on the raw scores (key kt*64 + i > pos), then the maximum over eight
+      // independent partial chains; scores stay unscaled (the scale is positive, so the
+      // maximum commutes with it) and P = 2^(s * scale - m) is one FFMA per element
+      if (kt * kKeys + kKeys - 1 > pos_lo) {
+        const int lim = pos - kt * kKeys;
 #pragma unroll
-      for (int i = 0; i < kKeys; ++i) {
-        float v = sv[i] * p.scale_log2;
-        if (needs_mask && kt * kKeys + i > pos) v = -INFINITY;
-        sv[i] = v;
-        mx = fmaxf(mx, v);
+        for (int i = 0; i < kKeys; ++i)
+          if (i > lim) sv[i] = -INFINITY;
       }
-      const float m_new = fmaxf(m_used, mx);
+      float pm[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) pm[j] = sv[j];
+#pragma unroll
+      for (int i = 8; i < kKeys; ++i) pm[i & 7] = fmaxf(pm[i & 7], sv[i]);
+      const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                             fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+      const float m_new = fmaxf(m_used, mx * p.scale_log2);
       // (the P buffer is free: P V of tile kt - 1 was issued before S of tile kt, and the
       // tensor cores complete in issue order, so it is done now that S is)
       const bool need = kt > 0 && m_new > m_used + kRescale;
@@ -463,16 +470,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         }
       }
       if (kt == 0) m_used = m_new;
-      // P = 2^(s - m) (0 for a row with nothing unmasked yet), rounded, into its buffer
-      float rs = 0.f;
+      // P = 2^(s * scale - m) (0 for a row with nothing unmasked yet), rounded, into its
+      // buffer; the row sum over eight partial chains
+      float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      const bool live_row = m_used != -INFINITY;
+      const float neg_m = -m_used;
       uint8_t* prow = sm.p[t];
 #pragma unroll
       for (int c = 0; c < kKeys / 8; ++c) {
         float e[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          e[j] = m_used == -INFINITY ? 0.f : ex2(sv[8 * c + j] - m_used);
-          rs += e[j];
+          e[j] = live_row ? ex2(fmaf(sv[8 * c + j], p.scale_log2, neg_m)) : 0.f;
+          ps[j] += e[j];
         }
         uint4 w;
         w.x = pack2<T>(e[0], e[1]);
@@ -481,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         w.w = pack2<T>(e[6], e[7]);
         *reinterpret_cast<uint4*>(prow + swz(kRows, r, c)) = w;
       }
-      l_run += rs;
+      l_run += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       fence_async_smem();  // P (generic writes) before the tensor cores read it
       tc_fence_before();
       mbar_arrive(smem_addr(&sm.p_full[t][b]));
