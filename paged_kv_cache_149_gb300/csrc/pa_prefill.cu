@@ -74,11 +74,9 @@ struct Smem {
   uint8_t q[kTiles][kRows * D * 2];            // K-major, 128-byte swizzle; 1024-byte aligned
   uint8_t k[kStages][kKeys * D * 2];           // [64-column half][64 keys][128 B]
   uint8_t v[kStages][kKeys * D * 2];
-  uint8_t p[kTiles][kRows * kKeys * 2];        // P of a tile (reused once S of the next keys is
-                                               // done: the tensor cores complete in order)
   unsigned long long q_full;
   unsigned long long kv_full[kStages], kv_empty[kStages];
-  unsigned long long s_full[kTiles][2], s_free[kTiles][2];
+  unsigned long long s_full[kTiles][2];
   unsigned long long p_full[kTiles][2], o_done[kTiles][2];
   unsigned long long fin;  // the MMA thread's last commit
   uint32_t tmem;
@@ -152,6 +150,26 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 16 columns (32 packed 16-bit values) written to this thread's lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+
+// tcgen05.mma with A from tensor memory (lane = row, column c = elements 2c and 2c + 1).
+__device__ __forceinline__ void mma_f16_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t db,
+                                           uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(db), "r"(idesc), "r"(static_cast<uint32_t>(accumulate))
+      : "memory");
 }
 
 // The same 32 columns written back.
@@ -257,7 +275,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     for (int t = 0; t < kTiles; ++t)
       for (int b = 0; b < 2; ++b) {
         mbar_init(smem_addr(&sm.s_full[t][b]), 1);
-        mbar_init(smem_addr(&sm.s_free[t][b]), kRows);
         mbar_init(smem_addr(&sm.p_full[t][b]), kRows);
         mbar_init(smem_addr(&sm.o_done[t][b]), 1);
       }
@@ -353,7 +370,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       constexpr uint32_t id_o = idesc_f16<T>(kRows, D, true);
       auto issue_s = [&](int t, int kt) -> bool {
         const int b = kt & 1;
-        if (kt >= 2 && !wait(sm.s_free[t][b], ((kt - 2) >> 1) & 1)) return false;
+        // S buffer b holds the P of tile kt - 2 (read by its P V): wait for that P V
+        if (kt >= 2 && !wait(sm.o_done[t][b], ((kt - 2) >> 1) & 1)) return false;
         tc_fence_after();
         const uint32_t d = tmem + t * kTileCols + b * kKeys;
         const uint32_t qa = smem_addr(sm.q[t]), kb = smem_addr(sm.k[kt % kStages]);
@@ -370,11 +388,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         const int b = kt & 1;
         if (!wait(sm.p_full[t][b], (kt >> 1) & 1)) return false;
         tc_fence_after();
-        const uint32_t pa = smem_addr(sm.p[t]), vb = smem_addr(sm.v[kt % kStages]);
+        const uint32_t vb = smem_addr(sm.v[kt % kStages]);
 #pragma unroll
-        for (int ks = 0; ks < KS2; ++ks)
-          mma_f16(tmem + t * kTileCols + kColO, desc_sw128(pa + ks * 32, 16, 1024),
-                  desc_sw128(vb + ks * 16 * 128, kKeys * 128, 1024), id_o, kt > 0 || ks > 0);
+        for (int ks = 0; ks < KS2; ++ks)  // P from tensor memory: 16 keys = 8 columns
+          mma_f16_ts(tmem + t * kTileCols + kColO, tmem + t * kTileCols + b * kKeys + ks * 8,
+                     desc_sw128(vb + ks * 16 * 128, kKeys * 128, 1024), id_o, kt > 0 || ks > 0);
         mma_commit(smem_addr(&sm.o_done[t][b]));
         return true;
       };
@@ -428,8 +446,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #pragma unroll
         for (int i = 0; i < 32; ++i) sv[32 + i] = tmp[i];
       }
-      tc_fence_before();
-      mbar_arrive(smem_addr(&sm.s_free[t][b]));
       // causal mask on the raw scores (key kt*64 + i > pos), then the maximum over eight
       // independent partial chains; scores stay unscaled (the scale is positive, so the
       // maximum commutes with it) and P = 2^(s * scale - m) is one FFMA per element
@@ -447,8 +463,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
                              fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
       const float m_new = fmaxf(m_used, mx * p.scale_log2);
-      // (the P buffer is free: P V of tile kt - 1 was issued before S of tile kt, and the
-      // tensor cores complete in issue order, so it is done now that S is)
       const bool need = kt > 0 && m_new > m_used + kRescale;
       if (__any_sync(0xffffffffu, need)) {
         // rescale O (rows whose maximum grew too far) once P V of tile kt - 1 is done
@@ -470,30 +484,28 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         }
       }
       if (kt == 0) m_used = m_new;
-      // P = 2^(s * scale - m) (0 for a row with nothing unmasked yet), rounded, into its
-      // buffer; the row sum over eight partial chains
+      // P = 2^(s * scale - m) (0 for a row with nothing unmasked yet), rounded, packed two
+      // per column over the S columns just read (P V reads it there); the row sum over
+      // eight partial chains
       float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       const bool live_row = m_used != -INFINITY;
       const float neg_m = -m_used;
-      uint8_t* prow = sm.p[t];
 #pragma unroll
-      for (int c = 0; c < kKeys / 8; ++c) {
-        float e[8];
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pk[16];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          e[j] = live_row ? ex2(fmaf(sv[8 * c + j], p.scale_log2, neg_m)) : 0.f;
-          ps[j] += e[j];
+        for (int i = 0; i < 32; i += 2) {
+          const float e0 = live_row ? ex2(fmaf(sv[32 * h + i], p.scale_log2, neg_m)) : 0.f;
+          const float e1 = live_row ? ex2(fmaf(sv[32 * h + i + 1], p.scale_log2, neg_m)) : 0.f;
+          ps[i & 7] += e0;
+          ps[(i + 1) & 7] += e1;
+          pk[i >> 1] = pack2<T>(e0, e1);
         }
-        uint4 w;
-        w.x = pack2<T>(e[0], e[1]);
-        w.y = pack2<T>(e[2], e[3]);
-        w.z = pack2<T>(e[4], e[5]);
-        w.w = pack2<T>(e[6], e[7]);
-        *reinterpret_cast<uint4*>(prow + swz(kRows, r, c)) = w;
+        tmem_st16(tl + b * kKeys + 16 * h, pk);
       }
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       l_run += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-      fence_async_smem();  // P (generic writes) before the tensor cores read it
-      tc_fence_before();
+      tc_fence_before();  // the P stores before the MMA thread reads them
       mbar_arrive(smem_addr(&sm.p_full[t][b]));
     }
     if (ok && nt[t] > 0) {
