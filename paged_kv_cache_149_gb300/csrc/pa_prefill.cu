@@ -210,6 +210,13 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // 4-D tiled TMA load (x = d, y = row in the block, z = kv head, w = block), completion
 // counted in bytes on `bar`.  x is 0 or 64 (128-byte multiples).
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int x, int y,
@@ -455,13 +462,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         for (int i = 0; i < kKeys; ++i)
           if (i > lim) sv[i] = -INFINITY;
       }
-      float pm[8];
+      float pm[4];  // four chains of three-input maxima
 #pragma unroll
-      for (int j = 0; j < 8; ++j) pm[j] = sv[j];
+      for (int j = 0; j < 4; ++j) pm[j] = fmaxf(sv[2 * j], sv[2 * j + 1]);
 #pragma unroll
-      for (int i = 8; i < kKeys; ++i) pm[i & 7] = fmaxf(pm[i & 7], sv[i]);
-      const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                             fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+      for (int i = 8; i < kKeys; i += 8)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) pm[j] = fmax3(pm[j], sv[i + 2 * j], sv[i + 2 * j + 1]);
+      const float mx = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
       const float m_new = fmaxf(m_used, mx * p.scale_log2);
       const bool need = kt > 0 && m_new > m_used + kRescale;
       if (__any_sync(0xffffffffu, need)) {
@@ -487,24 +495,28 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       // P = 2^(s * scale - m) (0 for a row with nothing unmasked yet), rounded, packed two
       // per column over the S columns just read (P V reads it there); the row sum over
       // eight partial chains
-      float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      const bool live_row = m_used != -INFINITY;
-      const float neg_m = -m_used;
+      // (a row with nothing unmasked yet has every score at -inf, so any finite offset
+      // gives it P = 0; packed FP32 pairs halve the FMA and add counts)
+      const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
+      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(neg_m, neg_m);
+      float2 ps[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                      make_float2(0.f, 0.f)};
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const float e0 = live_row ? ex2(fmaf(sv[32 * h + i], p.scale_log2, neg_m)) : 0.f;
-          const float e1 = live_row ? ex2(fmaf(sv[32 * h + i + 1], p.scale_log2, neg_m)) : 0.f;
-          ps[i & 7] += e0;
-          ps[(i + 1) & 7] += e1;
-          pk[i >> 1] = pack2<T>(e0, e1);
+          const float2 x = __ffma2_rn(make_float2(sv[32 * h + i], sv[32 * h + i + 1]), sc2, nm2);
+          const float2 e = make_float2(ex2(x.x), ex2(x.y));
+          ps[(i >> 1) & 3] = __fadd2_rn(ps[(i >> 1) & 3], e);
+          pk[i >> 1] = pack2<T>(e.x, e.y);
         }
         tmem_st16(tl + b * kKeys + 16 * h, pk);
       }
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-      l_run += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+      const float2 s01 = __fadd2_rn(ps[0], ps[1]), s23 = __fadd2_rn(ps[2], ps[3]);
+      const float2 sall = __fadd2_rn(s01, s23);
+      l_run += sall.x + sall.y;
       tc_fence_before();  // the P stores before the MMA thread reads them
       mbar_arrive(smem_addr(&sm.p_full[t][b]));
     }
