@@ -375,18 +375,28 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_f16<T>(kRows, kKeys, false);
       constexpr uint32_t id_o = idesc_f16<T>(kRows, D, true);
+      // Descriptors built once: the start address is the low field (address / 16, 14
+      // bits; shared addresses here stay below 256 KB), so a byte offset o inside a tile is
+      // a plain add of o / 16 -- the issue loop is then a few adds per MMA.
+      constexpr uint32_t kStageBytes = kKeys * D * 2;
+      const uint64_t dq0 = desc_sw128(smem_addr(sm.q[0]), 16, 1024);
+      const uint64_t dq1 = desc_sw128(smem_addr(sm.q[1]), 16, 1024);
+      const uint64_t dk0 = desc_sw128(smem_addr(sm.k[0]), 16, 1024);
+      const uint64_t dv0 = desc_sw128(smem_addr(sm.v[0]), kKeys * 128, 1024);
       auto issue_s = [&](int t, int kt) -> bool {
         const int b = kt & 1;
         // S buffer b holds the P of tile kt - 2 (read by its P V): wait for that P V
         if (kt >= 2 && !wait(sm.o_done[t][b], ((kt - 2) >> 1) & 1)) return false;
         tc_fence_after();
         const uint32_t d = tmem + t * kTileCols + b * kKeys;
-        const uint32_t qa = smem_addr(sm.q[t]), kb = smem_addr(sm.k[kt % kStages]);
+        const uint64_t qd = t == 0 ? dq0 : dq1;
+        const uint64_t kd = dk0 + (((kt % kStages) * kStageBytes) >> 4);
+        mma_f16(d, qd, kd, id_s, false);
 #pragma unroll
-        for (int ks = 0; ks < KS1; ++ks) {
-          const uint32_t koff = (ks & 3) * 32;  // 16 columns = 32 bytes within a column block
-          mma_f16(d, desc_sw128(qa + (ks >> 2) * kRows * 128 + koff, 16, 1024),
-                  desc_sw128(kb + (ks >> 2) * kKeys * 128 + koff, 16, 1024), id_s, ks > 0);
+        for (int ks = 1; ks < KS1; ++ks) {
+          // k-step ks: 16 columns = 32 bytes within 64-column block ks / 4
+          mma_f16(d, qd + (((ks >> 2) * kRows * 128 + (ks & 3) * 32) >> 4),
+                  kd + (((ks >> 2) * kKeys * 128 + (ks & 3) * 32) >> 4), id_s, true);
         }
         mma_commit(smem_addr(&sm.s_full[t][b]));
         return true;
@@ -395,11 +405,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         const int b = kt & 1;
         if (!wait(sm.p_full[t][b], (kt >> 1) & 1)) return false;
         tc_fence_after();
-        const uint32_t vb = smem_addr(sm.v[kt % kStages]);
+        const uint64_t vd = dv0 + (((kt % kStages) * kStageBytes) >> 4);
+        const uint32_t o = tmem + t * kTileCols + kColO, pa = tmem + t * kTileCols + b * kKeys;
+        mma_f16_ts(o, pa, vd, id_o, kt > 0);
 #pragma unroll
-        for (int ks = 0; ks < KS2; ++ks)  // P from tensor memory: 16 keys = 8 columns
-          mma_f16_ts(tmem + t * kTileCols + kColO, tmem + t * kTileCols + b * kKeys + ks * 8,
-                     desc_sw128(vb + ks * 16 * 128, kKeys * 128, 1024), id_o, kt > 0 || ks > 0);
+        for (int ks = 1; ks < KS2; ++ks)  // P from tensor memory: 16 keys = 8 columns
+          mma_f16_ts(o, pa + ks * 8, vd + ((ks * 16 * 128) >> 4), id_o, true);
         mma_commit(smem_addr(&sm.o_done[t][b]));
         return true;
       };
