@@ -19,13 +19,15 @@
 //   cache: d, row, kv head, block; one copy per block and 64-column half); the ragged last
 //   block and the blocks past the context by cp.async with zero fill, so no row past the
 //   context is ever read (its V row must be zero: P is 0 there, and 0 x NaN is NaN).
-// * MMA warp (one thread): S = Q K^T per query tile into tensor memory (two buffers per
-//   tile), and O += P V with O kept in tensor memory across the whole key range.  The two
-//   tiles alternate so that the tensor cores work on one tile while the other's softmax
-//   runs (S of tile 0 for the next keys is issued between the P V of tiles 0 and 1).
+// * Two MMA warps, one issuing thread per query tile: S = Q K^T into tensor memory (two
+//   buffers per tile), and O += P V with P read from tensor memory (the A operand, packed
+//   over the S columns it came from) and O kept there across the whole key range.  S of a
+//   tile's next keys is issued before its current P V, so the tensor cores compute it
+//   while that tile's softmax runs, and the two tiles interleave on the tensor cores.
 // * Two softmax warpgroups, one per query tile, one thread per row (= tensor-memory
 //   lane): read the row of S, mask causally, keep the running maximum m and sum l in
-//   exp2 units, write the row of P (input type) into shared memory.  O is rescaled only
+//   exp2 units, write the row of P (input type) back over the S columns it came from.
+//   O is rescaled only
 //   when a row's maximum grows by more than 8 (in log2 units), so P <= 2^8 and the
 //   rescale (a read-modify-write of the row in tensor memory) is rare after the first
 //   tiles; the final O / l uses the same m, so the result is exact softmax.
@@ -48,8 +50,8 @@ constexpr int kRows = 128;      // rows of a query tile (MMA M, tensor-memory la
 constexpr int kKeys = 64;       // keys of a K/V tile (MMA N of S, K of P V)
 constexpr int kStages = 4;      // K/V ring
 constexpr int kLoadWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;   // 2 x 128 softmax threads, a loader warp, an MMA warp
+constexpr int kMmaWarp = 9;     // MMA issue for tile 0; tile 1 has the next warp
+constexpr int kThreads = 352;   // 2 x 128 softmax threads, a loader warp, two MMA warps
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescale = 8.f;  // log2 growth of a row's maximum that forces a rescale of O
 
@@ -277,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     mbar_init(smem_addr(&sm.q_full), 32);
     for (int i = 0; i < kStages; ++i) {
       mbar_init(smem_addr(&sm.kv_full[i]), 33);  // the TMA issuer's expect-tx + 32 copy lanes
-      mbar_init(smem_addr(&sm.kv_empty[i]), 1);
+      mbar_init(smem_addr(&sm.kv_empty[i]), kTiles);  // one commit per MMA thread
     }
     for (int t = 0; t < kTiles; ++t)
       for (int b = 0; b < 2; ++b) {
@@ -285,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         mbar_init(smem_addr(&sm.p_full[t][b]), kRows);
         mbar_init(smem_addr(&sm.o_done[t][b]), 1);
       }
-    mbar_init(smem_addr(&sm.fin), 1);
+    mbar_init(smem_addr(&sm.fin), kTiles);
     fence_mbar_init();
     sm.bad = 0;
     sm.abort = 0;
@@ -370,8 +372,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       cp_async_arrive(smem_addr(&sm.kv_full[st]));
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
-  } else if (warp == kMmaWarp) {
-    // ================= MMA issue: one thread =================
+  } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+    // ============ MMA issue: one thread per query tile (issue cost is per thread) ============
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_f16<T>(kRows, kKeys, false);
       constexpr uint32_t id_o = idesc_f16<T>(kRows, D, true);
@@ -419,21 +421,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         fence_async_smem();  // rows the loader's lanes copied (generic proxy) -> tensor cores
         return true;
       };
+      // S of the next keys goes in before P V of the current ones, so the tensor cores
+      // compute it while this tile's softmax runs.  A thread whose tile needs no more keys
+      // still releases each stage, after it has landed (one commit per stage and use).
+      const int t = warp - kMmaWarp;
       bool ok = wait(sm.q_full, 0);
       if (ok) fence_async_smem();
       ok = ok && kv_ready(0);
-      ok = ok && (nt[0] == 0 || issue_s(0, 0));
-      ok = ok && (nt[1] == 0 || issue_s(1, 0));
+      ok = ok && (nt[t] == 0 || issue_s(t, 0));
       for (int kt = 0; ok && kt < n; ++kt) {
-        const bool more = kt + 1 < n;
-        ok = kt >= nt[0] || issue_pv(0, kt);
-        ok = ok && (!more || kv_ready(kt + 1));
-        ok = ok && (!more || kt + 1 >= nt[0] || issue_s(0, kt + 1));
-        ok = ok && (kt >= nt[1] || issue_pv(1, kt));
+        if (kt + 1 < n) {
+          ok = kv_ready(kt + 1);
+          ok = ok && (kt + 1 >= nt[t] || issue_s(t, kt + 1));
+        }
+        ok = ok && (kt >= nt[t] || issue_pv(t, kt));
         if (ok) mma_commit(smem_addr(&sm.kv_empty[kt % kStages]));
-        ok = ok && (!more || kt + 1 >= nt[1] || issue_s(1, kt + 1));
       }
-      mma_commit(smem_addr(&sm.fin));  // every MMA issued so far
+      mma_commit(smem_addr(&sm.fin));  // every MMA this thread issued
       wait(sm.fin, 0);
     }
     __syncwarp();
