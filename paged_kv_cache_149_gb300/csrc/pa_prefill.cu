@@ -27,10 +27,10 @@
 // * Two softmax warpgroups, one per query tile, one thread per row (= tensor-memory
 //   lane): read the row of S, mask causally, keep the running maximum m and sum l in
 //   exp2 units, write the row of P (input type) back over the S columns it came from.
-//   O is rescaled only
-//   when a row's maximum grows by more than 8 (in log2 units), so P <= 2^8 and the
-//   rescale (a read-modify-write of the row in tensor memory) is rare after the first
-//   tiles; the final O / l uses the same m, so the result is exact softmax.
+//   O is rescaled only when a row's maximum grows by more than 8 (in log2 units), so
+//   P <= 2^8 and the rescale (a read-modify-write of the row in tensor memory) is rare
+//   after the first tiles; the final O / l uses the same m, so the result is exact
+//   softmax.
 // Every mbarrier wait is bounded (about 1 s) and checks a shared abort flag, so a stuck
 // role ends the CTA with PA_DEVERR_TIMEOUT instead of hanging.
 #include <cuda.h>
