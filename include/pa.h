@@ -397,6 +397,15 @@ int pa_pool_allocate_prefix_batch(pa_pool* pool, int n, const int64_t* seq_ids,
                                   const uint8_t* extras, const int64_t* extra_start,
                                   int* cached_out, int64_t* slots_out, int32_t* tables_out,
                                   int table_width, int* n_done);
+/* The same placement from digests computed earlier (pa_prefix_block_hashes when a request
+ * arrives, say, so that hashing stays off the scheduling step): request r holds
+ * n_tokens[r] tokens, and `digests` holds the 32-byte digests of every request's
+ * n_tokens[r] / B full blocks, request after request.  Results equal
+ * pa_pool_allocate_prefix_batch on the tokens those digests came from. */
+int pa_pool_allocate_hashed_batch(pa_pool* pool, int n, const int64_t* seq_ids,
+                                  const int32_t* n_tokens, const uint8_t* digests,
+                                  int* cached_out, int64_t* slots_out, int32_t* tables_out,
+                                  int table_width, int* n_done);
 /* pa_pool_free of n sequences in order; stops at the first error. */
 int pa_pool_free_batch(pa_pool* pool, const int64_t* seq_ids, int n);
 /* Number of blocks registered under a digest (in use or waiting in the free list). */

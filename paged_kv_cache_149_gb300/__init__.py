@@ -93,6 +93,8 @@ SIGNATURES = {
     "pa_pool_num_cached": (_i32, [_vp]),
     "pa_pool_allocate_prefix_batch": (_i32, [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                              _i32, _c.POINTER(_c.c_int)]),
+    "pa_pool_allocate_hashed_batch": (_i32, [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32,
+                                             _c.POINTER(_c.c_int)]),
     "pa_pool_free_batch": (_i32, [_vp, _vp, _i32]),
     "pa_pool_block_digest": (_i32, [_vp, _c.c_int32, _vp]),
     "pa_prefix_block_hashes": (_i32, [_vp, _i32, _i32, _vp, _i32, _vp, _i32]),
@@ -651,6 +653,30 @@ class BlockPool:
             cached.ctypes.data, slots.ctypes.data, tables.ctypes.data, int(table_width),
             ctypes.byref(done)), "allocate_prefix_batch")
         used = int((lens - cached).sum())
+        return cached, slots[:used], tables
+
+    def allocate_hashed_batch(self, seq_ids, n_tokens, digests, table_width, out=None):
+        """Place a batch from digests computed earlier (bytes or uint8 array holding every
+        request's full-block digests in order, as block_hashes returns them joined).
+        Returns (cached, slots of the uncached tokens, tables)."""
+        import numpy as np
+        ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
+        n = ids.size
+        nt = np.ascontiguousarray(np.asarray(n_tokens, dtype=np.int32))
+        dg = np.ascontiguousarray(np.frombuffer(digests, dtype=np.uint8) if isinstance(
+            digests, (bytes, bytearray)) else np.asarray(digests, dtype=np.uint8))
+        if out is None:
+            cached = np.zeros(n, dtype=np.int32)
+            slots = np.zeros(int(nt.sum()), dtype=np.int64)
+            tables = np.zeros((n, table_width), dtype=np.int32)
+        else:
+            cached, slots, tables = out
+        done = ctypes.c_int(0)
+        _check(lib().pa_pool_allocate_hashed_batch(
+            self._h, n, ids.ctypes.data, nt.ctypes.data, dg.ctypes.data if dg.size else None,
+            cached.ctypes.data, slots.ctypes.data, tables.ctypes.data, int(table_width),
+            ctypes.byref(done)), "allocate_hashed_batch")
+        used = int((nt - cached).sum())
         return cached, slots[:used], tables
 
     def free_batch(self, seq_ids):

@@ -208,11 +208,23 @@ inline void put_u32(uint8_t* p, uint32_t v) {
   p[3] = static_cast<uint8_t>(v >> 24);
 }
 
+// A 32-byte digest held by value (no allocation); its first 8 bytes, uniformly random
+// for SHA-256, serve as the hash-table hash.
+struct Digest {
+  uint64_t w[4];
+  bool operator==(const Digest& o) const {
+    return w[0] == o.w[0] && w[1] == o.w[1] && w[2] == o.w[2] && w[3] == o.w[3];
+  }
+};
+struct DigestHash {
+  size_t operator()(const Digest& d) const { return static_cast<size_t>(d.w[0]); }
+};
+
 // Digests of the n / B full blocks of a token list, chained.  Each block's message is
 // laid out in one buffer and hashed in one pass.
-std::vector<std::string> block_digests(const int32_t* tokens, int n, int bs, const uint8_t* extra,
-                                       int extra_len) {
-  std::vector<std::string> out;
+std::vector<Digest> block_digests(const int32_t* tokens, int n, int bs, const uint8_t* extra,
+                                  int extra_len) {
+  std::vector<Digest> out;
   const int m = n / bs;
   out.reserve(static_cast<size_t>(m));
   std::vector<uint8_t> msg(32 + 4 + 4 * static_cast<size_t>(bs) + 4);
@@ -227,7 +239,9 @@ std::vector<std::string> block_digests(const int32_t* tokens, int n, int bs, con
     h.update(msg.data(), msg.size());
     if (extra_len > 0) h.update(extra, static_cast<size_t>(extra_len));
     h.finish(parent);
-    out.emplace_back(reinterpret_cast<const char*>(parent), 32);
+    Digest d;
+    std::memcpy(d.w, parent, 32);
+    out.push_back(d);
   }
   return out;
 }
@@ -300,15 +314,16 @@ struct pa_pool {
   int block_size = 0;
   Tier gpu, cpu;
   std::unordered_map<int64_t, SeqState> seqs;
-  std::unordered_map<std::string, int32_t> cached;  // digest -> device block
-  std::vector<std::string> digest_of;                // device block -> digest ("" = none)
+  std::unordered_map<Digest, int32_t, DigestHash> cached;  // digest -> device block
+  std::vector<Digest> digest_of;                             // device block -> digest
+  std::vector<char> has_digest;                              //   (valid where set)
 
   // a device block from the head of the free list; a cached one is evicted
   int32_t take() {
     const int32_t b = gpu.pop();
-    if (!digest_of[b].empty()) {
+    if (has_digest[b]) {
       cached.erase(digest_of[b]);
-      digest_of[b].clear();
+      has_digest[b] = 0;
     }
     return b;
   }
@@ -328,7 +343,9 @@ pa_pool* pa_pool_create_tiered(int num_blocks, int block_size, const int32_t* in
       delete p;
       return nullptr;
     }
-    p->digest_of.assign(num_blocks, std::string());
+    p->digest_of.assign(num_blocks, Digest{});
+    p->has_digest.assign(num_blocks, 0);
+    p->cached.reserve(static_cast<size_t>(num_blocks));
   } catch (...) {
     delete p;
     return nullptr;
@@ -543,12 +560,12 @@ int pa_pool_cpu_refcount(const pa_pool* pool, int32_t block) {
 
 // Prefill with prefix caching of one request whose digests are known.
 static int allocate_prefix_core(pa_pool* pool, int64_t seq_id, int n_tokens,
-                                const std::vector<std::string>& dg, int* cached_tokens_out) {
+                                const std::vector<Digest>& dg, int* cached_tokens_out) {
   if (pool->seqs.count(seq_id)) return PA_ERR_UNKNOWN_SEQ;
   const int bs = pool->block_size;
   // the longest run of leading full blocks already cached
   std::vector<int32_t> hits;
-  for (const std::string& d : dg) {
+  for (const Digest& d : dg) {
     auto it = pool->cached.find(d);
     if (it == pool->cached.end()) break;
     hits.push_back(it->second);
@@ -567,13 +584,40 @@ static int allocate_prefix_core(pa_pool* pool, int64_t seq_id, int n_tokens,
   }
   for (int64_t i = 0; i < need; ++i) st.table.push_back(pool->take());
   for (size_t i = hits.size(); i < dg.size(); ++i) {
-    if (pool->cached.count(dg[i])) continue;  // another block already answers this digest
-    pool->cached.emplace(dg[i], st.table[i]);
+    if (!pool->cached.emplace(dg[i], st.table[i]).second) continue;  // another block answers it
     pool->digest_of[st.table[i]] = dg[i];
+    pool->has_digest[st.table[i]] = 1;
   }
   st.ctx = n_tokens;
   pool->seqs.emplace(seq_id, std::move(st));
   if (cached_tokens_out) *cached_tokens_out = static_cast<int>(hits.size()) * bs;
+  return PA_OK;
+}
+
+// Lookups and allocation of a batch whose digests are known, in request order, with the
+// slots of the uncached tokens and the block tables written out.
+static int place_batch(pa_pool* pool, int n, const int64_t* seq_ids, const std::vector<int>& lens,
+                       const std::vector<std::vector<Digest>>& dg, int* cached_out,
+                       int64_t* slots_out, int32_t* tables_out, int table_width, int* n_done) {
+  const int bs = pool->block_size;
+  int64_t o = 0;
+  for (int r = 0; r < n; ++r) {
+    const int len = lens[r];
+    int cached = 0;
+    const int st = allocate_prefix_core(pool, seq_ids[r], len, dg[r], &cached);
+    if (st < 0) return st;
+    cached_out[r] = cached;
+    const SeqState& seq = pool->seqs.find(seq_ids[r])->second;
+    if (slots_out)
+      for (int t = cached; t < len; ++t)
+        slots_out[o++] = static_cast<int64_t>(seq.table[t / bs]) * bs + t % bs;
+    if (tables_out) {
+      int32_t* row = tables_out + static_cast<size_t>(r) * table_width;
+      const int nt = static_cast<int>(seq.table.size());
+      for (int j = 0; j < table_width; ++j) row[j] = j < nt ? seq.table[j] : 0;
+    }
+    if (n_done) *n_done = r + 1;
+  }
   return PA_OK;
 }
 
@@ -585,7 +629,7 @@ int pa_pool_allocate_prefix(pa_pool* pool, int64_t seq_id, const int32_t* tokens
       (extra_len > 0 && !extra))
     return PA_ERR_ARG;
   if (pool->seqs.count(seq_id)) return PA_ERR_UNKNOWN_SEQ;
-  std::vector<std::string> dg;
+  std::vector<Digest> dg;
   try {
     dg = block_digests(tokens, n_tokens, pool->block_size, extra, extra_len);
     return allocate_prefix_core(pool, seq_id, n_tokens, dg, cached_tokens_out);
@@ -613,7 +657,7 @@ int pa_pool_allocate_prefix_batch(pa_pool* pool, int n, const int64_t* seq_ids,
   }
   try {
     // the digest chains, one request per task
-    std::vector<std::vector<std::string>> dg(static_cast<size_t>(n));
+    std::vector<std::vector<Digest>> dg(static_cast<size_t>(n));
     std::atomic<bool> failed{false};
     const std::function<void(int)> hash_one = [&](int r) {
       try {
@@ -632,29 +676,41 @@ int pa_pool_allocate_prefix_batch(pa_pool* pool, int n, const int64_t* seq_ids,
     else
       for (int r = 0; r < n; ++r) hash_one(r);
     if (failed.load()) return PA_ERR_ARG;
-    // lookups and allocation, in request order
-    int64_t o = 0;
-    for (int r = 0; r < n; ++r) {
-      const int len = static_cast<int>(token_start[r + 1] - token_start[r]);
-      int cached = 0;
-      const int st = allocate_prefix_core(pool, seq_ids[r], len, dg[r], &cached);
-      if (st < 0) return st;
-      cached_out[r] = cached;
-      const SeqState& seq = pool->seqs.find(seq_ids[r])->second;
-      if (slots_out)
-        for (int t = cached; t < len; ++t)
-          slots_out[o++] = static_cast<int64_t>(seq.table[t / bs]) * bs + t % bs;
-      if (tables_out) {
-        int32_t* row = tables_out + static_cast<size_t>(r) * table_width;
-        const int nt = static_cast<int>(seq.table.size());
-        for (int j = 0; j < table_width; ++j) row[j] = j < nt ? seq.table[j] : 0;
-      }
-      if (n_done) *n_done = r + 1;
-    }
+    std::vector<int> lens(static_cast<size_t>(n));
+    for (int r = 0; r < n; ++r) lens[r] = static_cast<int>(token_start[r + 1] - token_start[r]);
+    return place_batch(pool, n, seq_ids, lens, dg, cached_out, slots_out, tables_out, table_width,
+                       n_done);
   } catch (...) {
     return PA_ERR_ARG;
   }
-  return PA_OK;
+}
+
+int pa_pool_allocate_hashed_batch(pa_pool* pool, int n, const int64_t* seq_ids,
+                                  const int32_t* n_tokens, const uint8_t* digests,
+                                  int* cached_out, int64_t* slots_out, int32_t* tables_out,
+                                  int table_width, int* n_done) {
+  if (n_done) *n_done = 0;
+  if (!pool || n < 0 || (n > 0 && (!seq_ids || !n_tokens || !cached_out)) || table_width < 0)
+    return PA_ERR_ARG;
+  if (n == 0) return PA_OK;
+  const int bs = pool->block_size;
+  try {
+    std::vector<int> lens(static_cast<size_t>(n));
+    std::vector<std::vector<Digest>> dg(static_cast<size_t>(n));
+    const uint8_t* d = digests;
+    for (int r = 0; r < n; ++r) {
+      lens[r] = n_tokens[r];
+      if (lens[r] < 0 || (tables_out && (lens[r] + bs - 1) / bs > table_width)) return PA_ERR_ARG;
+      const int m = lens[r] / bs;
+      if (m > 0 && !digests) return PA_ERR_ARG;
+      dg[r].resize(static_cast<size_t>(m));
+      for (int i = 0; i < m; ++i, d += 32) std::memcpy(dg[r][i].w, d, 32);
+    }
+    return place_batch(pool, n, seq_ids, lens, dg, cached_out, slots_out, tables_out, table_width,
+                       n_done);
+  } catch (...) {
+    return PA_ERR_ARG;
+  }
 }
 
 int pa_pool_free_batch(pa_pool* pool, const int64_t* seq_ids, int n) {
@@ -672,9 +728,8 @@ int pa_pool_num_cached(const pa_pool* pool) {
 
 int pa_pool_block_digest(const pa_pool* pool, int32_t block, uint8_t* digest_out) {
   if (!pool || !digest_out || block < 0 || block >= pool->gpu.num_blocks) return PA_ERR_ARG;
-  const std::string& d = pool->digest_of[block];
-  if (d.empty()) return 0;
-  std::memcpy(digest_out, d.data(), 32);
+  if (!pool->has_digest[block]) return 0;
+  std::memcpy(digest_out, pool->digest_of[block].w, 32);
   return 1;
 }
 
@@ -685,8 +740,8 @@ int pa_prefix_block_hashes(const int32_t* tokens, int n_tokens, int block_size,
     return PA_ERR_ARG;
   const int m = n_tokens / block_size;
   if (m > cap || (m > 0 && !digests_out)) return PA_ERR_ARG;
-  const std::vector<std::string> dg = block_digests(tokens, n_tokens, block_size, extra, extra_len);
-  for (int i = 0; i < m; ++i) std::memcpy(digests_out + 32 * i, dg[i].data(), 32);
+  const std::vector<Digest> dg = block_digests(tokens, n_tokens, block_size, extra, extra_len);
+  for (int i = 0; i < m; ++i) std::memcpy(digests_out + 32 * i, dg[i].w, 32);
   return m;
 }
 

@@ -344,3 +344,29 @@ def test_batch_allocation_equals_sequential_calls(libpa, seed):
             seq.free(i)
             ref.free(i)
         same_cache(batch, ref)
+
+
+def test_hashed_batch_equals_token_batch(libpa):
+    """Placing from digests computed earlier gives the pool, hits, slots and tables that
+    placing from the tokens does."""
+    rng = np.random.default_rng(11)
+    nb, bs = 2048, 16
+    order = rng.permutation(nb)
+    a, b = libpa.BlockPool(nb, bs, order), libpa.BlockPool(nb, bs, order)
+    system = rng.integers(0, 1000, size=40 * bs).tolist()
+    for rnd in range(4):
+        n = int(rng.integers(1, 12))
+        ids = [rnd * 100 + r for r in range(n)]
+        prompts = [system[:int(rng.integers(0, len(system)))] +
+                   rng.integers(0, 1000, size=int(rng.integers(0, 4 * bs))).tolist() for _ in range(n)]
+        ts = np.zeros(n + 1, dtype=np.int64)
+        np.cumsum([len(p) for p in prompts], out=ts[1:])
+        toks = np.concatenate([np.asarray(p, np.int32) for p in prompts] + [np.zeros(0, np.int32)])
+        want = a.allocate_prefix_batch(ids, toks, ts, table_width=48)
+        digests = b"".join(d for p in prompts for d in libpa.block_hashes(p, bs))
+        got = b.allocate_hashed_batch(ids, [len(p) for p in prompts], digests, 48)
+        for x, y in zip(want, got):
+            np.testing.assert_array_equal(x, y)
+        assert list(a.free_list()) == list(b.free_list()) and a.num_cached() == b.num_cached()
+        a.free_batch(ids[::3])
+        b.free_batch(ids[::3])
