@@ -141,6 +141,17 @@ class ClockSampler:
                 "window": "timed region" if inside else "after the timed region (too short to sample)"}
 
 
+def rotation_pool(wl, rotate):
+    """Blocks and free order of a pool that holds `rotate` copies of the batch: the
+    workload's own pool when it is large enough, else one sized for the copies (a seeded
+    shuffle, like the workload's)."""
+    import numpy as np
+    need = rotate * sum(-(-int(c) // wl.block_size) for c in wl.context_lens)
+    if need <= wl.num_blocks:
+        return wl.num_blocks, wl.free_order
+    return need, np.random.default_rng(1).permutation(need).astype(np.int32)
+
+
 def build_batches(wl, device, rotate):
     """Place `rotate` copies of the batch in disjoint blocks of one pool and write every
     token except each sequence's newest one (the step writes those)."""
@@ -153,10 +164,11 @@ def build_batches(wl, device, rotate):
     def up(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(dt)
 
-    shape = (wl.num_blocks, wl.num_kv_heads, wl.block_size, wl.head_dim)
+    nb, order = rotation_pool(wl, rotate)
+    shape = (nb, wl.num_kv_heads, wl.block_size, wl.head_dim)
     k_cache = torch.zeros(shape, dtype=dt, device=device)
     v_cache = torch.zeros(shape, dtype=dt, device=device)
-    pool = pa.BlockPool(wl.num_blocks, wl.block_size, wl.free_order)
+    pool = pa.BlockPool(nb, wl.block_size, order)
     n, T = wl.num_seqs, wl.max_blocks_per_seq
     keys, values = up(wl.keys), up(wl.values)
     last_rows = torch.from_numpy(wl.seq_start[1:] - 1).to(device)
@@ -1170,10 +1182,11 @@ def run_gpu_fp8(args, rank, world, local_rank):
 
     def up(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(dt)
-    shape = (wl.num_blocks, wl.num_kv_heads, wl.block_size, wl.head_dim)
+    nb, order = rotation_pool(wl, ROTATE)
+    shape = (nb, wl.num_kv_heads, wl.block_size, wl.head_dim)
     k8 = torch.zeros(shape, dtype=torch.uint8, device=device)
     v8 = torch.zeros(shape, dtype=torch.uint8, device=device)
-    pool = pa.BlockPool(wl.num_blocks, wl.block_size, wl.free_order)
+    pool = pa.BlockPool(nb, wl.block_size, order)
     n, T = wl.num_seqs, wl.max_blocks_per_seq
     keys, values = up(wl.keys), up(wl.values)
     last_rows = torch.from_numpy(wl.seq_start[1:] - 1).to(device)
@@ -1350,9 +1363,9 @@ def fp8_line(args, res, world):
             "l2": f"{ROTATE} batches in disjoint blocks rotated every step "
                   f"({dec_b / 1e6:.0f} MB of decode bytes per batch)",
             "parallelism": f"replicas x{world}",
-            "step": "pa_decode_append_fp8: the newest rows quantised into the cache and the "
-                    "decode, one kernel (two-call step: pa_reshape_and_cache_fp8 + "
-                    "pa_decode_fp8)",
+            "step": "pa_decode_append_fp8: the newest rows quantised into their slots, then "
+                    "the decode as a programmatic dependent (two launches; the two-call step "
+                    "is pa_reshape_and_cache_fp8 + pa_decode_fp8)",
         },
         "roofline": {"bound": "hbm", "kernel": "decode_kernel<F8> (pa_decode_fp8)",
                      "achieved": round(achieved, 1), "peak": peak,
@@ -1467,7 +1480,7 @@ def main(argv=None, runner=None, backend="nccl"):
             "workload": (f"{wl.name}: {wl.num_seqs} seqs, ctx {int(wl.context_lens.min())}..."
                          f"{int(wl.context_lens.max())} (sum {int(wl.context_lens.sum())}), "
                          f"{wl.num_q_heads} q / {wl.num_kv_heads} kv heads, head_dim {wl.head_dim}, "
-                         f"block_size {wl.block_size}, pool {wl.num_blocks} blocks; step = "
+                         f"block_size {wl.block_size}, pool {rotation_pool(wl, ROTATE)[0]} blocks; step = "
                          f"cache write of {wl.num_seqs} new tokens + paged decode, one kernel "
                          f"(pa_decode_append)"),
             "l2": f"each batch's K/V ({dec_b / 1e6:.0f} MB) exceeds L2; {ROTATE} batches in "

@@ -332,7 +332,8 @@ def decode_fp8(q, k_cache, v_cache, block_tables, context_lens, scale, k_scale, 
 def decode_append_fp8(q, key_new, value_new, k_cache, v_cache, block_tables, context_lens,
                       scale, k_scale, v_scale, out=None, workspace=None, stream=None):
     """One FP8 decode step: quantise each sequence's newest K/V row into its slot at
-    position ctx - 1 and decode, in one kernel (= reshape_and_cache_fp8 + decode_fp8)."""
+    position ctx - 1 and decode (= reshape_and_cache_fp8 + decode_fp8, with the slots read
+    from the block tables): two launches, the decode a programmatic dependent of the write."""
     import torch
     n, hq, d = q.shape
     nb, hkv, bs, d2 = k_cache.shape

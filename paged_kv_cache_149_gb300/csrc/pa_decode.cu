@@ -68,7 +68,8 @@ int decode_launch(const DecodeArgs& a, int grid, cudaStream_t stream) {
   p.log2_block = a.block_size == 8 ? 3 : (a.block_size == 16 ? 4 : 5);
   p.num_blocks = a.num_blocks;
   p.max_ctx = a.max_blocks_per_seq * a.block_size;
-  p.seg_cost = decode::kSegCost;
+  p.log2_stage = a.kv_fp8 ? 5 : 4;  // 32-token stages over FP8 blocks, 16 over 16-bit ones
+  p.seg_cost = decode::kSegCost >> (p.log2_stage - 4);  // the same charge in tokens
   // FP8 blocks: scores are k_scale * <q, codes>, outputs v_scale * (weighted codes)
   p.scale_log2 = a.scale * (a.kv_fp8 ? a.k_scale : 1.f) * decode::kLog2e;
   p.out_scale = a.kv_fp8 ? a.v_scale : 1.f;

@@ -69,19 +69,25 @@ constexpr float kLog2e = 1.4426950408889634f;
 // 64: 58.4 us on 64 sequences of 128..2048 tokens; 16 x 8192 tokens: 102.9 / 96.5 / 93.9).
 constexpr int kSegCost = 32;
 
-// EB: bytes per cached K/V element (2 for fp16/bf16 blocks, 1 for FP8 E4M3 blocks).
+// EB: bytes per cached K/V element (2 for fp16/bf16 blocks, 1 for FP8 E4M3 blocks).  A
+// stage of FP8 blocks holds 32 tokens (the bytes of 16 tokens of a 16-bit cache), so the
+// per-stage work that does not scale with bytes (softmax reductions, bookkeeping) is paid
+// once per 32 tokens.
 template <int D, int EB = 2>
 struct Geo {
+  static constexpr int kTok = EB == 1 ? 2 * kStageTok : kStageTok;  // tokens per stage
+  static constexpr int kLog2Tok = EB == 1 ? 5 : 4;
   static constexpr int kRowBytes = D * EB;
   static constexpr int kRowChunks = kRowBytes / 16;         // 16-byte chunks per row
-  static constexpr int kKBytes = kStageTok * kRowBytes;     // K rows of a stage
+  static constexpr int kKBytes = kTok * kRowBytes;          // K rows of a stage
   static constexpr int kStageBytes = 2 * kKBytes;           // K then V
   // Ring slots per warp (192 KB in all, at most 32) and how many stages ahead a warp loads.
   static constexpr int kSlots0 = (192 * 1024) / (kStageBytes * kWarps);
   static constexpr int kSlots = kSlots0 > 32 ? 32 : kSlots0;
   static constexpr int kAhead = kSlots - 1;
   static constexpr int kRowsPerPass = 32 / kRowChunks;      // rows one warp-wide copy covers
-  static constexpr int kPasses = kStageTok / kRowsPerPass;  // copies per lane per K (or V)
+  static constexpr int kPasses = kTok / kRowsPerPass;       // copies per lane per K (or V)
+  static constexpr int kMaxSpan = kTok / 8;                 // blocks a stage can span (B >= 8)
   static constexpr int kKSteps = D / 16;                    // MMA k-steps of K Q^T
 };
 
@@ -99,7 +105,8 @@ struct Params {
   int num_seqs, num_q_heads, num_kv_heads, group, heads_per_pair, head_chunks;
   int gs, log2_gs, ngroups, phases;  // pairs per family, families per sequence, warps per pair
   int max_blocks_per_seq, block_size, log2_block, num_blocks, max_ctx;
-  int seg_cost;  // stage units charged per family on top of its stages
+  int log2_stage;  // tokens per stage: 16 (16-bit blocks) or 32 (FP8 blocks)
+  int seg_cost;    // stage units charged per family on top of its stages
   float scale_log2;
   float out_scale;  // FP8 blocks: v_scale, applied to every output row (else unused)
   // [grid][gs]: arrivals at cut pair (first CTA, pi): epoch tag << 24 | pieces counted in
@@ -110,9 +117,9 @@ struct Params {
   unsigned* err;
 };
 
-// Units (16-token stages per pair) of a sequence; an invalid context length counts one.
-__device__ __forceinline__ int pair_stages(int ctx, int max_ctx) {
-  return (ctx >= 1 && ctx <= max_ctx) ? (ctx + kStageTok - 1) / kStageTok : 1;
+// Units (stages per pair) of a sequence; an invalid context length counts one.
+__device__ __forceinline__ int pair_stages(int ctx, const Params& p) {
+  return (ctx >= 1 && ctx <= p.max_ctx) ? ((ctx - 1) >> p.log2_stage) + 1 : 1;
 }
 
 // Family (sequence s, pair group g) and its place in the batch's stage order.
@@ -126,7 +133,7 @@ struct Fam {
 __device__ __forceinline__ void fam_load(Fam& f, const Params& p) {
   f.ctx = __ldg(p.context_lens + f.s);
   f.ok = f.ctx >= 1 && f.ctx <= p.max_ctx;
-  f.ns = pair_stages(f.ctx, p.max_ctx);
+  f.ns = pair_stages(f.ctx, p);
   f.fw = static_cast<long long>(f.ns) * p.gs + p.seg_cost;
 }
 
@@ -190,7 +197,7 @@ __device__ __forceinline__ PairHeads pair_heads(const Params& p, int pair) {
 // This warp's stages in order: for every family of the share, the units of its pair with
 // unit index = its phase (mod P).  Families with an invalid context carry no stages.
 struct Stage {
-  int s, kvh, t0, nt;  // sequence, kv head, first token, valid tokens (1..16)
+  int s, kvh, t0, nt;  // sequence, kv head, first token, valid tokens (1..tokens per stage)
   bool last;           // holds the context's last token
 };
 
@@ -217,8 +224,8 @@ __device__ __forceinline__ bool next_stage(StageIt& it, int pi, int phase, long 
     if (it.j < it.jb) {
       st.s = it.f.s;
       st.kvh = it.kvh;
-      st.t0 = it.j * kStageTok;
-      st.nt = min(kStageTok, it.f.ctx - st.t0);
+      st.t0 = it.j << p.log2_stage;
+      st.nt = min(1 << p.log2_stage, it.f.ctx - st.t0);
       st.last = st.t0 + st.nt == it.f.ctx;
       it.j += p.phases;
       return true;
@@ -229,15 +236,16 @@ __device__ __forceinline__ bool next_stage(StageIt& it, int pi, int phase, long 
   }
 }
 
-// Block-table entries of a stage: x = the block holding its first token, y = the next
-// block when the stage spans two blocks (block_size 8), else x.
-__device__ __forceinline__ int2 stage_entries(const Stage& st, const Params& p) {
+// Block-table entries of a stage: e[k] = the k-th block holding its tokens (the entry of
+// block t0 / B + k); entries past the stage's last token repeat e[0] and are not read.
+template <int NE>
+__device__ __forceinline__ void stage_entries(const Stage& st, const Params& p, int (&e)[NE]) {
   const int32_t* trow = p.block_tables + static_cast<size_t>(st.s) * p.max_blocks_per_seq;
   const int j0 = st.t0 >> p.log2_block;
-  int2 e;
-  e.x = __ldg(trow + j0);
-  e.y = ((st.t0 & (p.block_size - 1)) + st.nt > p.block_size) ? __ldg(trow + j0 + 1) : e.x;
-  return e;
+  const int jl = (st.t0 + st.nt - 1) >> p.log2_block;
+  e[0] = __ldg(trow + j0);
+#pragma unroll
+  for (int k = 1; k < NE; ++k) e[k] = j0 + k <= jl ? __ldg(trow + j0 + k) : e[0];
 }
 
 // 16-byte global -> shared copy through L2 only; the bytes past src_bytes (0 or 16) are
@@ -323,12 +331,29 @@ __device__ __forceinline__ int drow(int mt, int r) {
   return F8 ? (r & 7) * (D / 8) + 2 * mt + (r >> 3) : 16 * mt + r;
 }
 
-// Two E4M3 values (low byte first) -> f16x2, exact (every E4M3 value is an f16 normal).
-__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t two_bytes) {
+// Two E4M3 values (low byte first) -> f16x2, exact (every E4M3 value is an f16 normal):
+// from the low or the high half of a 32-bit word.
+__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t w) {
   uint32_t r;
-  const uint16_t v = static_cast<uint16_t>(two_bytes);
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}"
+      : "=r"(r)
+      : "r"(w));
   return r;
+}
+__device__ __forceinline__ uint32_t e4m3x2_f16x2_hi(uint32_t w) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, hi;\n\t}"
+      : "=r"(r)
+      : "r"(w));
+  return r;
+}
+
+// 2^x on the SFU (ex2.approx, subnormal results flushed to zero; 2^-inf = 0).  The
+// softmax only takes it of x <= 0.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // A piece of a cut pair as every holder of a piece sees it: the CTAs holding its first and
@@ -418,15 +443,18 @@ __device__ void merge_pieces(const Params& p, int pi, int c, int first_slot, int
   }
 }
 
-// Wait for phase 0 of a single-use mbarrier, bounded by kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait_once(uint32_t bar) {
-  if (mbar_try_wait(bar, 0)) return true;
+// Wait for the phase of `bar` with parity `parity`, bounded by kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
-  for (;;) {
-    if (mbar_try_wait(bar, 0)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 31u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) return false;
   }
 }
+
+// Wait for phase 0 of a single-use mbarrier, bounded by kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait_once(uint32_t bar) { return mbar_wait_limit(bar, 0); }
 
 // One warp merges the cut pairs it completed (up to two) through its own ring, which is
 // idle once the share is streamed: every piece's O is copied in by one bulk copy per piece
@@ -637,6 +665,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   using TM = typename std::conditional<F8, __half, T>::type;  // MMA operand type
   constexpr int R = G_::kSlots;
   constexpr int KS = G_::kKSteps;
+  constexpr int ST = G_::kTok;  // tokens per stage
+  constexpr int U = ST / 16;    // 16-token m-tiles per stage
   constexpr int MT = D / 16;  // m-tiles of O^T (16 rows of d each)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
@@ -675,7 +705,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   long long mine = 0;
   for (int s = sa; s < sb; ++s)
     mine += static_cast<long long>(p.ngroups) *
-            (static_cast<long long>(pair_stages(__ldg(p.context_lens + s), p.max_ctx)) * p.gs +
+            (static_cast<long long>(pair_stages(__ldg(p.context_lens + s), p)) * p.gs +
              p.seg_cost);
   long long incl = mine;  // inclusive scan of `mine` over the block
 #pragma unroll
@@ -700,7 +730,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     int s = sa;
     for (;; ++s) {
       const long long u = static_cast<long long>(p.ngroups) *
-                          (static_cast<long long>(pair_stages(__ldg(p.context_lens + s), p.max_ctx)) *
+                          (static_cast<long long>(pair_stages(__ldg(p.context_lens + s), p)) *
                                p.gs + p.seg_cost);
       if (w0 < pre + u) break;
       pre += u;
@@ -728,31 +758,41 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   StageIt sit;
   sit.f = first;
   stage_it_enter(sit, pi, phase, w0, w1, p);
+  constexpr int NE = G_::kMaxSpan;
   Stage nxt;
   bool nxt_ok = next_stage(sit, pi, phase, w0, w1, nxt, p);
-  int2 nxt_e = nxt_ok ? stage_entries(nxt, p) : make_int2(0, 0);
+  int nxt_e[NE];
+#pragma unroll
+  for (int k = 0; k < NE; ++k) nxt_e[k] = 0;
+  if (nxt_ok) stage_entries<NE>(nxt, p, nxt_e);
   uint32_t issued = 0;   // stages this warp has issued (slot = count % R)
   uint32_t badbits = 0;  // slots whose stage has an out-of-range block id
 
   auto issue_one = [&]() {
     if (nxt_ok) {
       const uint32_t slot = issued % R;
-      const bool two = (nxt.t0 & (p.block_size - 1)) + nxt.nt > p.block_size;
-      const bool bad = nxt_e.x < 0 || nxt_e.x >= p.num_blocks ||
-                       (two && (nxt_e.y < 0 || nxt_e.y >= p.num_blocks));
+      bool bad = false;
+#pragma unroll
+      for (int k = 0; k < NE; ++k) bad = bad || nxt_e[k] < 0 || nxt_e[k] >= p.num_blocks;
       badbits = bad ? (badbits | (1u << slot)) : (badbits & ~(1u << slot));
       if (!bad) {
         const uint32_t dst = ring + slot * G_::kStageBytes;
         const int row0 = nxt.t0 & (p.block_size - 1);
-        const size_t row_x = static_cast<size_t>((nxt_e.x * p.num_kv_heads + nxt.kvh) * p.block_size);
-        const size_t row_y = static_cast<size_t>((nxt_e.y * p.num_kv_heads + nxt.kvh) * p.block_size);
+        size_t rbase[NE];  // first cache row of (block e[k], kv head)
+#pragma unroll
+        for (int k = 0; k < NE; ++k)
+          rbase[k] = static_cast<size_t>((nxt_e[k] * p.num_kv_heads + nxt.kvh) * p.block_size);
 #pragma unroll
         for (int j = 0; j < G_::kPasses; ++j) {
           const int row = rsub + j * G_::kRowsPerPass;
           const int r = row0 + row;
           const bool live = row < nxt.nt;
-          // rows past the context: zero-filled, nothing read (the source stays in block x)
-          const size_t grow = !live ? row_x : (r < p.block_size ? row_x + r : row_y + (r - p.block_size));
+          const int kk = r >> p.log2_block;  // which of the stage's blocks
+          size_t rb = rbase[0];
+#pragma unroll
+          for (int k = 1; k < NE; ++k) rb = kk == k ? rbase[k] : rb;
+          // rows past the context: zero-filled, nothing read (the source stays in block e[0])
+          const size_t grow = !live ? rbase[0] : rb + (r & (p.block_size - 1));
           const size_t src = grow * G_::kRowBytes + ch * 16;
           const uint32_t so = F8 ? swz8<D>(row, ch) : swz(row, ch);
           if (!F8 && p.key_new && nxt.last && row == nxt.nt - 1) {
@@ -768,7 +808,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       }
       ++issued;
       nxt_ok = next_stage(sit, pi, phase, w0, w1, nxt, p);
-      if (nxt_ok) nxt_e = stage_entries(nxt, p);
+      if (nxt_ok) stage_entries<NE>(nxt, p, nxt_e);
     }
     cp_async_commit();  // one group per call, empty or not
   };
@@ -848,49 +888,54 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     const int j_first = r.x + (phase - r.x % P + P) % P;
     for (int j = j_first; j < r.y; j += P) {
       issue_one();                   // stage used + kAhead goes in flight
-      cp_async_wait<G_::kAhead>();   // this lane's copies of stage `used` have landed
-      __syncwarp();                  // ... and every other lane's
       const uint32_t slot = used % R;
       ++used;
-      const int nt_tok = min(kStageTok, f.ctx - j * kStageTok);
+      cp_async_wait<G_::kAhead>();   // this lane's copies of stage `used` have landed
+      __syncwarp();                  // ... and every other lane's
+      const int nt_tok = min(ST, f.ctx - j * ST);
       if (badbits & (1u << slot)) {
         seg_bad = true;
       } else {
         const uint32_t kb = ring + slot * G_::kStageBytes;
         const uint32_t vb = kb + G_::kKBytes;
-        // ---- S^T = K Q^T: rows = the stage's 16 tokens, columns = heads ----
-        float sacc[NTH][4], sodd[NTH][4];
+        // ---- S^T = K Q^T: rows = the stage's tokens (U m-tiles of 16), columns = heads ----
+        float sacc[U][NTH][4], sodd[U][NTH][4];
 #pragma unroll
-        for (int nt = 0; nt < NTH; ++nt)
+        for (int u = 0; u < U; ++u)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) sacc[nt][e] = sodd[nt][e] = 0.f;
-        if (F8) {
-          // K rows r0 and r0 + 8, bytes [(D/4) t, (D/4)(t+1)): word ks of a row holds the
+          for (int nt = 0; nt < NTH; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sacc[u][nt][e] = sodd[u][nt][e] = 0.f;
+        if constexpr (F8) {
+          // K rows 16u + r0 and + 8, bytes [(D/4) t, (D/4)(t+1)): word ks of a row holds the
           // four d of k-step ks (the order load_q8 gives q)
-          uint32_t kw[2][KS];
 #pragma unroll
-          for (int hr = 0; hr < 2; ++hr)
+          for (int u = 0; u < U; ++u) {
+            uint32_t kw[2][KS];
 #pragma unroll
-            for (int i = 0; i < KS / 4; ++i) {
-              const uint32_t addr = kb + swz8<D>(r0 + 8 * hr, (KS / 4) * (lane & 3) + i);
-              asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                           : "=r"(kw[hr][4 * i]), "=r"(kw[hr][4 * i + 1]), "=r"(kw[hr][4 * i + 2]),
-                             "=r"(kw[hr][4 * i + 3])
-                           : "r"(addr));
-            }
+            for (int hr = 0; hr < 2; ++hr)
 #pragma unroll
-          for (int ks = 0; ks < KS; ++ks) {
-            uint32_t a[4];
-            a[0] = e4m3x2_f16x2(kw[0][ks]);
-            a[1] = e4m3x2_f16x2(kw[1][ks]);
-            a[2] = e4m3x2_f16x2(kw[0][ks] >> 16);
-            a[3] = e4m3x2_f16x2(kw[1][ks] >> 16);
+              for (int i = 0; i < KS / 4; ++i) {
+                const uint32_t addr = kb + swz8<D>(16 * u + r0 + 8 * hr, (KS / 4) * (lane & 3) + i);
+                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(kw[hr][4 * i]), "=r"(kw[hr][4 * i + 1]), "=r"(kw[hr][4 * i + 2]),
+                               "=r"(kw[hr][4 * i + 3])
+                             : "r"(addr));
+              }
 #pragma unroll
-            for (int nt = 0; nt < NTH; ++nt) {
-              if (ks & 1)
-                mma16816<TM>(sodd[nt], a, qb[ks][nt][0], qb[ks][nt][1]);
-              else
-                mma16816<TM>(sacc[nt], a, qb[ks][nt][0], qb[ks][nt][1]);
+            for (int ks = 0; ks < KS; ++ks) {
+              uint32_t a[4];
+              a[0] = e4m3x2_f16x2(kw[0][ks]);
+              a[1] = e4m3x2_f16x2(kw[1][ks]);
+              a[2] = e4m3x2_f16x2_hi(kw[0][ks]);
+              a[3] = e4m3x2_f16x2_hi(kw[1][ks]);
+#pragma unroll
+              for (int nt = 0; nt < NTH; ++nt) {
+                if (ks & 1)
+                  mma16816<TM>(sodd[u][nt], a, qb[ks][nt][0], qb[ks][nt][1]);
+                else
+                  mma16816<TM>(sacc[u][nt], a, qb[ks][nt][0], qb[ks][nt][1]);
+              }
             }
           }
         } else {
@@ -901,37 +946,44 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
 #pragma unroll
             for (int nt = 0; nt < NTH; ++nt) {
               if (ks & 1)
-                mma16816<TM>(sodd[nt], a, qb[ks][nt][0], qb[ks][nt][1]);
+                mma16816<TM>(sodd[0][nt], a, qb[ks][nt][0], qb[ks][nt][1]);
               else
-                mma16816<TM>(sacc[nt], a, qb[ks][nt][0], qb[ks][nt][1]);
+                mma16816<TM>(sacc[0][nt], a, qb[ks][nt][0], qb[ks][nt][1]);
             }
           }
         }
-        // ---- online softmax per head (column) over the 16 tokens (rows) ----
-        // c0,c1: token r0, heads qc, qc+1; c2,c3: token r0 + 8, same heads
-        const bool v_lo = r0 < nt_tok, v_hi = r0 + 8 < nt_tok;
-        uint32_t pb[NTH][2];
+        // ---- online softmax per head (column) over the stage's tokens (rows) ----
+        // m-tile u: c0,c1 = token 16u + r0, heads qc, qc+1; c2,c3 = token 16u + r0 + 8
+        uint32_t pb[U][NTH][2];
         float alpha[NTH][2];
 #pragma unroll
         for (int nt = 0; nt < NTH; ++nt) {
-          float x[4];
+          float x[U][4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float v = (sacc[nt][e] + sodd[nt][e]) * p.scale_log2;
-            x[e] = (e < 2 ? v_lo : v_hi) ? v : -INFINITY;
-          }
-          float pr[4];
+          for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float v = (sacc[u][nt][e] + sodd[u][nt][e]) * p.scale_log2;
+              x[u][e] = 16 * u + r0 + (e < 2 ? 0 : 8) < nt_tok ? v : -INFINITY;
+            }
+          float pr[U][4];
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
-            float mx = fmaxf(x[cc], x[cc + 2]);
+            float mx = fmaxf(x[0][cc], x[0][cc + 2]);
+#pragma unroll
+            for (int u = 1; u < U; ++u) mx = fmaxf(mx, fmaxf(x[u][cc], x[u][cc + 2]));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
             const float m_new = fmaxf(m_run[nt][cc], mx);
-            alpha[nt][cc] = exp2f(m_run[nt][cc] - m_new);  // 0 on the first stage
-            pr[cc] = exp2f(x[cc] - m_new);
-            pr[cc + 2] = exp2f(x[cc + 2] - m_new);
-            float sum = pr[cc] + pr[cc + 2];
+            alpha[nt][cc] = fast_exp2(m_run[nt][cc] - m_new);  // 0 on the first stage
+            float sum = 0.f;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+              pr[u][cc] = fast_exp2(x[u][cc] - m_new);
+              pr[u][cc + 2] = fast_exp2(x[u][cc + 2] - m_new);
+              sum = u == 0 ? pr[u][cc] + pr[u][cc + 2] : sum + (pr[u][cc] + pr[u][cc + 2]);
+            }
             sum += __shfl_xor_sync(0xffffffffu, sum, 4);
             sum += __shfl_xor_sync(0xffffffffu, sum, 8);
             sum += __shfl_xor_sync(0xffffffffu, sum, 16);
@@ -939,8 +991,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
             m_run[nt][cc] = m_new;
           }
           // P^T as B fragments: transpose the (token x head) 8x8 blocks in registers
-          pb[nt][0] = movmatrix_t(pack2<TM>(pr[0], pr[1]));  // tokens 0-7
-          pb[nt][1] = movmatrix_t(pack2<TM>(pr[2], pr[3]));  // tokens 8-15
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            pb[u][nt][0] = movmatrix_t(pack2<TM>(pr[u][0], pr[u][1]));  // tokens 16u + 0-7
+            pb[u][nt][1] = movmatrix_t(pack2<TM>(pr[u][2], pr[u][3]));  // tokens 16u + 8-15
+          }
         }
         bool all_one = true;
 #pragma unroll
@@ -958,40 +1013,43 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         }
         // ---- O^T += V^T P^T: rows = d (16 per m-tile), k = tokens, columns = heads ----
         // (V rows past the context were zero-filled by the copy, so 0 * garbage cannot occur)
-        if (F8) {
-          // V rows (tokens) 2t, 2t+1, 2t+8, 2t+9, bytes [(D/8) r0, (D/8)(r0+1)): m-tile mt
-          // takes bytes 2 mt and 2 mt + 1 (its rows r0 and r0 + 8, see drow); a byte
-          // permute pairs the two tokens of each A register before widening
+        if constexpr (F8) {
+          // k-step u: V rows (tokens) 16u + {2t, 2t+1, 2t+8, 2t+9}, bytes [(D/8) r0,
+          // (D/8)(r0+1)): m-tile mt takes bytes 2 mt and 2 mt + 1 (its rows r0 and r0 + 8,
+          // see drow); a byte permute pairs the two tokens of each A register before widening
           constexpr int VW = D / 32;  // 32-bit words of this lane's bytes of one V row
-          uint32_t vw[4][VW];
           const int tq = lane & 3;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int row = 2 * tq + (k & 1) + 8 * (k >> 1);
-            if constexpr (VW == 4) {
-              const uint32_t addr = vb + swz8<D>(row, r0);
-              asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                           : "=r"(vw[k][0]), "=r"(vw[k][1]), "=r"(vw[k][2]), "=r"(vw[k][3])
-                           : "r"(addr));
-            } else {
-              const uint32_t addr = vb + swz8<D>(row, r0 >> 1) + 8 * (r0 & 1);
-              asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
-                           : "=r"(vw[k][0]), "=r"(vw[k][1])
-                           : "r"(addr));
+          for (int u = 0; u < U; ++u) {
+            uint32_t vw[4][VW];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int row = 16 * u + 2 * tq + (k & 1) + 8 * (k >> 1);
+              if constexpr (VW == 4) {
+                const uint32_t addr = vb + swz8<D>(row, r0);
+                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(vw[k][0]), "=r"(vw[k][1]), "=r"(vw[k][2]), "=r"(vw[k][3])
+                             : "r"(addr));
+              } else {
+                const uint32_t addr = vb + swz8<D>(row, r0 >> 1) + 8 * (r0 & 1);
+                asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
+                             : "=r"(vw[k][0]), "=r"(vw[k][1])
+                             : "r"(addr));
+              }
             }
-          }
 #pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
-            const uint32_t lo = __byte_perm(vw[0][mt >> 1], vw[1][mt >> 1], sel);  // tokens 2t, 2t+1
-            const uint32_t hi = __byte_perm(vw[2][mt >> 1], vw[3][mt >> 1], sel);  // 2t+8, 2t+9
-            uint32_t a[4];
-            a[0] = e4m3x2_f16x2(lo);
-            a[1] = e4m3x2_f16x2(lo >> 16);
-            a[2] = e4m3x2_f16x2(hi);
-            a[3] = e4m3x2_f16x2(hi >> 16);
+            for (int mt = 0; mt < MT; ++mt) {
+              const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+              const uint32_t lo = __byte_perm(vw[0][mt >> 1], vw[1][mt >> 1], sel);  // 2t, 2t+1
+              const uint32_t hi = __byte_perm(vw[2][mt >> 1], vw[3][mt >> 1], sel);  // 2t+8, 2t+9
+              uint32_t a[4];
+              a[0] = e4m3x2_f16x2(lo);
+              a[1] = e4m3x2_f16x2_hi(lo);
+              a[2] = e4m3x2_f16x2(hi);
+              a[3] = e4m3x2_f16x2_hi(hi);
 #pragma unroll
-            for (int nt = 0; nt < NTH; ++nt) mma16816<TM>(o[mt][nt], a, pb[nt][0], pb[nt][1]);
+              for (int nt = 0; nt < NTH; ++nt) mma16816<TM>(o[mt][nt], a, pb[u][nt][0], pb[u][nt][1]);
+            }
           }
         } else {
 #pragma unroll
@@ -999,7 +1057,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
             uint32_t a[4];  // V^T: d chunks 2mt / 2mt+1, tokens 0-7 / 8-15
             ldsm_x4_t(vb + swz(lrow + ((lmat >> 1) << 3), 2 * mt + (lmat & 1)), a);
 #pragma unroll
-            for (int nt = 0; nt < NTH; ++nt) mma16816<TM>(o[mt][nt], a, pb[nt][0], pb[nt][1]);
+            for (int nt = 0; nt < NTH; ++nt) mma16816<TM>(o[mt][nt], a, pb[0][nt][0], pb[0][nt][1]);
           }
         }
         if (!F8 && p.key_new && j == f.ns - 1) {

@@ -1,6 +1,7 @@
 // Internal interface between the C ABI layer (pa_api.cu) and the kernel files.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstddef>
@@ -74,6 +75,13 @@ int swap_blocks_launch(const void* src_k, const void* src_v, void* dst_k, void* 
                        const int32_t* block_mapping, int num_pairs, int src_num_blocks,
                        int dst_num_blocks, int num_kv_heads, int row_bytes, int block_size,
                        unsigned* err, cudaStream_t stream);
+
+// A cache [num_blocks][Hkv][B][d] of elem_bytes-byte values (2: fp16/bf16, 1: FP8 codes)
+// as a 4-D tensor (d, row, kv head, block) read in boxes of (128 bytes of d, B, 1, 1): the
+// 128-byte swizzle when a row is 128 bytes or more, none for 64-byte rows.  False when the
+// driver's encoder is missing or rejects the tensor.
+bool kv_cache_map(CUtensorMap* map, const void* base, int elem_bytes, int num_blocks, int hkv,
+                  int bs, int d);
 
 // Raise a kernel's dynamic shared-memory limit once per device; false on failure.
 bool ensure_smem_attr(const void* func, size_t bytes);

@@ -219,17 +219,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
-// 4-D tiled TMA load (x = d, y = row in the block, z = kv head, w = block), completion
-// counted in bytes on `bar`.  x is 0 or 64 (128-byte multiples).
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            int z, int w, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
-      : "memory");
-}
-
 template <int D, typename T>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ Params p) {
   constexpr int CH = D / 8;                  // 16-byte chunks of a 16-bit row
@@ -599,6 +588,8 @@ int launch(const Params& prm, int max_query_len, cudaStream_t stream) {
   return 0;
 }
 
+}  // namespace prefill
+
 // cuTensorMapEncodeTiled, looked up once through the runtime (no link to the driver
 // library).
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -606,7 +597,7 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-EncodeTiledFn encode_tiled() {
+static EncodeTiledFn encode_tiled() {
   static EncodeTiledFn fn = nullptr;
   if (!fn) {
     void* f = nullptr;
@@ -619,31 +610,32 @@ EncodeTiledFn encode_tiled() {
   return fn;
 }
 
-// A cache [num_blocks][Hkv][B][d] of 16-bit values as a 4-D tensor (d, row, kv head,
-// block) read in boxes of (64, B, 1, 1) with the 128-byte swizzle.
-bool cache_map(CUtensorMap* map, const void* base, int num_blocks, int hkv, int bs, int d) {
+bool kv_cache_map(CUtensorMap* map, const void* base, int elem_bytes, int num_blocks, int hkv,
+                  int bs, int d) {
   EncodeTiledFn fn = encode_tiled();
-  if (!fn) return false;
+  if (!fn || (elem_bytes != 1 && elem_bytes != 2)) return false;
+  const cuuint64_t eb = static_cast<cuuint64_t>(elem_bytes);
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(bs),
                               static_cast<cuuint64_t>(hkv), static_cast<cuuint64_t>(num_blocks)};
-  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2,
-                                 static_cast<cuuint64_t>(bs) * d * 2,
-                                 static_cast<cuuint64_t>(hkv) * bs * d * 2};
-  const cuuint32_t box[4] = {64u, static_cast<cuuint32_t>(bs), 1u, 1u};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * eb,
+                                 static_cast<cuuint64_t>(bs) * d * eb,
+                                 static_cast<cuuint64_t>(hkv) * bs * d * eb};
+  const int row_bytes = d * elem_bytes;
+  const cuuint32_t box_x = static_cast<cuuint32_t>((row_bytes < 128 ? row_bytes : 128) / elem_bytes);
+  const cuuint32_t box[4] = {box_x, static_cast<cuuint32_t>(bs), 1u, 1u};
   const cuuint32_t es[4] = {1u, 1u, 1u, 1u};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void*>(base), dims, strides, box,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  return fn(map, elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+            4, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            row_bytes >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-}  // namespace prefill
-
 int prefill_launch(const PrefillArgs& a, cudaStream_t stream) {
   prefill::Params p;
-  if (!prefill::cache_map(&p.kmap, a.k_cache, a.num_blocks, a.num_kv_heads, a.block_size,
-                          a.head_dim) ||
-      !prefill::cache_map(&p.vmap, a.v_cache, a.num_blocks, a.num_kv_heads, a.block_size,
-                          a.head_dim))
+  if (!kv_cache_map(&p.kmap, a.k_cache, 2, a.num_blocks, a.num_kv_heads, a.block_size,
+                    a.head_dim) ||
+      !kv_cache_map(&p.vmap, a.v_cache, 2, a.num_blocks, a.num_kv_heads, a.block_size,
+                    a.head_dim))
     return -3;
   p.q = static_cast<const uint8_t*>(a.q);
   p.k_cache = static_cast<const uint8_t*>(a.k_cache);
