@@ -26,6 +26,8 @@ Modules:
     sizing      -- the closed forms the pages print (block counts, bytes, capacity).
     prefill     -- causal multi-query attention of each sequence's newest tokens.
     fp8         -- FP8 (E4M3) KV blocks: the format, the quantising cache write, decode.
+    int4        -- INT4 KV blocks (codes with one scale per row): the format, the
+                   quantising cache write, decode.
 
 Every function is pinned by ``tests/test_oracle_*.py`` against something other than
 itself: values the pages print, closed forms, library special cases (NumPy float16,
