@@ -161,6 +161,61 @@ int pa_decode_append_fp8(const void* q, const void* key_new, const void* value_n
                          cudaStream_t stream);
 
 /*
+ * INT4 KV blocks (the other quantised format horeb.top, section 生态现状, names).  The
+ * pages give no INT4 format; this one is symmetric integer quantisation with one scale
+ * per cached row:
+ *   codes   [num_blocks][Hkv][B][d/2] uint8: two 4-bit codes per byte, element 2i in the
+ *           low nibble of byte i, each stored as u = c + 8 for a code c in [-7, 7];
+ *   scales  [num_blocks][Hkv][B] float32, one per (block, kv head, row), K and V apart.
+ * A row (one token of one kv head) means the values c_i * s.  All arrays 16-byte aligned,
+ * owned by the caller.
+ */
+/* Quantising cache write: for each token i with slot = slot_mapping[i] >= 0 and each kv
+ * head h, the row x = key[i, h, :] gets s = max_j |x_j| / 7 and c_j = x_j / s (both IEEE
+ * float32 divisions) rounded to nearest-even and clamped to [-7, 7] (s = 0 and c = 0 for
+ * an all-zero row); likewise value.  Inputs are finite fp16 or bf16 (`dtype`); other
+ * rules as pa_reshape_and_cache. */
+int pa_reshape_and_cache_int4(const void* key, const void* value, void* k_codes, void* v_codes,
+                              float* k_scales, float* v_scales, const int64_t* slot_mapping,
+                              int num_tokens, int num_blocks, int num_kv_heads, int head_dim,
+                              int block_size, pa_dtype dtype, cudaStream_t stream);
+/* pa_decode over INT4 blocks: z_t = scale * sK_t * <q, cK_t>, out = sum_t softmax(z)_t *
+ * sV_t * cV_t.  q and out are fp16 or bf16 (`dtype`).  The codes are widened to f16
+ * exactly and multiplied on the tensor cores in f16 (bf16 queries rounded to f16); each
+ * token's K scale multiplies its fp32 scores, and each token's V scale multiplies its
+ * softmax weight before that weight is rounded to f16 for P V (so V rows need
+ * max|v| < 7 * 65504, and rows with max|v| below about 4e-4 lose precision to f16
+ * subnormals).  Same workspace, error and determinism rules as pa_decode. */
+int pa_decode_int4(const void* q, const void* k_codes, const void* v_codes, const float* k_scales,
+                   const float* v_scales, const int32_t* block_tables, int max_blocks_per_seq,
+                   const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+                   int head_dim, int block_size, int num_blocks, float scale, void* out,
+                   void* workspace, size_t workspace_bytes, pa_dtype dtype, cudaStream_t stream);
+/* One INT4 decode step in one call: each sequence's newest token (key_new / value_new
+ * [num_seqs][Hkv][d]) quantised into position context_lens[s] - 1 through the table, with
+ * the arithmetic of pa_reshape_and_cache_int4, then pa_decode_int4 (two launches, the
+ * second a programmatic dependent of the first; a sequence whose newest slot is invalid
+ * writes nothing and the decode flags it). */
+int pa_decode_append_int4(const void* q, const void* key_new, const void* value_new,
+                          void* k_codes, void* v_codes, float* k_scales, float* v_scales,
+                          const int32_t* block_tables, int max_blocks_per_seq,
+                          const int32_t* context_lens, int num_seqs, int num_q_heads,
+                          int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                          float scale, void* out, void* workspace, size_t workspace_bytes,
+                          pa_dtype dtype, cudaStream_t stream);
+/* pa_copy_blocks for INT4 blocks: the codes and the scales of each pair (two launches). */
+int pa_copy_blocks_int4(void* k_codes, void* v_codes, float* k_scales, float* v_scales,
+                        const int32_t* block_mapping, int num_pairs, int num_blocks,
+                        int num_kv_heads, int head_dim, int block_size, cudaStream_t stream);
+/* pa_swap_blocks for INT4 blocks: codes and scales move together between two pools (one
+ * of them may be pinned host memory); the same pair rules. */
+int pa_swap_blocks_int4(const void* src_k, const void* src_v, const float* src_ks,
+                        const float* src_vs, void* dst_k, void* dst_v, float* dst_ks,
+                        float* dst_vs, const int32_t* block_mapping, int num_pairs,
+                        int src_num_blocks, int dst_num_blocks, int num_kv_heads, int head_dim,
+                        int block_size, cudaStream_t stream);
+
+/*
  * pa_prefill -- causal multi-query attention of each sequence's newest tokens over its
  * paged context (a prompt from scratch, or a chunk of one).
  *

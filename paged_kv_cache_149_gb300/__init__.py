@@ -58,6 +58,16 @@ SIGNATURES = {
                                     _vp]),
     "pa_reshape_and_cache_fp8": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
                                         _f32, _f32, _i32, _vp]),
+    "pa_reshape_and_cache_int4": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
+                                         _i32, _i32, _i32, _vp]),
+    "pa_decode_int4": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
+                              _i32, _i32, _f32, _vp, _vp, _sz, _i32, _vp]),
+    "pa_decode_append_int4": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32,
+                                     _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _sz, _i32,
+                                     _vp]),
+    "pa_copy_blocks_int4": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp]),
+    "pa_swap_blocks_int4": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
+                                   _i32, _i32, _i32, _vp]),
     "pa_prefill": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
                           _i32, _i32, _f32, _vp, _i32, _vp]),
     "pa_decode_workspace_size": (_sz, [_i32, _i32, _i32]),
@@ -406,6 +416,128 @@ def decode_fixed_scratch(q, k_cache, v_cache, block_tables, context_lens, scale,
         _dev(out, "out"), _dtype_code(q), _stream_ptr(stream, q.device))
     _check(st, "pa_decode_fixed_scratch")
     return out
+
+
+def _int4_cache(codes, scales, name):
+    import torch
+    _need(codes.dtype == torch.uint8, f"{name} codes must be uint8 (two 4-bit codes a byte)")
+    _need(scales.dtype == torch.float32, f"{name} scales must be float32")
+    _need(codes.dim() == 4 and scales.shape == codes.shape[:3],
+          f"{name}: codes [NB, Hkv, B, d/2] and scales [NB, Hkv, B]")
+    return _dev(codes, name), _dev(scales, name + " scales")
+
+
+def reshape_and_cache_int4(key, value, k_codes, v_codes, k_scales, v_scales, slot_mapping,
+                           stream=None):
+    """INT4 cache write: the row key[i, h] gets s = max|x| / 7 and codes rint(x / s) in
+    [-7, 7] at slot_mapping[i] (and V likewise)."""
+    import torch
+    n, hkv, d = key.shape
+    nb, hkv2, bs, d2 = k_codes.shape
+    _need(value.shape == key.shape and v_codes.shape == k_codes.shape, "shape mismatch")
+    _need(hkv == hkv2 and d == 2 * d2 and slot_mapping.shape == (n,), "shape mismatch")
+    _need(key.dtype == value.dtype, "dtype mismatch")
+    kc, ks = _int4_cache(k_codes, k_scales, "k")
+    vc, vs = _int4_cache(v_codes, v_scales, "v")
+    st = lib().pa_reshape_and_cache_int4(
+        _dev(key, "key"), _dev(value, "value"), kc, vc, ks, vs,
+        _dev(slot_mapping, "slot_mapping", torch.int64), n, nb, hkv, d, bs, _dtype_code(key),
+        _stream_ptr(stream, key.device))
+    _check(st, "pa_reshape_and_cache_int4")
+
+
+def decode_int4(q, k_codes, v_codes, k_scales, v_scales, block_tables, context_lens, scale,
+                out=None, workspace=None, stream=None):
+    """Paged decode over INT4 blocks (codes [NB, Hkv, B, d/2] uint8, scales [NB, Hkv, B])."""
+    import torch
+    n, hq, d = q.shape
+    nb, hkv, bs, d2 = k_codes.shape
+    _need(v_codes.shape == k_codes.shape and d == 2 * d2, "shape mismatch")
+    _need(block_tables.dim() == 2 and block_tables.shape[0] == n, "block_tables must be [num_seqs, T]")
+    _need(context_lens.shape == (n,), "context_lens must be [num_seqs]")
+    kc, ks = _int4_cache(k_codes, k_scales, "k")
+    vc, vs = _int4_cache(v_codes, v_scales, "v")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out.shape == q.shape and out.dtype == q.dtype, "out must match q")
+    if workspace is None:
+        workspace = make_workspace(hq, hkv, d, q.device)
+    st = lib().pa_decode_int4(
+        _dev(q, "q"), kc, vc, ks, vs, _dev(block_tables, "block_tables", torch.int32),
+        block_tables.shape[1], _dev(context_lens, "context_lens", torch.int32), n, hq, hkv, d, bs,
+        nb, float(scale), _dev(out, "out"), _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _dtype_code(q), _stream_ptr(stream, q.device))
+    _check(st, "pa_decode_int4")
+    return out
+
+
+def decode_append_int4(q, key_new, value_new, k_codes, v_codes, k_scales, v_scales, block_tables,
+                       context_lens, scale, out=None, workspace=None, stream=None):
+    """One INT4 decode step: each sequence's newest K/V row quantised into its slot at
+    position ctx - 1, then the decode (= reshape_and_cache_int4 + decode_int4): two launches,
+    the decode a programmatic dependent of the write."""
+    import torch
+    n, hq, d = q.shape
+    nb, hkv, bs, d2 = k_codes.shape
+    _need(v_codes.shape == k_codes.shape and d == 2 * d2, "shape mismatch")
+    _need(key_new.shape == (n, hkv, d) and value_new.shape == key_new.shape, "key_new must be [n, Hkv, d]")
+    _need(key_new.dtype == value_new.dtype == q.dtype, "dtype mismatch")
+    _need(block_tables.dim() == 2 and block_tables.shape[0] == n, "block_tables must be [num_seqs, T]")
+    _need(context_lens.shape == (n,), "context_lens must be [num_seqs]")
+    kc, ks = _int4_cache(k_codes, k_scales, "k")
+    vc, vs = _int4_cache(v_codes, v_scales, "v")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out.shape == q.shape and out.dtype == q.dtype, "out must match q")
+    if workspace is None:
+        workspace = make_workspace(hq, hkv, d, q.device)
+    st = lib().pa_decode_append_int4(
+        _dev(q, "q"), _dev(key_new, "key_new"), _dev(value_new, "value_new"), kc, vc, ks, vs,
+        _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+        _dev(context_lens, "context_lens", torch.int32), n, hq, hkv, d, bs, nb, float(scale),
+        _dev(out, "out"), _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _dtype_code(q), _stream_ptr(stream, q.device))
+    _check(st, "pa_decode_append_int4")
+    return out
+
+
+def copy_blocks_int4(k_codes, v_codes, k_scales, v_scales, block_mapping, stream=None):
+    """copy_blocks for INT4 blocks: codes and scales of each (src, dst) pair."""
+    import torch
+    nb, hkv, bs, d2 = k_codes.shape
+    _need(v_codes.shape == k_codes.shape, "shape mismatch")
+    _need(block_mapping.dim() == 2 and block_mapping.shape[1] == 2, "block_mapping must be [n, 2]")
+    kc, ks = _int4_cache(k_codes, k_scales, "k")
+    vc, vs = _int4_cache(v_codes, v_scales, "v")
+    st = lib().pa_copy_blocks_int4(kc, vc, ks, vs, _dev(block_mapping, "block_mapping", torch.int32),
+                                   block_mapping.shape[0], nb, hkv, 2 * d2, bs,
+                                   _stream_ptr(stream, k_codes.device))
+    _check(st, "pa_copy_blocks_int4")
+
+
+def swap_blocks_int4(src, dst, block_mapping, stream=None, device=None):
+    """swap_blocks for INT4 blocks; src and dst are (k_codes, v_codes, k_scales, v_scales)
+    pools, CUDA tensors or pinned CPU tensors."""
+    import torch
+    nbs, hkv, bs, d2 = src[0].shape
+    nbd = dst[0].shape[0]
+    _need(all(t.shape == src[0].shape for t in src[:2]) and all(t.shape == dst[0].shape for t in dst[:2]),
+          "shape mismatch")
+    _need(dst[0].shape[1:] == src[0].shape[1:], "pools must share Hkv, B, d")
+    _need(all(t.dtype == torch.uint8 for t in (src[0], src[1], dst[0], dst[1])) and
+          all(t.dtype == torch.float32 and t.shape == c.shape[:3]
+              for t, c in ((src[2], src[0]), (src[3], src[0]), (dst[2], dst[0]), (dst[3], dst[0]))),
+          "codes uint8 [NB, Hkv, B, d/2], scales float32 [NB, Hkv, B]")
+    _need(block_mapping.dim() == 2 and block_mapping.shape[1] == 2, "block_mapping must be [n, 2]")
+    if device is None:
+        device = next((t.device for t in (src[0], dst[0]) if t.is_cuda), torch.device("cuda"))
+    names = ("k", "v", "k scales", "v scales")
+    st = lib().pa_swap_blocks_int4(
+        *[_reachable(t, "src " + nm) for t, nm in zip(src, names)],
+        *[_reachable(t, "dst " + nm) for t, nm in zip(dst, names)],
+        _reachable(block_mapping, "block_mapping", torch.int32), block_mapping.shape[0], nbs, nbd,
+        hkv, 2 * d2, bs, _stream_ptr(stream, device))
+    _check(st, "pa_swap_blocks_int4")
 
 
 def copy_blocks(k_cache, v_cache, block_mapping, stream=None):

@@ -140,7 +140,11 @@ int decode_call(const void* q, const void* key_new, const void* value_new, const
                 const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
                 int head_dim, int block_size, int num_blocks, float scale, void* out,
                 void* workspace, size_t workspace_bytes, pa_dtype dtype, cudaStream_t stream,
-                bool kv_fp8 = false, float k_scale = 1.f, float v_scale = 1.f) {
+                bool kv_fp8 = false, float k_scale = 1.f, float v_scale = 1.f,
+                const float* k_scales = nullptr, const float* v_scales = nullptr) {
+  const bool kv_int4 = k_scales != nullptr || v_scales != nullptr;
+  if (kv_int4 && (!k_scales || !v_scales || !aligned16(k_scales) || !aligned16(v_scales)))
+    return PA_ERR_ARG;
   if (kv_fp8 && (!std::isfinite(k_scale) || !std::isfinite(v_scale) || !(k_scale > 0.f) ||
                  !(v_scale > 0.f)))
     return PA_ERR_ARG;
@@ -184,6 +188,9 @@ int decode_call(const void* q, const void* key_new, const void* value_new, const
   a.kv_fp8 = kv_fp8;
   a.k_scale = k_scale;
   a.v_scale = v_scale;
+  a.kv_int4 = kv_int4;
+  a.k_scales = k_scales;
+  a.v_scales = v_scales;
   a.err = di.err;
   return pa::decode_launch(a, di.sm_count, stream);
 }
@@ -269,6 +276,115 @@ int pa_reshape_and_cache_fp8(const void* key, const void* value, void* k_cache, 
   return pa::reshape_and_cache_fp8_launch(key, value, k_cache, v_cache, slot_mapping, num_tokens,
                                           num_blocks, num_kv_heads, head_dim, block_size, k_scale,
                                           v_scale, dtype == PA_BF16, di.err, stream);
+}
+
+// ---- INT4 K/V blocks: codes [NB][Hkv][B][d/2] (two per byte) + float32 scales [NB][Hkv][B] ----
+
+namespace {
+bool int4_arrays_ok(const void* kc, const void* vc, const void* ks, const void* vs) {
+  return kc && vc && ks && vs && aligned16(kc) && aligned16(vc) && aligned16(ks) && aligned16(vs);
+}
+}  // namespace
+
+int pa_reshape_and_cache_int4(const void* key, const void* value, void* k_codes, void* v_codes,
+                              float* k_scales, float* v_scales, const int64_t* slot_mapping,
+                              int num_tokens, int num_blocks, int num_kv_heads, int head_dim,
+                              int block_size, pa_dtype dtype, cudaStream_t stream) {
+  if (num_tokens < 0 || num_blocks < 1 || !shape_ok(num_kv_heads, head_dim, block_size) ||
+      (dtype != PA_FP16 && dtype != PA_BF16))
+    return PA_ERR_ARG;
+  if (num_tokens == 0) return PA_OK;
+  if (!key || !value || !slot_mapping || !aligned16(key) || !aligned16(value) ||
+      !int4_arrays_ok(k_codes, v_codes, k_scales, v_scales))
+    return PA_ERR_ARG;
+  DeviceInfo di;
+  if (!device_info(&di)) return PA_ERR_CUDA;
+  return pa::cache_int4_launch(key, value, k_codes, v_codes, k_scales, v_scales, slot_mapping,
+                               nullptr, 0, nullptr, num_tokens, num_blocks, num_kv_heads, head_dim,
+                               block_size, dtype == PA_BF16, di.err, stream);
+}
+
+int pa_decode_int4(const void* q, const void* k_codes, const void* v_codes, const float* k_scales,
+                   const float* v_scales, const int32_t* block_tables, int max_blocks_per_seq,
+                   const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+                   int head_dim, int block_size, int num_blocks, float scale, void* out,
+                   void* workspace, size_t workspace_bytes, pa_dtype dtype, cudaStream_t stream) {
+  if (num_seqs > 0 && (!k_scales || !v_scales)) return PA_ERR_ARG;
+  return decode_call(q, nullptr, nullptr, k_codes, v_codes, block_tables, max_blocks_per_seq,
+                     context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                     num_blocks, scale, out, workspace, workspace_bytes, dtype, stream, false, 1.f,
+                     1.f, k_scales, v_scales);
+}
+
+int pa_decode_append_int4(const void* q, const void* key_new, const void* value_new,
+                          void* k_codes, void* v_codes, float* k_scales, float* v_scales,
+                          const int32_t* block_tables, int max_blocks_per_seq,
+                          const int32_t* context_lens, int num_seqs, int num_q_heads,
+                          int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                          float scale, void* out, void* workspace, size_t workspace_bytes,
+                          pa_dtype dtype, cudaStream_t stream) {
+  if (num_seqs < 0) return PA_ERR_ARG;
+  if (num_seqs == 0) return PA_OK;
+  if (!key_new || !value_new || !context_lens || !block_tables || num_blocks < 1 ||
+      max_blocks_per_seq < 1 || !shape_ok(num_kv_heads, head_dim, block_size) ||
+      (dtype != PA_FP16 && dtype != PA_BF16) || !aligned16(key_new) || !aligned16(value_new) ||
+      !int4_arrays_ok(k_codes, v_codes, k_scales, v_scales))
+    return PA_ERR_ARG;
+  // the newest rows first (their slots are read from the table on the device), then decode
+  const int st = pa::cache_int4_launch(key_new, value_new, k_codes, v_codes, k_scales, v_scales,
+                                       nullptr, block_tables, max_blocks_per_seq, context_lens,
+                                       num_seqs, num_blocks, num_kv_heads, head_dim, block_size,
+                                       dtype == PA_BF16, nullptr, stream);
+  if (st != 0) return PA_ERR_CUDA;
+  return decode_call(q, nullptr, nullptr, k_codes, v_codes, block_tables, max_blocks_per_seq,
+                     context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                     num_blocks, scale, out, workspace, workspace_bytes, dtype, stream, false, 1.f,
+                     1.f, k_scales, v_scales);
+}
+
+int pa_copy_blocks_int4(void* k_codes, void* v_codes, float* k_scales, float* v_scales,
+                        const int32_t* block_mapping, int num_pairs, int num_blocks,
+                        int num_kv_heads, int head_dim, int block_size, cudaStream_t stream) {
+  if (num_pairs < 0 || num_blocks < 1 || !shape_ok(num_kv_heads, head_dim, block_size))
+    return PA_ERR_ARG;
+  if (num_pairs == 0) return PA_OK;
+  if (!block_mapping || !int4_arrays_ok(k_codes, v_codes, k_scales, v_scales)) return PA_ERR_ARG;
+  DeviceInfo di;
+  if (!device_info(&di)) return PA_ERR_CUDA;
+  int st = pa::copy_blocks_launch(k_codes, v_codes, block_mapping, num_pairs, num_blocks,
+                                  num_kv_heads, head_dim / 2, block_size, di.err, stream);
+  if (st != 0) return PA_ERR_CUDA;
+  st = pa::copy_blocks_launch(k_scales, v_scales, block_mapping, num_pairs, num_blocks,
+                              num_kv_heads, 4, block_size, di.err, stream);
+  return st == 0 ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_swap_blocks_int4(const void* src_k, const void* src_v, const float* src_ks,
+                        const float* src_vs, void* dst_k, void* dst_v, float* dst_ks,
+                        float* dst_vs, const int32_t* block_mapping, int num_pairs,
+                        int src_num_blocks, int dst_num_blocks, int num_kv_heads, int head_dim,
+                        int block_size, cudaStream_t stream) {
+  if (num_pairs < 0 || src_num_blocks < 1 || dst_num_blocks < 1 ||
+      !shape_ok(num_kv_heads, head_dim, block_size))
+    return PA_ERR_ARG;
+  if (num_pairs == 0) return PA_OK;
+  const void* ptrs[9] = {src_k, src_v, src_ks, src_vs, dst_k, dst_v, dst_ks, dst_vs, block_mapping};
+  void* dev[9];
+  for (int i = 0; i < 9; ++i) {
+    dev[i] = device_view(ptrs[i]);
+    if (!dev[i]) return PA_ERR_ARG;
+    if (i < 8 && !aligned16(dev[i])) return PA_ERR_ARG;
+  }
+  DeviceInfo di;
+  if (!device_info(&di)) return PA_ERR_CUDA;
+  const auto* map = static_cast<const int32_t*>(dev[8]);
+  int st = pa::swap_blocks_launch(dev[0], dev[1], dev[4], dev[5], map, num_pairs, src_num_blocks,
+                                  dst_num_blocks, num_kv_heads, head_dim / 2, block_size, di.err,
+                                  stream);
+  if (st != 0) return PA_ERR_CUDA;
+  st = pa::swap_blocks_launch(dev[2], dev[3], dev[6], dev[7], map, num_pairs, src_num_blocks,
+                              dst_num_blocks, num_kv_heads, 4, block_size, di.err, stream);
+  return st == 0 ? PA_OK : PA_ERR_CUDA;
 }
 
 int pa_prefill(const void* q, const void* k_cache, const void* v_cache,

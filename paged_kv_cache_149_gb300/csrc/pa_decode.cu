@@ -68,11 +68,15 @@ int decode_launch(const DecodeArgs& a, int grid, cudaStream_t stream) {
   p.log2_block = a.block_size == 8 ? 3 : (a.block_size == 16 ? 4 : 5);
   p.num_blocks = a.num_blocks;
   p.max_ctx = a.max_blocks_per_seq * a.block_size;
-  p.log2_stage = a.kv_fp8 ? 5 : 4;  // 32-token stages over FP8 blocks, 16 over 16-bit ones
+  const bool quantised = a.kv_fp8 || a.kv_int4;
+  p.log2_stage = quantised ? 5 : 4;  // 32-token stages over quantised blocks, 16 over 16-bit ones
   p.seg_cost = decode::kSegCost >> (p.log2_stage - 4);  // the same charge in tokens
   // FP8 blocks: scores are k_scale * <q, codes>, outputs v_scale * (weighted codes)
   p.scale_log2 = a.scale * (a.kv_fp8 ? a.k_scale : 1.f) * decode::kLog2e;
   p.out_scale = a.kv_fp8 ? a.v_scale : 1.f;
+  // INT4 blocks: a scale per row, applied in the kernel
+  p.k_scales = static_cast<const float*>(a.k_scales);
+  p.v_scales = static_cast<const float*>(a.v_scales);
   p.err = a.err;
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
@@ -85,10 +89,11 @@ int decode_launch(const DecodeArgs& a, int grid, cudaStream_t stream) {
 
   // heads of a pair are MMA columns: one n-tile of 8, or two for up to 16
   if (a.kv_fp8) return decode_launch_fp8(p, grid, a.head_dim, a.bf16, stream);
+  if (a.kv_int4) return decode_launch_int4(p, grid, a.head_dim, a.bf16, stream);
 #define PA_DECODE_CASE(DD, NN)                                                           \
   if (a.head_dim == DD && (p.heads_per_pair > 8) == (NN == 2))                           \
-    return a.bf16 ? decode::launch<DD, NN, __nv_bfloat16, false>(p, grid, stream) \
-                  : decode::launch<DD, NN, __half, false>(p, grid, stream);
+    return a.bf16 ? decode::launch<DD, NN, __nv_bfloat16, decode::kKv16>(p, grid, stream) \
+                  : decode::launch<DD, NN, __half, decode::kKv16>(p, grid, stream);
   PA_DECODE_CASE(128, 1)
   PA_DECODE_CASE(128, 2)
   PA_DECODE_CASE(64, 1)

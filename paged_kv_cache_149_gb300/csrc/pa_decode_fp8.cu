@@ -6,10 +6,10 @@ namespace pa {
 
 int decode_launch_fp8(const decode::Params& p, int grid, int head_dim, bool bf16,
                       cudaStream_t stream) {
-#define PA_DECODE_FP8_CASE(DD, NN)                                                 \
-  if (head_dim == DD && (p.heads_per_pair > 8) == (NN == 2))                       \
-    return bf16 ? decode::launch<DD, NN, __nv_bfloat16, true>(p, grid, stream)     \
-                : decode::launch<DD, NN, __half, true>(p, grid, stream);
+#define PA_DECODE_FP8_CASE(DD, NN)                                                       \
+  if (head_dim == DD && (p.heads_per_pair > 8) == (NN == 2))                            \
+    return bf16 ? decode::launch<DD, NN, __nv_bfloat16, decode::kKvFp8>(p, grid, stream) \
+                : decode::launch<DD, NN, __half, decode::kKvFp8>(p, grid, stream);
   PA_DECODE_FP8_CASE(128, 1)
   PA_DECODE_FP8_CASE(128, 2)
   PA_DECODE_FP8_CASE(64, 1)

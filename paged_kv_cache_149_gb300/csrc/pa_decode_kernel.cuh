@@ -69,18 +69,23 @@ constexpr float kLog2e = 1.4426950408889634f;
 // 64: 58.4 us on 64 sequences of 128..2048 tokens; 16 x 8192 tokens: 102.9 / 96.5 / 93.9).
 constexpr int kSegCost = 32;
 
-// EB: bytes per cached K/V element (2 for fp16/bf16 blocks, 1 for FP8 E4M3 blocks).  A
-// stage of FP8 blocks holds 32 tokens (the bytes of 16 tokens of a 16-bit cache), so the
-// per-stage work that does not scale with bytes (softmax reductions, bookkeeping) is paid
-// once per 32 tokens.
-template <int D, int EB = 2>
+// Cached K/V formats: 16-bit values, FP8 (E4M3) codes with one scale per cache, INT4
+// codes (two per byte) with one float32 scale per row.
+constexpr int kKv16 = 0;
+constexpr int kKvFp8 = 1;
+constexpr int kKvInt4 = 2;
+
+// A stage of quantised blocks holds 32 tokens, so the per-stage work that does not scale
+// with bytes (softmax reductions, bookkeeping) is paid once per 32 tokens.  INT4 stages
+// carry the rows' scales after the codes (K scales, then V scales).
+template <int D, int KV = kKv16>
 struct Geo {
-  static constexpr int kTok = EB == 1 ? 2 * kStageTok : kStageTok;  // tokens per stage
-  static constexpr int kLog2Tok = EB == 1 ? 5 : 4;
-  static constexpr int kRowBytes = D * EB;
+  static constexpr int kTok = KV == kKv16 ? kStageTok : 2 * kStageTok;  // tokens per stage
+  static constexpr int kRowBytes = KV == kKv16 ? 2 * D : (KV == kKvFp8 ? D : D / 2);
   static constexpr int kRowChunks = kRowBytes / 16;         // 16-byte chunks per row
   static constexpr int kKBytes = kTok * kRowBytes;          // K rows of a stage
-  static constexpr int kStageBytes = 2 * kKBytes;           // K then V
+  static constexpr int kScaleBytes = KV == kKvInt4 ? 4 * kTok : 0;  // K (or V) row scales
+  static constexpr int kStageBytes = 2 * kKBytes + 2 * kScaleBytes;  // K, V, K scales, V scales
   // Ring slots per warp (192 KB in all, at most 32) and how many stages ahead a warp loads.
   static constexpr int kSlots0 = (192 * 1024) / (kStageBytes * kWarps);
   static constexpr int kSlots = kSlots0 > 32 ? 32 : kSlots0;
@@ -108,7 +113,10 @@ struct Params {
   int log2_stage;  // tokens per stage: 16 (16-bit blocks) or 32 (FP8 blocks)
   int seg_cost;    // stage units charged per family on top of its stages
   float scale_log2;
-  float out_scale;  // FP8 blocks: v_scale, applied to every output row (else unused)
+  float out_scale;  // FP8 blocks: v_scale, applied to every output row (else 1)
+  // INT4 blocks: float32 scale of each cached row, [num_blocks][Hkv][B] (else null)
+  const float* k_scales;
+  const float* v_scales;
   // [grid][gs]: arrivals at cut pair (first CTA, pi): epoch tag << 24 | pieces counted in
   unsigned long long* counters;
   unsigned long long epoch;  // 40-bit tag, different from the previous call's
@@ -324,11 +332,11 @@ __device__ __forceinline__ uint32_t swz8(int row, int chunk) {
 }
 
 // Row of O^T held in MMA accumulator row r (0..15) of m-tile mt.  16-bit blocks: d = 16 mt
-// + r.  FP8 blocks permute d so that every lane builds its V fragments from contiguous
-// bytes: rows r and r + 8 are the adjacent d = (D/8)(r % 8) + 2 mt and that + 1.
-template <int D, bool F8>
+// + r.  Quantised blocks (QK) permute d so that every lane builds its V fragments from
+// contiguous bytes: rows r and r + 8 are the adjacent d = (D/8)(r % 8) + 2 mt and that + 1.
+template <int D, bool QK>
 __device__ __forceinline__ int drow(int mt, int r) {
-  return F8 ? (r & 7) * (D / 8) + 2 * mt + (r >> 3) : 16 * mt + r;
+  return QK ? (r & 7) * (D / 8) + 2 * mt + (r >> 3) : 16 * mt + r;
 }
 
 // Two E4M3 values (low byte first) -> f16x2, exact (every E4M3 value is an f16 normal):
@@ -346,6 +354,39 @@ __device__ __forceinline__ uint32_t e4m3x2_f16x2_hi(uint32_t w) {
       : "=r"(r)
       : "r"(w));
   return r;
+}
+
+// INT4 stages: a row is D / 2 bytes.  At D = 128 row r is stored in row slot
+// r ^ ((r >> 1) & 1): the K fragment loads (eight consecutive rows) still read 512
+// contiguous bytes, and the V fragment loads (rows c, c + 2, c + 4, c + 6) fall two into
+// each half of the banks.  At D = 64 rows are packed as they come.
+template <int D>
+__device__ __forceinline__ uint32_t swz4(int row, int chunk) {
+  return D == 128 ? static_cast<uint32_t>(64 * (row ^ ((row >> 1) & 1)) + 16 * chunk)
+                  : static_cast<uint32_t>(32 * row + 16 * chunk);
+}
+
+// INT4 nibbles -> f16x2, exact.  The nibble u (= code + 8) at bits 0-3 and 16-19 of w
+// (i4x2_lo) or at bits 4-7 and 20-23 (i4x2_hi) is placed in the mantissa of 1024.0
+// (0x6400): 1024 + u, or 1024 + 16 u; subtracting 1032, or scaling by 1/16 and adding
+// -72, leaves u - 8 exactly.
+__device__ __forceinline__ uint32_t i4x2_lo(uint32_t w) {
+  const uint32_t x = (w & 0x000F000Fu) | 0x64006400u;
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(0x64086408u));
+  return r;
+}
+__device__ __forceinline__ uint32_t i4x2_hi(uint32_t w) {
+  const uint32_t x = (w & 0x00F000F0u) | 0x64006400u;
+  uint32_t r;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(x), "r"(0x2C002C00u), "r"(0xD480D480u));
+  return r;
+}
+
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
 }
 
 // 2^x on the SFU (ex2.approx, subnormal results flushed to zero; 2^-inf = 0).  The
@@ -401,7 +442,7 @@ __device__ __forceinline__ int arrive(unsigned long long* ctr, unsigned long lon
 // (the log-sum-exp rescaling of online softmax); zeros when a piece saw a bad block.
 // merge_staged computes the same sums in the same order with the same fused multiply-adds,
 // so a pair's output does not depend on which of the two merges it.
-template <int D, typename T, bool F8>
+template <int D, typename T, bool QK>
 __device__ void merge_pieces(const Params& p, int pi, int c, int first_slot, int c_last, int nh,
                              T* out_rows, int gt, int gthreads) {
   constexpr int C4 = D / 4;  // 4-float chunks per head row
@@ -435,7 +476,7 @@ __device__ void merge_pieces(const Params& p, int pi, int c, int first_slot, int
     }
     uint2 packed = make_uint2(0u, 0u);
     if (!bad) {
-      const float inv = F8 ? p.out_scale / L : 1.f / L;
+      const float inv = QK ? p.out_scale / L : 1.f / L;
       packed.x = pack2<T>(O.x * inv, O.y * inv);
       packed.y = pack2<T>(O.z * inv, O.w * inv);
     }
@@ -462,7 +503,7 @@ __device__ __forceinline__ bool mbar_wait_once(uint32_t bar) { return mbar_wait_
 // pieces are folded in CTA order: M = max m_i, w_i = 2^(m_i - M), L = sum l_i w_i,
 // out = sum w_i acc_i / L.  Returns false, having done nothing, when the pieces do not fit
 // in the ring.
-template <int D, typename T, bool F8>
+template <int D, typename T, bool QK>
 __device__ bool merge_staged(const Params& p, int pi, const CutPiece& job0, const CutPiece& job1,
                              int njobs, uint32_t ring, uint8_t* ring_ptr, int ring_bytes,
                              uint32_t bar, int lane) {
@@ -568,7 +609,7 @@ __device__ bool merge_staged(const Params& p, int pi, const CutPiece& job0, cons
       const float L = ml[moff + h].y;
       uint2 packed = make_uint2(0u, 0u);
       if (L >= 0.f) {
-        const float inv = F8 ? p.out_scale / L : 1.f / L;
+        const float inv = QK ? p.out_scale / L : 1.f / L;
         packed.x = pack2<T>(O.x * inv, O.y * inv);
         packed.y = pack2<T>(O.z * inv, O.w * inv);
       }
@@ -580,9 +621,9 @@ __device__ bool merge_staged(const Params& p, int pi, const CutPiece& job0, cons
   return true;
 }
 
-template <int D, int EB>
+template <int D, int KV>
 struct Smem {
-  uint8_t ring[kWarps][Geo<D, EB>::kSlots][Geo<D, EB>::kStageBytes];  // 1024-byte aligned
+  uint8_t ring[kWarps][Geo<D, KV>::kSlots][Geo<D, KV>::kStageBytes];  // 1024-byte aligned
   float xo[kWarps][4][D];  // per-warp O rows, 4 heads per exchange round
   float xm[kWarps][kMaxHeads], xl[kWarps][kMaxHeads];
   long long scan[kWarps];
@@ -641,6 +682,32 @@ __device__ __forceinline__ void load_q8(const Params& p, int s, int h0, int nh, 
   }
 }
 
+// Q^T for INT4 blocks, as f16, in the d order the K fragments use: k-steps 2j and 2j + 1
+// take the eight d = (D/4) t + 8 j + {0..7} of word j of a K row, k-step 2j + e getting
+// d + 2e and d + 2e + 4 in b0 and d + 2e + 1 and d + 2e + 5 in b1 (t = lane % 4).
+template <int D, int NTH, typename T>
+__device__ __forceinline__ void load_q4(const Params& p, int s, int h0, int nh, int lane,
+                                        uint32_t (&qb)[D / 16][NTH][2]) {
+  const int r0 = lane >> 2, t = lane & 3;
+  const uint4* qrow = reinterpret_cast<const uint4*>(
+      p.q + (static_cast<size_t>(s) * p.num_q_heads + h0) * D * 2);
+#pragma unroll
+  for (int nt = 0; nt < NTH; ++nt) {
+    const int h = nt * 8 + r0;
+    const bool hv = h < nh;
+#pragma unroll
+    for (int j = 0; j < D / 32; ++j) {
+      const uint4 w = hv ? __ldg(qrow + (h * D + (D / 4) * t + 8 * j) / 8) : make_uint4(0u, 0u, 0u, 0u);
+      const float2 a = unpack2<T>(w.x), b = unpack2<T>(w.y), c = unpack2<T>(w.z),
+                   d = unpack2<T>(w.w);  // d + 0,1 / 2,3 / 4,5 / 6,7
+      qb[2 * j][nt][0] = pack2<__half>(a.x, c.x);
+      qb[2 * j][nt][1] = pack2<__half>(a.y, c.y);
+      qb[2 * j + 1][nt][0] = pack2<__half>(b.x, d.x);
+      qb[2 * j + 1][nt][1] = pack2<__half>(b.y, d.y);
+    }
+  }
+}
+
 // The next family (after f) where pair pi has units to compute; false at the share's end.
 __device__ __forceinline__ bool next_busy_fam(Fam f, int pi, long long w0, long long w1,
                                               const Params& p, Fam& out) {
@@ -655,14 +722,18 @@ __device__ __forceinline__ bool next_busy_fam(Fam f, int pi, long long w0, long 
   }
 }
 
-// F8: K/V blocks hold E4M3 codes (scales folded into scale_log2 and out_scale); the MMAs
-// then run in f16 on the widened values.  The fused cache write (key_new) exists for
-// 16-bit blocks only.
-template <int D, int NTH, typename T, bool F8>
+// KV = kKvFp8: K/V blocks hold E4M3 codes (scales folded into scale_log2 and out_scale).
+// KV = kKvInt4: K/V blocks hold INT4 codes with a float32 scale per row: a token's K scale
+// multiplies its scores, its V scale its weights in P V.  Both quantised formats run the
+// MMAs in f16 on values widened exactly, with 32-token stages and the permuted d order of
+// O (drow).  The fused cache write (key_new) exists for 16-bit blocks only.
+template <int D, int NTH, typename T, int KV>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ Params p) {
-  constexpr int EB = F8 ? 1 : 2;
-  using G_ = Geo<D, EB>;
-  using TM = typename std::conditional<F8, __half, T>::type;  // MMA operand type
+  constexpr bool F8 = KV == kKvFp8;
+  constexpr bool I4 = KV == kKvInt4;
+  constexpr bool QK = KV != kKv16;  // quantised blocks
+  using G_ = Geo<D, KV>;
+  using TM = typename std::conditional<QK, __half, T>::type;  // MMA operand type
   constexpr int R = G_::kSlots;
   constexpr int KS = G_::kKSteps;
   constexpr int ST = G_::kTok;  // tokens per stage
@@ -670,7 +741,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   constexpr int MT = D / 16;  // m-tiles of O^T (16 rows of d each)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
-  Smem<D, EB>& sm = *reinterpret_cast<Smem<D, EB>*>(smem_raw + (((raw_addr + 1023) & ~1023u) - raw_addr));
+  Smem<D, KV>& sm = *reinterpret_cast<Smem<D, KV>*>(smem_raw + (((raw_addr + 1023) & ~1023u) - raw_addr));
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -794,8 +865,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
           // rows past the context: zero-filled, nothing read (the source stays in block e[0])
           const size_t grow = !live ? rbase[0] : rb + (r & (p.block_size - 1));
           const size_t src = grow * G_::kRowBytes + ch * 16;
-          const uint32_t so = F8 ? swz8<D>(row, ch) : swz(row, ch);
-          if (!F8 && p.key_new && nxt.last && row == nxt.nt - 1) {
+          const uint32_t so = I4 ? swz4<D>(row, ch) : (F8 ? swz8<D>(row, ch) : swz(row, ch));
+          if (!QK && p.key_new && nxt.last && row == nxt.nt - 1) {
             // the newest token: from the step's input (the cache row is written later)
             const size_t nsrc = ((static_cast<size_t>(nxt.s) * p.num_kv_heads + nxt.kvh) * D + ch * 8) * 2;
             cp_async16(dst + so, p.key_new + nsrc, 16u);
@@ -803,6 +874,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
           } else {
             cp_async16(dst + so, p.k_cache + src, live ? 16u : 0u);
             cp_async16(dst + G_::kKBytes + so, p.v_cache + src, live ? 16u : 0u);
+          }
+        }
+        if constexpr (I4) {
+          // the rows' scales: lanes 0-7 copy K's, 8-15 V's, four tokens (16 bytes) each; a
+          // token past the context gets scale 0 (its codes are zero-filled too)
+          constexpr int SC = G_::kTok / 4;  // 16-byte chunks of one stage's K scales
+          if (lane < 2 * SC) {
+            const int cc = lane % SC;
+            const int r = row0 + 4 * cc;
+            const int kk = r >> p.log2_block;
+            size_t rb = rbase[0];
+#pragma unroll
+            for (int k = 1; k < NE; ++k) rb = kk == k ? rbase[k] : rb;
+            const int live = max(0, min(4, nxt.nt - 4 * cc));
+            const size_t srow = live ? rb + (r & (p.block_size - 1)) : rbase[0];
+            const float* sbase = lane < SC ? p.k_scales : p.v_scales;
+            cp_async16(dst + 2 * G_::kKBytes + (lane < SC ? 0 : G_::kScaleBytes) + 16 * cc,
+                       sbase + srow, 4u * live);
           }
         }
       }
@@ -830,7 +919,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     else have = next_busy_fam(first, pi, w0, w1, p, qf);
     if (have) {
       const PairHeads ph = pair_heads(p, qf.g * p.gs + pi);
-      if (F8) load_q8<D, NTH, T>(p, qf.s, ph.h0, ph.nh, lane, qn);
+      if (I4) load_q4<D, NTH, T>(p, qf.s, ph.h0, ph.nh, lane, qn);
+      else if (F8) load_q8<D, NTH, T>(p, qf.s, ph.h0, ph.nh, lane, qn);
       else load_q<D, NTH>(p, qf.s, ph.h0, ph.nh, lane, qn);
     }
   }
@@ -868,7 +958,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       Fam qf;
       if (next_busy_fam(f, pi, w0, w1, p, qf)) {
         const PairHeads lh = pair_heads(p, qf.g * p.gs + pi);
-        if (F8) load_q8<D, NTH, T>(p, qf.s, lh.h0, lh.nh, lane, qn);
+        if (I4) load_q4<D, NTH, T>(p, qf.s, lh.h0, lh.nh, lane, qn);
+        else if (F8) load_q8<D, NTH, T>(p, qf.s, lh.h0, lh.nh, lane, qn);
         else load_q<D, NTH>(p, qf.s, lh.h0, lh.nh, lane, qn);
       }
     }
@@ -906,7 +997,62 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
           for (int nt = 0; nt < NTH; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) sacc[u][nt][e] = sodd[u][nt][e] = 0.f;
-        if constexpr (F8) {
+        // INT4: the K and V scales of this lane's rows 16u + r0 and 16u + r0 + 8
+        float ksc[U][2], vsc[U][2];
+        if constexpr (I4) {
+#pragma unroll
+          for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+              const uint32_t sa = kb + 2 * G_::kKBytes + 4 * (16 * u + r0 + 8 * hr);
+              ksc[u][hr] = lds_f32(sa);
+              vsc[u][hr] = lds_f32(sa + G_::kScaleBytes);
+            }
+        }
+        if constexpr (I4) {
+          // K rows 16u + r0 and + 8, bytes [(D/8) t, (D/8)(t+1)): word j holds the eight d
+          // of k-steps 2j and 2j + 1 (the order load_q4 gives q)
+          constexpr int KW = D / 32;
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            uint32_t kw[2][KW];
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+              const int row = 16 * u + r0 + 8 * hr;
+              if constexpr (KW == 4) {
+                const uint32_t addr = kb + swz4<D>(row, lane & 3);
+                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(kw[hr][0]), "=r"(kw[hr][1]), "=r"(kw[hr][2]), "=r"(kw[hr][3])
+                             : "r"(addr));
+              } else {
+                const uint32_t addr = kb + swz4<D>(row, (lane & 3) >> 1) + 8 * (lane & 1);
+                asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
+                             : "=r"(kw[hr][0]), "=r"(kw[hr][1])
+                             : "r"(addr));
+              }
+            }
+#pragma unroll
+            for (int jw = 0; jw < KW; ++jw)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const uint32_t w0 = e ? kw[0][jw] >> 8 : kw[0][jw];
+                const uint32_t w1 = e ? kw[1][jw] >> 8 : kw[1][jw];
+                uint32_t a[4];
+                a[0] = i4x2_lo(w0);
+                a[1] = i4x2_lo(w1);
+                a[2] = i4x2_hi(w0);
+                a[3] = i4x2_hi(w1);
+                const int ks = 2 * jw + e;
+#pragma unroll
+                for (int nt = 0; nt < NTH; ++nt) {
+                  if (ks & 1)
+                    mma16816<TM>(sodd[u][nt], a, qb[ks][nt][0], qb[ks][nt][1]);
+                  else
+                    mma16816<TM>(sacc[u][nt], a, qb[ks][nt][0], qb[ks][nt][1]);
+                }
+              }
+          }
+        } else if constexpr (F8) {
           // K rows 16u + r0 and + 8, bytes [(D/4) t, (D/4)(t+1)): word ks of a row holds the
           // four d of k-step ks (the order load_q8 gives q)
 #pragma unroll
@@ -963,7 +1109,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
           for (int u = 0; u < U; ++u)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float v = (sacc[u][nt][e] + sodd[u][nt][e]) * p.scale_log2;
+              const float v = (sacc[u][nt][e] + sodd[u][nt][e]) *
+                              (I4 ? ksc[u][e >> 1] * p.scale_log2 : p.scale_log2);
               x[u][e] = 16 * u + r0 + (e < 2 ? 0 : 8) < nt_tok ? v : -INFINITY;
             }
           float pr[U][4];
@@ -993,8 +1140,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
           // P^T as B fragments: transpose the (token x head) 8x8 blocks in registers
 #pragma unroll
           for (int u = 0; u < U; ++u) {
-            pb[u][nt][0] = movmatrix_t(pack2<TM>(pr[u][0], pr[u][1]));  // tokens 16u + 0-7
-            pb[u][nt][1] = movmatrix_t(pack2<TM>(pr[u][2], pr[u][3]));  // tokens 16u + 8-15
+            // (INT4: each token's weight times its V scale; the sums l keep the weights)
+            const float v0 = I4 ? vsc[u][0] : 1.f, v1 = I4 ? vsc[u][1] : 1.f;
+            pb[u][nt][0] = movmatrix_t(pack2<TM>(pr[u][0] * v0, pr[u][1] * v0));  // tokens 16u + 0-7
+            pb[u][nt][1] = movmatrix_t(pack2<TM>(pr[u][2] * v1, pr[u][3] * v1));  // tokens 16u + 8-15
           }
         }
         bool all_one = true;
@@ -1013,7 +1162,52 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         }
         // ---- O^T += V^T P^T: rows = d (16 per m-tile), k = tokens, columns = heads ----
         // (V rows past the context were zero-filled by the copy, so 0 * garbage cannot occur)
-        if constexpr (F8) {
+        if constexpr (I4) {
+          // k-step u: V rows (tokens) 16u + {2t, 2t+1, 2t+8, 2t+9}, bytes [(D/16) r0,
+          // (D/16)(r0+1)) = d [(D/8) r0, (D/8)(r0+1)).  Byte permutes interleave the rows of
+          // tokens 2t and 2t + 1 (and 2t + 8, 2t + 9) so that each nibble pair of an A
+          // register is one d of the two tokens; word i's d 8i + 2m and 8i + 2m + 1 are
+          // m-tile 4i + m's rows r0 and r0 + 8 (see drow).
+          constexpr int VW = D / 64;  // 32-bit words of this lane's bytes of one V row
+          const int tq = lane & 3;
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            uint32_t vw[4][VW];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int row = 16 * u + 2 * tq + (k & 1) + 8 * (k >> 1);
+              if constexpr (VW == 2) {
+                const uint32_t addr = vb + swz4<D>(row, r0 >> 1) + 8 * (r0 & 1);
+                asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
+                             : "=r"(vw[k][0]), "=r"(vw[k][1])
+                             : "r"(addr));
+              } else {
+                const uint32_t addr = vb + swz4<D>(row, r0 >> 2) + 4 * (r0 & 3);
+                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(vw[k][0]) : "r"(addr));
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < VW; ++i) {
+              const uint32_t z[4] = {__byte_perm(vw[0][i], vw[1][i], 0x5410u),    // tokens 2t, 2t+1
+                                     __byte_perm(vw[0][i], vw[1][i], 0x7632u),
+                                     __byte_perm(vw[2][i], vw[3][i], 0x5410u),    // 2t+8, 2t+9
+                                     __byte_perm(vw[2][i], vw[3][i], 0x7632u)};
+#pragma unroll
+              for (int m = 0; m < 4; ++m) {
+                const uint32_t x = (m & 1) ? z[m >> 1] >> 8 : z[m >> 1];
+                const uint32_t y = (m & 1) ? z[2 + (m >> 1)] >> 8 : z[2 + (m >> 1)];
+                uint32_t a[4];
+                a[0] = i4x2_lo(x);
+                a[1] = i4x2_hi(x);
+                a[2] = i4x2_lo(y);
+                a[3] = i4x2_hi(y);
+#pragma unroll
+                for (int nt = 0; nt < NTH; ++nt)
+                  mma16816<TM>(o[4 * i + m][nt], a, pb[u][nt][0], pb[u][nt][1]);
+              }
+            }
+          }
+        } else if constexpr (F8) {
           // k-step u: V rows (tokens) 16u + {2t, 2t+1, 2t+8, 2t+9}, bytes [(D/8) r0,
           // (D/8)(r0+1)): m-tile mt takes bytes 2 mt and 2 mt + 1 (its rows r0 and r0 + 8,
           // see drow); a byte permute pairs the two tokens of each A register before widening
@@ -1060,7 +1254,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
             for (int nt = 0; nt < NTH; ++nt) mma16816<TM>(o[mt][nt], a, pb[0][nt][0], pb[0][nt][1]);
           }
         }
-        if (!F8 && p.key_new && j == f.ns - 1) {
+        if (!QK && p.key_new && j == f.ns - 1) {
           // fused cache write: the newest token's K and V rows, from the slot, to position
           // ctx - 1 of the sequence (lanes take the 16-byte chunks of K, then of V)
           constexpr int CH = G_::kRowChunks;
@@ -1105,8 +1299,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
             if (h < ph.nh) {
 #pragma unroll
               for (int mt = 0; mt < MT; ++mt) {
-                pacc[h * D + drow<D, F8>(mt, r0)] = o[mt][nt][cc];
-                pacc[h * D + drow<D, F8>(mt, r0 + 8)] = o[mt][nt][cc + 2];
+                pacc[h * D + drow<D, QK>(mt, r0)] = o[mt][nt][cc];
+                pacc[h * D + drow<D, QK>(mt, r0 + 8)] = o[mt][nt][cc + 2];
               }
               if (r0 == 0) {  // an empty piece (m = -inf) gets l = 0: weight 0 in the merge
                 pml[h * 2 + 0] = m_run[nt][cc];
@@ -1122,7 +1316,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       const bool bad = any_bad;
       // out = O / l, rounded; transposed in registers (movmatrix) so that each lane stores
       // two adjacent d of one head: lane (r0, qc) writes out[h = 8*nt + r0][16*mt + qc (+8)].
-      if (F8) {
+      if (QK) {
         // rows r0 and r0 + 8 of an m-tile are the adjacent d = drow(mt, r0), + 1: each lane
         // stores its two heads' pairs directly
 #pragma unroll
@@ -1134,7 +1328,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
             if (h < ph.nh) {
 #pragma unroll
               for (int mt = 0; mt < MT; ++mt)
-                *reinterpret_cast<uint32_t*>(out_rows + h * D + drow<D, F8>(mt, r0)) =
+                *reinterpret_cast<uint32_t*>(out_rows + h * D + drow<D, QK>(mt, r0)) =
                     pack2<T>(o[mt][nt][cc] * inv, o[mt][nt][cc + 2] * inv);
             }
           }
@@ -1185,8 +1379,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
           if (h >= rbase && h < rbase + 4) {
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
-              sm.xo[warp][h - rbase][drow<D, F8>(mt, r0)] = o[mt][nt][cc];
-              sm.xo[warp][h - rbase][drow<D, F8>(mt, r0 + 8)] = o[mt][nt][cc + 2];
+              sm.xo[warp][h - rbase][drow<D, QK>(mt, r0)] = o[mt][nt][cc];
+              sm.xo[warp][h - rbase][drow<D, QK>(mt, r0 + 8)] = o[mt][nt][cc + 2];
             }
           }
         }
@@ -1213,7 +1407,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         if (whole) {
           uint2 packed = make_uint2(0u, 0u);  // zeros for a pair with a bad block
           if (!any_bad) {
-            const float inv = F8 ? p.out_scale / L : 1.f / L;
+            const float inv = QK ? p.out_scale / L : 1.f / L;
             packed.x = pack2<T>(acc.x * inv, acc.y * inv);
             packed.y = pack2<T>(acc.z * inv, acc.w * inv);
           }
@@ -1265,7 +1459,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     if (P == 1 && bits) {
       const int nj = (bits & 1) + ((bits >> 1) & 1);
       const CutPiece& j0 = (bits & 1) ? cut_a : cut_b;
-      if (merge_staged<D, T, F8>(p, pi, j0, cut_b, nj, ring, sm.ring[warp][0], R * G_::kStageBytes,
+      if (merge_staged<D, T, QK>(p, pi, j0, cut_b, nj, ring, sm.ring[warp][0], R * G_::kStageBytes,
                              smem_addr(&sm.merge_bar[warp]), lane))
         bits = 0;
     }
@@ -1274,16 +1468,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       const CutPiece& cp = k == 0 ? cut_a : cut_b;
       T* out_rows =
           reinterpret_cast<T*>(p.out) + (static_cast<size_t>(cp.s) * p.num_q_heads + cp.h0) * D;
-      merge_pieces<D, T, F8>(p, pi, cp.c_first, cp.first_slot, cp.c_last, cp.nh, out_rows, gt,
+      merge_pieces<D, T, QK>(p, pi, cp.c_first, cp.first_slot, cp.c_last, cp.nh, out_rows, gt,
                          gthreads);
     }
   }
 }
 
-template <int D, int NTH, typename T, bool F8>
+template <int D, int NTH, typename T, int KV>
 int launch(const Params& prm, int grid, cudaStream_t stream) {
-  const size_t smem = sizeof(Smem<D, F8 ? 1 : 2>) + 1024;  // + alignment slack for the ring
-  auto* kern = decode_kernel<D, NTH, T, F8>;
+  const size_t smem = sizeof(Smem<D, KV>) + 1024;  // + alignment slack for the ring
+  auto* kern = decode_kernel<D, NTH, T, KV>;
   if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), smem)) return -3;
   // a programmatic dependent of the previous kernel in the stream (see pdl_wait_primary)
   cudaLaunchConfig_t cfg = {};
@@ -1302,9 +1496,12 @@ int launch(const Params& prm, int grid, cudaStream_t stream) {
 
 }  // namespace decode
 
-// FP8 instantiations live in their own translation unit (pa_decode_fp8.cu).
+// FP8 and INT4 instantiations live in their own translation units (pa_decode_fp8.cu,
+// pa_decode_int4.cu).
 int decode_launch_fp8(const decode::Params& p, int grid, int head_dim, bool bf16,
                       cudaStream_t stream);
+int decode_launch_int4(const decode::Params& p, int grid, int head_dim, bool bf16,
+                       cudaStream_t stream);
 
 }  // namespace pa
 

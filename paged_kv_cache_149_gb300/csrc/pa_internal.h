@@ -24,6 +24,9 @@ struct DecodeArgs {
   bool bf16;       // q / out type (and the cache type unless kv_fp8)
   bool kv_fp8;     // caches hold FP8 E4M3 codes with scales k_scale, v_scale
   float k_scale = 1.f, v_scale = 1.f;
+  bool kv_int4 = false;  // caches hold INT4 codes [NB][Hkv][B][d/2] with a scale per row
+  const void* k_scales = nullptr;  // INT4: float32 [NB][Hkv][B]
+  const void* v_scales = nullptr;
   unsigned* err;  // device address of the per-device error word
 };
 
@@ -71,6 +74,13 @@ int append_newest_fp8_launch(const void* key, const void* value, void* k_cache, 
                              const int32_t* context_lens, int num_seqs, int num_blocks,
                              int num_kv_heads, int head_dim, int block_size, float k_scale,
                              float v_scale, bool bf16, cudaStream_t stream);
+// INT4 cache write: `count` rows' tokens through slot_mapping (null: the newest token of
+// each of `count` sequences through the table, position context_lens[s] - 1).
+int cache_int4_launch(const void* key, const void* value, void* k_codes, void* v_codes,
+                      float* k_scales, float* v_scales, const int64_t* slot_mapping,
+                      const int32_t* block_tables, int max_blocks_per_seq,
+                      const int32_t* context_lens, int count, int num_blocks, int num_kv_heads,
+                      int head_dim, int block_size, bool bf16, unsigned* err, cudaStream_t stream);
 int swap_blocks_launch(const void* src_k, const void* src_v, void* dst_k, void* dst_v,
                        const int32_t* block_mapping, int num_pairs, int src_num_blocks,
                        int dst_num_blocks, int num_kv_heads, int row_bytes, int block_size,
