@@ -1148,25 +1148,40 @@ def prefix_line(args, res, world):
 
 FP8_WORKLOADS = {"kv8_llama31_8b": "llama31_8b", "kv8_llama7b_mha": "llama7b_mha",
                  "kv8_tiny": "tiny"}
+INT4_WORKLOADS = {"kv4_llama31_8b": "llama31_8b", "kv4_llama7b_mha": "llama7b_mha",
+                  "kv4_tiny": "tiny"}
 FP8_SCALE = 0.0123   # k_scale = v_scale: about max|N(0,1) draw| / 448 for these batches
 
 
-def fp8_step_bytes(wl):
-    """Algorithmic bytes of one FP8 step: decode reads the valid tokens' K/V codes (one
-    byte each), q, the table entries and lengths, and writes out; the cache write reads
-    the newest rows (16-bit) and writes their codes."""
+def quant_recipe(name):
+    """(format, batch recipe) of a quantised-KV workload name."""
+    return ("int4", INT4_WORKLOADS[name]) if name in INT4_WORKLOADS else ("fp8", FP8_WORKLOADS[name])
+
+
+def row_bytes(fmt, d):
+    """Cached bytes of one token of one kv head, K or V: one byte a code for FP8; a nibble
+    a code plus the float32 scale for INT4."""
+    return d if fmt == "fp8" else d // 2 + 4
+
+
+def fp8_step_bytes(wl, fmt="fp8"):
+    """Algorithmic bytes of one quantised-KV step: decode reads the valid tokens' K/V rows
+    (codes, and INT4 scales), q, the table entries and lengths, and writes out; the cache
+    write reads the newest rows (16-bit) and writes their codes (and scales)."""
     n, hq, hkv, d, bs = wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.block_size
     ctx = [int(c) for c in wl.context_lens]
-    decode = sum(ctx) * hkv * d * 2 + 2 * n * hq * d * 2 + sum(-(-c // bs) for c in ctx) * 4 + 4 * n
-    reshape = n * hkv * d * (2 + 1) * 2
+    rb = row_bytes(fmt, d)
+    decode = sum(ctx) * hkv * rb * 2 + 2 * n * hq * d * 2 + sum(-(-c // bs) for c in ctx) * 4 + 4 * n
+    reshape = n * hkv * (2 * d + rb) * 2
     return decode, reshape
 
 
 def run_gpu_fp8(args, rank, world, local_rank):
-    """The decode step over FP8 blocks: the newest tokens' rows quantised into the cache
-    (pa_reshape_and_cache_fp8), then paged decode over the codes (pa_decode_fp8), the two
-    launches back to back (programmatic dependent launch); the decode kernel alone timed
-    beside it; end to end with host buffers.  ROTATE batches in disjoint blocks."""
+    """The decode step over FP8 (or INT4) blocks: the newest tokens' rows quantised into
+    the cache, then paged decode over the codes (pa_decode_append_fp8 / _int4: two launches
+    back to back, programmatic dependent launch); the decode kernel alone and the two-call
+    step timed beside it; end to end with host buffers.  ROTATE batches in disjoint
+    blocks."""
     import torch
 
     import paged_kv_cache_149_gb300 as pa
@@ -1176,16 +1191,36 @@ def run_gpu_fp8(args, rank, world, local_rank):
     _build.build()
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
-    wl = workloads.RECIPES[FP8_WORKLOADS[args.workload]]()
+    fmt, recipe = quant_recipe(args.workload)
+    wl = workloads.RECIPES[recipe]()
     dt = {"fp16": torch.float16, "bf16": torch.bfloat16}[wl.dtype]
     ks = vs = FP8_SCALE
 
     def up(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(dt)
     nb, order = rotation_pool(wl, ROTATE)
-    shape = (nb, wl.num_kv_heads, wl.block_size, wl.head_dim)
+    d_bytes = wl.head_dim if fmt == "fp8" else wl.head_dim // 2
+    shape = (nb, wl.num_kv_heads, wl.block_size, d_bytes)
     k8 = torch.zeros(shape, dtype=torch.uint8, device=device)
     v8 = torch.zeros(shape, dtype=torch.uint8, device=device)
+    if fmt == "int4":
+        k4s = torch.zeros(shape[:3], dtype=torch.float32, device=device)
+        v4s = torch.zeros(shape[:3], dtype=torch.float32, device=device)
+
+    def cache_write(key, value, slots):
+        if fmt == "fp8":
+            pa.reshape_and_cache_fp8(key, value, k8, v8, slots, ks, vs, stream=stream)
+        else:
+            pa.reshape_and_cache_int4(key, value, k8, v8, k4s, v4s, slots, stream=stream)
+
+    def decode(b, out):
+        if fmt == "fp8":
+            pa.decode_fp8(b["q"], k8, v8, b["tables"], b["ctx"], wl.scale, ks, vs, out=out,
+                          workspace=ws, stream=stream)
+        else:
+            pa.decode_int4(b["q"], k8, v8, k4s, v4s, b["tables"], b["ctx"], wl.scale, out=out,
+                           workspace=ws, stream=stream)
+    stream = None
     pool = pa.BlockPool(nb, wl.block_size, order)
     n, T = wl.num_seqs, wl.max_blocks_per_seq
     keys, values = up(wl.keys), up(wl.values)
@@ -1199,8 +1234,7 @@ def run_gpu_fp8(args, rank, world, local_rank):
             t = pool.block_table(r * n + s)
             tables[s, :len(t)] = t
             slots.append(pool.slots(r * n + s, 0, int(wl.context_lens[s])))
-        pa.reshape_and_cache_fp8(keys, values, k8, v8,
-                                 torch.from_numpy(np.concatenate(slots)).to(device), ks, vs)
+        cache_write(keys, values, torch.from_numpy(np.concatenate(slots)).to(device))
         batches.append({
             "q": up(wl.q), "tables": torch.from_numpy(tables).to(device),
             "ctx": torch.from_numpy(np.ascontiguousarray(wl.context_lens, np.int32)).to(device),
@@ -1215,19 +1249,21 @@ def run_gpu_fp8(args, rank, world, local_rank):
 
     def step(i, b=None):
         b = b or batches[i % ROTATE]
-        pa.decode_append_fp8(b["q"], b["key"], b["value"], k8, v8, b["tables"], b["ctx"],
-                             wl.scale, ks, vs, out=b["out"], workspace=ws, stream=stream)
+        if fmt == "fp8":
+            pa.decode_append_fp8(b["q"], b["key"], b["value"], k8, v8, b["tables"], b["ctx"],
+                                 wl.scale, ks, vs, out=b["out"], workspace=ws, stream=stream)
+        else:
+            pa.decode_append_int4(b["q"], b["key"], b["value"], k8, v8, k4s, v4s, b["tables"],
+                                  b["ctx"], wl.scale, out=b["out"], workspace=ws, stream=stream)
 
     def step_two_calls(i):
         b = batches[i % ROTATE]
-        pa.reshape_and_cache_fp8(b["key"], b["value"], k8, v8, b["slots"], ks, vs, stream=stream)
-        pa.decode_fp8(b["q"], k8, v8, b["tables"], b["ctx"], wl.scale, ks, vs, out=b["out"],
-                      workspace=ws, stream=stream)
+        cache_write(b["key"], b["value"], b["slots"])
+        decode(b, b["out"])
 
     def decode_only(i):
         b = batches[i % ROTATE]
-        pa.decode_fp8(b["q"], k8, v8, b["tables"], b["ctx"], wl.scale, ks, vs, out=b["out"],
-                      workspace=ws, stream=stream)
+        decode(b, b["out"])
 
     for i in range(args.warmup):
         step(i)
@@ -1295,8 +1331,11 @@ def run_gpu_fp8(args, rank, world, local_rank):
 
 
 def oracle_fp8_sample(name, budget_s):
-    """The FP8 decode oracle on whole sequences of the batch (codes made by the oracle's own
-    cache write), single thread, until budget_s of CPU time is spent."""
+    """The FP8 (or INT4) decode oracle on whole sequences of the batch (codes made by the
+    oracle's own cache write), single thread, until budget_s of CPU time is spent."""
+    fmt, recipe = quant_recipe(name)
+    if fmt == "int4":
+        return oracle_int4_sample(recipe, budget_s)
     code = f"""
 import json, sys, time
 sys.path.insert(0, {ROOT!r})
@@ -1304,7 +1343,7 @@ import numpy as np
 import workloads
 from oracle import fp8
 from oracle.block_pool import BlockPool
-wl = workloads.RECIPES[{FP8_WORKLOADS[name]!r}]()
+wl = workloads.RECIPES[{recipe!r}]()
 pool = BlockPool(wl.num_blocks, wl.block_size, wl.free_order)
 n, T = wl.num_seqs, wl.max_blocks_per_seq
 tables = np.full((n, T), -1, dtype=np.int32)
@@ -1334,9 +1373,50 @@ print(json.dumps({{"seqs": done, "seconds": time.process_time() - t0, "bytes": n
     return json.loads(r.stdout.strip().splitlines()[-1])
 
 
+def oracle_int4_sample(recipe, budget_s):
+    """The INT4 decode oracle on whole sequences of the batch, as oracle_fp8_sample."""
+    code = f"""
+import json, sys, time
+sys.path.insert(0, {ROOT!r})
+import numpy as np
+import workloads
+from oracle import int4
+from oracle.block_pool import BlockPool
+wl = workloads.RECIPES[{recipe!r}]()
+pool = BlockPool(wl.num_blocks, wl.block_size, wl.free_order)
+n, T = wl.num_seqs, wl.max_blocks_per_seq
+tables = np.full((n, T), -1, dtype=np.int32)
+slots = []
+for s in range(n):
+    c = int(wl.context_lens[s]); pool.allocate(s, c)
+    t = pool.block_table(s); tables[s, :len(t)] = t
+    slots += [pool.slot(s, i) for i in range(c)]
+kc = np.zeros((wl.num_blocks, wl.num_kv_heads, wl.block_size, wl.head_dim // 2), np.uint8)
+ks = np.zeros((wl.num_blocks, wl.num_kv_heads, wl.block_size), np.float32)
+kc, vc, ks, vs = int4.reshape_and_cache(kc, kc.copy(), ks, ks.copy(), wl.keys, wl.values,
+                                        np.array(slots), wl.dtype)
+done, nbytes, t0 = 0, 0, time.process_time()
+while time.process_time() - t0 < {budget_s} and done < n:
+    int4.paged_decode_bits(wl.q, kc, vc, ks, vs, tables, wl.context_lens, wl.scale,
+                           wl.block_size, wl.dtype, seqs=[done])
+    c = int(wl.context_lens[done])
+    nbytes += c * wl.num_kv_heads * (wl.head_dim // 2 + 4) * 2 + 2 * wl.num_q_heads * wl.head_dim * 2
+    done += 1
+print(json.dumps({{"seqs": done, "seconds": time.process_time() - t0, "bytes": nbytes}}))
+"""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
+    if r.returncode != 0:
+        raise RuntimeError("int4 oracle baseline failed:\n" + r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
 def fp8_line(args, res, world):
     wl = res["wl"]
-    dec_b, resh_b = fp8_step_bytes(wl)
+    fmt, _ = quant_recipe(args.workload)
+    dec_b, resh_b = fp8_step_bytes(wl, fmt)
+    fp8 = fmt == "fp8"
     step_s = res["total_ms"] / 1e3 / args.steps
     value = world * (dec_b + resh_b) / step_s / 1e9
     peak, peak_kind = measured_peak()
@@ -1345,29 +1425,34 @@ def fp8_line(args, res, world):
         if args.cpu_baseline_seconds > 0 else None
     ctx = wl.context_lens
     return {
-        "metric": "paged decode KV GB/s over FP8 (E4M3) blocks and % of GB300 HBM peak; "
-                  "µs per decode step",
+        "metric": ("paged decode KV GB/s over FP8 (E4M3) blocks and % of GB300 HBM peak; "
+                   "µs per decode step" if fp8 else
+                   "paged decode KV GB/s over INT4 blocks (4-bit codes + a float32 scale per "
+                   "row) and % of GB300 HBM peak; µs per decode step"),
         "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(res["total_ms"] / args.steps, 5),
         "us_per_step": round(1e3 * res["total_ms"] / args.steps, 2),
         "us_per_step_two_calls": round(1e3 * res["two_calls_ms"], 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": f"e4m3 K/V, {wl.dtype} q/out, f16 MMA",
+        "dtype": (f"e4m3 K/V, {wl.dtype} q/out, f16 MMA" if fp8 else
+                  f"int4 K/V codes + f32 row scales, {wl.dtype} q/out, f16 MMA"),
         "data": "synthetic (seeded normals; no dataset or weights)",
         "config": {
             "workload": (f"{args.workload}: the {wl.name} batch ({wl.num_seqs} seqs, ctx "
                          f"{int(ctx.min())}..{int(ctx.max())}, sum {int(ctx.sum())}, "
                          f"{wl.num_q_heads} q / {wl.num_kv_heads} kv heads, head_dim "
-                         f"{wl.head_dim}, block_size {wl.block_size}) with E4M3 K/V blocks, "
-                         f"k_scale = v_scale = {FP8_SCALE}"),
+                         f"{wl.head_dim}, block_size {wl.block_size}) with "
+                         + (f"E4M3 K/V blocks, k_scale = v_scale = {FP8_SCALE}" if fp8 else
+                            "INT4 K/V blocks (codes in [-7, 7], scale max|x| / 7 per row)")),
             "l2": f"{ROTATE} batches in disjoint blocks rotated every step "
                   f"({dec_b / 1e6:.0f} MB of decode bytes per batch)",
             "parallelism": f"replicas x{world}",
-            "step": "pa_decode_append_fp8: the newest rows quantised into their slots, then "
-                    "the decode as a programmatic dependent (two launches; the two-call step "
-                    "is pa_reshape_and_cache_fp8 + pa_decode_fp8)",
+            "step": (f"pa_decode_append_{fmt}: the newest rows quantised into their slots, "
+                     "then the decode as a programmatic dependent (two launches; the two-call "
+                     f"step is pa_reshape_and_cache_{fmt} + pa_decode_{fmt})"),
         },
-        "roofline": {"bound": "hbm", "kernel": "decode_kernel<F8> (pa_decode_fp8)",
+        "roofline": {"bound": "hbm", "kernel": (f"decode_kernel<{'F8' if fp8 else 'INT4'}> "
+                                                f"(pa_decode_{fmt})"),
                      "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": f"{peak_kind} (copy bandwidth)", "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": None,
@@ -1376,8 +1461,8 @@ def fp8_line(args, res, world):
         "cpu_baseline": None if cpu is None else {
             "value": round(cpu["bytes"] / cpu["seconds"] / 1e9, 4), "unit": "GB/s", "cores": 1,
             "kind": "oracle",
-            "sample": f"float64 FP8 decode oracle, single thread, {cpu['seqs']} whole "
-                      "sequences of the batch"},
+            "sample": f"float64 {fmt.upper()} decode oracle, single thread, {cpu['seqs']} "
+                      "whole sequences of the batch"},
         "e2e": {"value": round(world * (dec_b + resh_b) / (res["e2e_ms"] / 1e3) / 1e9, 1),
                 "unit": "GB/s", "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
                 "us_per_step": round(1e3 * res["e2e_ms"], 2)},
@@ -1432,7 +1517,7 @@ def main(argv=None, runner=None, backend="nccl"):
     is_prefill = args.workload.startswith("prefill")
     is_swap = args.workload in SWAP_WORKLOADS
     is_prefix = args.workload in PREFIX_WORKLOADS
-    is_fp8 = args.workload in FP8_WORKLOADS
+    is_fp8 = args.workload in FP8_WORKLOADS or args.workload in INT4_WORKLOADS
     default_runner = (run_gpu_prefill if is_prefill else run_gpu_swap if is_swap else
                       run_gpu_prefix if is_prefix else run_gpu_fp8 if is_fp8 else run_gpu)
     res = (runner or default_runner)(args, rank, world, local_rank)
