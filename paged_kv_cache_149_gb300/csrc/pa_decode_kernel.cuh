@@ -356,32 +356,30 @@ __device__ __forceinline__ uint32_t e4m3x2_f16x2_hi(uint32_t w) {
   return r;
 }
 
-// INT4 stages: a row is D / 2 bytes.  At D = 128 row r is stored in row slot
-// r ^ ((r >> 1) & 1): the K fragment loads (eight consecutive rows) still read 512
-// contiguous bytes, and the V fragment loads (rows c, c + 2, c + 4, c + 6) fall two into
-// each half of the banks.  At D = 64 rows are packed as they come.
+// INT4 stages: a row is D / 2 bytes.  The V fragment loads read, per half-warp, the same
+// bytes of rows c, c + 2, c + 4, c + 6; the K fragment loads and the copies read or write
+// whole consecutive rows.  At D = 128 (64-byte rows) row r sits in row slot
+// r ^ ((r >> 1) & 1) with its 16-byte chunks XORed by 2 ((r >> 2) & 1); at D = 64
+// (32-byte rows) row r sits in slot r ^ ((r >> 2) & 1).  Either way those four rows fall
+// on distinct banks and consecutive rows stay whole and contiguous.
 template <int D>
 __device__ __forceinline__ uint32_t swz4(int row, int chunk) {
-  return D == 128 ? static_cast<uint32_t>(64 * (row ^ ((row >> 1) & 1)) + 16 * chunk)
-                  : static_cast<uint32_t>(32 * row + 16 * chunk);
+  return D == 128
+             ? static_cast<uint32_t>(64 * (row ^ ((row >> 1) & 1)) + 16 * (chunk ^ (2 * ((row >> 2) & 1))))
+             : static_cast<uint32_t>(32 * (row ^ ((row >> 2) & 1)) + 16 * chunk);
 }
 
-// INT4 nibbles -> f16x2, exact.  The nibble u (= code + 8) at bits 0-3 and 16-19 of w
-// (i4x2_lo) or at bits 4-7 and 20-23 (i4x2_hi) is placed in the mantissa of 1024.0
-// (0x6400): 1024 + u, or 1024 + 16 u; subtracting 1032, or scaling by 1/16 and adding
-// -72, leaves u - 8 exactly.
-__device__ __forceinline__ uint32_t i4x2_lo(uint32_t w) {
-  const uint32_t x = (w & 0x000F000Fu) | 0x64006400u;
-  uint32_t r;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(0x64086408u));
-  return r;
-}
-__device__ __forceinline__ uint32_t i4x2_hi(uint32_t w) {
-  const uint32_t x = (w & 0x00F000F0u) | 0x64006400u;
-  uint32_t r;
-  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(x), "r"(0x2C002C00u), "r"(0xD480D480u));
-  return r;
-}
+// INT4 nibbles -> f16x2 with one logic operation, exact: the nibble u (= code + 8) at
+// bits 0-3 and 16-19 of w (i4x2_lo) or at bits 4-7 and 20-23 (i4x2_hi) is placed in the
+// mantissa of 1024.0 (0x6400), which reads 1024 + u, or 1024 + 16 u.  The offsets never
+// pass through these registers: the products are exact in the fp32 accumulators, and the
+// kernel removes them there.  For K the high nibbles meet q / 16, so a score gains
+// 1032 Q_lo + 72 Q_hi (Q_lo, Q_hi: the sums of q over the low- and high-nibble d), which
+// the score accumulators start from minus.  For V a low-nibble output row holds
+// O + 1032 W and a high-nibble row 16 (O + 72 W), W = the sum of the weights that entered
+// P V, taken out at the pair end.
+__device__ __forceinline__ uint32_t i4x2_lo(uint32_t w) { return (w & 0x000F000Fu) | 0x64006400u; }
+__device__ __forceinline__ uint32_t i4x2_hi(uint32_t w) { return (w & 0x00F000F0u) | 0x64006400u; }
 
 __device__ __forceinline__ float lds_f32(uint32_t addr) {
   float v;
@@ -684,7 +682,9 @@ __device__ __forceinline__ void load_q8(const Params& p, int s, int h0, int nh, 
 
 // Q^T for INT4 blocks, as f16, in the d order the K fragments use: k-steps 2j and 2j + 1
 // take the eight d = (D/4) t + 8 j + {0..7} of word j of a K row, k-step 2j + e getting
-// d + 2e and d + 2e + 4 in b0 and d + 2e + 1 and d + 2e + 5 in b1 (t = lane % 4).
+// d + 2e and d + 2e + 4 in b0 and d + 2e + 1 and d + 2e + 5 in b1 (t = lane % 4).  b1
+// meets the high nibbles (1024 + 16 u), so it holds q / 16 (exact unless q / 16 is an f16
+// subnormal, |q| < 2^-10).
 template <int D, int NTH, typename T>
 __device__ __forceinline__ void load_q4(const Params& p, int s, int h0, int nh, int lane,
                                         uint32_t (&qb)[D / 16][NTH][2]) {
@@ -701,9 +701,9 @@ __device__ __forceinline__ void load_q4(const Params& p, int s, int h0, int nh, 
       const float2 a = unpack2<T>(w.x), b = unpack2<T>(w.y), c = unpack2<T>(w.z),
                    d = unpack2<T>(w.w);  // d + 0,1 / 2,3 / 4,5 / 6,7
       qb[2 * j][nt][0] = pack2<__half>(a.x, c.x);
-      qb[2 * j][nt][1] = pack2<__half>(a.y, c.y);
+      qb[2 * j][nt][1] = pack2<__half>(a.y * 0.0625f, c.y * 0.0625f);
       qb[2 * j + 1][nt][0] = pack2<__half>(b.x, d.x);
-      qb[2 * j + 1][nt][1] = pack2<__half>(b.y, d.y);
+      qb[2 * j + 1][nt][1] = pack2<__half>(b.y * 0.0625f, d.y * 0.0625f);
     }
   }
 }
@@ -964,6 +964,32 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       }
     }
 
+    // INT4: each score starts from -(1032 Q_lo + 72 Q_hi) of its head, from the f16 q
+    // values the MMAs use (lane (r0, t) holds column r0's b fragments for its t; sums over
+    // t, then each lane takes its columns qc, qc + 1).  W: this lane's share of the
+    // weights that entered P V (see i4x2_lo).
+    float kofs[NTH][2], wsum[NTH][2];
+    if constexpr (I4) {
+#pragma unroll
+      for (int nt = 0; nt < NTH; ++nt) {
+        wsum[nt][0] = wsum[nt][1] = 0.f;
+        kofs[nt][0] = kofs[nt][1] = 0.f;
+        if (!computes) continue;
+        float ql = 0.f, qh = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          const float2 a = unpack2<__half>(qb[ks][nt][0]), b = unpack2<__half>(qb[ks][nt][1]);
+          ql += a.x + a.y;
+          qh += b.x + b.y;  // (q / 16)
+        }
+        float c = 1032.f * ql + 1152.f * qh;  // 72 * 16 = 1152
+        c += __shfl_xor_sync(0xffffffffu, c, 1);
+        c += __shfl_xor_sync(0xffffffffu, c, 2);
+        kofs[nt][0] = -__shfl_sync(0xffffffffu, c, 4 * qc);
+        kofs[nt][1] = -__shfl_sync(0xffffffffu, c, 4 * (qc + 1));
+      }
+    }
+
     // This lane's softmax columns: heads 8*nt + qc and + 1 of every n-tile.
     float m_run[NTH][2], l_run[NTH][2];
     float o[MT][NTH][4];  // O^T: rows d = 16*mt + r0 (+8), columns = heads
@@ -996,7 +1022,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
 #pragma unroll
           for (int nt = 0; nt < NTH; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) sacc[u][nt][e] = sodd[u][nt][e] = 0.f;
+            for (int e = 0; e < 4; ++e) {
+              sacc[u][nt][e] = I4 ? kofs[nt][e & 1] : 0.f;
+              sodd[u][nt][e] = 0.f;
+            }
         // INT4: the K and V scales of this lane's rows 16u + r0 and 16u + r0 + 8
         float ksc[U][2], vsc[U][2];
         if constexpr (I4) {
@@ -1138,12 +1167,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
             m_run[nt][cc] = m_new;
           }
           // P^T as B fragments: transpose the (token x head) 8x8 blocks in registers
+          float wst0 = 0.f, wst1 = 0.f;
 #pragma unroll
           for (int u = 0; u < U; ++u) {
-            // (INT4: each token's weight times its V scale; the sums l keep the weights)
+            // (INT4: each token's weight times its V scale; the sums l keep the weights,
+            // W the rounded products that enter P V)
             const float v0 = I4 ? vsc[u][0] : 1.f, v1 = I4 ? vsc[u][1] : 1.f;
-            pb[u][nt][0] = movmatrix_t(pack2<TM>(pr[u][0] * v0, pr[u][1] * v0));  // tokens 16u + 0-7
-            pb[u][nt][1] = movmatrix_t(pack2<TM>(pr[u][2] * v1, pr[u][3] * v1));  // tokens 16u + 8-15
+            const uint32_t w01 = pack2<TM>(pr[u][0] * v0, pr[u][1] * v0);  // tokens 16u + 0-7
+            const uint32_t w23 = pack2<TM>(pr[u][2] * v1, pr[u][3] * v1);  // tokens 16u + 8-15
+            if constexpr (I4) {
+              const float2 f01 = unpack2<__half>(w01), f23 = unpack2<__half>(w23);
+              wst0 += f01.x + f23.x;
+              wst1 += f01.y + f23.y;
+            }
+            pb[u][nt][0] = movmatrix_t(w01);
+            pb[u][nt][1] = movmatrix_t(w23);
+          }
+          if constexpr (I4) {
+            wsum[nt][0] = fmaf(wsum[nt][0], alpha[nt][0], wst0);
+            wsum[nt][1] = fmaf(wsum[nt][1], alpha[nt][1], wst1);
           }
         }
         bool all_one = true;
@@ -1277,6 +1319,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       __syncwarp();  // every lane is done with the slot before a later stage refills it
     }
 
+    if constexpr (I4) {
+      // take the V offsets out of O (see i4x2_lo), W summed over the lanes of a column
+#pragma unroll
+      for (int nt = 0; nt < NTH; ++nt)
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          float w = wsum[nt][cc];
+          w += __shfl_xor_sync(0xffffffffu, w, 4);
+          w += __shfl_xor_sync(0xffffffffu, w, 8);
+          w += __shfl_xor_sync(0xffffffffu, w, 16);
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            o[mt][nt][cc] = fmaf(-1032.f, w, o[mt][nt][cc]);                 // low-nibble d
+            o[mt][nt][cc + 2] = fmaf(o[mt][nt][cc + 2], 0.0625f, -72.f * w);  // high-nibble d
+          }
+        }
+    }
     const bool whole = r.x == 0 && r.y == f.ns;
     const int slot_out = cta_first ? 0 : 1;
     const size_t piece = (static_cast<size_t>(c) * 2 + slot_out) * p.gs + pi;
