@@ -369,6 +369,23 @@ __device__ __forceinline__ uint32_t swz4(int row, int chunk) {
              : static_cast<uint32_t>(32 * (row ^ ((row >> 2) & 1)) + 16 * chunk);
 }
 
+// Shared-memory offset, within a stage's K (or V) rows, of the 16-byte chunk `ch` that a
+// lane copies in pass j (its row rsub + j * rows-per-pass), in closed form: the XOR
+// patterns of swz / swz8 / swz4 reduce to a lane-dependent base and a per-pass constant.
+template <int D, int KV, int ROWB>
+__device__ __forceinline__ uint32_t copy_dst(int rsub, int ch, int j) {
+  if constexpr (ROWB == 256) {  // 16-bit rows of 128 values, two rows a pass
+    return static_cast<uint32_t>((ch >> 3) * 2048 + rsub * 128 + 256 * j +
+                                 ((16 * ((ch & 7) ^ rsub)) ^ (32 * (j & 3))));
+  } else if constexpr (ROWB == 128) {  // 128-byte rows (16-bit d = 64, FP8 d = 128), four a pass
+    return static_cast<uint32_t>(128 * rsub + 512 * j + ((16 * (ch ^ rsub)) ^ (64 * (j & 1))));
+  } else if constexpr (KV == 2) {  // INT4 rows: a pass spans 512 bytes of whole rows
+    return swz4<D>(rsub, ch) + 512u * j;
+  } else {  // FP8 rows of 64 bytes, packed
+    return static_cast<uint32_t>(64 * rsub + 16 * ch + 512 * j);
+  }
+}
+
 // INT4 nibbles -> f16x2 with one logic operation, exact: the nibble u (= code + 8) at
 // bits 0-3 and 16-19 of w (i4x2_lo) or at bits 4-7 and 20-23 (i4x2_hi) is placed in the
 // mantissa of 1024.0 (0x6400), which reads 1024 + u, or 1024 + 16 u.  The offsets never
@@ -853,6 +870,38 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
 #pragma unroll
         for (int k = 0; k < NE; ++k)
           rbase[k] = static_cast<size_t>((nxt_e[k] * p.num_kv_heads + nxt.kvh) * p.block_size);
+        // A whole stage whose rows a pass never splits between blocks (rows per pass <= B):
+        // each pass's block and row offset are constants for the block size, so the copies
+        // need one base address per block.
+        auto copy_whole = [&](auto lbc) {
+          constexpr int LB = decltype(lbc)::value;
+          constexpr int B = 1 << LB;
+          constexpr int RPP = G_::kRowsPerPass;
+          constexpr int NEU = ST / B > 1 ? ST / B : 1;
+          const uint8_t* gk[NEU];
+          const uint8_t* gv[NEU];
+#pragma unroll
+          for (int k = 0; k < NEU; ++k) {
+            const size_t off = (rbase[k] + row0 + rsub) * G_::kRowBytes + ch * 16;
+            gk[k] = p.k_cache + off;
+            gv[k] = p.v_cache + off;
+          }
+#pragma unroll
+          for (int j = 0; j < G_::kPasses; ++j) {
+            const int kk = min(NEU - 1, (RPP * j) >> LB);
+            const ptrdiff_t goff = static_cast<ptrdiff_t>(RPP * j - kk * B) * G_::kRowBytes;
+            const uint32_t so = dst + copy_dst<D, KV, G_::kRowBytes>(rsub, ch, j);
+            cp_async16(so, gk[kk] + goff, 16u);
+            cp_async16(so + G_::kKBytes, gv[kk] + goff, 16u);
+          }
+        };
+        const bool whole_stage = nxt.nt == ST && G_::kRowsPerPass <= p.block_size &&
+                                 !(!QK && p.key_new && nxt.last);
+        if (whole_stage) {
+          if (p.log2_block == 3) copy_whole(std::integral_constant<int, 3>());
+          else if (p.log2_block == 4) copy_whole(std::integral_constant<int, 4>());
+          else copy_whole(std::integral_constant<int, 5>());
+        } else {
 #pragma unroll
         for (int j = 0; j < G_::kPasses; ++j) {
           const int row = rsub + j * G_::kRowsPerPass;
@@ -875,6 +924,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
             cp_async16(dst + so, p.k_cache + src, live ? 16u : 0u);
             cp_async16(dst + G_::kKBytes + so, p.v_cache + src, live ? 16u : 0u);
           }
+        }
         }
         if constexpr (I4) {
           // the rows' scales: lanes 0-7 copy K's, 8-15 V's, four tokens (16 bytes) each; a
