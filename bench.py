@@ -1177,11 +1177,10 @@ def fp8_step_bytes(wl, fmt="fp8"):
 
 
 def run_gpu_fp8(args, rank, world, local_rank):
-    """The decode step over FP8 (or INT4) blocks: the newest tokens' rows quantised into
-    the cache, then paged decode over the codes (pa_decode_append_fp8 / _int4: two launches
-    back to back, programmatic dependent launch); the decode kernel alone and the two-call
-    step timed beside it; end to end with host buffers.  ROTATE batches in disjoint
-    blocks."""
+    """The decode step over FP8 (or INT4) blocks: pa_decode_append_fp8 / _int4, one kernel
+    that quantises the newest tokens' rows into the cache and decodes over the codes; the
+    decode kernel alone and the two-call step timed beside it; end to end with host
+    buffers.  ROTATE batches in disjoint blocks."""
     import torch
 
     import paged_kv_cache_149_gb300 as pa
@@ -1447,9 +1446,9 @@ def fp8_line(args, res, world):
             "l2": f"{ROTATE} batches in disjoint blocks rotated every step "
                   f"({dec_b / 1e6:.0f} MB of decode bytes per batch)",
             "parallelism": f"replicas x{world}",
-            "step": (f"pa_decode_append_{fmt}: the newest rows quantised into their slots, "
-                     "then the decode as a programmatic dependent (two launches; the two-call "
-                     f"step is pa_reshape_and_cache_{fmt} + pa_decode_{fmt})"),
+            "step": (f"pa_decode_append_{fmt}: one kernel quantises each sequence's newest "
+                     "rows into their slots and decodes (the two-call step is "
+                     f"pa_reshape_and_cache_{fmt} + pa_decode_{fmt})"),
         },
         "roofline": {"bound": "hbm", "kernel": (f"decode_kernel<{'F8' if fp8 else 'INT4'}> "
                                                 f"(pa_decode_{fmt})"),

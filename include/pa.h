@@ -146,12 +146,12 @@ int pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
                   float v_scale, void* out, void* workspace, size_t workspace_bytes,
                   pa_dtype dtype, cudaStream_t stream);
 
-/* One FP8 decode step in one call: each sequence's newest token (key_new / value_new
- * [num_seqs][Hkv][d], fp16 or bf16) quantised into position context_lens[s] - 1 through
- * the table, with the arithmetic of pa_reshape_and_cache_fp8, then pa_decode_fp8.  Two
- * launches, the second a programmatic dependent of the first; caches and output equal
- * pa_reshape_and_cache_fp8 + pa_decode_fp8 bit for bit.  (A sequence whose newest slot is
- * invalid writes nothing; the decode flags it.) */
+/* One FP8 decode step in one call and one launch: each sequence's newest token (key_new /
+ * value_new [num_seqs][Hkv][d], fp16 or bf16) is quantised with the arithmetic of
+ * pa_reshape_and_cache_fp8 by the warp that computes the sequence's last stage, attended
+ * from there and stored at position context_lens[s] - 1 through the table; caches and
+ * output equal pa_reshape_and_cache_fp8 + pa_decode_fp8 bit for bit.  (A sequence whose
+ * newest slot is invalid writes nothing; the decode flags it.) */
 int pa_decode_append_fp8(const void* q, const void* key_new, const void* value_new,
                          void* k_cache, void* v_cache, const int32_t* block_tables,
                          int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
@@ -191,11 +191,12 @@ int pa_decode_int4(const void* q, const void* k_codes, const void* v_codes, cons
                    const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
                    int head_dim, int block_size, int num_blocks, float scale, void* out,
                    void* workspace, size_t workspace_bytes, pa_dtype dtype, cudaStream_t stream);
-/* One INT4 decode step in one call: each sequence's newest token (key_new / value_new
- * [num_seqs][Hkv][d]) quantised into position context_lens[s] - 1 through the table, with
- * the arithmetic of pa_reshape_and_cache_int4, then pa_decode_int4 (two launches, the
- * second a programmatic dependent of the first; a sequence whose newest slot is invalid
- * writes nothing and the decode flags it). */
+/* One INT4 decode step in one call and one launch: each sequence's newest token (key_new /
+ * value_new [num_seqs][Hkv][d]) is quantised with the arithmetic of
+ * pa_reshape_and_cache_int4 by the warp that computes its last stage, attended from there
+ * and stored (codes and scales) at position context_lens[s] - 1 through the table; equal to
+ * pa_reshape_and_cache_int4 + pa_decode_int4 bit for bit (a sequence whose newest slot is
+ * invalid writes nothing and the decode flags it). */
 int pa_decode_append_int4(const void* q, const void* key_new, const void* value_new,
                           void* k_codes, void* v_codes, float* k_scales, float* v_scales,
                           const int32_t* block_tables, int max_blocks_per_seq,

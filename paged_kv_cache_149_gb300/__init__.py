@@ -341,9 +341,9 @@ def decode_fp8(q, k_cache, v_cache, block_tables, context_lens, scale, k_scale, 
 
 def decode_append_fp8(q, key_new, value_new, k_cache, v_cache, block_tables, context_lens,
                       scale, k_scale, v_scale, out=None, workspace=None, stream=None):
-    """One FP8 decode step: quantise each sequence's newest K/V row into its slot at
-    position ctx - 1 and decode (= reshape_and_cache_fp8 + decode_fp8, with the slots read
-    from the block tables): two launches, the decode a programmatic dependent of the write."""
+    """One FP8 decode step in one kernel: each sequence's newest K/V row is quantised into
+    its slot at position ctx - 1 (read from the block tables) and attended (= bit for bit
+    reshape_and_cache_fp8 + decode_fp8)."""
     import torch
     n, hq, d = q.shape
     nb, hkv, bs, d2 = k_cache.shape
@@ -473,9 +473,9 @@ def decode_int4(q, k_codes, v_codes, k_scales, v_scales, block_tables, context_l
 
 def decode_append_int4(q, key_new, value_new, k_codes, v_codes, k_scales, v_scales, block_tables,
                        context_lens, scale, out=None, workspace=None, stream=None):
-    """One INT4 decode step: each sequence's newest K/V row quantised into its slot at
-    position ctx - 1, then the decode (= reshape_and_cache_int4 + decode_int4): two launches,
-    the decode a programmatic dependent of the write."""
+    """One INT4 decode step in one kernel: each sequence's newest K/V row is quantised into
+    its slot at position ctx - 1 and attended (= bit for bit reshape_and_cache_int4 +
+    decode_int4)."""
     import torch
     n, hq, d = q.shape
     nb, hkv, bs, d2 = k_codes.shape

@@ -219,25 +219,6 @@ int pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
                      k_scale, v_scale);
 }
 
-// pa_decode_append_fp8's first launch: the newest rows quantised into their slots.
-static int cache_newest_fp8(const void* key_new, const void* value_new, void* k_cache, void* v_cache,
-                     const int32_t* block_tables, int max_blocks_per_seq,
-                     const int32_t* context_lens, int num_seqs, int num_blocks, int num_kv_heads,
-                     int head_dim, int block_size, float k_scale, float v_scale, pa_dtype dtype,
-                     cudaStream_t stream) {
-  if (num_blocks < 1 || max_blocks_per_seq < 1 || !shape_ok(num_kv_heads, head_dim, block_size) ||
-      (dtype != PA_FP16 && dtype != PA_BF16) || !std::isfinite(k_scale) ||
-      !std::isfinite(v_scale) || !(k_scale > 0.f) || !(v_scale > 0.f))
-    return PA_ERR_ARG;
-  if (!k_cache || !v_cache || !aligned16(key_new) || !aligned16(value_new) ||
-      !aligned16(k_cache) || !aligned16(v_cache))
-    return PA_ERR_ARG;
-  return pa::append_newest_fp8_launch(key_new, value_new, k_cache, v_cache, block_tables,
-                                      max_blocks_per_seq, context_lens, num_seqs, num_blocks,
-                                      num_kv_heads, head_dim, block_size, k_scale, v_scale,
-                                      dtype == PA_BF16, stream);
-}
-
 int pa_decode_append_fp8(const void* q, const void* key_new, const void* value_new,
                          void* k_cache, void* v_cache, const int32_t* block_tables,
                          int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
@@ -245,15 +226,9 @@ int pa_decode_append_fp8(const void* q, const void* key_new, const void* value_n
                          int num_blocks, float scale, float k_scale, float v_scale, void* out,
                          void* workspace, size_t workspace_bytes, pa_dtype dtype,
                          cudaStream_t stream) {
-  if (num_seqs < 0) return PA_ERR_ARG;
-  if (num_seqs == 0) return PA_OK;
-  if (!key_new || !value_new || !context_lens || !block_tables) return PA_ERR_ARG;
-  // the newest rows first (their slots are read from the table on the device), then decode
-  int st = cache_newest_fp8(key_new, value_new, k_cache, v_cache, block_tables,
-                            max_blocks_per_seq, context_lens, num_seqs, num_blocks,
-                            num_kv_heads, head_dim, block_size, k_scale, v_scale, dtype, stream);
-  if (st != PA_OK) return st;
-  return decode_call(q, nullptr, nullptr, k_cache, v_cache, block_tables, max_blocks_per_seq,
+  if (num_seqs > 0 && (!key_new || !value_new)) return PA_ERR_ARG;
+  // one launch: the warp that computes a sequence's last stage quantises its newest rows
+  return decode_call(q, key_new, value_new, k_cache, v_cache, block_tables, max_blocks_per_seq,
                      context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                      num_blocks, scale, out, workspace, workspace_bytes, dtype, stream, true,
                      k_scale, v_scale);
@@ -300,8 +275,8 @@ int pa_reshape_and_cache_int4(const void* key, const void* value, void* k_codes,
   DeviceInfo di;
   if (!device_info(&di)) return PA_ERR_CUDA;
   return pa::cache_int4_launch(key, value, k_codes, v_codes, k_scales, v_scales, slot_mapping,
-                               nullptr, 0, nullptr, num_tokens, num_blocks, num_kv_heads, head_dim,
-                               block_size, dtype == PA_BF16, di.err, stream);
+                               num_tokens, num_blocks, num_kv_heads, head_dim, block_size,
+                               dtype == PA_BF16, di.err, stream);
 }
 
 int pa_decode_int4(const void* q, const void* k_codes, const void* v_codes, const float* k_scales,
@@ -323,20 +298,9 @@ int pa_decode_append_int4(const void* q, const void* key_new, const void* value_
                           int num_kv_heads, int head_dim, int block_size, int num_blocks,
                           float scale, void* out, void* workspace, size_t workspace_bytes,
                           pa_dtype dtype, cudaStream_t stream) {
-  if (num_seqs < 0) return PA_ERR_ARG;
-  if (num_seqs == 0) return PA_OK;
-  if (!key_new || !value_new || !context_lens || !block_tables || num_blocks < 1 ||
-      max_blocks_per_seq < 1 || !shape_ok(num_kv_heads, head_dim, block_size) ||
-      (dtype != PA_FP16 && dtype != PA_BF16) || !aligned16(key_new) || !aligned16(value_new) ||
-      !int4_arrays_ok(k_codes, v_codes, k_scales, v_scales))
-    return PA_ERR_ARG;
-  // the newest rows first (their slots are read from the table on the device), then decode
-  const int st = pa::cache_int4_launch(key_new, value_new, k_codes, v_codes, k_scales, v_scales,
-                                       nullptr, block_tables, max_blocks_per_seq, context_lens,
-                                       num_seqs, num_blocks, num_kv_heads, head_dim, block_size,
-                                       dtype == PA_BF16, nullptr, stream);
-  if (st != 0) return PA_ERR_CUDA;
-  return decode_call(q, nullptr, nullptr, k_codes, v_codes, block_tables, max_blocks_per_seq,
+  if (num_seqs > 0 && (!key_new || !value_new || !k_scales || !v_scales)) return PA_ERR_ARG;
+  // one launch: the warp that computes a sequence's last stage quantises its newest rows
+  return decode_call(q, key_new, value_new, k_codes, v_codes, block_tables, max_blocks_per_seq,
                      context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                      num_blocks, scale, out, workspace, workspace_bytes, dtype, stream, false, 1.f,
                      1.f, k_scales, v_scales);

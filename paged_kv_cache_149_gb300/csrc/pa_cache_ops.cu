@@ -86,101 +86,36 @@ __global__ void __launch_bounds__(128) reshape_and_cache_fp8_kernel(
   }
 }
 
-// The FP8 cache write of one decode step's newest tokens: sequence s's row goes to position
-// context_lens[s] - 1, found through the table.  A sequence whose length or table entry is
-// invalid writes nothing (the decode that follows flags and zeroes it).  One CTA per
-// sequence.
-template <typename T>
-__global__ void __launch_bounds__(128) append_newest_fp8_kernel(
-    const uint4* __restrict__ key, const uint4* __restrict__ value, uint4* __restrict__ k_cache,
-    uint4* __restrict__ v_cache, const int32_t* __restrict__ block_tables, int max_blocks_per_seq,
-    const int32_t* __restrict__ context_lens, int num_blocks, int num_kv_heads, int chunks_per_row,
-    int block_size, float k_scale, float v_scale) {
-  pdl_wait_primary();
-  pdl_launch_dependents();
-  const int s = blockIdx.x;
-  const int ctx = context_lens[s];
-  if (ctx < 1 || static_cast<long long>(ctx) > static_cast<long long>(max_blocks_per_seq) * block_size)
-    return;
-  const int t = ctx - 1;
-  const int blk = block_tables[static_cast<size_t>(s) * max_blocks_per_seq + t / block_size];
-  if (blk < 0 || blk >= num_blocks) return;
-  const int row = t % block_size;
-  const int n = num_kv_heads * chunks_per_row;
-  for (int j = threadIdx.x; j < 2 * n; j += blockDim.x) {
-    const bool is_v = j >= n;
-    const int jj = is_v ? j - n : j;
-    const int h = jj / chunks_per_row;
-    const int c = jj - h * chunks_per_row;
-    const uint4* src = (is_v ? value : key) +
-                       ((static_cast<size_t>(s) * num_kv_heads + h) * chunks_per_row + c) * 2;
-    const size_t dst =
-        ((static_cast<size_t>(blk) * num_kv_heads + h) * block_size + row) * chunks_per_row + c;
-    (is_v ? v_cache : k_cache)[dst] = quantize16_e4m3<T>(src[0], src[1], is_v ? v_scale : k_scale);
-  }
-}
-
-// INT4 rows: one warp quantises one d-value row (a token's K or V for one kv head):
-// s = max |x| / 7 (IEEE float32), c = x / s rounded half to even and clamped to [-7, 7]
-// (0 for an all-zero row), stored as nibbles u = c + 8, element 2i in the low nibble of
-// byte i, and s beside the block's codes.  Each lane takes D / 32 consecutive values.
+// INT4 rows: one warp quantises one d-value row (a token's K or V for one kv head) with
+// int4_quantize_lane; the codes go to the row's D / 2 bytes (element 2i in the low nibble
+// of byte i) and the scale beside the block's codes.
 template <typename T, int D>
 __device__ __forceinline__ void quantize_row_int4(const T* __restrict__ src, uint8_t* __restrict__ codes,
                                                   float* __restrict__ scale, int lane) {
-  constexpr int PER = D / 32;  // values per lane: 4 (D = 128) or 2 (D = 64)
-  float x[PER];
-  if constexpr (PER == 4) {
-    const uint2 w = *reinterpret_cast<const uint2*>(src + 4 * lane);
-    const float2 a = unpack2<T>(w.x), b = unpack2<T>(w.y);
-    x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
-  } else {
-    const float2 a = unpack2<T>(*reinterpret_cast<const uint32_t*>(src + 2 * lane));
-    x[0] = a.x; x[1] = a.y;
-  }
-  float amax = 0.f;
-#pragma unroll
-  for (int i = 0; i < PER; ++i) amax = fmaxf(amax, fabsf(x[i]));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  const float s = __fdiv_rn(amax, 7.f);
-  uint32_t packed = 0;
-#pragma unroll
-  for (int i = 0; i < PER; ++i) {
-    const float c = amax == 0.f ? 0.f : fminf(7.f, fmaxf(-7.f, rintf(__fdiv_rn(x[i], s))));
-    packed |= static_cast<uint32_t>(static_cast<int>(c) + 8) << (4 * i);
-  }
-  if constexpr (PER == 4) reinterpret_cast<uint16_t*>(codes)[lane] = static_cast<uint16_t>(packed);
+  float x[D / 32];
+  int4_row_values<T, D>(src, lane, x);
+  float s;
+  const uint32_t packed = int4_quantize_lane<D>(x, s);
+  if constexpr (D / 32 == 4) reinterpret_cast<uint16_t*>(codes)[lane] = static_cast<uint16_t>(packed);
   else codes[lane] = static_cast<uint8_t>(packed);
   if (lane == 0) *scale = s;
 }
 
-// grid = rows' tokens (slot mapping) or sequences (newest token through the table);
-// warps take the 2 * Hkv rows (K then V) of their token.
+// grid = the rows' tokens; warps take the 2 * Hkv rows (K then V) of their token.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) cache_int4_kernel(
     const T* __restrict__ key, const T* __restrict__ value, uint8_t* __restrict__ k_codes,
     uint8_t* __restrict__ v_codes, float* __restrict__ k_scales, float* __restrict__ v_scales,
-    const int64_t* __restrict__ slot_mapping, const int32_t* __restrict__ block_tables,
-    int max_blocks_per_seq, const int32_t* __restrict__ context_lens, int num_blocks,
-    int num_kv_heads, int block_size, unsigned* err) {
+    const int64_t* __restrict__ slot_mapping, int num_blocks, int num_kv_heads, int block_size,
+    unsigned* err) {
   pdl_wait_primary();
   pdl_launch_dependents();
   const int i = blockIdx.x;
-  long long slot;
-  if (slot_mapping) {
-    slot = slot_mapping[i];
-    if (slot < 0) return;
-    if (slot >= static_cast<long long>(num_blocks) * block_size) {
-      if (threadIdx.x == 0 && err) atomicOr(err, kErrBadSlot);
-      return;
-    }
-  } else {  // the newest token of sequence i, at position ctx - 1 (invalid: nothing written)
-    const int ctx = context_lens[i];
-    if (ctx < 1 || static_cast<long long>(ctx) > static_cast<long long>(max_blocks_per_seq) * block_size)
-      return;
-    const int blk = block_tables[static_cast<size_t>(i) * max_blocks_per_seq + (ctx - 1) / block_size];
-    if (blk < 0 || blk >= num_blocks) return;
-    slot = static_cast<long long>(blk) * block_size + (ctx - 1) % block_size;
+  const long long slot = slot_mapping[i];
+  if (slot < 0) return;
+  if (slot >= static_cast<long long>(num_blocks) * block_size) {
+    if (threadIdx.x == 0) atomicOr(err, kErrBadSlot);
+    return;
   }
   const long long blk = slot / block_size;
   const int row = static_cast<int>(slot % block_size);
@@ -199,12 +134,11 @@ __global__ void __launch_bounds__(256) cache_int4_kernel(
 
 int cache_int4_launch(const void* key, const void* value, void* k_codes, void* v_codes,
                       float* k_scales, float* v_scales, const int64_t* slot_mapping,
-                      const int32_t* block_tables, int max_blocks_per_seq,
-                      const int32_t* context_lens, int count, int num_blocks, int num_kv_heads,
-                      int head_dim, int block_size, bool bf16, unsigned* err, cudaStream_t stream) {
-  if (count == 0) return 0;
+                      int num_tokens, int num_blocks, int num_kv_heads, int head_dim,
+                      int block_size, bool bf16, unsigned* err, cudaStream_t stream) {
+  if (num_tokens == 0) return 0;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(count);
+  cfg.gridDim = dim3(num_tokens);
   cfg.blockDim = dim3(256);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -215,11 +149,10 @@ int cache_int4_launch(const void* key, const void* value, void* k_codes, void* v
   auto* kc = static_cast<uint8_t*>(k_codes);
   auto* vc = static_cast<uint8_t*>(v_codes);
   cudaError_t e = cudaErrorInvalidValue;
-#define PA_INT4_CASE(TT, DD)                                                                   \
-  e = cudaLaunchKernelEx(&cfg, cache_int4_kernel<TT, DD>, static_cast<const TT*>(key),         \
+#define PA_INT4_CASE(TT, DD)                                                                      \
+  e = cudaLaunchKernelEx(&cfg, cache_int4_kernel<TT, DD>, static_cast<const TT*>(key),            \
                          static_cast<const TT*>(value), kc, vc, k_scales, v_scales, slot_mapping, \
-                         block_tables, max_blocks_per_seq, context_lens, num_blocks,           \
-                         num_kv_heads, block_size, err)
+                         num_blocks, num_kv_heads, block_size, err)
   if (head_dim == 128) {
     if (bf16) PA_INT4_CASE(__nv_bfloat16, 128); else PA_INT4_CASE(__half, 128);
   } else if (head_dim == 64) {
@@ -331,35 +264,6 @@ int reshape_and_cache_fp8_launch(const void* key, const void* value, void* k_cac
                                 static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
                                 slot_mapping, slots, num_kv_heads, head_dim / 16, block_size,
                                 k_scale, v_scale, err);
-  return e == cudaSuccess ? 0 : -3;
-}
-
-int append_newest_fp8_launch(const void* key, const void* value, void* k_cache, void* v_cache,
-                             const int32_t* block_tables, int max_blocks_per_seq,
-                             const int32_t* context_lens, int num_seqs, int num_blocks,
-                             int num_kv_heads, int head_dim, int block_size, float k_scale,
-                             float v_scale, bool bf16, cudaStream_t stream) {
-  if (num_seqs == 0) return 0;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(num_seqs);
-  cfg.blockDim = dim3(128);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const cudaError_t e =
-      bf16 ? cudaLaunchKernelEx(&cfg, append_newest_fp8_kernel<__nv_bfloat16>,
-                                static_cast<const uint4*>(key), static_cast<const uint4*>(value),
-                                static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
-                                block_tables, max_blocks_per_seq, context_lens, num_blocks,
-                                num_kv_heads, head_dim / 16, block_size, k_scale, v_scale)
-           : cudaLaunchKernelEx(&cfg, append_newest_fp8_kernel<__half>,
-                                static_cast<const uint4*>(key), static_cast<const uint4*>(value),
-                                static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
-                                block_tables, max_blocks_per_seq, context_lens, num_blocks,
-                                num_kv_heads, head_dim / 16, block_size, k_scale, v_scale);
   return e == cudaSuccess ? 0 : -3;
 }
 

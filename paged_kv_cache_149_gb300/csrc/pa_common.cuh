@@ -197,4 +197,41 @@ __device__ __forceinline__ uint4 quantize16_e4m3(const uint4& a, const uint4& b,
   return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
+// INT4 quantisation of one row of D values spread over a warp, lane l holding values
+// (D/32) l .. (D/32) l + D/32 - 1, shared by the cache-write kernel and the fused decode
+// step so that both produce the same codes: s = max |x| / 7 (IEEE float32), c = x / s
+// rounded half to even and clamped to [-7, 7] (0 for an all-zero row), nibble u = c + 8,
+// this lane's nibbles packed low first.  Returns the packed nibbles; s in `scale`.
+template <int D>
+__device__ __forceinline__ uint32_t int4_quantize_lane(const float (&x)[D / 32], float& scale) {
+  constexpr int PER = D / 32;
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float s = __fdiv_rn(amax, 7.f);
+  uint32_t packed = 0;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const float c = amax == 0.f ? 0.f : fminf(7.f, fmaxf(-7.f, rintf(__fdiv_rn(x[i], s))));
+    packed |= static_cast<uint32_t>(static_cast<int>(c) + 8) << (4 * i);
+  }
+  scale = s;
+  return packed;
+}
+
+// This lane's D/32 values of a 16-bit row at `src` (lane l: values (D/32) l ..).
+template <typename T, int D>
+__device__ __forceinline__ void int4_row_values(const T* src, int lane, float (&x)[D / 32]) {
+  if constexpr (D / 32 == 4) {
+    const uint2 w = *reinterpret_cast<const uint2*>(src + 4 * lane);
+    const float2 a = unpack2<T>(w.x), b = unpack2<T>(w.y);
+    x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+  } else {
+    const float2 a = unpack2<T>(*reinterpret_cast<const uint32_t*>(src + 2 * lane));
+    x[0] = a.x; x[1] = a.y;
+  }
+}
+
 }  // namespace pa

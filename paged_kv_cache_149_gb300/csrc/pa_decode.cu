@@ -74,6 +74,8 @@ int decode_launch(const DecodeArgs& a, int grid, cudaStream_t stream) {
   // FP8 blocks: scores are k_scale * <q, codes>, outputs v_scale * (weighted codes)
   p.scale_log2 = a.scale * (a.kv_fp8 ? a.k_scale : 1.f) * decode::kLog2e;
   p.out_scale = a.kv_fp8 ? a.v_scale : 1.f;
+  p.k_quant = a.k_scale;
+  p.v_quant = a.v_scale;
   // INT4 blocks: a scale per row, applied in the kernel
   p.k_scales = static_cast<const float*>(a.k_scales);
   p.v_scales = static_cast<const float*>(a.v_scales);

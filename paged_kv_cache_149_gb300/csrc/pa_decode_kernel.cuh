@@ -100,8 +100,9 @@ struct Params {
   const uint8_t* q;
   const uint8_t* k_cache;
   const uint8_t* v_cache;
-  // Fused cache write (pa_decode_append), else null: the newest token of each sequence,
-  // [n][Hkv][D].  Its row is attended from here and stored at position ctx - 1.
+  // Fused cache write (pa_decode_append*), else null: the newest token of each sequence,
+  // [n][Hkv][D] 16-bit.  Its row is attended from here (quantised first for FP8 / INT4
+  // blocks) and stored at position ctx - 1.
   const uint8_t* key_new;
   const uint8_t* value_new;
   const int32_t* block_tables;
@@ -114,6 +115,7 @@ struct Params {
   int seg_cost;    // stage units charged per family on top of its stages
   float scale_log2;
   float out_scale;  // FP8 blocks: v_scale, applied to every output row (else 1)
+  float k_quant, v_quant;  // FP8 blocks: k_scale, v_scale for the fused step's newest rows
   // INT4 blocks: float32 scale of each cached row, [num_blocks][Hkv][B] (else null)
   const float* k_scales;
   const float* v_scales;
@@ -639,6 +641,8 @@ __device__ bool merge_staged(const Params& p, int pi, const CutPiece& job0, cons
 template <int D, int KV>
 struct Smem {
   uint8_t ring[kWarps][Geo<D, KV>::kSlots][Geo<D, KV>::kStageBytes];  // 1024-byte aligned
+  // quantised blocks, fused step: the newest token's 16-bit K and V rows, per ring slot
+  uint8_t newrow[kWarps][Geo<D, KV>::kSlots][KV == kKv16 ? 16 : 4 * D];
   float xo[kWarps][4][D];  // per-warp O rows, 4 heads per exchange round
   float xm[kWarps][kMaxHeads], xl[kWarps][kMaxHeads];
   long long scan[kWarps];
@@ -743,7 +747,7 @@ __device__ __forceinline__ bool next_busy_fam(Fam f, int pi, long long w0, long 
 // KV = kKvInt4: K/V blocks hold INT4 codes with a float32 scale per row: a token's K scale
 // multiplies its scores, its V scale its weights in P V.  Both quantised formats run the
 // MMAs in f16 on values widened exactly, with 32-token stages and the permuted d order of
-// O (drow).  The fused cache write (key_new) exists for 16-bit blocks only.
+// O (drow).  The fused step (key_new) quantises the newest rows in the kernel.
 template <int D, int NTH, typename T, int KV>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ Params p) {
   constexpr bool F8 = KV == kKvFp8;
@@ -926,6 +930,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
           }
         }
         }
+        if constexpr (QK) {
+          // fused step: the newest token's 16-bit K and V rows into this slot's scratch
+          // (quantised when the stage is computed)
+          constexpr int CR = D / 8;  // 16-byte chunks of a 16-bit row
+          if (p.key_new && nxt.last && lane < 2 * CR) {
+            const int isv = lane >= CR ? 1 : 0, c = lane % CR;
+            const size_t nsrc = ((static_cast<size_t>(nxt.s) * p.num_kv_heads + nxt.kvh) * D + c * 8) * 2;
+            cp_async16(smem_addr(sm.newrow[warp][slot]) + isv * 2 * D + 16 * c,
+                       (isv ? p.value_new : p.key_new) + nsrc, 16u);
+          }
+        }
         if constexpr (I4) {
           // the rows' scales: lanes 0-7 copy K's, 8-15 V's, four tokens (16 bytes) each; a
           // token past the context gets scale 0 (its codes are zero-filled too)
@@ -1065,6 +1080,53 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       } else {
         const uint32_t kb = ring + slot * G_::kStageBytes;
         const uint32_t vb = kb + G_::kKBytes;
+        if constexpr (QK) {
+          if (p.key_new && j == f.ns - 1) {
+            // Fused step: the newest token (stage row nt_tok - 1) is quantised from the
+            // step's input with the cache-write arithmetic; the codes (and INT4 scales)
+            // replace the stage row and go to the cache slot at position ctx - 1.  No other
+            // reader of that slot exists in the call.
+            const int t = f.ctx - 1, nr = nt_tok - 1;
+            const int blk = __ldg(p.block_tables + static_cast<size_t>(f.s) * p.max_blocks_per_seq +
+                                  (t >> p.log2_block));
+            const size_t grow = (static_cast<size_t>(blk) * p.num_kv_heads + ph.kvh) * p.block_size +
+                                (t & (p.block_size - 1));
+            const uint8_t* nrow = sm.newrow[warp][slot];
+            uint8_t* stage = sm.ring[warp][slot];
+            if constexpr (F8) {
+              constexpr int CK = D / 16;  // 16-code chunks of a row
+              if (lane < 2 * CK) {
+                const int isv = lane >= CK ? 1 : 0, c = lane % CK;
+                const uint4* src = reinterpret_cast<const uint4*>(nrow + isv * 2 * D + 32 * c);
+                const uint4 codes = quantize16_e4m3<T>(src[0], src[1], isv ? p.v_quant : p.k_quant);
+                *reinterpret_cast<uint4*>(stage + isv * G_::kKBytes + swz8<D>(nr, c)) = codes;
+                reinterpret_cast<uint4*>(const_cast<uint8_t*>(isv ? p.v_cache : p.k_cache))[grow * CK + c] = codes;
+              }
+            } else {
+#pragma unroll
+              for (int isv = 0; isv < 2; ++isv) {
+                float x[D / 32];
+                int4_row_values<T, D>(reinterpret_cast<const T*>(nrow + isv * 2 * D), lane, x);
+                float sc;
+                const uint32_t packed = int4_quantize_lane<D>(x, sc);
+                uint8_t* gcodes = const_cast<uint8_t*>(isv ? p.v_cache : p.k_cache) + grow * (D / 2);
+                if constexpr (D == 128) {
+                  *reinterpret_cast<uint16_t*>(stage + isv * G_::kKBytes + swz4<D>(nr, lane >> 3) +
+                                               2 * (lane & 7)) = static_cast<uint16_t>(packed);
+                  reinterpret_cast<uint16_t*>(gcodes)[lane] = static_cast<uint16_t>(packed);
+                } else {
+                  stage[isv * G_::kKBytes + swz4<D>(nr, lane >> 4) + (lane & 15)] = static_cast<uint8_t>(packed);
+                  gcodes[lane] = static_cast<uint8_t>(packed);
+                }
+                if (lane == 0) {
+                  *reinterpret_cast<float*>(stage + 2 * G_::kKBytes + isv * G_::kScaleBytes + 4 * nr) = sc;
+                  const_cast<float*>(isv ? p.v_scales : p.k_scales)[grow] = sc;
+                }
+              }
+            }
+            __syncwarp();  // the stage row is rewritten before any lane reads it
+          }
+        }
         // ---- S^T = K Q^T: rows = the stage's tokens (U m-tiles of 16), columns = heads ----
         float sacc[U][NTH][4], sodd[U][NTH][4];
 #pragma unroll

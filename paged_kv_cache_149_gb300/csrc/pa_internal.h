@@ -69,18 +69,11 @@ int reshape_and_cache_fp8_launch(const void* key, const void* value, void* k_cac
                                  int num_blocks, int num_kv_heads, int head_dim, int block_size,
                                  float k_scale, float v_scale, bool bf16, unsigned* err,
                                  cudaStream_t stream);
-int append_newest_fp8_launch(const void* key, const void* value, void* k_cache, void* v_cache,
-                             const int32_t* block_tables, int max_blocks_per_seq,
-                             const int32_t* context_lens, int num_seqs, int num_blocks,
-                             int num_kv_heads, int head_dim, int block_size, float k_scale,
-                             float v_scale, bool bf16, cudaStream_t stream);
-// INT4 cache write: `count` rows' tokens through slot_mapping (null: the newest token of
-// each of `count` sequences through the table, position context_lens[s] - 1).
+// INT4 cache write of num_tokens rows' tokens through slot_mapping.
 int cache_int4_launch(const void* key, const void* value, void* k_codes, void* v_codes,
                       float* k_scales, float* v_scales, const int64_t* slot_mapping,
-                      const int32_t* block_tables, int max_blocks_per_seq,
-                      const int32_t* context_lens, int count, int num_blocks, int num_kv_heads,
-                      int head_dim, int block_size, bool bf16, unsigned* err, cudaStream_t stream);
+                      int num_tokens, int num_blocks, int num_kv_heads, int head_dim,
+                      int block_size, bool bf16, unsigned* err, cudaStream_t stream);
 int swap_blocks_launch(const void* src_k, const void* src_v, void* dst_k, void* dst_v,
                        const int32_t* block_mapping, int num_pairs, int src_num_blocks,
                        int dst_num_blocks, int num_kv_heads, int row_bytes, int block_size,
