@@ -196,6 +196,75 @@ def build_batches(wl, device, rotate):
     return k_cache, v_cache, batches
 
 
+E2E_METHOD = ("each step: its inputs (q, tables, lengths, newest K/V rows) copied from one "
+              "pinned host buffer, the public pa_decode_append* call, its output copied to "
+              "pinned host memory; steps are independent batches, so a copy stream overlaps "
+              "the neighbouring steps' copies with the kernel (two device staging slots)")
+
+
+def pipelined_e2e(batches, names, launch, out_like, device, steps, warmup):
+    """Decode steps end to end from pinned host memory: every step copies its inputs
+    (`names` of its batch, packed into one pinned staging buffer, so one copy a step) to
+    the device, runs `launch(dev_inputs, dev_out, stream)` and reads its output back.
+    Consecutive steps are independent batches, so the copies overlap the neighbouring
+    steps' kernels: two device staging slots; a copy stream reads step i's output back and
+    then uploads step i + 2's inputs (slot i % 2 is free once kernel i has run); kernel i
+    waits for its upload.  Returns (ms per step, H2D bytes per step, D2H bytes per step)."""
+    import torch
+
+    align = 256
+    layout, off = {}, 0
+    for k in names:
+        t = batches[0][k]
+        layout[k] = (off, t.shape, t.dtype, t.numel() * t.element_size())
+        off += -(-layout[k][3] // align) * align
+    host = []
+    for b in batches:
+        h = torch.empty(off, dtype=torch.uint8).pin_memory()
+        for k in names:
+            o, _, _, nb = layout[k]
+            h[o:o + nb].copy_(b[k].contiguous().view(-1).view(torch.uint8).cpu())
+        host.append(h)
+    dev = [torch.empty(off, dtype=torch.uint8, device=device) for _ in range(2)]
+    views = [{k: d[o:o + nb].view(dt).view(shape) for k, (o, shape, dt, nb) in layout.items()}
+             for d in dev]
+    outs = [torch.empty_like(out_like) for _ in range(2)]
+    host_out = [torch.empty(out_like.shape, dtype=out_like.dtype).pin_memory() for _ in range(2)]
+    comp = torch.cuda.Stream(device)
+    copy = torch.cuda.Stream(device)
+    nrot = len(batches)
+
+    def run(n):
+        up = [torch.cuda.Event() for _ in range(n)]
+        done = [torch.cuda.Event() for _ in range(n)]
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(copy)
+        comp.wait_event(start)
+        for i in range(min(2, n)):
+            with torch.cuda.stream(copy):
+                dev[i % 2].copy_(host[i % nrot], non_blocking=True)
+            up[i].record(copy)
+        for i in range(n):
+            comp.wait_event(up[i])
+            launch(views[i % 2], outs[i % 2], comp)
+            done[i].record(comp)
+            copy.wait_event(done[i])
+            with torch.cuda.stream(copy):
+                host_out[i % 2].copy_(outs[i % 2], non_blocking=True)
+                if i + 2 < n:
+                    dev[i % 2].copy_(host[(i + 2) % nrot], non_blocking=True)
+            if i + 2 < n:
+                up[i + 2].record(copy)
+        end.record(copy)
+        torch.cuda.synchronize(device)
+        return start.elapsed_time(end) / n
+
+    run(max(3, warmup))
+    ms = run(max(1, min(steps, 2000)))
+    d2h = out_like.numel() * out_like.element_size()
+    return ms, sum(layout[k][3] for k in names), d2h
+
+
 def run_gpu(args, rank, world, local_rank):
     import numpy as np
     import torch
@@ -277,36 +346,12 @@ def run_gpu(args, rank, world, local_rank):
     two_calls_ms = ev[4].elapsed_time(ev[5]) / K
 
     # end to end through the binding with host buffers: inputs from pinned host memory
-    # every step, the output read back every step
-    names = ("q", "tables", "ctx", "key", "value")
-    host_in = [{k: b[k].cpu().pin_memory() for k in names} for b in batches]
-    host_out = torch.empty(batches[0]["out"].shape, dtype=batches[0]["out"].dtype).pin_memory()
-    dev_in = {k: torch.empty_like(batches[0][k]) for k in names}
-    dev_out = torch.empty_like(batches[0]["out"])
-    h2d = sum(v.numel() * v.element_size() for v in host_in[0].values())
-    d2h = host_out.numel() * host_out.element_size()
-
-    def e2e_step(i):
-        with torch.cuda.stream(stream):
-            for k, v in host_in[i % ROTATE].items():
-                dev_in[k].copy_(v, non_blocking=True)
-            pa.decode_append(dev_in["q"], dev_in["key"], dev_in["value"], k_cache, v_cache,
-                             dev_in["tables"], dev_in["ctx"], wl.scale, out=dev_out,
-                             workspace=ws, stream=stream)
-            host_out.copy_(dev_out, non_blocking=True)
-
-    for i in range(max(3, args.warmup)):
-        e2e_step(i)
-    torch.cuda.synchronize(device)
-    ke = max(1, min(K, 2000))
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(ke):
-        e2e_step(i)
-    e1.record(stream)
-    torch.cuda.synchronize(device)
-    e2e_ms = e0.elapsed_time(e1) / ke
+    # every step, the output read back every step (copies pipelined with the kernels)
+    def e2e_launch(d, out, st):
+        pa.decode_append(d["q"], d["key"], d["value"], k_cache, v_cache, d["tables"], d["ctx"],
+                         wl.scale, out=out, workspace=ws, stream=st)
+    e2e_ms, h2d, d2h = pipelined_e2e(batches, ("q", "tables", "ctx", "key", "value"), e2e_launch,
+                                     batches[0]["out"], device, K, args.warmup)
     return {"wl": wl, "total_ms": total_ms, "decode_ms": decode_ms, "e2e_ms": e2e_ms,
             "two_calls_ms": two_calls_ms,
             "h2d": h2d, "d2h": d2h, "clocks": clocks, "flags": flags}
@@ -1299,34 +1344,21 @@ def run_gpu_fp8(args, rank, world, local_rank):
     t1 = time.time()
     clocks = sampler.stop(t0, t1) if sampler else None
     flags = pa.get_device_error(stream=stream)
-    names = ("q", "tables", "ctx", "key", "value", "slots")
-    host_in = [{k: b[k].cpu().pin_memory() for k in names} for b in batches]
-    host_out = torch.empty(batches[0]["out"].shape, dtype=dt).pin_memory()
-    dev = {k: torch.empty_like(batches[0][k]) for k in names}
-    dev["out"] = torch.empty_like(batches[0]["out"])
-
-    def e2e_step(i):
-        with torch.cuda.stream(stream):
-            for k, v in host_in[i % ROTATE].items():
-                dev[k].copy_(v, non_blocking=True)
-        step(i, dev)
-        with torch.cuda.stream(stream):
-            host_out.copy_(dev["out"], non_blocking=True)
-    for i in range(3):
-        e2e_step(i)
-    torch.cuda.synchronize(device)
-    ke = max(1, min(K, 2000))
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(ke):
-        e2e_step(i)
-    e1.record(stream)
-    torch.cuda.synchronize(device)
-    flags |= pa.get_device_error(stream=stream)
+    # end to end with host buffers: every step's inputs from pinned host memory, its
+    # output read back (copies pipelined with the kernels)
+    def e2e_launch(d, out, st):
+        if fmt == "fp8":
+            pa.decode_append_fp8(d["q"], d["key"], d["value"], k8, v8, d["tables"], d["ctx"],
+                                 wl.scale, ks, vs, out=out, workspace=ws, stream=st)
+        else:
+            pa.decode_append_int4(d["q"], d["key"], d["value"], k8, v8, k4s, v4s, d["tables"],
+                                  d["ctx"], wl.scale, out=out, workspace=ws, stream=st)
+    e2e_ms, h2d, d2h = pipelined_e2e(batches, ("q", "tables", "ctx", "key", "value"), e2e_launch,
+                                     batches[0]["out"], device, K, args.warmup)
+    flags |= pa.get_device_error()
     return {"wl": wl, "total_ms": ev[0].elapsed_time(ev[1]), "decode_ms": ev[2].elapsed_time(ev[3]) / K,
-            "two_calls_ms": ev[4].elapsed_time(ev[5]) / K, "e2e_ms": e0.elapsed_time(e1) / ke,
-            "h2d": sum(v.numel() * v.element_size() for v in host_in[0].values()),
-            "d2h": host_out.numel() * host_out.element_size(), "clocks": clocks, "flags": flags}
+            "two_calls_ms": ev[4].elapsed_time(ev[5]) / K, "e2e_ms": e2e_ms, "h2d": h2d, "d2h": d2h,
+            "clocks": clocks, "flags": flags}
 
 
 def oracle_fp8_sample(name, budget_s):
@@ -1464,7 +1496,7 @@ def fp8_line(args, res, world):
                       "whole sequences of the batch"},
         "e2e": {"value": round(world * (dec_b + resh_b) / (res["e2e_ms"] / 1e3) / 1e9, 1),
                 "unit": "GB/s", "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
-                "us_per_step": round(1e3 * res["e2e_ms"], 2)},
+                "us_per_step": round(1e3 * res["e2e_ms"], 2), "method": E2E_METHOD},
         "clocks": res["clocks"],
         "gpu_launches": args.steps,
         "device_error_flags": res["flags"],
@@ -1609,6 +1641,7 @@ def main(argv=None, runner=None, backend="nccl"):
             "h2d_bytes_per_step": res["h2d"],
             "d2h_bytes_per_step": res["d2h"],
             "us_per_step": round(1e3 * res["e2e_ms"], 2),
+            "method": E2E_METHOD,
         },
         "clocks": res["clocks"],
         # timed: steps (1 kernel each), decode alone (1 each), two-call steps (2 each)
