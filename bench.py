@@ -196,20 +196,20 @@ def build_batches(wl, device, rotate):
     return k_cache, v_cache, batches
 
 
-E2E_METHOD = ("each step: its inputs (q, tables, lengths, newest K/V rows) copied from one "
-              "pinned host buffer, the public pa_decode_append* call, its output copied to "
-              "pinned host memory; steps are independent batches, so a copy stream overlaps "
-              "the neighbouring steps' copies with the kernel (two device staging slots)")
+E2E_METHOD = ("each step: its inputs copied from one pinned host buffer, the public call, "
+              "its output copied to pinned host memory; steps are independent, so an upload "
+              "stream and a download stream overlap the neighbouring steps' copies with the "
+              "kernel (two device staging slots)")
 
 
 def pipelined_e2e(batches, names, launch, out_like, device, steps, warmup):
-    """Decode steps end to end from pinned host memory: every step copies its inputs
-    (`names` of its batch, packed into one pinned staging buffer, so one copy a step) to
-    the device, runs `launch(dev_inputs, dev_out, stream)` and reads its output back.
-    Consecutive steps are independent batches, so the copies overlap the neighbouring
-    steps' kernels: two device staging slots; a copy stream reads step i's output back and
-    then uploads step i + 2's inputs (slot i % 2 is free once kernel i has run); kernel i
-    waits for its upload.  Returns (ms per step, H2D bytes per step, D2H bytes per step)."""
+    """Steps end to end from pinned host memory: every step copies its inputs (`names` of
+    its batch, packed into one pinned staging buffer, so one upload a step) to the device,
+    runs `launch(dev_inputs, dev_out, stream)` and downloads its output.  Consecutive steps
+    are independent, so the copies overlap the neighbouring steps' kernels: two device
+    staging slots and two output slots; the upload of step i + 2 waits for kernel i (slot
+    i % 2 free), the download of step i for kernel i, and kernel i + 2 for that download
+    (its output slot).  Returns (ms per step, H2D bytes per step, D2H bytes per step)."""
     import torch
 
     align = 256
@@ -230,32 +230,38 @@ def pipelined_e2e(batches, names, launch, out_like, device, steps, warmup):
              for d in dev]
     outs = [torch.empty_like(out_like) for _ in range(2)]
     host_out = [torch.empty(out_like.shape, dtype=out_like.dtype).pin_memory() for _ in range(2)]
-    comp = torch.cuda.Stream(device)
-    copy = torch.cuda.Stream(device)
+    comp, up_s, down_s = (torch.cuda.Stream(device) for _ in range(3))
     nrot = len(batches)
 
     def run(n):
         up = [torch.cuda.Event() for _ in range(n)]
         done = [torch.cuda.Event() for _ in range(n)]
+        down = [torch.cuda.Event() for _ in range(n)]
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        start.record(copy)
-        comp.wait_event(start)
+        start.record(comp)
+        up_s.wait_event(start)
+        down_s.wait_event(start)
         for i in range(min(2, n)):
-            with torch.cuda.stream(copy):
+            with torch.cuda.stream(up_s):
                 dev[i % 2].copy_(host[i % nrot], non_blocking=True)
-            up[i].record(copy)
+            up[i].record(up_s)
         for i in range(n):
             comp.wait_event(up[i])
+            if i >= 2:
+                comp.wait_event(down[i - 2])
             launch(views[i % 2], outs[i % 2], comp)
             done[i].record(comp)
-            copy.wait_event(done[i])
-            with torch.cuda.stream(copy):
+            down_s.wait_event(done[i])
+            with torch.cuda.stream(down_s):
                 host_out[i % 2].copy_(outs[i % 2], non_blocking=True)
-                if i + 2 < n:
-                    dev[i % 2].copy_(host[(i + 2) % nrot], non_blocking=True)
+            down[i].record(down_s)
             if i + 2 < n:
-                up[i + 2].record(copy)
-        end.record(copy)
+                up_s.wait_event(done[i])
+                with torch.cuda.stream(up_s):
+                    dev[i % 2].copy_(host[(i + 2) % nrot], non_blocking=True)
+                up[i + 2].record(up_s)
+        comp.wait_event(down[n - 1])
+        end.record(comp)
         torch.cuda.synchronize(device)
         return start.elapsed_time(end) / n
 
@@ -536,34 +542,17 @@ def run_gpu_prefill(args, rank, world, local_rank):
     clocks = sampler.stop(t0, t1) if sampler else None
     flags = pa.get_device_error(stream=stream)
     total_ms = ev[0].elapsed_time(ev[1])
-    # end to end: q from pinned host memory, out read back, every pass
-    host_q = batches[0]["q"].cpu().pin_memory()
-    host_out = torch.empty_like(host_q).pin_memory()
-    dev_q = torch.empty_like(batches[0]["q"])
+    # end to end: q from pinned host memory, out read back, every pass (copies pipelined)
     b0 = batches[0]
 
-    def e2e_step():
-        with torch.cuda.stream(stream):
-            dev_q.copy_(host_q, non_blocking=True)
-            pa.prefill(dev_q, k_cache, v_cache, b0["tables"], b0["ctx"], qs, wl.scale, maxq,
-                       out=b0["out"], stream=stream)
-            host_out.copy_(b0["out"], non_blocking=True)
-
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize(device)
-    ke = max(1, min(K, 20))
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(ke):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize(device)
-    nbytes = host_q.numel() * host_q.element_size()
+    def e2e_launch(d, out, st):
+        pa.prefill(d["q"], k_cache, v_cache, b0["tables"], b0["ctx"], qs, wl.scale, maxq, out=out,
+                   stream=st)
+    e2e_ms, h2d, d2h = pipelined_e2e([b0], ("q",), e2e_launch, b0["out"], device, min(K, 50),
+                                     args.warmup)
     return {"wl": wl, "total_ms": total_ms, "decode_ms": total_ms / K,
-            "two_calls_ms": total_ms / K, "e2e_ms": e0.elapsed_time(e1) / ke,
-            "h2d": nbytes, "d2h": nbytes, "clocks": clocks, "flags": flags}
+            "two_calls_ms": total_ms / K, "e2e_ms": e2e_ms,
+            "h2d": h2d, "d2h": d2h, "clocks": clocks, "flags": flags}
 
 
 def oracle_prefill_sample(name, budget_s):
@@ -652,7 +641,7 @@ def prefill_line(args, res, world):
                       f"tokens of sequence 0 (a {cpu['tokens']}-token prompt)"},
         "e2e": {"value": round(world * flops / (res["e2e_ms"] / 1e3) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
-                "us_per_step": round(1e3 * res["e2e_ms"], 2)},
+                "us_per_step": round(1e3 * res["e2e_ms"], 2), "method": E2E_METHOD},
         "clocks": res["clocks"],
         "gpu_launches": args.steps,
         "device_error_flags": res["flags"],
