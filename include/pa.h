@@ -109,6 +109,14 @@ int pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void
  * split pieces, 16-byte aligned, owned by the caller, not read before it is written.
  * Concurrent pa_decode calls must not share a workspace.  Returns PA_ERR_WORKSPACE if
  * it is NULL or too small.  num_seqs == 0 is a no-op.
+ *
+ * Ordering: a launch is a programmatic dependent of the kernel before it in the stream.
+ * It reads context_lens and block_tables (to plan its work) while that kernel drains,
+ * and q, the caches and the workspace only after it has finished.  So block_tables and
+ * context_lens must not be written by the kernel immediately before it in the stream
+ * when that kernel lets its dependents start early (no kernel of this library writes
+ * them; a plain copy or a kernel without programmatic launch is always safe).  The same
+ * holds for every decode entry point below.
  */
 int pa_decode(const void* q, const void* k_cache, const void* v_cache,
               const int32_t* block_tables, int max_blocks_per_seq,

@@ -781,9 +781,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     return P == 1 ? (__any_sync(0xffffffffu, v) != 0) : bar_red_or(1 + pi, gthreads, v);
   };
 
-  // The kernel before this one in the stream (say the cache write) has finished and its
-  // writes are visible past this point; the next one may start launching.
-  pdl_wait_primary();
+  // The next kernel in the stream may start launching.  Everything up to the first copy
+  // reads only context_lens and block_tables (the share, the first family, the first
+  // stages' table entries), which no kernel of this library writes; it runs while the
+  // kernel before this one drains.  The wait comes before anything touches q, the caches
+  // or the workspace.
   pdl_launch_dependents();
 
   if (lane == 0) {
@@ -966,6 +968,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     }
     cp_async_commit();  // one group per call, empty or not
   };
+  // the kernel before this one (say the cache write) has finished and its writes are
+  // visible past this point
+  pdl_wait_primary();
 #pragma unroll
   for (int a = 0; a < G_::kAhead; ++a) issue_one();
 
