@@ -99,6 +99,13 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* map, int x
       : "memory");
 }
 
+// Bulk prefetch of [src, src + bytes) into L2 (a hint: no data moves to the SM, and a
+// later write by another kernel is seen by later reads).  src 16-byte aligned, bytes a
+// multiple of 16.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }

@@ -968,6 +968,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     }
     cp_async_commit();  // one group per call, empty or not
   };
+  // Warm L2 with the blocks of this warp's first kAhead stages (those tokens of its first
+  // pair) while the kernel before this one drains: one lane per block, one bulk prefetch
+  // per block's K rows and V rows (and INT4 scales) of the pair's kv head.
+  if (nxt_ok) {
+    const int j0 = nxt.t0 >> p.log2_block;
+    const int tl = min(p.max_ctx, min(__ldg(p.context_lens + nxt.s), nxt.t0 + G_::kAhead * ST)) - 1;
+    const int nbk = (tl >> p.log2_block) - j0 + 1;
+    if (lane < nbk) {
+      const int e = __ldg(p.block_tables + static_cast<size_t>(nxt.s) * p.max_blocks_per_seq + j0 + lane);
+      if (e >= 0 && e < p.num_blocks) {
+        const size_t row = (static_cast<size_t>(e) * p.num_kv_heads + nxt.kvh) * p.block_size;
+        const uint32_t bytes = static_cast<uint32_t>(p.block_size) * G_::kRowBytes;
+        prefetch_l2(p.k_cache + row * G_::kRowBytes, bytes);
+        prefetch_l2(p.v_cache + row * G_::kRowBytes, bytes);
+        if constexpr (I4) {
+          prefetch_l2(p.k_scales + row, 4u * p.block_size);
+          prefetch_l2(p.v_scales + row, 4u * p.block_size);
+        }
+      }
+    }
+  }
   // the kernel before this one (say the cache write) has finished and its writes are
   // visible past this point
   pdl_wait_primary();
