@@ -196,16 +196,18 @@ def build_batches(wl, device, rotate):
     return k_cache, v_cache, batches
 
 
-E2E_METHOD = ("each step: its inputs copied from one pinned host buffer, the public call, "
-              "its output copied to pinned host memory; steps are independent, so an upload "
-              "stream and a download stream overlap the neighbouring steps' copies with the "
-              "kernel (two device staging slots)")
+E2E_METHOD = ("each step: its inputs copied from one pinned host buffer, the public call "
+              "(decode steps: a Launch planned once per staging slot), its output copied to "
+              "pinned host memory; steps are independent, so an upload stream and a download "
+              "stream overlap the neighbouring steps' copies with the kernel (two device "
+              "staging slots)")
 
 
-def pipelined_e2e(batches, names, launch, out_like, device, steps, warmup):
+def pipelined_e2e(batches, names, make_launch, out_like, device, steps, warmup):
     """Steps end to end from pinned host memory: every step copies its inputs (`names` of
     its batch, packed into one pinned staging buffer, so one upload a step) to the device,
-    runs `launch(dev_inputs, dev_out, stream)` and downloads its output.  Consecutive steps
+    runs the step (`make_launch(dev_inputs, dev_out)` gives a callable taking the stream,
+    made once per staging slot) and downloads its output.  Consecutive steps
     are independent, so the copies overlap the neighbouring steps' kernels: two device
     staging slots and two output slots; the upload of step i + 2 waits for kernel i (slot
     i % 2 free), the download of step i for kernel i, and kernel i + 2 for that download
@@ -232,6 +234,7 @@ def pipelined_e2e(batches, names, launch, out_like, device, steps, warmup):
     host_out = [torch.empty(out_like.shape, dtype=out_like.dtype).pin_memory() for _ in range(2)]
     comp, up_s, down_s = (torch.cuda.Stream(device) for _ in range(3))
     nrot = len(batches)
+    launches = [make_launch(views[i], outs[i]) for i in range(2)]
 
     def run(n):
         up = [torch.cuda.Event() for _ in range(n)]
@@ -249,7 +252,7 @@ def pipelined_e2e(batches, names, launch, out_like, device, steps, warmup):
             comp.wait_event(up[i])
             if i >= 2:
                 comp.wait_event(down[i - 2])
-            launch(views[i % 2], outs[i % 2], comp)
+            launches[i % 2](comp)
             done[i].record(comp)
             down_s.wait_event(done[i])
             with torch.cuda.stream(down_s):
@@ -353,9 +356,9 @@ def run_gpu(args, rank, world, local_rank):
 
     # end to end through the binding with host buffers: inputs from pinned host memory
     # every step, the output read back every step (copies pipelined with the kernels)
-    def e2e_launch(d, out, st):
-        pa.decode_append(d["q"], d["key"], d["value"], k_cache, v_cache, d["tables"], d["ctx"],
-                         wl.scale, out=out, workspace=ws, stream=st)
+    def e2e_launch(d, out):
+        return pa.decode_append(d["q"], d["key"], d["value"], k_cache, v_cache, d["tables"],
+                                d["ctx"], wl.scale, out=out, workspace=ws, plan=True).run
     e2e_ms, h2d, d2h = pipelined_e2e(batches, ("q", "tables", "ctx", "key", "value"), e2e_launch,
                                      batches[0]["out"], device, K, args.warmup)
     return {"wl": wl, "total_ms": total_ms, "decode_ms": decode_ms, "e2e_ms": e2e_ms,
@@ -545,9 +548,9 @@ def run_gpu_prefill(args, rank, world, local_rank):
     # end to end: q from pinned host memory, out read back, every pass (copies pipelined)
     b0 = batches[0]
 
-    def e2e_launch(d, out, st):
-        pa.prefill(d["q"], k_cache, v_cache, b0["tables"], b0["ctx"], qs, wl.scale, maxq, out=out,
-                   stream=st)
+    def e2e_launch(d, out):
+        return lambda st: pa.prefill(d["q"], k_cache, v_cache, b0["tables"], b0["ctx"], qs, wl.scale,
+                                     maxq, out=out, stream=st)
     e2e_ms, h2d, d2h = pipelined_e2e([b0], ("q",), e2e_launch, b0["out"], device, min(K, 50),
                                      args.warmup)
     return {"wl": wl, "total_ms": total_ms, "decode_ms": total_ms / K,
@@ -1335,13 +1338,12 @@ def run_gpu_fp8(args, rank, world, local_rank):
     flags = pa.get_device_error(stream=stream)
     # end to end with host buffers: every step's inputs from pinned host memory, its
     # output read back (copies pipelined with the kernels)
-    def e2e_launch(d, out, st):
+    def e2e_launch(d, out):
         if fmt == "fp8":
-            pa.decode_append_fp8(d["q"], d["key"], d["value"], k8, v8, d["tables"], d["ctx"],
-                                 wl.scale, ks, vs, out=out, workspace=ws, stream=st)
-        else:
-            pa.decode_append_int4(d["q"], d["key"], d["value"], k8, v8, k4s, v4s, d["tables"],
-                                  d["ctx"], wl.scale, out=out, workspace=ws, stream=st)
+            return pa.decode_append_fp8(d["q"], d["key"], d["value"], k8, v8, d["tables"], d["ctx"],
+                                        wl.scale, ks, vs, out=out, workspace=ws, plan=True).run
+        return pa.decode_append_int4(d["q"], d["key"], d["value"], k8, v8, k4s, v4s, d["tables"],
+                                     d["ctx"], wl.scale, out=out, workspace=ws, plan=True).run
     e2e_ms, h2d, d2h = pipelined_e2e(batches, ("q", "tables", "ctx", "key", "value"), e2e_launch,
                                      batches[0]["out"], device, K, args.warmup)
     flags |= pa.get_device_error()

@@ -165,6 +165,25 @@ def _check(status, what):
     return status
 
 
+class Launch:
+    """A library call whose arguments were checked and marshalled once (``plan=True`` on
+    the decode step functions): ``run(stream)`` issues it again on ``stream`` over the
+    same buffers, whose contents may change between runs.  For serving loops that launch
+    the same step shape many times; the per-call cost is one foreign call."""
+
+    def __init__(self, name, args, out):
+        self._fn = getattr(lib(), name)
+        self._name = name
+        self._args = args
+        self.out = out
+
+    def run(self, stream):
+        st = self._fn(*self._args, stream.cuda_stream)
+        if st < 0:
+            _check(st, self._name)
+        return self.out
+
+
 # ----------------------------------------------------------------- device calls
 
 def _dtype_code(t):
@@ -259,11 +278,12 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=None, wor
 
 
 def decode_append(q, key_new, value_new, k_cache, v_cache, block_tables, context_lens, scale,
-                  out=None, workspace=None, stream=None):
+                  out=None, workspace=None, stream=None, plan=False):
     """One decode step in one kernel: writes each sequence's newest token (``key_new`` /
     ``value_new`` [num_seqs, num_kv_heads, head_dim], at position context_lens[s] - 1) into
     the caches and returns attention over contexts that include it.  Same results as
-    reshape_and_cache into those slots followed by decode."""
+    reshape_and_cache into those slots followed by decode.  plan=True returns a Launch
+    instead of launching."""
     import torch
     n, hq, d = q.shape
     nb, hkv, bs, d2 = k_cache.shape
@@ -279,14 +299,15 @@ def decode_append(q, key_new, value_new, k_cache, v_cache, block_tables, context
     _need(out.shape == q.shape and out.dtype == q.dtype, "out must match q")
     if workspace is None:
         workspace = make_workspace(hq, hkv, d, q.device)
-    st = lib().pa_decode_append(
-        _dev(q, "q"), _dev(key_new, "key_new"), _dev(value_new, "value_new"),
-        _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
-        _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
-        _dev(context_lens, "context_lens", torch.int32), n, hq, hkv, d, bs, nb, float(scale),
-        _dev(out, "out"), _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
-        _dtype_code(q), _stream_ptr(stream, q.device))
-    _check(st, "pa_decode_append")
+    args = (_dev(q, "q"), _dev(key_new, "key_new"), _dev(value_new, "value_new"),
+            _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+            _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+            _dev(context_lens, "context_lens", torch.int32), n, hq, hkv, d, bs, nb, float(scale),
+            _dev(out, "out"), _dev(workspace, "workspace"),
+            workspace.numel() * workspace.element_size(), _dtype_code(q))
+    if plan:
+        return Launch("pa_decode_append", args, out)
+    _check(lib().pa_decode_append(*args, _stream_ptr(stream, q.device)), "pa_decode_append")
     return out
 
 
@@ -340,10 +361,10 @@ def decode_fp8(q, k_cache, v_cache, block_tables, context_lens, scale, k_scale, 
 
 
 def decode_append_fp8(q, key_new, value_new, k_cache, v_cache, block_tables, context_lens,
-                      scale, k_scale, v_scale, out=None, workspace=None, stream=None):
+                      scale, k_scale, v_scale, out=None, workspace=None, stream=None, plan=False):
     """One FP8 decode step in one kernel: each sequence's newest K/V row is quantised into
     its slot at position ctx - 1 (read from the block tables) and attended (= bit for bit
-    reshape_and_cache_fp8 + decode_fp8)."""
+    reshape_and_cache_fp8 + decode_fp8).  plan=True returns a Launch instead of launching."""
     import torch
     n, hq, d = q.shape
     nb, hkv, bs, d2 = k_cache.shape
@@ -357,14 +378,15 @@ def decode_append_fp8(q, key_new, value_new, k_cache, v_cache, block_tables, con
     _need(out.shape == q.shape and out.dtype == q.dtype, "out must match q")
     if workspace is None:
         workspace = make_workspace(hq, hkv, d, q.device)
-    st = lib().pa_decode_append_fp8(
-        _dev(q, "q"), _dev(key_new, "key_new"), _dev(value_new, "value_new"),
-        _fp8_cache(k_cache, "k_cache"), _fp8_cache(v_cache, "v_cache"),
-        _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
-        _dev(context_lens, "context_lens", torch.int32), n, hq, hkv, d, bs, nb, float(scale),
-        float(k_scale), float(v_scale), _dev(out, "out"), _dev(workspace, "workspace"),
-        workspace.numel() * workspace.element_size(), _dtype_code(q), _stream_ptr(stream, q.device))
-    _check(st, "pa_decode_append_fp8")
+    args = (_dev(q, "q"), _dev(key_new, "key_new"), _dev(value_new, "value_new"),
+            _fp8_cache(k_cache, "k_cache"), _fp8_cache(v_cache, "v_cache"),
+            _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+            _dev(context_lens, "context_lens", torch.int32), n, hq, hkv, d, bs, nb, float(scale),
+            float(k_scale), float(v_scale), _dev(out, "out"), _dev(workspace, "workspace"),
+            workspace.numel() * workspace.element_size(), _dtype_code(q))
+    if plan:
+        return Launch("pa_decode_append_fp8", args, out)
+    _check(lib().pa_decode_append_fp8(*args, _stream_ptr(stream, q.device)), "pa_decode_append_fp8")
     return out
 
 
@@ -472,10 +494,10 @@ def decode_int4(q, k_codes, v_codes, k_scales, v_scales, block_tables, context_l
 
 
 def decode_append_int4(q, key_new, value_new, k_codes, v_codes, k_scales, v_scales, block_tables,
-                       context_lens, scale, out=None, workspace=None, stream=None):
+                       context_lens, scale, out=None, workspace=None, stream=None, plan=False):
     """One INT4 decode step in one kernel: each sequence's newest K/V row is quantised into
     its slot at position ctx - 1 and attended (= bit for bit reshape_and_cache_int4 +
-    decode_int4)."""
+    decode_int4).  plan=True returns a Launch instead of launching."""
     import torch
     n, hq, d = q.shape
     nb, hkv, bs, d2 = k_codes.shape
@@ -491,13 +513,14 @@ def decode_append_int4(q, key_new, value_new, k_codes, v_codes, k_scales, v_scal
     _need(out.shape == q.shape and out.dtype == q.dtype, "out must match q")
     if workspace is None:
         workspace = make_workspace(hq, hkv, d, q.device)
-    st = lib().pa_decode_append_int4(
-        _dev(q, "q"), _dev(key_new, "key_new"), _dev(value_new, "value_new"), kc, vc, ks, vs,
-        _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
-        _dev(context_lens, "context_lens", torch.int32), n, hq, hkv, d, bs, nb, float(scale),
-        _dev(out, "out"), _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
-        _dtype_code(q), _stream_ptr(stream, q.device))
-    _check(st, "pa_decode_append_int4")
+    args = (_dev(q, "q"), _dev(key_new, "key_new"), _dev(value_new, "value_new"), kc, vc, ks, vs,
+            _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+            _dev(context_lens, "context_lens", torch.int32), n, hq, hkv, d, bs, nb, float(scale),
+            _dev(out, "out"), _dev(workspace, "workspace"),
+            workspace.numel() * workspace.element_size(), _dtype_code(q))
+    if plan:
+        return Launch("pa_decode_append_int4", args, out)
+    _check(lib().pa_decode_append_int4(*args, _stream_ptr(stream, q.device)), "pa_decode_append_int4")
     return out
 
 

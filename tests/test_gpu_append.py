@@ -134,3 +134,44 @@ def test_missing_new_rows_is_an_argument_error():
         ctypes.c_float(wl.scale), torch.empty_like(gb.q).data_ptr(), ws.data_ptr(),
         ws.numel() * ws.element_size(), 0 if wl.dtype == "fp16" else 1, None)
     assert st == -1  # PA_ERR_ARG
+
+
+@pytest.mark.parametrize("fmt", ["16", "fp8", "int4"])
+def test_planned_launch_equals_the_call(fmt):
+    """A Launch planned once (plan=True) and run on a stream gives the same output and
+    caches as the plain call, for every block format."""
+    wl = workloads.llama31_8b(num_seqs=12)
+    kn, vn = (to_device(x, wl.dtype) for x in newest_rows(wl))
+    stream = torch.cuda.Stream()
+    results = []
+    for planned in (False, True):
+        if fmt == "16":
+            gb, _ = pre_step(wl)
+            caches = (gb.k_cache, gb.v_cache)
+            call = lambda **kw: pa.decode_append(gb.q, kn, vn, gb.k_cache, gb.v_cache, gb.tables,
+                                                 gb.ctx, wl.scale, **kw)
+        else:
+            from test_gpu_fp8 import Fp8Batch
+            from test_gpu_int4 import Int4Batch
+            gb = Fp8Batch(wl, 0.0123, 0.0234) if fmt == "fp8" else Int4Batch(wl)
+            if fmt == "fp8":
+                caches = (gb.k8, gb.v8)
+                call = lambda **kw: pa.decode_append_fp8(gb.q, kn, vn, gb.k8, gb.v8, gb.tables,
+                                                         gb.ctx, wl.scale, 0.0123, 0.0234, **kw)
+            else:
+                caches = (gb.kc, gb.vc, gb.ks.view(torch.int32), gb.vs.view(torch.int32))
+                call = lambda **kw: pa.decode_append_int4(gb.q, kn, vn, gb.kc, gb.vc, gb.ks, gb.vs,
+                                                          gb.tables, gb.ctx, wl.scale, **kw)
+        out = torch.empty((wl.num_seqs, wl.num_q_heads, wl.head_dim), dtype=kn.dtype, device="cuda")
+        torch.cuda.synchronize()  # the caches were built on the default stream
+        if planned:
+            launch = call(out=out, plan=True)
+            launch.run(stream)
+            launch.run(stream)  # a second run over the same buffers gives the same result
+        else:
+            call(out=out, stream=stream)
+        stream.synchronize()
+        assert device_error() == 0
+        results.append([to_bits(out)] + [c.contiguous().view(torch.uint8).cpu().numpy() for c in caches])
+    for a, b in zip(*results):
+        np.testing.assert_array_equal(a, b)
