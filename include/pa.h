@@ -99,11 +99,12 @@ int pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void
  * (daiw.org "Paged Attention", section 定义, Attention 内核; chenyuan1125, section
  * 页表真正解开的…).  Accumulation is fp32; the output is rounded to nearest-even.
  *
- * Work is split into equal shares of 16-token K/V stages, one share per SM, so a long
- * sequence may be cut into pieces; the SM holding a pair's first piece merges them with
- * a log-sum-exp reduction (split-KV) inside the same kernel.  Cut points depend only on
- * logical token positions and the batch's context lengths, never on where blocks sit,
- * so permuting physical blocks (and the table with them) gives bit-identical output.
+ * Work is split into equal shares of K/V stages (16 tokens; 32 over FP8 / INT4 blocks),
+ * one share per SM, so a long sequence may be cut into pieces; the SM that finishes a
+ * pair's last outstanding piece merges them with a log-sum-exp reduction (split-KV)
+ * inside the same kernel, in a fixed order.  Cut points depend only on logical token
+ * positions and the batch's context lengths, never on where blocks sit, so permuting
+ * physical blocks (and the table with them) gives bit-identical output.
  *
  * workspace: device scratch of at least pa_decode_workspace_size(...) bytes for the
  * split pieces, 16-byte aligned, owned by the caller, not read before it is written.

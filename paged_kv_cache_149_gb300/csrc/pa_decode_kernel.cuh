@@ -13,9 +13,10 @@
 // * A "pair" is one kv head (or a chunk of up to 16 of its query heads) of one sequence.
 //   The pairs of a sequence are taken in groups of gs (the largest power of two <= 8 that
 //   divides the pair count); a "family" is one sequence's group.  A family's work is
-//   ns(s) units of 16 tokens x gs pairs (a "stage" is one unit of one pair: 16 K rows and
-//   16 V rows), plus a fixed charge.  The batch's stages, in (family, unit, pair) order,
-//   are cut into gridDim.x equal contiguous shares, one per persistent CTA (one per SM).
+//   ns(s) units of 16 tokens (32 over FP8 / INT4 blocks) x gs pairs (a "stage" is one
+//   unit of one pair: its K rows and V rows), plus a fixed charge.  The batch's stages, in
+//   (family, unit, pair) order, are cut into gridDim.x equal contiguous shares, one per
+//   persistent CTA (one per SM).
 // * Warp w of a CTA works on pair w / P of every family (P = 8 / gs warps per pair, each
 //   taking every P-th unit).  With 8 or more kv heads (gs = 8) a warp owns one kv head
 //   outright: it streams its pair's stages straight across family boundaries and never
@@ -29,10 +30,13 @@
 //   per SM on GB300.  Rows past the context are zero-filled by the copy itself (source
 //   size 0) and never read.
 // * Math per stage on warp-level tensor cores (m16n8k16, fp32 accumulate) with the pair's
-//   query heads as the N = 8 (or 16) columns: S^T = K Q^T (rows = the stage's 16 tokens),
-//   then O^T += V^T P^T (rows = d) with P = 2^(S - m) rounded to the input type and moved
-//   into B-fragment layout by an in-register transpose (movmatrix); online softmax with a
-//   running max and sum per head.  The swizzle makes every ldmatrix conflict-free.
+//   query heads as the N = 8 (or 16) columns: S^T = K Q^T (rows = the stage's tokens, 16
+//   per m-tile), then O^T += V^T P^T (rows = d) with P = 2^(S - m) rounded to the MMA type
+//   and moved into B-fragment layout by an in-register transpose (movmatrix); online
+//   softmax with a running max and sum per head.  The swizzles make every fragment load
+//   conflict-free.  FP8 and INT4 codes are widened to f16 exactly in registers.
+// * Whole stages (every row inside the context, no pass split between blocks) copy from
+//   one base address per block with constant offsets; others take a per-row path.
 // * A pair cut between CTAs (split-KV) leaves one partial softmax state (O, m, l) per
 //   piece in the workspace.  When a CTA has streamed its whole share (no copies left in
 //   flight, so a fence is cheap), it counts its pieces in on a per-pair counter; the CTA
@@ -41,8 +45,10 @@
 //   section 它和 FlashAttention…, names as FlashAttention's technique).  No CTA ever waits
 //   for another.  Cut points depend on logical positions and context lengths only, and
 //   the merge order is fixed, so permuting physical blocks gives bit-identical output.
-// * Launched as a programmatic dependent of the kernel before it in the stream: the grid
-//   is resident while that kernel drains and starts at griddepcontrol.wait.
+// * Launched as a programmatic dependent of the kernel before it in the stream: while
+//   that kernel drains, the grid plans its shares from the context lengths and block
+//   tables and warms L2 with each warp's first blocks; q, the caches and the workspace
+//   are touched only after griddepcontrol.wait.
 #include <cuda_runtime.h>
 
 #include <atomic>
