@@ -68,6 +68,22 @@ def step_bytes(wl):
     return decode, reshape, padded_kv
 
 
+def decode_config(wl, world):
+    """The `config` of a 16-bit decode line (the native arm's and the reference arm's)."""
+    dec_b = step_bytes(wl)[0]
+    return {
+        "workload": (f"{wl.name}: {wl.num_seqs} seqs, ctx {int(wl.context_lens.min())}..."
+                     f"{int(wl.context_lens.max())} (sum {int(wl.context_lens.sum())}), "
+                     f"{wl.num_q_heads} q / {wl.num_kv_heads} kv heads, head_dim {wl.head_dim}, "
+                     f"block_size {wl.block_size}, pool {rotation_pool(wl, ROTATE)[0]} blocks; step = "
+                     f"cache write of {wl.num_seqs} new tokens + paged decode, one kernel "
+                     f"(pa_decode_append)"),
+        "l2": f"each batch's K/V ({dec_b / 1e6:.0f} MB) exceeds L2; {ROTATE} batches in "
+              "disjoint blocks rotated every step",
+        "parallelism": f"replicas x{world}",
+    }
+
+
 def measured_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -1583,17 +1599,7 @@ def main(argv=None, runner=None, backend="nccl"):
         "vs_baseline": None,
         "dtype": wl.dtype,
         "data": "synthetic (seeded normals; no dataset or weights)",
-        "config": {
-            "workload": (f"{wl.name}: {wl.num_seqs} seqs, ctx {int(wl.context_lens.min())}..."
-                         f"{int(wl.context_lens.max())} (sum {int(wl.context_lens.sum())}), "
-                         f"{wl.num_q_heads} q / {wl.num_kv_heads} kv heads, head_dim {wl.head_dim}, "
-                         f"block_size {wl.block_size}, pool {rotation_pool(wl, ROTATE)[0]} blocks; step = "
-                         f"cache write of {wl.num_seqs} new tokens + paged decode, one kernel "
-                         f"(pa_decode_append)"),
-            "l2": f"each batch's K/V ({dec_b / 1e6:.0f} MB) exceeds L2; {ROTATE} batches in "
-                  "disjoint blocks rotated every step",
-            "parallelism": f"replicas x{world}",
-        },
+        "config": decode_config(wl, world),
         "roofline": {
             "bound": "hbm",
             "kernel": "decode_kernel (pa_decode: persistent paged decode with in-kernel split-KV merge)",
@@ -1649,7 +1655,10 @@ def reference_arm(args):
     """The oracle as it stands, timed on the host cores: each step decodes a bounded
     sample of the same batch."""
     import workloads
-    wl = workloads.RECIPES[args.workload]()
+    wl = workloads.RECIPES.get(args.workload, lambda: None)()
+    if not isinstance(wl, workloads.DecodeWorkload) or isinstance(wl, workloads.PrefillWorkload):
+        raise SystemExit(f"--impl reference times the 16-bit decode oracle; {args.workload!r} "
+                         "is not a 16-bit decode workload")
     # calibrate: the per-sequence cost sets how many sequences fit in one step
     cal = oracle_sample(args.workload, 1.0, 4)
     per_seq = cal["seconds"] / max(1, cal["seqs"])
@@ -1668,7 +1677,7 @@ def reference_arm(args):
         "ms_per_step": round(1e3 * secs / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "impl": "reference",
-        "config": {"workload": f"{wl.name} (see the native arm's line)"},
+        "config": decode_config(wl, args.gpus),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": f"{per_step} sequence(s) of the batch per step, single thread; "
                                    f"{wall:.0f} s wall including setup"},

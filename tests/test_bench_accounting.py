@@ -2,8 +2,12 @@
 checked against what the workload's own arrays hold: the bytes of the rows a step reads
 and writes, the oracle's quantised rows for the FP8/INT4 formats, and a brute-force count
 of the causal (query, key) pairs for prefill.  Also the pool that holds the bench's
-rotated copies of a batch."""
+rotated copies of a batch, and the reference arm's line (the oracle timed on the host),
+which names the same workload config as the native decode line."""
+import json
+
 import numpy as np
+import pytest
 
 import bench
 import workloads
@@ -71,3 +75,26 @@ def test_rotation_pool_holds_disjoint_copies():
     assert nb == rotate * need
     assert np.array_equal(np.sort(order), np.arange(nb))
     assert order.dtype == np.int32
+
+
+def test_reference_arm_line_names_the_native_config(capsys, monkeypatch):
+    monkeypatch.delenv("RANK", raising=False)
+    bench.main(["--impl", "reference", "--workload", "tiny", "--steps", "3", "--warmup", "3"])
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["config"] == bench.decode_config(workloads.tiny(), 1)
+    assert line["unit"] == "GB/s" and line["higher_is_better"] is True
+    assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    # another rank of a multi-rank launch does no work and prints nothing
+    monkeypatch.setenv("RANK", "1")
+    bench.main(["--impl", "reference", "--workload", "tiny", "--steps", "3", "--warmup", "3"])
+    assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_rejects_what_it_does_not_time(monkeypatch):
+    monkeypatch.delenv("RANK", raising=False)
+    for name in ("prefill_tiny", "kv8_llama31_8b"):
+        with pytest.raises(SystemExit):
+            bench.main(["--impl", "reference", "--workload", name, "--steps", "3", "--warmup", "3"])
