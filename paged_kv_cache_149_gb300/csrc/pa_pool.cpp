@@ -22,6 +22,7 @@
 //
 // Each pool's free list is a doubly linked list over block ids (O(1) pop at the head,
 // push at the tail and removal of a revived block).
+#include <algorithm>
 #include <atomic>
 #include <condition_variable>
 #include <cstdint>
@@ -208,16 +209,83 @@ inline void put_u32(uint8_t* p, uint32_t v) {
   p[3] = static_cast<uint8_t>(v >> 24);
 }
 
-// A 32-byte digest held by value (no allocation); its first 8 bytes, uniformly random
-// for SHA-256, serve as the hash-table hash.
+// A 32-byte digest held by value (no allocation).
 struct Digest {
   uint64_t w[4];
   bool operator==(const Digest& o) const {
     return w[0] == o.w[0] && w[1] == o.w[1] && w[2] == o.w[2] && w[3] == o.w[3];
   }
 };
-struct DigestHash {
-  size_t operator()(const Digest& d) const { return static_cast<size_t>(d.w[0]); }
+
+// The digests that name device blocks, and the lookup from a digest to its block: an
+// open-addressing table (linear probing; a removal shifts the entries after it back, so
+// no deleted markers build up).  A slot holds a block id and the low 32 bits of the
+// block's digest (SHA-256 output is uniformly distributed: those bits pick the home slot
+// and reject most mismatches without reading the digest).  A block carries at most one
+// digest, so with at least twice as many slots as blocks the table is at most half full
+// and every probe meets an empty slot.  Nothing is allocated after init.
+class DigestTable {
+ public:
+  void init(int num_blocks) {
+    size_t cap = 16;
+    while (cap < 2 * static_cast<size_t>(num_blocks)) cap <<= 1;
+    slot_.assign(cap, Slot{-1, 0});
+    mask_ = static_cast<uint32_t>(cap - 1);
+    key_.assign(static_cast<size_t>(num_blocks), Digest{});
+    named_.assign(static_cast<size_t>(num_blocks), 0);
+    size_ = 0;
+  }
+  // the block named d, or -1
+  int32_t find(const Digest& d) const {
+    const uint32_t tag = tag_of(d);
+    for (uint32_t i = tag & mask_;; i = (i + 1) & mask_) {
+      const Slot& e = slot_[i];
+      if (e.block < 0) return -1;
+      if (e.tag == tag && key_[e.block] == d) return e.block;
+    }
+  }
+  bool named(int32_t b) const { return named_[b] != 0; }
+  const Digest& digest(int32_t b) const { return key_[b]; }
+  // name block b (unnamed) by d (naming no block)
+  void name(int32_t b, const Digest& d) {
+    key_[b] = d;
+    named_[b] = 1;
+    const uint32_t tag = tag_of(d);
+    uint32_t i = tag & mask_;
+    while (slot_[i].block >= 0) i = (i + 1) & mask_;
+    slot_[i] = Slot{b, tag};
+    ++size_;
+  }
+  // take block b's (present) digest away
+  void unname(int32_t b) {
+    uint32_t i = tag_of(key_[b]) & mask_;
+    while (slot_[i].block != b) i = (i + 1) & mask_;
+    // Close the hole at i: an entry further along the run moves into it when the hole
+    // lies on that entry's probe path (between its home slot and where it sits).
+    for (uint32_t j = (i + 1) & mask_; slot_[j].block >= 0; j = (j + 1) & mask_) {
+      const uint32_t h = slot_[j].tag & mask_;
+      if (((j - h) & mask_) >= ((j - i) & mask_)) {
+        slot_[i] = slot_[j];
+        i = j;
+      }
+    }
+    slot_[i] = Slot{-1, 0};
+    named_[b] = 0;
+    --size_;
+  }
+  int size() const { return size_; }
+
+ private:
+  struct Slot {
+    int32_t block;  // -1: empty
+    uint32_t tag;   // low 32 bits of the block's digest
+  };
+  static uint32_t tag_of(const Digest& d) { return static_cast<uint32_t>(d.w[0]); }
+  std::vector<Slot> slot_;
+  uint32_t mask_ = 0;
+  std::vector<Digest> key_;
+  std::vector<char> named_;
+  int size_ = 0;
 };
 
 // Digests of the n / B full blocks of a token list, chained.  Each block's message is
@@ -314,17 +382,12 @@ struct pa_pool {
   int block_size = 0;
   Tier gpu, cpu;
   std::unordered_map<int64_t, SeqState> seqs;
-  std::unordered_map<Digest, int32_t, DigestHash> cached;  // digest -> device block
-  std::vector<Digest> digest_of;                             // device block -> digest
-  std::vector<char> has_digest;                              //   (valid where set)
+  DigestTable names;  // digests of cached device blocks, and digest -> block
 
   // a device block from the head of the free list; a cached one is evicted
   int32_t take() {
     const int32_t b = gpu.pop();
-    if (has_digest[b]) {
-      cached.erase(digest_of[b]);
-      has_digest[b] = 0;
-    }
+    if (names.named(b)) names.unname(b);
     return b;
   }
 };
@@ -343,9 +406,7 @@ pa_pool* pa_pool_create_tiered(int num_blocks, int block_size, const int32_t* in
       delete p;
       return nullptr;
     }
-    p->digest_of.assign(num_blocks, Digest{});
-    p->has_digest.assign(num_blocks, 0);
-    p->cached.reserve(static_cast<size_t>(num_blocks));
+    p->names.init(num_blocks);
   } catch (...) {
     delete p;
     return nullptr;
@@ -566,9 +627,9 @@ static int allocate_prefix_core(pa_pool* pool, int64_t seq_id, int n_tokens,
   // the longest run of leading full blocks already cached
   std::vector<int32_t> hits;
   for (const Digest& d : dg) {
-    auto it = pool->cached.find(d);
-    if (it == pool->cached.end()) break;
-    hits.push_back(it->second);
+    const int32_t b = pool->names.find(d);
+    if (b < 0) break;
+    hits.push_back(b);
   }
   const int64_t nblk = (static_cast<int64_t>(n_tokens) + bs - 1) / bs;
   const int64_t need = nblk - static_cast<int64_t>(hits.size());
@@ -584,9 +645,8 @@ static int allocate_prefix_core(pa_pool* pool, int64_t seq_id, int n_tokens,
   }
   for (int64_t i = 0; i < need; ++i) st.table.push_back(pool->take());
   for (size_t i = hits.size(); i < dg.size(); ++i) {
-    if (!pool->cached.emplace(dg[i], st.table[i]).second) continue;  // another block answers it
-    pool->digest_of[st.table[i]] = dg[i];
-    pool->has_digest[st.table[i]] = 1;
+    if (pool->names.find(dg[i]) >= 0) continue;  // another block answers it
+    pool->names.name(st.table[i], dg[i]);
   }
   st.ctx = n_tokens;
   pool->seqs.emplace(seq_id, std::move(st));
@@ -608,9 +668,12 @@ static int place_batch(pa_pool* pool, int n, const int64_t* seq_ids, const std::
     if (st < 0) return st;
     cached_out[r] = cached;
     const SeqState& seq = pool->seqs.find(seq_ids[r])->second;
-    if (slots_out)
-      for (int t = cached; t < len; ++t)
-        slots_out[o++] = static_cast<int64_t>(seq.table[t / bs]) * bs + t % bs;
+    if (slots_out)  // block by block: slot = block * B + offset, no division per token
+      for (int t = cached; t < len;) {
+        const int64_t base = static_cast<int64_t>(seq.table[t / bs]) * bs;
+        const int end = std::min(len, (t / bs + 1) * bs);
+        for (int off = t % bs; t < end; ++t, ++off) slots_out[o++] = base + off;
+      }
     if (tables_out) {
       int32_t* row = tables_out + static_cast<size_t>(r) * table_width;
       const int nt = static_cast<int>(seq.table.size());
@@ -723,13 +786,13 @@ int pa_pool_free_batch(pa_pool* pool, const int64_t* seq_ids, int n) {
 }
 
 int pa_pool_num_cached(const pa_pool* pool) {
-  return pool ? static_cast<int>(pool->cached.size()) : PA_ERR_ARG;
+  return pool ? pool->names.size() : PA_ERR_ARG;
 }
 
 int pa_pool_block_digest(const pa_pool* pool, int32_t block, uint8_t* digest_out) {
   if (!pool || !digest_out || block < 0 || block >= pool->gpu.num_blocks) return PA_ERR_ARG;
-  if (!pool->has_digest[block]) return 0;
-  std::memcpy(digest_out, pool->digest_of[block].w, 32);
+  if (!pool->names.named(block)) return 0;
+  std::memcpy(digest_out, pool->names.digest(block).w, 32);
   return 1;
 }
 

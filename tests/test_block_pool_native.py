@@ -370,3 +370,31 @@ def test_hashed_batch_equals_token_batch(libpa):
         assert list(a.free_list()) == list(b.free_list()) and a.num_cached() == b.num_cached()
         a.free_batch(ids[::3])
         b.free_batch(ids[::3])
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_cache_churn_keeps_every_lookup_right(libpa, seed):
+    """A full cache under steady churn: one-token blocks, prompts drawn from a small set of
+    token runs so that hits, partial hits and misses all happen, and most allocations evict
+    the oldest cached block.  Every answer (tokens found cached, tables) and the digest of
+    every block match the oracle's pool, whose lookups are a plain dictionary."""
+    rng = random.Random(9000 + seed)
+    nb = rng.choice([61, 64, 100])
+    order = rng.sample(range(nb), nb)
+    native = libpa.BlockPool(nb, 1, np.array(order))
+    ref = OraclePool(nb, 1, order)
+    live = []
+    for i in range(1500):
+        toks = [rng.randint(0, 5) for _ in range(rng.randint(1, 4))]
+        if ref.num_free() < 4 or (live and rng.random() < 0.45):
+            seq = live.pop(rng.randrange(len(live)))
+            ref.free(seq)
+            native.free(seq)
+            continue
+        assert native.allocate_prefix(i, toks) == ref.allocate_prefix(i, toks)
+        assert list(native.block_table(i)) == ref.block_table(i)
+        live.append(i)
+        if i % 50 == 0:
+            same_cache(native, ref)
+    same_cache(native, ref)
+    assert ref.num_cached() > nb // 2
