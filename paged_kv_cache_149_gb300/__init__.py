@@ -215,6 +215,17 @@ def _need(cond, msg):
         raise ValueError(msg)
 
 
+def _host_out(arr, dtype, size, name):
+    """A caller's host array the library writes `size` elements of: a writeable C-contiguous
+    NumPy array of `dtype` with room for them."""
+    import numpy as np
+    _need(isinstance(arr, np.ndarray) and arr.dtype == np.dtype(dtype)
+          and arr.flags.c_contiguous and arr.flags.writeable,
+          f"{name} must be a writeable C-contiguous {np.dtype(dtype).name} array")
+    _need(arr.size >= size, f"{name} holds {arr.size} entries, {size} needed")
+    return arr
+
+
 def _dev(t, name, dtype=None):
     _need(t.is_cuda, f"{name} must be a CUDA tensor")
     _need(t.is_contiguous(), f"{name} must be contiguous")
@@ -791,17 +802,25 @@ class BlockPool:
         lens = np.diff(ts)
         if table_width is None:
             table_width = int(-(-lens.max() // self.block_size)) if n else 0
+        _need(n == 0 or (ts[0] >= 0 and ts[-1] <= tok.size and (lens >= 0).all()),
+              "token_start must be non-decreasing within tokens")
         if out is None:
             cached = np.zeros(n, dtype=np.int32)
             slots = np.zeros(int(lens.sum()), dtype=np.int64)
             tables = np.zeros((n, table_width), dtype=np.int32)
         else:
             cached, slots, tables = out
+            _host_out(cached, np.int32, n, "cached")
+            _host_out(slots, np.int64, int(lens.sum()), "slots")
+            _host_out(tables, np.int32, n * int(table_width), "tables")
         ex = es = None
         if extras is not None:
             ex = np.ascontiguousarray(np.frombuffer(bytes(extras), dtype=np.uint8)) if not \
                 isinstance(extras, np.ndarray) else np.ascontiguousarray(extras, dtype=np.uint8)
             es = np.ascontiguousarray(np.asarray(extra_start, dtype=np.int64))
+            _need(es.shape == (n + 1,), "extra_start must have n + 1 entries")
+            _need(n == 0 or (es[0] >= 0 and es[-1] <= ex.size and (np.diff(es) >= 0).all()),
+                  "extra_start must be non-decreasing within extras")
         done = ctypes.c_int(0)
         _check(lib().pa_pool_allocate_prefix_batch(
             self._h, n, ids.ctypes.data, tok.ctypes.data, ts.ctypes.data,
@@ -821,12 +840,18 @@ class BlockPool:
         nt = np.ascontiguousarray(np.asarray(n_tokens, dtype=np.int32))
         dg = np.ascontiguousarray(np.frombuffer(digests, dtype=np.uint8) if isinstance(
             digests, (bytes, bytearray)) else np.asarray(digests, dtype=np.uint8))
+        _need(nt.shape == (n,), "n_tokens must have one entry a request")
+        _need(dg.size >= 32 * int((np.maximum(nt, 0) // self.block_size).sum()),
+              "digests must hold 32 bytes for every full block of every request")
         if out is None:
             cached = np.zeros(n, dtype=np.int32)
             slots = np.zeros(int(nt.sum()), dtype=np.int64)
             tables = np.zeros((n, table_width), dtype=np.int32)
         else:
             cached, slots, tables = out
+            _host_out(cached, np.int32, n, "cached")
+            _host_out(slots, np.int64, int(nt.sum()), "slots")
+            _host_out(tables, np.int32, n * int(table_width), "tables")
         done = ctypes.c_int(0)
         _check(lib().pa_pool_allocate_hashed_batch(
             self._h, n, ids.ctypes.data, nt.ctypes.data, dg.ctypes.data if dg.size else None,

@@ -398,3 +398,37 @@ def test_cache_churn_keeps_every_lookup_right(libpa, seed):
             same_cache(native, ref)
     same_cache(native, ref)
     assert ref.num_cached() > nb // 2
+
+
+def test_batch_calls_refuse_buffers_too_small(libpa):
+    """The library writes into caller arrays and reads caller spans by offsets: the binding
+    refuses arrays too small, of the wrong type, or offsets past their data, before the
+    call, and the pool is left as it was."""
+    bs = 4
+    pool = libpa.BlockPool(32, bs, np.arange(32))
+    toks = np.arange(20, dtype=np.int32)
+    ts = np.array([0, 9, 20], dtype=np.int64)
+    digests = b"".join(d for a, b in ((0, 9), (9, 20)) for d in libpa.block_hashes(toks[a:b], bs))
+    good = (np.zeros(2, np.int32), np.zeros(20, np.int64), np.zeros((2, 3), np.int32))
+    bad_outs = [
+        (np.zeros(1, np.int32), good[1], good[2]),
+        (good[0], np.zeros(19, np.int64), good[2]),
+        (good[0], good[1], np.zeros((2, 2), np.int32)),
+        (good[0], np.zeros(20, np.int32), good[2]),
+        (good[0], np.zeros(40, np.int64)[::2], good[2]),
+    ]
+    for out in bad_outs:
+        with pytest.raises(ValueError):
+            pool.allocate_prefix_batch([0, 1], toks, ts, table_width=3, out=out)
+        with pytest.raises(ValueError):
+            pool.allocate_hashed_batch([0, 1], [9, 11], digests, 3, out=out)
+    with pytest.raises(ValueError):
+        pool.allocate_prefix_batch([0, 1], toks, np.array([0, 9, 21]), table_width=3)
+    with pytest.raises(ValueError):
+        pool.allocate_prefix_batch([0, 1], toks, ts, extras=b"ab", extra_start=[0, 1, 3],
+                                   table_width=3)
+    with pytest.raises(ValueError):
+        pool.allocate_hashed_batch([0, 1], [9, 11], digests[:-1], 3)
+    assert pool.num_free() == 32 and pool.num_cached() == 0
+    cached, slots, tables = pool.allocate_hashed_batch([0, 1], [9, 11], digests, 3, out=good)
+    assert list(cached) == [0, 0] and len(slots) == 20 and tables.shape == (2, 3)
