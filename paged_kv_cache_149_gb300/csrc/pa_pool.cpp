@@ -153,15 +153,18 @@ class Sha256 {
                     static_cast<uint8_t>(v >> 16), static_cast<uint8_t>(v >> 24)};
     update(b, 4);
   }
+  // Padding: a one bit, zeros up to 56 bytes into the last block (a further block when
+  // fewer than 9 bytes are left), then the message length in bits, big-endian.
   void finish(uint8_t out[32]) {
-    const uint64_t bits = bits_;
-    uint8_t pad = 0x80;
-    update(&pad, 1);
-    pad = 0;
-    while (fill_ != 56) update(&pad, 1);
-    uint8_t len[8];
-    for (int i = 0; i < 8; ++i) len[i] = static_cast<uint8_t>(bits >> (56 - 8 * i));
-    update(len, 8);
+    buf_[fill_++] = 0x80;
+    if (fill_ > 56) {
+      std::memset(buf_ + fill_, 0, static_cast<size_t>(64 - fill_));
+      block(buf_);
+      fill_ = 0;
+    }
+    std::memset(buf_ + fill_, 0, static_cast<size_t>(56 - fill_));
+    for (int i = 0; i < 8; ++i) buf_[56 + i] = static_cast<uint8_t>(bits_ >> (56 - 8 * i));
+    block(buf_);
     for (int i = 0; i < 8; ++i)
       for (int j = 0; j < 4; ++j) out[4 * i + j] = static_cast<uint8_t>(h_[i] >> (24 - 8 * j));
   }
