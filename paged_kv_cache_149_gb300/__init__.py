@@ -169,12 +169,16 @@ class Launch:
     """A library call whose arguments were checked and marshalled once (``plan=True`` on
     the decode step functions): ``run(stream)`` issues it again on ``stream`` over the
     same buffers, whose contents may change between runs.  For serving loops that launch
-    the same step shape many times; the per-call cost is one foreign call."""
+    the same step shape many times; the per-call cost is one foreign call.  The marshalled
+    arguments are raw device addresses, so the Launch holds a reference to every tensor
+    they point into (a workspace the call created included): none is freed, and its
+    memory reused, while the Launch can still run."""
 
-    def __init__(self, name, args, out):
+    def __init__(self, name, args, out, keep=()):
         self._fn = getattr(lib(), name)
         self._name = name
         self._args = args
+        self._keep = tuple(keep)
         self.out = out
 
     def run(self, stream):
@@ -317,7 +321,9 @@ def decode_append(q, key_new, value_new, k_cache, v_cache, block_tables, context
             _dev(out, "out"), _dev(workspace, "workspace"),
             workspace.numel() * workspace.element_size(), _dtype_code(q))
     if plan:
-        return Launch("pa_decode_append", args, out)
+        return Launch("pa_decode_append", args, out,
+                      keep=(q, key_new, value_new, k_cache, v_cache, block_tables,
+                            context_lens, out, workspace))
     _check(lib().pa_decode_append(*args, _stream_ptr(stream, q.device)), "pa_decode_append")
     return out
 
@@ -396,7 +402,9 @@ def decode_append_fp8(q, key_new, value_new, k_cache, v_cache, block_tables, con
             float(k_scale), float(v_scale), _dev(out, "out"), _dev(workspace, "workspace"),
             workspace.numel() * workspace.element_size(), _dtype_code(q))
     if plan:
-        return Launch("pa_decode_append_fp8", args, out)
+        return Launch("pa_decode_append_fp8", args, out,
+                      keep=(q, key_new, value_new, k_cache, v_cache, block_tables,
+                            context_lens, out, workspace))
     _check(lib().pa_decode_append_fp8(*args, _stream_ptr(stream, q.device)), "pa_decode_append_fp8")
     return out
 
@@ -530,7 +538,9 @@ def decode_append_int4(q, key_new, value_new, k_codes, v_codes, k_scales, v_scal
             _dev(out, "out"), _dev(workspace, "workspace"),
             workspace.numel() * workspace.element_size(), _dtype_code(q))
     if plan:
-        return Launch("pa_decode_append_int4", args, out)
+        return Launch("pa_decode_append_int4", args, out,
+                      keep=(q, key_new, value_new, k_codes, v_codes, k_scales, v_scales,
+                            block_tables, context_lens, out, workspace))
     _check(lib().pa_decode_append_int4(*args, _stream_ptr(stream, q.device)), "pa_decode_append_int4")
     return out
 

@@ -1,0 +1,70 @@
+"""Host-side logic of the Python binding, on CPU with no GPU work: a planned launch
+(plan=True on the decode step functions) holds every tensor its marshalled device
+addresses point into, including a workspace the call created itself, for as long as the
+launch object lives.  The device checks are replaced by address lookups so that the
+marshalling runs on CPU tensors; nothing is launched."""
+import gc
+import weakref
+
+import pytest
+import torch
+
+N, HQ, HKV, D, NB, B, T = 3, 8, 2, 64, 8, 16, 4
+
+
+@pytest.fixture
+def cpu_marshal(libpa, monkeypatch):
+    made = []
+
+    def workspace(hq, hkv, d, device=None):
+        w = torch.empty(256, dtype=torch.uint8)
+        made.append(weakref.ref(w))
+        return w
+    monkeypatch.setattr(libpa, "_dev", lambda t, name, dtype=None: t.data_ptr())
+    monkeypatch.setattr(libpa, "_fp8_cache", lambda t, name: t.data_ptr())
+    monkeypatch.setattr(libpa, "_int4_cache", lambda c, s, name: (c.data_ptr(), s.data_ptr()))
+    monkeypatch.setattr(libpa, "make_workspace", workspace)
+    return libpa, made
+
+
+def step_inputs(dtype=torch.bfloat16):
+    return dict(q=torch.zeros(N, HQ, D, dtype=dtype),
+                key_new=torch.zeros(N, HKV, D, dtype=dtype),
+                value_new=torch.zeros(N, HKV, D, dtype=dtype),
+                block_tables=torch.zeros(N, T, dtype=torch.int32),
+                context_lens=torch.ones(N, dtype=torch.int32))
+
+
+def plans(pa):
+    i = step_inputs()
+    yield "16-bit", lambda: pa.decode_append(
+        i["q"], i["key_new"], i["value_new"], torch.zeros(NB, HKV, B, D, dtype=torch.bfloat16),
+        torch.zeros(NB, HKV, B, D, dtype=torch.bfloat16), i["block_tables"], i["context_lens"],
+        0.125, plan=True)
+    yield "fp8", lambda: pa.decode_append_fp8(
+        i["q"], i["key_new"], i["value_new"], torch.zeros(NB, HKV, B, D, dtype=torch.uint8),
+        torch.zeros(NB, HKV, B, D, dtype=torch.uint8), i["block_tables"], i["context_lens"],
+        0.125, 0.5, 0.5, plan=True)
+    yield "int4", lambda: pa.decode_append_int4(
+        i["q"], i["key_new"], i["value_new"], torch.zeros(NB, HKV, B, D // 2, dtype=torch.uint8),
+        torch.zeros(NB, HKV, B, D // 2, dtype=torch.uint8), torch.zeros(NB, HKV, B),
+        torch.zeros(NB, HKV, B), i["block_tables"], i["context_lens"], 0.125, plan=True)
+
+
+def test_planned_launch_holds_its_tensors(cpu_marshal):
+    pa, made = cpu_marshal
+    for name, make in plans(pa):
+        made.clear()
+        launch = make()
+        gc.collect()
+        assert isinstance(launch, pa.Launch), name
+        # the workspace the call made is alive while the launch is
+        assert len(made) == 1 and made[0]() is not None, name
+        # every tensor address in the marshalled arguments is one the launch holds
+        held = {t.data_ptr() for t in launch._keep}
+        ptrs = [a for a in launch._args if isinstance(a, int) and a in held]
+        assert made[0]().data_ptr() in ptrs and launch.out.data_ptr() in ptrs, name
+        assert len(ptrs) >= 9, name
+        del launch
+        gc.collect()
+        assert made[0]() is None, name
