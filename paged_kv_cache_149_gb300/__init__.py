@@ -172,7 +172,8 @@ class Launch:
     the same step shape many times; the per-call cost is one foreign call.  The marshalled
     arguments are raw device addresses, so the Launch holds a reference to every tensor
     they point into (a workspace the call created included): none is freed, and its
-    memory reused, while the Launch can still run."""
+    memory reused, while the Launch can still run.  Drop the Launch only after its last
+    run has finished, or ordered before later work on the stream it ran on."""
 
     def __init__(self, name, args, out, keep=()):
         self._fn = getattr(lib(), name)
@@ -267,6 +268,17 @@ def make_workspace(num_q_heads, num_kv_heads, head_dim, device=None):
                        dtype=torch.uint8, device=device or "cuda")
 
 
+def _scratch(num_q_heads, num_kv_heads, head_dim, device, stream):
+    """A workspace for one call launched on `stream`, allocated on that stream: the caching
+    allocator then reuses its memory, once the call returns and the tensor is dropped, only
+    for work ordered after the call on that stream."""
+    import torch
+    if stream is None:
+        return make_workspace(num_q_heads, num_kv_heads, head_dim, device)
+    with torch.cuda.stream(stream):
+        return make_workspace(num_q_heads, num_kv_heads, head_dim, device)
+
+
 def decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=None, workspace=None,
            stream=None):
     """Paged decode attention; returns ``out`` [num_seqs, num_q_heads, head_dim]."""
@@ -281,7 +293,7 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=None, wor
         out = torch.empty_like(q)
     _need(out.shape == q.shape and out.dtype == q.dtype, "out must match q")
     if workspace is None:
-        workspace = make_workspace(hq, hkv, d, q.device)
+        workspace = _scratch(hq, hkv, d, q.device, stream)
     st = lib().pa_decode(
         _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
         _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
@@ -313,7 +325,7 @@ def decode_append(q, key_new, value_new, k_cache, v_cache, block_tables, context
         out = torch.empty_like(q)
     _need(out.shape == q.shape and out.dtype == q.dtype, "out must match q")
     if workspace is None:
-        workspace = make_workspace(hq, hkv, d, q.device)
+        workspace = _scratch(hq, hkv, d, q.device, stream)
     args = (_dev(q, "q"), _dev(key_new, "key_new"), _dev(value_new, "value_new"),
             _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
             _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
@@ -366,7 +378,7 @@ def decode_fp8(q, k_cache, v_cache, block_tables, context_lens, scale, k_scale, 
         out = torch.empty_like(q)
     _need(out.shape == q.shape and out.dtype == q.dtype, "out must match q")
     if workspace is None:
-        workspace = make_workspace(hq, hkv, d, q.device)
+        workspace = _scratch(hq, hkv, d, q.device, stream)
     st = lib().pa_decode_fp8(
         _dev(q, "q"), _fp8_cache(k_cache, "k_cache"), _fp8_cache(v_cache, "v_cache"),
         _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
@@ -394,7 +406,7 @@ def decode_append_fp8(q, key_new, value_new, k_cache, v_cache, block_tables, con
         out = torch.empty_like(q)
     _need(out.shape == q.shape and out.dtype == q.dtype, "out must match q")
     if workspace is None:
-        workspace = make_workspace(hq, hkv, d, q.device)
+        workspace = _scratch(hq, hkv, d, q.device, stream)
     args = (_dev(q, "q"), _dev(key_new, "key_new"), _dev(value_new, "value_new"),
             _fp8_cache(k_cache, "k_cache"), _fp8_cache(v_cache, "v_cache"),
             _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
@@ -502,7 +514,7 @@ def decode_int4(q, k_codes, v_codes, k_scales, v_scales, block_tables, context_l
         out = torch.empty_like(q)
     _need(out.shape == q.shape and out.dtype == q.dtype, "out must match q")
     if workspace is None:
-        workspace = make_workspace(hq, hkv, d, q.device)
+        workspace = _scratch(hq, hkv, d, q.device, stream)
     st = lib().pa_decode_int4(
         _dev(q, "q"), kc, vc, ks, vs, _dev(block_tables, "block_tables", torch.int32),
         block_tables.shape[1], _dev(context_lens, "context_lens", torch.int32), n, hq, hkv, d, bs,
@@ -531,7 +543,7 @@ def decode_append_int4(q, key_new, value_new, k_codes, v_codes, k_scales, v_scal
         out = torch.empty_like(q)
     _need(out.shape == q.shape and out.dtype == q.dtype, "out must match q")
     if workspace is None:
-        workspace = make_workspace(hq, hkv, d, q.device)
+        workspace = _scratch(hq, hkv, d, q.device, stream)
     args = (_dev(q, "q"), _dev(key_new, "key_new"), _dev(value_new, "value_new"), kc, vc, ks, vs,
             _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
             _dev(context_lens, "context_lens", torch.int32), n, hq, hkv, d, bs, nb, float(scale),
