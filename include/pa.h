@@ -454,9 +454,11 @@ int pa_pool_allocate_prefix(pa_pool* pool, int64_t seq_id, const int32_t* tokens
  * parallel on a small pool of host threads (the library's own; batch calls are serialised
  * on it).  Outputs: cached_out[n]; slots_out (may be NULL) the slots of every request's
  * uncached tokens, request after request (what pa_reshape_and_cache takes for the new
- * rows); tables_out (may be NULL) [n][table_width] block tables padded with 0.  On an
- * error the requests before the failing one stay allocated: *n_done (may be NULL) says
- * how many. */
+ * rows); tables_out (may be NULL) [n][table_width] block tables padded with 0.
+ * token_start and extra_start must start at 0 or above and never decrease.  A negative
+ * start, a decreasing offset, a span longer than INT_MAX or a table wider than
+ * table_width is PA_ERR_ARG before anything changes.  On a later error the requests
+ * before the failing one stay allocated: *n_done (may be NULL) says how many. */
 int pa_pool_allocate_prefix_batch(pa_pool* pool, int n, const int64_t* seq_ids,
                                   const int32_t* tokens, const int64_t* token_start,
                                   const uint8_t* extras, const int64_t* extra_start,

@@ -715,10 +715,13 @@ int pa_pool_allocate_prefix_batch(pa_pool* pool, int n, const int64_t* seq_ids,
     return PA_ERR_ARG;
   if (n == 0) return PA_OK;
   const int bs = pool->block_size;
+  if (token_start[0] < 0 || (extras && extra_start[0] < 0)) return PA_ERR_ARG;
   for (int r = 0; r < n; ++r) {
     const int64_t len = token_start[r + 1] - token_start[r];
     if (len < 0 || len > 0x7fffffff || (len > 0 && !tokens)) return PA_ERR_ARG;
-    if (extras && extra_start[r + 1] < extra_start[r]) return PA_ERR_ARG;
+    if (extras && (extra_start[r + 1] < extra_start[r] ||
+                   extra_start[r + 1] - extra_start[r] > 0x7fffffff))
+      return PA_ERR_ARG;
     if (tables_out && (len + bs - 1) / bs > table_width) return PA_ERR_ARG;
   }
   try {
@@ -766,7 +769,9 @@ int pa_pool_allocate_hashed_batch(pa_pool* pool, int n, const int64_t* seq_ids,
     const uint8_t* d = digests;
     for (int r = 0; r < n; ++r) {
       lens[r] = n_tokens[r];
-      if (lens[r] < 0 || (tables_out && (lens[r] + bs - 1) / bs > table_width)) return PA_ERR_ARG;
+      if (lens[r] < 0 ||
+          (tables_out && (static_cast<int64_t>(lens[r]) + bs - 1) / bs > table_width))
+        return PA_ERR_ARG;
       const int m = lens[r] / bs;
       if (m > 0 && !digests) return PA_ERR_ARG;
       dg[r].resize(static_cast<size_t>(m));

@@ -432,3 +432,29 @@ def test_batch_calls_refuse_buffers_too_small(libpa):
     assert pool.num_free() == 32 and pool.num_cached() == 0
     cached, slots, tables = pool.allocate_hashed_batch([0, 1], [9, 11], digests, 3, out=good)
     assert list(cached) == [0, 0] and len(slots) == 20 and tables.shape == (2, 3)
+
+
+def test_batch_placement_rejects_bad_offsets_in_the_library(libpa):
+    """The C entry point itself (no binding checks in front) refuses a negative first offset
+    or a decreasing one, for tokens and extra bytes, and changes nothing."""
+    import ctypes
+    lib = libpa.lib()
+    pool = libpa.BlockPool(16, 4, np.arange(16))
+    ids = np.array([0, 1], dtype=np.int64)
+    toks = np.arange(12, dtype=np.int32)
+    extras = np.frombuffer(b"abcdef", dtype=np.uint8).copy()
+    cached = np.zeros(2, dtype=np.int32)
+    done = ctypes.c_int(-1)
+
+    def call(ts, es=None):
+        ts = np.asarray(ts, dtype=np.int64)
+        es = None if es is None else np.asarray(es, dtype=np.int64)
+        return lib.pa_pool_allocate_prefix_batch(
+            pool._h, 2, ids.ctypes.data, toks.ctypes.data, ts.ctypes.data,
+            None if es is None else extras.ctypes.data, None if es is None else es.ctypes.data,
+            cached.ctypes.data, None, None, 0, ctypes.byref(done))
+    for ts, es in (([-4, 4, 12], None), ([0, 8, 4], None), ([0, 4, 12], [-1, 2, 6]),
+                   ([0, 4, 12], [0, 4, 2])):
+        assert call(ts, es) == libpa.PA_ERR_ARG
+        assert done.value == 0 and pool.num_free() == 16
+    assert call([0, 4, 12], [0, 2, 6]) == 0 and done.value == 2 and pool.num_free() == 13
