@@ -224,18 +224,20 @@ def _host_out(arr, dtype, size, name):
     """A caller's host array the library writes `size` elements of: a writeable C-contiguous
     NumPy array of `dtype` with room for them."""
     import numpy as np
-    _need(isinstance(arr, np.ndarray) and arr.dtype == np.dtype(dtype)
-          and arr.flags.c_contiguous and arr.flags.writeable,
-          f"{name} must be a writeable C-contiguous {np.dtype(dtype).name} array")
-    _need(arr.size >= size, f"{name} holds {arr.size} entries, {size} needed")
+    # (messages are formatted only on failure: these checks run on every serving step)
+    if not (isinstance(arr, np.ndarray) and arr.dtype == dtype and arr.flags.c_contiguous
+            and arr.flags.writeable):
+        raise ValueError(f"{name} must be a writeable C-contiguous {np.dtype(dtype).name} array")
+    if arr.size < size:
+        raise ValueError(f"{name} holds {arr.size} entries, {size} needed")
     return arr
 
 
 def _dev(t, name, dtype=None):
-    _need(t.is_cuda, f"{name} must be a CUDA tensor")
-    _need(t.is_contiguous(), f"{name} must be contiguous")
-    if dtype is not None:
-        _need(t.dtype == dtype, f"{name} must be {dtype}, got {t.dtype}")
+    if not (t.is_cuda and t.is_contiguous() and (dtype is None or t.dtype == dtype)):
+        _need(t.is_cuda, f"{name} must be a CUDA tensor")
+        _need(t.is_contiguous(), f"{name} must be contiguous")
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
     return t.data_ptr()
 
 
@@ -342,8 +344,8 @@ def decode_append(q, key_new, value_new, k_cache, v_cache, block_tables, context
 
 def _fp8_cache(t, name):
     import torch
-    _need(t.dtype in (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8)),
-          f"{name} must hold E4M3 codes (uint8 or float8_e4m3fn), got {t.dtype}")
+    if t.dtype not in (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8)):
+        raise ValueError(f"{name} must hold E4M3 codes (uint8 or float8_e4m3fn), got {t.dtype}")
     return _dev(t, name)
 
 
@@ -473,10 +475,12 @@ def decode_fixed_scratch(q, k_cache, v_cache, block_tables, context_lens, scale,
 
 def _int4_cache(codes, scales, name):
     import torch
-    _need(codes.dtype == torch.uint8, f"{name} codes must be uint8 (two 4-bit codes a byte)")
-    _need(scales.dtype == torch.float32, f"{name} scales must be float32")
-    _need(codes.dim() == 4 and scales.shape == codes.shape[:3],
-          f"{name}: codes [NB, Hkv, B, d/2] and scales [NB, Hkv, B]")
+    if codes.dtype != torch.uint8:
+        raise ValueError(f"{name} codes must be uint8 (two 4-bit codes a byte)")
+    if scales.dtype != torch.float32:
+        raise ValueError(f"{name} scales must be float32")
+    if not (codes.dim() == 4 and scales.shape == codes.shape[:3]):
+        raise ValueError(f"{name}: codes [NB, Hkv, B, d/2] and scales [NB, Hkv, B]")
     return _dev(codes, name), _dev(scales, name + " scales")
 
 
@@ -611,10 +615,11 @@ def copy_blocks(k_cache, v_cache, block_mapping, stream=None):
 
 def _reachable(t, name, dtype=None):
     """A CUDA tensor, or a page-locked (pinned) CPU tensor that the GPU can address."""
-    _need(t.is_cuda or t.is_pinned(), f"{name} must be a CUDA tensor or a pinned CPU tensor")
-    _need(t.is_contiguous(), f"{name} must be contiguous")
-    if dtype is not None:
-        _need(t.dtype == dtype, f"{name} must be {dtype}, got {t.dtype}")
+    if not ((t.is_cuda or t.is_pinned()) and t.is_contiguous()
+            and (dtype is None or t.dtype == dtype)):
+        _need(t.is_cuda or t.is_pinned(), f"{name} must be a CUDA tensor or a pinned CPU tensor")
+        _need(t.is_contiguous(), f"{name} must be contiguous")
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
     return t.data_ptr()
 
 

@@ -68,3 +68,31 @@ def test_planned_launch_holds_its_tensors(cpu_marshal):
         del launch
         gc.collect()
         assert made[0]() is None, name
+
+
+def test_argument_checks_name_the_argument(libpa):
+    """The checks in front of the library raise ValueError naming the bad argument (their
+    messages are built only on failure)."""
+    import numpy as np
+    t = torch.zeros(4, dtype=torch.int64)
+    with pytest.raises(ValueError, match="slot_mapping must be a CUDA tensor"):
+        libpa._dev(t, "slot_mapping", torch.int64)
+    with pytest.raises(ValueError, match="tables must be a writeable C-contiguous int32"):
+        libpa._host_out(np.zeros(8, np.int64), np.int32, 4, "tables")
+    with pytest.raises(ValueError, match="slots holds 3 entries, 4 needed"):
+        libpa._host_out(np.zeros(3, np.int64), np.int64, 4, "slots")
+    ro = np.zeros(8, np.int32)
+    ro.flags.writeable = False
+    with pytest.raises(ValueError, match="cached must be a writeable"):
+        libpa._host_out(ro, np.int32, 4, "cached")
+    a = np.zeros(8, np.int32)
+    assert libpa._host_out(a, np.int32, 8, "cached") is a
+    with pytest.raises(ValueError, match="k codes must be uint8"):
+        libpa._int4_cache(torch.zeros(2, 2, 2, 2, dtype=torch.int8), torch.zeros(2, 2, 2), "k")
+    with pytest.raises(ValueError, match="v scales must be float32"):
+        libpa._int4_cache(torch.zeros(2, 2, 2, 2, dtype=torch.uint8),
+                          torch.zeros(2, 2, 2, dtype=torch.float16), "v")
+    with pytest.raises(ValueError, match="must hold E4M3 codes"):
+        libpa._fp8_cache(torch.zeros(2, dtype=torch.float16), "k_cache")
+    with pytest.raises(ValueError, match="must be a CUDA tensor or a pinned CPU tensor"):
+        libpa._reachable(t, "src_k")
