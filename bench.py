@@ -168,9 +168,70 @@ def rotation_pool(wl, rotate):
     return need, np.random.default_rng(1).permutation(need).astype(np.int32)
 
 
-def build_batches(wl, device, rotate):
+# Timed loops: each timed loop runs exactly --steps steps between a barrier plus a device
+# synchronise and the next; a line reports the median over REPEATS-many such loops, the
+# count chosen so that each kind of loop runs for about LOOP_SECONDS in all.
+LOOP_SECONDS = 0.4
+MAX_REPEATS = 400
+
+
+def repeats_for(ms_per_step, steps):
+    return int(min(MAX_REPEATS, max(5, round(LOOP_SECONDS * 1e3 / max(1e-3, ms_per_step * steps)))))
+
+
+def timed_median(fn, steps, stream, device, world, repeats):
+    """Median (and all) of the ms per step of `repeats` loops of `steps` calls fn(i), CUDA
+    events on `stream` around each loop, a barrier and a synchronise on both sides."""
+    import torch
+    per = []
+    for _ in range(repeats):
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(steps):
+            fn(i)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        per.append(e0.elapsed_time(e1) / steps)
+    return float(np.median(per)), per
+
+
+def estimate_ms(fn, stream, device, n=5):
+    """A rough ms per call (to size the repeats)."""
+    import torch
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(n):
+        fn(i)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    return e0.elapsed_time(e1) / n
+
+
+def kv_memory(wl, used_blocks):
+    """KV memory use of the batch's placement: the paged pool's slots against the tokens
+    held (effective utilisation, aiqz.cc section 新旧方案对比), and the fragmentation of a
+    contiguous allocator that reserves the recipe's maximum context per sequence
+    (aiqz.cc section 连续分配之殇)."""
+    tokens = int(sum(int(c) for c in wl.context_lens))
+    slots = used_blocks * wl.block_size
+    reserved = wl.num_seqs * wl.max_blocks_per_seq * wl.block_size
+    return {"tokens": tokens, "paged_slots": slots,
+            "paged_utilisation": round(tokens / slots, 5),
+            "paged_waste_tokens": slots - tokens,
+            "contiguous_reserved_tokens": reserved,
+            "contiguous_fragmentation": round(1.0 - tokens / reserved, 5)}
+
+
+def build_batches(wl, device, rotate, identity=False):
     """Place `rotate` copies of the batch in disjoint blocks of one pool and write every
-    token except each sequence's newest one (the step writes those)."""
+    token except each sequence's newest one (the step writes those).  identity=True takes
+    blocks in physical order (each sequence's blocks consecutive: the contiguous case)
+    instead of the shuffled free list.  Returns the caches, the batches and the blocks one
+    copy holds."""
     import numpy as np
     import torch
 
@@ -181,6 +242,8 @@ def build_batches(wl, device, rotate):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(dt)
 
     nb, order = rotation_pool(wl, rotate)
+    if identity:
+        order = np.arange(nb, dtype=np.int32)
     shape = (nb, wl.num_kv_heads, wl.block_size, wl.head_dim)
     k_cache = torch.zeros(shape, dtype=dt, device=device)
     v_cache = torch.zeros(shape, dtype=dt, device=device)
@@ -189,7 +252,10 @@ def build_batches(wl, device, rotate):
     keys, values = up(wl.keys), up(wl.values)
     last_rows = torch.from_numpy(wl.seq_start[1:] - 1).to(device)
     batches = []
+    free0 = pool.num_free()
     for r in range(rotate):
+        if r == 1:
+            used = free0 - pool.num_free()
         tables = np.full((n, T), 0, dtype=np.int32)
         slots = []
         for s in range(n):
@@ -209,25 +275,34 @@ def build_batches(wl, device, rotate):
             "value": values[last_rows].contiguous(),
             "out": torch.empty((n, wl.num_q_heads, wl.head_dim), dtype=dt, device=device),
         })
-    return k_cache, v_cache, batches
+    if rotate == 1:
+        used = free0 - pool.num_free()
+    return k_cache, v_cache, batches, used
 
 
-E2E_METHOD = ("each step: its inputs copied from one pinned host buffer, the public call "
+E2E_METHOD = ("each step: its inputs copied from pinned host memory, the public call "
               "(decode steps: a Launch planned once per staging slot), its output copied to "
-              "pinned host memory; steps are independent, so an upload stream and a download "
-              "stream overlap the neighbouring steps' copies with the kernel (two device "
-              "staging slots)")
+              "pinned host memory.  Steps are independent, so they are staged in groups: one "
+              "upload of a group's inputs on an upload stream, the group's calls back to back "
+              "on the compute stream (no stream wait between them), one download of the "
+              "group's outputs on a download stream; two groups of staging slots, so each "
+              "group's copies overlap the neighbouring groups' kernels")
+
+E2E_GROUP = 10  # steps staged together
 
 
-def pipelined_e2e(batches, names, make_launch, out_like, device, steps, warmup):
-    """Steps end to end from pinned host memory: every step copies its inputs (`names` of
-    its batch, packed into one pinned staging buffer, so one upload a step) to the device,
-    runs the step (`make_launch(dev_inputs, dev_out)` gives a callable taking the stream,
-    made once per staging slot) and downloads its output.  Consecutive steps
-    are independent, so the copies overlap the neighbouring steps' kernels: two device
-    staging slots and two output slots; the upload of step i + 2 waits for kernel i (slot
-    i % 2 free), the download of step i for kernel i, and kernel i + 2 for that download
-    (its output slot).  Returns (ms per step, H2D bytes per step, D2H bytes per step)."""
+def pipelined_e2e(batches, names, make_launch, out_like, device, steps, warmup, repeats=1,
+                  group=E2E_GROUP):
+    """Steps end to end from pinned host memory: every step's inputs (`names` of its batch,
+    packed) come from pinned host memory, the step runs (`make_launch(dev_inputs, dev_out)`
+    gives a callable taking the stream, made once per staging slot), and its output goes
+    back to pinned host memory.  Consecutive steps are independent, so they are staged
+    `group` at a time: a group's inputs go up in one copy on an upload stream, its calls
+    run back to back on the compute stream (so each kernel may start while the one before
+    it drains), and its outputs come down in one copy on a download stream.  Two groups of
+    slots: the upload of group g + 2 waits for group g's kernels, group g + 2's kernels for
+    group g's download.  Each timed run is `steps` steps; returns (the median ms per step
+    over `repeats` runs, H2D bytes per step, D2H bytes per step)."""
     import torch
 
     align = 256
@@ -236,56 +311,76 @@ def pipelined_e2e(batches, names, make_launch, out_like, device, steps, warmup):
         t = batches[0][k]
         layout[k] = (off, t.shape, t.dtype, t.numel() * t.element_size())
         off += -(-layout[k][3] // align) * align
-    host = []
-    for b in batches:
-        h = torch.empty(off, dtype=torch.uint8).pin_memory()
-        for k in names:
-            o, _, _, nb = layout[k]
-            h[o:o + nb].copy_(b[k].contiguous().view(-1).view(torch.uint8).cpu())
-        host.append(h)
-    dev = [torch.empty(off, dtype=torch.uint8, device=device) for _ in range(2)]
-    views = [{k: d[o:o + nb].view(dt).view(shape) for k, (o, shape, dt, nb) in layout.items()}
-             for d in dev]
-    outs = [torch.empty_like(out_like) for _ in range(2)]
-    host_out = [torch.empty(out_like.shape, dtype=out_like.dtype).pin_memory() for _ in range(2)]
-    comp, up_s, down_s = (torch.cuda.Stream(device) for _ in range(3))
+    S = max(1, group)
     nrot = len(batches)
-    launches = [make_launch(views[i], outs[i]) for i in range(2)]
+    # a group's inputs, step after step (step k of a group uses rotation k % nrot; a group
+    # starting at step i uses rotations i .. i + S - 1, so the host buffer is built per
+    # starting rotation)
+    def packed(first_rot):
+        h = torch.empty(S * off, dtype=torch.uint8).pin_memory()
+        for k_ in range(S):
+            b = batches[(first_rot + k_) % nrot]
+            for k in names:
+                o, _, _, nb = layout[k]
+                h[k_ * off + o:k_ * off + o + nb].copy_(b[k].contiguous().view(-1).view(torch.uint8).cpu())
+        return h
+    host = [packed(r) for r in range(nrot)]
+    dev = [torch.empty(S * off, dtype=torch.uint8, device=device) for _ in range(2)]
+    nout = out_like.numel()
+    outs = [torch.empty((S,) + tuple(out_like.shape), dtype=out_like.dtype, device=device)
+            for _ in range(2)]
+    host_out = [torch.empty((S,) + tuple(out_like.shape), dtype=out_like.dtype).pin_memory()
+                for _ in range(2)]
+    launches = []
+    for g in range(2):
+        row = []
+        for k_ in range(S):
+            v = {k: dev[g][k_ * off + o:k_ * off + o + nb].view(dt).view(shape)
+                 for k, (o, shape, dt, nb) in layout.items()}
+            row.append(make_launch(v, outs[g][k_]))
+        launches.append(row)
+    comp, up_s, down_s = (torch.cuda.Stream(device) for _ in range(3))
+    del nout
 
     def run(n):
-        up = [torch.cuda.Event() for _ in range(n)]
-        done = [torch.cuda.Event() for _ in range(n)]
-        down = [torch.cuda.Event() for _ in range(n)]
+        ng = -(-n // S)
+        up = [torch.cuda.Event() for _ in range(ng)]
+        done = [torch.cuda.Event() for _ in range(ng)]
+        down = [torch.cuda.Event() for _ in range(ng)]
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         start.record(comp)
         up_s.wait_event(start)
         down_s.wait_event(start)
-        for i in range(min(2, n)):
+
+        def upload(g):
+            if g >= 2:
+                up_s.wait_event(done[g - 2])
             with torch.cuda.stream(up_s):
-                dev[i % 2].copy_(host[i % nrot], non_blocking=True)
-            up[i].record(up_s)
-        for i in range(n):
-            comp.wait_event(up[i])
-            if i >= 2:
-                comp.wait_event(down[i - 2])
-            launches[i % 2](comp)
-            done[i].record(comp)
-            down_s.wait_event(done[i])
+                dev[g % 2].copy_(host[(g * S) % nrot], non_blocking=True)
+            up[g].record(up_s)
+        for g in range(min(2, ng)):
+            upload(g)
+        for g in range(ng):
+            m = min(S, n - g * S)
+            comp.wait_event(up[g])
+            if g >= 2:
+                comp.wait_event(down[g - 2])
+            for k_ in range(m):
+                launches[g % 2][k_](comp)
+            done[g].record(comp)
+            down_s.wait_event(done[g])
             with torch.cuda.stream(down_s):
-                host_out[i % 2].copy_(outs[i % 2], non_blocking=True)
-            down[i].record(down_s)
-            if i + 2 < n:
-                up_s.wait_event(done[i])
-                with torch.cuda.stream(up_s):
-                    dev[i % 2].copy_(host[(i + 2) % nrot], non_blocking=True)
-                up[i + 2].record(up_s)
-        comp.wait_event(down[n - 1])
+                host_out[g % 2][:m].copy_(outs[g % 2][:m], non_blocking=True)
+            down[g].record(down_s)
+            if g + 2 < ng:
+                upload(g + 2)
+        comp.wait_event(down[ng - 1])
         end.record(comp)
         torch.cuda.synchronize(device)
         return start.elapsed_time(end) / n
 
     run(max(3, warmup))
-    ms = run(max(1, min(steps, 2000)))
+    ms = float(np.median([run(max(1, min(steps, 2000))) for _ in range(max(1, repeats))]))
     d2h = out_like.numel() * out_like.element_size()
     return ms, sum(layout[k][3] for k in names), d2h
 
@@ -302,7 +397,9 @@ def run_gpu(args, rank, world, local_rank):
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
     wl = workloads.RECIPES[args.workload]()
-    k_cache, v_cache, batches = build_batches(wl, device, ROTATE)
+    k_cache, v_cache, batches, used = build_batches(wl, device, ROTATE)
+    # the same batches placed contiguously (identity tables), for the paging overhead
+    k_id, v_id, batches_id, _ = build_batches(wl, device, ROTATE, identity=True)
     ws = pa.make_workspace(wl.num_q_heads, wl.num_kv_heads, wl.head_dim, device)
     stream = torch.cuda.Stream(device)
     torch.cuda.synchronize(device)
@@ -324,51 +421,39 @@ def run_gpu(args, rank, world, local_rank):
         pa.decode(b["q"], k_cache, v_cache, b["tables"], b["ctx"], wl.scale, out=b["out"],
                   workspace=ws, stream=stream)
 
+    def decode_identity(i):
+        b = batches_id[i % ROTATE]
+        pa.decode(b["q"], k_id, v_id, b["tables"], b["ctx"], wl.scale, out=b["out"],
+                  workspace=ws, stream=stream)
+
     for i in range(args.warmup):
         step(i)
         decode_only(i)
         step_two_calls(i)
+        decode_identity(i)
     torch.cuda.synchronize(device)
     if pa.get_device_error(stream=stream):
         raise RuntimeError("device error flags set during warm-up")
+    K = args.steps
+    R = repeats_for(estimate_ms(step, stream, device), K)
 
     sampler = ClockSampler(local_rank) if rank == 0 else None
     if sampler:
         sampler.start()
         time.sleep(0.3)
-    K = args.steps
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize(device)
     t0 = time.time()
     # the step loop: nothing between the launches, so each kernel may start while the one
     # before it drains (programmatic dependent launch)
-    ev[0].record(stream)
-    for i in range(K):
-        step(i)
-    ev[1].record(stream)
-    torch.cuda.synchronize(device)
-    if world > 1:
-        torch.distributed.barrier()
-    # the decode kernel alone, K launches back to back on the same stream: its duration
-    ev[2].record(stream)
-    for i in range(K):
-        decode_only(i)
-    ev[3].record(stream)
-    torch.cuda.synchronize(device)
+    step_ms, step_all = timed_median(step, K, stream, device, world, R)
+    # the decode alone (decode kernel + merge kernel), back to back on the same stream
+    decode_ms, _ = timed_median(decode_only, K, stream, device, world, R)
     # the same step as two calls
-    ev[4].record(stream)
-    for i in range(K):
-        step_two_calls(i)
-    ev[5].record(stream)
-    torch.cuda.synchronize(device)
+    two_calls_ms, _ = timed_median(step_two_calls, K, stream, device, world, R)
+    # the decode over the same batches placed contiguously
+    identity_ms, _ = timed_median(decode_identity, K, stream, device, world, R)
     t1 = time.time()
     clocks = sampler.stop(t0, t1) if sampler else None
     flags = pa.get_device_error(stream=stream)
-    total_ms = ev[0].elapsed_time(ev[1])
-    decode_ms = ev[2].elapsed_time(ev[3]) / K
-    two_calls_ms = ev[4].elapsed_time(ev[5]) / K
 
     # end to end through the binding with host buffers: inputs from pinned host memory
     # every step, the output read back every step (copies pipelined with the kernels)
@@ -376,9 +461,13 @@ def run_gpu(args, rank, world, local_rank):
         return pa.decode_append(d["q"], d["key"], d["value"], k_cache, v_cache, d["tables"],
                                 d["ctx"], wl.scale, out=out, workspace=ws, plan=True).run
     e2e_ms, h2d, d2h = pipelined_e2e(batches, ("q", "tables", "ctx", "key", "value"), e2e_launch,
-                                     batches[0]["out"], device, K, args.warmup)
-    return {"wl": wl, "total_ms": total_ms, "decode_ms": decode_ms, "e2e_ms": e2e_ms,
-            "two_calls_ms": two_calls_ms,
+                                     batches[0]["out"], device, K, args.warmup,
+                                     repeats=max(5, R // 4))
+    flags |= pa.get_device_error()
+    return {"wl": wl, "step_ms": step_ms, "decode_ms": decode_ms, "e2e_ms": e2e_ms,
+            "two_calls_ms": two_calls_ms, "identity_ms": identity_ms, "repeats": R,
+            "step_ms_spread": [round(min(step_all), 5), round(max(step_all), 5)],
+            "used_blocks": used,
             "h2d": h2d, "d2h": d2h, "clocks": clocks, "flags": flags}
 
 
@@ -542,25 +631,17 @@ def run_gpu_prefill(args, rank, world, local_rank):
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize(device)
+    K = args.steps
+    R = repeats_for(estimate_ms(step, stream, device), K)
     sampler = ClockSampler(local_rank) if rank == 0 else None
     if sampler:
         sampler.start()
         time.sleep(0.3)
-    K = args.steps
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize(device)
     t0 = time.time()
-    ev[0].record(stream)
-    for i in range(K):
-        step(i)
-    ev[1].record(stream)
-    torch.cuda.synchronize(device)
+    step_ms, _ = timed_median(step, K, stream, device, world, R)
     t1 = time.time()
     clocks = sampler.stop(t0, t1) if sampler else None
     flags = pa.get_device_error(stream=stream)
-    total_ms = ev[0].elapsed_time(ev[1])
     # end to end: q from pinned host memory, out read back, every pass (copies pipelined)
     b0 = batches[0]
 
@@ -568,9 +649,9 @@ def run_gpu_prefill(args, rank, world, local_rank):
         return lambda st: pa.prefill(d["q"], k_cache, v_cache, b0["tables"], b0["ctx"], qs, wl.scale,
                                      maxq, out=out, stream=st)
     e2e_ms, h2d, d2h = pipelined_e2e([b0], ("q",), e2e_launch, b0["out"], device, min(K, 50),
-                                     args.warmup)
-    return {"wl": wl, "total_ms": total_ms, "decode_ms": total_ms / K,
-            "two_calls_ms": total_ms / K, "e2e_ms": e2e_ms,
+                                     args.warmup, repeats=max(3, R // 4))
+    return {"wl": wl, "step_ms": step_ms, "decode_ms": step_ms, "repeats": R,
+            "two_calls_ms": step_ms, "e2e_ms": e2e_ms,
             "h2d": h2d, "d2h": d2h, "clocks": clocks, "flags": flags}
 
 
@@ -623,7 +704,7 @@ print(json.dumps({{"tokens": k, "seconds": dt, "flops": flops}}))
 def prefill_line(args, res, world):
     wl = res["wl"]
     flops = prefill_flops(wl)
-    step_s = res["total_ms"] / 1e3 / args.steps
+    step_s = res["step_ms"] / 1e3
     value = world * flops / step_s / 1e12
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -636,7 +717,7 @@ def prefill_line(args, res, world):
     return {
         "metric": "paged prefill attention TFLOP/s (causal, over the block table)",
         "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(res["total_ms"] / args.steps, 4),
+        "warmup": args.warmup, "ms_per_step": round(res["step_ms"], 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
         "data": "synthetic (seeded normals; no dataset or weights)",
         "config": {
@@ -662,7 +743,7 @@ def prefill_line(args, res, world):
                 "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
                 "us_per_step": round(1e3 * res["e2e_ms"], 2), "method": E2E_METHOD},
         "clocks": res["clocks"],
-        "gpu_launches": args.steps,
+        "gpu_launches": res.get("repeats", 1) * 1 * args.steps,
         "device_error_flags": res["flags"],
     }
 
@@ -736,16 +817,14 @@ def run_gpu_swap(args, rank, world, local_rank):
 
     for i in range(args.warmup):
         step(i)
+    K = args.steps
+    R = repeats_for(estimate_ms(step, stream, device, n=2), K)
     sampler = ClockSampler(local_rank) if rank == 0 else None
     if sampler:
         sampler.start()
         time.sleep(0.3)
-    K = args.steps
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize(device)
     t0 = time.time()
-    total_ms = timed(step, K)
+    step_ms, _ = timed_median(step, K, stream, device, world, R)
     t1 = time.time()
     clocks = sampler.stop(t0, t1) if sampler else None
     flags = pa.get_device_error(stream=stream)
@@ -785,7 +864,7 @@ def run_gpu_swap(args, rank, world, local_rank):
     torch.cuda.synchronize(device)
     e2e_ms = (time.perf_counter() - w0) * 1e3 / ke
     flags |= pa.get_device_error(stream=stream)
-    return {"wl": wl, "total_ms": total_ms, "decode_ms": total_ms / K, "two_calls_ms": ce_ms,
+    return {"wl": wl, "step_ms": step_ms, "decode_ms": step_ms, "two_calls_ms": ce_ms, "repeats": R,
             "e2e_ms": e2e_ms, "h2d": moved + 8 * (len(out_pairs) + len(in_pairs)), "d2h": moved,
             "moved": moved, "blocks": len(out_pairs), "clocks": clocks, "flags": flags}
 
@@ -828,7 +907,7 @@ print(json.dumps({{"blocks": m, "seconds": dt, "bytes": 2 * dk.nbytes * 2}}))
 def swap_line(args, res, world):
     wl = res["wl"]
     step_bytes_ = 2 * res["moved"]  # out and in
-    step_s = res["total_ms"] / 1e3 / args.steps
+    step_s = res["step_ms"] / 1e3
     value = world * step_bytes_ / step_s / 1e9
     link = step_bytes_ / (res["two_calls_ms"] / 1e3) / 1e9
     cpu = oracle_swap_sample(args.workload, args.cpu_baseline_seconds) \
@@ -837,7 +916,7 @@ def swap_line(args, res, world):
         "metric": "paged KV swap GB/s (device pool -> pinned CPU pool -> device pool, "
                   "through the block tables)",
         "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(res["total_ms"] / args.steps, 4),
+        "warmup": args.warmup, "ms_per_step": round(res["step_ms"], 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u16 (bit copy)",
         "data": "synthetic (seeded normals; no dataset or weights)",
         "config": {
@@ -863,7 +942,7 @@ def swap_line(args, res, world):
                 "d2h_bytes_per_step": res["d2h"], "us_per_step": round(1e3 * res["e2e_ms"], 2),
                 "includes": "host planning by the C++ pool, pair upload, both launches"},
         "clocks": res["clocks"],
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": res.get("repeats", 1) * 2 * args.steps,
         "device_error_flags": res["flags"],
     }
 
@@ -996,6 +1075,8 @@ def run_gpu_prefix(args, rank, world, local_rank):
         pool.free_batch(ids)
 
     def timed(arm, K, host_inputs=None):
+        if world > 1:
+            torch.distributed.barrier()
         torch.cuda.synchronize(device)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         w0 = time.perf_counter()
@@ -1037,14 +1118,15 @@ def run_gpu_prefix(args, rank, world, local_rank):
     kev[1].record(stream)
     torch.cuda.synchronize(device)
     prefill_ms = kev[0].elapsed_time(kev[1]) / K
+    R = repeats_for(timed("cached", 3)[0], K)
     sampler = ClockSampler(local_rank) if rank == 0 else None
     if sampler:
         sampler.start()
         time.sleep(0.3)
-    if world > 1:
-        torch.distributed.barrier()
     t0 = time.time()
-    cached_ms, cached_dev_ms = timed("cached", K)
+    runs = [timed("cached", K) for _ in range(R)]   # (wall, device) ms per step
+    cached_ms = float(np.median([r_[0] for r_ in runs]))
+    cached_dev_ms = float(np.median([r_[1] for r_ in runs]))
     t1 = time.time()
     clocks = sampler.stop(t0, t1) if sampler else None
     uncached_ms, _ = timed("uncached", max(3, K // 4))
@@ -1077,7 +1159,7 @@ def run_gpu_prefix(args, rank, world, local_rank):
     e2e_ms, _ = timed("cached", max(3, min(K, 20)), host)
     flags = pa.get_device_error(stream=stream)
     h = host["cached"]
-    return {"wl": wl, "total_ms": cached_ms * K, "decode_ms": prefill_ms,
+    return {"wl": wl, "step_ms": cached_ms, "decode_ms": prefill_ms, "repeats": R,
             "two_calls_ms": uncached_ms, "e2e_ms": e2e_ms, "cached_dev_ms": cached_dev_ms,
             "h2d": sum(t.numel() * t.element_size() for t in h[:3]) + int(own.sum()) * 8 + n * T * 4,
             "d2h": h[3].numel() * h[3].element_size(), "hit": hit,
@@ -1138,7 +1220,7 @@ def prefix_line(args, res, world):
     wl = res["wl"]
     n = wl.num_seqs
     tokens = int(wl.context_lens.sum())
-    step_s = res["total_ms"] / 1e3 / args.steps
+    step_s = res["step_ms"] / 1e3
     value = world * tokens / step_s
     # FLOPs of the prefill launch: each uncached row at position p scores p + 1 keys
     flops = 0
@@ -1160,7 +1242,7 @@ def prefix_line(args, res, world):
                   "prompt; host lookup by block digests computed at arrival + cache write + "
                   "paged prefill of the uncached tokens)",
         "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(res["total_ms"] / args.steps, 4),
+        "warmup": args.warmup, "ms_per_step": round(res["step_ms"], 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
         "data": "synthetic (seeded normals and token ids; no dataset or weights)",
         "config": {
@@ -1194,7 +1276,7 @@ def prefix_line(args, res, world):
                 "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
                 "us_per_step": round(1e3 * res["e2e_ms"], 2)},
         "clocks": res["clocks"],
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": res.get("repeats", 1) * 2 * args.steps,
         "device_error_flags": res["flags"],
     }
 
@@ -1324,31 +1406,16 @@ def run_gpu_fp8(args, rank, world, local_rank):
     torch.cuda.synchronize(device)
     if pa.get_device_error(stream=stream):
         raise RuntimeError("device error flags set during warm-up")
+    K = args.steps
+    R = repeats_for(estimate_ms(step, stream, device), K)
     sampler = ClockSampler(local_rank) if rank == 0 else None
     if sampler:
         sampler.start()
         time.sleep(0.3)
-    K = args.steps
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize(device)
     t0 = time.time()
-    ev[0].record(stream)
-    for i in range(K):
-        step(i)
-    ev[1].record(stream)
-    torch.cuda.synchronize(device)
-    ev[2].record(stream)
-    for i in range(K):
-        decode_only(i)
-    ev[3].record(stream)
-    torch.cuda.synchronize(device)
-    ev[4].record(stream)
-    for i in range(K):
-        step_two_calls(i)
-    ev[5].record(stream)
-    torch.cuda.synchronize(device)
+    step_ms, _ = timed_median(step, K, stream, device, world, R)
+    decode_ms, _ = timed_median(decode_only, K, stream, device, world, R)
+    two_calls_ms, _ = timed_median(step_two_calls, K, stream, device, world, R)
     t1 = time.time()
     clocks = sampler.stop(t0, t1) if sampler else None
     flags = pa.get_device_error(stream=stream)
@@ -1361,10 +1428,11 @@ def run_gpu_fp8(args, rank, world, local_rank):
         return pa.decode_append_int4(d["q"], d["key"], d["value"], k8, v8, k4s, v4s, d["tables"],
                                      d["ctx"], wl.scale, out=out, workspace=ws, plan=True).run
     e2e_ms, h2d, d2h = pipelined_e2e(batches, ("q", "tables", "ctx", "key", "value"), e2e_launch,
-                                     batches[0]["out"], device, K, args.warmup)
+                                     batches[0]["out"], device, K, args.warmup,
+                                     repeats=max(5, R // 4))
     flags |= pa.get_device_error()
-    return {"wl": wl, "total_ms": ev[0].elapsed_time(ev[1]), "decode_ms": ev[2].elapsed_time(ev[3]) / K,
-            "two_calls_ms": ev[4].elapsed_time(ev[5]) / K, "e2e_ms": e2e_ms, "h2d": h2d, "d2h": d2h,
+    return {"wl": wl, "step_ms": step_ms, "decode_ms": decode_ms, "repeats": R,
+            "two_calls_ms": two_calls_ms, "e2e_ms": e2e_ms, "h2d": h2d, "d2h": d2h,
             "clocks": clocks, "flags": flags}
 
 
@@ -1455,7 +1523,7 @@ def fp8_line(args, res, world):
     fmt, _ = quant_recipe(args.workload)
     dec_b, resh_b = fp8_step_bytes(wl, fmt)
     fp8 = fmt == "fp8"
-    step_s = res["total_ms"] / 1e3 / args.steps
+    step_s = res["step_ms"] / 1e3
     value = world * (dec_b + resh_b) / step_s / 1e9
     peak, peak_kind = measured_peak()
     achieved = dec_b / (res["decode_ms"] / 1e3) / 1e9
@@ -1468,8 +1536,8 @@ def fp8_line(args, res, world):
                    "paged decode KV GB/s over INT4 blocks (4-bit codes + a float32 scale per "
                    "row) and % of GB300 HBM peak; µs per decode step"),
         "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(res["total_ms"] / args.steps, 5),
-        "us_per_step": round(1e3 * res["total_ms"] / args.steps, 2),
+        "warmup": args.warmup, "ms_per_step": round(res["step_ms"], 5),
+        "us_per_step": round(1e3 * res["step_ms"], 2),
         "us_per_step_two_calls": round(1e3 * res["two_calls_ms"], 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": (f"e4m3 K/V, {wl.dtype} q/out, f16 MMA" if fp8 else
@@ -1505,9 +1573,280 @@ def fp8_line(args, res, world):
                 "unit": "GB/s", "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
                 "us_per_step": round(1e3 * res["e2e_ms"], 2), "method": E2E_METHOD},
         "clocks": res["clocks"],
-        "gpu_launches": args.steps,
+        # per timed loop: steps (1 kernel each), decode alone (1), two-call steps (2)
+        "gpu_launches": res.get("repeats", 1) * 4 * args.steps,
+        "repeats": res.get("repeats", 1),
         "device_error_flags": res["flags"],
     }
+
+
+# ---------------------------------------------------------------- shared-prefix beams
+
+BEAM_WORKLOADS = ("beam",)
+
+
+def beam_place(pool, wl, base):
+    """Shared-prefix beams through the block pool (sequence ids base ..): each prompt's
+    parent holds the prefix and one generated token, forks into its beams, and each beam
+    then writes its private tokens; a beam's first write into the shared, partly filled
+    last block plans a copy.  Returns (slots and rows of the shared tokens per prompt,
+    the copy pairs, the private tokens' slots, block tables, context lengths)."""
+    import numpy as np
+    shared = []
+    for p in range(wl.prompts):
+        root = base + p * wl.beams
+        pool.allocate(root, wl.shared_tokens - 1)
+        slots = list(pool.slots(root, 0, wl.shared_tokens - 1))
+        s_new, cow = pool.append_slot(root)
+        assert cow is None
+        shared.append(np.array(slots + [s_new], dtype=np.int64))
+        for b in range(1, wl.beams):
+            pool.fork(root, root + b)
+    cows, slots = [], []
+    for k in range(wl.prompts * wl.beams):
+        for _ in range(int(wl.private_tokens[k])):
+            s_, cow = pool.append_slot(base + k)
+            if cow:
+                cows.append(cow)
+            slots.append(s_)
+    n = wl.prompts * wl.beams
+    tables = np.zeros((n, wl.max_blocks_per_seq), dtype=np.int32)
+    ctx = np.zeros(n, dtype=np.int32)
+    for k in range(n):
+        t = pool.block_table(base + k)
+        tables[k, :len(t)] = t
+        ctx[k] = pool.context_len(base + k)
+    return shared, cows, np.array(slots, dtype=np.int64), tables, ctx
+
+
+def beam_bytes(wl, ctx, n_pairs):
+    """Algorithmic bytes of a beam step: the decode's (every sequence reads its whole
+    context, shared blocks once per sequence), the copy-on-write block copies (read and
+    written, both caches) and the private rows written; and the distinct K/V bytes the
+    decode touches (shared blocks once)."""
+    e, hkv, d, B = 2, wl.num_kv_heads, wl.head_dim, wl.block_size
+    n = wl.prompts * wl.beams
+    kv = int(ctx.sum()) * hkv * d * e * 2
+    decode = kv + 2 * n * wl.num_q_heads * d * e + sum(-(-int(c) // B) for c in ctx) * 4 + 4 * n
+    copy = n_pairs * 2 * hkv * B * d * e * 2
+    rows = int(wl.private_tokens.sum()) * hkv * d * e * 2
+    unique_kv = (wl.prompts * wl.shared_tokens + int(wl.private_tokens.sum())) * hkv * d * e * 2
+    return decode, copy, rows, unique_kv
+
+
+def run_gpu_beam(args, rank, world, local_rank):
+    """The beam step (config of 2 prompts x 8 beams over a shared 1024-token prefix): the
+    copy-on-write copies of the shared last blocks (pa_copy_blocks), the beams' private
+    rows written (pa_reshape_and_cache), then decode over all 16 sequences (pa_decode).
+    Every step redoes the same copies and writes, so steps are identical.  ROTATE
+    placements in disjoint blocks of one pool rotate every step."""
+    import torch
+
+    import paged_kv_cache_149_gb300 as pa
+    import workloads
+    from paged_kv_cache_149_gb300 import build as _build
+
+    _build.build()
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    wl = workloads.beam()
+    dt = {"fp16": torch.float16, "bf16": torch.bfloat16}[wl.dtype]
+
+    def up(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(dt)
+    nb = ROTATE * wl.num_blocks
+    order = np.random.default_rng(1).permutation(nb).astype(np.int32)
+    pool = pa.BlockPool(nb, wl.block_size, order)
+    shape = (nb, wl.num_kv_heads, wl.block_size, wl.head_dim)
+    k_cache = torch.zeros(shape, dtype=dt, device=device)
+    v_cache = torch.zeros(shape, dtype=dt, device=device)
+    n = wl.prompts * wl.beams
+    pk = up(np.concatenate(wl.private_keys))
+    pv = up(np.concatenate(wl.private_values))
+    free0 = pool.num_free()
+    batches = []
+    for r in range(ROTATE):
+        shared, cows, slots, tables, ctx = beam_place(pool, wl, r * n)
+        if r == 0:
+            used = free0 - pool.num_free()
+        for p in range(wl.prompts):
+            pa.reshape_and_cache(up(wl.shared_keys[p]), up(wl.shared_values[p]), k_cache, v_cache,
+                                 torch.from_numpy(shared[p]).to(device))
+        pa.check_block_mapping(cows, nb)
+        batches.append({"pairs": torch.tensor(cows, dtype=torch.int32, device=device),
+                        "slots": torch.from_numpy(slots).to(device), "ctx_np": ctx,
+                        "tables": torch.from_numpy(tables).to(device),
+                        "ctx": torch.from_numpy(ctx).to(device), "q": up(wl.q),
+                        "out": torch.empty((n, wl.num_q_heads, wl.head_dim), dtype=dt, device=device)})
+    ws = pa.make_workspace(wl.num_q_heads, wl.num_kv_heads, wl.head_dim, device)
+    stream = torch.cuda.Stream(device)
+    torch.cuda.synchronize(device)
+    pa.get_device_error()
+
+    def step(i):
+        b = batches[i % ROTATE]
+        pa.copy_blocks(k_cache, v_cache, b["pairs"], stream=stream)
+        pa.reshape_and_cache(pk, pv, k_cache, v_cache, b["slots"], stream=stream)
+        pa.decode(b["q"], k_cache, v_cache, b["tables"], b["ctx"], wl.scale, out=b["out"],
+                  workspace=ws, stream=stream)
+
+    def decode_only(i):
+        b = batches[i % ROTATE]
+        pa.decode(b["q"], k_cache, v_cache, b["tables"], b["ctx"], wl.scale, out=b["out"],
+                  workspace=ws, stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+        decode_only(i)
+    torch.cuda.synchronize(device)
+    if pa.get_device_error(stream=stream):
+        raise RuntimeError("device error flags set during warm-up")
+    K = args.steps
+    R = repeats_for(estimate_ms(step, stream, device), K)
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    t0 = time.time()
+    step_ms, _ = timed_median(step, K, stream, device, world, R)
+    decode_ms, _ = timed_median(decode_only, K, stream, device, world, R)
+    t1 = time.time()
+    clocks = sampler.stop(t0, t1) if sampler else None
+    flags = pa.get_device_error(stream=stream)
+
+    # end to end: q, tables, lengths, private rows, slots and pairs from pinned host memory,
+    # the output read back
+    for b in batches:
+        b["pk"], b["pv"] = pk, pv
+
+    def e2e_launch(d, out):
+        def run(st):
+            pa.copy_blocks(k_cache, v_cache, d["pairs"], stream=st)
+            pa.reshape_and_cache(d["pk"], d["pv"], k_cache, v_cache, d["slots"], stream=st)
+            pa.decode(d["q"], k_cache, v_cache, d["tables"], d["ctx"], wl.scale, out=out,
+                      workspace=ws, stream=st)
+        return run
+    e2e_ms, h2d, d2h = pipelined_e2e(batches, ("q", "tables", "ctx", "pairs", "slots", "pk", "pv"),
+                                     e2e_launch, batches[0]["out"], device, K, args.warmup,
+                                     repeats=max(5, R // 4))
+    flags |= pa.get_device_error()
+    return {"wl": wl, "ctx": batches[0]["ctx_np"], "pairs": int(batches[0]["pairs"].shape[0]),
+            "step_ms": step_ms, "decode_ms": decode_ms, "two_calls_ms": step_ms, "repeats": R,
+            "e2e_ms": e2e_ms, "h2d": h2d, "d2h": d2h, "used_blocks": used, "clocks": clocks,
+            "flags": flags}
+
+
+def oracle_beam_sample(budget_s):
+    """The oracle's side of the beam step, single thread: its pool, cache writes and
+    copy-on-write copies, then its decode of whole beams until budget_s of CPU time."""
+    code = f"""
+import json, sys, time
+sys.path.insert(0, {ROOT!r})
+import numpy as np
+import workloads
+from oracle import attention, cache_ops, formats
+from oracle.block_pool import BlockPool
+wl = workloads.beam()
+B = wl.block_size
+pool = BlockPool(wl.num_blocks, B, wl.free_order)
+shape = (wl.num_blocks, wl.num_kv_heads, B, wl.head_dim)
+kc = np.zeros(shape, np.uint16); vc = kc.copy()
+for p in range(wl.prompts):
+    root = p * wl.beams
+    pool.allocate(root, wl.shared_tokens - 1)
+    sl = [pool.slot(root, t) for t in range(wl.shared_tokens - 1)]
+    s_new, _ = pool.append_slot(root)
+    kc, vc = cache_ops.reshape_and_cache(kc, vc, wl.shared_keys[p], wl.shared_values[p],
+                                         np.array(sl + [s_new], np.int64))
+    for b in range(1, wl.beams):
+        pool.fork(root, root + b)
+n = wl.prompts * wl.beams
+cows, slots, keys, values = [], [], [], []
+for k in range(n):
+    for i in range(int(wl.private_tokens[k])):
+        s_, cow = pool.append_slot(k)
+        if cow:
+            cows.append(cow)
+        slots.append(s_); keys.append(wl.private_keys[k][i]); values.append(wl.private_values[k][i])
+kc, vc = cache_ops.copy_blocks(kc, vc, cows)
+kc, vc = cache_ops.reshape_and_cache(kc, vc, np.stack(keys), np.stack(values), np.array(slots, np.int64))
+tables = np.zeros((n, wl.max_blocks_per_seq), np.int32); ctx = np.zeros(n, np.int32)
+for k in range(n):
+    t = pool.block_table(k); tables[k, :len(t)] = t; ctx[k] = pool.context_len(k)
+per, t0 = [], time.process_time()
+while time.process_time() - t0 < {budget_s} or not per:
+    s = len(per) % n
+    a = time.process_time()
+    attention.paged_decode_bits(wl.q, kc, vc, tables, ctx, wl.scale, B, wl.dtype, seqs=[s])
+    c = int(ctx[s])
+    nb = c * wl.num_kv_heads * wl.head_dim * 4 + 2 * wl.num_q_heads * wl.head_dim * 2 + (-(-c // B)) * 4 + 4
+    per.append((time.process_time() - a, nb))
+print(json.dumps({{"seqs": len(per), "seconds": sum(p[0] for p in per), "bytes": sum(p[1] for p in per)}}))
+"""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
+    if r.returncode != 0:
+        raise RuntimeError("beam oracle baseline failed:\n" + r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def beam_line(args, res, world):
+    wl = res["wl"]
+    dec_b, copy_b, rows_b, unique_kv = beam_bytes(wl, res["ctx"], res["pairs"])
+    step_b = dec_b + copy_b + rows_b
+    value = world * step_b / (res["step_ms"] / 1e3) / 1e9
+    peak, peak_kind = measured_peak()
+    achieved = dec_b / (res["decode_ms"] / 1e3) / 1e9
+    cpu = oracle_beam_sample(args.cpu_baseline_seconds) if args.cpu_baseline_seconds > 0 else None
+    n = wl.prompts * wl.beams
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(res["step_ms"], 5),
+        "us_per_step": round(1e3 * res["step_ms"], 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "data": "synthetic (seeded normals; no dataset or weights)",
+        "config": {
+            "workload": (f"beam: {wl.prompts} prompts x {wl.beams} beams sharing a "
+                         f"{wl.shared_tokens - 1}-token prefix + 1 shared token (65 blocks, "
+                         f"reference count {wl.beams}), 1..15 private tokens per beam (ctx "
+                         f"{int(res['ctx'].min())}..{int(res['ctx'].max())}), "
+                         f"{wl.num_q_heads} q / {wl.num_kv_heads} kv heads, head_dim "
+                         f"{wl.head_dim}, block_size {wl.block_size}; step = "
+                         f"{res['pairs']} copy-on-write block copies + the private rows "
+                         "written + decode over every beam"),
+            "l2": f"{ROTATE} placements in disjoint blocks rotated every step; a step's "
+                  f"distinct K/V ({unique_kv / 1e6:.0f} MB) fits in L2, and the beams of a "
+                  "prompt read the same prefix blocks, so L2 serves part of the decode",
+            "parallelism": f"replicas x{world}",
+        },
+        "roofline": {"bound": "hbm", "kernel": "decode_kernel (pa_decode)",
+                     "achieved": round(achieved, 1), "peak": peak,
+                     "peak_kind": f"{peak_kind} (HBM copy)", "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "algorithmic_bytes": dec_b, "distinct_kv_bytes": unique_kv,
+                     "decode_us": round(1e3 * res["decode_ms"], 2),
+                     "note": "algorithmic bytes count each beam's reads of the shared prefix; "
+                             "L2 absorbs the repeats, so the fraction can pass 1"},
+        "cpu_baseline": None if cpu is None else {
+            "value": round(cpu["bytes"] / cpu["seconds"] / 1e9, 4), "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"float64 NumPy oracle, single thread, {cpu['seqs']} beams decoded"},
+        "e2e": {"value": round(world * step_b / (res["e2e_ms"] / 1e3) / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
+                "us_per_step": round(1e3 * res["e2e_ms"], 2), "method": E2E_METHOD},
+        "clocks": res["clocks"],
+        # per timed loop: steps (copy + write + decode), decode alone (1)
+        "gpu_launches": res.get("repeats", 1) * 4 * args.steps,
+        "repeats": res.get("repeats", 1),
+        "device_error_flags": res["flags"],
+        "kv_memory": {"beams": n, "blocks_used": res["used_blocks"],
+                      "blocks_without_sharing": int(sum(-(-int(c) // wl.block_size)
+                                                        for c in res["ctx"])),
+                      "saved": round(1 - res["used_blocks"] /
+                                     sum(-(-int(c) // wl.block_size) for c in res["ctx"]), 4)},
+    }
+    return line
 
 
 def max_over_ranks(values):
@@ -1522,7 +1861,7 @@ def max_over_ranks(values):
 
 
 # per-rank times that the JSON line takes as the maximum over ranks
-RANK_TIMES = ("total_ms", "decode_ms", "two_calls_ms", "e2e_ms")
+RANK_TIMES = ("step_ms", "decode_ms", "two_calls_ms", "e2e_ms")
 
 
 def main(argv=None, runner=None, backend="nccl"):
@@ -1556,8 +1895,10 @@ def main(argv=None, runner=None, backend="nccl"):
     is_swap = args.workload in SWAP_WORKLOADS
     is_prefix = args.workload in PREFIX_WORKLOADS
     is_fp8 = args.workload in FP8_WORKLOADS or args.workload in INT4_WORKLOADS
+    is_beam = args.workload in BEAM_WORKLOADS
     default_runner = (run_gpu_prefill if is_prefill else run_gpu_swap if is_swap else
-                      run_gpu_prefix if is_prefix else run_gpu_fp8 if is_fp8 else run_gpu)
+                      run_gpu_prefix if is_prefix else run_gpu_fp8 if is_fp8 else
+                      run_gpu_beam if is_beam else run_gpu)
     res = (runner or default_runner)(args, rank, world, local_rank)
     if world > 1:
         res.update(zip(RANK_TIMES, max_over_ranks([res[k] for k in RANK_TIMES])))
@@ -1566,9 +1907,9 @@ def main(argv=None, runner=None, backend="nccl"):
             import torch
             torch.distributed.destroy_process_group()
         return
-    if is_prefill or is_swap or is_prefix or is_fp8:
+    if is_prefill or is_swap or is_prefix or is_fp8 or is_beam:
         line = (prefill_line if is_prefill else swap_line if is_swap else
-                prefix_line if is_prefix else fp8_line)
+                prefix_line if is_prefix else fp8_line if is_fp8 else beam_line)
         print(json.dumps(line(args, res, world)))
         if world > 1:
             import torch
@@ -1576,7 +1917,7 @@ def main(argv=None, runner=None, backend="nccl"):
         return
     wl = res["wl"]
     dec_b, resh_b, padded = step_bytes(wl)
-    step_s = res["total_ms"] / 1e3 / args.steps
+    step_s = res["step_ms"] / 1e3
     value = world * (dec_b + resh_b) / step_s / 1e9
     peak, peak_kind = measured_peak()
     achieved = dec_b / (res["decode_ms"] / 1e3) / 1e9
@@ -1591,8 +1932,8 @@ def main(argv=None, runner=None, backend="nccl"):
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(res["total_ms"] / args.steps, 5),
-        "us_per_step": round(1e3 * res["total_ms"] / args.steps, 2),
+        "ms_per_step": round(res["step_ms"], 5),
+        "us_per_step": round(1e3 * res["step_ms"], 2),
         "us_per_step_two_calls": round(1e3 * res["two_calls_ms"], 2),
         "higher_is_better": True,
         "scaling": "weak",
@@ -1641,10 +1982,26 @@ def main(argv=None, runner=None, backend="nccl"):
             "method": E2E_METHOD,
         },
         "clocks": res["clocks"],
-        # timed: steps (1 kernel each), decode alone (1 each), two-call steps (2 each)
-        "gpu_launches": 4 * args.steps,
+        # per timed loop: steps (1 kernel each), decode alone (1 each), two-call steps (2
+        # each), decode over contiguous placement (1 each)
+        "gpu_launches": res.get("repeats", 1) * 5 * args.steps,
+        "repeats": res.get("repeats", 1),
+        "timing": "median over `repeats` timed loops of exactly `steps` steps (each loop "
+                  "between a synchronise on both sides)",
         "device_error_flags": res["flags"],
     }
+    if "identity_ms" in res:
+        # the cost of paging: the same decode over the same batches placed in shuffled
+        # blocks (the step's placement) against each sequence's blocks in physical order
+        line["paged_overhead"] = {
+            "shuffled_us": round(1e3 * res["decode_ms"], 2),
+            "contiguous_us": round(1e3 * res["identity_ms"], 2),
+            "ratio": round(res["decode_ms"] / res["identity_ms"], 4),
+            "method": "pa_decode on identity block tables (each sequence's blocks consecutive "
+                      "in memory) against the shuffled pool placement; same kernel, same batch",
+        }
+    if "used_blocks" in res:
+        line["kv_memory"] = kv_memory(wl, res["used_blocks"])
     print(json.dumps(line))
     if world > 1:
         import torch

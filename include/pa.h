@@ -68,7 +68,8 @@ enum {
 #define PA_DEVERR_BAD_CONTEXT 0x2u  /* decode: context length < 1 or > max_blocks_per_seq * B */
 #define PA_DEVERR_BAD_SLOT    0x4u  /* reshape_and_cache: slot >= num_blocks * B */
 #define PA_DEVERR_BAD_PAIR    0x8u  /* copy_blocks / swap_blocks: a block id outside its pool */
-#define PA_DEVERR_TIMEOUT     0x10u /* decode: a pipeline wait gave up (about 1 s); output invalid */
+#define PA_DEVERR_TIMEOUT     0x10u /* a bounded wait gave up (about 1 s; prefill pipeline, decode
+                                         split-KV merge): output invalid */
 
 /*
  * pa_reshape_and_cache -- write each new token's K and V rows into its cache slot.
@@ -107,9 +108,12 @@ int pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void
  * physical blocks (and the table with them) gives bit-identical output.
  *
  * workspace: device scratch of at least pa_decode_workspace_size(...) bytes for the
- * split pieces, 16-byte aligned, owned by the caller, not read before it is written.
- * Concurrent pa_decode calls must not share a workspace.  Returns PA_ERR_WORKSPACE if
- * it is NULL or too small.  num_seqs == 0 is a no-op.
+ * split pieces and their arrival counters, 16-byte aligned, owned by the caller.  Its
+ * contents between calls do not matter: a counter left by another call (or never
+ * written) is recognised by a tag that differs from call to call, and each merge leaves
+ * its counter at zero, so calls replayed from a captured CUDA graph, which repeat their
+ * tag, start from zero too.  Concurrent pa_decode calls must not share a workspace.
+ * Returns PA_ERR_WORKSPACE if it is NULL or too small.  num_seqs == 0 is a no-op.
  *
  * Ordering: a launch is a programmatic dependent of the kernel before it in the stream.
  * It reads context_lens and block_tables (to plan its work) while that kernel drains,
@@ -294,7 +298,9 @@ int pa_decode_append(const void* q, const void* key_new, const void* value_new, 
  *     first call before any stream capture begins.
  *   - A device and head shape needing more than 32 MiB of decode scratch (more than about
  *     250 SMs at 16 query heads per kv head and head_dim 128) gets PA_ERR_WORKSPACE and
- *     nothing is launched.  Other errors are pa_decode's.
+ *     nothing is launched.
+ *   - q must be device memory of the current device (the scratch is per device); a q
+ *     elsewhere gets PA_ERR_ARG.  Other errors are pa_decode's.
  */
 int pa_decode_fixed_scratch(const void* q, const void* k_cache, const void* v_cache,
                             const int32_t* block_tables, int max_blocks_per_seq,
@@ -459,6 +465,10 @@ int pa_pool_allocate_prefix(pa_pool* pool, int64_t seq_id, const int32_t* tokens
  * start, a decreasing offset, a span longer than INT_MAX or a table wider than
  * table_width is PA_ERR_ARG before anything changes.  On a later error the requests
  * before the failing one stay allocated: *n_done (may be NULL) says how many. */
+/* The table width a batch of n requests needs (tokens token_start[r] .. token_start[r+1]-1
+ * each): the largest number of blocks one of them takes, ceil(tokens / B); PA_ERR_ARG for
+ * a negative start or a decreasing offset. */
+int pa_pool_table_width(const pa_pool* pool, int n, const int64_t* token_start);
 int pa_pool_allocate_prefix_batch(pa_pool* pool, int n, const int64_t* seq_ids,
                                   const int32_t* tokens, const int64_t* token_start,
                                   const uint8_t* extras, const int64_t* extra_start,

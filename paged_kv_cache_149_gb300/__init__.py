@@ -18,6 +18,7 @@ Layouts (row-major):
     block_mapping [num_pairs, 2] int32
 """
 import ctypes
+import functools
 import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -101,6 +102,7 @@ SIGNATURES = {
     "pa_pool_cpu_refcount": (_i32, [_vp, _c.c_int32]),
     "pa_pool_allocate_prefix": (_i32, [_vp, _i64, _vp, _i32, _vp, _i32, _c.POINTER(_c.c_int)]),
     "pa_pool_num_cached": (_i32, [_vp]),
+    "pa_pool_table_width": (_i32, [_vp, _i32, _vp]),
     "pa_pool_allocate_prefix_batch": (_i32, [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                              _i32, _c.POINTER(_c.c_int)]),
     "pa_pool_allocate_hashed_batch": (_i32, [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32,
@@ -165,6 +167,43 @@ def _check(status, what):
     return status
 
 
+def _switch_to(dev):
+    """The device to make current for a call on tensors of `dev`, or None when it already
+    is (the library works on the current device: its SM count, error word and scratch)."""
+    import torch
+    if dev is None or dev.type != "cuda" or dev.index is None:
+        return None
+    return None if dev.index == torch.cuda.current_device() else dev
+
+
+def _runs_on(pick):
+    """Decorator: run the call with the device `pick(*args, **kw)` current."""
+    def deco(fn):
+        @functools.wraps(fn)
+        def wrapped(*args, **kw):
+            dev = _switch_to(pick(*args, **kw))
+            if dev is None:
+                return fn(*args, **kw)
+            import torch
+            with torch.cuda.device(dev):
+                return fn(*args, **kw)
+        return wrapped
+    return deco
+
+
+# the device of the call's first tensor argument
+_on_first = _runs_on(lambda t, *args, **kw: t.device)
+
+
+def _pool_device(src, dst, *args, device=None, **kw):
+    """The device of a copy between pools that may be pinned CPU memory."""
+    import torch
+    if device is not None:
+        return torch.device(device)
+    firsts = (src[0], dst[0]) if isinstance(src, (tuple, list)) else (src, dst)
+    return next((t.device for t in firsts if t.is_cuda), None)
+
+
 class Launch:
     """A library call whose arguments were checked and marshalled once (``plan=True`` on
     the decode step functions): ``run(stream)`` issues it again on ``stream`` over the
@@ -173,7 +212,8 @@ class Launch:
     arguments are raw device addresses, so the Launch holds a reference to every tensor
     they point into (a workspace the call created included): none is freed, and its
     memory reused, while the Launch can still run.  Drop the Launch only after its last
-    run has finished, or ordered before later work on the stream it ran on."""
+    run has finished, or ordered before later work on the stream it ran on.  A run makes
+    the planned tensors' device current if another one is."""
 
     def __init__(self, name, args, out, keep=()):
         self._fn = getattr(lib(), name)
@@ -181,9 +221,16 @@ class Launch:
         self._args = args
         self._keep = tuple(keep)
         self.out = out
+        self.device = out.device
 
     def run(self, stream):
-        st = self._fn(*self._args, stream.cuda_stream)
+        dev = _switch_to(self.device)
+        if dev is None:
+            st = self._fn(*self._args, stream.cuda_stream)
+        else:
+            import torch
+            with torch.cuda.device(dev):
+                st = self._fn(*self._args, stream.cuda_stream)
         if st < 0:
             _check(st, self._name)
         return self.out
@@ -241,6 +288,7 @@ def _dev(t, name, dtype=None):
     return t.data_ptr()
 
 
+@_on_first
 def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, stream=None):
     """k_cache[slot // B, h, slot % B] = key[i, h] (and V) for every slot >= 0."""
     import torch
@@ -281,6 +329,7 @@ def _scratch(num_q_heads, num_kv_heads, head_dim, device, stream):
         return make_workspace(num_q_heads, num_kv_heads, head_dim, device)
 
 
+@_on_first
 def decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=None, workspace=None,
            stream=None):
     """Paged decode attention; returns ``out`` [num_seqs, num_q_heads, head_dim]."""
@@ -306,6 +355,7 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=None, wor
     return out
 
 
+@_on_first
 def decode_append(q, key_new, value_new, k_cache, v_cache, block_tables, context_lens, scale,
                   out=None, workspace=None, stream=None, plan=False):
     """One decode step in one kernel: writes each sequence's newest token (``key_new`` /
@@ -349,6 +399,7 @@ def _fp8_cache(t, name):
     return _dev(t, name)
 
 
+@_on_first
 def reshape_and_cache_fp8(key, value, k_cache, v_cache, slot_mapping, k_scale, v_scale,
                           stream=None):
     """FP8 cache write: k_cache[slot // B, h, slot % B] = E4M3(key[i, h] / k_scale) (and V)."""
@@ -366,6 +417,7 @@ def reshape_and_cache_fp8(key, value, k_cache, v_cache, slot_mapping, k_scale, v
     _check(st, "pa_reshape_and_cache_fp8")
 
 
+@_on_first
 def decode_fp8(q, k_cache, v_cache, block_tables, context_lens, scale, k_scale, v_scale,
                out=None, workspace=None, stream=None):
     """Paged decode over FP8 E4M3 blocks (codes times k_scale / v_scale); q and out are
@@ -391,6 +443,7 @@ def decode_fp8(q, k_cache, v_cache, block_tables, context_lens, scale, k_scale, 
     return out
 
 
+@_on_first
 def decode_append_fp8(q, key_new, value_new, k_cache, v_cache, block_tables, context_lens,
                       scale, k_scale, v_scale, out=None, workspace=None, stream=None, plan=False):
     """One FP8 decode step in one kernel: each sequence's newest K/V row is quantised into
@@ -423,6 +476,7 @@ def decode_append_fp8(q, key_new, value_new, k_cache, v_cache, block_tables, con
     return out
 
 
+@_on_first
 def prefill(q, k_cache, v_cache, block_tables, context_lens, query_start, scale,
             max_query_len, out=None, stream=None):
     """Causal attention of each sequence's newest tokens (q rows query_start[s] ..
@@ -449,6 +503,7 @@ def prefill(q, k_cache, v_cache, block_tables, context_lens, query_start, scale,
     return out
 
 
+@_on_first
 def decode_fixed_scratch(q, k_cache, v_cache, block_tables, context_lens, scale, out=None,
                          stream=None):
     """Paged decode that allocates nothing on the device: its scratch is a fixed array
@@ -484,6 +539,7 @@ def _int4_cache(codes, scales, name):
     return _dev(codes, name), _dev(scales, name + " scales")
 
 
+@_on_first
 def reshape_and_cache_int4(key, value, k_codes, v_codes, k_scales, v_scales, slot_mapping,
                            stream=None):
     """INT4 cache write: the row key[i, h] gets s = max|x| / 7 and codes rint(x / s) in
@@ -503,6 +559,7 @@ def reshape_and_cache_int4(key, value, k_codes, v_codes, k_scales, v_scales, slo
     _check(st, "pa_reshape_and_cache_int4")
 
 
+@_on_first
 def decode_int4(q, k_codes, v_codes, k_scales, v_scales, block_tables, context_lens, scale,
                 out=None, workspace=None, stream=None):
     """Paged decode over INT4 blocks (codes [NB, Hkv, B, d/2] uint8, scales [NB, Hkv, B])."""
@@ -528,6 +585,7 @@ def decode_int4(q, k_codes, v_codes, k_scales, v_scales, block_tables, context_l
     return out
 
 
+@_on_first
 def decode_append_int4(q, key_new, value_new, k_codes, v_codes, k_scales, v_scales, block_tables,
                        context_lens, scale, out=None, workspace=None, stream=None, plan=False):
     """One INT4 decode step in one kernel: each sequence's newest K/V row is quantised into
@@ -561,6 +619,7 @@ def decode_append_int4(q, key_new, value_new, k_codes, v_codes, k_scales, v_scal
     return out
 
 
+@_on_first
 def copy_blocks_int4(k_codes, v_codes, k_scales, v_scales, block_mapping, stream=None):
     """copy_blocks for INT4 blocks: codes and scales of each (src, dst) pair."""
     import torch
@@ -575,6 +634,7 @@ def copy_blocks_int4(k_codes, v_codes, k_scales, v_scales, block_mapping, stream
     _check(st, "pa_copy_blocks_int4")
 
 
+@_runs_on(_pool_device)
 def swap_blocks_int4(src, dst, block_mapping, stream=None, device=None):
     """swap_blocks for INT4 blocks; src and dst are (k_codes, v_codes, k_scales, v_scales)
     pools, CUDA tensors or pinned CPU tensors."""
@@ -600,6 +660,7 @@ def swap_blocks_int4(src, dst, block_mapping, stream=None, device=None):
     _check(st, "pa_swap_blocks_int4")
 
 
+@_on_first
 def copy_blocks(k_cache, v_cache, block_mapping, stream=None):
     """k_cache[dst] = k_cache[src] and v_cache[dst] = v_cache[src] for each (src, dst)."""
     import torch
@@ -623,6 +684,7 @@ def _reachable(t, name, dtype=None):
     return t.data_ptr()
 
 
+@_runs_on(_pool_device)
 def swap_blocks(src_k, src_v, dst_k, dst_v, block_mapping, stream=None, device=None):
     """dst_k[d] = src_k[s] and dst_v[d] = src_v[s] for each (s, d) of block_mapping, in one
     kernel launch.  Pools and mapping may be CUDA tensors or pinned CPU tensors (swap-out:
@@ -653,11 +715,21 @@ def check_block_mapping(pairs, num_blocks):
 
 
 def get_device_error(stream=None, device=None):
-    """Synchronise the stream, then read and clear the device error word."""
+    """Synchronise the stream, then read and clear the error word of `device` (default:
+    the stream's device, else the current one)."""
     import torch
-    dev = torch.device("cuda") if device is None else torch.device(device)
+    if device is None:
+        dev = stream.device if stream is not None else torch.device("cuda", torch.cuda.current_device())
+    else:
+        dev = torch.device(device)
+    sw = _switch_to(dev)
     v = ctypes.c_uint32(0)
-    _check(lib().pa_get_device_error(_stream_ptr(stream, dev), ctypes.byref(v)), "pa_get_device_error")
+    if sw is None:
+        st = lib().pa_get_device_error(_stream_ptr(stream, dev), ctypes.byref(v))
+    else:
+        with torch.cuda.device(sw):
+            st = lib().pa_get_device_error(_stream_ptr(stream, dev), ctypes.byref(v))
+    _check(st, "pa_get_device_error")
     return v.value
 
 
@@ -828,7 +900,8 @@ class BlockPool:
         _need(ts.shape == (n + 1,), "token_start must have n + 1 entries")
         lens = np.diff(ts)
         if table_width is None:
-            table_width = int(-(-lens.max() // self.block_size)) if n else 0
+            table_width = _check(lib().pa_pool_table_width(self._h, n, ts.ctypes.data),
+                                 "pa_pool_table_width")
         _need(n == 0 or (ts[0] >= 0 and ts[-1] <= tok.size and (lens >= 0).all()),
               "token_start must be non-decreasing within tokens")
         if out is None:

@@ -57,6 +57,7 @@
 #include <random>
 #include <type_traits>
 
+#include "pa_arrive.h"
 #include "pa_common.cuh"
 #include "pa_internal.h"
 
@@ -443,19 +444,24 @@ __device__ __forceinline__ CutPiece cut_piece(const Fam& f, int pi, const PairHe
   return cp;
 }
 
-// Count one piece in at a pair's counter; returns the pieces counted so far this call.  The
-// counter holds epoch << 24 | count; a value with another epoch is stale (an earlier call
-// or never-written workspace) and counts as zero.  The loop retries only when another
-// arrival changed the counter in between, so it ends after at most one try per piece.
-__device__ __forceinline__ int arrive(unsigned long long* ctr, unsigned long long epoch) {
-  unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(ctr);
-  for (int tries = 0; tries < (1 << 20); ++tries) {
-    const unsigned long long want = (cur >> 24) == epoch ? cur + 1 : (epoch << 24) | 1ull;
-    const unsigned long long prev = atomicCAS(ctr, cur, want);
-    if (prev == cur) return static_cast<int>(want & 0xffffffull);
-    cur = prev;
+// Count one piece in at a pair's counter (pa_arrive.h): the count this arrival makes
+// (n: it completed the pair, and the counter is back at zero), or -1 if it gave up.  The
+// loop retries only when another arrival changed the counter in between, so it ends after
+// at most one try per piece.
+struct DeviceCas {
+  __device__ unsigned long long operator()(unsigned long long* a, unsigned long long e,
+                                           unsigned long long d) const {
+    return atomicCAS(a, e, d);
   }
-  return -1;  // (unreachable in practice: no merge rather than a wrong one)
+};
+struct DeviceLoad {
+  __device__ unsigned long long operator()(unsigned long long* a) const {
+    return *reinterpret_cast<volatile unsigned long long*>(a);
+  }
+};
+
+__device__ __forceinline__ int arrive(unsigned long long* ctr, unsigned long long epoch, int n) {
+  return arrive_count(ctr, epoch, n, DeviceCas(), DeviceLoad());
 }
 
 // Merge the pieces of a cut pair held by CTAs c..c_last (c's piece in slot `first_slot`,
@@ -517,29 +523,14 @@ __device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity) {
   }
 }
 
-// Wait for phase 0 of a single-use mbarrier, bounded by kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait_once(uint32_t bar) { return mbar_wait_limit(bar, 0); }
 
-// One warp merges the cut pairs it completed (up to two) through its own ring, which is
-// idle once the share is streamed: every piece's O is copied in by one bulk copy per piece
-// and its (m, l) by plain loads (a single round trip to L2 for all pieces), then the
-// pieces are folded in CTA order: M = max m_i, w_i = 2^(m_i - M), L = sum l_i w_i,
-// out = sum w_i acc_i / L.  Returns false, having done nothing, when the pieces do not fit
-// in the ring.
+// merge_staged when every piece of both pairs fits in the ring at once: every piece's O
+// by one bulk copy, the (m, l) by plain loads behind them, a single round trip.
 template <int D, typename T, bool QK>
-__device__ bool merge_staged(const Params& p, int pi, const CutPiece& job0, const CutPiece& job1,
-                             int njobs, uint32_t ring, uint8_t* ring_ptr, int ring_bytes,
-                             uint32_t bar, int lane) {
+__device__ bool merge_staged_once(const Params& p, int pi, const CutPiece& job0,
+                                  const CutPiece& job1, int njobs, uint32_t ring,
+                                  uint8_t* ring_ptr, uint32_t bar, uint32_t& bar_phase, int lane) {
   const int hpp = p.heads_per_pair;
-  int need = 0;
-  for (int j = 0; j < njobs; ++j) {
-    const CutPiece& cp = j == 0 ? job0 : job1;
-    need += (cp.c_last - cp.c_first + 1) * cp.nh * (D * 4 + 8);
-  }
-  if (need > ring_bytes) return false;
-  // layout in the ring: per job, per piece: acc [nh][D] floats, then all (m, l) pairs.
-  // Lane i copies piece i's acc with one bulk copy (cp.async.bulk; completion counted in
-  // bytes on this warp's mbarrier); the (m, l) pairs come in through plain loads.
   const int np0 = job0.c_last - job0.c_first + 1;
   const int np1 = njobs > 1 ? job1.c_last - job1.c_first + 1 : 0;
   const uint32_t rb0 = job0.nh * D * 4, rb1 = job1.nh * D * 4;
@@ -574,16 +565,14 @@ __device__ bool merge_staged(const Params& p, int pi, const CutPiece& job0, cons
     }
   }
   __syncwarp();  // (the (m, l) stores, before lanes read other lanes' entries)
-  // Pass 1, one lane per (job, head): M = max m_i, then each piece's weight 2^(m_i - M)
-  // (0 for an empty piece) in place of m_i, and L = sum l_i 2^(m_i - M) in place of the
-  // first piece's l (bad pieces, l < 0, make L negative: the head's output is zeros).
+  // Pass 1, one lane per (job, head): M, the weights in place of the m_i, and L in place
+  // of the first piece's l (negative for a bad piece: zeros out).
   {
     int moff = 0;
     for (int j = 0; j < njobs; ++j) {
       const CutPiece& cp = j == 0 ? job0 : job1;
       const int np = cp.c_last - cp.c_first + 1;
-      if (lane < cp.nh) {
-        const int h = lane;
+      for (int h = lane; h < cp.nh; h += 32) {
         float M = -INFINITY;
         bool bad = false;
         for (int i = 0; i < np; ++i) {
@@ -599,12 +588,14 @@ __device__ bool merge_staged(const Params& p, int pi, const CutPiece& job0, cons
           v.x = w;
           ml[moff + i * cp.nh + h] = v;
         }
-        ml[moff + h].y = bad ? -1.f : L;  // (read back below only through this slot)
+        ml[moff + h].y = bad ? -1.f : L;
       }
       moff += np * cp.nh;
     }
   }
-  if (!mbar_wait_once(bar)) {  // (bounded; never expected to expire)
+  const bool landed = mbar_wait_limit(bar, bar_phase);  // (bounded; never expected to expire)
+  bar_phase ^= 1u;
+  if (!landed) {
     if (lane == 0) atomicOr(p.err, kErrTimeout);
     return true;
   }
@@ -644,6 +635,187 @@ __device__ bool merge_staged(const Params& p, int pi, const CutPiece& job0, cons
   return true;
 }
 
+// One warp merges the cut pairs it completed (up to two) through its own ring, which is
+// idle once the share is streamed.  When everything fits, merge_staged_once stages it in
+// one round trip.  Otherwise every piece's (m, l) comes in by plain loads (one round trip
+// for all pieces of both pairs), then every piece's O by one bulk copy per piece, as many
+// pieces at a time as the ring holds, so a pair cut into any number of pieces is merged in
+// ring-sized chunks.  The pieces are folded in CTA order:
+//   M = max m_i,  w_i = 2^(m_i - M),  L = sum l_i w_i,  out = sum w_i acc_i / L,
+// with the same fused multiply-adds as merge_pieces, so a pair's output does not depend on
+// which CTA merges it.  Returns false, having done nothing, when the (m, l) of the pieces
+// do not fit in half the ring (a pair cut into thousands of pieces): merge_pieces then.
+// (Not inlined: the chunked path is rare, and its registers stay out of the decode loop's
+// budget.)
+template <int D, typename T, bool QK>
+__device__ __noinline__ bool merge_staged_chunked(const Params& p, int pi, const CutPiece& job0,
+                                                  const CutPiece& job1, int njobs, uint32_t ring,
+                                                  uint8_t* ring_ptr, int ring_bytes, uint32_t bar,
+                                                  uint32_t& bar_phase, int lane);
+
+template <int D, typename T, bool QK>
+__device__ __forceinline__ bool merge_staged(const Params& p, int pi, const CutPiece& job0,
+                                             const CutPiece& job1, int njobs, uint32_t ring,
+                                             uint8_t* ring_ptr, int ring_bytes, uint32_t bar,
+                                             uint32_t& bar_phase, int lane) {
+  int mlen = 0;  // (m, l) entries of every piece of every job
+  for (int j = 0; j < njobs; ++j) {
+    const CutPiece& cp = j == 0 ? job0 : job1;
+    mlen += (cp.c_last - cp.c_first + 1) * cp.nh;
+  }
+  const uint32_t ml_bytes = (static_cast<uint32_t>(mlen) * 8u + 127u) & ~127u;
+  const int np0 = job0.c_last - job0.c_first + 1;
+  const int np1 = njobs > 1 ? job1.c_last - job1.c_first + 1 : 0;
+  const uint32_t acc_bytes = np0 * job0.nh * D * 4 + np1 * job1.nh * D * 4;
+  if (acc_bytes + ml_bytes <= static_cast<uint32_t>(ring_bytes))
+    return merge_staged_once<D, T, QK>(p, pi, job0, job1, njobs, ring, ring_ptr, bar, bar_phase,
+                                       lane);
+  return merge_staged_chunked<D, T, QK>(p, pi, job0, job1, njobs, ring, ring_ptr, ring_bytes, bar,
+                                        bar_phase, lane);
+}
+
+template <int D, typename T, bool QK>
+__device__ __noinline__ bool merge_staged_chunked(const Params& p, int pi, const CutPiece& job0,
+                                                  const CutPiece& job1, int njobs, uint32_t ring,
+                                                  uint8_t* ring_ptr, int ring_bytes, uint32_t bar,
+                                                  uint32_t& bar_phase, int lane) {
+  constexpr int C4 = D / 4;  // 4-float chunks of a head row
+  constexpr int NI = 8;      // a lane's chunks of a pair's rows per round (256 a warp)
+  const int hpp = p.heads_per_pair;
+  auto piece_of = [&](const CutPiece& cp, int cc) {
+    return (static_cast<size_t>(cc) * 2 + (cc == cp.c_first ? cp.first_slot : 0)) * p.gs + pi;
+  };
+  int mlen = 0;  // (m, l) entries of every piece of every job
+  for (int j = 0; j < njobs; ++j) {
+    const CutPiece& cp = j == 0 ? job0 : job1;
+    mlen += (cp.c_last - cp.c_first + 1) * cp.nh;
+  }
+  const uint32_t ml_bytes = (static_cast<uint32_t>(mlen) * 8u + 127u) & ~127u;
+  if (2 * static_cast<int>(ml_bytes) > ring_bytes) return false;
+  // (m, l) of every piece at the start of the ring; the O chunks after them.
+  float2* ml = reinterpret_cast<float2*>(ring_ptr);
+  const uint32_t acc0 = ml_bytes;
+  const int acc_room = ring_bytes - static_cast<int>(ml_bytes);
+  __syncwarp();  // (every lane is done with the ring's last stage)
+  {
+    int k = 0;
+    for (int j = 0; j < njobs; ++j) {
+      const CutPiece& cp = j == 0 ? job0 : job1;
+      const int np = cp.c_last - cp.c_first + 1;
+      for (int i = lane; i < np * cp.nh; i += 32) {
+        const int cc = cp.c_first + i / cp.nh, h = i % cp.nh;
+        const float* src = p.part_ml + (piece_of(cp, cc) * hpp + h) * 2;
+        ml[k + i] = make_float2(__ldcg(src), __ldcg(src + 1));
+      }
+      k += np * cp.nh;
+    }
+  }
+  __syncwarp();  // (the (m, l) stores, before lanes read other lanes' entries)
+  // Pass 1, one lane per (job, head): M = max m_i, then each piece's weight 2^(m_i - M)
+  // (0 for an empty piece) in place of m_i, and L = sum l_i 2^(m_i - M) in place of the
+  // first piece's l (bad pieces, l < 0, make L negative: the head's output is zeros).
+  {
+    int moff = 0;
+    for (int j = 0; j < njobs; ++j) {
+      const CutPiece& cp = j == 0 ? job0 : job1;
+      const int np = cp.c_last - cp.c_first + 1;
+      for (int h = lane; h < cp.nh; h += 32) {
+        float M = -INFINITY;
+        bool bad = false;
+        for (int i = 0; i < np; ++i) {
+          const float2 v = ml[moff + i * cp.nh + h];
+          M = fmaxf(M, v.x);
+          bad |= v.y < 0.f;
+        }
+        float L = 0.f;
+        for (int i = 0; i < np; ++i) {
+          float2 v = ml[moff + i * cp.nh + h];
+          const float w = v.x == -INFINITY ? 0.f : exp2f(v.x - M);
+          L = fmaf(v.y, w, L);
+          v.x = w;
+          ml[moff + i * cp.nh + h] = v;
+        }
+        ml[moff + h].y = bad ? -1.f : L;  // (read back below only through this slot)
+      }
+      moff += np * cp.nh;
+    }
+  }
+  // Pass 2, per job and round of 256 output chunks: out = sum_i w_i acc_i / L, pieces in
+  // CTA order, staged in chunks.
+  int moff = 0;
+  for (int j = 0; j < njobs; ++j) {
+    const CutPiece& cp = j == 0 ? job0 : job1;
+    const int np = cp.c_last - cp.c_first + 1;
+    const uint32_t rb = static_cast<uint32_t>(cp.nh) * D * 4;  // O bytes of one piece
+    const int cap = acc_room / static_cast<int>(rb);          // pieces a chunk holds
+    for (int base = 0; base < cp.nh * C4; base += 32 * NI) {
+    float4 O[NI];
+#pragma unroll
+    for (int i = 0; i < NI; ++i) O[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c0 = 0; c0 < np; c0 += cap) {
+      const int nc = min(cap, np - c0);
+      __syncwarp();  // (every lane is done reading the previous chunk)
+      // the ring was last read through the generic proxy; the bulk copies write it
+      // through the async proxy
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nc) * rb);
+      __syncwarp();
+      for (int i = lane; i < nc; i += 32)
+        bulk_g2s(ring + acc0 + i * rb, p.part_acc + piece_of(cp, cp.c_first + c0 + i) * hpp * D,
+                 rb, bar);
+      const bool landed = mbar_wait_limit(bar, bar_phase);  // (bounded; never expected to expire)
+      bar_phase ^= 1u;
+      if (!landed) {
+        if (lane == 0) atomicOr(p.err, kErrTimeout);
+        // the copies may still land: leave the ring (and the rest of the merge) alone
+        return true;
+      }
+      const float* acc = reinterpret_cast<const float*>(ring_ptr + acc0);
+#pragma unroll
+      for (int it = 0; it < NI; ++it) {
+        const int idx = base + lane + 32 * it;
+        if (idx >= cp.nh * C4) continue;
+        const int h = idx / C4, d4 = (idx % C4) * 4;
+#pragma unroll 4
+        for (int i = 0; i < nc; ++i) {
+          const float w = ml[moff + (c0 + i) * cp.nh + h].x;
+          const float4 a = *reinterpret_cast<const float4*>(acc + (i * cp.nh + h) * D + d4);
+          O[it].x = fmaf(a.x, w, O[it].x);
+          O[it].y = fmaf(a.y, w, O[it].y);
+          O[it].z = fmaf(a.z, w, O[it].z);
+          O[it].w = fmaf(a.w, w, O[it].w);
+        }
+      }
+    }
+    T* out_rows = reinterpret_cast<T*>(p.out) + (static_cast<size_t>(cp.s) * p.num_q_heads + cp.h0) * D;
+#pragma unroll
+    for (int it = 0; it < NI; ++it) {
+      const int idx = base + lane + 32 * it;
+      if (idx >= cp.nh * C4) continue;
+      const int h = idx / C4, d4 = (idx % C4) * 4;
+      const float L = ml[moff + h].y;
+      uint2 packed = make_uint2(0u, 0u);
+      if (L >= 0.f) {
+        const float inv = QK ? p.out_scale / L : 1.f / L;
+        packed.x = pack2<T>(O[it].x * inv, O[it].y * inv);
+        packed.y = pack2<T>(O[it].z * inv, O[it].w * inv);
+      }
+      *reinterpret_cast<uint2*>(out_rows + h * D + d4) = packed;
+    }
+    }
+    moff += np * cp.nh;
+  }
+  return true;
+}
+
+// A pair whose arrival gave up (no merge will come): zeros for its output rows.
+template <int D, typename T>
+__device__ void zero_pair(const Params& p, const CutPiece& cp, int gt, int gthreads) {
+  T* out_rows = reinterpret_cast<T*>(p.out) + (static_cast<size_t>(cp.s) * p.num_q_heads + cp.h0) * D;
+  for (int i = gt; i < cp.nh * D / 8; i += gthreads)
+    reinterpret_cast<uint4*>(out_rows)[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
 template <int D, int KV>
 struct Smem {
   uint8_t ring[kWarps][Geo<D, KV>::kSlots][Geo<D, KV>::kStageBytes];  // 1024-byte aligned
@@ -655,7 +827,7 @@ struct Smem {
   long long start_pre;
   int start_s;
   int last[kWarps];  // per pair group: this CTA's arrival completed the pair
-  unsigned long long merge_bar[kWarps];  // per warp, single use: the staged merge's copies
+  unsigned long long merge_bar[kWarps];  // per warp: the staged merge's copies, one phase a chunk
 };
 
 // Q^T of a pair as MMA B fragments (column n = head 8*nt + lane / 4; heads >= nh are zero).
@@ -1644,31 +1816,40 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   // (ncut is the same in every warp of a pair.)  Lanes 0 and 1 of the pair's first warp
   // count in its two pieces side by side, each after a fence ordering the piece's stores
   // before its arrival; an arrival that completes a pair fences again before the merge's
-  // loads.
+  // loads.  An arrival that gives up (pa_arrive.h) flags the call and zeros the pair.
   if (ncut > 0) {
     gsync();  // every thread of the pair has stored its parts of the pieces
-    int bits = 0;
+    int bits = 0, lost = 0;
     if (gt < ncut) {
       const CutPiece& cp = gt == 0 ? cut_a : cut_b;
       __threadfence();
       const int n = cp.c_last - cp.c_first + 1;
-      if (arrive(p.counters + static_cast<size_t>(cp.c_first) * p.gs + pi, p.epoch) == n) {
+      const int got = arrive(p.counters + static_cast<size_t>(cp.c_first) * p.gs + pi, p.epoch, n);
+      if (got == n) {
         __threadfence();
         bits = 1 << gt;
+      } else if (got < 0) {
+        atomicOr(p.err, kErrTimeout);
+        lost = 1 << gt;
       }
     }
     __syncwarp();
     bits = static_cast<int>(__reduce_or_sync(0xffffffffu, static_cast<unsigned>(bits)));
+    lost = static_cast<int>(__reduce_or_sync(0xffffffffu, static_cast<unsigned>(lost)));
     if (P > 1) {
-      if (gt == 0) sm.last[pi] = bits;
+      if (gt == 0) sm.last[pi] = bits | (lost << 2);
       gsync();
-      bits = sm.last[pi];
+      bits = sm.last[pi] & 3;
+      lost = sm.last[pi] >> 2;
     }
+    for (int k = 0; k < ncut; ++k)
+      if (lost & (1 << k)) zero_pair<D, T>(p, k == 0 ? cut_a : cut_b, gt, gthreads);
     if (P == 1 && bits) {
       const int nj = (bits & 1) + ((bits >> 1) & 1);
       const CutPiece& j0 = (bits & 1) ? cut_a : cut_b;
+      uint32_t phase = 0;
       if (merge_staged<D, T, QK>(p, pi, j0, cut_b, nj, ring, sm.ring[warp][0], R * G_::kStageBytes,
-                             smem_addr(&sm.merge_bar[warp]), lane))
+                                 smem_addr(&sm.merge_bar[warp]), phase, lane))
         bits = 0;
     }
     for (int k = 0; k < ncut; ++k) {

@@ -18,6 +18,8 @@
 //   Make that first call before any stream capture begins.
 // * If a device needs more scratch than the fixed maximum below (very many SMs), the call
 //   returns PA_ERR_WORKSPACE and launches nothing.
+// * q must be device memory of the current device (the scratch address is looked up per
+//   device); otherwise the call returns PA_ERR_ARG.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -62,6 +64,17 @@ extern "C" int pa_decode_fixed_scratch(const void* q, const void* k_cache, const
   void* scratch = nullptr;
   const int st = scratch_address(&scratch);
   if (st != PA_OK) return st;
+  // The scratch address is the current device's: q must live there too.
+  if (q) {
+    int dev = 0;
+    cudaPointerAttributes attr;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+    if (cudaPointerGetAttributes(&attr, q) != cudaSuccess) {
+      cudaGetLastError();
+      return PA_ERR_ARG;
+    }
+    if (attr.type != cudaMemoryTypeDevice || attr.device != dev) return PA_ERR_ARG;
+  }
   // pa_decode checks every argument and rejects a scratch smaller than this device needs.
   return pa_decode(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                    num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,

@@ -704,6 +704,19 @@ int pa_pool_allocate_prefix(pa_pool* pool, int64_t seq_id, const int32_t* tokens
   }
 }
 
+int pa_pool_table_width(const pa_pool* pool, int n, const int64_t* token_start) {
+  if (!pool || n < 0 || (n > 0 && !token_start)) return PA_ERR_ARG;
+  if (n > 0 && token_start[0] < 0) return PA_ERR_ARG;
+  const int64_t bs = pool->block_size;
+  int64_t width = 0;
+  for (int r = 0; r < n; ++r) {
+    const int64_t len = token_start[r + 1] - token_start[r];
+    if (len < 0 || len > 0x7fffffff) return PA_ERR_ARG;
+    width = std::max(width, (len + bs - 1) / bs);
+  }
+  return static_cast<int>(width);
+}
+
 int pa_pool_allocate_prefix_batch(pa_pool* pool, int n, const int64_t* seq_ids,
                                   const int32_t* tokens, const int64_t* token_start,
                                   const uint8_t* extras, const int64_t* extra_start,

@@ -21,7 +21,7 @@ CONTRACT = ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step
 
 def fake_runner(wl_name, **extra):
     def run(args, rank, world, local_rank):
-        res = {"wl": workloads.RECIPES[wl_name](), "total_ms": STEP * STEPS, "decode_ms": DECODE,
+        res = {"wl": workloads.RECIPES[wl_name](), "step_ms": STEP, "decode_ms": DECODE,
                "two_calls_ms": TWO, "e2e_ms": E2E, "h2d": 1000, "d2h": 500, "clocks": None,
                "flags": 0}
         res.update(extra)
@@ -76,6 +76,18 @@ def test_prefix_line(capsys):
     assert line["unit"] == "tokens/s"
     assert line["value"] == pytest.approx(int(wl.context_lens.sum()) / (STEP * 1e-3), rel=1e-3)
     assert line["uncached"]["speedup_from_cache"] == pytest.approx(TWO / STEP, rel=1e-2)
+
+
+def test_beam_line(capsys):
+    import numpy as np
+    wl = workloads.beam()
+    ctx = (wl.shared_tokens + wl.private_tokens).astype(np.int32)
+    line = line_of(capsys, "beam", fake_runner("beam", ctx=ctx, pairs=14, used_blocks=146))
+    dec, copy, rows, unique = bench.beam_bytes(wl, ctx, 14)
+    assert line["value"] == pytest.approx((dec + copy + rows) / (STEP * 1e-3) / 1e9, rel=1e-3)
+    assert line["roofline"]["achieved"] == pytest.approx(dec / (DECODE * 1e-3) / 1e9, rel=1e-3)
+    assert unique < dec
+    assert line["kv_memory"]["blocks_used"] == 146
 
 
 def test_swap_line(capsys):

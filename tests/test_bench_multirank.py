@@ -18,7 +18,7 @@ import bench, workloads
 def fake_run(args, rank, world, local_rank):
     wl = workloads.RECIPES[args.workload]()
     slow = 1.0 + rank  # rank 1 takes twice as long as rank 0
-    return {{"wl": wl, "total_ms": 0.05 * slow * args.steps, "decode_ms": 0.04 * slow,
+    return {{"wl": wl, "step_ms": 0.05 * slow, "decode_ms": 0.04 * slow,
             "two_calls_ms": 0.06 * slow, "e2e_ms": 0.08 * slow, "h2d": 1000, "d2h": 500,
             "clocks": None, "flags": 0}}
 

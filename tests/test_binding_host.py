@@ -96,3 +96,48 @@ def test_argument_checks_name_the_argument(libpa):
         libpa._fp8_cache(torch.zeros(2, dtype=torch.float16), "k_cache")
     with pytest.raises(ValueError, match="must be a CUDA tensor or a pinned CPU tensor"):
         libpa._reachable(t, "src_k")
+
+
+def test_calls_run_on_their_tensors_device(libpa, monkeypatch):
+    """A call on tensors of another device than the current one makes that device current
+    for the call (the library's per-device state is the current device's)."""
+    pa = libpa
+    entered = []
+
+    class FakeDevice:
+        def __init__(self, dev):
+            self.dev = dev
+
+        def __enter__(self):
+            entered.append(self.dev)
+
+        def __exit__(self, *exc):
+            return False
+
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+    monkeypatch.setattr(torch.cuda, "device", FakeDevice)
+
+    class T:
+        def __init__(self, index):
+            self.device = torch.device("cuda", index)
+
+    seen = []
+    fn = pa._runs_on(lambda t: t.device)(lambda t: seen.append(len(entered)))
+    fn(T(0))
+    assert entered == [] and seen == [0]
+    fn(T(1))
+    assert entered == [torch.device("cuda", 1)] and seen == [0, 1]
+    # every device call of the binding is wrapped so
+    for name in ("reshape_and_cache", "decode", "decode_append", "decode_fp8", "decode_int4",
+                 "decode_append_fp8", "decode_append_int4", "prefill", "decode_fixed_scratch",
+                 "copy_blocks", "copy_blocks_int4", "swap_blocks", "swap_blocks_int4",
+                 "reshape_and_cache_fp8", "reshape_and_cache_int4"):
+        assert hasattr(getattr(pa, name), "__wrapped__"), name
+    # pools: the device named, else the CUDA side of the copy (a pinned CPU pool has none)
+    class P:
+        def __init__(self, index):
+            self.device = torch.device("cuda", index) if index is not None else torch.device("cpu")
+            self.is_cuda = index is not None
+    assert pa._pool_device(P(None), P(2)) == torch.device("cuda", 2)
+    assert pa._pool_device((P(3),), (P(None),)) == torch.device("cuda", 3)
+    assert pa._pool_device(P(3), P(None), device="cuda:1") == torch.device("cuda", 1)

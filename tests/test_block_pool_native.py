@@ -458,3 +458,25 @@ def test_batch_placement_rejects_bad_offsets_in_the_library(libpa):
         assert call(ts, es) == libpa.PA_ERR_ARG
         assert done.value == 0 and pool.num_free() == 16
     assert call([0, 4, 12], [0, 2, 6]) == 0 and done.value == 2 and pool.num_free() == 13
+
+
+def test_table_width_is_the_widest_request(libpa):
+    """pa_pool_table_width: the most blocks one request of the batch takes, ceil(len / B),
+    checked against the pages' N = ceil(S / B) on the printed examples and brute force."""
+    import ctypes
+    import numpy as np
+    for B, lens in ((16, [1000, 19, 0, 256]), (8, [1000]), (32, [1000, 31, 33]), (16, [])):
+        pool = libpa.BlockPool(64, B)
+        ts = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+        want = max([-(-x // B) for x in lens], default=0)
+        got = libpa.lib().pa_pool_table_width(pool._h, len(lens), ts.ctypes.data)
+        assert got == want, (B, lens, got)
+    # 1000 tokens: 63 blocks at B = 16 (the pages' worked example)
+    pool = libpa.BlockPool(64, 16)
+    ts = np.array([0, 1000], np.int64)
+    assert libpa.lib().pa_pool_table_width(pool._h, 1, ts.ctypes.data) == 63
+    bad = np.array([0, 10, 5], np.int64)     # a decreasing offset
+    assert libpa.lib().pa_pool_table_width(pool._h, 2, bad.ctypes.data) == libpa.PA_ERR_ARG
+    neg = np.array([-1, 10], np.int64)
+    assert libpa.lib().pa_pool_table_width(pool._h, 1, neg.ctypes.data) == libpa.PA_ERR_ARG
+    assert libpa.lib().pa_pool_table_width(None, 1, ts.ctypes.data) == libpa.PA_ERR_ARG

@@ -1,14 +1,13 @@
 """The five workload recipes at full size, in the launch configuration the benchmark
-times: block tables and caches bit-exact against the oracle's placement (sampled blocks
-where the pool is large), decode outputs against the oracle on sampled sequences, and
-properties that hold at any size on every output."""
+times: block tables bit-exact against the oracle's placement, and every output element of
+every sequence against the oracle's float64 decode of that sequence's logical rows."""
 import numpy as np
 import pytest
 import torch
 
 import paged_kv_cache_149_gb300 as pa
 import workloads
-from gpu_harness import (TOL, GpuBatch, device_error, max_err, nan_cache, oracle_rows,
+from gpu_harness import (TOL, GpuBatch, device_error, max_err, nan_cache,
                          oracle_seq_bits, to_bits, to_device)
 from oracle import attention, cache_ops, formats
 from oracle.block_pool import BlockPool as OraclePool
@@ -32,30 +31,9 @@ def oracle_tables(wl):
     return tables
 
 
-def sample_seqs(wl, k=6):
-    ctx = wl.context_lens
-    picks = {0, wl.num_seqs - 1, int(np.argmax(ctx)), int(np.argmin(ctx))}
-    rng = np.random.default_rng(1234)
-    picks.update(int(x) for x in rng.choice(wl.num_seqs, size=min(k, wl.num_seqs), replace=False))
-    return sorted(picks)
-
-
-def convex_bound_ok(wl, out_bits):
-    """Every output is a convex combination of its kv head's V rows: it lies within the
-    per-column [min, max] of those rows (plus output rounding)."""
-    out = formats.decode_bits(out_bits, wl.dtype)
-    g = wl.num_q_heads // wl.num_kv_heads
-    v = formats.decode_bits(wl.values, wl.dtype)
-    for s in range(wl.num_seqs):
-        a, b = wl.seq_start[s], wl.seq_start[s + 1]
-        lo = v[a:b].min(axis=0)
-        hi = v[a:b].max(axis=0)
-        for h in range(wl.num_q_heads):
-            o = out[s, h]
-            slack = np.abs(o) * 2.0 ** -7 + 1e-6
-            if np.any(o < lo[h // g] - slack) or np.any(o > hi[h // g] + slack):
-                return False
-    return True
+def worst_error(wl, out_bits):
+    """max |gpu - oracle| over every element of every sequence."""
+    return max(max_err(out_bits[s], oracle_seq_bits(wl, s), wl.dtype) for s in range(wl.num_seqs))
 
 
 @pytest.mark.parametrize("name", ["llama31_8b", "llama7b_mha", "long_b8", "long_b16", "long_b32"])
@@ -66,12 +44,8 @@ def test_recipe_full_size(name):
     out = to_bits(gb.decode())
     assert device_error() == 0
     assert not np.isnan(formats.decode_bits(out, wl.dtype)).any()
-    worst = 0.0
-    for s in sample_seqs(wl):
-        worst = max(worst, max_err(out[s], oracle_seq_bits(wl, s), wl.dtype))
+    worst = worst_error(wl, out)
     assert worst <= TOL[wl.dtype], f"{name}: max abs error {worst}"
-    if wl.num_seqs <= 64:
-        assert convex_bound_ok(wl, out)
 
 
 def test_llama31_8b_step_writes_new_tokens_then_decodes():
@@ -93,11 +67,12 @@ def test_llama31_8b_step_writes_new_tokens_then_decodes():
     out = to_bits(gb.decode())
     assert device_error() == 0
     # the written rows, read back at their slots, are the newest logical rows
-    kb = to_bits(gb.k_cache)
-    for s in sample_seqs(wl):
+    kb, vb = to_bits(gb.k_cache), to_bits(gb.v_cache)
+    for s in range(n):
         blk, row = divmod(int(last[s]), wl.block_size)
         np.testing.assert_array_equal(kb[blk, :, row, :], wl.keys[rows[s]])
-        assert max_err(out[s], oracle_seq_bits(wl, s), wl.dtype) <= TOL[wl.dtype]
+        np.testing.assert_array_equal(vb[blk, :, row, :], wl.values[rows[s]])
+    assert worst_error(wl, out) <= TOL[wl.dtype]
 
 
 def test_llama31_8b_permutation_bit_identical_full_size():

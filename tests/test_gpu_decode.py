@@ -158,3 +158,31 @@ def test_nondefault_stream():
         out = gb.decode()
     s.synchronize()
     np.testing.assert_array_equal(to_bits(out), ref)
+
+
+def test_graph_replays_match_uncaptured_calls():
+    """pa_decode captured once in a CUDA graph and replayed with new queries between
+    replays gives the same bits as uncaptured calls on those queries.  The long sequence is
+    cut across many CTAs, so every replay runs the split-KV merge over the workspace the
+    replay before it left behind."""
+    wl = workloads.custom("graph", [20000, 300, 4096], "fp16", 8, 2, 128, 16, 1600, 20480, seed=21)
+    gb = GpuBatch(wl)
+    out = torch.empty_like(gb.q)
+    q_in = gb.q.clone()
+    gb.decode(out=out)              # first call outside the capture (kernel attributes)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        pa.decode(q_in, gb.k_cache, gb.v_cache, gb.tables, gb.ctx, wl.scale, out=out,
+                  workspace=gb.workspace)
+    rng = np.random.default_rng(77)
+    for _ in range(3):
+        q_new = to_device(workloads.normal_bits(rng, wl.q.shape, 1.0, wl.dtype), wl.dtype)
+        q_in.copy_(q_new)
+        graph.replay()
+        torch.cuda.synchronize()
+        got = to_bits(out)
+        want = to_bits(pa.decode(q_new, gb.k_cache, gb.v_cache, gb.tables, gb.ctx, wl.scale,
+                                 workspace=torch.empty_like(gb.workspace)))
+        np.testing.assert_array_equal(got, want)
+    assert device_error() == 0

@@ -166,9 +166,9 @@ def test_one_long_sequence_cut_across_every_cta():
     check(wl)
 
 
-def test_llama_batch_sampled():
+def test_llama_batch_every_sequence():
     wl = workloads.llama31_8b()
-    check(wl, seqs=[0, 7, 31, 63])
+    check(wl)
 
 
 def test_permutation_bit_identical():

@@ -4,17 +4,20 @@ Such callers (a server that reserved nearly all HBM for the KV block pool, a hos
 framework that owns every device buffer) cannot pass pa_decode a workspace; this entry
 point uses a fixed scratch array inside the library instead.  These tests call it
 through the C ABI and check it against pa_decode on the same inputs, twice in a row
-(the second call runs on scratch the first one left behind).  The file is named to be
-collected last.
+(the second call runs on scratch the first one left behind): the same kernels in the
+same order, so the same bits.  They also check that the calls allocate nothing: torch's
+allocator is untouched, and the device's free memory does not change across a call once
+the library's scratch array is loaded.  The file is named to be collected last.
 """
 import ctypes
+import gc
 
 import numpy as np
 import pytest
 import torch
 
 import workloads
-from gpu_harness import TOL, GpuBatch, device_error, max_err, to_bits
+from gpu_harness import TOL, GpuBatch, device_error, max_err, oracle_seq_bits, to_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -35,6 +38,15 @@ def fixed_scratch_call(lib, gb, out):
         1 if wl.dtype == "bf16" else 0, ctypes.c_void_p(stream))
 
 
+def memory_state():
+    """(torch's allocated bytes, its reserved bytes, the device's free bytes), with Python's
+    garbage collected first so that no unrelated tensor is freed in between."""
+    gc.collect()
+    torch.cuda.synchronize()
+    return (torch.cuda.memory_allocated(), torch.cuda.memory_reserved(),
+            torch.cuda.mem_get_info()[0])
+
+
 @pytest.mark.parametrize("recipe", ["llama31_8b", "long_cut"])
 def test_fixed_scratch_matches_pa_decode_twice(libpa, recipe):
     if recipe == "llama31_8b":
@@ -44,12 +56,23 @@ def test_fixed_scratch_matches_pa_decode_twice(libpa, recipe):
     gb = GpuBatch(wl)
     ref = to_bits(gb.decode())
     lib = libpa.lib()
-    for _ in range(2):
-        out = torch.full_like(gb.q, float("nan"))
+    outs = [torch.full_like(gb.q, float("nan")) for _ in range(2)]
+    states = []
+    for out in outs:
+        states.append(memory_state())
         assert fixed_scratch_call(lib, gb, out) == libpa.PA_OK
-        got = to_bits(out)
-        assert max_err(got, ref, wl.dtype) <= TOL[wl.dtype]
+        states.append(memory_state())
+        np.testing.assert_array_equal(to_bits(out), ref)
         assert device_error() == 0
+    # torch's allocator grew by nothing over either call
+    for before, after in ((states[0], states[1]), (states[2], states[3])):
+        assert after[0] <= before[0] and after[1] <= before[1]
+    # and the device lost no memory over the second call (the first one may load the
+    # library's scratch array, where CUDA loads modules lazily)
+    assert states[3][2] >= states[2][2]
+    got = to_bits(outs[1])
+    worst = max(max_err(got[s], oracle_seq_bits(wl, s), wl.dtype) for s in range(wl.num_seqs))
+    assert worst <= TOL[wl.dtype]
 
 
 def test_fixed_scratch_rejects_bad_arguments(libpa):

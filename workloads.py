@@ -277,6 +277,7 @@ RECIPES = {
     "long_b8": lambda seed=0: long_context(8, seed),
     "long_b16": lambda seed=0: long_context(16, seed),
     "long_b32": lambda seed=0: long_context(32, seed),
+    "beam": beam,
     "prefill_tiny": prefill_tiny,
     "prefill_llama31_8b": prefill_llama31_8b,
     "prefill_chunked": prefill_chunked,
