@@ -645,13 +645,11 @@ __device__ bool merge_staged_once(const Params& p, int pi, const CutPiece& job0,
 // with the same fused multiply-adds as merge_pieces, so a pair's output does not depend on
 // which CTA merges it.  Returns false, having done nothing, when the (m, l) of the pieces
 // do not fit in half the ring (a pair cut into thousands of pieces): merge_pieces then.
-// (Not inlined: the chunked path is rare, and its registers stay out of the decode loop's
-// budget.)
 template <int D, typename T, bool QK>
-__device__ __noinline__ bool merge_staged_chunked(const Params& p, int pi, const CutPiece& job0,
-                                                  const CutPiece& job1, int njobs, uint32_t ring,
-                                                  uint8_t* ring_ptr, int ring_bytes, uint32_t bar,
-                                                  uint32_t& bar_phase, int lane);
+__device__ bool merge_staged_chunked(const Params& p, int pi, const CutPiece& job0,
+                                     const CutPiece& job1, int njobs, uint32_t ring,
+                                     uint8_t* ring_ptr, int ring_bytes, uint32_t bar,
+                                     uint32_t& bar_phase, int lane);
 
 template <int D, typename T, bool QK>
 __device__ __forceinline__ bool merge_staged(const Params& p, int pi, const CutPiece& job0,
@@ -675,12 +673,12 @@ __device__ __forceinline__ bool merge_staged(const Params& p, int pi, const CutP
 }
 
 template <int D, typename T, bool QK>
-__device__ __noinline__ bool merge_staged_chunked(const Params& p, int pi, const CutPiece& job0,
-                                                  const CutPiece& job1, int njobs, uint32_t ring,
-                                                  uint8_t* ring_ptr, int ring_bytes, uint32_t bar,
-                                                  uint32_t& bar_phase, int lane) {
+__device__ bool merge_staged_chunked(const Params& p, int pi, const CutPiece& job0,
+                                     const CutPiece& job1, int njobs, uint32_t ring,
+                                     uint8_t* ring_ptr, int ring_bytes, uint32_t bar,
+                                     uint32_t& bar_phase, int lane) {
   constexpr int C4 = D / 4;  // 4-float chunks of a head row
-  constexpr int NI = 8;      // a lane's chunks of a pair's rows per round (256 a warp)
+  constexpr int NI = 4;      // a lane's chunks of a pair's rows per round (128 a warp)
   const int hpp = p.heads_per_pair;
   auto piece_of = [&](const CutPiece& cp, int cc) {
     return (static_cast<size_t>(cc) * 2 + (cc == cp.c_first ? cp.first_slot : 0)) * p.gs + pi;
@@ -740,7 +738,7 @@ __device__ __noinline__ bool merge_staged_chunked(const Params& p, int pi, const
       moff += np * cp.nh;
     }
   }
-  // Pass 2, per job and round of 256 output chunks: out = sum_i w_i acc_i / L, pieces in
+  // Pass 2, per job and round of 128 output chunks: out = sum_i w_i acc_i / L, pieces in
   // CTA order, staged in chunks.
   int moff = 0;
   for (int j = 0; j < njobs; ++j) {
