@@ -40,6 +40,7 @@ FALLBACK_HBM_GBS = 6800.0
 ROTATE = 3
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_llama31_8b_traffic.json")
 KERNEL_SOURCES = ["paged_kv_cache_149_gb300/csrc/pa_decode_kernel.cuh",
+                  "paged_kv_cache_149_gb300/csrc/pa_arrive.h",
                   "paged_kv_cache_149_gb300/csrc/pa_decode.cu",
                   "paged_kv_cache_149_gb300/csrc/pa_common.cuh"]
 
@@ -288,11 +289,11 @@ E2E_METHOD = ("each step: its inputs copied from pinned host memory, the public 
               "group's outputs on a download stream; two groups of staging slots, so each "
               "group's copies overlap the neighbouring groups' kernels")
 
-E2E_GROUP = 10  # steps staged together
+E2E_GROUP_BYTES = 8 << 20  # inputs staged together: about this many bytes, 1..10 steps
 
 
 def pipelined_e2e(batches, names, make_launch, out_like, device, steps, warmup, repeats=1,
-                  group=E2E_GROUP):
+                  group=None):
     """Steps end to end from pinned host memory: every step's inputs (`names` of its batch,
     packed) come from pinned host memory, the step runs (`make_launch(dev_inputs, dev_out)`
     gives a callable taking the stream, made once per staging slot), and its output goes
@@ -311,6 +312,8 @@ def pipelined_e2e(batches, names, make_launch, out_like, device, steps, warmup, 
         t = batches[0][k]
         layout[k] = (off, t.shape, t.dtype, t.numel() * t.element_size())
         off += -(-layout[k][3] // align) * align
+    if group is None:  # small steps in groups of up to 10, large ones one at a time
+        group = int(min(10, max(1, E2E_GROUP_BYTES // max(1, off))))
     S = max(1, group)
     nrot = len(batches)
     # a group's inputs, step after step (step k of a group uses rotation k % nrot; a group

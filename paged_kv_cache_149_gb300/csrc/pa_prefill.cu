@@ -8,25 +8,30 @@
 // has to read the block table; chenyuan1125 "vllm-pagedattention", section 它和
 // FlashAttention…: prefill works on large blocks of queries).
 //
-// Design: one CTA per (pair of 128-row query tiles, sequence, kv head), 320 threads in
+// Design: one CTA per (pair of 128-row query tiles, sequence, kv head), 384 threads in
 // four roles that run concurrently and hand work over through mbarriers:
 // * A query tile's rows are (token, query head of the kv head) pairs, 128 / G tokens x G
 //   heads, so every K/V tile is read once for all heads of the group (GQA), and both
 //   query tiles of the CTA share the K/V tiles.
-// * Loader warp: Q of both tiles once (16-byte cp.async, zero-filled past the batch), then
-//   64-key K and V tiles into a four-stage ring, in the 128-byte swizzled layout the
-//   tcgen05 descriptors read.  Whole blocks come by TMA (a 4-D tensor map over the
-//   cache: d, row, kv head, block; one copy per block and 64-column half); the ragged last
-//   block and the blocks past the context by cp.async with zero fill, so no row past the
-//   context is ever read (its V row must be zero: P is 0 there, and 0 x NaN is NaN).
-// * Two MMA warps, one issuing thread per query tile: S = Q K^T into tensor memory (two
-//   buffers per tile), and O += P V with P read from tensor memory (the A operand, packed
-//   over the S columns it came from) and O kept there across the whole key range.  S of a
-//   tile's next keys is issued before its current P V, so the tensor cores compute it
-//   while that tile's softmax runs, and the two tiles interleave on the tensor cores.
+// * Two loader warps: Q of both tiles once (16-byte cp.async, zero-filled past the
+//   batch), then 64-key K tiles (one warp) and V tiles (the other) into a four-stage
+//   ring, in the 128-byte swizzled layout the tcgen05 descriptors read.  Whole blocks
+//   come by TMA (a 4-D tensor map over the cache: d, row, kv head, block; one copy per
+//   block and 64-column half); the ragged last block and the blocks past the context by
+//   cp.async with zero fill, so no row past the context is ever read (its V row must be
+//   zero: P is 0 there, and 0 x NaN is NaN).  Block-table entries are looked up four
+//   tiles ahead.  One thread issuing TMA copies moves only about 26 GB/s per SM, so K and
+//   V each get their own issuer.
+// * Two MMA warps, one issuing thread per query tile: S = Q K^T into tensor memory (one
+//   buffer per tile), and O += P V with P read from tensor memory (the A operand, two
+//   slots per tile, packed two values a column) and O kept there across the whole key
+//   range.  S of a tile's next keys is issued as soon as the softmax has loaded the
+//   current S into registers, before the current P V, so the tensor cores compute it while
+//   that tile's softmax runs, and the two tiles interleave on the tensor cores.
 // * Two softmax warpgroups, one per query tile, one thread per row (= tensor-memory
 //   lane): read the row of S, mask causally, keep the running maximum m and sum l in
-//   exp2 units, write the row of P (input type) back over the S columns it came from.
+//   exp2 units, write the row of P (input type) into the tile's next P slot (once the
+//   P V that read it two tiles back is done).
 //   O is rescaled only when a row's maximum grows by more than 8 (in log2 units), so
 //   P <= 2^8 and the rescale (a read-modify-write of the row in tensor memory) is rare
 //   after the first tiles; the final O / l uses the same m, so the result is exact
@@ -49,9 +54,11 @@ constexpr int kTiles = 2;       // query tiles per CTA (softmax warpgroups)
 constexpr int kRows = 128;      // rows of a query tile (MMA M, tensor-memory lanes)
 constexpr int kKeys = 64;       // keys of a K/V tile (MMA N of S, K of P V)
 constexpr int kStages = 4;      // K/V ring
-constexpr int kLoadWarp = 8;
+constexpr int kTableAhead = 4;  // tiles the loader looks block-table entries up ahead
+constexpr int kLoadWarp = 8;    // loads Q and the K tiles
+constexpr int kLoadWarpV = 11;  // loads the V tiles
 constexpr int kMmaWarp = 9;     // MMA issue for tile 0; tile 1 has the next warp
-constexpr int kThreads = 352;   // 2 x 128 softmax threads, a loader warp, two MMA warps
+constexpr int kThreads = 384;   // 2 x 128 softmax threads, two loader warps, two MMA warps
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescale = 8.f;  // log2 growth of a row's maximum that forces a rescale of O
 
@@ -78,7 +85,7 @@ struct Smem {
   uint8_t v[kStages][kKeys * D * 2];
   unsigned long long q_full;
   unsigned long long kv_full[kStages], kv_empty[kStages];
-  unsigned long long s_full[kTiles][2];
+  unsigned long long s_full[kTiles][2], s_read[kTiles][2];
   unsigned long long p_full[kTiles][2], o_done[kTiles][2];
   unsigned long long fin;  // the MMA thread's last commit
   uint32_t tmem;
@@ -224,8 +231,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   constexpr int CH = D / 8;                  // 16-byte chunks of a 16-bit row
   constexpr int KS1 = D / 16;                // MMA k-steps of S = Q K^T
   constexpr int KS2 = kKeys / 16;            // MMA k-steps of P V
-  constexpr uint32_t kTileCols = 256;        // TMEM columns per query tile
-  constexpr uint32_t kColO = 2 * kKeys;      //   S buffers [0, 128), O [128, 128 + D)
+  constexpr uint32_t kTileCols = 256;        // TMEM columns per query tile:
+  constexpr uint32_t kColP = kKeys;          //   S [0, 64), P slots [64, 96) and [96, 128),
+  constexpr uint32_t kColO = 2 * kKeys;      //   O [128, 128 + D)
   constexpr uint32_t kTmemCols = kTiles * kTileCols;
   constexpr uint32_t kHalf = kKeys * 128;    // bytes of a 64-column half of a K/V tile
   extern __shared__ uint8_t smem_raw[];
@@ -267,12 +275,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   if (tid == 0) {
     mbar_init(smem_addr(&sm.q_full), 32);
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(smem_addr(&sm.kv_full[i]), 33);  // the TMA issuer's expect-tx + 32 copy lanes
+      mbar_init(smem_addr(&sm.kv_full[i]), 66);  // per loader: TMA expect-tx + 32 copy lanes
       mbar_init(smem_addr(&sm.kv_empty[i]), kTiles);  // one commit per MMA thread
     }
     for (int t = 0; t < kTiles; ++t)
       for (int b = 0; b < 2; ++b) {
         mbar_init(smem_addr(&sm.s_full[t][b]), 1);
+        mbar_init(smem_addr(&sm.s_read[t][b]), kRows);
         mbar_init(smem_addr(&sm.p_full[t][b]), kRows);
         mbar_init(smem_addr(&sm.o_done[t][b]), 1);
       }
@@ -298,28 +307,46 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     return false;
   };
 
-  if (warp == kLoadWarp) {
-    // ================= loader: Q once, then the K/V ring =================
-    for (int e = lane; e < kTiles * kRows * CH; e += 32) {
-      const int t = e / (kRows * CH), rem = e % (kRows * CH), r = rem / CH, c = rem % CH;
-      const int tok = tok0 + t * tpt + r / G;
-      const bool live = r / G < tpt && tok < qlen;
-      const size_t row = live ? static_cast<size_t>(qs + tok) * p.num_q_heads + g * G + r % G : 0;
-      cp_async16(smem_addr(sm.q[t]) + swz(kRows, r, c), p.q + (row * D + c * 8) * 2, live ? 16u : 0u);
+  if (warp == kLoadWarp || warp == kLoadWarpV) {
+    // ===== loaders: Q once (the K loader), then the K (or V) tiles of the ring =====
+    // Two warps, because one thread issuing TMA copies moves only about 26 GB/s per SM:
+    // with one loader a 64-key step of both query tiles (32 KB of K and V) took about 2200
+    // cycles to issue, against about 1300 cycles of tensor work.
+    const bool is_v = warp == kLoadWarpV;
+    if (!is_v) {
+      for (int e = lane; e < kTiles * kRows * CH; e += 32) {
+        const int t = e / (kRows * CH), rem = e % (kRows * CH), r = rem / CH, c = rem % CH;
+        const int tok = tok0 + t * tpt + r / G;
+        const bool live = r / G < tpt && tok < qlen;
+        const size_t row = live ? static_cast<size_t>(qs + tok) * p.num_q_heads + g * G + r % G : 0;
+        cp_async16(smem_addr(sm.q[t]) + swz(kRows, r, c), p.q + (row * D + c * 8) * 2, live ? 16u : 0u);
+      }
+      cp_async_arrive(smem_addr(&sm.q_full));
     }
-    cp_async_arrive(smem_addr(&sm.q_full));
+    const uint8_t* cache = is_v ? p.v_cache : p.k_cache;
+    const CUtensorMap* tmap = is_v ? &p.vmap : &p.kmap;
     const int B = p.block_size, nbk = kKeys / B;
     const int32_t* trow = p.block_tables + static_cast<size_t>(s) * p.max_blocks_per_seq;
+    // Block-table entries, lane j holding block j of a tile, looked up kTableAhead tiles
+    // before the tile is issued: a lookup is a dependent load from global memory, and
+    // waiting for it at each tile made the loader the slowest role (about 2500 cycles a
+    // tile, against about 1300 of tensor work for both query tiles).
+    auto lookup = [&](int kt) -> int {
+      const int lb = kt * nbk + lane;
+      return (lane < nbk && kt < n && lb * B < ctx) ? __ldg(trow + lb) : -1;
+    };
+    int ahead[kTableAhead];
+#pragma unroll
+    for (int i = 0; i < kTableAhead; ++i) ahead[i] = lookup(i);
     for (int kt = 0; kt < n; ++kt) {
       const int st = kt % kStages;
-      // this tile's blocks: lane j looks up block j (one round trip for all)
-      int my_e = -1;
-      if (lane < nbk) {
-        const int lb = kt * nbk + lane;
-        if (lb * B < ctx) my_e = __ldg(trow + lb);
-      }
+      // this tile's blocks (lane j: block j), and the lookup kTableAhead tiles on
+      const int my_e = ahead[0];
+#pragma unroll
+      for (int i = 0; i + 1 < kTableAhead; ++i) ahead[i] = ahead[i + 1];
+      ahead[kTableAhead - 1] = lookup(kt + kTableAhead);
       if (kt >= kStages && !wait(sm.kv_empty[st], ((kt - kStages) / kStages) & 1)) break;
-      const uint32_t kb = smem_addr(sm.k[st]), vb = smem_addr(sm.v[st]);
+      const uint32_t kb = smem_addr(is_v ? sm.v[st] : sm.k[st]);
       uint32_t full_mask = 0;  // blocks that come whole by TMA
       for (int j = 0; j < nbk; ++j) {
         const int e = __shfl_sync(0xffffffffu, my_e, j);
@@ -328,18 +355,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       }
       if (lane == 0) {  // whole blocks by TMA
         mbar_arrive_expect_tx(smem_addr(&sm.kv_full[st]),
-                              static_cast<uint32_t>(__popc(full_mask)) * 2u * B * D * 2);
+                              static_cast<uint32_t>(__popc(full_mask)) * B * D * 2);
       }
-      for (int j = 0; j < nbk; ++j) {
-        const int e = __shfl_sync(0xffffffffu, my_e, j);
-        if (lane == 0 && (full_mask >> j & 1)) {
-#pragma unroll
-          for (int h = 0; h < D / 64; ++h) {
-            const uint32_t off = h * kHalf + j * B * 128;
-            tma_load_4d(kb + off, &p.kmap, h * 64, 0, g, e, smem_addr(&sm.kv_full[st]));
-            tma_load_4d(vb + off, &p.vmap, h * 64, 0, g, e, smem_addr(&sm.kv_full[st]));
-          }
-        }
+      {
+        // lane (j, h) copies block j's 64-column half h (the copies of a tile issue side by
+        // side)
+        constexpr int NH = D / 64;
+        const int j = lane / NH, h = lane % NH;
+        const int e = __shfl_sync(0xffffffffu, my_e, j < nbk ? j : 0);
+        if (j < nbk && (full_mask >> j & 1))
+          tma_load_4d(kb + h * kHalf + j * B * 128, tmap, h * 64, 0, g, e, smem_addr(&sm.kv_full[st]));
       }
       // the ragged block and blocks past the context: rows by cp.async, zero-filled
       for (int j = 0; j < nbk; ++j) {
@@ -353,9 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           const bool live = ok && r < rows;
           const size_t src =
               (((static_cast<size_t>(live ? e : 0) * p.num_kv_heads + g) * B + (live ? r : 0)) * D + c * 8) * 2;
-          const uint32_t so = swz(kKeys, j * B + r, c);
-          cp_async16(kb + so, p.k_cache + src, live ? 16u : 0u);
-          cp_async16(vb + so, p.v_cache + src, live ? 16u : 0u);
+          cp_async16(kb + swz(kKeys, j * B + r, c), cache + src, live ? 16u : 0u);
         }
       }
       cp_async_arrive(smem_addr(&sm.kv_full[st]));
@@ -376,10 +399,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       const uint64_t dv0 = desc_sw128(smem_addr(sm.v[0]), kKeys * 128, 1024);
       auto issue_s = [&](int t, int kt) -> bool {
         const int b = kt & 1;
-        // S buffer b holds the P of tile kt - 2 (read by its P V): wait for that P V
-        if (kt >= 2 && !wait(sm.o_done[t][b], ((kt - 2) >> 1) & 1)) return false;
+        // one S buffer: the softmax has loaded S of the keys before these
+        if (kt >= 1 && !wait(sm.s_read[t][(kt - 1) & 1], ((kt - 1) >> 1) & 1)) return false;
         tc_fence_after();
-        const uint32_t d = tmem + t * kTileCols + b * kKeys;
+        const uint32_t d = tmem + t * kTileCols;
         const uint64_t qd = t == 0 ? dq0 : dq1;
         const uint64_t kd = dk0 + (((kt % kStages) * kStageBytes) >> 4);
         mma_f16(d, qd, kd, id_s, false);
@@ -397,7 +420,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         if (!wait(sm.p_full[t][b], (kt >> 1) & 1)) return false;
         tc_fence_after();
         const uint64_t vd = dv0 + (((kt % kStages) * kStageBytes) >> 4);
-        const uint32_t o = tmem + t * kTileCols + kColO, pa = tmem + t * kTileCols + b * kKeys;
+        const uint32_t o = tmem + t * kTileCols + kColO;
+        const uint32_t pa = tmem + t * kTileCols + kColP + b * (kKeys / 2);
         mma_f16_ts(o, pa, vd, id_o, kt > 0);
 #pragma unroll
         for (int ks = 1; ks < KS2; ++ks)  // P from tensor memory: 16 keys = 8 columns
@@ -450,13 +474,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       float sv[kKeys];
       {
         float tmp[32];
-        tmem_ld32(tl + b * kKeys, tmp);
+        tmem_ld32(tl, tmp);
 #pragma unroll
         for (int i = 0; i < 32; ++i) sv[i] = tmp[i];
-        tmem_ld32(tl + b * kKeys + 32, tmp);
+        tmem_ld32(tl + 32, tmp);
 #pragma unroll
         for (int i = 0; i < 32; ++i) sv[32 + i] = tmp[i];
       }
+      // S is in registers: the MMA thread may write the next keys' S over it
+      tc_fence_before();
+      mbar_arrive(smem_addr(&sm.s_read[t][b]));
       // causal mask on the raw scores (key kt*64 + i > pos), then the maximum over eight
       // independent partial chains; scores stay unscaled (the scale is positive, so the
       // maximum commutes with it) and P = 2^(s * scale - m) is one FFMA per element
@@ -501,6 +528,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       // eight partial chains
       // (a row with nothing unmasked yet has every score at -inf, so any finite offset
       // gives it P = 0; packed FP32 pairs halve the FMA and add counts)
+      // P goes to slot b, which P V of the keys two tiles back read: that P V is done
+      if (kt >= 2 && !(ok = wwait(sm.o_done[t][b], ((kt - 2) >> 1) & 1))) break;
+      tc_fence_after();
       const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
       const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(neg_m, neg_m);
       float2 ps[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
@@ -515,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           ps[(i >> 1) & 3] = __fadd2_rn(ps[(i >> 1) & 3], e);
           pk[i >> 1] = pack2<T>(e.x, e.y);
         }
-        tmem_st16(tl + b * kKeys + 16 * h, pk);
+        tmem_st16(tl + kColP + b * (kKeys / 2) + 16 * h, pk);
       }
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       const float2 s01 = __fadd2_rn(ps[0], ps[1]), s23 = __fadd2_rn(ps[2], ps[3]);
