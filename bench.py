@@ -176,7 +176,12 @@ LOOP_SECONDS = 0.4
 MAX_REPEATS = 400
 
 
+FIXED_REPEATS = None  # --repeats: a fixed count (profiling runs), else sized by LOOP_SECONDS
+
+
 def repeats_for(ms_per_step, steps):
+    if FIXED_REPEATS:
+        return FIXED_REPEATS
     return int(min(MAX_REPEATS, max(5, round(LOOP_SECONDS * 1e3 / max(1e-3, ms_per_step * steps)))))
 
 
@@ -1877,7 +1882,11 @@ def main(argv=None, runner=None, backend="nccl"):
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="llama31_8b")
     ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
+    ap.add_argument("--repeats", type=int, default=0,
+                    help="timed loops of --steps steps each (default: enough for ~0.4 s)")
     args = ap.parse_args(argv)
+    global FIXED_REPEATS
+    FIXED_REPEATS = args.repeats if args.repeats > 0 else None
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
 

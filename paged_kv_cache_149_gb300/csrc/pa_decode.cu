@@ -70,7 +70,9 @@ int decode_launch(const DecodeArgs& a, int grid, cudaStream_t stream) {
   p.max_ctx = a.max_blocks_per_seq * a.block_size;
   const bool quantised = a.kv_fp8 || a.kv_int4;
   p.log2_stage = quantised ? 5 : 4;  // 32-token stages over quantised blocks, 16 over 16-bit ones
-  p.seg_cost = decode::kSegCost >> (p.log2_stage - 4);  // the same charge in tokens
+  // per-family charge (the same charge in tokens for 32-token stages)
+  p.seg_cost = decode::seg_cost_for(static_cast<long long>(a.num_seqs) * p.ngroups, grid) >>
+               (p.log2_stage - 4);
   // FP8 blocks: scores are k_scale * <q, codes>, outputs v_scale * (weighted codes)
   p.scale_log2 = a.scale * (a.kv_fp8 ? a.k_scale : 1.f) * decode::kLog2e;
   p.out_scale = a.kv_fp8 ? a.v_scale : 1.f;

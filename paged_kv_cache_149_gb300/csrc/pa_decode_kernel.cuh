@@ -69,12 +69,23 @@ constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxHeads = 16;  // query heads per pair (MMA columns)
 constexpr float kLog2e = 1.4426950408889634f;
-// Stage-equivalents charged per family on top of its stages when cutting the batch into
-// per-SM shares.  A family switch (a new table row, the pair-end writes) and the cut-pair
-// work at the ends of a share cost it time; on GB300 a charge of 32 stages balanced the
-// shares best over batches of long, short and mixed sequences (16: 58.7 us, 32: 56.8 us,
-// 64: 58.4 us on 64 sequences of 128..2048 tokens; 16 x 8192 tokens: 102.9 / 96.5 / 93.9).
-constexpr int kSegCost = 32;
+// Stage-equivalents (16-token stages) charged per family on top of its stages when
+// cutting the batch into per-SM shares: a family switch (a new table row, the pair-end
+// writes) costs time, and when families are larger than shares a family start in a share
+// also means one more cut piece to count in and merge at the share's end.  So the charge
+// is kSegCostFew stages when the batch has no more families than shares, falling towards
+// kSegCostMany as families outnumber shares (seg_cost_for).  On GB300 (one box, 16-bit
+// blocks, charge 16 / 32 / 48 / 64): 64 sequences of 128..2048 tokens (64 families)
+// 53.4 / 52.8 / 51.8 / 51.4 us; 256 MHA sequences (1024 families) 385.9 / 387.7 / 391.5 /
+// 395.7 us; 8 sequences of 8-32 K tokens flat within 1 us.
+constexpr int kSegCostFew = 64;
+constexpr int kSegCostMany = 16;
+
+// The charge for `families` families cut into `shares` shares, in 16-token stages.
+inline int seg_cost_for(long long families, int shares) {
+  const long long f = families > shares ? families : shares;
+  return kSegCostMany + static_cast<int>((kSegCostFew - kSegCostMany) * static_cast<long long>(shares) / f);
+}
 
 // Cached K/V formats: 16-bit values, FP8 (E4M3) codes with one scale per cache, INT4
 // codes (two per byte) with one float32 scale per row.
