@@ -38,12 +38,13 @@
 // * Whole stages (every row inside the context, no pass split between blocks) copy from
 //   one base address per block with constant offsets; others take a per-row path.
 // * A pair cut between CTAs (split-KV) leaves one partial softmax state (O, m, l) per
-//   piece in the workspace.  When a CTA has streamed its whole share (no copies left in
-//   flight, so a fence is cheap), it counts its pieces in on a per-pair counter; the CTA
-//   that brings a pair's count to its number of pieces merges them in CTA order with a
-//   log-sum-exp reduction (the rescaling identity of online softmax that chenyuan1125,
-//   section 它和 FlashAttention…, names as FlashAttention's technique).  No CTA ever waits
-//   for another.  Cut points depend on logical positions and context lengths only, and
+//   piece in the workspace.  A CTA counts its pieces in on per-pair counters: a piece
+//   whose family is not the share's last right after it is stored (one warp per pair),
+//   the share's last one when the whole share is streamed (no copies left in flight, so
+//   a fence is cheap).  The CTA that brings a pair's count to its number of pieces
+//   merges them in CTA order with a log-sum-exp reduction (the rescaling identity of
+//   online softmax that chenyuan1125, section 它和 FlashAttention…, names as
+//   FlashAttention's technique), after its share.  No CTA ever waits for another.  Cut points depend on logical positions and context lengths only, and
 //   the merge order is fixed, so permuting physical blocks gives bit-identical output.
 // * Launched as a programmatic dependent of the kernel before it in the stream: while
 //   that kernel drains, the grid plans its shares from the context lengths and block
@@ -1214,6 +1215,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   // counted in after the share is streamed.
   CutPiece cut_a, cut_b;
   int ncut = 0;
+  int early = 0, early_last = 0, early_lost = 0;  // pieces counted in before the share's end
   for (Fam f = first; f.s < p.num_seqs && f.pre < w1; fam_next(f, p), cta_first = false) {
     const int2 r = unit_range(f, pi, w0, w1, p);
     if (!has_piece(r, f.ns)) continue;
@@ -1678,8 +1680,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       // the running max/sum of those heads.
       const bool any_bad = __any_sync(0xffffffffu, seg_bad);
       if (!whole) {
-        // A piece of a cut pair: store (O, m, l) in [head][d] order; it is counted in (and
-        // maybe merged) after the share is streamed.
+        // A piece of a cut pair: store (O, m, l) in [head][d] order; it is counted in
+        // below or after the share is streamed, and merged after the share.
 #pragma unroll
         for (int nt = 0; nt < NTH; ++nt)
 #pragma unroll
@@ -1697,7 +1699,26 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
               }
             }
           }
-        (ncut == 0 ? cut_a : cut_b) = cut_piece(f, pi, ph, W, G, p);
+        CutPiece& cpr = ncut == 0 ? cut_a : cut_b;
+        cpr = cut_piece(f, pi, ph, W, G, p);
+        if (f.pre + f.fw < w1) {
+          // More of the share follows (this is its first family, or a middle one): count
+          // the piece in now, so that the share's end has one arrival and merge fewer.
+          // The pair's other pieces lie in earlier shares, so this arrival rarely
+          // completes it; if it does, the merge waits for the share's end.
+          __syncwarp();
+          const int n = cpr.c_last - cpr.c_first + 1;
+          int got = 0;
+          if (lane == 0) {
+            __threadfence();
+            got = arrive(p.counters + static_cast<size_t>(cpr.c_first) * p.gs + pi, p.epoch, n);
+            if (got == n) __threadfence();
+          }
+          got = __shfl_sync(0xffffffffu, got, 0);
+          early |= 1 << ncut;
+          if (got == n) early_last |= 1 << ncut;
+          else if (got < 0) early_lost |= 1 << ncut;
+        }
         ++ncut;
         if (lane == 0 && any_bad) atomicOr(p.err, kErrBadBlock);
         continue;
@@ -1829,7 +1850,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   if (ncut > 0) {
     gsync();  // every thread of the pair has stored its parts of the pieces
     int bits = 0, lost = 0;
-    if (gt < ncut) {
+    if (gt < ncut && !(early & (1 << gt))) {
       const CutPiece& cp = gt == 0 ? cut_a : cut_b;
       __threadfence();
       const int n = cp.c_last - cp.c_first + 1;
@@ -1845,6 +1866,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     __syncwarp();
     bits = static_cast<int>(__reduce_or_sync(0xffffffffu, static_cast<unsigned>(bits)));
     lost = static_cast<int>(__reduce_or_sync(0xffffffffu, static_cast<unsigned>(lost)));
+    bits |= early_last;
+    lost |= early_lost;
+    if (early_lost && gt == 0) atomicOr(p.err, kErrTimeout);
     if (P > 1) {
       if (gt == 0) sm.last[pi] = bits | (lost << 2);
       gsync();
