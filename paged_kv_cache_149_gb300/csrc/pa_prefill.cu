@@ -13,15 +13,21 @@
 // * A query tile's rows are (token, query head of the kv head) pairs, 128 / G tokens x G
 //   heads, so every K/V tile is read once for all heads of the group (GQA), and both
 //   query tiles of the CTA share the K/V tiles.
-// * Two loader warps: Q of both tiles once (16-byte cp.async, zero-filled past the
-//   batch), then 64-key K tiles (one warp) and V tiles (the other) into a four-stage
-//   ring, in the 128-byte swizzled layout the tcgen05 descriptors read.  Whole blocks
-//   come by TMA (a 4-D tensor map over the cache: d, row, kv head, block; one copy per
-//   block and 64-column half); the ragged last block and the blocks past the context by
-//   cp.async with zero fill, so no row past the context is ever read (its V row must be
-//   zero: P is 0 there, and 0 x NaN is NaN).  Block-table entries are looked up four
-//   tiles ahead.  One thread issuing TMA copies moves only about 26 GB/s per SM, so K and
-//   V each get their own issuer.
+// * Two loader warps: Q of both tiles once, then 64-key K tiles (one warp) and V tiles
+//   (the other) into a four-stage ring, in the 128-byte swizzled layout the tcgen05
+//   descriptors read.  A query tile that lies wholly inside its sequence comes by TMA (a
+//   3-D tensor map over q: d, head, token; a token's G heads are adjacent rows of the
+//   tile), one copy per 64-column half; a tile that runs past its sequence comes by
+//   16-byte cp.async, zero-filled past the last token.  (Loading every Q row that way,
+//   with an integer division by G per 16-byte copy, held each CTA for about 19000 cycles
+//   before its first K tile.)  Whole K/V blocks come by TMA (a 4-D tensor map over the
+//   cache: d, row, kv head, block; one copy per block and 64-column half); the ragged last
+//   block and the blocks past the context by cp.async with zero fill, so no row past the
+//   context is ever read (its V row must be zero: P is 0 there, and 0 x NaN is NaN).
+//   Block-table entries are looked up four tiles ahead.  One thread issuing TMA copies
+//   moves only about 26 GB/s per SM, so K and V each get their own issuer.  A stage of
+//   the ring is free again once P V of both query tiles has read it (the same barrier
+//   tells the softmax that P V is done).
 // * Two MMA warps, one issuing thread per query tile: S = Q K^T into tensor memory (one
 //   buffer per tile), and O += P V with P read from tensor memory (the A operand, two
 //   slots per tile, packed two values a column) and O kept there across the whole key
@@ -65,6 +71,8 @@ constexpr float kRescale = 8.f;  // log2 growth of a row's maximum that forces a
 struct Params {
   CUtensorMap kmap;  // the caches as [num_blocks][Hkv][B][d] 16-bit, box (64, B, 1, 1)
   CUtensorMap vmap;
+  CUtensorMap qmap;  // q as [tokens][Hq][d], box (64, G, 128 / G): one query tile's half
+  int q_tma;         // qmap is valid (G divides 128, q 16-byte aligned)
   const uint8_t* q;
   const uint8_t* k_cache;
   const uint8_t* v_cache;
@@ -84,9 +92,10 @@ struct Smem {
   uint8_t k[kStages][kKeys * D * 2];           // [64-column half][64 keys][128 B]
   uint8_t v[kStages][kKeys * D * 2];
   unsigned long long q_full;
-  unsigned long long kv_full[kStages], kv_empty[kStages];
+  unsigned long long kv_full[kStages];
   unsigned long long s_full[kTiles][2], s_read[kTiles][2];
-  unsigned long long p_full[kTiles][2], o_done[kTiles][2];
+  unsigned long long p_full[kTiles][2];
+  unsigned long long o_done[kTiles][kStages];  // P V of tile kt done (frees stage kt % kStages)
   unsigned long long fin;  // the MMA thread's last commit
   uint32_t tmem;
   int bad;    // a block id of this CTA's keys is out of range
@@ -226,6 +235,17 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
+// 3-D tiled TMA load through the tensor map at `map` (a kernel parameter); completion
+// counted in bytes on `bar`.  x * the element size is a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, int x, int y, int z,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
 template <int D, typename T>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ Params p) {
   constexpr int CH = D / 8;                  // 16-byte chunks of a 16-bit row
@@ -273,18 +293,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 
   // ---- set-up: barriers, tensor memory ----
   if (tid == 0) {
-    mbar_init(smem_addr(&sm.q_full), 32);
+    mbar_init(smem_addr(&sm.q_full), 33);  // TMA expect-tx + 32 copy lanes
     for (int i = 0; i < kStages; ++i) {
       mbar_init(smem_addr(&sm.kv_full[i]), 66);  // per loader: TMA expect-tx + 32 copy lanes
-      mbar_init(smem_addr(&sm.kv_empty[i]), kTiles);  // one commit per MMA thread
     }
     for (int t = 0; t < kTiles; ++t)
       for (int b = 0; b < 2; ++b) {
         mbar_init(smem_addr(&sm.s_full[t][b]), 1);
         mbar_init(smem_addr(&sm.s_read[t][b]), kRows);
         mbar_init(smem_addr(&sm.p_full[t][b]), kRows);
-        mbar_init(smem_addr(&sm.o_done[t][b]), 1);
       }
+    for (int t = 0; t < kTiles; ++t)
+      for (int i = 0; i < kStages; ++i) mbar_init(smem_addr(&sm.o_done[t][i]), 1);
     mbar_init(smem_addr(&sm.fin), kTiles);
     fence_mbar_init();
     sm.bad = 0;
@@ -314,12 +334,41 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     // cycles to issue, against about 1300 cycles of tensor work.
     const bool is_v = warp == kLoadWarpV;
     if (!is_v) {
-      for (int e = lane; e < kTiles * kRows * CH; e += 32) {
-        const int t = e / (kRows * CH), rem = e % (kRows * CH), r = rem / CH, c = rem % CH;
-        const int tok = tok0 + t * tpt + r / G;
-        const bool live = r / G < tpt && tok < qlen;
-        const size_t row = live ? static_cast<size_t>(qs + tok) * p.num_q_heads + g * G + r % G : 0;
-        cp_async16(smem_addr(sm.q[t]) + swz(kRows, r, c), p.q + (row * D + c * 8) * 2, live ? 16u : 0u);
+      // Q of both tiles: a whole tile (tpt tokens x G heads = 128 rows, each token's G rows
+      // contiguous in q) by TMA, one copy per 64-column half; a tile that runs past the
+      // sequence by 16-byte copies, zero-filled past its last token (token-major, no
+      // divisions: for one token the G x D values are contiguous)
+      uint32_t tma_bytes = 0;
+#pragma unroll
+      for (int t = 0; t < kTiles; ++t) {
+        const int first = tok0 + t * tpt;
+        if (first >= qlen) continue;
+        if (p.q_tma && first + tpt <= qlen) {
+          tma_bytes += kRows * D * 2;
+          continue;
+        }
+        for (int tl = 0; tl < tpt; ++tl) {
+          const int tok = first + tl;
+          const bool live = tok < qlen;
+          const uint8_t* src =
+              p.q + (static_cast<size_t>(qs + (live ? tok : 0)) * p.num_q_heads + g * G) * D * 2;
+          for (int u = lane; u < G * CH; u += 32) {
+            const int r = tl * G + u / CH, c = u % CH;
+            cp_async16(smem_addr(sm.q[t]) + swz(kRows, r, c), src + u * 16, live ? 16u : 0u);
+          }
+        }
+      }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(smem_addr(&sm.q_full), tma_bytes);
+#pragma unroll
+        for (int t = 0; t < kTiles; ++t) {
+          const int first = tok0 + t * tpt;
+          if (!(p.q_tma && first < qlen && first + tpt <= qlen)) continue;
+#pragma unroll
+          for (int h = 0; h < D / 64; ++h)
+            tma_load_3d(smem_addr(sm.q[t]) + h * kRows * 128, &p.qmap, h * 64, g * G, qs + first,
+                        smem_addr(&sm.q_full));
+        }
       }
       cp_async_arrive(smem_addr(&sm.q_full));
     }
@@ -345,7 +394,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #pragma unroll
       for (int i = 0; i + 1 < kTableAhead; ++i) ahead[i] = ahead[i + 1];
       ahead[kTableAhead - 1] = lookup(kt + kTableAhead);
-      if (kt >= kStages && !wait(sm.kv_empty[st], ((kt - kStages) / kStages) & 1)) break;
+      if (kt >= kStages && !(wait(sm.o_done[0][st], ((kt - kStages) / kStages) & 1) &&
+                             wait(sm.o_done[1][st], ((kt - kStages) / kStages) & 1)))
+        break;
       const uint32_t kb = smem_addr(is_v ? sm.v[st] : sm.k[st]);
       uint32_t full_mask = 0;  // blocks that come whole by TMA
       for (int j = 0; j < nbk; ++j) {
@@ -426,7 +477,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #pragma unroll
         for (int ks = 1; ks < KS2; ++ks)  // P from tensor memory: 16 keys = 8 columns
           mma_f16_ts(o, pa + ks * 8, vd + ((ks * 16 * 128) >> 4), id_o, true);
-        mma_commit(smem_addr(&sm.o_done[t][b]));
         return true;
       };
       auto kv_ready = [&](int kt) -> bool {
@@ -448,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           ok = ok && (kt + 1 >= nt[t] || issue_s(t, kt + 1));
         }
         ok = ok && (kt >= nt[t] || issue_pv(t, kt));
-        if (ok) mma_commit(smem_addr(&sm.kv_empty[kt % kStages]));
+        if (ok) mma_commit(smem_addr(&sm.o_done[t][kt % kStages]));
       }
       mma_commit(smem_addr(&sm.fin));  // every MMA this thread issued
       wait(sm.fin, 0);
@@ -505,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       const bool need = kt > 0 && m_new > m_used + kRescale;
       if (__any_sync(0xffffffffu, need)) {
         // rescale O (rows whose maximum grew too far) once P V of tile kt - 1 is done
-        if (!(ok = wwait(sm.o_done[t][(kt - 1) & 1], ((kt - 1) >> 1) & 1))) break;
+        if (!(ok = wwait(sm.o_done[t][(kt - 1) % kStages], ((kt - 1) / kStages) & 1))) break;
         tc_fence_after();
         const float alpha = need ? ex2(m_used - m_new) : 1.f;
 #pragma unroll
@@ -529,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       // (a row with nothing unmasked yet has every score at -inf, so any finite offset
       // gives it P = 0; packed FP32 pairs halve the FMA and add counts)
       // P goes to slot b, which P V of the keys two tiles back read: that P V is done
-      if (kt >= 2 && !(ok = wwait(sm.o_done[t][b], ((kt - 2) >> 1) & 1))) break;
+      if (kt >= 2 && !(ok = wwait(sm.o_done[t][(kt - 2) % kStages], ((kt - 2) / kStages) & 1))) break;
       tc_fence_after();
       const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
       const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(neg_m, neg_m);
@@ -556,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     }
     if (ok && nt[t] > 0) {
       const int last = nt[t] - 1;
-      ok = wwait(sm.o_done[t][last & 1], (last >> 1) & 1);
+      ok = wwait(sm.o_done[t][last % kStages], (last / kStages) & 1);
     }
     // ---- out = O / l, after every role is done (the loader's bad-block flag is final) ----
     tc_fence_before();
@@ -660,6 +710,22 @@ bool kv_cache_map(CUtensorMap* map, const void* base, int elem_bytes, int num_bl
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// q as [tokens][Hq][d] 16-bit with a box of one query tile's 64-column half: (64, G,
+// 128 / G).  `tokens` bounds the rows a launch may read (num_seqs x max_query_len); only
+// tiles that lie wholly inside their sequence are read through it.
+static bool q_map(CUtensorMap* map, const void* q, int hq, int d, int g, long long tokens) {
+  EncodeTiledFn fn = encode_tiled();
+  if (!fn || prefill::kRows % g != 0 || tokens < 1) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(hq),
+                              static_cast<cuuint64_t>(tokens)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(hq) * d * 2};
+  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(g), static_cast<cuuint32_t>(prefill::kRows / g)};
+  const cuuint32_t es[3] = {1u, 1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(q), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int prefill_launch(const PrefillArgs& a, cudaStream_t stream) {
   prefill::Params p;
   if (!kv_cache_map(&p.kmap, a.k_cache, 2, a.num_blocks, a.num_kv_heads, a.block_size,
@@ -683,6 +749,9 @@ int prefill_launch(const PrefillArgs& a, cudaStream_t stream) {
   p.block_size = a.block_size;
   p.num_blocks = a.num_blocks;
   p.scale_log2 = a.scale * prefill::kLog2e;
+  p.q_tma = q_map(&p.qmap, a.q, a.num_q_heads, a.head_dim, p.group,
+                  static_cast<long long>(a.num_seqs) * a.max_query_len)
+                ? 1 : 0;
   p.err = a.err;
   if (a.head_dim == 128)
     return a.bf16 ? prefill::launch<128, __nv_bfloat16>(p, a.max_query_len, stream)
