@@ -28,16 +28,18 @@
 //   moves only about 26 GB/s per SM, so K and V each get their own issuer.  A stage of
 //   the ring is free again once P V of both query tiles has read it (the same barrier
 //   tells the softmax that P V is done).
-// * Two MMA warps, one issuing thread per query tile: S = Q K^T into tensor memory (one
-//   buffer per tile), and O += P V with P read from tensor memory (the A operand, two
-//   slots per tile, packed two values a column) and O kept there across the whole key
-//   range.  S of a tile's next keys is issued as soon as the softmax has loaded the
-//   current S into registers, before the current P V, so the tensor cores compute it while
-//   that tile's softmax runs, and the two tiles interleave on the tensor cores.
+// * Two MMA warps, one issuing thread per query tile: S = Q K^T into tensor memory (two
+//   buffers per tile, alternate key tiles), and O += P V with P read from tensor memory
+//   (the A operand, packed two values a column over the first half of its own S buffer)
+//   and O kept there across the whole key range.  S of a tile's next keys is issued before
+//   the current P V, so the tensor cores compute it while that tile's softmax runs, and the
+//   two tiles interleave on the tensor cores.  The S MMA that refills a buffer comes after
+//   the P V that read its P, and the tensor pipe runs one thread's MMAs in order: neither
+//   the MMA thread nor the softmax waits for the other over a buffer, which took two
+//   barrier waits off each step of the MMA thread's critical path.
 // * Two softmax warpgroups, one per query tile, one thread per row (= tensor-memory
 //   lane): read the row of S, mask causally, keep the running maximum m and sum l in
-//   exp2 units, write the row of P (input type) into the tile's next P slot (once the
-//   P V that read it two tiles back is done).
+//   exp2 units, write the row of P (input type) over the row of S just read.
 //   O is rescaled only when a row's maximum grows by more than 8 (in log2 units), so
 //   P <= 2^8 and the rescale (a read-modify-write of the row in tensor memory) is rare
 //   after the first tiles; the final O / l uses the same m, so the result is exact
@@ -95,7 +97,7 @@ struct Smem {
   uint8_t v[kStages][kKeys * D * 2];
   unsigned long long q_full;
   unsigned long long kv_full[kStages];
-  unsigned long long s_full[kTiles][2], s_read[kTiles][2];
+  unsigned long long s_full[kTiles][2];
   unsigned long long p_full[kTiles][2];
   unsigned long long o_done[kTiles][kStages];  // P V of tile kt done (frees stage kt % kStages)
   unsigned long long fin;  // the MMA thread's last commit
@@ -254,7 +256,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   constexpr int KS1 = D / 16;                // MMA k-steps of S = Q K^T
   constexpr int KS2 = kKeys / 16;            // MMA k-steps of P V
   constexpr uint32_t kTileCols = 256;        // TMEM columns per query tile:
-  constexpr uint32_t kColP = kKeys;          //   S [0, 64), P slots [64, 96) and [96, 128),
+  constexpr uint32_t kColS = kKeys;          //   S of keys kt in [64 (kt % 2), + 64), its P over
+                                             //   the first 32 of those columns,
   constexpr uint32_t kColO = 2 * kKeys;      //   O [128, 128 + D)
   constexpr uint32_t kTmemCols = kTiles * kTileCols;
   constexpr uint32_t kHalf = kKeys * 128;    // bytes of a 64-column half of a K/V tile
@@ -302,7 +305,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     for (int t = 0; t < kTiles; ++t)
       for (int b = 0; b < 2; ++b) {
         mbar_init(smem_addr(&sm.s_full[t][b]), 1);
-        mbar_init(smem_addr(&sm.s_read[t][b]), kRows);
         mbar_init(smem_addr(&sm.p_full[t][b]), kRows);
       }
     for (int t = 0; t < kTiles; ++t)
@@ -452,10 +454,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       const uint64_t dv0 = desc_sw128(smem_addr(sm.v[0]), kKeys * 128, 1024);
       auto issue_s = [&](int t, int kt) -> bool {
         const int b = kt & 1;
-        // one S buffer: the softmax has loaded S of the keys before these
-        if (kt >= 1 && !wait(sm.s_read[t][(kt - 1) & 1], ((kt - 1) >> 1) & 1)) return false;
-        tc_fence_after();
-        const uint32_t d = tmem + t * kTileCols;
+        // S buffer b last held S and P of the keys two tiles back, whose P V this thread
+        // issued before this S: the tensor pipe runs them in order
+        const uint32_t d = tmem + t * kTileCols + b * kColS;
         const uint64_t qd = t == 0 ? dq0 : dq1;
         const uint64_t kd = dk0 + (((kt % kStages) * kStageBytes) >> 4);
         mma_f16(d, qd, kd, id_s, false);
@@ -474,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         tc_fence_after();
         const uint64_t vd = dv0 + (((kt % kStages) * kStageBytes) >> 4);
         const uint32_t o = tmem + t * kTileCols + kColO;
-        const uint32_t pa = tmem + t * kTileCols + kColP + b * (kKeys / 2);
+        const uint32_t pa = tmem + t * kTileCols + b * kColS;
         mma_f16_ts(o, pa, vd, id_o, kt > 0);
 #pragma unroll
         for (int ks = 1; ks < KS2; ++ks)  // P from tensor memory: 16 keys = 8 columns
@@ -526,16 +527,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       float sv[kKeys];
       {
         float tmp[32];
-        tmem_ld32(tl, tmp);
+        tmem_ld32(tl + b * kColS, tmp);
 #pragma unroll
         for (int i = 0; i < 32; ++i) sv[i] = tmp[i];
-        tmem_ld32(tl + 32, tmp);
+        tmem_ld32(tl + b * kColS + 32, tmp);
 #pragma unroll
         for (int i = 0; i < 32; ++i) sv[32 + i] = tmp[i];
       }
-      // S is in registers: the MMA thread may write the next keys' S over it
-      tc_fence_before();
-      mbar_arrive(smem_addr(&sm.s_read[t][b]));
       // causal mask on the raw scores (key kt*64 + i > pos), then the maximum over eight
       // independent partial chains; scores stay unscaled (the scale is positive, so the
       // maximum commutes with it) and P = 2^(s * scale - m) is one FFMA per element
@@ -580,9 +578,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       // eight partial chains
       // (a row with nothing unmasked yet has every score at -inf, so any finite offset
       // gives it P = 0; packed FP32 pairs halve the FMA and add counts)
-      // P goes to slot b, which P V of the keys two tiles back read: that P V is done
-      if (kt >= 2 && !(ok = wwait(sm.o_done[t][(kt - 2) % kStages], ((kt - 2) / kStages) & 1))) break;
-      tc_fence_after();
+      // P goes over this thread's own row of S, already in registers (the P V that last
+      // read this buffer ran before the S MMA that filled it)
       const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
       const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(neg_m, neg_m);
       float2 ps[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
@@ -597,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           ps[(i >> 1) & 3] = __fadd2_rn(ps[(i >> 1) & 3], e);
           pk[i >> 1] = pack2<T>(e.x, e.y);
         }
-        tmem_st16(tl + kColP + b * (kKeys / 2) + 16 * h, pk);
+        tmem_st16(tl + b * kColS + 16 * h, pk);
       }
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       const float2 s01 = __fadd2_rn(ps[0], ps[1]), s23 = __fadd2_rn(ps[2], ps[3]);
