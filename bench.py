@@ -1591,6 +1591,7 @@ def fp8_line(args, res, world):
 # ---------------------------------------------------------------- shared-prefix beams
 
 BEAM_WORKLOADS = ("beam",)
+DECODE16_WORKLOADS = ("tiny", "llama31_8b", "llama7b_mha", "long_b8", "long_b16", "long_b32")
 
 
 def beam_place(pool, wl, base):
@@ -1872,6 +1873,96 @@ def max_over_ranks(values):
 RANK_TIMES = ("step_ms", "decode_ms", "two_calls_ms", "e2e_ms")
 
 
+def timeline_phases(a, b):
+    """Phases of launch `a` and the gap to launch `b` from their pa_decode_timeline stamps
+    ([cta][warp][k] ns: k = 0 the programmatic wait released, 1 the warp's streaming done,
+    2 its end; a CTA with no work left zeros), in µs from the first release of `a`."""
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    live = (a > 0).all(axis=(1, 2))
+    a = a[live]
+    t0 = a[:, :, 0].min()
+    rel = lambda x: (x - t0) / 1e3
+    release = rel(a[:, :, 0].min(axis=1))
+    stream_end = rel(a[:, :, 1].max(axis=1))
+    cta_end = rel(a[:, :, 2].max(axis=1))
+    tail = cta_end - stream_end
+    pct = lambda x, q: [round(float(v), 2) for v in np.percentile(x, q)]
+    bl = b[(b[:, :, 0] > 0).all(axis=1)]  # (only the release stamps of `b` are read)
+    nxt = rel(bl[:, :, 0].min()) if len(bl) else None
+    return {
+        "ctas": int(live.sum()),
+        "release_spread_us": round(float(release.max()), 2),
+        "stream_end_us": dict(zip(("p10", "p50", "p90", "max"), pct(stream_end, [10, 50, 90, 100]))),
+        "cta_end_us": dict(zip(("p50", "max"), pct(cta_end, [50, 100]))),
+        "end_phase_us": dict(zip(("p50", "max"), pct(tail, [50, 100]))),
+        "longest_end_phases": [{"cta": int(np.flatnonzero(live)[c]), "released": round(float(release[c]), 2),
+                                "stream_end": round(float(stream_end[c]), 2),
+                                "end": round(float(cta_end[c]), 2)}
+                               for c in np.argsort(tail)[::-1][:3]],
+        "next_release_us": None if nxt is None else round(float(nxt), 2),
+        "gap_after_last_end_us": None if nxt is None else round(float(nxt - cta_end.max()), 2),
+    }
+
+
+def run_timeline(args):
+    """--timeline: the decode kernel alone, --steps launches back to back on one stream as
+    in the roofline loop; the last two run the stamped copy of the kernel
+    (pa_decode_timeline).  Prints one JSON line with the phases of the second-to-last launch
+    and the gap to the last one."""
+    import torch
+
+    import paged_kv_cache_149_gb300 as pa
+    import workloads
+    from paged_kv_cache_149_gb300 import build as _build
+
+    _build.build()
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    wl = workloads.RECIPES[args.workload]()
+    k_cache, v_cache, batches, _ = build_batches(wl, device, ROTATE)
+    ws = pa.make_workspace(wl.num_q_heads, wl.num_kv_heads, wl.head_dim, device)
+    stream = torch.cuda.Stream(device)
+    nsm = torch.cuda.get_device_properties(device).multi_processor_count
+    bufs = [torch.zeros(nsm * 8 * 3, dtype=torch.int64, device=device) for _ in range(2)]
+    torch.cuda.synchronize(device)
+
+    def launch(i):
+        b = batches[i % ROTATE]
+        pa.decode(b["q"], k_cache, v_cache, b["tables"], b["ctx"], wl.scale, out=b["out"],
+                  workspace=ws, stream=stream)
+
+    for i in range(args.warmup):
+        launch(i)
+    try:  # the stamped kernel once too, so that loading it is not timed
+        pa.decode_timeline(bufs[0])
+        launch(0)
+    finally:
+        pa.decode_timeline(None)
+    torch.cuda.synchronize(device)
+    bufs[0].zero_()
+    K = max(3, args.steps)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(K - 2):
+        launch(i)
+    try:
+        pa.decode_timeline(bufs[0])
+        launch(K - 2)
+        pa.decode_timeline(bufs[1])
+        launch(K - 1)
+    finally:
+        pa.decode_timeline(None)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    if pa.get_device_error(stream=stream):
+        raise RuntimeError("device error flags set")
+    a, b = (x.view(nsm, 8, 3).cpu().numpy() for x in bufs)
+    print(json.dumps({"workload": args.workload, "launches": K,
+                      "us_per_launch": round(e0.elapsed_time(e1) * 1e3 / K, 2),
+                      "phases": timeline_phases(a, b)}))
+
+
 def main(argv=None, runner=None, backend="nccl"):
     """One JSON line on rank 0.  `runner` (default: the GPU run) and `backend` are
     parameters so that the multi-rank host logic can run on CPU ranks."""
@@ -1884,6 +1975,8 @@ def main(argv=None, runner=None, backend="nccl"):
     ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
     ap.add_argument("--repeats", type=int, default=0,
                     help="timed loops of --steps steps each (default: enough for ~0.4 s)")
+    ap.add_argument("--timeline", action="store_true",
+                    help="16-bit decode workloads: print the phase stamps of a launch instead")
     args = ap.parse_args(argv)
     global FIXED_REPEATS
     FIXED_REPEATS = args.repeats if args.repeats > 0 else None
@@ -1898,6 +1991,11 @@ def main(argv=None, runner=None, backend="nccl"):
         if rank != 0:
             return
         reference_arm(args)
+        return
+    if args.timeline:
+        if args.workload not in DECODE16_WORKLOADS:
+            ap.error("--timeline takes a 16-bit decode workload")
+        run_timeline(args)
         return
 
     if world > 1:

@@ -72,6 +72,7 @@ SIGNATURES = {
     "pa_prefill": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
                           _i32, _i32, _f32, _vp, _i32, _vp]),
     "pa_decode_workspace_size": (_sz, [_i32, _i32, _i32]),
+    "pa_decode_timeline": (_i32, [_vp, _sz]),
     "pa_decode_fixed_scratch": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                                        _i32, _f32, _vp, _i32, _vp]),
     "pa_copy_blocks": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp]),
@@ -310,6 +311,19 @@ def decode_workspace_size(num_q_heads, num_kv_heads, head_dim):
     if n == 0:
         raise PagedAttentionError(PA_ERR_ARG, "pa_decode_workspace_size")
     return n
+
+
+def decode_timeline(buffer=None):
+    """Diagnostics (pa_decode_timeline): while `buffer` is set -- a device int64 tensor of
+    at least SM count x 8 x 3 entries -- every 16-bit decode launch from this thread writes
+    its warps' phase stamps into it, [cta][warp][k]; None clears the setting."""
+    if buffer is None:
+        _check(lib().pa_decode_timeline(None, 0), "pa_decode_timeline")
+        return
+    import torch
+    if buffer.dtype != torch.int64 or not buffer.is_cuda or not buffer.is_contiguous():
+        raise PagedAttentionError(PA_ERR_ARG, "pa_decode_timeline: a contiguous device int64 tensor")
+    _check(lib().pa_decode_timeline(buffer.data_ptr(), buffer.numel() * 8), "pa_decode_timeline")
 
 
 def make_workspace(num_q_heads, num_kv_heads, head_dim, device=None):

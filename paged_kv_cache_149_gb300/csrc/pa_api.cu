@@ -197,6 +197,12 @@ int decode_call(const void* q, const void* key_new, const void* value_new, const
 
 }  // namespace
 
+int pa_decode_timeline(void* buffer, size_t bytes) {
+  if (buffer && (reinterpret_cast<uintptr_t>(buffer) & 7u)) return PA_ERR_ARG;
+  pa::decode_set_timeline(buffer, bytes);
+  return PA_OK;
+}
+
 int pa_decode(const void* q, const void* k_cache, const void* v_cache,
               const int32_t* block_tables, int max_blocks_per_seq,
               const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,

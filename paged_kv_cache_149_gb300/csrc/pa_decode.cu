@@ -43,7 +43,23 @@ static unsigned long long next_epoch() {
   return (counter.fetch_add(1, std::memory_order_relaxed) + 1) & ((1ull << 40) - 1);
 }
 
+// The diagnostic timeline buffer of this host thread (pa_decode_timeline), or null.
+static thread_local unsigned long long* t_timeline = nullptr;
+static thread_local size_t t_timeline_bytes = 0;
+
+void decode_set_timeline(void* buffer, size_t bytes) {
+  t_timeline = static_cast<unsigned long long*>(buffer);
+  t_timeline_bytes = buffer ? bytes : 0;
+}
+
 int decode_launch(const DecodeArgs& a, int grid, cudaStream_t stream) {
+  // a timeline buffer set: the stamped copy of the 16-bit kernel (pa_decode_timed.cu), for
+  // head_dim 128 and up to 8 query heads a pair only
+  if (t_timeline &&
+      (a.kv_fp8 || a.kv_int4 || a.head_dim != 128 ||
+       decode_heads_per_pair(a.num_q_heads, a.num_kv_heads) > 8 ||
+       t_timeline_bytes < static_cast<size_t>(grid) * decode::kWarps * 3 * sizeof(unsigned long long)))
+    return -1;
   decode::Params p;
   p.q = static_cast<const uint8_t*>(a.q);
   p.k_cache = static_cast<const uint8_t*>(a.k_cache);
@@ -94,6 +110,7 @@ int decode_launch(const DecodeArgs& a, int grid, cudaStream_t stream) {
   // heads of a pair are MMA columns: one n-tile of 8, or two for up to 16
   if (a.kv_fp8) return decode_launch_fp8(p, grid, a.head_dim, a.bf16, stream);
   if (a.kv_int4) return decode_launch_int4(p, grid, a.head_dim, a.bf16, stream);
+  if (t_timeline) return decode_launch_timed(p, grid, a.bf16, stream, t_timeline);
 #define PA_DECODE_CASE(DD, NN)                                                           \
   if (a.head_dim == DD && (p.heads_per_pair > 8) == (NN == 2))                           \
     return a.bf16 ? decode::launch<DD, NN, __nv_bfloat16, decode::kKv16>(p, grid, stream) \

@@ -62,6 +62,32 @@
 #include "pa_common.cuh"
 #include "pa_internal.h"
 
+// Diagnostics (pa_decode_timeline).  pa_decode_timed.cu defines PA_DECODE_TIMELINE before
+// including this file, which compiles the 16-bit kernel once more under another name, with
+// a `timeline` argument -- null, or [grid][kWarps][3] globaltimer readings (ns) -- into
+// which lane 0 of each warp writes when the programmatic wait released (0), when its
+// streaming is done (1) and at its end (2).  Everywhere else the stamps are empty
+// statements, so the kernels that serve calls are compiled without them: an extra argument
+// or Params field, or a stamp in the stage loop, measurably slowed the FP8 and 16-bit
+// kernels.
+#ifdef PA_DECODE_TIMELINE
+#define PA_DECODE_KERNEL decode_kernel_timed
+#define PA_DECODE_LAUNCH launch_timed
+#define PA_DECODE_TIMELINE_ARG , unsigned long long* timeline
+#define PA_DECODE_TIMELINE_PASS , timeline
+#define PA_DECODE_STAMP(k)                                                                     \
+  do {                                                                                        \
+    if (timeline != nullptr && lane == 0)                                                     \
+      timeline[(static_cast<size_t>(blockIdx.x) * kWarps + warp) * 3 + (k)] = global_timer_ns(); \
+  } while (0)
+#else
+#define PA_DECODE_KERNEL decode_kernel
+#define PA_DECODE_LAUNCH launch
+#define PA_DECODE_TIMELINE_ARG
+#define PA_DECODE_TIMELINE_PASS
+#define PA_DECODE_STAMP(k)
+#endif
+
 namespace pa {
 namespace decode {
 
@@ -937,7 +963,8 @@ __device__ __forceinline__ bool next_busy_fam(Fam f, int pi, long long w0, long 
 // MMAs in f16 on values widened exactly, with 32-token stages and the permuted d order of
 // O (drow).  The fused step (key_new) quantises the newest rows in the kernel.
 template <int D, int NTH, typename T, int KV>
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(kThreads, 1) PA_DECODE_KERNEL(const __grid_constant__ Params p
+                                                                  PA_DECODE_TIMELINE_ARG) {
   constexpr bool F8 = KV == kKvFp8;
   constexpr bool I4 = KV == kKvInt4;
   constexpr bool QK = KV != kKv16;  // quantised blocks
@@ -1185,6 +1212,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   // the kernel before this one (say the cache write) has finished and its writes are
   // visible past this point
   pdl_wait_primary();
+  PA_DECODE_STAMP(0);
 #pragma unroll
   for (int a = 0; a < G_::kAhead; ++a) issue_one();
 
@@ -1841,6 +1869,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     if (gt == 0 && any_bad) atomicOr(p.err, kErrBadBlock);
   }
   cp_async_wait<0>();  // (only empty groups can be left; leave none behind)
+  PA_DECODE_STAMP(1);
 
   // ---- count this share's pieces in; the last arrival at a pair merges its pieces ----
   // (ncut is the same in every warp of a pair.)  Lanes 0 and 1 of the pair's first warp
@@ -1894,12 +1923,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
                          gthreads);
     }
   }
+  PA_DECODE_STAMP(2);
 }
 
 template <int D, int NTH, typename T, int KV>
-int launch(const Params& prm, int grid, cudaStream_t stream) {
+int PA_DECODE_LAUNCH(const Params& prm, int grid, cudaStream_t stream PA_DECODE_TIMELINE_ARG) {
   const size_t smem = sizeof(Smem<D, KV>) + 1024;  // + alignment slack for the ring
-  auto* kern = decode_kernel<D, NTH, T, KV>;
+  auto* kern = PA_DECODE_KERNEL<D, NTH, T, KV>;
   if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), smem)) return -3;
   // a programmatic dependent of the previous kernel in the stream (see pdl_wait_primary)
   cudaLaunchConfig_t cfg = {};
@@ -1912,7 +1942,7 @@ int launch(const Params& prm, int grid, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, prm) != cudaSuccess) return -3;
+  if (cudaLaunchKernelEx(&cfg, kern, prm PA_DECODE_TIMELINE_PASS) != cudaSuccess) return -3;
   return 0;
 }
 
@@ -1924,6 +1954,9 @@ int decode_launch_fp8(const decode::Params& p, int grid, int head_dim, bool bf16
                       cudaStream_t stream);
 int decode_launch_int4(const decode::Params& p, int grid, int head_dim, bool bf16,
                        cudaStream_t stream);
+// The stamped 16-bit kernel (pa_decode_timed.cu): head_dim 128, up to 8 heads a pair.
+int decode_launch_timed(const decode::Params& p, int grid, bool bf16, cudaStream_t stream,
+                        unsigned long long* timeline);
 
 }  // namespace pa
 

@@ -36,6 +36,9 @@ size_t decode_workspace_bytes(int grid, int num_q_heads, int num_kv_heads, int h
 int decode_heads_per_pair(int num_q_heads, int num_kv_heads);
 // Launch the decode kernel; 0 or a negative PA_ERR_* code.
 int decode_launch(const DecodeArgs& a, int grid, cudaStream_t stream);
+// Diagnostics: every 16-bit decode launch of this host thread stamps its warps' phases
+// into `buffer` (device, [grid][8][3] unsigned long long) until called with NULL.
+void decode_set_timeline(void* buffer, size_t bytes);
 
 struct PrefillArgs {
   const void* q;  // [num_q_rows, Hq, d]

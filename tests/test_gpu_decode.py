@@ -186,3 +186,33 @@ def test_graph_replays_match_uncaptured_calls():
                                  workspace=torch.empty_like(gb.workspace)))
         np.testing.assert_array_equal(got, want)
     assert device_error() == 0
+
+
+@pytest.mark.gpu
+def test_timeline_stamps_leave_outputs_unchanged():
+    """pa_decode_timeline: the same bits with the stamps on, every warp's three stamps in
+    order, and a buffer too small for the grid refused before anything is launched."""
+    wl = workloads.custom("timeline", [20000, 300, 4096, 17], "bf16", 32, 8, 128, 16, 1800, 20480,
+                          seed=23)
+    gb = GpuBatch(wl)
+    want = to_bits(gb.decode())
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    buf = torch.zeros(nsm * 8 * 3, dtype=torch.int64, device="cuda")
+    try:
+        pa.decode_timeline(buf)
+        got = to_bits(gb.decode())
+    finally:
+        pa.decode_timeline(None)
+    np.testing.assert_array_equal(got, want)
+    st = buf.view(nsm, 8, 3).cpu().numpy()
+    live = st[(st > 0).all(axis=2)]
+    assert len(live) >= 8                                   # at least one CTA's warps stamped
+    assert (np.diff(live, axis=1) >= 0).all()               # released <= streamed <= end
+    small = torch.zeros(8, dtype=torch.int64, device="cuda")
+    try:
+        pa.decode_timeline(small)
+        with pytest.raises(pa.PagedAttentionError):
+            gb.decode()
+    finally:
+        pa.decode_timeline(None)
+    assert device_error() == 0
