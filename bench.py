@@ -1900,6 +1900,9 @@ def timeline_phases(a, b):
                                 "stream_end": round(float(stream_end[c]), 2),
                                 "end": round(float(cta_end[c]), 2)}
                                for c in np.argsort(tail)[::-1][:3]],
+        "latest_released": [{"cta": int(np.flatnonzero(live)[c]), "released": round(float(release[c]), 2),
+                             "stream_end": round(float(stream_end[c]), 2)}
+                            for c in np.argsort(release)[::-1][:6]],
         "next_release_us": None if nxt is None else round(float(nxt), 2),
         "gap_after_last_end_us": None if nxt is None else round(float(nxt - cta_end.max()), 2),
     }

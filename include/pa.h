@@ -312,20 +312,21 @@ int pa_decode_fixed_scratch(const void* q, const void* k_cache, const void* v_ca
  * pa_decode_timeline -- diagnostics: time the phases of 16-bit decode launches.
  *
  * The pages have no counterpart; it exists to measure where a launch's time goes.  While
- * a buffer is set, every decode launch over 16-bit blocks at head_dim 128 with at most 8
- * query heads per kv head made by this host thread (pa_decode, pa_decode_append,
- * pa_decode_fixed_scratch) runs a copy of the kernel in which lane 0 of each warp writes
- * three %globaltimer readings (ns) into it; the launches without a buffer run the kernel
- * without that code.  The layout is [cta][warp][k] unsigned long
- * long with 8 warps a CTA, and k is:
+ * a buffer is set, every decode launch made by this host thread (pa_decode,
+ * pa_decode_append, pa_decode_fixed_scratch) runs a copy of the kernel in which lane 0 of
+ * each warp writes three %globaltimer readings (ns) into the buffer.  That works for
+ * 16-bit blocks at head_dim 128 with at most 8 query heads per kv head.  Launches made
+ * without a buffer run the kernel without that code.  The layout is [cta][warp][k]
+ * unsigned long long with 8 warps a CTA, and k is:
  *   0  the programmatic wait on the previous kernel released,
  *   1  the warp's streaming done (before the cut pieces are counted in),
  *   2  its end (after any merge).
- * A CTA with no work writes nothing, so zero the buffer first.  buffer is device memory
- * of at least SM count x 8 x 3 x 8 bytes (29 184 bytes on 152 SMs).  While a buffer is
- * set, a decode launch with a smaller one, over FP8 or INT4 blocks, or of another shape
- * returns PA_ERR_ARG and launches nothing.  NULL clears the setting.  The caller owns the buffer.  Outputs
- * are unaffected.  Returns PA_ERR_ARG for a non-null buffer that is not 8-byte aligned.
+ * A CTA with no work writes nothing, so zero the buffer first.  buffer is device memory of
+ * at least SM count x 8 x 3 x 8 bytes (29 184 bytes on 152 SMs).  While a buffer is set,
+ * a decode launch returns PA_ERR_ARG and launches nothing if the buffer is smaller than
+ * that, if the blocks are FP8 or INT4, or if the shape is another one.  NULL clears the
+ * setting.  The caller owns the buffer, and outputs are unaffected.  Returns PA_ERR_ARG
+ * for a non-null buffer that is not 8-byte aligned.
  */
 int pa_decode_timeline(void* buffer, size_t bytes);
 
