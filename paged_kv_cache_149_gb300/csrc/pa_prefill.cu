@@ -9,7 +9,7 @@
 // FlashAttention…: prefill works on large blocks of queries).
 //
 // Design: one CTA per (pair of 128-row query tiles, sequence, kv head), 384 threads in
-// four roles that run concurrently and hand work over through mbarriers:
+// three roles that run concurrently and hand work over through mbarriers:
 // * A query tile's rows are (token, query head of the kv head) pairs, 128 / G tokens x G
 //   heads, so every K/V tile is read once for all heads of the group (GQA), and both
 //   query tiles of the CTA share the K/V tiles.
@@ -44,8 +44,8 @@
 //   P <= 2^8 and the rescale (a read-modify-write of the row in tensor memory) is rare
 //   after the first tiles; the final O / l uses the same m, so the result is exact
 //   softmax.  The rows of out leave through shared memory (the idle K/V ring) so that
-//   every store instruction of a warp writes whole rows: one row per thread, as the
-//   tensor-memory lanes give them, cost about 8 % of the from-scratch time.
+//   every store instruction of a warp writes whole rows; storing them one row per thread,
+//   as the tensor-memory lanes hold them, cost about 8 % of the from-scratch time.
 // Every mbarrier wait is bounded (about 1 s) and checks a shared abort flag, so a stuck
 // role ends the CTA with PA_DEVERR_TIMEOUT instead of hanging.
 #include <cuda.h>
