@@ -86,6 +86,7 @@ struct Params {
   uint8_t* out;
   int num_seqs, num_q_heads, num_kv_heads, group, tpt;  // tpt = tokens per query tile = 128 / G
   int max_blocks_per_seq, block_size, num_blocks;
+  int ncb;  // query blocks (of kTiles x tpt tokens) of the longest sequence
   float scale_log2;
   unsigned* err;
 };
@@ -269,8 +270,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   pdl_launch_dependents();
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int s = blockIdx.y, g = blockIdx.z;
-  const int cb = gridDim.x - 1 - blockIdx.x;  // later query blocks (more keys) first
+  // Launch order: the later half of every sequence's query blocks (the most keys) first,
+  // then the earlier half, latest block first within each; the blocks of one (sequence,
+  // kv head) stay together within a half, so they share their K/V in L2.  The long CTAs no
+  // longer come last: 986 -> 1001 TFLOP/s on 2048-token prompts from scratch.
+  const int s = blockIdx.y, g = blockIdx.z % p.num_kv_heads, half = blockIdx.z / p.num_kv_heads;
+  const int nearly = p.ncb - static_cast<int>(gridDim.x);  // blocks in the earlier half
+  if (half == 1 && static_cast<int>(blockIdx.x) >= nearly) return;  // (uniform over the CTA)
+  const int cb = (half == 0 ? p.ncb : nearly) - 1 - static_cast<int>(blockIdx.x);
   const int qs = __ldg(p.query_start + s), qlen = __ldg(p.query_start + s + 1) - qs;
   const int tpt = p.tpt, G = p.group;
   const int tok0 = cb * kTiles * tpt;
@@ -679,7 +686,12 @@ int launch(const Params& prm, int max_query_len, cudaStream_t stream) {
   if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), smem)) return -3;
   cudaLaunchConfig_t cfg = {};
   const int per_cta = kTiles * prm.tpt;
-  cfg.gridDim = dim3((max_query_len + per_cta - 1) / per_cta, prm.num_seqs, prm.num_kv_heads);
+  const int ncb = (max_query_len + per_cta - 1) / per_cta;
+  Params q = prm;
+  q.ncb = ncb;
+  // x: a block within its half (the later half has ceil(ncb / 2)), y: sequence,
+  // z: half x kv head
+  cfg.gridDim = dim3((ncb + 1) / 2, prm.num_seqs, 2 * prm.num_kv_heads);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
@@ -688,7 +700,7 @@ int launch(const Params& prm, int max_query_len, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, prm) != cudaSuccess) return -3;
+  if (cudaLaunchKernelEx(&cfg, kern, q) != cudaSuccess) return -3;
   return 0;
 }
 
