@@ -15,7 +15,8 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libpa.so")
-SOURCES = ["pa_api.cu", "pa_decode.cu", "pa_decode_fp8.cu", "pa_decode_int4.cu", "pa_decode_timed.cu",
+SOURCES = ["pa_api.cu", "pa_decode.cu", "pa_decode_fp8.cu", "pa_decode_int4.cu", "pa_decode_append.cu",
+           "pa_decode_append_fp8.cu", "pa_decode_append_int4.cu", "pa_decode_timed.cu",
            "pa_prefill.cu", "pa_cache_ops.cu", "pa_fixed_scratch.cu", "pa_pool.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -1,5 +1,5 @@
-// Paged decode attention for sm_103a: host side and the 16-bit instantiations of the
-// kernel in pa_decode_kernel.cuh (whose header comment describes the design).
+// Paged decode attention for sm_103a: host side and the 16-bit plain-decode instantiations
+// of the kernel in pa_decode_kernel.cuh (whose header comment describes the design).
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -107,20 +107,25 @@ int decode_launch(const DecodeArgs& a, int grid, cudaStream_t stream) {
   ws += up(static_cast<size_t>(grid) * 2 * p.gs * p.heads_per_pair * a.head_dim * sizeof(float));
   p.part_ml = reinterpret_cast<float*>(ws);
 
-  // heads of a pair are MMA columns: one n-tile of 8, or two for up to 16
-  if (a.kv_fp8) return decode_launch_fp8(p, grid, a.head_dim, a.bf16, stream);
-  if (a.kv_int4) return decode_launch_int4(p, grid, a.head_dim, a.bf16, stream);
+  // The fused step runs kernels compiled with the newest rows' write; a plain decode runs
+  // copies compiled without it.  On GB300 (decode alone, one box) that took the INT4 decode
+  // of 64 sequences from 37.3 to 36.1 us and of 256 MHA sequences from 229.3 to 218.0 us,
+  // FP8 from 35.2 to 34.2 us (64 sequences; 199.8 against 200.9 us on 256), 16-bit blocks
+  // from 51.4 to 51.2 and 381.2 to 378.5 us.
+  const bool fused = a.key_new != nullptr;
+  if (a.kv_fp8)
+    return fused ? decode::launch_format<decode::kKvFp8, true>(p, grid, a.head_dim, a.bf16, stream)
+                 : decode::launch_format<decode::kKvFp8, false>(p, grid, a.head_dim, a.bf16, stream);
+  if (a.kv_int4)
+    return fused ? decode::launch_format<decode::kKvInt4, true>(p, grid, a.head_dim, a.bf16, stream)
+                 : decode::launch_format<decode::kKvInt4, false>(p, grid, a.head_dim, a.bf16, stream);
   if (t_timeline) return decode_launch_timed(p, grid, a.bf16, stream, t_timeline);
-#define PA_DECODE_CASE(DD, NN)                                                           \
-  if (a.head_dim == DD && (p.heads_per_pair > 8) == (NN == 2))                           \
-    return a.bf16 ? decode::launch<DD, NN, __nv_bfloat16, decode::kKv16>(p, grid, stream) \
-                  : decode::launch<DD, NN, __half, decode::kKv16>(p, grid, stream);
-  PA_DECODE_CASE(128, 1)
-  PA_DECODE_CASE(128, 2)
-  PA_DECODE_CASE(64, 1)
-  PA_DECODE_CASE(64, 2)
-#undef PA_DECODE_CASE
-  return -1;
+  return fused ? decode::launch_format<decode::kKv16, true>(p, grid, a.head_dim, a.bf16, stream)
+               : decode::launch_format<decode::kKv16, false>(p, grid, a.head_dim, a.bf16, stream);
 }
+
+namespace decode {
+template int launch_format<kKv16, false>(const Params&, int, int, bool, cudaStream_t);
+}  // namespace decode
 
 }  // namespace pa

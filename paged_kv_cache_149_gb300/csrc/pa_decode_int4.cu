@@ -1,21 +1,9 @@
-// Paged decode attention over INT4 K/V blocks (codes with a float32 scale per row): the
-// INT4 instantiations of the kernel in pa_decode_kernel.cuh.
+// Paged decode attention over INT4 K/V blocks (codes with a float32 scale per row):
+// the plain-decode instantiations of the kernel in pa_decode_kernel.cuh.
 #include "pa_decode_kernel.cuh"
 
 namespace pa {
-
-int decode_launch_int4(const decode::Params& p, int grid, int head_dim, bool bf16,
-                       cudaStream_t stream) {
-#define PA_DECODE_INT4_CASE(DD, NN)                                                       \
-  if (head_dim == DD && (p.heads_per_pair > 8) == (NN == 2))                             \
-    return bf16 ? decode::launch<DD, NN, __nv_bfloat16, decode::kKvInt4>(p, grid, stream) \
-                : decode::launch<DD, NN, __half, decode::kKvInt4>(p, grid, stream);
-  PA_DECODE_INT4_CASE(128, 1)
-  PA_DECODE_INT4_CASE(128, 2)
-  PA_DECODE_INT4_CASE(64, 1)
-  PA_DECODE_INT4_CASE(64, 2)
-#undef PA_DECODE_INT4_CASE
-  return -1;
-}
-
+namespace decode {
+template int launch_format<kKvInt4, false>(const Params&, int, int, bool, cudaStream_t);
+}  // namespace decode
 }  // namespace pa

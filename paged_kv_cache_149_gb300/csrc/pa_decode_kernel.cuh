@@ -962,7 +962,9 @@ __device__ __forceinline__ bool next_busy_fam(Fam f, int pi, long long w0, long 
 // multiplies its scores, its V scale its weights in P V.  Both quantised formats run the
 // MMAs in f16 on values widened exactly, with 32-token stages and the permuted d order of
 // O (drow).  The fused step (key_new) quantises the newest rows in the kernel.
-template <int D, int NTH, typename T, int KV>
+// NEW: compiled for the fused step (key_new set); a plain decode runs a copy compiled
+// without that code, which uses fewer instructions and registers in the stage loop.
+template <int D, int NTH, typename T, int KV, bool NEW>
 __global__ void __launch_bounds__(kThreads, 1) PA_DECODE_KERNEL(const __grid_constant__ Params p
                                                                   PA_DECODE_TIMELINE_ARG) {
   constexpr bool F8 = KV == kKvFp8;
@@ -1117,7 +1119,7 @@ __global__ void __launch_bounds__(kThreads, 1) PA_DECODE_KERNEL(const __grid_con
           }
         };
         const bool whole_stage = nxt.nt == ST && G_::kRowsPerPass <= p.block_size &&
-                                 !(!QK && p.key_new && nxt.last);
+                                 !(!QK && NEW && nxt.last);
         if (whole_stage) {
           if (p.log2_block == 3) copy_whole(std::integral_constant<int, 3>());
           else if (p.log2_block == 4) copy_whole(std::integral_constant<int, 4>());
@@ -1136,7 +1138,7 @@ __global__ void __launch_bounds__(kThreads, 1) PA_DECODE_KERNEL(const __grid_con
           const size_t grow = !live ? rbase[0] : rb + (r & (p.block_size - 1));
           const size_t src = grow * G_::kRowBytes + ch * 16;
           const uint32_t so = I4 ? swz4<D>(row, ch) : (F8 ? swz8<D>(row, ch) : swz(row, ch));
-          if (!QK && p.key_new && nxt.last && row == nxt.nt - 1) {
+          if (!QK && NEW && nxt.last && row == nxt.nt - 1) {
             // the newest token: from the step's input (the cache row is written later)
             const size_t nsrc = ((static_cast<size_t>(nxt.s) * p.num_kv_heads + nxt.kvh) * D + ch * 8) * 2;
             cp_async16(dst + so, p.key_new + nsrc, 16u);
@@ -1151,7 +1153,7 @@ __global__ void __launch_bounds__(kThreads, 1) PA_DECODE_KERNEL(const __grid_con
           // fused step: the newest token's 16-bit K and V rows into this slot's scratch
           // (quantised when the stage is computed)
           constexpr int CR = D / 8;  // 16-byte chunks of a 16-bit row
-          if (p.key_new && nxt.last && lane < 2 * CR) {
+          if (NEW && nxt.last && lane < 2 * CR) {
             const int isv = lane >= CR ? 1 : 0, c = lane % CR;
             const size_t nsrc = ((static_cast<size_t>(nxt.s) * p.num_kv_heads + nxt.kvh) * D + c * 8) * 2;
             cp_async16(smem_addr(sm.newrow[warp][slot]) + isv * 2 * D + 16 * c,
@@ -1329,7 +1331,7 @@ __global__ void __launch_bounds__(kThreads, 1) PA_DECODE_KERNEL(const __grid_con
         const uint32_t kb = ring + slot * G_::kStageBytes;
         const uint32_t vb = kb + G_::kKBytes;
         if constexpr (QK) {
-          if (p.key_new && j == f.ns - 1) {
+          if (NEW && j == f.ns - 1) {
             // Fused step: the newest token (stage row nt_tok - 1) is quantised from the
             // step's input with the cache-write arithmetic; the codes (and INT4 scales)
             // replace the stage row and go to the cache slot at position ctx - 1.  No other
@@ -1656,7 +1658,7 @@ __global__ void __launch_bounds__(kThreads, 1) PA_DECODE_KERNEL(const __grid_con
             for (int nt = 0; nt < NTH; ++nt) mma16816<TM>(o[mt][nt], a, pb[0][nt][0], pb[0][nt][1]);
           }
         }
-        if (!QK && p.key_new && j == f.ns - 1) {
+        if (!QK && NEW && j == f.ns - 1) {
           // fused cache write: the newest token's K and V rows, from the slot, to position
           // ctx - 1 of the sequence (lanes take the 16-byte chunks of K, then of V)
           constexpr int CH = G_::kRowChunks;
@@ -1926,10 +1928,10 @@ __global__ void __launch_bounds__(kThreads, 1) PA_DECODE_KERNEL(const __grid_con
   PA_DECODE_STAMP(2);
 }
 
-template <int D, int NTH, typename T, int KV>
+template <int D, int NTH, typename T, int KV, bool NEW>
 int PA_DECODE_LAUNCH(const Params& prm, int grid, cudaStream_t stream PA_DECODE_TIMELINE_ARG) {
   const size_t smem = sizeof(Smem<D, KV>) + 1024;  // + alignment slack for the ring
-  auto* kern = PA_DECODE_KERNEL<D, NTH, T, KV>;
+  auto* kern = PA_DECODE_KERNEL<D, NTH, T, KV, NEW>;
   if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), smem)) return -3;
   // a programmatic dependent of the previous kernel in the stream (see pdl_wait_primary)
   cudaLaunchConfig_t cfg = {};
@@ -1946,14 +1948,35 @@ int PA_DECODE_LAUNCH(const Params& prm, int grid, cudaStream_t stream PA_DECODE_
   return 0;
 }
 
+#ifndef PA_DECODE_TIMELINE
+// Every kernel of one K/V format, for the plain decode (NEW false) or the fused step (NEW
+// true): head_dim 128 or 64, one n-tile of heads or two, bf16 or fp16.  Each (format, NEW)
+// is instantiated in a translation unit of its own, so that the six compile in parallel:
+// pa_decode.cu, pa_decode_fp8.cu, pa_decode_int4.cu (plain decode) and pa_decode_append.cu,
+// pa_decode_append_fp8.cu, pa_decode_append_int4.cu (fused step).
+template <int KV, bool NEW>
+int launch_format(const Params& p, int grid, int head_dim, bool bf16, cudaStream_t stream) {
+#define PA_DECODE_CASE(DD, NN)                                                   \
+  if (head_dim == DD && (p.heads_per_pair > 8) == (NN == 2))                     \
+    return bf16 ? launch<DD, NN, __nv_bfloat16, KV, NEW>(p, grid, stream)        \
+                : launch<DD, NN, __half, KV, NEW>(p, grid, stream);
+  PA_DECODE_CASE(128, 1)
+  PA_DECODE_CASE(128, 2)
+  PA_DECODE_CASE(64, 1)
+  PA_DECODE_CASE(64, 2)
+#undef PA_DECODE_CASE
+  return -1;
+}
+extern template int launch_format<kKv16, false>(const Params&, int, int, bool, cudaStream_t);
+extern template int launch_format<kKv16, true>(const Params&, int, int, bool, cudaStream_t);
+extern template int launch_format<kKvFp8, false>(const Params&, int, int, bool, cudaStream_t);
+extern template int launch_format<kKvFp8, true>(const Params&, int, int, bool, cudaStream_t);
+extern template int launch_format<kKvInt4, false>(const Params&, int, int, bool, cudaStream_t);
+extern template int launch_format<kKvInt4, true>(const Params&, int, int, bool, cudaStream_t);
+#endif
+
 }  // namespace decode
 
-// FP8 and INT4 instantiations live in their own translation units (pa_decode_fp8.cu,
-// pa_decode_int4.cu).
-int decode_launch_fp8(const decode::Params& p, int grid, int head_dim, bool bf16,
-                      cudaStream_t stream);
-int decode_launch_int4(const decode::Params& p, int grid, int head_dim, bool bf16,
-                       cudaStream_t stream);
 // The stamped 16-bit kernel (pa_decode_timed.cu): head_dim 128, up to 8 heads a pair.
 int decode_launch_timed(const decode::Params& p, int grid, bool bf16, cudaStream_t stream,
                         unsigned long long* timeline);

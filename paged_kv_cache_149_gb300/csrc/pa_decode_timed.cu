@@ -9,8 +9,11 @@ namespace pa {
 
 int decode_launch_timed(const decode::Params& p, int grid, bool bf16, cudaStream_t stream,
                         unsigned long long* timeline) {
-  return bf16 ? decode::launch_timed<128, 1, __nv_bfloat16, decode::kKv16>(p, grid, stream, timeline)
-              : decode::launch_timed<128, 1, __half, decode::kKv16>(p, grid, stream, timeline);
+  if (p.key_new)
+    return bf16 ? decode::launch_timed<128, 1, __nv_bfloat16, decode::kKv16, true>(p, grid, stream, timeline)
+                : decode::launch_timed<128, 1, __half, decode::kKv16, true>(p, grid, stream, timeline);
+  return bf16 ? decode::launch_timed<128, 1, __nv_bfloat16, decode::kKv16, false>(p, grid, stream, timeline)
+              : decode::launch_timed<128, 1, __half, decode::kKv16, false>(p, grid, stream, timeline);
 }
 
 }  // namespace pa
