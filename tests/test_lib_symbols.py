@@ -61,3 +61,28 @@ def test_check_block_mapping(libpa):
     for bad in ([(0, 3), (1, 3)], [(0, 3), (3, 4)], [(0, 8)], [(-1, 2)]):
         with pytest.raises(libpa.PagedAttentionError):
             libpa.check_block_mapping(bad, 8)
+
+
+def test_build_compiles_every_source():
+    """build() compiles the sources it lists and nothing else, on whichever host builds the
+    library: every .cu / .cpp under csrc must be listed."""
+    from paged_kv_cache_149_gb300 import build as b
+    on_disk = sorted(f for f in os.listdir(b.CSRC) if f.endswith((".cu", ".cpp")))
+    assert sorted(b.SOURCES) == on_disk
+
+
+def test_each_decode_variant_is_instantiated_once():
+    """Every (K/V format, fused step or not) set of decode kernels is explicitly
+    instantiated in exactly one translation unit, and declared extern everywhere else."""
+    from paged_kv_cache_149_gb300 import build as b
+    found = {}
+    for f in b.SOURCES:
+        src = open(os.path.join(b.CSRC, f)).read()
+        for kv, new in re.findall(r"^\s*template int launch_format<(\w+), (true|false)>", src, re.M):
+            found.setdefault((kv, new), []).append(f)
+    want = {(kv, new) for kv in ("kKv16", "kKvFp8", "kKvInt4") for new in ("true", "false")}
+    assert set(found) == want
+    assert all(len(v) == 1 for v in found.values()), found
+    hdr = open(os.path.join(b.CSRC, "pa_decode_kernel.cuh")).read()
+    externs = set(re.findall(r"extern template int launch_format<(\w+), (true|false)>", hdr))
+    assert externs == want
