@@ -207,7 +207,8 @@ def _pool_device(src, dst, *args, device=None, **kw):
 
 class Launch:
     """A library call whose arguments were checked and marshalled once (``plan=True`` on
-    the decode step functions): ``run(stream)`` issues it again on ``stream`` over the
+    the decode step functions, prefill and reshape_and_cache): ``run(stream)`` issues it
+    again on ``stream`` over the
     same buffers, whose contents may change between runs.  For serving loops that launch
     the same step shape many times; the per-call cost is one foreign call.  The marshalled
     arguments are raw device addresses, so the Launch holds a reference to every tensor
@@ -290,18 +291,22 @@ def _dev(t, name, dtype=None):
 
 
 @_on_first
-def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, stream=None):
-    """k_cache[slot // B, h, slot % B] = key[i, h] (and V) for every slot >= 0."""
+def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, stream=None, plan=False):
+    """k_cache[slot // B, h, slot % B] = key[i, h] (and V) for every slot >= 0.  plan=True
+    returns a Launch (whose run writes the rows the buffers hold then) instead of writing."""
     import torch
     n, hkv, d = key.shape
     nb, hkv2, bs, d2 = k_cache.shape
     _need(value.shape == key.shape and v_cache.shape == k_cache.shape, "shape mismatch")
     _need(hkv == hkv2 and d == d2 and slot_mapping.shape == (n,), "shape mismatch")
     _need(key.dtype == value.dtype == k_cache.dtype == v_cache.dtype, "dtype mismatch")
-    st = lib().pa_reshape_and_cache(
-        _dev(key, "key"), _dev(value, "value"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
-        _dev(slot_mapping, "slot_mapping", torch.int64), n, nb, hkv, d, bs, _dtype_code(key),
-        _stream_ptr(stream, key.device))
+    args = (_dev(key, "key"), _dev(value, "value"), _dev(k_cache, "k_cache"),
+            _dev(v_cache, "v_cache"), _dev(slot_mapping, "slot_mapping", torch.int64), n, nb, hkv,
+            d, bs, _dtype_code(key))
+    if plan:
+        return Launch("pa_reshape_and_cache", args, k_cache,
+                      keep=(key, value, v_cache, slot_mapping))
+    st = lib().pa_reshape_and_cache(*args, _stream_ptr(stream, key.device))
     _check(st, "pa_reshape_and_cache")
 
 
@@ -492,10 +497,12 @@ def decode_append_fp8(q, key_new, value_new, k_cache, v_cache, block_tables, con
 
 @_on_first
 def prefill(q, k_cache, v_cache, block_tables, context_lens, query_start, scale,
-            max_query_len, out=None, stream=None):
+            max_query_len, out=None, stream=None, plan=False):
     """Causal attention of each sequence's newest tokens (q rows query_start[s] ..
     query_start[s+1]-1, at positions ctx - q_len .. ctx - 1, their K/V already in the cache)
-    over its paged context; returns ``out`` shaped like q."""
+    over its paged context; returns ``out`` shaped like q.  plan=True returns a Launch
+    instead of launching: its runs read the tables, lengths and offsets the buffers hold
+    then, so max_query_len must stay an upper bound of the query counts."""
     import torch
     ntok, hq, d = q.shape
     nb, hkv, bs, d2 = k_cache.shape
@@ -507,12 +514,15 @@ def prefill(q, k_cache, v_cache, block_tables, context_lens, query_start, scale,
     if out is None:
         out = torch.empty_like(q)
     _need(out.shape == q.shape and out.dtype == q.dtype, "out must match q")
-    st = lib().pa_prefill(
-        _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
-        _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
-        _dev(context_lens, "context_lens", torch.int32),
-        _dev(query_start, "query_start", torch.int32), n, int(max_query_len), hq, hkv, d, bs,
-        nb, float(scale), _dev(out, "out"), _dtype_code(q), _stream_ptr(stream, q.device))
+    args = (_dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+            _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+            _dev(context_lens, "context_lens", torch.int32),
+            _dev(query_start, "query_start", torch.int32), n, int(max_query_len), hq, hkv, d, bs,
+            nb, float(scale), _dev(out, "out"), _dtype_code(q))
+    if plan:
+        return Launch("pa_prefill", args, out,
+                      keep=(q, k_cache, v_cache, block_tables, context_lens, query_start))
+    st = lib().pa_prefill(*args, _stream_ptr(stream, q.device))
     _check(st, "pa_prefill")
     return out
 

@@ -111,3 +111,57 @@ def test_chunked_batch_every_sequence():
 def test_prompts_from_scratch_every_sequence():
     """The benchmark's batch of 8 prompts of 2048 tokens from scratch, every row."""
     check(workloads.prefill_llama31_8b())
+
+
+def test_planned_launches_match_direct_calls():
+    """plan=True: a Launch marshalled once writes the same cache rows and the same outputs,
+    bit for bit, as the direct calls, and each run reads what the buffers hold then."""
+    rng = np.random.default_rng(61)
+    wl = workloads._prefill("plan", rng, [300, 77, 513], [300, 40, 129], "bf16", 32, 8, 128,
+                            16, 80, 528, 1.0 / np.sqrt(128))
+    gb = GpuBatch(wl)
+    qs = torch.from_numpy(wl.query_start.astype(np.int32)).cuda()
+    maxq = int(np.diff(wl.query_start).max())
+    n_new = int(wl.query_start[-1])
+    g = torch.Generator(device="cuda").manual_seed(7)
+    kn = torch.randn((n_new, wl.num_kv_heads, wl.head_dim), generator=g, device="cuda").to(gb.q.dtype)
+    vn = torch.randn(kn.shape, generator=g, device="cuda").to(gb.q.dtype)
+    slots = []
+    for s in range(wl.num_seqs):
+        c, ql = int(wl.context_lens[s]), int(wl.query_start[s + 1] - wl.query_start[s])
+        row = gb.tables[s].cpu().numpy()
+        for t in range(c - ql, c):
+            slots.append(int(row[t // wl.block_size]) * wl.block_size + t % wl.block_size)
+    slots = torch.tensor(slots, dtype=torch.int64, device="cuda")
+    kc0, vc0 = gb.k_cache.clone(), gb.v_cache.clone()
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()  # (the batch was set up on the default stream)
+
+    pa.reshape_and_cache(kn, vn, gb.k_cache, gb.v_cache, slots, stream=stream)
+    want = pa.prefill(gb.q, gb.k_cache, gb.v_cache, gb.tables, gb.ctx, qs, wl.scale, maxq,
+                      stream=stream)
+    stream.synchronize()
+    want_k, want_v, want = gb.k_cache.clone(), gb.v_cache.clone(), want.clone()
+
+    gb.k_cache.copy_(kc0)
+    gb.v_cache.copy_(vc0)
+    out = torch.empty_like(gb.q)
+    w = pa.reshape_and_cache(kn, vn, gb.k_cache, gb.v_cache, slots, plan=True)
+    pf = pa.prefill(gb.q, gb.k_cache, gb.v_cache, gb.tables, gb.ctx, qs, wl.scale, maxq,
+                    out=out, plan=True)
+    torch.cuda.synchronize()
+    w.run(stream)
+    pf.run(stream)
+    stream.synchronize()
+    bits = lambda t: t.view(torch.int16)  # (unused cache slots hold NaN)
+    assert torch.equal(bits(gb.k_cache), bits(want_k)) and torch.equal(bits(gb.v_cache), bits(want_v))
+    assert torch.equal(bits(out), bits(want))
+    # a later run reads the buffers' new contents
+    gb.q.mul_(-1)
+    torch.cuda.synchronize()
+    pf.run(stream)
+    direct = pa.prefill(gb.q, gb.k_cache, gb.v_cache, gb.tables, gb.ctx, qs, wl.scale, maxq,
+                        stream=stream)
+    stream.synchronize()
+    assert torch.equal(bits(out), bits(direct)) and not torch.equal(bits(out), bits(want))
+    assert device_error() == 0
